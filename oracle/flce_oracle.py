@@ -1,0 +1,220 @@
+"""fp64 CPU oracle for the chunked LM-head cross-entropy -- TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may call
+this module.  The CUDA library never imports it, and it imports nothing from
+the library: the two share no code.  It is written to be read against the
+pages, not to be fast; numpy's matmul is the only library primitive used for
+the contractions.
+
+What it computes (one row i of the flattened batch x context tokens, vocab
+index v, hidden index k; bf16 inputs widened exactly to fp64):
+
+    z[i,v]  = sum_k h[i,k] * W[v,k]                 logits, "hidden_states @ lm_head"
+    lse[i]  = log sum_v exp(z[i,v])                 (max-shifted)
+    m[i]    = [t_i != ignore_index]
+    logp[i] = m[i] * (z[i,t_i] - lse[i])            selective log-softmax
+    n_valid = sum_i m[i]
+    loss    = -sum_i m[i] w[i] logp[i] / n_valid    (0 when n_valid == 0)
+    D[i,v]  = (exp(z[i,v] - lse[i]) - [v == t_i]) * m[i] * w[i] * g
+    dH      = D @ W        dW = D^T @ h
+
+Sources:
+  * Unsloth, "Reinforcement Learning GRPO with 7x longer context",
+    section "Flattened sequence-length chunking": rows are the flattened
+    (batch x context) tokens, processed in chunks; each chunk's logits are
+    ``hidden_states_chunk @ lm_head``, upcast to float32 for accuracy (fp64
+    here), followed by a log-softmax and a gather of the completion token.
+    Equations 1-3 of the same section give the logit-memory estimates
+    reproduced in ``logit_memory_gb``.
+  * Same page, section "Offloading activations for log-softmax": the
+    backward recomputes the chunk's logits and back-propagates through them;
+    the gradient is the textbook softmax-minus-one-hot.
+  * TRL v1.13 release article ("Training Beyond 1M Tokens"), section on the
+    four hurdles: the loss is computed 256 rows at a time and the chunk
+    losses are summed (loss_type="chunked_nll").
+  * Per-token weights and the GRPO-style loss -sum(w*logp)/sum(mask) are the
+    weighted form of the same masked mean; with w = 1 it is the mean NLL.
+
+Readings where the pages are silent: ignored rows have logp = 0, a zero
+dlogits row and no influence on anything but their own lse; n_valid = 0 gives
+loss 0; the denominator counts unmasked rows, not the sum of weights; a
+target outside [0, V) that is not ignore_index is an error here.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+IGNORE_INDEX = -100
+
+
+def widen(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact fp64; float arrays -> fp64."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def logits(h: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """z = h @ W^T in fp64 (one chunk's "hidden_states @ lm_head")."""
+    return widen(h) @ widen(W).T
+
+
+def logsumexp_rows(z: np.ndarray) -> np.ndarray:
+    """log sum_v exp(z[i,v]) per row, shifted by the row max."""
+    m = z.max(axis=1, keepdims=True)
+    return (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
+
+
+def _mask(targets: np.ndarray, V: int, ignore_index: int) -> np.ndarray:
+    t = np.asarray(targets, dtype=np.int64)
+    m = t != ignore_index
+    bad = m & ((t < 0) | (t >= V))
+    if bad.any():
+        raise ValueError(f"{int(bad.sum())} targets outside [0, V) and != ignore_index")
+    return m
+
+
+def _weights(weights, N: int) -> np.ndarray:
+    if weights is None:
+        return np.ones(N, dtype=np.float64)
+    return np.asarray(weights, dtype=np.float64)
+
+
+@dataclasses.dataclass
+class Forward:
+    lse: np.ndarray  # [N] fp64
+    logp: np.ndarray  # [N] fp64, 0 on ignored rows
+    n_valid: int
+    loss: float
+
+
+def selective_log_softmax(z: np.ndarray, targets: np.ndarray, mask: np.ndarray):
+    """Per-row (lse, logp) of a logits block: log_softmax, then gather t_i."""
+    lse = logsumexp_rows(z)
+    rows = np.arange(z.shape[0])
+    t = np.where(mask, targets, 0)
+    logp = np.where(mask, z[rows, t] - lse, 0.0)
+    return lse, logp
+
+
+def forward(h, W, targets, weights=None, ignore_index: int = IGNORE_INDEX,
+            chunk_rows: int | None = None) -> Forward:
+    """Chunked selective log-softmax and masked (weighted) mean NLL.
+
+    Rows are taken ``chunk_rows`` at a time (all at once when None); each
+    chunk's logits are formed in full, log-softmaxed, the target column is
+    gathered, and the chunk's loss terms are summed into the total.
+    """
+    hf, Wf = widen(h), widen(W)
+    N, V = hf.shape[0], Wf.shape[0]
+    t = np.asarray(targets, dtype=np.int64)
+    m = _mask(t, V, ignore_index)
+    w = _weights(weights, N)
+    step = N if chunk_rows is None else max(1, int(chunk_rows))
+    lse = np.zeros(N)
+    logp = np.zeros(N)
+    total = 0.0
+    for r0 in range(0, N, step):
+        r1 = min(N, r0 + step)
+        z = hf[r0:r1] @ Wf.T
+        lse[r0:r1], logp[r0:r1] = selective_log_softmax(z, t[r0:r1], m[r0:r1])
+        total += float(np.sum(m[r0:r1] * w[r0:r1] * logp[r0:r1]))
+    n_valid = int(m.sum())
+    loss = -total / n_valid if n_valid > 0 else 0.0
+    return Forward(lse, logp, n_valid, loss)
+
+
+def probs(z: np.ndarray, lse: np.ndarray) -> np.ndarray:
+    """Softmax rows p[i,v] = exp(z[i,v] - lse[i])."""
+    return np.exp(z - lse[:, None])
+
+
+def dlogits(z, lse, targets, mask, w, g: float) -> np.ndarray:
+    """D = (softmax - onehot(t)) * m * w * g for a block of rows."""
+    D = probs(z, lse)
+    rows = np.nonzero(mask)[0]
+    D[rows, np.asarray(targets)[rows]] -= 1.0
+    return D * (mask * w * g)[:, None]
+
+
+@dataclasses.dataclass
+class Backward:
+    dH: np.ndarray  # [N,H] fp64
+    dW: np.ndarray  # [V,H] fp64
+
+
+def backward(h, W, targets, weights=None, g: float = 1.0,
+             ignore_index: int = IGNORE_INDEX, chunk_rows: int | None = None,
+             lse: np.ndarray | None = None) -> Backward:
+    """dH = D W and dW = D^T h, recomputing each chunk's logits.
+
+    ``lse`` defaults to the oracle's own forward.  g multiplies D literally
+    (g = 1/n_valid gives the gradient of the mean loss).
+    """
+    hf, Wf = widen(h), widen(W)
+    N, V = hf.shape[0], Wf.shape[0]
+    t = np.asarray(targets, dtype=np.int64)
+    m = _mask(t, V, ignore_index)
+    w = _weights(weights, N)
+    step = N if chunk_rows is None else max(1, int(chunk_rows))
+    dH = np.zeros_like(hf)
+    dW = np.zeros_like(Wf)
+    for r0 in range(0, N, step):
+        r1 = min(N, r0 + step)
+        z = hf[r0:r1] @ Wf.T
+        l = logsumexp_rows(z) if lse is None else np.asarray(lse[r0:r1], dtype=np.float64)
+        D = dlogits(z, l, t[r0:r1], m[r0:r1], w[r0:r1], g)
+        dH[r0:r1] = D @ Wf
+        dW += D.T @ hf[r0:r1]
+    return Backward(dH, dW)
+
+
+def rows_forward(h, W, targets, rows, ignore_index: int = IGNORE_INDEX):
+    """(lse, logp) of the selected rows only; the same formulas as forward()."""
+    rows = np.asarray(rows, dtype=np.int64)
+    Wf = widen(W)
+    t = np.asarray(targets, dtype=np.int64)[rows]
+    m = _mask(t, Wf.shape[0], ignore_index)
+    z = widen(np.asarray(h)[rows]) @ Wf.T
+    return selective_log_softmax(z, t, m)
+
+
+def rows_backward(h, W, targets, rows, weights=None, g: float = 1.0,
+                  ignore_index: int = IGNORE_INDEX, vocab_rows=None):
+    """dH of the selected rows and those rows' contribution to dW.
+
+    Returns (dH[rows], dW_part) where dW_part = D[rows]^T h[rows], restricted
+    to ``vocab_rows`` when given.  Each row's lse is the oracle's own.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    hf = widen(np.asarray(h)[rows])
+    Wf = widen(W)
+    t = np.asarray(targets, dtype=np.int64)[rows]
+    m = _mask(t, Wf.shape[0], ignore_index)
+    w = _weights(None if weights is None else np.asarray(weights)[rows], len(rows))
+    z = hf @ Wf.T
+    D = dlogits(z, logsumexp_rows(z), t, m, w, g)
+    dH = D @ Wf
+    if vocab_rows is not None:
+        D = D[:, np.asarray(vocab_rows, dtype=np.int64)]
+    return dH, D.T @ hf
+
+
+def logit_memory_gb(context_length: int, vocab_dim: int, batch_size: int = 1,
+                    multiplier: int = 1) -> float:
+    """Unsloth GRPO page, flattened-chunking section, Equations 1-3.
+
+    Eq.1 (whole batch): batch x context x vocab / 1024^3;
+    Eq.2 (one sample at a time): context x vocab / 1024^3;
+    Eq.3 (sequence chunked): (context / multiplier) x vocab / 1024^3.
+    The formula counts elements; multiply by the element size for bytes.
+    """
+    return batch_size * (context_length / multiplier) * vocab_dim / 1024 ** 3
+
+
+def default_chunk_multiplier(context_length: int) -> int:
+    """Same section: the default sequence-chunk multiplier max(4, L // 4096)."""
+    return max(4, context_length // 4096)

@@ -1,0 +1,303 @@
+"""Pins of the fp64 oracle against closed forms, invariants, finite differences,
+a library routine (torch cross_entropy + autograd in fp64) and the numbers the
+pages print.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import flce_oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(N, H, V, seed=0, ignore=(), scale_w=0.3, weights=False):
+    r = np.random.default_rng(seed)
+    h = r.standard_normal((N, H))
+    W = r.standard_normal((V, H)) * scale_w
+    t = r.integers(0, V, N)
+    for i in ignore:
+        t[i] = O.IGNORE_INDEX
+    w = r.standard_normal(N) if weights else None
+    return h, W, t, w
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_zero_weight_matrix_closed_form():
+    N, H, V = 9, 6, 11
+    h, _, t, w = _rand(N, H, V, seed=1, ignore=(2, 5), weights=True)
+    W = np.zeros((V, H))
+    g = 0.37
+    f = O.forward(h, W, t, w)
+    m = t != O.IGNORE_INDEX
+    assert np.allclose(f.lse, math.log(V), atol=1e-14)
+    assert np.allclose(f.logp[m], -math.log(V), atol=1e-14)
+    assert np.all(f.logp[~m] == 0)
+    assert f.n_valid == 7
+    assert f.loss == pytest.approx(-np.sum(w[m]) * (-math.log(V)) / 7, rel=1e-13)
+    b = O.backward(h, W, t, w, g=g)
+    assert np.all(b.dH == 0)
+    # dW[v,:] = sum_i (1/V - [v == t_i]) m_i w_i g h_i, by explicit loops
+    ref = np.zeros((V, H))
+    for i in range(N):
+        if not m[i]:
+            continue
+        for v in range(V):
+            ref[v] += (1.0 / V - (1.0 if v == t[i] else 0.0)) * w[i] * g * h[i]
+    assert np.allclose(b.dW, ref, atol=1e-13)
+
+
+def test_single_word_vocab():
+    h, W, t, _ = _rand(5, 4, 1, seed=2)
+    f = O.forward(h, W, t)
+    assert np.allclose(f.logp, 0, atol=1e-14)
+    assert np.allclose(f.lse, (h @ W.T)[:, 0], atol=1e-13)
+    b = O.backward(h, W, t, g=1.0)
+    assert np.allclose(b.dH, 0, atol=1e-14) and np.allclose(b.dW, 0, atol=1e-14)
+
+
+def test_two_word_vocab_is_softplus():
+    h, W, t, _ = _rand(40, 7, 2, seed=3, scale_w=2.0)
+    f = O.forward(h, W, t)
+    z = h @ W.T
+    rows = np.arange(40)
+    other = z[rows, 1 - t] - z[rows, t]
+    assert np.allclose(f.logp, -np.logaddexp(0.0, other), atol=1e-13)
+
+
+def test_row_constant_shift_leaves_logp():
+    h, W, t, _ = _rand(12, 5, 17, seed=4)
+    f = O.forward(h, W, t)
+    for c in (3.0, 1000.0):  # 1000 also checks the max shift (exp(1000) overflows)
+        h2 = np.concatenate([h, np.ones((12, 1))], axis=1)
+        W2 = np.concatenate([W, np.full((17, 1), c)], axis=1)
+        f2 = O.forward(h2, W2, t)
+        assert np.all(np.isfinite(f2.lse))
+        assert np.allclose(f2.logp, f.logp, atol=1e-10)
+        assert np.allclose(f2.lse, f.lse + c, atol=1e-10)
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_softmax_rows_sum_to_one_and_dlogits_rows_to_zero():
+    h, W, t, w = _rand(20, 8, 31, seed=5, ignore=(3,), weights=True)
+    z = O.logits(h, W)
+    lse = O.logsumexp_rows(z)
+    assert np.allclose(O.probs(z, lse).sum(axis=1), 1.0, atol=1e-12)
+    D = O.dlogits(z, lse, np.where(t == O.IGNORE_INDEX, 0, t), t != O.IGNORE_INDEX, w, 0.5)
+    assert np.allclose(D.sum(axis=1), 0.0, atol=1e-12)
+    assert np.all(D[3] == 0)
+
+
+def test_ignored_rows_have_no_influence():
+    ign = (0, 4, 9)
+    h, W, t, w = _rand(12, 6, 13, seed=6, ignore=ign, weights=True)
+    f = O.forward(h, W, t, w)
+    b = O.backward(h, W, t, w, g=0.25)
+    h2 = h.copy()
+    h2[list(ign)] += np.random.default_rng(7).standard_normal((3, 6)) * 5
+    f2 = O.forward(h2, W, t, w)
+    b2 = O.backward(h2, W, t, w, g=0.25)
+    keep = np.setdiff1d(np.arange(12), ign)
+    assert np.allclose(f2.lse[keep], f.lse[keep], atol=1e-13)
+    assert not np.allclose(f2.lse[list(ign)], f.lse[list(ign)])
+    assert np.all(f2.logp[list(ign)] == 0)
+    assert f2.loss == pytest.approx(f.loss, rel=1e-13)
+    assert np.allclose(b2.dH, b.dH, atol=1e-13) and np.all(b2.dH[list(ign)] == 0)
+    assert np.allclose(b2.dW, b.dW, atol=1e-13)
+
+
+@pytest.mark.parametrize("chunk", [1, 16, 64, None])
+def test_chunk_size_independence(chunk):
+    h, W, t, w = _rand(64, 16, 50, seed=8, ignore=(1, 30, 63), weights=True)
+    f0 = O.forward(h, W, t, w)
+    b0 = O.backward(h, W, t, w, g=1 / f0.n_valid)
+    f = O.forward(h, W, t, w, chunk_rows=chunk)
+    b = O.backward(h, W, t, w, g=1 / f0.n_valid, chunk_rows=chunk)
+    assert np.allclose(f.lse, f0.lse, atol=1e-12) and np.allclose(f.logp, f0.logp, atol=1e-12)
+    assert f.loss == pytest.approx(f0.loss, rel=1e-12, abs=1e-15)
+    assert np.allclose(b.dH, b0.dH, atol=1e-12) and np.allclose(b.dW, b0.dW, atol=1e-12)
+
+
+def test_row_and_vocab_permutation_equivariance():
+    h, W, t, w = _rand(15, 6, 19, seed=9, ignore=(2,), weights=True)
+    f = O.forward(h, W, t, w)
+    b = O.backward(h, W, t, w, g=0.3)
+    r = np.random.default_rng(10)
+    pr = r.permutation(15)
+    fr = O.forward(h[pr], W, t[pr], w[pr])
+    br = O.backward(h[pr], W, t[pr], w[pr], g=0.3)
+    assert np.allclose(fr.logp, f.logp[pr], atol=1e-13) and np.allclose(br.dH, b.dH[pr], atol=1e-13)
+    assert np.allclose(br.dW, b.dW, atol=1e-12)
+    pv = r.permutation(19)  # new vocab index j holds old word pv[j]
+    inv = np.argsort(pv)
+    t2 = np.where(t == O.IGNORE_INDEX, t, inv[np.where(t == O.IGNORE_INDEX, 0, t)])
+    fv = O.forward(h, W[pv], t2, w)
+    bv = O.backward(h, W[pv], t2, w, g=0.3)
+    assert np.allclose(fv.logp, f.logp, atol=1e-13) and np.allclose(fv.lse, f.lse, atol=1e-13)
+    assert np.allclose(bv.dW, b.dW[pv], atol=1e-13) and np.allclose(bv.dH, b.dH, atol=1e-13)
+
+
+def test_gradients_linear_in_grad_scale():
+    h, W, t, w = _rand(10, 5, 9, seed=11, weights=True)
+    b1 = O.backward(h, W, t, w, g=1.0)
+    b3 = O.backward(h, W, t, w, g=-2.5)
+    assert np.allclose(b3.dH, -2.5 * b1.dH, atol=1e-13) and np.allclose(b3.dW, -2.5 * b1.dW, atol=1e-13)
+
+
+def test_n_valid_exact_and_empty_batch():
+    h, W, t, _ = _rand(33, 4, 8, seed=12, ignore=range(0, 33, 4))
+    assert O.forward(h, W, t).n_valid == 33 - 9
+    t_all = np.full(33, O.IGNORE_INDEX)
+    f = O.forward(h, W, t_all)
+    assert f.n_valid == 0 and f.loss == 0.0 and np.all(f.logp == 0)
+    b = O.backward(h, W, t_all, g=1.0)
+    assert np.all(b.dH == 0) and np.all(b.dW == 0)
+
+
+def test_bad_target_is_an_error():
+    h, W, t, _ = _rand(4, 3, 5, seed=13)
+    t[1] = 5
+    with pytest.raises(ValueError):
+        O.forward(h, W, t)
+
+
+# ---------------------------------------------------------- finite differences
+
+def test_central_finite_differences():
+    N, H, V = 3, 5, 7
+    h, W, t, w = _rand(N, H, V, seed=14, weights=True)
+    f = O.forward(h, W, t, w)
+    b = O.backward(h, W, t, w, g=1.0 / f.n_valid)
+    eps = 1e-6
+
+    def loss(hh, WW):
+        return O.forward(hh, WW, t, w).loss
+
+    num_dH = np.zeros_like(h)
+    for i in range(N):
+        for k in range(H):
+            e = np.zeros_like(h)
+            e[i, k] = eps
+            num_dH[i, k] = (loss(h + e, W) - loss(h - e, W)) / (2 * eps)
+    num_dW = np.zeros_like(W)
+    for v in range(V):
+        for k in range(H):
+            e = np.zeros_like(W)
+            e[v, k] = eps
+            num_dW[v, k] = (loss(h, W + e) - loss(h, W - e)) / (2 * eps)
+    assert np.linalg.norm(num_dH - b.dH) <= 1e-7 * np.linalg.norm(b.dH)
+    assert np.linalg.norm(num_dW - b.dW) <= 1e-7 * np.linalg.norm(b.dW)
+
+
+# ------------------------------------------------------------- library routine
+
+def _torch_ref(h, W, t, w, ignore_index=O.IGNORE_INDEX):
+    """torch fp64 cross_entropy (per token) and autograd for the weighted loss."""
+    ht = torch.tensor(O.widen(h), requires_grad=True)
+    Wt = torch.tensor(O.widen(W), requires_grad=True)
+    tt = torch.tensor(np.asarray(t, dtype=np.int64))
+    ce = torch.nn.functional.cross_entropy(ht @ Wt.T, tt, ignore_index=ignore_index, reduction="none")
+    n_valid = int((tt != ignore_index).sum())
+    wt = torch.ones_like(ce) if w is None else torch.tensor(np.asarray(w, dtype=np.float64))
+    loss = (wt * ce).sum() / max(n_valid, 1)
+    loss.backward()
+    return -ce.detach().numpy(), float(loss.detach()), ht.grad.numpy(), Wt.grad.numpy(), n_valid
+
+
+def test_matches_torch_cross_entropy_on_tiny_workload():
+    from chunked_lm_head_gb300 import workloads as WL
+    inp = WL.make_inputs("tiny")
+    logp_t, loss_t, dH_t, dW_t, nv = _torch_ref(inp.h, inp.W, inp.targets, None)
+    f = O.forward(inp.h, inp.W, inp.targets, chunk_rows=16)
+    b = O.backward(inp.h, inp.W, inp.targets, g=1.0 / f.n_valid, chunk_rows=16)
+    assert f.n_valid == nv == 61
+    assert np.allclose(f.logp, logp_t, atol=1e-12)
+    assert f.loss == pytest.approx(loss_t, rel=1e-12)
+    # mean reduction of the library equals the oracle's loss with w = 1
+    ce_mean = torch.nn.functional.cross_entropy(
+        torch.tensor(O.logits(inp.h, inp.W)), torch.tensor(inp.targets), ignore_index=-100)
+    assert f.loss == pytest.approx(float(ce_mean), rel=1e-12)
+    assert np.allclose(b.dH, dH_t, atol=1e-12) and np.allclose(b.dW, dW_t, atol=1e-12)
+
+
+def test_matches_torch_on_weighted_grpo_shape():
+    from chunked_lm_head_gb300 import workloads as WL
+    wl = WL.custom("grpo_small", 4 * 96, 128, 3000, 64, w_std=0.02, targets="zipf",
+                   grpo_seqs=4, prompt_len=16, seed=77)
+    inp = WL.make_inputs(wl)
+    assert inp.weights is not None and inp.n_ignored == 64
+    logp_t, loss_t, dH_t, dW_t, nv = _torch_ref(inp.h, inp.W, inp.targets, inp.weights)
+    f = O.forward(inp.h, inp.W, inp.targets, inp.weights, chunk_rows=64)
+    b = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / f.n_valid, chunk_rows=64)
+    assert f.n_valid == nv
+    assert np.allclose(f.logp, logp_t, atol=1e-12)
+    assert f.loss == pytest.approx(loss_t, rel=1e-11)
+    # per-sequence form: sum_s a_s * (summed CE over the sequence) / n_valid
+    z = torch.tensor(O.logits(inp.h, inp.W))
+    tt = torch.tensor(inp.targets)
+    seg = 0.0
+    L = wl.N // 4
+    for s in range(4):
+        ce_s = torch.nn.functional.cross_entropy(z[s * L:(s + 1) * L], tt[s * L:(s + 1) * L],
+                                                 ignore_index=-100, reduction="sum")
+        seg += float(inp.weights[s * L]) * float(ce_s)
+    assert f.loss == pytest.approx(seg / f.n_valid, rel=1e-11)
+    assert np.allclose(b.dH, dH_t, atol=1e-12) and np.allclose(b.dW, dW_t, atol=1e-12)
+
+
+def test_sampled_row_functions_match_full():
+    h, W, t, w = _rand(40, 9, 23, seed=15, ignore=(5, 6), weights=True)
+    f = O.forward(h, W, t, w)
+    b = O.backward(h, W, t, w, g=0.1)
+    rows = np.array([0, 5, 17, 39])
+    lse, logp = O.rows_forward(h, W, t, rows)
+    assert np.allclose(lse, f.lse[rows], atol=1e-13) and np.allclose(logp, f.logp[rows], atol=1e-13)
+    dH, dWp = O.rows_backward(h, W, t, np.arange(40), w, g=0.1, vocab_rows=[1, 22])
+    assert np.allclose(dH, b.dH, atol=1e-13) and np.allclose(dWp, b.dW[[1, 22]], atol=1e-13)
+    # linearity in the per-row weights: weights zero outside a row subset keep
+    # only those rows' dW contribution
+    w0 = np.zeros(40)
+    w0[rows] = w[rows]
+    b0 = O.backward(h, W, t, w0, g=0.1)
+    _, part = O.rows_backward(h, W, t, rows, w, g=0.1)
+    assert np.allclose(b0.dW, part, atol=1e-13)
+
+
+# --------------------------------------------------------- the pages' numbers
+
+def test_logit_memory_equations():
+    g = json.load(open(os.path.join(GOLD, "logit_memory.json")))
+    ex = g["example"]
+    B, L, V = ex["batch_size"], ex["context_length"], ex["vocab_dim"]
+    eq1 = O.logit_memory_gb(L, V, batch_size=B)
+    eq2 = O.logit_memory_gb(L, V)
+    mult = O.default_chunk_multiplier(L)
+    assert mult == ex["multiplier"] == 4
+    eq3 = O.logit_memory_gb(L, V, multiplier=mult)
+    assert eq1 == pytest.approx(3.906, abs=1e-3)
+    assert eq2 == pytest.approx(0.977, abs=1e-3)
+    assert eq3 == pytest.approx(0.244, abs=1e-3)
+    p = g["printed_gb"]
+    # the printed values keep the formula's x4 steps ...
+    assert eq1 / eq2 == pytest.approx(4.0) and eq2 / eq3 == pytest.approx(4.0)
+    assert p["eq1_whole_batch"] / p["eq2_one_sample"] == pytest.approx(4.0, rel=0.01)
+    assert p["eq2_one_sample"] / p["eq3_sequence_chunked"] == pytest.approx(4.0, rel=0.01)
+    # ... but not its values: 3.3 / 0.83 / 0.207 sit ~15% under the formula
+    assert p["eq1_whole_batch"] / eq1 == pytest.approx(0.845, abs=0.01)
+    hs = g["hidden_states_example"]
+    hs_all = O.logit_memory_gb(hs["context_length"], hs["hidden_states_dim"], batch_size=hs["batch_size"])
+    hs_one = O.logit_memory_gb(hs["context_length"], hs["hidden_states_dim"])
+    assert hs_all == pytest.approx(g["hidden_states_printed_gb"]["whole_batch"], rel=0.03)
+    assert hs_one == pytest.approx(g["hidden_states_printed_gb"]["per_sample"], abs=5e-4)
+    # long-context workload: full bf16 logits would be ~40 GB (never allocated)
+    assert 131072 * 151936 * 2 / 1e9 == pytest.approx(39.83, abs=0.01)
+
+
+def test_fp32_weight_copy_bytes():
+    g = json.load(open(os.path.join(GOLD, "trl_fp32_copy.json")))
+    assert g["vocab"] * g["hidden"] * g["bytes_per_element"] / 1e9 == pytest.approx(g["printed_gb"], abs=0.005)
