@@ -1,0 +1,387 @@
+"""Benchmark of the fused LM-head cross-entropy forward+backward (libflce).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload sft_16k] [--impl gb300|reference]
+
+One step = flce_forward + flce_backward (dH and dW) over one batch of the
+workload, through the C ABI, inputs resident in HBM.  Prints ONE JSON line.
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (weak scaling, no collective on the data path); rank 0 prints.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload (the only reference this method has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_lm_head_gb300 import workloads as WL  # noqa: E402
+
+METRIC = "fused LM-head+CE fwd+bwd tokens/s; % of GB300 BF16 tensor peak (1 GPU)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+# DRAM bytes per launch of each kernel kind from the committed ncu capture
+# (profiles/); None when no capture of the current kernel exists.
+NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {}
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.split(",") for r in self.tmp.read().strip().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if self.uuid:
+            mine = [r for r in rows if self.uuid in r[0]]
+            rows = mine or rows
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU baseline
+def cpu_oracle_rate(inp, target_s: float = 12.0, max_rows: int = 4096) -> dict:
+    """Time the fp64 oracle (fwd + bwd contributions) on a bounded row sample."""
+    from oracle import flce_oracle as O  # test/benchmark-only use of the oracle
+    wl = inp.wl
+    nvalid = int((inp.targets != WL.IGNORE_INDEX).sum())
+    g = 1.0 / max(nvalid, 1)
+
+    def run(k):
+        rows = WL.sample_rows(wl.N, k, seed=wl.seed + 7)
+        t0 = time.perf_counter()
+        O.rows_forward(inp.h, inp.W, inp.targets, rows)
+        O.rows_backward(inp.h, inp.W, inp.targets, rows, inp.weights, g=g)
+        return time.perf_counter() - t0
+
+    k = 16
+    dt = run(k)
+    if dt < target_s / 4 and k < max_rows:
+        k = int(min(max_rows, max(k, k * target_s / max(dt, 1e-3))))
+        k = min(k, wl.N)
+        dt = run(k)
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    return {"value": k / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{k} of {wl.N} rows of {wl.name} (full V={wl.V}, H={wl.H}): fp64 logits, "
+                      f"log-softmax, dlogits, dH rows and the rows' dW contribution; {dt:.1f} s",
+            "seconds": dt, "rows": k}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    inp = WL.make_inputs(args.workload)
+    vals = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        info = cpu_oracle_rate(inp, target_s=args.ref_step_s, max_rows=4096)
+        if i >= args.warmup:
+            vals.append(info["value"])
+    v = statistics.median(vals)
+    wl = inp.wl
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.N / v * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "V": wl.V,
+                       "chunk_rows": args.chunk_rows or wl.chunk_rows},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW")
+
+
+def gpu_arm(args):
+    import torch
+    from chunked_lm_head_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    lib = _lib.load()
+    wl = WL.WORKLOADS[args.workload]
+    chunk_rows = args.chunk_rows or wl.chunk_rows
+    inp = WL.make_inputs(wl)
+    N, H, V = wl.N, wl.H, wl.V
+    dev = torch.device("cuda", local)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    h = up(inp.h)
+    W = up(inp.W)
+    t = torch.from_numpy(inp.targets).to(dev)
+    w = None if inp.weights is None else torch.from_numpy(inp.weights).to(dev)
+    n_valid_host = int((inp.targets != WL.IGNORE_INDEX).sum())
+    g = 1.0 / max(n_valid_host, 1)
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    nv = torch.empty(1, dtype=torch.int64, device=dev)
+    dH = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    ws_bytes = _lib.flce_workspace_bytes(N, H, V, chunk_rows)
+    mem0 = torch.cuda.memory_allocated(dev)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    def step():
+        s = lib.flce_forward(h.data_ptr(), W.data_ptr(), t.data_ptr(),
+                             None if w is None else w.data_ptr(), N, H, V, chunk_rows, -100,
+                             logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(),
+                             workspace.data_ptr(), ws_bytes, sh)
+        if s != 0:
+            raise RuntimeError(f"flce_forward: {_lib.STATUS_NAMES.get(s, s)}")
+        s = lib.flce_backward(h.data_ptr(), W.data_ptr(), t.data_ptr(),
+                              None if w is None else w.data_ptr(), lse.data_ptr(), g,
+                              dH.data_ptr(), dW.data_ptr(), N, H, V, chunk_rows, -100,
+                              workspace.data_ptr(), ws_bytes, sh)
+        if s != 0:
+            raise RuntimeError(f"flce_backward: {_lib.STATUS_NAMES.get(s, s)}")
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    st = _lib.flce_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {_lib.STATUS_NAMES.get(st)}")
+    extra_mem = torch.cuda.max_memory_allocated(dev) - mem0
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    _lib.profile_enable(True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    prof = _lib.profile_read()
+    _lib.profile_enable(False)
+    st = _lib.flce_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {_lib.STATUS_NAMES.get(st)}")
+    ms = e0.elapsed_time(e1)
+    if ws > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+    value = ws * N / (ms_step / 1e3)
+
+    # ---- end to end through the public API with pinned host buffers
+    from chunked_lm_head_gb300 import api
+    h_host = torch.from_numpy(inp.h.view(np.int16)).pin_memory()
+    t_host = torch.from_numpy(inp.targets).pin_memory()
+    w_host = None if inp.weights is None else torch.from_numpy(inp.weights).pin_memory()
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    logp_host = torch.empty(N, dtype=torch.float32).pin_memory()
+    h_e = torch.empty((N, H), dtype=torch.int16, device=dev)
+    t_e = torch.empty(N, dtype=torch.int64, device=dev)
+    w_e = None if w_host is None else torch.empty(N, dtype=torch.float32, device=dev)
+
+    def e2e_step():
+        h_e.copy_(h_host, non_blocking=True)
+        t_e.copy_(t_host, non_blocking=True)
+        if w_e is not None:
+            w_e.copy_(w_host, non_blocking=True)
+        hb = h_e.view(torch.bfloat16)
+        out = api.forward(hb, W, t_e, w_e, chunk_rows, workspace=workspace)
+        api.backward(hb, W, t_e, w_e, out["lse"], g, chunk_rows, workspace=workspace)
+        loss_host.copy_(out["loss"].view(1), non_blocking=True)
+        logp_host.copy_(out["logp"], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e3 = torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e3.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e2.elapsed_time(e3) / e2e_steps
+    h2d = N * H * 2 + N * 8 + (0 if w_host is None else N * 4)
+    d2h = 4 + N * 4
+
+    # ---- roofline of the dominant kernel (algorithmic FLOPs / live event time)
+    peaks = load_peaks()
+    flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dlogits": 2.0 * N * V * H,
+                  "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
+    kern = {}
+    for k, (tot_ms, n) in prof.items():
+        if n:
+            kern[k] = {"ms_per_step": tot_ms / args.steps, "launches_per_step": n / args.steps,
+                       "share": None}
+    tot = sum(v["ms_per_step"] for v in kern.values())
+    for k in kern:
+        kern[k]["share"] = kern[k]["ms_per_step"] / tot if tot else None
+        if k in flops_step:
+            kern[k]["tflops"] = flops_step[k] / (kern[k]["ms_per_step"] / 1e3) / 1e12
+    dom = max((k for k in kern if k in GEMM_KINDS), key=lambda k: kern[k]["ms_per_step"])
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    launches_dom = kern[dom]["launches_per_step"]
+    achieved = kern[dom]["tflops"]
+    traffic = NCU_TRAFFIC_BYTES_PER_LAUNCH.get(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
+                "flops_per_launch": flops_step[dom] / launches_dom,
+                "launch_ms": kern[dom]["ms_per_step"] / launches_dom}
+    step_tflops = 8.0 * N * V * H / (ms_step / 1e3) / 1e12
+    gpu_launches = int(round(sum(n for _, n in prof.values())))
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            cpu = cpu_oracle_rate(inp, target_s=args.cpu_s)
+            cpu.pop("seconds", None)
+            cpu.pop("rows", None)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "N": N, "H": H, "V": V, "chunk_rows": chunk_rows,
+                       "targets": wl.targets, "l2": "inputs larger than L2 (W alone "
+                       f"{V * H * 2 / 1e9:.2f} GB > 129 MB); no flush",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "tflops": step_tflops,
+            "tensor_frac_of_peak": {"measured_burst": step_tflops / peaks["bf16_tflops"],
+                                    "measured_sustained": step_tflops / peak_tf,
+                                    "nominal_2250": step_tflops / 2250.0},
+            "roofline": roofline,
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": {"value": ws * N / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": gpu_launches,
+            "peak_extra_mem_bytes": int(extra_mem),
+            "workspace_bytes": ws_bytes,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="sft_16k", choices=WL.WORKLOAD_ORDER)
+    ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of the CPU-oracle sample")
+    ap.add_argument("--ref-step-s", type=float, default=8.0, help="reference arm: seconds per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,8 @@
+"""libflce: chunked fused LM-head cross-entropy on GB300 (sm_103a).
+
+The compute lives in the C-ABI CUDA library (include/flce.h, csrc/); this
+package holds its ctypes binding, a thin torch-facing API and the seeded
+synthetic workloads.
+"""
+from .api import (IGNORE_INDEX, LinearCrossEntropy, backward, forward,  # noqa: F401
+                  linear_cross_entropy, workspace_bytes)

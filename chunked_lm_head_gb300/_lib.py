@@ -1,0 +1,144 @@
+"""ctypes binding of libflce's C ABI (include/flce.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind these calls.  torch tensors are accepted for convenience and
+turned into raw device pointers; torch supplies device memory and streams.
+There is no fallback: if the library cannot be loaded the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import build as _build
+
+FLCE_OK = 0
+STATUS_NAMES = {
+    0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_BAD_TARGET",
+    3: "FLCE_ERR_UNSUPPORTED", 4: "FLCE_ERR_OOM", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TIMEOUT",
+}
+
+_c_i64 = ctypes.c_int64
+_c_vp = ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/flce.h
+SIGNATURES = {
+    "flce_forward": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
+                                    _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp,
+                                     _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, ctypes.c_size_t,
+                                     _c_vp]),
+    "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
+    "flce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "flce_device_status": (ctypes.c_int, [_c_vp]),
+    "flce_profile_enable": (ctypes.c_int, [ctypes.c_int]),
+    "flce_profile_num_kinds": (ctypes.c_int, []),
+    "flce_profile_kind_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "flce_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_int64)]),
+}
+
+_LIB = None
+
+
+class FlceError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def header_symbols() -> list[str]:
+    """Function names declared in include/flce.h."""
+    src = open(os.path.join(_build.INCLUDE, "flce.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"\b(flce_[a-z_]+)\s*\(", src)
+
+
+def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libflce.so (building it in-tree first when it is absent)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        if not build_if_missing:
+            raise FileNotFoundError(p)
+        _build.build()
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def check(fn: str, status: int) -> None:
+    if status != FLCE_OK:
+        raise FlceError(fn, status)
+
+
+def flce_forward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp, out_lse,
+                 out_loss, out_n_valid, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call; tensors or integer device pointers.  Returns the status."""
+    lib = load()
+    return lib.flce_forward(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), N, H, V, chunk_rows,
+                            ignore_index, _ptr(out_logp), _ptr(out_lse), _ptr(out_loss),
+                            _ptr(out_n_valid), _ptr(workspace), workspace_bytes,
+                            _stream_handle(stream))
+
+
+def flce_backward(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                  ignore_index, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call; tensors or integer device pointers.  Returns the status."""
+    lib = load()
+    return lib.flce_backward(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), _ptr(lse),
+                             float(grad_scale), _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
+                             ignore_index, _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_workspace_bytes(N, H, V, chunk_rows) -> int:
+    return int(load().flce_workspace_bytes(N, H, V, chunk_rows))
+
+
+def flce_status_string(status: int) -> str:
+    return load().flce_status_string(status).decode()
+
+
+def flce_device_status(stream=None) -> int:
+    return load().flce_device_status(_stream_handle(stream))
+
+
+def profile_enable(on: bool) -> None:
+    check("flce_profile_enable", load().flce_profile_enable(1 if on else 0))
+
+
+def profile_read() -> dict:
+    """{kernel kind: (total_ms, launches)} accumulated since profile_enable."""
+    lib = load()
+    out = {}
+    for k in range(lib.flce_profile_num_kinds()):
+        ms = ctypes.c_double()
+        n = ctypes.c_int64()
+        check("flce_profile_read", lib.flce_profile_read(k, ctypes.byref(ms), ctypes.byref(n)))
+        out[lib.flce_profile_kind_name(k).decode()] = (ms.value, n.value)
+    return out

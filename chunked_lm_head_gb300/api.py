@@ -1,0 +1,101 @@
+"""PyTorch-facing calls of libflce (device memory and streams from torch).
+
+Every arithmetic step runs in libflce's CUDA kernels; this module only checks
+tensor properties, allocates outputs and passes pointers.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+IGNORE_INDEX = -100
+
+
+def _check(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, weights):
+    if not (h.is_cuda and W.is_cuda and targets.is_cuda):
+        raise ValueError("h, W and targets must be CUDA tensors")
+    if h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("h and W must be bfloat16")
+    if targets.dtype != torch.int64:
+        raise ValueError("targets must be int64")
+    if h.dim() != 2 or W.dim() != 2 or h.shape[1] != W.shape[1] or targets.shape != (h.shape[0],):
+        raise ValueError("expected h[N,H], W[V,H], targets[N]")
+    if not (h.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
+        raise ValueError("h, W and targets must be contiguous")
+    if weights is not None:
+        if weights.dtype != torch.float32 or weights.shape != (h.shape[0],) or not weights.is_contiguous():
+            raise ValueError("weights must be a contiguous float32 [N] tensor")
+
+
+def workspace_bytes(N: int, H: int, V: int, chunk_rows: int) -> int:
+    return _lib.flce_workspace_bytes(N, H, V, chunk_rows)
+
+
+def forward(h, W, targets, weights=None, chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX,
+            workspace: torch.Tensor | None = None, stream=None):
+    """Returns dict(logp[N] f32, lse[N] f32, loss[] f32, n_valid[] i64), on device."""
+    _check(h, W, targets, weights)
+    N, H = h.shape
+    V = W.shape[0]
+    dev = h.device
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    n_valid = torch.empty((), dtype=torch.int64, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.flce_forward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, logp, lse,
+                           loss, n_valid, workspace, ws_bytes, stream)
+    _lib.check("flce_forward", st)
+    return {"logp": logp, "lse": lse, "loss": loss, "n_valid": n_valid}
+
+
+def backward(h, W, targets, weights, lse, grad_scale: float, chunk_rows: int = 256,
+             ignore_index: int = IGNORE_INDEX, need_dH: bool = True, need_dW: bool = True,
+             workspace: torch.Tensor | None = None, stream=None):
+    """Returns (dH[N,H] bf16 or None, dW[V,H] f32 or None)."""
+    _check(h, W, targets, weights)
+    N, H = h.shape
+    V = W.shape[0]
+    dH = torch.empty_like(h) if need_dH else None
+    dW = torch.empty((V, H), dtype=torch.float32, device=h.device) if need_dW else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.flce_backward(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                            ignore_index, workspace, ws_bytes, stream)
+    _lib.check("flce_backward", st)
+    return dH, dW
+
+
+class LinearCrossEntropy(torch.autograd.Function):
+    """loss = -sum(w * logp) / n_valid with logits recomputed in backward.
+
+    The forward keeps no logits; the backward recomputes them chunk by chunk
+    (the recompute-in-backward of Unsloth's offloaded log-softmax function).
+    """
+
+    @staticmethod
+    def forward(ctx, h, W, targets, weights, chunk_rows, ignore_index):
+        out = forward(h, W, targets, weights, chunk_rows, ignore_index)
+        ctx.save_for_backward(h, W, targets, weights if weights is not None else torch.empty(0),
+                              out["lse"], out["n_valid"])
+        ctx.has_weights = weights is not None
+        ctx.chunk_rows = chunk_rows
+        ctx.ignore_index = ignore_index
+        ctx.mark_non_differentiable(out["logp"], out["n_valid"])
+        return out["loss"], out["logp"], out["n_valid"]
+
+    @staticmethod
+    def backward(ctx, grad_loss, grad_logp, grad_n):
+        h, W, targets, weights, lse, n_valid = ctx.saved_tensors
+        weights = weights if ctx.has_weights else None
+        n = int(n_valid.item())
+        g = float(grad_loss.item()) / n if n > 0 else 0.0
+        dH, dW = backward(h, W, targets, weights, lse, g, ctx.chunk_rows, ctx.ignore_index,
+                          need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1])
+        return dH, dW, None, None, None, None
+
+
+def linear_cross_entropy(h, W, targets, weights=None, chunk_rows: int = 256,
+                         ignore_index: int = IGNORE_INDEX):
+    """Differentiable masked (weighted) mean NLL of softmax(h W^T); returns (loss, logp, n_valid)."""
+    return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index)

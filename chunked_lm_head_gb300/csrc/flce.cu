@@ -1,0 +1,722 @@
+// libflce: C-ABI entry points, host-side planning, tensor maps and the small
+// CUDA-core kernels (target prep, split-vocabulary combine, deterministic loss
+// reduction, split-K reduction of dH).  The tensor-core work lives in
+// gemm.cuh.  See include/flce.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <type_traits>
+#include <vector>
+
+#include "flce.h"
+#include "gemm.cuh"
+
+namespace flce {
+
+__device__ int g_device_error;  // bit DEVERR_TIMEOUT: a bounded wait ran out
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int SMALL_THREADS = 256;
+
+// ------------------------------------------------------------ small kernels
+
+// Target prep (mask step): the target-logit slots start as NaN so that a row
+// whose target is never met in any vocabulary tile (out of range) yields NaN;
+// optionally counts targets outside [0, V) that are not ignore_index.
+__global__ void prep_kernel(const int64_t* __restrict__ targets, int N, int V, long long ignore,
+                            float* __restrict__ zt, int* bad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < N) {
+    if (zt != nullptr) zt[i] = __int_as_float(0x7fc00000);
+    if (bad != nullptr) {
+      const long long t = targets[i];
+      if (t != ignore && (t < 0 || t >= V)) atomicAdd(bad, 1);
+    }
+  }
+}
+
+// Split-vocabulary combine: lse = M + log sum_s s_s 2^(m_s - M) (log2 domain,
+// converted to natural log), logp = z_t - lse on non-ignored rows, and this
+// block's share of sum(w * logp) and of the valid-row count.
+template <bool kLong>
+__global__ void combine_kernel(const float2* __restrict__ part, int S, int N,
+                               const float* __restrict__ zt, const int64_t* __restrict__ targets,
+                               const float* __restrict__ weights, long long ignore,
+                               float* __restrict__ out_logp, float* __restrict__ out_lse,
+                               double* __restrict__ blk_sum, long long* __restrict__ blk_cnt) {
+  using idx_t = typename std::conditional<kLong, long long, int>::type;
+  const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
+  double contrib = 0.0;
+  long long cnt = 0;
+  if (i < N) {
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, part[static_cast<idx_t>(s) * N + i].x);
+    float sum = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float2 q = part[static_cast<idx_t>(s) * N + i];
+      sum += q.y * exp2f(q.x - M);
+    }
+    const float lse = (M + log2f(sum)) * kLn2;
+    const long long t = targets[i];
+    const bool valid = t != ignore;
+    const float logp = valid ? zt[i] - lse : 0.f;
+    if (out_lse) out_lse[i] = lse;
+    if (out_logp) out_logp[i] = logp;
+    if (valid) {
+      cnt = 1;
+      contrib = static_cast<double>(weights ? weights[i] : 1.f) * static_cast<double>(logp);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
+    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
+  }
+  __shared__ double ssum[SMALL_THREADS / 32];
+  __shared__ long long scnt[SMALL_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) {
+    ssum[threadIdx.x >> 5] = contrib;
+    scnt[threadIdx.x >> 5] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0;
+    long long c = 0;
+    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
+      a += ssum[w];
+      c += scnt[w];
+    }
+    blk_sum[blockIdx.x] = a;
+    blk_cnt[blockIdx.x] = c;
+  }
+}
+
+// Loss = -sum(w logp) / n_valid over the block partials, in a fixed order
+// (deterministic run to run); 0 when n_valid == 0.
+__global__ void final_kernel(const double* __restrict__ blk_sum, const long long* __restrict__ blk_cnt,
+                             int nblk, float* out_loss, long long* out_n_valid) {
+  double a = 0.0;
+  long long c = 0;
+  for (int b = threadIdx.x; b < nblk; b += SMALL_THREADS) {
+    a += blk_sum[b];
+    c += blk_cnt[b];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_down_sync(0xffffffffu, a, off);
+    c += __shfl_down_sync(0xffffffffu, c, off);
+  }
+  __shared__ double ssum[SMALL_THREADS / 32];
+  __shared__ long long scnt[SMALL_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) {
+    ssum[threadIdx.x >> 5] = a;
+    scnt[threadIdx.x >> 5] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    long long n = 0;
+    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
+      s += ssum[w];
+      n += scnt[w];
+    }
+    if (out_n_valid) *out_n_valid = n;
+    if (out_loss) *out_loss = n > 0 ? static_cast<float>(-s / static_cast<double>(n)) : 0.f;
+  }
+}
+
+// dH[row0 + r, :] = bf16(sum over k-splits of the fp32 partials), split order fixed.
+template <bool kLong>
+__global__ void dh_reduce_kernel(const float* __restrict__ part, int splits, int rows, int rows_cap,
+                                 int H, int row0, uint16_t* __restrict__ dH) {
+  using idx_t = typename std::conditional<kLong, long long, int>::type;
+  const int h4 = H / 4;
+  const idx_t total = static_cast<idx_t>(rows) * h4;
+  for (idx_t e = static_cast<idx_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<idx_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(e / h4);
+    const int c = static_cast<int>(e - static_cast<idx_t>(r) * h4) * 4;
+    float4 s = *reinterpret_cast<const float4*>(part + static_cast<idx_t>(r) * H + c);
+    for (int k = 1; k < splits; ++k) {
+      const float4 q =
+          *reinterpret_cast<const float4*>(part + (static_cast<idx_t>(k) * rows_cap + r) * H + c);
+      s.x += q.x;
+      s.y += q.y;
+      s.z += q.z;
+      s.w += q.w;
+    }
+    *reinterpret_cast<uint2*>(dH + static_cast<idx_t>(row0 + r) * H + c) =
+        make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+  }
+}
+
+}  // namespace flce
+
+// ====================================================================== host
+namespace {
+
+using namespace flce;
+
+constexpr int kDefaultSms = 152;
+
+enum Kind { K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COUNT };
+const char* const kKindNames[K_COUNT] = {"prep_targets", "fwd_logits_lse", "fwd_combine",
+                                         "fwd_loss",     "bwd_dlogits",    "bwd_dH",
+                                         "bwd_dH_reduce", "bwd_dW"};
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_pending;
+double g_prof_ms[K_COUNT];
+long long g_prof_n[K_COUNT];
+
+struct ProfScope {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ProfScope(int k, cudaStream_t s) : kind(k), st(s) {
+    if (g_prof_on && cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess)
+      cudaEventRecord(a, st);
+  }
+  ~ProfScope() {
+    if (b != nullptr) {
+      cudaEventRecord(b, st);
+      g_prof_pending.push_back({kind, a, b});
+    }
+  }
+};
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  return n;
+}
+
+struct FwdPlan {
+  int m_tiles = 0, n_tiles = 0, k_blocks = 0, S = 1, tps = 1, units = 0, grid = 0, nblk = 0;
+};
+
+// Split the vocabulary tiles of every 128-row block into S contiguous ranges
+// so that (row blocks x S) units fill the SMs in near-whole waves.
+FwdPlan plan_forward(long long N, long long H, long long V, int sms) {
+  FwdPlan f;
+  f.m_tiles = static_cast<int>(ceil_div(N, BM));
+  f.n_tiles = static_cast<int>(ceil_div(V, BN));
+  f.k_blocks = static_cast<int>(ceil_div(H, BK));
+  f.nblk = static_cast<int>(ceil_div(N, SMALL_THREADS));
+  long long best = LLONG_MAX;
+  const int smax = std::min(f.n_tiles, 256);
+  for (int s = 1; s <= smax; ++s) {
+    const int tps = static_cast<int>(ceil_div(f.n_tiles, s));
+    const int se = static_cast<int>(ceil_div(f.n_tiles, tps));
+    const long long units = static_cast<long long>(f.m_tiles) * se;
+    const long long cost = ceil_div(std::max(units, 1LL), sms) * tps;
+    if (cost < best) {
+      best = cost;
+      f.S = se;
+      f.tps = tps;
+    }
+  }
+  f.units = f.m_tiles * f.S;
+  f.grid = std::min(f.units, sms);
+  return f;
+}
+
+struct BwdPlan {
+  long long R = 0, ldD = 0;
+  int dh_splits = 1;
+  int dh_kb_per_split = 1;
+};
+
+BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int sms) {
+  BwdPlan b;
+  b.R = round_up(std::max(1LL, chunk_rows), BM);
+  b.R = std::min(b.R, round_up(std::max(1LL, N), BM));
+  b.ldD = round_up(V, 8);
+  const long long tiles = ceil_div(b.R, BM) * ceil_div(H, BN);
+  const long long kb = ceil_div(V, BK);
+  int best_s = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= 16; ++s) {
+    if (s > 1 && kb / s < 8) break;
+    const double waves = static_cast<double>(tiles * s) / sms;
+    const double eff = waves / std::ceil(waves);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best_s = s;
+    }
+    if (eff >= 0.9) break;
+  }
+  b.dh_splits = best_s;
+  b.dh_kb_per_split = static_cast<int>(ceil_div(kb, best_s));
+  b.dh_splits = static_cast<int>(ceil_div(kb, b.dh_kb_per_split));
+  return b;
+}
+
+struct FwdLayout {
+  size_t zt = 0, part = 0, bsum = 0, bcnt = 0, bad = 0, total = 0;
+};
+FwdLayout fwd_layout(long long N, const FwdPlan& f) {
+  FwdLayout L;
+  size_t o = 0;
+  L.zt = o;
+  o += align256(static_cast<size_t>(N) * 4);
+  L.part = o;
+  o += align256(static_cast<size_t>(f.S) * N * 8);
+  L.bsum = o;
+  o += align256(static_cast<size_t>(f.nblk) * 8);
+  L.bcnt = o;
+  o += align256(static_cast<size_t>(f.nblk) * 8);
+  L.bad = o;
+  o += 256;
+  L.total = o;
+  return L;
+}
+
+struct BwdLayout {
+  size_t D = 0, dh_part = 0, bad = 0, total = 0;
+};
+BwdLayout bwd_layout(long long H, const BwdPlan& b) {
+  BwdLayout L;
+  size_t o = 0;
+  L.D = o;
+  o += align256(static_cast<size_t>(b.R) * b.ldD * 2);
+  L.dh_part = o;
+  if (b.dh_splits > 1) o += align256(static_cast<size_t>(b.dh_splits) * b.R * H * 4);
+  L.bad = o;
+  o += 256;
+  L.total = o;
+  return L;
+}
+
+bool sizes_ok(long long N, long long H, long long V) {
+  return N >= 0 && H > 0 && V > 0 && N < INT_MAX && H < INT_MAX && V < INT_MAX;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// --------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map: `inner` contiguous elements per row, `outer` rows of
+// `ld_elems` elements; box box_inner x box_outer with 128-byte swizzle;
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long ld_elems,
+              int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, bool kLong>
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                          cudaStream_t st) {
+  auto k = flce_gemm_kernel<MODE, kLong>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  k<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, st>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_gemm(bool kLong, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                        int grid, cudaStream_t st) {
+  return kLong ? launch_gemm_t<MODE, true>(a, b, p, grid, st)
+               : launch_gemm_t<MODE, false>(a, b, p, grid, st);
+}
+
+bool validate_env() {
+  const char* s = std::getenv("FLCE_VALIDATE");
+  return s != nullptr && s[0] != '\0' && s[0] != '0';
+}
+
+// Stream-ordered workspace: the caller's, or one allocated here and freed on
+// the same stream when the call ends.
+struct Workspace {
+  void* ptr = nullptr;
+  bool owned = false;
+  cudaStream_t st = nullptr;
+  ~Workspace() {
+    if (owned && ptr != nullptr) cudaFreeAsync(ptr, st);
+  }
+};
+
+flce_status get_workspace(Workspace& ws, void* user, size_t user_bytes, size_t need, cudaStream_t st) {
+  ws.st = st;
+  if (user != nullptr) {
+    if (user_bytes < need || !aligned(user, 256)) return FLCE_ERR_INVALID_ARG;
+    ws.ptr = user;
+    return FLCE_OK;
+  }
+  if (cudaMallocAsync(&ws.ptr, std::max<size_t>(need, 256), st) != cudaSuccess) {
+    cudaGetLastError();
+    ws.ptr = nullptr;
+    return FLCE_ERR_OOM;
+  }
+  ws.owned = true;
+  return FLCE_OK;
+}
+
+#define FLCE_CUDA_TRY(x)                 \
+  do {                                   \
+    if ((x) != cudaSuccess) {            \
+      cudaGetLastError();                \
+      return FLCE_ERR_CUDA;              \
+    }                                    \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG";
+    case FLCE_ERR_BAD_TARGET: return "FLCE_ERR_BAD_TARGET";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED";
+    case FLCE_ERR_OOM: return "FLCE_ERR_OOM";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+  }
+  return "FLCE_ERR_UNKNOWN";
+}
+
+size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
+  if (!sizes_ok(N, H, V)) return 0;
+  const int sms = device_sms();
+  const FwdLayout fl = fwd_layout(N, plan_forward(N, H, V, sms));
+  const BwdLayout bl = bwd_layout(H, plan_backward(N, H, V, chunk_rows, sms));
+  return std::max(fl.total, bl.total);
+}
+
+flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                         const float* weights, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                         int64_t ignore_index, float* out_logp, float* out_lse, float* out_loss,
+                         int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  (void)chunk_rows;
+  if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  if (!out_logp && !out_lse && !out_loss && !out_n_valid) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!h || !W || !targets)) return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(targets, 8) || !aligned(weights, 4) ||
+      !aligned(out_logp, 4) || !aligned(out_lse, 4) || !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = device_sms();
+  const FwdPlan f = plan_forward(N, H, V, sms);
+  const FwdLayout L = fwd_layout(N, f);
+  Workspace ws;
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  float* zt = reinterpret_cast<float*>(wb + L.zt);
+  float2* part = reinterpret_cast<float2*>(wb + L.part);
+  double* bsum = reinterpret_cast<double*>(wb + L.bsum);
+  long long* bcnt = reinterpret_cast<long long*>(wb + L.bcnt);
+  int* bad = reinterpret_cast<int*>(wb + L.bad);
+  const bool validate = validate_env();
+  const int Ni = static_cast<int>(N);
+
+  if (N > 0) {
+    if (validate) FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
+    {
+      ProfScope ps(K_PREP, st);
+      prep_kernel<<<static_cast<int>(ceil_div(N, SMALL_THREADS)), SMALL_THREADS, 0, st>>>(
+          targets, Ni, static_cast<int>(V), ignore_index, zt, validate ? bad : nullptr);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    if (validate) {
+      int nbad = 0;
+      FLCE_CUDA_TRY(cudaMemcpyAsync(&nbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st));
+      FLCE_CUDA_TRY(cudaStreamSynchronize(st));
+      if (nbad != 0) return FLCE_ERR_BAD_TARGET;
+    }
+    CUtensorMap tA, tB;
+    if (!make_map(&tA, h, H, N, H, BK, BM) || !make_map(&tB, W, H, V, H, BK, BN)) return FLCE_ERR_CUDA;
+    GemmParams p{};
+    p.m_tiles = f.m_tiles;
+    p.n_tiles = f.n_tiles;
+    p.k_blocks = f.k_blocks;
+    p.cols = f.S;
+    p.n_per_unit = f.tps;
+    p.kb_per_split = f.k_blocks;
+    p.num_units = f.units;
+    p.group_m = std::min(8, f.m_tiles);
+    p.row0 = 0;
+    p.rows = Ni;
+    p.rows_cap = Ni;
+    p.N = Ni;
+    p.H = static_cast<int>(H);
+    p.V = static_cast<int>(V);
+    p.ldD = 0;
+    p.targets = targets;
+    p.weights = weights;
+    p.ignore_index = ignore_index;
+    p.partials = part;
+    p.zt = zt;
+    int* err = nullptr;
+    FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+    p.err = err;
+    const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
+                       static_cast<long long>(f.S) * N >= INT_MAX;
+    {
+      ProfScope ps(K_FWD, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(kLong, tA, tB, p, f.grid, st));
+    }
+    {
+      ProfScope ps(K_COMBINE, st);
+      if (kLong)
+        combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
+                                                               ignore_index, out_logp, out_lse, bsum, bcnt);
+      else
+        combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
+                                                                ignore_index, out_logp, out_lse, bsum, bcnt);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+  }
+  if (out_loss || out_n_valid) {
+    ProfScope ps(K_FINAL, st);
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
+                                              reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
+}
+
+flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                          const float* weights, const float* lse, float grad_scale, flce_bf16* dH,
+                          float* dW, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                          int64_t ignore_index, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  if (!dH && !dW) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!h || !W || !targets || !lse)) return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(dH, 16) || !aligned(dW, 16) ||
+      !aligned(targets, 8) || !aligned(weights, 4) || !aligned(lse, 4))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (dW) FLCE_CUDA_TRY(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, st));
+    return FLCE_OK;
+  }
+  const int sms = device_sms();
+  const BwdPlan b = plan_backward(N, H, V, chunk_rows, sms);
+  const BwdLayout L = bwd_layout(H, b);
+  Workspace ws;
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  uint16_t* Dbuf = reinterpret_cast<uint16_t*>(wb + L.D);
+  float* dh_part = b.dh_splits > 1 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
+
+  if (validate_env()) {
+    int* bad = reinterpret_cast<int*>(wb + L.bad);
+    FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
+    prep_kernel<<<static_cast<int>(ceil_div(N, SMALL_THREADS)), SMALL_THREADS, 0, st>>>(
+        targets, static_cast<int>(N), static_cast<int>(V), ignore_index, nullptr, bad);
+    FLCE_CUDA_TRY(cudaGetLastError());
+    int nbad = 0;
+    FLCE_CUDA_TRY(cudaMemcpyAsync(&nbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st));
+    FLCE_CUDA_TRY(cudaStreamSynchronize(st));
+    if (nbad != 0) return FLCE_ERR_BAD_TARGET;
+  }
+
+  int* err = nullptr;
+  FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+  CUtensorMap h_k, W_k, W_mn, h_mn;
+  if (!make_map(&h_k, h, H, N, H, BK, BM) || !make_map(&W_k, W, H, V, H, BK, BN) ||
+      !make_map(&W_mn, W, H, V, H, 64, BK) || !make_map(&h_mn, h, H, N, H, 64, BK))
+    return FLCE_ERR_CUDA;
+  const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
+                     b.R * b.ldD >= INT_MAX || static_cast<long long>(N) * H >= INT_MAX ||
+                     static_cast<long long>(V) * H >= INT_MAX ||
+                     static_cast<long long>(b.dh_splits) * b.R * H >= INT_MAX;
+
+  GemmParams base{};
+  base.N = static_cast<int>(N);
+  base.H = static_cast<int>(H);
+  base.V = static_cast<int>(V);
+  base.ldD = static_cast<int>(b.ldD);
+  base.targets = targets;
+  base.weights = weights;
+  base.lse = lse;
+  base.grad_scale = grad_scale;
+  base.ignore_index = ignore_index;
+  base.D = Dbuf;
+  base.dH = dH;
+  base.dH_part = dh_part;
+  base.dW = dW;
+  base.err = err;
+  base.rows_cap = static_cast<int>(b.R);
+
+  int chunk = 0;
+  for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
+    const int rows = static_cast<int>(std::min(b.R, N - row0));
+    GemmParams p = base;
+    p.row0 = static_cast<int>(row0);
+    p.rows = rows;
+    // (1) recompute logits, dlogits chunk -> D[rows, ldD] bf16
+    {
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(rows, BM));
+      q.n_tiles = static_cast<int>(ceil_div(V, BN));
+      q.k_blocks = static_cast<int>(ceil_div(H, BK));
+      q.cols = q.n_tiles;
+      q.n_per_unit = 1;
+      q.kb_per_split = q.k_blocks;
+      q.num_units = q.m_tiles * q.n_tiles;
+      q.group_m = std::min(8, q.m_tiles);
+      ProfScope ps(K_DLOGITS, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(kLong, h_k, W_k, q, std::min(q.num_units, sms), st));
+    }
+    CUtensorMap D_k, D_mn;
+    if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) || !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
+      return FLCE_ERR_CUDA;
+    // (2) dH[rows] = D W
+    if (dH) {
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(rows, BM));
+      q.n_tiles = static_cast<int>(ceil_div(H, BN));
+      q.k_blocks = static_cast<int>(ceil_div(V, BK));
+      q.cols = q.n_tiles;
+      q.n_per_unit = 1;
+      q.kb_per_split = b.dh_kb_per_split;
+      const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
+      q.num_units = splits * q.m_tiles * q.n_tiles;
+      q.group_m = q.m_tiles;
+      q.dH_part = splits > 1 ? dh_part : nullptr;
+      {
+        ProfScope ps(K_DH, st);
+        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(kLong, D_k, W_mn, q, std::min(q.num_units, sms), st));
+      }
+      if (splits > 1) {
+        ProfScope ps(K_DH_REDUCE, st);
+        const long long total = static_cast<long long>(rows) * (H / 4);
+        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * sms));
+        if (kLong)
+          dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
+                                                                 static_cast<int>(H), p.row0, dH);
+        else
+          dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
+                                                                  static_cast<int>(H), p.row0, dH);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
+    }
+    // (3) dW (+)= D^T h[rows]
+    if (dW) {
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(V, BM));
+      q.n_tiles = static_cast<int>(ceil_div(H, BN));
+      q.k_blocks = static_cast<int>(ceil_div(rows, BK));
+      q.cols = q.n_tiles;
+      q.n_per_unit = 1;
+      q.kb_per_split = q.k_blocks;
+      q.num_units = q.m_tiles * q.n_tiles;
+      q.group_m = std::min(8, q.m_tiles);
+      q.dW_accumulate = chunk > 0 ? 1 : 0;
+      ProfScope ps(K_DW, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(kLong, D_mn, h_mn, q, std::min(q.num_units, sms), st));
+    }
+  }
+  return FLCE_OK;
+}
+
+flce_status flce_device_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return FLCE_ERR_CUDA;
+  }
+  int e = 0;
+  if (cudaMemcpyFromSymbol(&e, g_device_error, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return FLCE_ERR_CUDA;
+  }
+  if (e != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return FLCE_ERR_TIMEOUT;
+  }
+  return FLCE_OK;
+}
+
+flce_status flce_profile_enable(int enable) {
+  for (auto& r : g_prof_pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof_pending.clear();
+  for (int k = 0; k < K_COUNT; ++k) {
+    g_prof_ms[k] = 0.0;
+    g_prof_n[k] = 0;
+  }
+  g_prof_on = enable != 0;
+  return FLCE_OK;
+}
+
+int flce_profile_num_kinds(void) { return K_COUNT; }
+
+const char* flce_profile_kind_name(int kind) {
+  return (kind >= 0 && kind < K_COUNT) ? kKindNames[kind] : nullptr;
+}
+
+flce_status flce_profile_read(int kind, double* total_ms, int64_t* launches) {
+  if (kind < 0 || kind >= K_COUNT || !total_ms || !launches) return FLCE_ERR_INVALID_ARG;
+  flce_status s = FLCE_OK;
+  for (auto& r : g_prof_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      cudaGetLastError();
+      s = FLCE_ERR_CUDA;
+    } else {
+      g_prof_ms[r.kind] += ms;
+      g_prof_n[r.kind] += 1;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof_pending.clear();
+  *total_ms = g_prof_ms[kind];
+  *launches = g_prof_n[kind];
+  return s;
+}
+
+}  // extern "C"

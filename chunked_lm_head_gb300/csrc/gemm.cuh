@@ -1,0 +1,481 @@
+// Persistent tcgen05 GEMM engine of libflce and its four epilogues.
+//
+// One CTA per SM.  Warp 0 (one lane) streams operand tiles with TMA into a
+// 4-stage shared-memory ring; warp 1 (one lane) issues tcgen05.mma into one
+// of two 128x256 fp32 TMEM accumulators; warps 2-5 drain the other
+// accumulator with tcgen05.ld and run the mode's epilogue, so the epilogue of
+// tile i overlaps the MMAs of tile i+1.
+//
+// Modes (the four contractions of the chunked LM-head cross-entropy):
+//   FWD      Z = h W^T over a split of the vocabulary; epilogue keeps an online
+//            row max / sum of exp in registers (each thread owns one row of
+//            the accumulator, so no cross-thread reduction is needed) and
+//            gathers the target logit.  Emits per-(row, split) partials.
+//   DLOGITS  the same Z recomputed for one row chunk; epilogue forms
+//            D = (exp(Z - lse) - onehot(t)) * m * w * g in bf16.
+//   DH       dH[chunk rows] = D W         (K = vocabulary; W read MN-major)
+//   DW       dW (+)= D^T h[chunk rows]    (K = chunk rows; D and h MN-major)
+//
+// Sources: Unsloth, "Reinforcement Learning GRPO with 7x longer context",
+// sections "Flattened sequence-length chunking" (chunk logits are
+// hidden @ lm_head, upcast to fp32, log-softmaxed, target gathered) and
+// "Offloading activations for log-softmax" (backward recomputes the chunk);
+// TRL v1.13 article, speed & memory section (keep both GEMM operands bf16 on
+// the tensor cores instead of the fp32 SIMT path).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <type_traits>
+
+#include "ptx.cuh"
+
+namespace flce {
+
+constexpr int BM = 128;  // accumulator rows (TMEM lanes)
+constexpr int BN = 256;  // accumulator columns (fp32 TMEM columns)
+constexpr int BK = 64;   // one 128-byte swizzle row of bf16 per stage
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) swizzled box
+constexpr int EPI_WARPS = 4;
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+constexpr int SMEM_BAR_BYTES = 256;
+constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + SMEM_BAR_BYTES;
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
+constexpr long long DRAIN_LIMIT_CYCLES = 400000000LL;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Mode : int { MODE_FWD = 0, MODE_DLOGITS = 1, MODE_DH = 2, MODE_DW = 3 };
+
+// bit 0 of the device error word: a bounded wait ran out.
+constexpr int DEVERR_TIMEOUT = 1;
+
+struct GemmParams {
+  int m_tiles, n_tiles, k_blocks;
+  int cols;           // column units per k-split: FWD vocabulary splits, else n_tiles
+  int n_per_unit;     // FWD: vocabulary tiles per split; else 1
+  int kb_per_split;   // DH split-K: k-blocks per split; else k_blocks
+  int num_units;      // = k_splits * m_tiles * cols
+  int group_m;        // rasterisation: row tiles that share column units
+  int row0, rows;     // first global row of this pass, rows in this pass
+  int rows_cap;       // row capacity of the chunk buffers (DH split partials)
+  int N, H, V, ldD;
+  const int64_t* targets;
+  const float* weights;
+  const float* lse;
+  float grad_scale;
+  long long ignore_index;
+  float2* partials;   // FWD: [splits][N] (max*log2e, sum exp2)
+  float* zt;          // FWD: [N] target logit
+  uint16_t* D;        // DLOGITS out [rows_cap][ldD] bf16
+  uint16_t* dH;       // DH out [N][H] bf16 (single split)
+  float* dH_part;     // DH out [k_splits][rows_cap][H] fp32 (split-K)
+  float* dW;          // DW out [V][H] fp32
+  int dW_accumulate;
+  int* err;           // device error word
+};
+
+struct Unit {
+  int m, n0, n1, kb0, kb1, split;
+};
+
+template <int MODE>
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+  const int per_split = p.m_tiles * p.cols;
+  const int ks = u / per_split;
+  const int r = u - ks * per_split;
+  const int full_groups = p.m_tiles / p.group_m;
+  int first_m, gsize, local;
+  if (r < full_groups * p.group_m * p.cols) {
+    const int g = r / (p.group_m * p.cols);
+    first_m = g * p.group_m;
+    gsize = p.group_m;
+    local = r - g * p.group_m * p.cols;
+  } else {
+    first_m = full_groups * p.group_m;
+    gsize = p.m_tiles - first_m;
+    local = r - full_groups * p.group_m * p.cols;
+  }
+  Unit t;
+  t.m = first_m + local % gsize;
+  const int c = local / gsize;
+  t.n0 = c * p.n_per_unit;
+  t.n1 = min(p.n_tiles, t.n0 + p.n_per_unit);
+  t.kb0 = ks * p.kb_per_split;
+  t.kb1 = min(p.k_blocks, t.kb0 + p.kb_per_split);
+  t.split = (MODE == MODE_FWD) ? c : ks;
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
+// abort flag and the device error word) when the limit runs out, or when
+// another role of the CTA has already aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      *abort_flag = 1;
+      atomicOr(err, DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bounded wait used only while shutting down (copies or MMAs in flight).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > DRAIN_LIMIT_CYCLES) {
+      atomicOr(err, DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensorMap* tB,
+                                           uint32_t sA, uint32_t sB, uint32_t bar,
+                                           const GemmParams& p, int m, int n, int kb) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_DLOGITS) {
+    // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x 256)
+    tma_load_2d(sA, tA, bar, kb * BK, p.row0 + m * BM);
+    tma_load_2d(sB, tB, bar, kb * BK, n * BN);
+  } else if constexpr (MODE == MODE_DH) {
+    // A = D rows of this chunk (K-major over the vocabulary), B = W with the
+    // hidden dimension contiguous (MN-major): four 64-wide boxes
+    tma_load_2d(sA, tA, bar, kb * BK, m * BM);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * MN_BOX_BYTES, tB, bar, n * BN + 64 * j, kb * BK);
+  } else {
+    // A = D^T (vocabulary contiguous: MN-major), B = h (hidden contiguous:
+    // MN-major); K runs over the chunk's rows
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tma_load_2d(sA + j * MN_BOX_BYTES, tA, bar, m * BM + 64 * j, kb * BK);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      tma_load_2d(sB + j * MN_BOX_BYTES, tB, bar, n * BN + 64 * j, p.row0 + kb * BK);
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sA, uint32_t sB, bool first) {
+  constexpr bool A_MN = (MODE == MODE_DW);
+  constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+#pragma unroll
+  for (int k = 0; k < BK / UMMA_K; ++k) {
+    // K-major: 8-row core groups 1024 B apart, K advances 32 B inside the
+    // swizzle row.  MN-major: 64-wide MN boxes MN_BOX_BYTES apart, 8-row K
+    // groups 1024 B apart, K advances 16 rows = 2048 B.
+    const uint64_t ad = A_MN ? smem_desc_sw128(sA + k * 2048, MN_BOX_BYTES, 1024)
+                             : smem_desc_sw128(sA + k * 32, 16, 1024);
+    const uint64_t bd = B_MN ? smem_desc_sw128(sB + k * 2048, MN_BOX_BYTES, 1024)
+                             : smem_desc_sw128(sB + k * 32, 16, 1024);
+    umma_bf16(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
+  }
+}
+
+// v[j] for a run-time j in [0, 32) without dynamic register indexing (which
+// would move v to local memory): a 5-level select tree on the bits of j.
+__device__ __forceinline__ float select32(const float (&v)[32], int j) {
+  float a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = (j & 16) ? v[i + 16] : v[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = (j & 8) ? a[i + 8] : a[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (j & 4) ? b[i + 4] : b[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) d[i] = (j & 2) ? c[i + 2] : c[i];
+  return (j & 1) ? d[1] : d[0];
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int MODE, bool kLong>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ GemmParams p) {
+  using idx_t = typename std::conditional<kLong, long long, int>::type;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  // barrier layout: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit t = decode_unit<MODE>(p, u);
+        for (int n = t.n0; n < t.n1 && ok; ++n) {
+          for (int kb = t.kb0; kb < t.kb1; ++kb) {
+            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sA = sbase + stage * STAGE_BYTES;
+            mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+            load_stage<MODE>(&tmA, &tmB, sA, sA + A_STAGE_BYTES, full_bar(stage), p, t.m, n, kb);
+            ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // make sure no copy into this CTA's shared memory is still in flight
+      for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+        drain_bar(full_bar(static_cast<int>(i % STAGES)), static_cast<uint32_t>((i / STAGES) & 1), p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit t = decode_unit<MODE>(p, u);
+        for (int n = t.n0; n < t.n1 && ok; ++n) {
+          if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = t.kb0; kb < t.kb1; ++kb) {
+            if (!wait_bar(full_bar(stage), phase, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sA = sbase + stage * STAGE_BYTES;
+            mma_stage<MODE>(d_tmem, sA, sA + A_STAGE_BYTES, kb == t.kb0);
+            umma_commit(empty_bar(stage));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(tfull_bar(acc));
+          acc ^= 1u;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued by this thread has finished before TMEM is freed
+      umma_commit(drain);
+      drain_bar(drain, 0, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;       // accumulator row owned by this thread
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const Unit t = decode_unit<MODE>(p, u);
+      // per-unit row state
+      const int lr = t.m * BM + r;  // row inside this pass (FWD: global row)
+      const int grow = p.row0 + lr;
+      bool row_ok;
+      long long tgt = -1;
+      float run_m = -INFINITY, run_s = 0.f;  // FWD: log2-domain max and sum
+      float scale = 0.f, nl2 = 0.f;          // DLOGITS
+      if constexpr (MODE == MODE_DW) {
+        row_ok = lr < p.V;  // rows of the accumulator are vocabulary rows here
+      } else {
+        row_ok = lr < p.rows;
+      }
+      if constexpr (MODE == MODE_FWD) {
+        if (row_ok) tgt = p.targets[grow];
+      }
+      if constexpr (MODE == MODE_DLOGITS) {
+        if (row_ok) {
+          tgt = p.targets[grow];
+          const bool valid = tgt != p.ignore_index;
+          const float w = p.weights ? p.weights[grow] : 1.f;
+          scale = valid ? w * p.grad_scale : 0.f;
+          nl2 = -p.lse[grow] * kLog2e;
+        }
+      }
+      for (int n = t.n0; n < t.n1; ++n) {
+        int got = 0;
+        if (lane == 0) got = wait_bar(tfull_bar(acc), acc_phase, abort_flag, p.err) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + lane_addr + acc * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int col0 = n * BN + c * 32;
+          if constexpr (MODE == MODE_FWD) {
+            if (col0 + 32 > p.V) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= p.V) v[j] = -INFINITY;
+            }
+            float cm = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
+            const float nm = fmaxf(run_m, cm * kLog2e);
+            if (nm != -INFINITY) {
+              float a = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) a += exp2f(fmaf(v[j], kLog2e, -nm));
+              run_s = run_s * exp2f(run_m - nm) + a;
+              run_m = nm;
+            }
+            const long long tj = tgt - col0;
+            if (tj >= 0 && tj < 32) {
+              const float z = select32(v, static_cast<int>(tj));
+              if (row_ok) p.zt[grow] = z;
+            }
+          } else if constexpr (MODE == MODE_DLOGITS) {
+            uint32_t pk[16];
+            const long long tjl = tgt - col0;
+            const int tj = (tjl >= 0 && tjl < 32) ? static_cast<int>(tjl) : -1;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float d0 = 0.f, d1 = 0.f;
+              if (scale != 0.f) {
+                float p0 = exp2f(fmaf(v[j], kLog2e, nl2));
+                float p1 = exp2f(fmaf(v[j + 1], kLog2e, nl2));
+                if (j == tj) p0 -= 1.f;
+                if (j + 1 == tj) p1 -= 1.f;
+                d0 = (col0 + j < p.V) ? p0 * scale : 0.f;
+                d1 = (col0 + j + 1 < p.V) ? p1 * scale : 0.f;
+              }
+              pk[j / 2] = pack_bf16x2(d0, d1);
+            }
+            if (row_ok) {
+              uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (col0 + 8 * g < p.ldD)
+                  *reinterpret_cast<uint4*>(dst + 8 * g) =
+                      make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
+          } else if constexpr (MODE == MODE_DH) {
+            if (row_ok) {
+              if (p.dH_part == nullptr) {
+                uint16_t* dst = p.dH + static_cast<idx_t>(grow) * p.H + col0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                  if (col0 + 8 * g < p.H)
+                    *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(
+                        pack_bf16x2(v[8 * g], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                        pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+              } else {
+                float* dst = p.dH_part + (static_cast<idx_t>(t.split) * p.rows_cap + lr) * p.H + col0;
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                  if (col0 + 4 * g < p.H)
+                    *reinterpret_cast<float4*>(dst + 4 * g) =
+                        make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+              }
+            }
+          } else {  // MODE_DW
+            if (row_ok) {
+              float* dst = p.dW + static_cast<idx_t>(lr) * p.H + col0;
+              if (p.dW_accumulate) {
+                float4 old[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                  if (col0 + 4 * g < p.H) old[g] = *reinterpret_cast<const float4*>(dst + 4 * g);
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                  if (col0 + 4 * g < p.H)
+                    *reinterpret_cast<float4*>(dst + 4 * g) =
+                        make_float4(old[g].x + v[4 * g], old[g].y + v[4 * g + 1],
+                                    old[g].z + v[4 * g + 2], old[g].w + v[4 * g + 3]);
+              } else {
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                  if (col0 + 4 * g < p.H)
+                    *reinterpret_cast<float4*>(dst + 4 * g) =
+                        make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if constexpr (MODE == MODE_FWD) {
+        if (ok && row_ok)
+          p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(run_m, run_s);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace flce

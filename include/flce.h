@@ -1,0 +1,167 @@
+/*
+ * libflce -- chunked fused LM-head cross-entropy on one GB300 (sm_103a).
+ *
+ * Given hidden states h[N,H] and the LM-head weight W[V,H] (bf16, row-major),
+ * the library computes, without ever storing the N x V logit matrix:
+ *
+ *   z[i,v]  = sum_k h[i,k] W[v,k]
+ *   lse[i]  = log sum_v exp(z[i,v])
+ *   m[i]    = (targets[i] != ignore_index)
+ *   logp[i] = m[i] * (z[i,targets[i]] - lse[i])          (0 on ignored rows)
+ *   n_valid = sum_i m[i]
+ *   loss    = -sum_i m[i] w[i] logp[i] / n_valid         (0 when n_valid == 0)
+ *   D[i,v]  = (exp(z[i,v] - lse[i]) - [v == targets[i]]) * m[i] * w[i] * grad_scale
+ *   dH      = D W            dW = D^T h
+ *
+ * Sources: Unsloth, "Reinforcement Learning GRPO with 7x longer context",
+ * section "Flattened sequence-length chunking" (rows are the flattened batch x
+ * context tokens, taken in chunks; each chunk's logits are hidden @ lm_head,
+ * upcast to fp32, log-softmaxed, and the completion token's log-prob is
+ * gathered) and section "Offloading activations for log-softmax" (the
+ * backward recomputes the chunk's logits instead of storing them); TRL v1.13
+ * article "Training Beyond 1M Tokens", loss section (256 rows per chunk,
+ * chunk losses summed) and speed & memory section (bf16 operands on the
+ * tensor cores).  With w = 1 the loss is the masked mean NLL; with per-token
+ * weights (e.g. GRPO advantages) it is -sum(w logp)/sum(mask).
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers on the current CUDA device unless
+ *     stated otherwise; the caller owns every buffer and the stream; the
+ *     library never frees caller memory.
+ *   - bf16 arrays are passed as uint16_t bit patterns (flce_bf16).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous and stream-ordered; nothing is synchronised unless
+ *     stated.
+ *   - Host-side argument checks return a status before any launch.  No C++
+ *     exception crosses this interface.
+ *   - H must be a multiple of 8 and h, W, D-type buffers 16-byte aligned
+ *     (TMA rows are 16-byte aligned), else FLCE_ERR_UNSUPPORTED.
+ *   - N, H, V must each be < 2^31.
+ *   - Not thread-safe for concurrent calls from several host threads while
+ *     profiling is enabled.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(FLCE_BUILDING_LIBRARY) && defined(__GNUC__)
+#define FLCE_API __attribute__((visibility("default")))
+#else
+#define FLCE_API
+#endif
+
+typedef uint16_t flce_bf16;
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,  /* null/ill-sized argument, workspace too small */
+  FLCE_ERR_BAD_TARGET = 2,   /* validation mode: a target outside [0,V) */
+  FLCE_ERR_UNSUPPORTED = 3,  /* shape/alignment the kernels do not handle */
+  FLCE_ERR_OOM = 4,          /* library-side workspace allocation failed */
+  FLCE_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  FLCE_ERR_TIMEOUT = 6       /* a kernel's bounded wait ran out (device error word) */
+} flce_status;
+
+/*
+ * Forward: per-token log-probs, log-sum-exp, masked (weighted) mean loss.
+ *
+ *   h        [N,H] bf16, row-major (row i = token i of the flattened batch).
+ *   W        [V,H] bf16, row-major (the lm_head weight).
+ *   targets  [N] int64; each in [0,V) or == ignore_index.  A target outside
+ *            [0,V) that is not ignore_index is never read out of bounds: its
+ *            row's logp is NaN (and so is the loss) unless FLCE_VALIDATE=1 is
+ *            set in the environment, in which case the call synchronises the
+ *            stream after a check kernel and returns FLCE_ERR_BAD_TARGET
+ *            before any GEMM runs.
+ *   weights  [N] fp32 per-token weights, or NULL for all ones.
+ *   N, H, V  sizes (N may be 0).
+ *   chunk_rows  rows per chunk (the pages' chunk size, 256 in TRL).  The
+ *            forward keeps logits in tensor memory only, so its workspace is
+ *            O(N * splits) whatever chunk_rows is; results do not depend on it.
+ *   ignore_index  target value that marks a row without loss (-100 in PyTorch).
+ *   out_logp [N] fp32 or NULL.  0 on ignored rows.
+ *   out_lse  [N] fp32 or NULL.  Computed for every row, ignored or not;
+ *            flce_backward needs it.
+ *   out_loss [1] fp32 or NULL.
+ *   out_n_valid [1] int64 or NULL: the exact count of non-ignored rows.
+ *   workspace, workspace_bytes: device scratch of at least
+ *            flce_workspace_bytes(N,H,V,chunk_rows) bytes, 256-byte aligned;
+ *            or NULL, in which case the call allocates it stream-ordered
+ *            (cudaMallocAsync) and frees it (cudaFreeAsync) on `stream`.
+ * At least one of out_logp, out_lse, out_loss, out_n_valid must be non-NULL.
+ */
+FLCE_API flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                         const float* weights, int64_t N, int64_t H, int64_t V,
+                         int64_t chunk_rows, int64_t ignore_index, float* out_logp,
+                         float* out_lse, float* out_loss, int64_t* out_n_valid,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: dH = D W and dW = D^T h with
+ *   D[i,v] = (exp(z[i,v] - lse[i]) - [v == targets[i]]) * m[i] * w[i] * grad_scale.
+ *
+ *   lse      [N] fp32 from flce_forward (same h, W).
+ *   grad_scale  g, applied literally.  The library does not divide by n_valid:
+ *            for the gradient of the mean loss pass g = dLoss / n_valid.  An
+ *            arbitrary per-token upstream gradient dL/dlogp[i] is obtained with
+ *            weights[i] = -dL/dlogp[i] and g = 1.
+ *   dH       [N,H] bf16 output (overwritten; ignored rows get 0), or NULL to
+ *            skip the dH GEMM.
+ *   dW       [V,H] fp32 output (overwritten), or NULL to skip the dW GEMM
+ *            (frozen lm_head).
+ *   chunk_rows  rows whose dlogits are held at once: the backward walks the
+ *            rows in chunks of R = chunk_rows rounded up to 128, keeping one
+ *            bf16 dlogits chunk [R, V] (plus, for small chunks, split-K
+ *            partials of dH [splits, R, H] fp32) in the workspace: extra memory
+ *            O(chunk_rows * V), never O(N * V).  Results do not depend on it
+ *            beyond fp32 summation order of dW across chunks.
+ * Other arguments as in flce_forward.  Rows with an out-of-range target get
+ * D = softmax * w * g (no one-hot term); FLCE_VALIDATE=1 rejects them.
+ */
+FLCE_API flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                          const float* weights, const float* lse, float grad_scale,
+                          flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
+                          int64_t chunk_rows, int64_t ignore_index, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Workspace bytes that both flce_forward and flce_backward need for these
+ * sizes on the current device (0 on invalid sizes).  Host-only; if no device
+ * can be queried it assumes 152 SMs. */
+FLCE_API size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows);
+
+/* Static, human-readable name of a status. */
+FLCE_API const char* flce_status_string(flce_status s);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word on the current device: FLCE_ERR_TIMEOUT if a kernel gave up a bounded
+ * wait since the last call, FLCE_ERR_CUDA if the stream reports an error,
+ * else FLCE_OK. */
+FLCE_API flce_status flce_device_status(void* stream);
+
+/* ---- profiling (CUDA events around each launch, on the launch stream) ---- */
+
+/* Enable (1) or disable (0) per-kernel event timing; enabling clears totals. */
+FLCE_API flce_status flce_profile_enable(int enable);
+
+/* Number of kernel kinds the profiler distinguishes. */
+FLCE_API int flce_profile_num_kinds(void);
+
+/* Static name of kernel kind `kind` (NULL if out of range). */
+FLCE_API const char* flce_profile_kind_name(int kind);
+
+/* Synchronises on the recorded events and returns the accumulated device
+ * time (ms) and launch count of kernel kind `kind` since profiling was
+ * enabled.  Host pointers. */
+FLCE_API flce_status flce_profile_read(int kind, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

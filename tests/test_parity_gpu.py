@@ -1,0 +1,213 @@
+"""GPU parity: libflce (through its C ABI) against the fp64 oracle on the same
+seeded inputs.  Small cases are compared element by element in full; the large
+workloads on seeded samples of rows (and, for dW, through its linearity in the
+per-row weights: with weights zero outside the sampled rows, dW must equal
+those rows' contribution, which the oracle computes from their own lse)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from chunked_lm_head_gb300 import _lib
+from chunked_lm_head_gb300 import workloads as WL
+from oracle import flce_oracle as O
+
+from gpu_util import (LOSS_RTOL, assert_grad_close, assert_logp_close, np64, run_backward,
+                      run_forward, upload)
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_check(inp, chunk_rows, g_scale=None):
+    """Forward + backward of a small workload, every output against the oracle."""
+    wl = inp.wl
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, chunk_rows)
+    ref = O.forward(inp.h, inp.W, inp.targets, inp.weights, chunk_rows=chunk_rows)
+    assert nv == ref.n_valid
+    assert_logp_close(np64(logp), ref.logp, "logp")
+    assert_logp_close(np64(lse), ref.lse, "lse")
+    if ref.n_valid > 0:
+        assert loss == pytest.approx(ref.loss, rel=LOSS_RTOL, abs=1e-6)
+    else:
+        assert loss == 0.0
+    g = (1.0 / ref.n_valid if ref.n_valid else 1.0) if g_scale is None else g_scale
+    dH, dW = run_backward(h, W, t, w, lse, g, chunk_rows)
+    refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g, chunk_rows=chunk_rows)
+    if np.linalg.norm(refb.dH) == 0:
+        assert np.all(np64(dH) == 0)
+    else:
+        assert_grad_close(np64(dH), refb.dH, "dH")
+    if np.linalg.norm(refb.dW) == 0:
+        assert np.all(np64(dW) == 0)
+    else:
+        assert_grad_close(np64(dW), refb.dW, "dW")
+    return logp, lse, loss, dH, dW
+
+
+def test_tiny_workload_full():
+    _full_check(WL.make_inputs("tiny"), 16)
+
+
+def test_ragged_multi_tile_multi_chunk_weighted():
+    # 3 row tiles (last 44 rows), K = 200 (ragged 64-blocks), 5 vocabulary
+    # tiles (last 76 columns), 3 backward chunks, GRPO-style weights
+    wl = WL.custom("ragged", 300, 200, 1100, 128, w_std=0.05, ignore_frac=0.1, seed=101)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(5).standard_normal(300).astype(np.float32)
+    _full_check(inp, 128)
+
+
+def test_multi_tile_zipf():
+    wl = WL.custom("multi", 1000, 512, 5000, 256, w_std=0.04, targets="zipf", ignore_frac=0.03, seed=102)
+    _full_check(WL.make_inputs(wl), 256)
+
+
+def test_wide_hidden_ragged():
+    # H = 1032: five 256-wide dH tiles (last one 8 wide), 17 K-blocks
+    wl = WL.custom("wide", 130, 1032, 777, 64, w_std=0.03, seed=103)
+    _full_check(WL.make_inputs(wl), 64)
+
+
+@pytest.mark.parametrize("V", [1, 2, 8, 257])
+def test_small_vocabularies(V):
+    wl = WL.custom(f"v{V}", 40, 64, V, 32, w_std=0.5, seed=104 + V)
+    _full_check(WL.make_inputs(wl), 32)
+
+
+def test_empty_batch():
+    wl = WL.custom("empty", 0, 64, 300, 16, seed=105)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    h = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    t = torch.empty((0,), dtype=torch.int64, device="cuda")
+    logp, lse, loss, nv = run_forward(h, W, t, None, 16)
+    assert nv == 0 and loss == 0.0
+    dH, dW = run_backward(h, W, t, None, lse, 1.0, 16)
+    assert torch.all(dW == 0)
+
+
+def test_all_rows_ignored():
+    wl = WL.custom("allign", 150, 64, 500, 64, seed=106)
+    inp = WL.make_inputs(wl)
+    inp.targets[:] = WL.IGNORE_INDEX
+    _, _, loss, dH, dW = _full_check(inp, 64, g_scale=1.0)
+    assert loss == 0.0
+    assert torch.all(dH == 0) and torch.all(dW == 0)
+
+
+def test_results_do_not_depend_on_chunk_rows_and_are_deterministic():
+    wl = WL.custom("chunks", 700, 256, 3000, 128, w_std=0.05, targets="zipf", seed=107)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    outs = []
+    for cr in (128, 256, 700, 128):
+        logp, lse, loss, nv = run_forward(h, W, t, w, cr)
+        dH, dW = run_backward(h, W, t, w, lse, 1.0 / nv, cr)
+        outs.append((logp, lse, loss, dH, dW))
+    # forward never depends on chunk_rows: bitwise equal
+    for o in outs[1:]:
+        assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1]) and o[2] == outs[0][2]
+    # same chunking twice: bitwise equal (no atomics in any reduction)
+    assert torch.equal(outs[3][3], outs[0][3]) and torch.equal(outs[3][4], outs[0][4])
+    # other chunkings: only the fp32 summation order of dW across chunks changes
+    ref = O.backward(inp.h, inp.W, inp.targets, None, g=1.0 / int((inp.targets != -100).sum()))
+    for o in outs:
+        assert_grad_close(np64(o[3]), ref.dH, "dH")
+        assert_grad_close(np64(o[4]), ref.dW, "dW")
+
+
+def test_out_of_range_target():
+    wl = WL.custom("bad", 64, 64, 300, 64, seed=108)
+    inp = WL.make_inputs(wl)
+    inp.targets[5] = 300  # == V: out of range
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, 64)
+    assert np.isnan(np64(logp)[5]) and np.isnan(loss)
+    ok = np.arange(64) != 5
+    ref_lse = O.logsumexp_rows(O.logits(inp.h, inp.W))
+    assert_logp_close(np64(lse), ref_lse, "lse")
+    # validation mode rejects the call before any GEMM
+    os.environ["FLCE_VALIDATE"] = "1"
+    try:
+        N, H, V = 64, 64, 300
+        out = torch.empty(N, dtype=torch.float32, device="cuda")
+        st = _lib.flce_forward(h, W, t, None, N, H, V, 64, -100, out, None, None, None, None, 0)
+        assert st == 2
+        dH = torch.empty_like(h)
+        st = _lib.flce_backward(h, W, t, None, lse, 1.0, dH, None, N, H, V, 64, -100, None, 0)
+        assert st == 2
+        t[5] = 7
+        assert _lib.flce_forward(h, W, t, None, N, H, V, 64, -100, out, None, None, None, None, 0) == 0
+    finally:
+        del os.environ["FLCE_VALIDATE"]
+    assert _lib.flce_device_status() == 0
+    assert ok.sum() == 63
+
+
+def test_frozen_head_and_caller_workspace():
+    wl = WL.custom("ws", 260, 128, 900, 128, seed=109)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    nbytes = _lib.flce_workspace_bytes(260, 128, 900, 128)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    logp, lse, loss, nv = run_forward(h, W, t, w, 128, workspace=ws)
+    dH, dW = run_backward(h, W, t, w, lse, 1.0 / nv, 128, need_dW=False, workspace=ws)
+    assert dW is None
+    ref = O.backward(inp.h, inp.W, inp.targets, None, g=1.0 / nv)
+    assert_grad_close(np64(dH), ref.dH, "dH")
+    # a workspace one byte short is refused
+    small = ws[: nbytes - 256]
+    st = _lib.flce_forward(h, W, t, None, 260, 128, 900, 128, -100, logp, None, None, None,
+                           small, small.numel())
+    assert st == 1
+
+
+def test_single_chunk_workload_full():
+    """256 x 248,320 x 2,048: the TRL single-chunk benchmark shape, in full."""
+    _full_check(WL.make_inputs("single_chunk"), 256)
+
+
+def _sampled_check(name, n_rows, n_vocab):
+    inp = WL.make_inputs(name)
+    wl = inp.wl
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, wl.chunk_rows)
+    m = inp.targets != WL.IGNORE_INDEX
+    assert nv == int(m.sum())
+    g = 1.0 / nv
+    dH, dW = run_backward(h, W, t, w, lse, g, wl.chunk_rows)
+    rows = WL.sample_rows(wl.N, n_rows, seed=wl.seed)
+    vrows = WL.sample_rows(wl.V, n_vocab, seed=wl.seed + 1)
+    ref_lse, ref_logp = O.rows_forward(inp.h, inp.W, inp.targets, rows)
+    assert_logp_close(np64(logp)[rows], ref_logp, "logp")
+    assert_logp_close(np64(lse)[rows], ref_lse, "lse")
+    # loss from the kernel's own per-token log-probs (exact property at any size)
+    lp = np64(logp)
+    wt = np.ones(wl.N) if inp.weights is None else inp.weights.astype(np.float64)
+    assert loss == pytest.approx(-np.sum(m * wt * lp) / nv, rel=LOSS_RTOL)
+    ref_dH, ref_dWpart = O.rows_backward(inp.h, inp.W, inp.targets, rows, inp.weights, g=g,
+                                         vocab_rows=vrows)
+    assert_grad_close(np64(dH[torch.from_numpy(rows).cuda()]), ref_dH, "dH (sampled rows)")
+    assert np.all(np.isfinite(np64(dW[torch.from_numpy(vrows).cuda()])))
+    # dW through its linearity in the per-row weights
+    w0 = np.zeros(wl.N, dtype=np.float32)
+    w0[rows] = 1.0 if inp.weights is None else inp.weights[rows]
+    _, dW0 = run_backward(h, W, t, torch.from_numpy(w0).cuda(), lse, g, wl.chunk_rows, need_dH=False)
+    assert_grad_close(np64(dW0[torch.from_numpy(vrows).cuda()]), ref_dWpart, "dW (sampled rows x vocab)")
+
+
+@pytest.mark.slow
+def test_sft_16k_sampled():
+    _sampled_check("sft_16k", 512, 512)
+
+
+@pytest.mark.slow
+def test_grpo_32k_sampled():
+    _sampled_check("grpo_32k", 1024, 512)
+
+
+@pytest.mark.slow
+def test_long_131k_sampled():
+    _sampled_check("long_131k", 1024, 512)
