@@ -178,6 +178,11 @@ def gpu_arm(args):
     torch.cuda.set_device(local)
     lib = _lib.load()
     wl = WL.WORKLOADS[args.workload]
+    if args.shape:
+        import dataclasses
+        n_, h_, v_ = (int(x) for x in args.shape.split(","))
+        wl = dataclasses.replace(wl, name=f"{wl.name}@{n_}x{h_}x{v_}", N=n_, H=h_, V=v_,
+                                 packed_seqs=min(wl.packed_seqs, n_), grpo_seqs=0, prompt_len=0)
     chunk_rows = args.chunk_rows or wl.chunk_rows
     inp = WL.make_inputs(wl)
     N, H, V = wl.N, wl.H, wl.V
@@ -332,7 +337,7 @@ def gpu_arm(args):
 
     if rank == 0:
         cpu = None
-        if not args.no_cpu_baseline and ws == 1:
+        if not args.no_cpu_baseline and ws == 1 and not args.shape:
             cpu = cpu_oracle_rate(inp, target_s=args.cpu_s)
             cpu.pop("seconds", None)
             cpu.pop("rows", None)
@@ -370,6 +375,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="sft_16k", choices=WL.WORKLOAD_ORDER)
     ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--shape", default="", help="N,H,V override of the workload's sizes (profiling small cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of the CPU-oracle sample")
     ap.add_argument("--ref-step-s", type=float, default=8.0, help="reference arm: seconds per step")

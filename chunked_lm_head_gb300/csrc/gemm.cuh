@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               run_m = nm;
             }
             const long long tj = tgt - col0;
-            if (tj >= 0 && tj < 32) {
+            if (tj >= 0 && tj < 32 && tgt < p.V) {
               const float z = select32(v, static_cast<int>(tj));
               if (row_ok) p.zt[grow] = z;
             }

@@ -203,6 +203,55 @@ def rows_backward(h, W, targets, rows, weights=None, g: float = 1.0,
     return dH, D.T @ hf
 
 
+def rows_all(h, W, targets, rows, weights=None, g: float = 1.0,
+             ignore_index: int = IGNORE_INDEX, vocab_rows=None):
+    """rows_forward and rows_backward of the same rows from one logits block.
+
+    Returns (lse, logp, dH[rows], dW_part) with dW_part = D[rows]^T h[rows]
+    (restricted to ``vocab_rows`` when given).
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    hf = widen(np.asarray(h)[rows])
+    Wf = widen(W)
+    t = np.asarray(targets, dtype=np.int64)[rows]
+    m = _mask(t, Wf.shape[0], ignore_index)
+    w = _weights(None if weights is None else np.asarray(weights)[rows], len(rows))
+    z = hf @ Wf.T
+    lse, logp = selective_log_softmax(z, t, m)
+    D = dlogits(z, lse, t, m, w, g)
+    del z
+    dH = D @ Wf
+    if vocab_rows is not None:
+        D = D[:, np.asarray(vocab_rows, dtype=np.int64)]
+    return lse, logp, dH, D.T @ hf
+
+
+def vocab_rows_dW(h, W, targets, lse, vocab_rows, weights=None, g: float = 1.0,
+                  ignore_index: int = IGNORE_INDEX, block_rows: int = 4096):
+    """dW restricted to the given vocabulary rows: D[:, vocab_rows]^T h.
+
+    Needs every row's lse (the oracle's own full forward); the columns of D
+    are formed from z[:, vocab_rows] = h W[vocab_rows]^T only.
+    """
+    vr = np.asarray(vocab_rows, dtype=np.int64)
+    Wv = widen(np.asarray(W)[vr])
+    hN = np.asarray(h)
+    N = hN.shape[0]
+    t = np.asarray(targets, dtype=np.int64)
+    m = _mask(t, np.asarray(W).shape[0], ignore_index)
+    w = _weights(weights, N)
+    out = np.zeros((len(vr), hN.shape[1]))
+    for r0 in range(0, N, block_rows):
+        r1 = min(N, r0 + block_rows)
+        hf = widen(hN[r0:r1])
+        Dv = np.exp(hf @ Wv.T - np.asarray(lse[r0:r1], dtype=np.float64)[:, None])
+        hit = (t[r0:r1][:, None] == vr[None, :]) & m[r0:r1][:, None]
+        Dv -= hit
+        Dv *= (m[r0:r1] * w[r0:r1] * g)[:, None]
+        out += Dv.T @ hf
+    return out
+
+
 def logit_memory_gb(context_length: int, vocab_dim: int, batch_size: int = 1,
                     multiplier: int = 1) -> float:
     """Unsloth GRPO page, flattened-chunking section, Equations 1-3.

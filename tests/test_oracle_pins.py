@@ -259,6 +259,15 @@ def test_sampled_row_functions_match_full():
     assert np.allclose(lse, f.lse[rows], atol=1e-13) and np.allclose(logp, f.logp[rows], atol=1e-13)
     dH, dWp = O.rows_backward(h, W, t, np.arange(40), w, g=0.1, vocab_rows=[1, 22])
     assert np.allclose(dH, b.dH, atol=1e-13) and np.allclose(dWp, b.dW[[1, 22]], atol=1e-13)
+    lse2, logp2, dH2, dWp2 = O.rows_all(h, W, t, rows, w, g=0.1, vocab_rows=[1, 22])
+    assert np.allclose(lse2, f.lse[rows], atol=1e-13) and np.allclose(logp2, f.logp[rows], atol=1e-13)
+    assert np.allclose(dH2, b.dH[rows], atol=1e-13)
+    w_rows = np.zeros(40)
+    w_rows[rows] = w[rows]
+    assert np.allclose(dWp2, O.backward(h, W, t, w_rows, g=0.1).dW[[1, 22]], atol=1e-13)
+    # dW columns from every row's lse
+    vr = [0, 7, 22]
+    assert np.allclose(O.vocab_rows_dW(h, W, t, f.lse, vr, w, g=0.1, block_rows=16), b.dW[vr], atol=1e-13)
     # linearity in the per-row weights: weights zero outside a row subset keep
     # only those rows' dW contribution
     w0 = np.zeros(40)
