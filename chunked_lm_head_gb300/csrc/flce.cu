@@ -327,37 +327,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map: `inner` contiguous elements per row, `outer` rows of
-// `ld_elems` elements; box box_inner x box_outer with 128-byte swizzle;
-// out-of-range elements read as zero.
-bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long ld_elems,
-              int box_inner, int box_outer) {
+// 2-D map: `inner` contiguous elements per row, `outer` rows of `ld_elems`
+// elements; box box_inner x box_outer with 128-byte swizzle; out-of-range
+// elements read as zero (loads) or are skipped (stores).
+bool make_map_t(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, long long inner,
+                long long outer, long long ld_elems, int box_inner, int box_outer) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * esize};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long ld_elems,
+              int box_inner, int box_outer) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld_elems, box_inner,
+                    box_outer);
 }
 
 template <int MODE, bool kLong>
-cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                          cudaStream_t st) {
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                          const GemmParams& p, int grid, cudaStream_t st) {
   auto k = flce_gemm_kernel<MODE, kLong>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  k<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, st>>>(a, b, p);
+  k<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, st>>>(a, b, c, p);
   return cudaGetLastError();
 }
 
+// `c` is the output map of the modes that write through TMA (dW); the other
+// modes ignore it.
 template <int MODE>
-cudaError_t launch_gemm(bool kLong, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                        int grid, cudaStream_t st) {
-  return kLong ? launch_gemm_t<MODE, true>(a, b, p, grid, st)
-               : launch_gemm_t<MODE, false>(a, b, p, grid, st);
+cudaError_t launch_gemm(bool kLong, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const GemmParams& p, int grid, cudaStream_t st) {
+  return kLong ? launch_gemm_t<MODE, true>(a, b, c, p, grid, st)
+               : launch_gemm_t<MODE, false>(a, b, c, p, grid, st);
 }
 
 bool validate_env() {
@@ -498,7 +506,7 @@ flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* 
                        static_cast<long long>(f.S) * N >= INT_MAX;
     {
       ProfScope ps(K_FWD, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(kLong, tA, tB, p, f.grid, st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(kLong, tA, tB, tB, p, f.grid, st));
     }
     {
       ProfScope ps(K_COMBINE, st);
@@ -561,9 +569,11 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
 
   int* err = nullptr;
   FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
-  CUtensorMap h_k, W_k, W_mn, h_mn;
+  CUtensorMap h_k, W_k, W_mn, h_mn, dW_map;
   if (!make_map(&h_k, h, H, N, H, BK, BM) || !make_map(&W_k, W, H, V, H, BK, BN) ||
       !make_map(&W_mn, W, H, V, H, 64, BK) || !make_map(&h_mn, h, H, N, H, 64, BK))
+    return FLCE_ERR_CUDA;
+  if (dW && !make_map_t(&dW_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, H, V, H, 32, 32))
     return FLCE_ERR_CUDA;
   const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
                      b.R * b.ldD >= INT_MAX || static_cast<long long>(N) * H >= INT_MAX ||
@@ -605,7 +615,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
       q.num_units = q.m_tiles * q.n_tiles;
       q.group_m = std::min(8, q.m_tiles);
       ProfScope ps(K_DLOGITS, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(kLong, h_k, W_k, q, std::min(q.num_units, sms), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(kLong, h_k, W_k, W_k, q, std::min(q.num_units, sms), st));
     }
     CUtensorMap D_k, D_mn;
     if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) || !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
@@ -625,7 +635,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
       q.dH_part = splits > 1 ? dh_part : nullptr;
       {
         ProfScope ps(K_DH, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(kLong, D_k, W_mn, q, std::min(q.num_units, sms), st));
+        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(kLong, D_k, W_mn, W_mn, q, std::min(q.num_units, sms), st));
       }
       if (splits > 1) {
         ProfScope ps(K_DH_REDUCE, st);
@@ -653,7 +663,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
       q.group_m = std::min(8, q.m_tiles);
       q.dW_accumulate = chunk > 0 ? 1 : 0;
       ProfScope ps(K_DW, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(kLong, D_mn, h_mn, q, std::min(q.num_units, sms), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(kLong, D_mn, h_mn, dW_map, q, std::min(q.num_units, sms), st));
     }
   }
   return FLCE_OK;

@@ -44,8 +44,13 @@ constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) swizzled box
 constexpr int EPI_WARPS = 4;
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+// dW epilogue staging: per epilogue warp two 32x32 fp32 boxes (128B-swizzled)
+// handed to TMA store / reduce-add.
+constexpr int OUT_BOX_BYTES = 32 * 32 * 4;
+constexpr int OUT_STAGE_BYTES = EPI_WARPS * 2 * OUT_BOX_BYTES;
 constexpr int SMEM_BAR_BYTES = 256;
-constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + SMEM_BAR_BYTES;
+constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_STAGE_BYTES + SMEM_BAR_BYTES;
+static_assert(GEMM_SMEM_BYTES <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 constexpr long long DRAIN_LIMIT_CYCLES = 400000000LL;
 
@@ -208,12 +213,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int MODE, bool kLong>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t out_stage = sbase + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + OUT_STAGE_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   // barrier layout: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -435,26 +441,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
             }
           } else {  // MODE_DW
-            if (row_ok) {
-              float* dst = p.dW + static_cast<idx_t>(lr) * p.H + col0;
-              if (p.dW_accumulate) {
-                float4 old[8];
+            // stage this warp's 32 x 32 box (row = lane) in 128B-swizzled
+            // shared memory, then one lane hands it to TMA: a plain store on
+            // the first row chunk, an fp32 reduce-add in L2 afterwards.  Rows
+            // and columns outside dW are clipped by TMA.
+            const uint32_t box = out_stage + (warp - 2) * (2 * OUT_BOX_BYTES) + (c & 1) * OUT_BOX_BYTES;
+            if (lane == 0) bulk_wait_read<1>();  // the copy that last used this box has read it
+            __syncwarp();
+            const uint32_t row_addr = box + lane * 128;
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                  if (col0 + 4 * g < p.H) old[g] = *reinterpret_cast<const float4*>(dst + 4 * g);
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                  if (col0 + 4 * g < p.H)
-                    *reinterpret_cast<float4*>(dst + 4 * g) =
-                        make_float4(old[g].x + v[4 * g], old[g].y + v[4 * g + 1],
-                                    old[g].z + v[4 * g + 2], old[g].w + v[4 * g + 3]);
-              } else {
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                  if (col0 + 4 * g < p.H)
-                    *reinterpret_cast<float4*>(dst + 4 * g) =
-                        make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            for (int g = 0; g < 8; ++g)
+              st_shared_v4(row_addr + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                           v[4 * g + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int vrow0 = t.m * BM + q * 32;
+              if (col0 < p.H && vrow0 < p.V) {  // boxes wholly outside dW are skipped
+                if (p.dW_accumulate)
+                  tma_reduce_add_2d(&tmC, box, col0, vrow0);
+                else
+                  tma_store_2d(&tmC, box, col0, vrow0);
               }
+              bulk_commit();
             }
           }
         }
@@ -471,6 +480,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
+  if constexpr (MODE == MODE_DW) {
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // dW boxes written before the CTA retires
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
