@@ -18,7 +18,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 import numpy as np
@@ -34,7 +33,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "source": "fallback"}
 # DRAM bytes per launch of each kernel kind from the committed ncu capture
 # (profiles/); None when no capture of the current kernel exists.
-NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {}
+# bwd_dW: profiles/bwd_dW_8192x4096x32768.md, scaled from V = 32,768 to the
+# workload's vocabulary (1 store launch + 3 reduce-add launches per step).
+NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {"bwd_dW": 6.37e9}
+NCU_TRAFFIC_WORKLOAD = "sft_16k"
 
 
 def load_peaks() -> dict:
@@ -51,6 +53,22 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Tokens/s of the whole job: every rank's rows over the slowest rank's step time."""
+    return world * rows_per_rank / (ms_per_step / 1e3)
 
 
 # ------------------------------------------------------------------ clocks
@@ -124,9 +142,10 @@ def cpu_oracle_rate(inp, target_s: float = 12.0, max_rows: int = 4096) -> dict:
 
     k = 16
     dt = run(k)
-    if dt < target_s / 4 and k < max_rows:
-        k = int(min(max_rows, max(k, k * target_s / max(dt, 1e-3))))
-        k = min(k, wl.N)
+    for _ in range(3):  # grow the sample until it is about target_s of work
+        if dt >= target_s / 2 or k >= min(max_rows, wl.N):
+            break
+        k = int(min(max_rows, wl.N, max(2 * k, k * target_s / max(dt, 1e-3))))
         dt = run(k)
     try:
         cores = len(os.sched_getaffinity(0))
@@ -262,13 +281,9 @@ def gpu_arm(args):
     st = _lib.flce_device_status(sh)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {_lib.STATUS_NAMES.get(st)}")
-    ms = e0.elapsed_time(e1)
-    if ws > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_max(e0.elapsed_time(e1), device=dev)
     ms_step = ms / args.steps
-    value = ws * N / (ms_step / 1e3)
+    value = whole_job_rate(N, ws, ms_step)
 
     # ---- end to end through the public API with pinned host buffers
     from chunked_lm_head_gb300 import api
@@ -304,7 +319,7 @@ def gpu_arm(args):
             e2e_step()
         e3.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e2.elapsed_time(e3) / e2e_steps
+    e2e_ms = reduce_max(e2.elapsed_time(e3), device=dev) / e2e_steps
     h2d = N * H * 2 + N * 8 + (0 if w_host is None else N * 4)
     d2h = 4 + N * 4
 
@@ -326,7 +341,8 @@ def gpu_arm(args):
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     launches_dom = kern[dom]["launches_per_step"]
     achieved = kern[dom]["tflops"]
-    traffic = NCU_TRAFFIC_BYTES_PER_LAUNCH.get(dom)
+    traffic = NCU_TRAFFIC_BYTES_PER_LAUNCH.get(dom) if (wl.name == NCU_TRAFFIC_WORKLOAD
+                                                         and chunk_rows == 4096) else None
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
@@ -357,7 +373,7 @@ def gpu_arm(args):
             "kernels": kern,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "e2e": {"value": ws * N / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": whole_job_rate(N, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": gpu_launches,
             "peak_extra_mem_bytes": int(extra_mem),
