@@ -29,6 +29,8 @@ SIGNATURES = {
     "flce_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp,
                                      _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, ctypes.c_size_t,
                                      _c_vp]),
+    "flce_forward_static_scratch": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
+                                                   _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
     "flce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "flce_device_status": (ctypes.c_int, [_c_vp]),
@@ -114,6 +116,15 @@ def flce_backward(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chun
     return lib.flce_backward(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), _ptr(lse),
                              float(grad_scale), _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
                              ignore_index, _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_forward_static_scratch(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp,
+                                out_lse, out_loss, out_n_valid, stream=None) -> int:
+    """Raw C call of the allocation-free forward (library-owned scratch)."""
+    lib = load()
+    return lib.flce_forward_static_scratch(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), N, H, V,
+                                           chunk_rows, ignore_index, _ptr(out_logp), _ptr(out_lse),
+                                           _ptr(out_loss), _ptr(out_n_valid), _stream_handle(stream))
 
 
 def flce_workspace_bytes(N, H, V, chunk_rows) -> int:

@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <type_traits>
 #include <vector>
 
@@ -730,3 +731,74 @@ flce_status flce_profile_read(int kind, double* total_ms, int64_t* launches) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Forward for callers that cannot allocate device memory.
+//
+// Some callers are not allowed to allocate at all: code that runs while a
+// CUDA graph is being captured (an allocation there would be recorded or is
+// forbidden), inference runtimes that own every byte of device memory through
+// a fixed pool, and callers that must keep a constant memory footprint.  This
+// entry point serves them: it takes the same inputs and outputs as
+// flce_forward, but its scratch lives in one file-scope device array that the
+// library owns, so nothing is allocated or freed by any call.
+//
+// The array is a fixed 16 MiB, resident on every device that loads this
+// library until the process exits.  On the host its name is only a stand-in
+// for the device copy, never a device address: the address is looked up once
+// per device with cudaGetSymbolAddress (device code could name the array
+// directly, host code must not).
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_flce_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxStaticScratchDevices = 128;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[kMaxStaticScratchDevices];
+
+// Device address of g_flce_static_scratch on the current device (looked up on
+// the first call per device, with that device current).
+flce_status static_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FLCE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxStaticScratchDevices) return FLCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_flce_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return FLCE_ERR_CUDA;
+    }
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return FLCE_OK;
+}
+}  // namespace
+
+extern "C" flce_status flce_forward_static_scratch(const flce_bf16* h, const flce_bf16* W,
+                                                   const int64_t* targets, const float* weights,
+                                                   int64_t N, int64_t H, int64_t V,
+                                                   int64_t chunk_rows, int64_t ignore_index,
+                                                   float* out_logp, float* out_lse, float* out_loss,
+                                                   int64_t* out_n_valid, void* stream) {
+  if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  const size_t need = fwd_layout(N, plan_forward(N, H, V, device_sms())).total;
+  if (need > kStaticScratchBytes) return FLCE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const flce_status s = static_scratch_address(&scratch);
+  if (s != FLCE_OK) return s;
+  // Every scratch word is written by this call before it is read (target
+  // slots by the prep kernel, partials by the GEMM, block sums by the
+  // combine, the validation counter by a memset), so stale contents of an
+  // earlier call never leak into the result.
+  return flce_forward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp, out_lse,
+                      out_loss, out_n_valid, scratch, kStaticScratchBytes, stream);
+}

@@ -130,6 +130,37 @@ FLCE_API flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const
                           int64_t chunk_rows, int64_t ignore_index, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/*
+ * Forward that allocates nothing (no counterpart on the source pages: the
+ * method itself does not need it).
+ *
+ * For callers that may not allocate device memory at all -- code running
+ * while a CUDA graph is captured, runtimes that hand out every byte of device
+ * memory from their own fixed pool, callers that must keep a constant
+ * footprint.  Same arguments and results as flce_forward with workspace =
+ * NULL, except that no workspace is allocated: the call uses a 16 MiB scratch
+ * array that the library keeps in device memory on every device that loads it,
+ * for the life of the process.
+ *   - Returns FLCE_ERR_UNSUPPORTED, before any launch, when the forward's
+ *     scratch for these sizes exceeds 16 MiB (about N * (4 + 8 * S) bytes with
+ *     S <= ceil(V / 256) vocabulary splits; e.g. N = 16,384 at V = 151,936
+ *     needs about 2.6 MiB).
+ *   - The first call on each device looks up the array's device address (a
+ *     one-time cudaGetSymbolAddress); make that first call outside any stream
+ *     capture.
+ *   - All calls share the one array: calls whose kernels may overlap on the
+ *     GPU (different streams without ordering between them) race on it and
+ *     must not be issued.  Each call writes every scratch word it reads, so
+ *     what an earlier call left there does not affect the result.
+ *   - Calls no cudaMalloc/cudaFree or other allocating routine.
+ */
+FLCE_API flce_status flce_forward_static_scratch(const flce_bf16* h, const flce_bf16* W,
+                                                 const int64_t* targets, const float* weights,
+                                                 int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                                                 int64_t ignore_index, float* out_logp,
+                                                 float* out_lse, float* out_loss,
+                                                 int64_t* out_n_valid, void* stream);
+
 /* Workspace bytes that both flce_forward and flce_backward need for these
  * sizes on the current device (0 on invalid sizes).  Host-only; if no device
  * can be queried it assumes 152 SMs. */
