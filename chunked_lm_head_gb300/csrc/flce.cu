@@ -215,11 +215,12 @@ struct FwdPlan {
   int m_tiles = 0, n_tiles = 0, k_blocks = 0, S = 1, tps = 1, units = 0, grid = 0, nblk = 0;
 };
 
-// Split the vocabulary tiles of every 128-row block into S contiguous ranges
-// so that (row blocks x S) units fill the SMs in near-whole waves.
-FwdPlan plan_forward(long long N, long long H, long long V, int sms) {
+// Split the vocabulary tiles of every row tile (tm rows) into S contiguous
+// ranges so that (row tiles x S) units fill the persistent workers in
+// near-whole waves.
+FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm) {
   FwdPlan f;
-  f.m_tiles = static_cast<int>(ceil_div(N, BM));
+  f.m_tiles = static_cast<int>(ceil_div(N, tm));
   f.n_tiles = static_cast<int>(ceil_div(V, BN));
   f.k_blocks = static_cast<int>(ceil_div(H, BK));
   f.nblk = static_cast<int>(ceil_div(N, SMALL_THREADS));
@@ -229,7 +230,7 @@ FwdPlan plan_forward(long long N, long long H, long long V, int sms) {
     const int tps = static_cast<int>(ceil_div(f.n_tiles, s));
     const int se = static_cast<int>(ceil_div(f.n_tiles, tps));
     const long long units = static_cast<long long>(f.m_tiles) * se;
-    const long long cost = ceil_div(std::max(units, 1LL), sms) * tps;
+    const long long cost = ceil_div(std::max(units, 1LL), workers) * tps;
     if (cost < best) {
       best = cost;
       f.S = se;
@@ -237,7 +238,7 @@ FwdPlan plan_forward(long long N, long long H, long long V, int sms) {
     }
   }
   f.units = f.m_tiles * f.S;
-  f.grid = std::min(f.units, sms);
+  f.grid = std::min(f.units, workers);
   return f;
 }
 
@@ -247,18 +248,19 @@ struct BwdPlan {
   int dh_kb_per_split = 1;
 };
 
-BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int sms) {
+BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int workers,
+                      int tm) {
   BwdPlan b;
   b.R = round_up(std::max(1LL, chunk_rows), BM);
   b.R = std::min(b.R, round_up(std::max(1LL, N), BM));
   b.ldD = round_up(V, 8);
-  const long long tiles = ceil_div(b.R, BM) * ceil_div(H, BN);
+  const long long tiles = ceil_div(b.R, tm) * ceil_div(H, BN);
   const long long kb = ceil_div(V, BK);
   int best_s = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && kb / s < 8) break;
-    const double waves = static_cast<double>(tiles * s) / sms;
+    const double waves = static_cast<double>(tiles * s) / workers;
     const double eff = waves / std::ceil(waves);
     if (eff > best_eff + 1e-9) {
       best_eff = eff;
@@ -350,23 +352,86 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer
                     box_outer);
 }
 
-template <int MODE, bool kLong>
+template <int MODE, bool kLong, int CG>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                          const GemmParams& p, int grid, cudaStream_t st) {
-  auto k = flce_gemm_kernel<MODE, kLong>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+                          const GemmParams& p, int workers, cudaStream_t st) {
+  auto k = flce_gemm_kernel<MODE, kLong, CG>;
+  constexpr int smem = TileCfg<CG>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, st>>>(a, b, c, p);
+  if constexpr (CG == 1) {
+    k<<<workers, GEMM_THREADS, smem, st>>>(a, b, c, p);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * workers, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k, a, b, c, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
-// `c` is the output map of the modes that write through TMA (dW); the other
-// modes ignore it.
+// `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
+// tile loop.  `c` is the output map of the modes that write through TMA (dW);
+// the other modes ignore it.
 template <int MODE>
-cudaError_t launch_gemm(bool kLong, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                        const GemmParams& p, int grid, cudaStream_t st) {
-  return kLong ? launch_gemm_t<MODE, true>(a, b, c, p, grid, st)
-               : launch_gemm_t<MODE, false>(a, b, c, p, grid, st);
+cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st) {
+  if (cg == 2)
+    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, p, workers, st)
+                 : launch_gemm_t<MODE, false, 2>(a, b, c, p, workers, st);
+  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, p, workers, st)
+               : launch_gemm_t<MODE, false, 1>(a, b, c, p, workers, st);
+}
+
+// CTA group of the GEMMs: 2 (SM pairs, 256-row tiles) unless FLCE_CTA_GROUP=1.
+int cta_group() {
+  const char* s = std::getenv("FLCE_CTA_GROUP");
+  return (s != nullptr && s[0] == '1') ? 1 : 2;
+}
+
+// Persistent workers the GPU holds at once: CTAs, or co-resident CTA pairs.
+int device_workers(int cg) {
+  const int sms = device_sms();
+  if (cg == 1) return sms;
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return sms / 2;
+  }
+  if (dev == cached_dev && cached > 0) return cached;
+  int n = 0;
+  auto k = flce_gemm_kernel<MODE_FWD, false, 2>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = TileCfg<2>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<2>::SMEM) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  cached_dev = dev;
+  cached = n;
+  return n;
 }
 
 bool validate_env() {
@@ -428,9 +493,10 @@ const char* flce_status_string(flce_status s) {
 
 size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
   if (!sizes_ok(N, H, V)) return 0;
-  const int sms = device_sms();
-  const FwdLayout fl = fwd_layout(N, plan_forward(N, H, V, sms));
-  const BwdLayout bl = bwd_layout(H, plan_backward(N, H, V, chunk_rows, sms));
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const FwdLayout fl = fwd_layout(N, plan_forward(N, H, V, workers, BM * cg));
+  const BwdLayout bl = bwd_layout(H, plan_backward(N, H, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
 
@@ -448,8 +514,9 @@ flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* 
       !aligned(out_logp, 4) || !aligned(out_lse, 4) || !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
     return FLCE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int sms = device_sms();
-  const FwdPlan f = plan_forward(N, H, V, sms);
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const FwdPlan f = plan_forward(N, H, V, workers, BM * cg);
   const FwdLayout L = fwd_layout(N, f);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
@@ -478,7 +545,8 @@ flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* 
       if (nbad != 0) return FLCE_ERR_BAD_TARGET;
     }
     CUtensorMap tA, tB;
-    if (!make_map(&tA, h, H, N, H, BK, BM) || !make_map(&tB, W, H, V, H, BK, BN)) return FLCE_ERR_CUDA;
+    if (!make_map(&tA, h, H, N, H, BK, BM) || !make_map(&tB, W, H, V, H, BK, BN / cg))
+      return FLCE_ERR_CUDA;
     GemmParams p{};
     p.m_tiles = f.m_tiles;
     p.n_tiles = f.n_tiles;
@@ -507,7 +575,7 @@ flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* 
                        static_cast<long long>(f.S) * N >= INT_MAX;
     {
       ProfScope ps(K_FWD, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(kLong, tA, tB, tB, p, f.grid, st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(cg, kLong, tA, tB, tB, p, f.grid, st));
     }
     {
       ProfScope ps(K_COMBINE, st);
@@ -546,8 +614,10 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
     if (dW) FLCE_CUDA_TRY(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, st));
     return FLCE_OK;
   }
-  const int sms = device_sms();
-  const BwdPlan b = plan_backward(N, H, V, chunk_rows, sms);
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const int tm = BM * cg;
+  const BwdPlan b = plan_backward(N, H, V, chunk_rows, workers, tm);
   const BwdLayout L = bwd_layout(H, b);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
@@ -571,7 +641,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
   int* err = nullptr;
   FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
   CUtensorMap h_k, W_k, W_mn, h_mn, dW_map;
-  if (!make_map(&h_k, h, H, N, H, BK, BM) || !make_map(&W_k, W, H, V, H, BK, BN) ||
+  if (!make_map(&h_k, h, H, N, H, BK, BM) || !make_map(&W_k, W, H, V, H, BK, BN / cg) ||
       !make_map(&W_mn, W, H, V, H, 64, BK) || !make_map(&h_mn, h, H, N, H, 64, BK))
     return FLCE_ERR_CUDA;
   if (dW && !make_map_t(&dW_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, H, V, H, 32, 32))
@@ -607,7 +677,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
     // (1) recompute logits, dlogits chunk -> D[rows, ldD] bf16
     {
       GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(rows, BM));
+      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
       q.n_tiles = static_cast<int>(ceil_div(V, BN));
       q.k_blocks = static_cast<int>(ceil_div(H, BK));
       q.cols = q.n_tiles;
@@ -616,7 +686,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
       q.num_units = q.m_tiles * q.n_tiles;
       q.group_m = std::min(8, q.m_tiles);
       ProfScope ps(K_DLOGITS, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(kLong, h_k, W_k, W_k, q, std::min(q.num_units, sms), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, h_k, W_k, W_k, q, std::min(q.num_units, workers), st));
     }
     CUtensorMap D_k, D_mn;
     if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) || !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
@@ -624,7 +694,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
     // (2) dH[rows] = D W
     if (dH) {
       GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(rows, BM));
+      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
       q.n_tiles = static_cast<int>(ceil_div(H, BN));
       q.k_blocks = static_cast<int>(ceil_div(V, BK));
       q.cols = q.n_tiles;
@@ -636,12 +706,12 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
       q.dH_part = splits > 1 ? dh_part : nullptr;
       {
         ProfScope ps(K_DH, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(kLong, D_k, W_mn, W_mn, q, std::min(q.num_units, sms), st));
+        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(cg, kLong, D_k, W_mn, W_mn, q, std::min(q.num_units, workers), st));
       }
       if (splits > 1) {
         ProfScope ps(K_DH_REDUCE, st);
         const long long total = static_cast<long long>(rows) * (H / 4);
-        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * sms));
+        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
         if (kLong)
           dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
                                                                  static_cast<int>(H), p.row0, dH);
@@ -654,7 +724,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
     // (3) dW (+)= D^T h[rows]
     if (dW) {
       GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(V, BM));
+      q.m_tiles = static_cast<int>(ceil_div(V, tm));
       q.n_tiles = static_cast<int>(ceil_div(H, BN));
       q.k_blocks = static_cast<int>(ceil_div(rows, BK));
       q.cols = q.n_tiles;
@@ -664,7 +734,7 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
       q.group_m = std::min(8, q.m_tiles);
       q.dW_accumulate = chunk > 0 ? 1 : 0;
       ProfScope ps(K_DW, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(kLong, D_mn, h_mn, dW_map, q, std::min(q.num_units, sms), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(cg, kLong, D_mn, h_mn, dW_map, q, std::min(q.num_units, workers), st));
     }
   }
   return FLCE_OK;
@@ -790,7 +860,8 @@ extern "C" flce_status flce_forward_static_scratch(const flce_bf16* h, const flc
                                                    float* out_logp, float* out_lse, float* out_loss,
                                                    int64_t* out_n_valid, void* stream) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
-  const size_t need = fwd_layout(N, plan_forward(N, H, V, device_sms())).total;
+  const int cg = cta_group();
+  const size_t need = fwd_layout(N, plan_forward(N, H, V, device_workers(cg), BM * cg)).total;
   if (need > kStaticScratchBytes) return FLCE_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   const flce_status s = static_scratch_address(&scratch);

@@ -32,14 +32,10 @@
 
 namespace flce {
 
-constexpr int BM = 128;  // accumulator rows (TMEM lanes)
+constexpr int BM = 128;  // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;  // accumulator columns (fp32 TMEM columns)
 constexpr int BK = 64;   // one 128-byte swizzle row of bf16 per stage
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) swizzled box
 constexpr int EPI_WARPS = 4;
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
@@ -49,8 +45,21 @@ constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int OUT_BOX_BYTES = 32 * 32 * 4;
 constexpr int OUT_STAGE_BYTES = EPI_WARPS * 2 * OUT_BOX_BYTES;
 constexpr int SMEM_BAR_BYTES = 256;
-constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_STAGE_BYTES + SMEM_BAR_BYTES;
-static_assert(GEMM_SMEM_BYTES <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+
+// Tile geometry of one CTA (CG = 1) or of an SM pair running 2-CTA MMAs
+// (CG = 2: a 256 x 256 tile, A rows and B columns split across the pair).
+template <int CG>
+struct TileCfg {
+  static constexpr int TM = BM * CG;         // tile rows of the CTA group
+  static constexpr int B_ROWS = BN / CG;     // B rows (output columns) held by each CTA
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;  // 48 KiB (CG 1) / 32 KiB (CG 2)
+  static constexpr int NSTAGE = CG == 1 ? 4 : 6;
+  static constexpr int SMEM = 1024 + NSTAGE * STAGE + OUT_STAGE_BYTES + SMEM_BAR_BYTES;
+  static_assert(SMEM <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+};
+constexpr int GEMM_SMEM_BYTES_MAX = TileCfg<1>::SMEM > TileCfg<2>::SMEM ? TileCfg<1>::SMEM : TileCfg<2>::SMEM;
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 constexpr long long DRAIN_LIMIT_CYCLES = 400000000LL;
 
@@ -147,36 +156,51 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int* er
   }
 }
 
-template <int MODE>
+template <int MODE, int CG>
+__device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                       int32_t c1) {
+  if constexpr (CG == 1)
+    tma_load_2d(dst, map, bar, c0, c1);
+  else
+    tma_load_2d_pair(dst, map, bar, c0, c1);
+}
+
+// One pipeline stage of this CTA: its BM rows of A and its B_ROWS rows of B.
+// `bar` is the full barrier of the MMA-issuing CTA (cluster address for CG 2).
+template <int MODE, int CG>
 __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensorMap* tB,
                                            uint32_t sA, uint32_t sB, uint32_t bar,
-                                           const GemmParams& p, int m, int n, int kb) {
+                                           const GemmParams& p, int m, int n, int kb, int rank) {
+  using C = TileCfg<CG>;
+  const int a0 = m * C::TM + rank * BM;         // first A row (M) of this CTA
+  const int b0 = n * BN + rank * C::B_ROWS;     // first B row (N) of this CTA
   if constexpr (MODE == MODE_FWD || MODE == MODE_DLOGITS) {
-    // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x 256)
-    tma_load_2d(sA, tA, bar, kb * BK, p.row0 + m * BM);
-    tma_load_2d(sB, tB, bar, kb * BK, n * BN);
+    // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x B_ROWS)
+    tma_ld<MODE, CG>(sA, tA, bar, kb * BK, p.row0 + a0);
+    tma_ld<MODE, CG>(sB, tB, bar, kb * BK, b0);
   } else if constexpr (MODE == MODE_DH) {
     // A = D rows of this chunk (K-major over the vocabulary), B = W with the
-    // hidden dimension contiguous (MN-major): four 64-wide boxes
-    tma_load_2d(sA, tA, bar, kb * BK, m * BM);
+    // hidden dimension contiguous (MN-major): 64-wide boxes
+    tma_ld<MODE, CG>(sA, tA, bar, kb * BK, a0);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * MN_BOX_BYTES, tB, bar, n * BN + 64 * j, kb * BK);
+    for (int j = 0; j < C::B_ROWS / 64; ++j)
+      tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, kb * BK);
   } else {
     // A = D^T (vocabulary contiguous: MN-major), B = h (hidden contiguous:
     // MN-major); K runs over the chunk's rows
 #pragma unroll
-    for (int j = 0; j < 2; ++j) tma_load_2d(sA + j * MN_BOX_BYTES, tA, bar, m * BM + 64 * j, kb * BK);
+    for (int j = 0; j < 2; ++j) tma_ld<MODE, CG>(sA + j * MN_BOX_BYTES, tA, bar, a0 + 64 * j, kb * BK);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      tma_load_2d(sB + j * MN_BOX_BYTES, tB, bar, n * BN + 64 * j, p.row0 + kb * BK);
+    for (int j = 0; j < C::B_ROWS / 64; ++j)
+      tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, p.row0 + kb * BK);
   }
 }
 
-template <int MODE>
+template <int MODE, int CG>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sA, uint32_t sB, bool first) {
   constexpr bool A_MN = (MODE == MODE_DW);
   constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = idesc_bf16_f32(TileCfg<CG>::TM, BN, A_MN, B_MN);
 #pragma unroll
   for (int k = 0; k < BK / UMMA_K; ++k) {
     // K-major: 8-row core groups 1024 B apart, K advances 32 B inside the
@@ -186,8 +210,19 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sA, uint32_t
                              : smem_desc_sw128(sA + k * 32, 16, 1024);
     const uint64_t bd = B_MN ? smem_desc_sw128(sB + k * 2048, MN_BOX_BYTES, 1024)
                              : smem_desc_sw128(sB + k * 32, 16, 1024);
-    umma_bf16(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
+    if constexpr (CG == 1)
+      umma_bf16(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
+    else
+      umma_bf16_pair(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
   }
+}
+
+template <int CG>
+__device__ __forceinline__ void mma_commit_all(uint32_t bar) {
+  if constexpr (CG == 1)
+    umma_commit(bar);
+  else
+    umma_commit_pair_mc(bar, 0x3);  // the barrier at this offset in both CTAs
 }
 
 // v[j] for a run-time j in [0, 32) without dynamic register indexing (which
@@ -210,45 +245,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int MODE, bool kLong>
+template <int MODE, bool kLong, int CG>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
+  using C = TileCfg<CG>;
+  constexpr int NST = C::NSTAGE;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t out_stage = sbase + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + OUT_STAGE_BYTES);
+  const uint32_t out_stage = sbase + NST * C::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE + OUT_STAGE_BYTES);
   const uint32_t bar0 = smem_u32(bars);
-  // barrier layout: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  // barrier layout: full[NST], empty[NST], tfull[2], tempty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (NST + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * NST + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * NST + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * NST + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CG 2: the pair's first CTA (rank 0) issues the MMAs; both CTAs load their
+  // half of the operands and drain their half of the accumulator rows.
+  const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool issuer = rank == 0;
+  const int worker = blockIdx.x / CG;
+  const int nworkers = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), EPI_WARPS);
+      mbar_init(tempty_bar(b), EPI_WARPS * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if constexpr (CG == 2) cluster_sync();  // peer barriers exist before any remote signal
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 1) {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -263,7 +312,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int u = worker; u < p.num_units && ok; u += nworkers) {
         const Unit t = decode_unit<MODE>(p, u);
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -271,28 +320,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               ok = false;
               break;
             }
-            const uint32_t sA = sbase + stage * STAGE_BYTES;
-            mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-            load_stage<MODE>(&tmA, &tmB, sA, sA + A_STAGE_BYTES, full_bar(stage), p, t.m, n, kb);
+            const uint32_t sA = sbase + stage * C::STAGE;
+            uint32_t fb = full_bar(stage);
+            if constexpr (CG == 2) fb = mapa_shared(fb, 0);
+            if (issuer) mbar_arrive_expect_tx(full_bar(stage), C::STAGE * CG);
+            load_stage<MODE, CG>(&tmA, &tmB, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank);
             ++issued;
-            if (++stage == STAGES) {
+            if (++stage == NST) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
       }
-      // make sure no copy into this CTA's shared memory is still in flight
-      for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
-        drain_bar(full_bar(static_cast<int>(i % STAGES)), static_cast<uint32_t>((i / STAGES) & 1), p.err);
+      // no copy into shared memory may still be in flight when the CTA
+      // retires: the issuing CTA's full barriers count both CTAs' bytes
+      if (issuer)
+        for (long long i = (issued > NST ? issued - NST : 0); i < issued; ++i)
+          drain_bar(full_bar(static_cast<int>(i % NST)), static_cast<uint32_t>((i / NST) & 1), p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && issuer) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int u = worker; u < p.num_units && ok; u += nworkers) {
         const Unit t = decode_unit<MODE>(p, u);
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
@@ -307,22 +360,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t sA = sbase + stage * STAGE_BYTES;
-            mma_stage<MODE>(d_tmem, sA, sA + A_STAGE_BYTES, kb == t.kb0);
-            umma_commit(empty_bar(stage));
-            if (++stage == STAGES) {
+            const uint32_t sA = sbase + stage * C::STAGE;
+            mma_stage<MODE, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
+            mma_commit_all<CG>(empty_bar(stage));
+            if (++stage == NST) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(tfull_bar(acc));
+          mma_commit_all<CG>(tfull_bar(acc));
           acc ^= 1u;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
       // every MMA issued by this thread has finished before TMEM is freed
-      umma_commit(drain);
+      if constexpr (CG == 1)
+        umma_commit(drain);
+      else
+        umma_commit_pair(drain);
       drain_bar(drain, 0, p.err);
     }
     __syncwarp();
@@ -331,12 +387,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // accumulator row owned by this thread
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t tempty_target0 = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    const uint32_t tempty_target1 = CG == 2 ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int u = worker; u < p.num_units && ok; u += nworkers) {
       const Unit t = decode_unit<MODE>(p, u);
       // per-unit row state
-      const int lr = t.m * BM + r;  // row inside this pass (FWD: global row)
+      const int lr = t.m * C::TM + rank * BM + r;  // row inside this pass (FWD: global row)
       const int grow = p.row0 + lr;
       bool row_ok;
       long long tgt = -1;
@@ -456,7 +514,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              const int vrow0 = t.m * BM + q * 32;
+              const int vrow0 = t.m * C::TM + rank * BM + q * 32;
               if (col0 < p.H && vrow0 < p.V) {  // boxes wholly outside dW are skipped
                 if (p.dW_accumulate)
                   tma_reduce_add_2d(&tmC, box, col0, vrow0);
@@ -469,7 +527,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        if (lane == 0) {
+          if constexpr (CG == 1)
+            mbar_arrive(acc ? tempty_target1 : tempty_target0);
+          else
+            mbar_arrive_cluster(acc ? tempty_target1 : tempty_target0);
+        }
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -484,9 +547,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp >= 2 && lane == 0) bulk_wait_all();  // dW boxes written before the CTA retires
   }
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA retires while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (CG == 1)
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 

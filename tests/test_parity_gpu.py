@@ -230,3 +230,15 @@ def test_grpo_32k_sampled():
 @pytest.mark.slow
 def test_long_131k_sampled():
     _large_check("long_131k", 4096, 512, full_forward=False)
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_both_cta_group_paths(cg, monkeypatch):
+    """Single-CTA tiles (FLCE_CTA_GROUP=1) and SM-pair tiles (the default) both
+    match the oracle on a ragged multi-tile, multi-chunk case."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    wl = WL.custom(f"cg{cg}", 600, 264, 2100, 256, w_std=0.05, targets="zipf", ignore_frac=0.05,
+                   seed=110)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(11).uniform(0.5, 1.5, wl.N).astype(np.float32)
+    _full_check(inp, 256)
