@@ -29,6 +29,12 @@ SIGNATURES = {
     "flce_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp,
                                      _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, ctypes.c_size_t,
                                      _c_vp]),
+    "flce_forward_ex": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
+                                       _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                       ctypes.c_size_t, _c_vp]),
+    "flce_backward_ex": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp,
+                                        _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
+                                        ctypes.c_size_t, _c_vp]),
     "flce_forward_static_scratch": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                                    _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
@@ -40,6 +46,22 @@ SIGNATURES = {
     "flce_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_int64)]),
 }
+
+class LogitTransform(ctypes.Structure):
+    """flce_logit_transform: multiply, divide, soft-cap, temperature (0/0/0/1 = identity)."""
+
+    _fields_ = [("scale_multiply", ctypes.c_float), ("scale_divide", ctypes.c_float),
+                ("softcap", ctypes.c_float), ("temperature", ctypes.c_float)]
+
+
+def make_transform(tf) -> "LogitTransform | None":
+    """None, a LogitTransform, or a dict with any of its four field names."""
+    if tf is None or isinstance(tf, LogitTransform):
+        return tf
+    d = {"scale_multiply": 0.0, "scale_divide": 0.0, "softcap": 0.0, "temperature": 1.0}
+    d.update(tf)
+    return LogitTransform(**d)
+
 
 _LIB = None
 
@@ -116,6 +138,34 @@ def flce_backward(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chun
     return lib.flce_backward(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), _ptr(lse),
                              float(grad_scale), _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
                              ignore_index, _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def _tf_ptr(tf):
+    t = make_transform(tf)
+    return None if t is None else ctypes.addressof(t), t
+
+
+def flce_forward_ex(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform, out_logp,
+                    out_lse, out_loss, out_n_valid, workspace=None, workspace_bytes=0,
+                    stream=None) -> int:
+    """Raw C call with a logit transform (None / dict / LogitTransform)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_forward_ex(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), N, H, V, chunk_rows,
+                               ignore_index, tp, _ptr(out_logp), _ptr(out_lse), _ptr(out_loss),
+                               _ptr(out_n_valid), _ptr(workspace), workspace_bytes,
+                               _stream_handle(stream))
+
+
+def flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                     ignore_index, transform, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call with a logit transform (None / dict / LogitTransform)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_backward_ex(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), _ptr(lse),
+                                float(grad_scale), _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
+                                ignore_index, tp, _ptr(workspace), workspace_bytes,
+                                _stream_handle(stream))
 
 
 def flce_forward_static_scratch(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp,

@@ -33,8 +33,11 @@ def workspace_bytes(N: int, H: int, V: int, chunk_rows: int) -> int:
 
 
 def forward(h, W, targets, weights=None, chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX,
-            workspace: torch.Tensor | None = None, stream=None):
-    """Returns dict(logp[N] f32, lse[N] f32, loss[] f32, n_valid[] i64), on device."""
+            workspace: torch.Tensor | None = None, stream=None, transform=None):
+    """Returns dict(logp[N] f32, lse[N] f32, loss[] f32, n_valid[] i64), on device.
+
+    ``transform``: None, or a dict with scale_multiply / scale_divide /
+    softcap / temperature (flce_logit_transform)."""
     _check(h, W, targets, weights)
     N, H = h.shape
     V = W.shape[0]
@@ -44,15 +47,15 @@ def forward(h, W, targets, weights=None, chunk_rows: int = 256, ignore_index: in
     loss = torch.empty((), dtype=torch.float32, device=dev)
     n_valid = torch.empty((), dtype=torch.int64, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_forward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, logp, lse,
-                           loss, n_valid, workspace, ws_bytes, stream)
-    _lib.check("flce_forward", st)
+    st = _lib.flce_forward_ex(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform,
+                              logp, lse, loss, n_valid, workspace, ws_bytes, stream)
+    _lib.check("flce_forward_ex", st)
     return {"logp": logp, "lse": lse, "loss": loss, "n_valid": n_valid}
 
 
 def backward(h, W, targets, weights, lse, grad_scale: float, chunk_rows: int = 256,
              ignore_index: int = IGNORE_INDEX, need_dH: bool = True, need_dW: bool = True,
-             workspace: torch.Tensor | None = None, stream=None):
+             workspace: torch.Tensor | None = None, stream=None, transform=None):
     """Returns (dH[N,H] bf16 or None, dW[V,H] f32 or None)."""
     _check(h, W, targets, weights)
     N, H = h.shape
@@ -60,9 +63,9 @@ def backward(h, W, targets, weights, lse, grad_scale: float, chunk_rows: int = 2
     dH = torch.empty_like(h) if need_dH else None
     dW = torch.empty((V, H), dtype=torch.float32, device=h.device) if need_dW else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_backward(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
-                            ignore_index, workspace, ws_bytes, stream)
-    _lib.check("flce_backward", st)
+    st = _lib.flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                               ignore_index, transform, workspace, ws_bytes, stream)
+    _lib.check("flce_backward_ex", st)
     return dH, dW
 
 
@@ -74,8 +77,9 @@ class LinearCrossEntropy(torch.autograd.Function):
     """
 
     @staticmethod
-    def forward(ctx, h, W, targets, weights, chunk_rows, ignore_index):
-        out = forward(h, W, targets, weights, chunk_rows, ignore_index)
+    def forward(ctx, h, W, targets, weights, chunk_rows, ignore_index, transform=None):
+        out = forward(h, W, targets, weights, chunk_rows, ignore_index, transform=transform)
+        ctx.transform = transform
         ctx.save_for_backward(h, W, targets, weights if weights is not None else torch.empty(0),
                               out["lse"], out["n_valid"])
         ctx.has_weights = weights is not None
@@ -91,11 +95,12 @@ class LinearCrossEntropy(torch.autograd.Function):
         n = int(n_valid.item())
         g = float(grad_loss.item()) / n if n > 0 else 0.0
         dH, dW = backward(h, W, targets, weights, lse, g, ctx.chunk_rows, ctx.ignore_index,
-                          need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1])
-        return dH, dW, None, None, None, None
+                          need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
+                          transform=ctx.transform)
+        return dH, dW, None, None, None, None, None
 
 
 def linear_cross_entropy(h, W, targets, weights=None, chunk_rows: int = 256,
-                         ignore_index: int = IGNORE_INDEX):
-    """Differentiable masked (weighted) mean NLL of softmax(h W^T); returns (loss, logp, n_valid)."""
-    return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index)
+                         ignore_index: int = IGNORE_INDEX, transform=None):
+    """Differentiable masked (weighted) mean NLL of softmax(f(h W^T)); returns (loss, logp, n_valid)."""
+    return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index, transform)

@@ -466,6 +466,30 @@ flce_status get_workspace(Workspace& ws, void* user, size_t user_bytes, size_t n
   return FLCE_OK;
 }
 
+// Kernel form of a logit transform (see flce_logit_transform): y = a * z, or
+// y = b * tanh(a * z) with dy/dz = d * (1 - tanh^2).  False on invalid values.
+bool transform_params(const flce_logit_transform* tf, GemmParams& p) {
+  p.tf_softcap = 0;
+  p.tf_a = 1.f;
+  p.tf_b = 1.f;
+  p.tf_d = 1.f;
+  if (tf == nullptr) return true;
+  const float mul = tf->scale_multiply, div = tf->scale_divide, cap = tf->softcap, T = tf->temperature;
+  if (!(std::isfinite(mul) && std::isfinite(div) && std::isfinite(cap) && std::isfinite(T))) return false;
+  if (mul < 0.f || div < 0.f || cap < 0.f || !(T > 0.f)) return false;
+  const float s1 = (mul != 0.f ? mul : 1.f) / (div != 0.f ? div : 1.f);
+  if (!(s1 > 0.f) || !std::isfinite(s1)) return false;
+  if (cap != 0.f) {
+    p.tf_softcap = 1;
+    p.tf_a = s1 / cap;
+    p.tf_b = cap / T;
+    p.tf_d = s1 / T;
+  } else {
+    p.tf_a = s1 / T;
+  }
+  return std::isfinite(p.tf_a) && std::isfinite(p.tf_b) && std::isfinite(p.tf_d) && p.tf_a > 0.f;
+}
+
 #define FLCE_CUDA_TRY(x)                 \
   do {                                   \
     if ((x) != cudaSuccess) {            \
@@ -500,13 +524,16 @@ size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows)
   return std::max(fl.total, bl.total);
 }
 
-flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
-                         const float* weights, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
-                         int64_t ignore_index, float* out_logp, float* out_lse, float* out_loss,
-                         int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                            const float* weights, int64_t N, int64_t H, int64_t V,
+                            int64_t chunk_rows, int64_t ignore_index,
+                            const flce_logit_transform* transform, float* out_logp, float* out_lse,
+                            float* out_loss, int64_t* out_n_valid, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   (void)chunk_rows;
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  GemmParams tfp{};
+  if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
   if (!out_logp && !out_lse && !out_loss && !out_n_valid) return FLCE_ERR_INVALID_ARG;
   if (N > 0 && (!h || !W || !targets)) return FLCE_ERR_INVALID_ARG;
   if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
@@ -568,6 +595,10 @@ flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* 
     p.ignore_index = ignore_index;
     p.partials = part;
     p.zt = zt;
+    p.tf_softcap = tfp.tf_softcap;
+    p.tf_a = tfp.tf_a;
+    p.tf_b = tfp.tf_b;
+    p.tf_d = tfp.tf_d;
     int* err = nullptr;
     FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
     p.err = err;
@@ -597,12 +628,15 @@ flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* 
   return FLCE_OK;
 }
 
-flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
-                          const float* weights, const float* lse, float grad_scale, flce_bf16* dH,
-                          float* dW, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
-                          int64_t ignore_index, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                             const float* weights, const float* lse, float grad_scale,
+                             flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
+                             int64_t chunk_rows, int64_t ignore_index,
+                             const flce_logit_transform* transform, void* workspace,
+                             size_t workspace_bytes, void* stream) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  GemmParams tfp{};
+  if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
   if (!dH && !dW) return FLCE_ERR_INVALID_ARG;
   if (N > 0 && (!h || !W || !targets || !lse)) return FLCE_ERR_INVALID_ARG;
   if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
@@ -667,6 +701,10 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
   base.dW = dW;
   base.err = err;
   base.rows_cap = static_cast<int>(b.R);
+  base.tf_softcap = tfp.tf_softcap;
+  base.tf_a = tfp.tf_a;
+  base.tf_b = tfp.tf_b;
+  base.tf_d = tfp.tf_d;
 
   int chunk = 0;
   for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
@@ -738,6 +776,24 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
     }
   }
   return FLCE_OK;
+}
+
+flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                         const float* weights, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                         int64_t ignore_index, float* out_logp, float* out_lse, float* out_loss,
+                         int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return flce_forward_ex(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, nullptr, out_logp,
+                         out_lse, out_loss, out_n_valid, workspace, workspace_bytes, stream);
+}
+
+flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                          const float* weights, const float* lse, float grad_scale, flce_bf16* dH,
+                          float* dW, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                          int64_t ignore_index, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  return flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                          ignore_index, nullptr, workspace, workspace_bytes, stream);
 }
 
 flce_status flce_device_status(void* stream) {

@@ -85,6 +85,11 @@ struct GemmParams {
   const float* lse;
   float grad_scale;
   long long ignore_index;
+  // logit transform y = f(z) before the log-softmax: linear y = tf_a * z
+  // (tf_softcap == 0), or soft-capped y = tf_b * tanh(tf_a * z) with
+  // dy/dz = tf_d * (1 - tanh^2)
+  int tf_softcap;
+  float tf_a, tf_b, tf_d;
   float2* partials;   // FWD: [splits][N] (max*log2e, sum exp2)
   float* zt;          // FWD: [N] target logit
   uint16_t* D;        // DLOGITS out [rows_cap][ldD] bf16
@@ -400,6 +405,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       long long tgt = -1;
       float run_m = -INFINITY, run_s = 0.f;  // FWD: log2-domain max and sum
       float scale = 0.f, nl2 = 0.f;          // DLOGITS
+      // linear transform folded into the exp2 prescale, the gathered target
+      // logit and the dlogits scale (soft-capped logits are formed explicitly)
+      const float lin_a = p.tf_softcap ? 1.f : p.tf_a;
+      const float l2a = kLog2e * lin_a;
       if constexpr (MODE == MODE_DW) {
         row_ok = lr < p.V;  // rows of the accumulator are vocabulary rows here
       } else {
@@ -417,6 +426,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           nl2 = -p.lse[grow] * kLog2e;
         }
       }
+      const float scale_a = scale * lin_a;
       for (int n = t.n0; n < t.n1; ++n) {
         int got = 0;
         if (lane == 0) got = wait_bar(tfull_bar(acc), acc_phase, abort_flag, p.err) ? 1 : 0;
@@ -433,6 +443,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tmem_ld32(tbase + c * 32, v);
           const int col0 = n * BN + c * 32;
           if constexpr (MODE == MODE_FWD) {
+            if (p.tf_softcap) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = p.tf_b * tanhf(p.tf_a * v[j]);
+            }
             if (col0 + 32 > p.V) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -441,35 +455,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             float cm = v[0];
 #pragma unroll
             for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
-            const float nm = fmaxf(run_m, cm * kLog2e);
+            const float nm = fmaxf(run_m, cm * l2a);
             if (nm != -INFINITY) {
               float a = 0.f;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) a += exp2f(fmaf(v[j], kLog2e, -nm));
+              for (int j = 0; j < 32; ++j) a += exp2f(fmaf(v[j], l2a, -nm));
               run_s = run_s * exp2f(run_m - nm) + a;
               run_m = nm;
             }
             const long long tj = tgt - col0;
             if (tj >= 0 && tj < 32 && tgt < p.V) {
-              const float z = select32(v, static_cast<int>(tj));
+              const float z = select32(v, static_cast<int>(tj)) * lin_a;
               if (row_ok) p.zt[grow] = z;
             }
           } else if constexpr (MODE == MODE_DLOGITS) {
             uint32_t pk[16];
             const long long tjl = tgt - col0;
             const int tj = (tjl >= 0 && tjl < 32) ? static_cast<int>(tjl) : -1;
+            if (!p.tf_softcap) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float d0 = 0.f, d1 = 0.f;
-              if (scale != 0.f) {
-                float p0 = exp2f(fmaf(v[j], kLog2e, nl2));
-                float p1 = exp2f(fmaf(v[j + 1], kLog2e, nl2));
-                if (j == tj) p0 -= 1.f;
-                if (j + 1 == tj) p1 -= 1.f;
-                d0 = (col0 + j < p.V) ? p0 * scale : 0.f;
-                d1 = (col0 + j + 1 < p.V) ? p1 * scale : 0.f;
+              for (int j = 0; j < 32; j += 2) {
+                float d0 = 0.f, d1 = 0.f;
+                if (scale != 0.f) {
+                  float p0 = exp2f(fmaf(v[j], l2a, nl2));
+                  float p1 = exp2f(fmaf(v[j + 1], l2a, nl2));
+                  if (j == tj) p0 -= 1.f;
+                  if (j + 1 == tj) p1 -= 1.f;
+                  d0 = (col0 + j < p.V) ? p0 * scale_a : 0.f;
+                  d1 = (col0 + j + 1 < p.V) ? p1 * scale_a : 0.f;
+                }
+                pk[j / 2] = pack_bf16x2(d0, d1);
               }
-              pk[j / 2] = pack_bf16x2(d0, d1);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float d0 = 0.f, d1 = 0.f;
+                if (scale != 0.f) {
+                  const float t0 = tanhf(p.tf_a * v[j]);
+                  const float t1 = tanhf(p.tf_a * v[j + 1]);
+                  float p0 = exp2f(fmaf(p.tf_b * t0, kLog2e, nl2));
+                  float p1 = exp2f(fmaf(p.tf_b * t1, kLog2e, nl2));
+                  if (j == tj) p0 -= 1.f;
+                  if (j + 1 == tj) p1 -= 1.f;
+                  d0 = (col0 + j < p.V) ? p0 * scale * p.tf_d * (1.f - t0 * t0) : 0.f;
+                  d1 = (col0 + j + 1 < p.V) ? p1 * scale * p.tf_d * (1.f - t1 * t1) : 0.f;
+                }
+                pk[j / 2] = pack_bf16x2(d0, d1);
+              }
             }
             if (row_ok) {
               uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;

@@ -69,6 +69,28 @@ typedef enum {
 } flce_status;
 
 /*
+ * Logit transforms applied elementwise to z before the log-softmax, in this
+ * order: multiply, divide, soft-cap, temperature.  Source: Unsloth,
+ * "Reinforcement Learning GRPO with 7x longer context", section "Flattened
+ * sequence-length chunking": the chunked selective log-softmax takes
+ * logit_scale_multiply, logit_scale_divide, logit_softcapping and
+ * temperature (the page prints neither their order nor their defaults; the
+ * order of its call is taken, and 0 disables the first three).
+ *   scale_multiply  y *= scale_multiply           (0 = off; must be >= 0)
+ *   scale_divide    y /= scale_divide             (0 = off; must be >= 0)
+ *   softcap         y = softcap * tanh(y/softcap) (0 = off; must be >= 0)
+ *   temperature     y /= temperature              (1 = off; must be > 0)
+ * lse and logp are those of y; the backward's D carries dy/dz.  Invalid
+ * values return FLCE_ERR_INVALID_ARG.
+ */
+typedef struct flce_logit_transform {
+  float scale_multiply;
+  float scale_divide;
+  float softcap;
+  float temperature;
+} flce_logit_transform;
+
+/*
  * Forward: per-token log-probs, log-sum-exp, masked (weighted) mean loss.
  *
  *   h        [N,H] bf16, row-major (row i = token i of the flattened batch).
@@ -102,6 +124,14 @@ FLCE_API flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const 
                          float* out_lse, float* out_loss, int64_t* out_n_valid,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* flce_forward with a logit transform (NULL = identity). */
+FLCE_API flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                     const float* weights, int64_t N, int64_t H, int64_t V,
+                                     int64_t chunk_rows, int64_t ignore_index,
+                                     const flce_logit_transform* transform, float* out_logp,
+                                     float* out_lse, float* out_loss, int64_t* out_n_valid,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Backward: dH = D W and dW = D^T h with
  *   D[i,v] = (exp(z[i,v] - lse[i]) - [v == targets[i]]) * m[i] * w[i] * grad_scale.
@@ -129,6 +159,15 @@ FLCE_API flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const
                           flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
                           int64_t chunk_rows, int64_t ignore_index, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* flce_backward with a logit transform (NULL = identity); `lse` must come
+ * from flce_forward_ex with the same transform. */
+FLCE_API flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W,
+                                      const int64_t* targets, const float* weights,
+                                      const float* lse, float grad_scale, flce_bf16* dH, float* dW,
+                                      int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                                      int64_t ignore_index, const flce_logit_transform* transform,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Forward that allocates nothing (no counterpart on the source pages: the

@@ -68,6 +68,57 @@ def logsumexp_rows(z: np.ndarray) -> np.ndarray:
     return (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
 
 
+@dataclasses.dataclass(frozen=True)
+class LogitTransform:
+    """Elementwise logit transforms applied before the log-softmax.
+
+    Unsloth GRPO page, section "Flattened sequence-length chunking": the
+    chunked selective log-softmax takes logit_scale_multiply,
+    logit_scale_divide, logit_softcapping and temperature.  Reading taken
+    (the page prints neither order nor defaults): applied in that order, 0
+    disables the first three, temperature 1 is the identity; soft-capping is
+    y -> c * tanh(y / c).
+    """
+
+    scale_multiply: float = 0.0
+    scale_divide: float = 0.0
+    softcap: float = 0.0
+    temperature: float = 1.0
+
+    def apply(self, z: np.ndarray) -> np.ndarray:
+        y = z
+        if self.scale_multiply != 0.0:
+            y = y * self.scale_multiply
+        if self.scale_divide != 0.0:
+            y = y / self.scale_divide
+        if self.softcap != 0.0:
+            y = self.softcap * np.tanh(y / self.softcap)
+        if self.temperature != 1.0:
+            y = y / self.temperature
+        return y
+
+    def grad(self, z: np.ndarray) -> np.ndarray:
+        """dy/dz of apply(), elementwise (chain rule of the steps above)."""
+        d = np.ones_like(z)
+        y = z
+        if self.scale_multiply != 0.0:
+            y = y * self.scale_multiply
+            d = d * self.scale_multiply
+        if self.scale_divide != 0.0:
+            y = y / self.scale_divide
+            d = d / self.scale_divide
+        if self.softcap != 0.0:
+            d = d * (1.0 - np.tanh(y / self.softcap) ** 2)
+            y = self.softcap * np.tanh(y / self.softcap)
+        if self.temperature != 1.0:
+            d = d / self.temperature
+        return d
+
+
+def _tf(z: np.ndarray, tf: "LogitTransform | None") -> np.ndarray:
+    return z if tf is None else tf.apply(z)
+
+
 def _mask(targets: np.ndarray, V: int, ignore_index: int) -> np.ndarray:
     t = np.asarray(targets, dtype=np.int64)
     m = t != ignore_index
@@ -101,7 +152,7 @@ def selective_log_softmax(z: np.ndarray, targets: np.ndarray, mask: np.ndarray):
 
 
 def forward(h, W, targets, weights=None, ignore_index: int = IGNORE_INDEX,
-            chunk_rows: int | None = None) -> Forward:
+            chunk_rows: int | None = None, tf: LogitTransform | None = None) -> Forward:
     """Chunked selective log-softmax and masked (weighted) mean NLL.
 
     Rows are taken ``chunk_rows`` at a time (all at once when None); each
@@ -119,7 +170,7 @@ def forward(h, W, targets, weights=None, ignore_index: int = IGNORE_INDEX,
     total = 0.0
     for r0 in range(0, N, step):
         r1 = min(N, r0 + step)
-        z = hf[r0:r1] @ Wf.T
+        z = _tf(hf[r0:r1] @ Wf.T, tf)
         lse[r0:r1], logp[r0:r1] = selective_log_softmax(z, t[r0:r1], m[r0:r1])
         total += float(np.sum(m[r0:r1] * w[r0:r1] * logp[r0:r1]))
     n_valid = int(m.sum())
@@ -148,11 +199,13 @@ class Backward:
 
 def backward(h, W, targets, weights=None, g: float = 1.0,
              ignore_index: int = IGNORE_INDEX, chunk_rows: int | None = None,
-             lse: np.ndarray | None = None) -> Backward:
+             lse: np.ndarray | None = None, tf: LogitTransform | None = None) -> Backward:
     """dH = D W and dW = D^T h, recomputing each chunk's logits.
 
     ``lse`` defaults to the oracle's own forward.  g multiplies D literally
-    (g = 1/n_valid gives the gradient of the mean loss).
+    (g = 1/n_valid gives the gradient of the mean loss).  With a logit
+    transform y = f(z), D is taken with respect to z: (softmax(y) - onehot)
+    times f'(z).
     """
     hf, Wf = widen(h), widen(W)
     N, V = hf.shape[0], Wf.shape[0]
@@ -165,25 +218,30 @@ def backward(h, W, targets, weights=None, g: float = 1.0,
     for r0 in range(0, N, step):
         r1 = min(N, r0 + step)
         z = hf[r0:r1] @ Wf.T
-        l = logsumexp_rows(z) if lse is None else np.asarray(lse[r0:r1], dtype=np.float64)
-        D = dlogits(z, l, t[r0:r1], m[r0:r1], w[r0:r1], g)
+        y = _tf(z, tf)
+        l = logsumexp_rows(y) if lse is None else np.asarray(lse[r0:r1], dtype=np.float64)
+        D = dlogits(y, l, t[r0:r1], m[r0:r1], w[r0:r1], g)
+        if tf is not None:
+            D *= tf.grad(z)
         dH[r0:r1] = D @ Wf
         dW += D.T @ hf[r0:r1]
     return Backward(dH, dW)
 
 
-def rows_forward(h, W, targets, rows, ignore_index: int = IGNORE_INDEX):
+def rows_forward(h, W, targets, rows, ignore_index: int = IGNORE_INDEX,
+                 tf: LogitTransform | None = None):
     """(lse, logp) of the selected rows only; the same formulas as forward()."""
     rows = np.asarray(rows, dtype=np.int64)
     Wf = widen(W)
     t = np.asarray(targets, dtype=np.int64)[rows]
     m = _mask(t, Wf.shape[0], ignore_index)
-    z = widen(np.asarray(h)[rows]) @ Wf.T
+    z = _tf(widen(np.asarray(h)[rows]) @ Wf.T, tf)
     return selective_log_softmax(z, t, m)
 
 
 def rows_backward(h, W, targets, rows, weights=None, g: float = 1.0,
-                  ignore_index: int = IGNORE_INDEX, vocab_rows=None):
+                  ignore_index: int = IGNORE_INDEX, vocab_rows=None,
+                  tf: LogitTransform | None = None):
     """dH of the selected rows and those rows' contribution to dW.
 
     Returns (dH[rows], dW_part) where dW_part = D[rows]^T h[rows], restricted
@@ -196,7 +254,11 @@ def rows_backward(h, W, targets, rows, weights=None, g: float = 1.0,
     m = _mask(t, Wf.shape[0], ignore_index)
     w = _weights(None if weights is None else np.asarray(weights)[rows], len(rows))
     z = hf @ Wf.T
-    D = dlogits(z, logsumexp_rows(z), t, m, w, g)
+    y = _tf(z, tf)
+    D = dlogits(y, logsumexp_rows(y), t, m, w, g)
+    if tf is not None:
+        D *= tf.grad(z)
+    del y
     dH = D @ Wf
     if vocab_rows is not None:
         D = D[:, np.asarray(vocab_rows, dtype=np.int64)]
@@ -204,7 +266,8 @@ def rows_backward(h, W, targets, rows, weights=None, g: float = 1.0,
 
 
 def rows_all(h, W, targets, rows, weights=None, g: float = 1.0,
-             ignore_index: int = IGNORE_INDEX, vocab_rows=None):
+             ignore_index: int = IGNORE_INDEX, vocab_rows=None,
+             tf: LogitTransform | None = None):
     """rows_forward and rows_backward of the same rows from one logits block.
 
     Returns (lse, logp, dH[rows], dW_part) with dW_part = D[rows]^T h[rows]
@@ -217,8 +280,12 @@ def rows_all(h, W, targets, rows, weights=None, g: float = 1.0,
     m = _mask(t, Wf.shape[0], ignore_index)
     w = _weights(None if weights is None else np.asarray(weights)[rows], len(rows))
     z = hf @ Wf.T
-    lse, logp = selective_log_softmax(z, t, m)
-    D = dlogits(z, lse, t, m, w, g)
+    y = _tf(z, tf)
+    lse, logp = selective_log_softmax(y, t, m)
+    D = dlogits(y, lse, t, m, w, g)
+    del y
+    if tf is not None:
+        D *= tf.grad(z)
     del z
     dH = D @ Wf
     if vocab_rows is not None:

@@ -26,7 +26,7 @@ def upload(inp):
     return h, W, t, w
 
 
-def run_forward(h, W, t, w, chunk_rows, ignore_index=-100, workspace=None):
+def run_forward(h, W, t, w, chunk_rows, ignore_index=-100, workspace=None, transform=None):
     N, H = h.shape
     V = W.shape[0]
     logp = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
@@ -34,22 +34,30 @@ def run_forward(h, W, t, w, chunk_rows, ignore_index=-100, workspace=None):
     loss = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
     nv = torch.full((1,), -1, dtype=torch.int64, device="cuda")
     ws_bytes = 0 if workspace is None else workspace.numel()
-    st = _lib.flce_forward(h, W, t, w, N, H, V, chunk_rows, ignore_index, logp, lse, loss, nv,
-                           workspace, ws_bytes)
+    if transform is None:
+        st = _lib.flce_forward(h, W, t, w, N, H, V, chunk_rows, ignore_index, logp, lse, loss, nv,
+                               workspace, ws_bytes)
+    else:
+        st = _lib.flce_forward_ex(h, W, t, w, N, H, V, chunk_rows, ignore_index, transform, logp, lse,
+                                  loss, nv, workspace, ws_bytes)
     assert st == 0, _lib.STATUS_NAMES.get(st)
     assert _lib.flce_device_status() == 0
     return logp, lse, float(loss.item()), int(nv.item())
 
 
 def run_backward(h, W, t, w, lse, g, chunk_rows, ignore_index=-100, need_dH=True, need_dW=True,
-                 workspace=None):
+                 workspace=None, transform=None):
     N, H = h.shape
     V = W.shape[0]
     dH = torch.full((N, H), float("nan"), dtype=torch.bfloat16, device="cuda") if need_dH else None
     dW = torch.full((V, H), float("nan"), dtype=torch.float32, device="cuda") if need_dW else None
     ws_bytes = 0 if workspace is None else workspace.numel()
-    st = _lib.flce_backward(h, W, t, w, lse, g, dH, dW, N, H, V, chunk_rows, ignore_index,
-                            workspace, ws_bytes)
+    if transform is None:
+        st = _lib.flce_backward(h, W, t, w, lse, g, dH, dW, N, H, V, chunk_rows, ignore_index,
+                                workspace, ws_bytes)
+    else:
+        st = _lib.flce_backward_ex(h, W, t, w, lse, g, dH, dW, N, H, V, chunk_rows, ignore_index,
+                                   transform, workspace, ws_bytes)
     assert st == 0, _lib.STATUS_NAMES.get(st)
     assert _lib.flce_device_status() == 0
     return dH, dW

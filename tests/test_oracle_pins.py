@@ -310,3 +310,86 @@ def test_logit_memory_equations():
 def test_fp32_weight_copy_bytes():
     g = json.load(open(os.path.join(GOLD, "trl_fp32_copy.json")))
     assert g["vocab"] * g["hidden"] * g["bytes_per_element"] / 1e9 == pytest.approx(g["printed_gb"], abs=0.005)
+
+
+# ------------------------------------------------------------ logit transforms
+
+def test_identity_transform_is_no_transform():
+    h, W, t, w = _rand(20, 6, 15, seed=30, ignore=(3,), weights=True)
+    tf = O.LogitTransform()
+    f0, f1 = O.forward(h, W, t, w), O.forward(h, W, t, w, tf=tf)
+    b0, b1 = O.backward(h, W, t, w, g=0.2), O.backward(h, W, t, w, g=0.2, tf=tf)
+    assert np.array_equal(f0.logp, f1.logp) and np.array_equal(b0.dH, b1.dH) and np.array_equal(b0.dW, b1.dW)
+
+
+def test_linear_transforms_equal_a_scaled_head():
+    # multiply / divide / temperature are one scale a on the logits: the same
+    # as using the weight matrix a*W (forward), with dH picking up a and dW
+    # (w.r.t. the original W) picking up a as well
+    h, W, t, w = _rand(25, 7, 19, seed=31, ignore=(0,), weights=True)
+    tf = O.LogitTransform(scale_multiply=3.0, scale_divide=2.0, temperature=0.5)
+    a = 3.0 / 2.0 / 0.5
+    f = O.forward(h, W, t, w, tf=tf)
+    fa = O.forward(h, a * W, t, w)
+    assert np.allclose(f.logp, fa.logp, atol=1e-12) and np.allclose(f.lse, fa.lse, atol=1e-12)
+    b = O.backward(h, W, t, w, g=0.3, tf=tf)
+    ba = O.backward(h, a * W, t, w, g=0.3)
+    assert np.allclose(b.dH, ba.dH, atol=1e-12) and np.allclose(b.dW, a * ba.dW, atol=1e-12)
+
+
+def test_softcap_bounds_logits_and_vanishes_for_large_cap():
+    h, W, t, _ = _rand(10, 6, 13, seed=32, scale_w=3.0)
+    z = O.logits(h, W)
+    y = O.LogitTransform(softcap=5.0).apply(z)
+    assert np.all(np.abs(y) < 5.0) and np.max(np.abs(z)) > 5.0
+    big = O.LogitTransform(softcap=1e7)
+    assert np.allclose(O.forward(h, W, t, tf=big).logp, O.forward(h, W, t).logp, atol=1e-9)
+
+
+def test_transform_gradients_by_finite_differences():
+    N, H, V = 3, 5, 7
+    h, W, t, w = _rand(N, H, V, seed=33, weights=True, scale_w=2.0)
+    tf = O.LogitTransform(scale_multiply=1.7, scale_divide=1.3, softcap=2.5, temperature=0.8)
+    f = O.forward(h, W, t, w, tf=tf)
+    b = O.backward(h, W, t, w, g=1.0 / f.n_valid, tf=tf)
+    eps = 1e-6
+
+    def loss(hh, WW):
+        return O.forward(hh, WW, t, w, tf=tf).loss
+
+    num_dH = np.zeros_like(h)
+    for i in range(N):
+        for k in range(H):
+            e = np.zeros_like(h)
+            e[i, k] = eps
+            num_dH[i, k] = (loss(h + e, W) - loss(h - e, W)) / (2 * eps)
+    num_dW = np.zeros_like(W)
+    for v in range(V):
+        for k in range(H):
+            e = np.zeros_like(W)
+            e[v, k] = eps
+            num_dW[v, k] = (loss(h, W + e) - loss(h, W - e)) / (2 * eps)
+    assert np.linalg.norm(num_dH - b.dH) <= 1e-7 * np.linalg.norm(b.dH)
+    assert np.linalg.norm(num_dW - b.dW) <= 1e-7 * np.linalg.norm(b.dW)
+
+
+def test_transform_matches_torch_autograd():
+    h, W, t, w = _rand(30, 8, 40, seed=34, ignore=(2, 9), weights=True, scale_w=1.5)
+    tf = O.LogitTransform(scale_multiply=0.9, softcap=4.0, temperature=1.3)
+    ht = torch.tensor(h, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    z = ht @ Wt.T * 0.9
+    z = 4.0 * torch.tanh(z / 4.0) / 1.3
+    ce = torch.nn.functional.cross_entropy(z, torch.tensor(t), ignore_index=-100, reduction="none")
+    nv = int((t != -100).sum())
+    loss = (torch.tensor(w) * ce).sum() / nv
+    loss.backward()
+    f = O.forward(h, W, t, w, tf=tf)
+    b = O.backward(h, W, t, w, g=1.0 / nv, tf=tf)
+    assert f.loss == pytest.approx(float(loss.detach()), rel=1e-12)
+    assert np.allclose(f.logp, -ce.detach().numpy(), atol=1e-12)
+    assert np.allclose(b.dH, ht.grad.numpy(), atol=1e-12) and np.allclose(b.dW, Wt.grad.numpy(), atol=1e-12)
+    lse, logp = O.rows_forward(h, W, t, [1, 5], tf=tf)
+    assert np.allclose(logp, f.logp[[1, 5]], atol=1e-13)
+    _, lp2, dH2, _ = O.rows_all(h, W, t, [1, 5], w, g=1.0 / nv, tf=tf)
+    assert np.allclose(dH2, b.dH[[1, 5]], atol=1e-13)
