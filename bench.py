@@ -31,11 +31,14 @@ METRIC = "fused LM-head+CE fwd+bwd tokens/s; % of GB300 BF16 tensor peak (1 GPU)
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "source": "fallback"}
-# DRAM bytes per launch of each kernel kind from the committed ncu capture
-# (profiles/); None when no capture of the current kernel exists.
-# bwd_dW: profiles/bwd_dW_8192x4096x32768.md, scaled from V = 32,768 to the
-# workload's vocabulary (1 store launch + 3 reduce-add launches per step).
-NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {"bwd_dW": 6.37e9}
+# DRAM bytes per launch of each kernel kind from the committed ncu captures
+# (profiles/gemm_kernels_8192x4096x32768.md), scaled from V = 32,768 to the
+# workload's V = 151,936 (D, W and dW grow with V; the h chunk and the dH
+# split partials do not); dW is the mean of 1 store + 3 reduce-add launches.
+# None where traffic does not grow in proportion (FWD) and no full-size
+# capture exists.
+NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {
+    "bwd_dW": 7.40e9, "bwd_dlogits": 3.71e9, "bwd_dH": 6.59e9, "fwd_logits_lse": None}
 NCU_TRAFFIC_WORKLOAD = "sft_16k"
 
 
