@@ -328,8 +328,11 @@ def gpu_arm(args):
 
     # ---- roofline of the dominant kernel (algorithmic FLOPs / live event time)
     peaks = load_peaks()
-    flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dlogits": 2.0 * N * V * H,
-                  "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
+    # algorithmic FLOPs: the forward needs every row's log-sum-exp; the
+    # backward GEMMs only the non-ignored rows (ignored rows have zero dlogits)
+    nv = n_valid_host
+    flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dlogits": 2.0 * nv * V * H,
+                  "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     kern = {}
     for k, (tot_ms, n) in prof.items():
         if n:
@@ -351,7 +354,7 @@ def gpu_arm(args):
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
                 "flops_per_launch": flops_step[dom] / launches_dom,
                 "launch_ms": kern[dom]["ms_per_step"] / launches_dom}
-    step_tflops = 8.0 * N * V * H / (ms_step / 1e3) / 1e12
+    step_tflops = sum(flops_step.values()) / (ms_step / 1e3) / 1e12
     gpu_launches = int(round(sum(n for _, n in prof.values())))
 
     if rank == 0:

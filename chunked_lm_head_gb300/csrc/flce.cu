@@ -133,11 +133,16 @@ __global__ void final_kernel(const double* __restrict__ blk_sum, const long long
   }
 }
 
-// dH[row0 + r, :] = bf16(sum over k-splits of the fp32 partials), split order fixed.
+// dH[row, :] = bf16(sum over k-splits of the fp32 partials), split order
+// fixed; row = row_idx[first + r] for a compacted pass (row count read from
+// dyn_count), else row0 + r.
 template <bool kLong>
 __global__ void dh_reduce_kernel(const float* __restrict__ part, int splits, int rows, int rows_cap,
-                                 int H, int row0, uint16_t* __restrict__ dH) {
+                                 int H, int row0, uint16_t* __restrict__ dH,
+                                 const int* __restrict__ row_idx, const int* __restrict__ dyn_count,
+                                 int first) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
+  if (dyn_count != nullptr) rows = max(0, min(*dyn_count - first, rows_cap));
   const int h4 = H / 4;
   const idx_t total = static_cast<idx_t>(rows) * h4;
   for (idx_t e = static_cast<idx_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -153,8 +158,86 @@ __global__ void dh_reduce_kernel(const float* __restrict__ part, int splits, int
       s.z += q.z;
       s.w += q.w;
     }
-    *reinterpret_cast<uint2*>(dH + static_cast<idx_t>(row0 + r) * H + c) =
+    const int out_row = row_idx != nullptr ? row_idx[first + r] : row0 + r;
+    *reinterpret_cast<uint2*>(dH + static_cast<idx_t>(out_row) * H + c) =
         make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+  }
+}
+
+// ---- row compaction: the indices of the non-ignored rows, in row order
+constexpr int COMPACT_ROWS_PER_THREAD = 4;
+constexpr int COMPACT_ROWS_PER_BLOCK = SMALL_THREADS * COMPACT_ROWS_PER_THREAD;
+
+__global__ void compact_count_kernel(const int64_t* __restrict__ targets, int N, long long ignore,
+                                     int* __restrict__ blk_cnt) {
+  const int base = blockIdx.x * COMPACT_ROWS_PER_BLOCK + threadIdx.x * COMPACT_ROWS_PER_THREAD;
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < COMPACT_ROWS_PER_THREAD; ++k)
+    if (base + k < N && targets[base + k] != ignore) ++c;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) c += __shfl_down_sync(0xffffffffu, c, off);
+  __shared__ int wsum[SMALL_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int s = 0;
+    for (int w = 0; w < SMALL_THREADS / 32; ++w) s += wsum[w];
+    blk_cnt[blockIdx.x] = s;
+  }
+}
+
+__global__ void compact_write_kernel(const int64_t* __restrict__ targets, int N, long long ignore,
+                                     const int* __restrict__ blk_cnt, int nblk, int* __restrict__ idx,
+                                     int* __restrict__ total) {
+  __shared__ int s_off;
+  __shared__ int wtot[SMALL_THREADS / 32];
+  if (threadIdx.x == 0) {
+    int o = 0;
+    for (int b = 0; b < static_cast<int>(blockIdx.x); ++b) o += blk_cnt[b];
+    s_off = o;
+    if (static_cast<int>(blockIdx.x) == nblk - 1) *total = o + blk_cnt[blockIdx.x];
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int base = blockIdx.x * COMPACT_ROWS_PER_BLOCK + threadIdx.x * COMPACT_ROWS_PER_THREAD;
+  bool keep[COMPACT_ROWS_PER_THREAD];
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < COMPACT_ROWS_PER_THREAD; ++k) {
+    keep[k] = base + k < N && targets[base + k] != ignore;
+    c += keep[k] ? 1 : 0;
+  }
+  int x = c;  // inclusive scan over the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) wtot[warp] = x;
+  __syncthreads();
+  int pos = s_off + x - c;
+  for (int w = 0; w < warp; ++w) pos += wtot[w];
+#pragma unroll
+  for (int k = 0; k < COMPACT_ROWS_PER_THREAD; ++k)
+    if (keep[k]) idx[pos++] = base + k;
+}
+
+// hc[r, :] = h[idx[first + r], :] for the pass's rows; zero rows up to the
+// next 64-row boundary (the dW pass reads whole 64-row K blocks).
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ h, int H, const int* __restrict__ idx,
+                                   const int* __restrict__ count, int first, int cap,
+                                   uint16_t* __restrict__ hc) {
+  const int rows = max(0, min(*count - first, cap));
+  const int pad = min((rows + 63) / 64 * 64, cap);
+  const int h8 = H / 8;
+  const long long total = static_cast<long long>(pad) * h8;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(e / h8);
+    const int c = static_cast<int>(e - static_cast<long long>(r) * h8) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) v = *reinterpret_cast<const uint4*>(h + static_cast<long long>(idx[first + r]) * H + c);
+    *reinterpret_cast<uint4*>(hc + static_cast<long long>(r) * H + c) = v;
   }
 }
 
@@ -167,10 +250,14 @@ using namespace flce;
 
 constexpr int kDefaultSms = 152;
 
-enum Kind { K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COUNT };
-const char* const kKindNames[K_COUNT] = {"prep_targets", "fwd_logits_lse", "fwd_combine",
-                                         "fwd_loss",     "bwd_dlogits",    "bwd_dH",
-                                         "bwd_dH_reduce", "bwd_dW"};
+enum Kind {
+  K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COMPACT, K_GATHER,
+  K_COUNT
+};
+const char* const kKindNames[K_COUNT] = {"prep_targets",  "fwd_logits_lse", "fwd_combine",
+                                         "fwd_loss",      "bwd_dlogits",    "bwd_dH",
+                                         "bwd_dH_reduce", "bwd_dW",         "bwd_compact_rows",
+                                         "bwd_gather_rows"};
 
 struct ProfRec {
   int kind;
@@ -295,9 +382,12 @@ FwdLayout fwd_layout(long long N, const FwdPlan& f) {
 }
 
 struct BwdLayout {
-  size_t D = 0, dh_part = 0, bad = 0, total = 0;
+  size_t D = 0, dh_part = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, total = 0;
 };
-BwdLayout bwd_layout(long long H, const BwdPlan& b) {
+// dlogits chunk, dH split-K partials, validation counter, and the row
+// compaction buffers (valid-row indices, per-block counts, their total, the
+// gathered h rows of one chunk).
+BwdLayout bwd_layout(long long N, long long H, const BwdPlan& b) {
   BwdLayout L;
   size_t o = 0;
   L.D = o;
@@ -306,6 +396,14 @@ BwdLayout bwd_layout(long long H, const BwdPlan& b) {
   if (b.dh_splits > 1) o += align256(static_cast<size_t>(b.dh_splits) * b.R * H * 4);
   L.bad = o;
   o += 256;
+  L.idx = o;
+  o += align256(static_cast<size_t>(N) * 4);
+  L.blk = o;
+  o += align256(static_cast<size_t>(ceil_div(N, COMPACT_ROWS_PER_BLOCK)) * 4);
+  L.count = o;
+  o += 256;
+  L.hc = o;
+  o += align256(static_cast<size_t>(b.R) * H * 2);
   L.total = o;
   return L;
 }
@@ -434,6 +532,12 @@ int device_workers(int cg) {
   return n;
 }
 
+// Backward on non-ignored rows only (default); FLCE_COMPACT=0 runs every row.
+bool compact_env() {
+  const char* s = std::getenv("FLCE_COMPACT");
+  return !(s != nullptr && s[0] == '0');
+}
+
 bool validate_env() {
   const char* s = std::getenv("FLCE_VALIDATE");
   return s != nullptr && s[0] != '\0' && s[0] != '0';
@@ -520,7 +624,7 @@ size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows)
   const int cg = cta_group();
   const int workers = device_workers(cg);
   const FwdLayout fl = fwd_layout(N, plan_forward(N, H, V, workers, BM * cg));
-  const BwdLayout bl = bwd_layout(H, plan_backward(N, H, V, chunk_rows, workers, BM * cg));
+  const BwdLayout bl = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
 
@@ -581,6 +685,7 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
     p.cols = f.S;
     p.n_per_unit = f.tps;
     p.kb_per_split = f.k_blocks;
+    p.k_splits = 1;
     p.num_units = f.units;
     p.group_m = std::min(8, f.m_tiles);
     p.row0 = 0;
@@ -652,7 +757,7 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
   const int workers = device_workers(cg);
   const int tm = BM * cg;
   const BwdPlan b = plan_backward(N, H, V, chunk_rows, workers, tm);
-  const BwdLayout L = bwd_layout(H, b);
+  const BwdLayout L = bwd_layout(N, H, b);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
   if (s != FLCE_OK) return s;
@@ -706,12 +811,57 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
   base.tf_b = tfp.tf_b;
   base.tf_d = tfp.tf_d;
 
+  // Row compaction: the chunks run over the non-ignored rows (count and
+  // indices stay on the device; the kernels read each chunk's row count), so
+  // ignored rows cost nothing in the three backward GEMMs.  Their dH rows are
+  // zeroed up front.
+  const bool compact = compact_env();
+  int* cidx = reinterpret_cast<int*>(wb + L.idx);
+  int* cblk = reinterpret_cast<int*>(wb + L.blk);
+  int* ccount = reinterpret_cast<int*>(wb + L.count);
+  uint16_t* hc = reinterpret_cast<uint16_t*>(wb + L.hc);
+  CUtensorMap hc_k, hc_mn, Dfix_k, Dfix_mn;
+  if (compact) {
+    const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
+    {
+      ProfScope ps(K_COMPACT, st);
+      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
+                                                           cblk);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    {
+      ProfScope ps(K_COMPACT, st);
+      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
+                                                           cblk, nblk, cidx, ccount);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    if (dH) FLCE_CUDA_TRY(cudaMemsetAsync(dH, 0, static_cast<size_t>(N) * H * 2, st));
+    if (!make_map(&hc_k, hc, H, b.R, H, BK, BM) || !make_map(&hc_mn, hc, H, b.R, H, 64, BK) ||
+        !make_map(&Dfix_k, Dbuf, b.ldD, b.R, b.ldD, BK, BM) ||
+        !make_map(&Dfix_mn, Dbuf, b.ldD, b.R, b.ldD, 64, BK))
+      return FLCE_ERR_CUDA;
+  }
+
   int chunk = 0;
   for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
-    const int rows = static_cast<int>(std::min(b.R, N - row0));
+    // rows: exact (plain) or the capacity whose live part the kernels read (compacted)
+    const int rows = compact ? static_cast<int>(b.R) : static_cast<int>(std::min(b.R, N - row0));
     GemmParams p = base;
-    p.row0 = static_cast<int>(row0);
+    p.row0 = compact ? 0 : static_cast<int>(row0);
     p.rows = rows;
+    if (compact) {
+      p.row_idx = cidx;
+      p.dyn_count = ccount;
+      p.chunk_first = static_cast<int>(row0);
+      const long long total = b.R * (H / 8);
+      const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
+      ProfScope ps(K_GATHER, st);
+      gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, ccount,
+                                                          static_cast<int>(row0), static_cast<int>(b.R), hc);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    const CUtensorMap& A_dl = compact ? hc_k : h_k;
+    const CUtensorMap& B_dw = compact ? hc_mn : h_mn;
     // (1) recompute logits, dlogits chunk -> D[rows, ldD] bf16
     {
       GemmParams q = p;
@@ -721,14 +871,20 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
       q.cols = q.n_tiles;
       q.n_per_unit = 1;
       q.kb_per_split = q.k_blocks;
+      q.k_splits = 1;
       q.num_units = q.m_tiles * q.n_tiles;
       q.group_m = std::min(8, q.m_tiles);
       ProfScope ps(K_DLOGITS, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, h_k, W_k, W_k, q, std::min(q.num_units, workers), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, A_dl, W_k, W_k, q, std::min(q.num_units, workers), st));
     }
     CUtensorMap D_k, D_mn;
-    if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) || !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
+    if (compact) {
+      D_k = Dfix_k;
+      D_mn = Dfix_mn;
+    } else if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) ||
+               !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK)) {
       return FLCE_ERR_CUDA;
+    }
     // (2) dH[rows] = D W
     if (dH) {
       GemmParams q = p;
@@ -739,6 +895,7 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
       q.n_per_unit = 1;
       q.kb_per_split = b.dh_kb_per_split;
       const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
+      q.k_splits = splits;
       q.num_units = splits * q.m_tiles * q.n_tiles;
       q.group_m = q.m_tiles;
       q.dH_part = splits > 1 ? dh_part : nullptr;
@@ -750,12 +907,16 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
         ProfScope ps(K_DH_REDUCE, st);
         const long long total = static_cast<long long>(rows) * (H / 4);
         const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
+        const int* ri = compact ? cidx : nullptr;
+        const int* dc = compact ? ccount : nullptr;
         if (kLong)
           dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
-                                                                 static_cast<int>(H), p.row0, dH);
+                                                                 static_cast<int>(H), p.row0, dH, ri, dc,
+                                                                 static_cast<int>(row0));
         else
           dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
-                                                                  static_cast<int>(H), p.row0, dH);
+                                                                  static_cast<int>(H), p.row0, dH, ri, dc,
+                                                                  static_cast<int>(row0));
         FLCE_CUDA_TRY(cudaGetLastError());
       }
     }
@@ -768,11 +929,12 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
       q.cols = q.n_tiles;
       q.n_per_unit = 1;
       q.kb_per_split = q.k_blocks;
+      q.k_splits = 1;
       q.num_units = q.m_tiles * q.n_tiles;
       q.group_m = std::min(8, q.m_tiles);
       q.dW_accumulate = chunk > 0 ? 1 : 0;
       ProfScope ps(K_DW, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(cg, kLong, D_mn, h_mn, dW_map, q, std::min(q.num_units, workers), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(cg, kLong, D_mn, B_dw, dW_map, q, std::min(q.num_units, workers), st));
     }
   }
   return FLCE_OK;

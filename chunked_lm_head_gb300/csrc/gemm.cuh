@@ -98,36 +98,70 @@ struct GemmParams {
   float* dW;          // DW out [V][H] fp32
   int dW_accumulate;
   int* err;           // device error word
+  // Row compaction (backward on non-ignored rows only): row_idx maps a
+  // compacted row to its original row; this pass holds compacted rows
+  // [chunk_first, chunk_first + rows) with rows = min(*dyn_count - chunk_first,
+  // rows_cap) read on the device.  row_idx == nullptr: rows are row0 + i.
+  const int* row_idx;
+  const int* dyn_count;
+  int chunk_first;
+  int k_splits;
 };
+
+// Problem extents that depend on the device-side row count of a compacted pass.
+struct DynShape {
+  int rows, m_tiles, k_blocks, kb_per_split, num_units;
+};
+
+template <int MODE, int TM>
+__device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
+  DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units};
+  if (p.dyn_count != nullptr) {
+    d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
+    if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH) {
+      d.m_tiles = (d.rows + TM - 1) / TM;
+      d.num_units = p.k_splits * d.m_tiles * p.cols;
+    } else if constexpr (MODE == MODE_DW) {
+      // K = the pass's rows; an empty first pass still writes zeros to dW,
+      // an empty later pass has nothing to add
+      d.k_blocks = (d.rows + BK - 1) / BK;
+      d.kb_per_split = max(d.k_blocks, 1);
+      d.num_units = (d.rows == 0 && p.dW_accumulate) ? 0 : p.m_tiles * p.cols;
+    }
+  }
+  return d;
+}
 
 struct Unit {
   int m, n0, n1, kb0, kb1, split;
 };
 
 template <int MODE>
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
-  const int per_split = p.m_tiles * p.cols;
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape& d, int u) {
+  const int m_tiles = d.m_tiles;
+  const int group_m = min(p.group_m, max(m_tiles, 1));
+  const int per_split = m_tiles * p.cols;
   const int ks = u / per_split;
   const int r = u - ks * per_split;
-  const int full_groups = p.m_tiles / p.group_m;
+  const int full_groups = m_tiles / group_m;
   int first_m, gsize, local;
-  if (r < full_groups * p.group_m * p.cols) {
-    const int g = r / (p.group_m * p.cols);
-    first_m = g * p.group_m;
-    gsize = p.group_m;
-    local = r - g * p.group_m * p.cols;
+  if (r < full_groups * group_m * p.cols) {
+    const int g = r / (group_m * p.cols);
+    first_m = g * group_m;
+    gsize = group_m;
+    local = r - g * group_m * p.cols;
   } else {
-    first_m = full_groups * p.group_m;
-    gsize = p.m_tiles - first_m;
-    local = r - full_groups * p.group_m * p.cols;
+    first_m = full_groups * group_m;
+    gsize = m_tiles - first_m;
+    local = r - full_groups * group_m * p.cols;
   }
   Unit t;
   t.m = first_m + local % gsize;
   const int c = local / gsize;
   t.n0 = c * p.n_per_unit;
   t.n1 = min(p.n_tiles, t.n0 + p.n_per_unit);
-  t.kb0 = ks * p.kb_per_split;
-  t.kb1 = min(p.k_blocks, t.kb0 + p.kb_per_split);
+  t.kb0 = ks * d.kb_per_split;
+  t.kb1 = min(d.k_blocks, t.kb0 + d.kb_per_split);
   t.split = (MODE == MODE_FWD) ? c : ks;
   return t;
 }
@@ -308,6 +342,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const DynShape dsh = dyn_shape<MODE, C::TM>(p);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -317,8 +352,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = worker; u < p.num_units && ok; u += nworkers) {
-        const Unit t = decode_unit<MODE>(p, u);
+      for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
+        const Unit t = decode_unit<MODE>(p, dsh, u);
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
@@ -350,8 +385,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0 && issuer) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = worker; u < p.num_units && ok; u += nworkers) {
-        const Unit t = decode_unit<MODE>(p, u);
+      for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
+        const Unit t = decode_unit<MODE>(p, dsh, u);
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -396,11 +431,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t tempty_target1 = CG == 2 ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int u = worker; u < p.num_units && ok; u += nworkers) {
-      const Unit t = decode_unit<MODE>(p, u);
+    for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
+      const Unit t = decode_unit<MODE>(p, dsh, u);
       // per-unit row state
       const int lr = t.m * C::TM + rank * BM + r;  // row inside this pass (FWD: global row)
-      const int grow = p.row0 + lr;
       bool row_ok;
       long long tgt = -1;
       float run_m = -INFINITY, run_s = 0.f;  // FWD: log2-domain max and sum
@@ -412,8 +446,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if constexpr (MODE == MODE_DW) {
         row_ok = lr < p.V;  // rows of the accumulator are vocabulary rows here
       } else {
-        row_ok = lr < p.rows;
+        row_ok = lr < dsh.rows;
       }
+      // original row of this accumulator row (targets, weights, lse, dH)
+      int grow = p.row0 + lr;
+      if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH) {
+        if (p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
+      }
+      // DLOGITS also writes zero rows up to the next 64-row K block so that
+      // the dW pass over this chunk reads zeros past its last row
+      const bool row_store = lr < min((dsh.rows + BK - 1) / BK * BK, p.rows_cap);
       if constexpr (MODE == MODE_FWD) {
         if (row_ok) tgt = p.targets[grow];
       }
@@ -440,7 +482,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
-          tmem_ld32(tbase + c * 32, v);
+          if (t.kb1 > t.kb0) {
+            tmem_ld32(tbase + c * 32, v);
+          } else {  // empty K range (a compacted pass without rows): the product is zero
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          }
           const int col0 = n * BN + c * 32;
           if constexpr (MODE == MODE_FWD) {
             if (p.tf_softcap) {
@@ -503,7 +550,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 pk[j / 2] = pack_bf16x2(d0, d1);
               }
             }
-            if (row_ok) {
+            if (row_store) {
               uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;
 #pragma unroll
               for (int g = 0; g < 4; ++g)

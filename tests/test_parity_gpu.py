@@ -242,3 +242,26 @@ def test_both_cta_group_paths(cg, monkeypatch):
     inp = WL.make_inputs(wl)
     inp.weights = np.random.default_rng(11).uniform(0.5, 1.5, wl.N).astype(np.float32)
     _full_check(inp, 256)
+
+
+def test_row_compaction_matches_full_rows(monkeypatch):
+    """The backward on non-ignored rows only (default) against the backward
+    over every row (FLCE_COMPACT=0) and the oracle, with a GRPO-like mask
+    (prompt prefixes ignored) spanning several chunks and an empty last chunk."""
+    wl = WL.custom("compact", 4 * 160, 192, 2500, 128, w_std=0.05, targets="zipf", grpo_seqs=4,
+                   prompt_len=70, seed=111)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, 128)
+    assert nv == 4 * 90
+    g = 1.0 / nv
+    dH_c, dW_c = run_backward(h, W, t, w, lse, g, 128)
+    monkeypatch.setenv("FLCE_COMPACT", "0")
+    dH_f, dW_f = run_backward(h, W, t, w, lse, g, 128)
+    ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g)
+    for name, got in (("dH compact", dH_c), ("dH full", dH_f)):
+        assert_grad_close(np64(got), ref.dH, name)
+    for name, got in (("dW compact", dW_c), ("dW full", dW_f)):
+        assert_grad_close(np64(got), ref.dW, name)
+    ign = torch.from_numpy(inp.targets == WL.IGNORE_INDEX).cuda()
+    assert torch.all(dH_c[ign] == 0)
