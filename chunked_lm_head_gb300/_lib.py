@@ -40,6 +40,7 @@ SIGNATURES = {
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
     "flce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "flce_device_status": (ctypes.c_int, [_c_vp]),
+    "flce_selftest_wait_timeout": (ctypes.c_int, [_c_i64, _c_vp]),
     "flce_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "flce_profile_num_kinds": (ctypes.c_int, []),
     "flce_profile_kind_name": (ctypes.c_char_p, [ctypes.c_int]),

@@ -22,6 +22,7 @@
 namespace flce {
 
 __device__ int g_device_error;  // bit DEVERR_TIMEOUT: a bounded wait ran out
+__device__ int g_selftest_flag;  // verdict of wait_selftest_kernel
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int SMALL_THREADS = 256;
@@ -238,6 +239,24 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ h, int H, const 
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) v = *reinterpret_cast<const uint4*>(h + static_cast<long long>(idx[first + r]) * H + c);
     *reinterpret_cast<uint4*>(hc + static_cast<long long>(r) * H + c) = v;
+  }
+}
+
+// Self-test of the bounded wait: one warp waits on an mbarrier that nothing
+// arrives on, through the same wait routine the GEMM pipelines use, with a
+// short limit; it must give up, raise the device error word and return.
+__global__ void wait_selftest_kernel(long long limit_cycles, int* err, int* gave_up) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = wait_bar(smem_u32(&bar), 0, &abort_flag, err, limit_cycles);
+    *gave_up = ok ? 0 : 1;
   }
 }
 
@@ -975,6 +994,21 @@ flce_status flce_device_status(void* stream) {
     return FLCE_ERR_TIMEOUT;
   }
   return FLCE_OK;
+}
+
+flce_status flce_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles <= 0 || limit_cycles > WAIT_LIMIT_CYCLES) return FLCE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = nullptr;
+  FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+  int* gave_up = nullptr;
+  FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&gave_up), g_selftest_flag));
+  wait_selftest_kernel<<<1, 32, 0, st>>>(static_cast<long long>(limit_cycles), err, gave_up);
+  FLCE_CUDA_TRY(cudaGetLastError());
+  int h_gave_up = 0;
+  FLCE_CUDA_TRY(cudaMemcpyAsync(&h_gave_up, gave_up, sizeof(int), cudaMemcpyDeviceToHost, st));
+  FLCE_CUDA_TRY(cudaStreamSynchronize(st));
+  return h_gave_up ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
 flce_status flce_profile_enable(int enable) {

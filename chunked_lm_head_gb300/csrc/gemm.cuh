@@ -170,12 +170,12 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape&
 // abort flag and the device error word) when the limit runs out, or when
 // another role of the CTA has already aborted.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         int* err) {
+                                         int* err, long long limit = WAIT_LIMIT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(err, DEVERR_TIMEOUT);
       return false;

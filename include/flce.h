@@ -214,6 +214,15 @@ FLCE_API const char* flce_status_string(flce_status s);
  * else FLCE_OK. */
 FLCE_API flce_status flce_device_status(void* stream);
 
+/* Diagnostic of the kernels' bounded waits (failure detection without a GPU
+ * fault).  Launches one warp that waits, through the same bounded-wait
+ * routine as the GEMM pipelines, on an mbarrier nothing arrives on, giving up
+ * after `limit_cycles` SM clock cycles (1 .. 2e9).  Synchronises `stream`.
+ * Returns FLCE_OK when the wait gave up and returned as designed; the device
+ * error word is then set, so the next flce_device_status returns
+ * FLCE_ERR_TIMEOUT (and clears it).  The CUDA context stays usable. */
+FLCE_API flce_status flce_selftest_wait_timeout(int64_t limit_cycles, void* stream);
+
 /* ---- profiling (CUDA events around each launch, on the launch stream) ---- */
 
 /* Enable (1) or disable (0) per-kernel event timing; enabling clears totals. */
