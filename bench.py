@@ -31,14 +31,11 @@ METRIC = "fused LM-head+CE fwd+bwd tokens/s; % of GB300 BF16 tensor peak (1 GPU)
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "source": "fallback"}
-# DRAM bytes per launch of each kernel kind from the committed ncu captures
-# (profiles/gemm_kernels_8192x4096x32768.md), scaled from V = 32,768 to the
-# workload's V = 151,936 (D, W and dW grow with V; the h chunk and the dH
-# split partials do not); dW is the mean of 1 store + 3 reduce-add launches.
-# None where traffic does not grow in proportion (FWD) and no full-size
-# capture exists.
+# DRAM bytes (read + write) per launch of each GEMM kind on the 16K SFT
+# workload, measured at full size (profiles/dram_sft_16k.md; mean over the
+# step's launches).
 NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {
-    "bwd_dW": 7.40e9, "bwd_dlogits": 3.71e9, "bwd_dH": 6.59e9, "fwd_logits_lse": None}
+    "fwd_logits_lse": 18.79e9, "bwd_dlogits": 3.10e9, "bwd_dH": 8.38e9, "bwd_dW": 7.66e9}
 NCU_TRAFFIC_WORKLOAD = "sft_16k"
 
 

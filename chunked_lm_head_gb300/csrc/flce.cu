@@ -706,7 +706,10 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
     p.kb_per_split = f.k_blocks;
     p.k_splits = 1;
     p.num_units = f.units;
-    p.group_m = std::min(8, f.m_tiles);
+    // 16 row tiles share each run of vocabulary tiles in L2 (measured on the
+    // 16K x 4096 x 151,936 case: DRAM reads 17.9 GB at 16 against 36.6 GB at
+    // 8 and 23.6 GB at 32, and the fastest launch)
+    p.group_m = std::min(16, f.m_tiles);
     p.row0 = 0;
     p.rows = Ni;
     p.rows_cap = Ni;
@@ -892,7 +895,9 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
       q.kb_per_split = q.k_blocks;
       q.k_splits = 1;
       q.num_units = q.m_tiles * q.n_tiles;
-      q.group_m = std::min(8, q.m_tiles);
+      // 16 row tiles per W run in L2 (16K x 4096 x 151,936: DRAM reads 1.9 GB
+      // per chunk at 16 against 3.5 GB at 8)
+      q.group_m = std::min(16, q.m_tiles);
       ProfScope ps(K_DLOGITS, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, A_dl, W_k, W_k, q, std::min(q.num_units, workers), st));
     }
