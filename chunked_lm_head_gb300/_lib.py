@@ -81,11 +81,13 @@ def header_symbols() -> list[str]:
 
 
 def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libflce.so (building it in-tree first when it is absent)."""
+    """Load libflce.so (building it in-tree first when it is absent).
+
+    FLCE_LIB_PATH in the environment selects another build of the library."""
     global _LIB
     if _LIB is not None and path is None:
         return _LIB
-    p = path or _build.LIB_PATH
+    p = path or os.environ.get("FLCE_LIB_PATH") or _build.LIB_PATH
     if not os.path.exists(p):
         if not build_if_missing:
             raise FileNotFoundError(p)

@@ -506,8 +506,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (nm != -INFINITY) {
               float a = 0.f;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) a += exp2f(fmaf(v[j], l2a, -nm));
-              run_s = run_s * exp2f(run_m - nm) + a;
+              for (int j = 0; j < 32; ++j) a += ex2_approx(fmaf(v[j], l2a, -nm));
+              run_s = run_s * ex2_approx(run_m - nm) + a;
               run_m = nm;
             }
             const long long tj = tgt - col0;
@@ -524,8 +524,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < 32; j += 2) {
                 float d0 = 0.f, d1 = 0.f;
                 if (scale != 0.f) {
-                  float p0 = exp2f(fmaf(v[j], l2a, nl2));
-                  float p1 = exp2f(fmaf(v[j + 1], l2a, nl2));
+                  float p0 = ex2_approx(fmaf(v[j], l2a, nl2));
+                  float p1 = ex2_approx(fmaf(v[j + 1], l2a, nl2));
                   if (j == tj) p0 -= 1.f;
                   if (j + 1 == tj) p1 -= 1.f;
                   d0 = (col0 + j < p.V) ? p0 * scale_a : 0.f;
@@ -540,8 +540,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (scale != 0.f) {
                   const float t0 = tanhf(p.tf_a * v[j]);
                   const float t1 = tanhf(p.tf_a * v[j + 1]);
-                  float p0 = exp2f(fmaf(p.tf_b * t0, kLog2e, nl2));
-                  float p1 = exp2f(fmaf(p.tf_b * t1, kLog2e, nl2));
+                  float p0 = ex2_approx(fmaf(p.tf_b * t0, kLog2e, nl2));
+                  float p1 = ex2_approx(fmaf(p.tf_b * t1, kLog2e, nl2));
                   if (j == tj) p0 -= 1.f;
                   if (j + 1 == tj) p1 -= 1.f;
                   d0 = (col0 + j < p.V) ? p0 * scale * p.tf_d * (1.f - t0 * t0) : 0.f;
