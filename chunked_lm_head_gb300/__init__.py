@@ -5,4 +5,4 @@ package holds its ctypes binding, a thin torch-facing API and the seeded
 synthetic workloads.
 """
 from .api import (IGNORE_INDEX, LinearCrossEntropy, backward, forward,  # noqa: F401
-                  linear_cross_entropy, workspace_bytes)
+                  kd_backward, kd_forward, linear_cross_entropy, workspace_bytes)

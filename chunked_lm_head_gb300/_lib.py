@@ -35,6 +35,13 @@ SIGNATURES = {
     "flce_backward_ex": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp,
                                         _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
                                         ctypes.c_size_t, _c_vp]),
+    "flce_kd_forward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                       _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp,
+                                       _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_kd_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                        _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp, _c_i64, _c_i64,
+                                        _c_i64, _c_i64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_kd_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64]),
     "flce_forward_static_scratch": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                                    _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
@@ -169,6 +176,30 @@ def flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, c
                                 float(grad_scale), _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
                                 ignore_index, tp, _ptr(workspace), workspace_bytes,
                                 _stream_handle(stream))
+
+
+def flce_kd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows, ignore_index,
+                    transform, out_kl, out_lse_s, out_lse_t, out_loss, out_n_valid, workspace=None,
+                    workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the distillation forward."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_kd_forward(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                               _ptr(weights), N, V, chunk_rows, ignore_index, tp, _ptr(out_kl),
+                               _ptr(out_lse_s), _ptr(out_lse_t), _ptr(out_loss), _ptr(out_n_valid),
+                               _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_kd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, grad_scale, dH_s,
+                     dW_s, N, V, chunk_rows, ignore_index, transform, workspace=None,
+                     workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the distillation backward (student gradients)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_kd_backward(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                _ptr(weights), _ptr(lse_s), _ptr(lse_t), float(grad_scale),
+                                _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows, ignore_index, tp,
+                                _ptr(workspace), workspace_bytes, _stream_handle(stream))
 
 
 def flce_forward_static_scratch(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp,

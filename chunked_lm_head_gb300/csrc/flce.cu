@@ -242,6 +242,73 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ h, int H, const 
   }
 }
 
+// Distillation combine: student and teacher log-sum-exps from the split
+// partials, KL(p_t || p_s) = C / S_t - lse_t + lse_s per row, and the block's
+// share of sum(m w kl) and of the counted rows (targets == NULL: all rows).
+template <bool kLong>
+__global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* __restrict__ pt,
+                                  const float* __restrict__ pc, int S, int N,
+                                  const int64_t* __restrict__ targets,
+                                  const float* __restrict__ weights, long long ignore,
+                                  float* __restrict__ out_kl, float* __restrict__ out_lse_s,
+                                  float* __restrict__ out_lse_t, double* __restrict__ blk_sum,
+                                  long long* __restrict__ blk_cnt) {
+  using idx_t = typename std::conditional<kLong, long long, int>::type;
+  const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
+  double contrib = 0.0;
+  long long cnt = 0;
+  if (i < N) {
+    float Ms = -INFINITY, Mt = -INFINITY;
+    for (int s = 0; s < S; ++s) {
+      Ms = fmaxf(Ms, ps[static_cast<idx_t>(s) * N + i].x);
+      Mt = fmaxf(Mt, pt[static_cast<idx_t>(s) * N + i].x);
+    }
+    float Ss = 0.f, St = 0.f, Cc = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const idx_t o = static_cast<idx_t>(s) * N + i;
+      Ss += ps[o].y * exp2f(ps[o].x - Ms);
+      const float r = exp2f(pt[o].x - Mt);
+      St += pt[o].y * r;
+      Cc += pc[o] * r;
+    }
+    const float lse_s = (Ms + log2f(Ss)) * kLn2;
+    const float lse_t = (Mt + log2f(St)) * kLn2;
+    const bool valid = targets == nullptr || targets[i] != ignore;
+    const float kl = valid ? Cc / St - lse_t + lse_s : 0.f;
+    if (out_kl) out_kl[i] = kl;
+    if (out_lse_s) out_lse_s[i] = lse_s;
+    if (out_lse_t) out_lse_t[i] = lse_t;
+    if (valid) {
+      cnt = 1;
+      // the final kernel negates the sum (it serves -sum(w logp) for the
+      // cross-entropy), so the KL enters with a minus sign
+      contrib = -static_cast<double>(weights ? weights[i] : 1.f) * static_cast<double>(kl);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
+    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
+  }
+  __shared__ double ssum[SMALL_THREADS / 32];
+  __shared__ long long scnt[SMALL_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) {
+    ssum[threadIdx.x >> 5] = contrib;
+    scnt[threadIdx.x >> 5] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0;
+    long long c = 0;
+    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
+      a += ssum[w];
+      c += scnt[w];
+    }
+    blk_sum[blockIdx.x] = a;
+    blk_cnt[blockIdx.x] = c;
+  }
+}
+
 // Self-test of the bounded wait: one warp waits on an mbarrier that nothing
 // arrives on, through the same wait routine the GEMM pipelines use, with a
 // short limit; it must give up, raise the device error word and return.
@@ -271,12 +338,12 @@ constexpr int kDefaultSms = 152;
 
 enum Kind {
   K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COMPACT, K_GATHER,
-  K_COUNT
+  K_KD_FWD, K_KD_DLOGITS, K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {"prep_targets",  "fwd_logits_lse", "fwd_combine",
                                          "fwd_loss",      "bwd_dlogits",    "bwd_dH",
                                          "bwd_dH_reduce", "bwd_dW",         "bwd_compact_rows",
-                                         "bwd_gather_rows"};
+                                         "bwd_gather_rows", "kd_fwd_logits",  "kd_bwd_dlogits"};
 
 struct ProfRec {
   int kind;
@@ -400,6 +467,28 @@ FwdLayout fwd_layout(long long N, const FwdPlan& f) {
   return L;
 }
 
+// Distillation forward scratch: student and teacher split partials, the
+// cross term, block sums.
+struct KdFwdLayout {
+  size_t ps = 0, pt = 0, pc = 0, bsum = 0, bcnt = 0, total = 0;
+};
+KdFwdLayout kd_fwd_layout(long long N, const FwdPlan& f) {
+  KdFwdLayout L;
+  size_t o = 0;
+  L.ps = o;
+  o += align256(static_cast<size_t>(f.S) * N * 8);
+  L.pt = o;
+  o += align256(static_cast<size_t>(f.S) * N * 8);
+  L.pc = o;
+  o += align256(static_cast<size_t>(f.S) * N * 4);
+  L.bsum = o;
+  o += align256(static_cast<size_t>(f.nblk) * 8);
+  L.bcnt = o;
+  o += align256(static_cast<size_t>(f.nblk) * 8);
+  L.total = o;
+  return L;
+}
+
 struct BwdLayout {
   size_t D = 0, dh_part = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, total = 0;
 };
@@ -471,13 +560,14 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer
 
 template <int MODE, bool kLong, int CG>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                          const GemmParams& p, int workers, cudaStream_t st) {
+                          const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p,
+                          int workers, cudaStream_t st) {
   auto k = flce_gemm_kernel<MODE, kLong, CG>;
   constexpr int smem = TileCfg<CG>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if constexpr (CG == 1) {
-    k<<<workers, GEMM_THREADS, smem, st>>>(a, b, c, p);
+    k<<<workers, GEMM_THREADS, smem, st>>>(a, b, c, a2, b2, p);
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * workers, 1, 1);
@@ -491,7 +581,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k, a, b, c, p);
+    e = cudaLaunchKernelEx(&cfg, k, a, b, c, a2, b2, p);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
@@ -502,12 +592,16 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
 // the other modes ignore it.
 template <int MODE>
 cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st) {
+                        const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st,
+                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr) {
+  // a2 / b2: the teacher's operands of the distillation modes (else unused)
+  const CUtensorMap& A2 = a2 ? *a2 : a;
+  const CUtensorMap& B2 = b2 ? *b2 : b;
   if (cg == 2)
-    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, p, workers, st)
-                 : launch_gemm_t<MODE, false, 2>(a, b, c, p, workers, st);
-  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, p, workers, st)
-               : launch_gemm_t<MODE, false, 1>(a, b, c, p, workers, st);
+    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, A2, B2, p, workers, st)
+                 : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, p, workers, st);
+  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, A2, B2, p, workers, st)
+               : launch_gemm_t<MODE, false, 1>(a, b, c, A2, B2, p, workers, st);
 }
 
 // CTA group of the GEMMs: 2 (SM pairs, 256-row tiles) unless FLCE_CTA_GROUP=1.
@@ -980,6 +1074,261 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
                           void* stream) {
   return flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
                           ignore_index, nullptr, workspace, workspace_bytes, stream);
+}
+
+size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, int64_t chunk_rows) {
+  if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return 0;
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const KdFwdLayout fl = kd_fwd_layout(N, plan_forward(N, H_s + H_t, V, workers, BM * cg));
+  const BwdLayout bl = bwd_layout(N, H_s, plan_backward(N, H_s, V, chunk_rows, workers, BM * cg));
+  return std::max(fl.total, bl.total);
+}
+
+flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                            const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                            const int64_t* targets, const float* weights, int64_t N, int64_t V,
+                            int64_t chunk_rows, int64_t ignore_index,
+                            const flce_logit_transform* transform, float* out_kl, float* out_lse_s,
+                            float* out_lse_t, float* out_loss, int64_t* out_n_valid,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  (void)chunk_rows;
+  if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return FLCE_ERR_INVALID_ARG;
+  GemmParams tfp{};
+  if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
+  if (!out_kl && !out_lse_s && !out_lse_t && !out_loss && !out_n_valid) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!h_s || !W_s || !h_t || !W_t)) return FLCE_ERR_INVALID_ARG;
+  if (H_s % 8 != 0 || H_t % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(h_s, 16) || !aligned(W_s, 16) || !aligned(h_t, 16) || !aligned(W_t, 16) ||
+      !aligned(targets, 8) || !aligned(weights, 4) || !aligned(out_kl, 4) || !aligned(out_lse_s, 4) ||
+      !aligned(out_lse_t, 4) || !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const int kbs = static_cast<int>(ceil_div(H_s, BK));
+  const int kbt = static_cast<int>(ceil_div(H_t, BK));
+  const FwdPlan f = plan_forward(N, H_s + H_t, V, workers, BM * cg);
+  const KdFwdLayout L = kd_fwd_layout(N, f);
+  Workspace ws;
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  float2* ps = reinterpret_cast<float2*>(wb + L.ps);
+  float2* pt = reinterpret_cast<float2*>(wb + L.pt);
+  float* pc = reinterpret_cast<float*>(wb + L.pc);
+  double* bsum = reinterpret_cast<double*>(wb + L.bsum);
+  long long* bcnt = reinterpret_cast<long long*>(wb + L.bcnt);
+  const int Ni = static_cast<int>(N);
+  if (N > 0) {
+    CUtensorMap hs_k, Ws_k, ht_k, Wt_k;
+    if (!make_map(&hs_k, h_s, H_s, N, H_s, BK, BM) || !make_map(&Ws_k, W_s, H_s, V, H_s, BK, BN / cg) ||
+        !make_map(&ht_k, h_t, H_t, N, H_t, BK, BM) || !make_map(&Wt_k, W_t, H_t, V, H_t, BK, BN / cg))
+      return FLCE_ERR_CUDA;
+    int* err = nullptr;
+    FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+    GemmParams p{};
+    p.m_tiles = f.m_tiles;
+    p.n_tiles = f.n_tiles;
+    p.k_blocks = kbs + kbt;
+    p.k_blocks_s = kbs;
+    p.cols = f.S;
+    p.n_per_unit = f.tps;
+    p.kb_per_split = kbs + kbt;
+    p.k_splits = 1;
+    p.num_units = f.units;
+    p.group_m = std::min(16, f.m_tiles);
+    p.rows = Ni;
+    p.rows_cap = Ni;
+    p.N = Ni;
+    p.H = static_cast<int>(H_s);
+    p.V = static_cast<int>(V);
+    p.targets = targets;
+    p.weights = weights;
+    p.ignore_index = ignore_index;
+    p.partials = ps;
+    p.partials_t = pt;
+    p.partials_c = pc;
+    p.err = err;
+    p.tf_softcap = tfp.tf_softcap;
+    p.tf_a = tfp.tf_a;
+    p.tf_b = tfp.tf_b;
+    p.tf_d = tfp.tf_d;
+    const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
+                       static_cast<long long>(f.S) * N >= INT_MAX;
+    {
+      ProfScope prof(K_KD_FWD, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_KD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, p, f.grid, st, &ht_k, &Wt_k));
+    }
+    {
+      ProfScope prof(K_COMBINE, st);
+      if (kLong)
+        kd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(ps, pt, pc, f.S, Ni, targets, weights,
+                                                                  ignore_index, out_kl, out_lse_s,
+                                                                  out_lse_t, bsum, bcnt);
+      else
+        kd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(ps, pt, pc, f.S, Ni, targets, weights,
+                                                                   ignore_index, out_kl, out_lse_s,
+                                                                   out_lse_t, bsum, bcnt);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+  }
+  if (out_loss || out_n_valid) {
+    ProfScope prof(K_FINAL, st);
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
+                                              reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
+}
+
+flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                             const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                             const int64_t* targets, const float* weights, const float* lse_s,
+                             const float* lse_t, float grad_scale, flce_bf16* dH_s, float* dW_s,
+                             int64_t N, int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                             const flce_logit_transform* transform, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return FLCE_ERR_INVALID_ARG;
+  GemmParams tfp{};
+  if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
+  if (!dH_s && !dW_s) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!h_s || !W_s || !h_t || !W_t || !lse_s || !lse_t)) return FLCE_ERR_INVALID_ARG;
+  if (H_s % 8 != 0 || H_t % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(h_s, 16) || !aligned(W_s, 16) || !aligned(h_t, 16) || !aligned(W_t, 16) ||
+      !aligned(dH_s, 16) || !aligned(dW_s, 16) || !aligned(targets, 8) || !aligned(weights, 4) ||
+      !aligned(lse_s, 4) || !aligned(lse_t, 4))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (dW_s) FLCE_CUDA_TRY(cudaMemsetAsync(dW_s, 0, static_cast<size_t>(V) * H_s * 4, st));
+    return FLCE_OK;
+  }
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const int tm = BM * cg;
+  const BwdPlan b = plan_backward(N, H_s, V, chunk_rows, workers, tm);
+  const BwdLayout L = bwd_layout(N, H_s, b);
+  Workspace ws;
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  uint16_t* Dbuf = reinterpret_cast<uint16_t*>(wb + L.D);
+  float* dh_part = b.dh_splits > 1 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
+  int* err = nullptr;
+  FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+  CUtensorMap hs_k, Ws_k, ht_k, Wt_k, Ws_mn, hs_mn, dW_map;
+  if (!make_map(&hs_k, h_s, H_s, N, H_s, BK, BM) || !make_map(&Ws_k, W_s, H_s, V, H_s, BK, BN / cg) ||
+      !make_map(&ht_k, h_t, H_t, N, H_t, BK, BM) || !make_map(&Wt_k, W_t, H_t, V, H_t, BK, BN / cg) ||
+      !make_map(&Ws_mn, W_s, H_s, V, H_s, 64, BK) || !make_map(&hs_mn, h_s, H_s, N, H_s, 64, BK))
+    return FLCE_ERR_CUDA;
+  if (dW_s && !make_map_t(&dW_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW_s, H_s, V, H_s, 32, 32))
+    return FLCE_ERR_CUDA;
+  const long long H = H_s;
+  const bool kLong = static_cast<long long>(N) * V >= INT_MAX || b.R * b.ldD >= INT_MAX ||
+                     static_cast<long long>(N) * H >= INT_MAX ||
+                     static_cast<long long>(V) * H >= INT_MAX ||
+                     static_cast<long long>(b.dh_splits) * b.R * H >= INT_MAX;
+  const int kbs = static_cast<int>(ceil_div(H_s, BK));
+  const int kbt = static_cast<int>(ceil_div(H_t, BK));
+
+  GemmParams base{};
+  base.N = static_cast<int>(N);
+  base.H = static_cast<int>(H_s);
+  base.V = static_cast<int>(V);
+  base.ldD = static_cast<int>(b.ldD);
+  base.targets = targets;
+  base.weights = weights;
+  base.lse = lse_s;
+  base.lse_t = lse_t;
+  base.grad_scale = grad_scale;
+  base.ignore_index = ignore_index;
+  base.D = Dbuf;
+  base.dH = dH_s;
+  base.dH_part = dh_part;
+  base.dW = dW_s;
+  base.err = err;
+  base.rows_cap = static_cast<int>(b.R);
+  base.k_blocks_s = kbs;
+  base.tf_softcap = tfp.tf_softcap;
+  base.tf_a = tfp.tf_a;
+  base.tf_b = tfp.tf_b;
+  base.tf_d = tfp.tf_d;
+
+  int chunk = 0;
+  for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
+    const int rows = static_cast<int>(std::min(b.R, N - row0));
+    GemmParams p = base;
+    p.row0 = static_cast<int>(row0);
+    p.rows = rows;
+    {  // (1) student and teacher logits, distillation dlogits -> D
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
+      q.n_tiles = static_cast<int>(ceil_div(V, BN));
+      q.k_blocks = kbs + kbt;
+      q.cols = q.n_tiles;
+      q.n_per_unit = 1;
+      q.kb_per_split = kbs + kbt;
+      q.k_splits = 1;
+      q.num_units = q.m_tiles * q.n_tiles;
+      q.group_m = std::min(16, q.m_tiles);
+      ProfScope prof(K_KD_DLOGITS, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
+                                                 std::min(q.num_units, workers), st, &ht_k, &Wt_k));
+    }
+    CUtensorMap D_k, D_mn;
+    if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) ||
+        !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
+      return FLCE_ERR_CUDA;
+    if (dH_s) {  // (2) dH_s[rows] = D W_s
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
+      q.n_tiles = static_cast<int>(ceil_div(H, BN));
+      q.k_blocks = static_cast<int>(ceil_div(V, BK));
+      q.cols = q.n_tiles;
+      q.n_per_unit = 1;
+      q.kb_per_split = b.dh_kb_per_split;
+      const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
+      q.k_splits = splits;
+      q.num_units = splits * q.m_tiles * q.n_tiles;
+      q.group_m = q.m_tiles;
+      q.dH_part = splits > 1 ? dh_part : nullptr;
+      {
+        ProfScope prof(K_DH, st);
+        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(cg, kLong, D_k, Ws_mn, Ws_mn, q, std::min(q.num_units, workers), st));
+      }
+      if (splits > 1) {
+        ProfScope prof(K_DH_REDUCE, st);
+        const long long total = static_cast<long long>(rows) * (H / 4);
+        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
+        if (kLong)
+          dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
+                                                                 static_cast<int>(H), p.row0, dH_s, nullptr,
+                                                                 nullptr, 0);
+        else
+          dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
+                                                                  static_cast<int>(H), p.row0, dH_s, nullptr,
+                                                                  nullptr, 0);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
+    }
+    if (dW_s) {  // (3) dW_s (+)= D^T h_s[rows]
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(V, tm));
+      q.n_tiles = static_cast<int>(ceil_div(H, BN));
+      q.k_blocks = static_cast<int>(ceil_div(rows, BK));
+      q.cols = q.n_tiles;
+      q.n_per_unit = 1;
+      q.kb_per_split = q.k_blocks;
+      q.k_splits = 1;
+      q.num_units = q.m_tiles * q.n_tiles;
+      q.group_m = std::min(8, q.m_tiles);
+      q.dW_accumulate = chunk > 0 ? 1 : 0;
+      ProfScope prof(K_DW, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(cg, kLong, D_mn, hs_mn, dW_map, q, std::min(q.num_units, workers), st));
+    }
+  }
+  return FLCE_OK;
 }
 
 flce_status flce_device_status(void* stream) {

@@ -65,7 +65,21 @@ constexpr long long DRAIN_LIMIT_CYCLES = 400000000LL;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum Mode : int { MODE_FWD = 0, MODE_DLOGITS = 1, MODE_DH = 2, MODE_DW = 3 };
+enum Mode : int {
+  MODE_FWD = 0,
+  MODE_DLOGITS = 1,
+  MODE_DH = 2,
+  MODE_DW = 3,
+  // distillation (student and teacher heads in one tile pipeline): K runs
+  // over the student's hidden blocks into TMEM columns [0, BN), then over the
+  // teacher's into [BN, 2 BN)
+  MODE_KD_FWD = 4,
+  MODE_KD_DLOGITS = 5
+};
+template <int MODE>
+__host__ __device__ constexpr bool is_kd() {
+  return MODE == MODE_KD_FWD || MODE == MODE_KD_DLOGITS;
+}
 
 // bit 0 of the device error word: a bounded wait ran out.
 constexpr int DEVERR_TIMEOUT = 1;
@@ -106,6 +120,12 @@ struct GemmParams {
   const int* dyn_count;
   int chunk_first;
   int k_splits;
+  // distillation: student K blocks (the rest of k_blocks are the teacher's),
+  // teacher log-sum-exp and the extra forward partials
+  int k_blocks_s;
+  const float* lse_t;
+  float2* partials_t;  // [splits][N] (teacher max*log2e, sum exp2)
+  float* partials_c;   // [splits][N] sum exp2(u_t - m_t) * (z_t - z_s)
 };
 
 // Problem extents that depend on the device-side row count of a compacted pass.
@@ -162,7 +182,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape&
   t.n1 = min(p.n_tiles, t.n0 + p.n_per_unit);
   t.kb0 = ks * d.kb_per_split;
   t.kb1 = min(d.k_blocks, t.kb0 + d.kb_per_split);
-  t.split = (MODE == MODE_FWD) ? c : ks;
+  t.split = (MODE == MODE_FWD || MODE == MODE_KD_FWD) ? c : ks;
   return t;
 }
 
@@ -208,12 +228,19 @@ __device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap* map, uin
 // `bar` is the full barrier of the MMA-issuing CTA (cluster address for CG 2).
 template <int MODE, int CG>
 __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensorMap* tB,
+                                           const CUtensorMap* tA2, const CUtensorMap* tB2,
                                            uint32_t sA, uint32_t sB, uint32_t bar,
                                            const GemmParams& p, int m, int n, int kb, int rank) {
   using C = TileCfg<CG>;
   const int a0 = m * C::TM + rank * BM;         // first A row (M) of this CTA
   const int b0 = n * BN + rank * C::B_ROWS;     // first B row (N) of this CTA
-  if constexpr (MODE == MODE_FWD || MODE == MODE_DLOGITS) {
+  if constexpr (is_kd<MODE>()) {
+    // student (h_s, W_s) blocks first, then the teacher's (h_t, W_t)
+    const bool teacher = kb >= p.k_blocks_s;
+    const int kk = teacher ? kb - p.k_blocks_s : kb;
+    tma_ld<MODE, CG>(sA, teacher ? tA2 : tA, bar, kk * BK, p.row0 + a0);
+    tma_ld<MODE, CG>(sB, teacher ? tB2 : tB, bar, kk * BK, b0);
+  } else if constexpr (MODE == MODE_FWD || MODE == MODE_DLOGITS) {
     // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x B_ROWS)
     tma_ld<MODE, CG>(sA, tA, bar, kb * BK, p.row0 + a0);
     tma_ld<MODE, CG>(sB, tB, bar, kb * BK, b0);
@@ -287,10 +314,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int MODE, bool kLong, int CG>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
+                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ GemmParams p) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   using C = TileCfg<CG>;
   constexpr int NST = C::NSTAGE;
+  // accumulator buffers in TMEM: two (double-buffered) tiles, or one tile of
+  // two accumulators (student, teacher) in the distillation modes
+  constexpr int NACC = is_kd<MODE>() ? 1 : 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -349,6 +380,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      if constexpr (is_kd<MODE>()) {
+        tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmB2);
+      }
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
@@ -364,7 +399,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t fb = full_bar(stage);
             if constexpr (CG == 2) fb = mapa_shared(fb, 0);
             if (issuer) mbar_arrive_expect_tx(full_bar(stage), C::STAGE * CG);
-            load_stage<MODE, CG>(&tmA, &tmB, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank);
+            load_stage<MODE, CG>(&tmA, &tmB, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank);
             ++issued;
             if (++stage == NST) {
               stage = 0;
@@ -401,7 +436,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t sA = sbase + stage * C::STAGE;
-            mma_stage<MODE, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
+            if constexpr (is_kd<MODE>()) {
+              const bool teacher = kb >= p.k_blocks_s;
+              mma_stage<MODE, CG>(d_tmem + (teacher ? BN : 0), sA, sA + C::A_BYTES,
+                                  kb == t.kb0 || kb == p.k_blocks_s);
+            } else {
+              mma_stage<MODE, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
+            }
             mma_commit_all<CG>(empty_bar(stage));
             if (++stage == NST) {
               stage = 0;
@@ -410,8 +451,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           if (!ok) break;
           mma_commit_all<CG>(tfull_bar(acc));
-          acc ^= 1u;
-          if (acc == 0) acc_phase ^= 1u;
+          if (++acc == NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
         }
       }
       // every MMA issued by this thread has finished before TMEM is freed
@@ -438,7 +481,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool row_ok;
       long long tgt = -1;
       float run_m = -INFINITY, run_s = 0.f;  // FWD: log2-domain max and sum
-      float scale = 0.f, nl2 = 0.f;          // DLOGITS
+      float run_mt = -INFINITY, run_st = 0.f, run_c = 0.f;  // KD_FWD teacher state
+      float scale = 0.f, nl2 = 0.f, nlt = 0.f;              // DLOGITS / KD_DLOGITS
       // linear transform folded into the exp2 prescale, the gathered target
       // logit and the dlogits scale (soft-capped logits are formed explicitly)
       const float lin_a = p.tf_softcap ? 1.f : p.tf_a;
@@ -466,6 +510,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const float w = p.weights ? p.weights[grow] : 1.f;
           scale = valid ? w * p.grad_scale : 0.f;
           nl2 = -p.lse[grow] * kLog2e;
+        }
+      }
+      if constexpr (MODE == MODE_KD_DLOGITS) {
+        if (row_ok) {
+          const bool valid = p.targets == nullptr || p.targets[grow] != p.ignore_index;
+          const float w = p.weights ? p.weights[grow] : 1.f;
+          scale = valid ? w * p.grad_scale : 0.f;
+          nl2 = -p.lse[grow] * kLog2e;
+          nlt = -p.lse_t[grow] * kLog2e;
         }
       }
       const float scale_a = scale * lin_a;
@@ -558,6 +611,89 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   *reinterpret_cast<uint4*>(dst + 8 * g) =
                       make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
             }
+          } else if constexpr (MODE == MODE_KD_FWD) {
+            float vt[32];
+            tmem_ld32(tbase + BN + c * 32, vt);
+            if (p.tf_softcap) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                v[j] = p.tf_b * tanhf(p.tf_a * v[j]);
+                vt[j] = p.tf_b * tanhf(p.tf_a * vt[j]);
+              }
+            }
+            const bool partial = col0 + 32 > p.V;
+            if (partial) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= p.V) {
+                  v[j] = -INFINITY;
+                  vt[j] = -INFINITY;
+                }
+            }
+            // student: online log-sum-exp (log2 domain)
+            float cm = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
+            const float nm = fmaxf(run_m, cm * l2a);
+            if (nm != -INFINITY) {
+              float a = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) a += ex2_approx(fmaf(v[j], l2a, -nm));
+              run_s = run_s * ex2_approx(run_m - nm) + a;
+              run_m = nm;
+            }
+            // teacher: online log-sum-exp and sum of 2^(u_t - m_t) (z_t - z_s)
+            float ct = vt[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) ct = fmaxf(ct, vt[j]);
+            const float nt = fmaxf(run_mt, ct * l2a);
+            if (nt != -INFINITY) {
+              float a = 0.f, cc = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float e = ex2_approx(fmaf(vt[j], l2a, -nt));
+                a += e;
+                if (!partial || col0 + j < p.V) cc += e * (vt[j] - v[j]);
+              }
+              const float rs = ex2_approx(run_mt - nt);
+              run_st = run_st * rs + a;
+              run_c = run_c * rs + cc * lin_a;
+              run_mt = nt;
+            }
+          } else if constexpr (MODE == MODE_KD_DLOGITS) {
+            float vt[32];
+            tmem_ld32(tbase + BN + c * 32, vt);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float d[2] = {0.f, 0.f};
+              if (scale != 0.f) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  float de;
+                  if (!p.tf_softcap) {
+                    const float ps = ex2_approx(fmaf(v[j + e], l2a, nl2));
+                    const float pt = ex2_approx(fmaf(vt[j + e], l2a, nlt));
+                    de = (ps - pt) * scale_a;
+                  } else {
+                    const float ts = tanhf(p.tf_a * v[j + e]);
+                    const float ps = ex2_approx(fmaf(p.tf_b * ts, kLog2e, nl2));
+                    const float pt = ex2_approx(fmaf(p.tf_b * tanhf(p.tf_a * vt[j + e]), kLog2e, nlt));
+                    de = (ps - pt) * scale * p.tf_d * (1.f - ts * ts);
+                  }
+                  d[e] = (col0 + j + e < p.V) ? de : 0.f;
+                }
+              }
+              pk[j / 2] = pack_bf16x2(d[0], d[1]);
+            }
+            if (row_store) {
+              uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (col0 + 8 * g < p.ldD)
+                  *reinterpret_cast<uint4*>(dst + 8 * g) =
+                      make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
           } else if constexpr (MODE == MODE_DH) {
             if (row_ok) {
               if (p.dH_part == nullptr) {
@@ -612,12 +748,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           else
             mbar_arrive_cluster(acc ? tempty_target1 : tempty_target0);
         }
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == NACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       if constexpr (MODE == MODE_FWD) {
         if (ok && row_ok)
           p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(run_m, run_s);
+      }
+      if constexpr (MODE == MODE_KD_FWD) {
+        if (ok && row_ok) {
+          const idx_t o = static_cast<idx_t>(t.split) * p.N + grow;
+          p.partials[o] = make_float2(run_m, run_s);
+          p.partials_t[o] = make_float2(run_mt, run_st);
+          p.partials_c[o] = run_c;
+        }
       }
     }
   }

@@ -170,6 +170,53 @@ FLCE_API flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Distillation: a student head (h_s [N,H_s], W_s [V,H_s]) learns a frozen
+ * teacher head's (h_t [N,H_t], W_t [V,H_t]) token distribution.  Source: TRL
+ * v1.13 article, speed & memory section: the distillation trainer computes
+ * every chunk twice, once with the student's head and once with the
+ * teacher's.  Reading taken (the page names no formula): per row
+ *   kl[i] = m[i] * KL(p_t || p_s) = m[i] * sum_v p_t (log p_t - log p_s),
+ *   loss  = sum_i m[i] w[i] kl[i] / sum_i m[i],
+ * with p = softmax of the transformed logits of each head (the same
+ * transform for both, e.g. a temperature) and m[i] = (targets[i] !=
+ * ignore_index), or 1 for every row when targets == NULL (targets are
+ * otherwise unused).  Both heads run in one tile pipeline (student and
+ * teacher logits of a tile sit side by side in tensor memory); the forward
+ * never stores either head's logits.  Outputs (each may be NULL, not all):
+ * out_kl [N], out_lse_s [N], out_lse_t [N] fp32, out_loss, out_n_valid.
+ * Other arguments and conventions as in flce_forward; the workspace size is
+ * flce_kd_workspace_bytes.
+ */
+FLCE_API flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                     const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                     const int64_t* targets, const float* weights, int64_t N,
+                                     int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                     const flce_logit_transform* transform, float* out_kl,
+                                     float* out_lse_s, float* out_lse_t, float* out_loss,
+                                     int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * Student gradients of the distillation loss (the teacher is frozen):
+ *   D[i,v] = (p_s[i,v] - p_t[i,v]) * m[i] * w[i] * grad_scale * dy/dz_s,
+ *   dH_s = D W_s ([N,H_s] bf16, or NULL),  dW_s = D^T h_s ([V,H_s] fp32, or NULL),
+ * recomputing both heads' logits chunk by chunk (chunk_rows as in
+ * flce_backward).  lse_s / lse_t come from flce_kd_forward.
+ */
+FLCE_API flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                      const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                      const int64_t* targets, const float* weights,
+                                      const float* lse_s, const float* lse_t, float grad_scale,
+                                      flce_bf16* dH_s, float* dW_s, int64_t N, int64_t V,
+                                      int64_t chunk_rows, int64_t ignore_index,
+                                      const flce_logit_transform* transform, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of flce_kd_forward and flce_kd_backward for these sizes. */
+FLCE_API size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V,
+                                        int64_t chunk_rows);
+
+/*
  * Forward that allocates nothing (no counterpart on the source pages: the
  * method itself does not need it).
  *

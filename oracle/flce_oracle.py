@@ -319,6 +319,80 @@ def vocab_rows_dW(h, W, targets, lse, vocab_rows, weights=None, g: float = 1.0,
     return out
 
 
+@dataclasses.dataclass
+class KDForward:
+    kl: np.ndarray  # [N] fp64, 0 on ignored rows
+    lse_s: np.ndarray  # [N] student log-sum-exp
+    lse_t: np.ndarray  # [N] teacher log-sum-exp
+    n_valid: int
+    loss: float
+
+
+def _kd_mask(targets, N: int, ignore_index: int) -> np.ndarray:
+    if targets is None:
+        return np.ones(N, dtype=bool)
+    return np.asarray(targets, dtype=np.int64) != ignore_index
+
+
+def kd_forward(hs, Ws, ht, Wt, targets=None, weights=None, ignore_index: int = IGNORE_INDEX,
+               tf: LogitTransform | None = None, chunk_rows: int | None = None) -> KDForward:
+    """Distillation of a teacher head into a student head, chunk by chunk.
+
+    TRL v1.13 article, speed & memory section: the distillation trainer
+    computes every chunk twice, once with the student's head and once with
+    the teacher's.  Reading taken (the page names no formula): the per-token
+    loss is KL(p_teacher || p_student) over the vocabulary, masked by
+    ignore_index rows of ``targets`` (all rows count when None) and weighted
+    like the cross-entropy; loss = sum(m w kl) / sum(m).  Both heads' logits
+    pass through the same transform (e.g. a distillation temperature).
+    """
+    hsf, Wsf, htf, Wtf = widen(hs), widen(Ws), widen(ht), widen(Wt)
+    N = hsf.shape[0]
+    m = _kd_mask(targets, N, ignore_index)
+    w = _weights(weights, N)
+    step = N if chunk_rows is None else max(1, int(chunk_rows))
+    kl = np.zeros(N)
+    lse_s = np.zeros(N)
+    lse_t = np.zeros(N)
+    for r0 in range(0, N, step):
+        r1 = min(N, r0 + step)
+        zs = _tf(hsf[r0:r1] @ Wsf.T, tf)
+        zt = _tf(htf[r0:r1] @ Wtf.T, tf)
+        ls, lt = logsumexp_rows(zs), logsumexp_rows(zt)
+        log_ps, log_pt = zs - ls[:, None], zt - lt[:, None]
+        kl[r0:r1] = np.where(m[r0:r1], np.sum(np.exp(log_pt) * (log_pt - log_ps), axis=1), 0.0)
+        lse_s[r0:r1], lse_t[r0:r1] = ls, lt
+    n_valid = int(m.sum())
+    loss = float(np.sum(m * w * kl)) / n_valid if n_valid > 0 else 0.0
+    return KDForward(kl, lse_s, lse_t, n_valid, loss)
+
+
+def kd_backward(hs, Ws, ht, Wt, targets=None, weights=None, g: float = 1.0,
+                ignore_index: int = IGNORE_INDEX, tf: LogitTransform | None = None,
+                chunk_rows: int | None = None) -> Backward:
+    """Student gradients of the distillation loss (teacher frozen):
+    D = (p_student - p_teacher) * m * w * g * f'(z_student); dH = D Ws, dW = D^T hs."""
+    hsf, Wsf, htf, Wtf = widen(hs), widen(Ws), widen(ht), widen(Wt)
+    N = hsf.shape[0]
+    m = _kd_mask(targets, N, ignore_index)
+    w = _weights(weights, N)
+    step = N if chunk_rows is None else max(1, int(chunk_rows))
+    dH = np.zeros_like(hsf)
+    dW = np.zeros_like(Wsf)
+    for r0 in range(0, N, step):
+        r1 = min(N, r0 + step)
+        z = hsf[r0:r1] @ Wsf.T
+        zs = _tf(z, tf)
+        zt = _tf(htf[r0:r1] @ Wtf.T, tf)
+        D = probs(zs, logsumexp_rows(zs)) - probs(zt, logsumexp_rows(zt))
+        D *= (m[r0:r1] * w[r0:r1] * g)[:, None]
+        if tf is not None:
+            D *= tf.grad(z)
+        dH[r0:r1] = D @ Wsf
+        dW += D.T @ hsf[r0:r1]
+    return Backward(dH, dW)
+
+
 def logit_memory_gb(context_length: int, vocab_dim: int, batch_size: int = 1,
                     multiplier: int = 1) -> float:
     """Unsloth GRPO page, flattened-chunking section, Equations 1-3.

@@ -393,3 +393,73 @@ def test_transform_matches_torch_autograd():
     assert np.allclose(logp, f.logp[[1, 5]], atol=1e-13)
     _, lp2, dH2, _ = O.rows_all(h, W, t, [1, 5], w, g=1.0 / nv, tf=tf)
     assert np.allclose(dH2, b.dH[[1, 5]], atol=1e-13)
+
+
+# ------------------------------------------------------------------ distillation
+
+def _kd_rand(N, Hs, Ht, V, seed):
+    r = np.random.default_rng(seed)
+    return (r.standard_normal((N, Hs)), r.standard_normal((V, Hs)) * 0.4,
+            r.standard_normal((N, Ht)), r.standard_normal((V, Ht)) * 0.4)
+
+
+def test_kd_is_zero_for_identical_heads_and_nonnegative():
+    hs, Ws, _, _ = _kd_rand(12, 6, 6, 17, 40)
+    f = O.kd_forward(hs, Ws, hs, Ws)
+    assert np.allclose(f.kl, 0.0, atol=1e-13) and f.loss == pytest.approx(0.0, abs=1e-13)
+    b = O.kd_backward(hs, Ws, hs, Ws, g=1.0)
+    assert np.allclose(b.dH, 0, atol=1e-13) and np.allclose(b.dW, 0, atol=1e-13)
+    hs, Ws, ht, Wt = _kd_rand(20, 6, 9, 17, 41)
+    f = O.kd_forward(hs, Ws, ht, Wt)
+    assert np.all(f.kl > 0)
+
+
+def test_kd_matches_torch_kl_div_and_autograd():
+    hs, Ws, ht, Wt = _kd_rand(25, 7, 5, 31, 42)
+    t = np.random.default_rng(1).integers(0, 31, 25)
+    t[[3, 8]] = O.IGNORE_INDEX
+    w = np.random.default_rng(2).uniform(0.5, 2, 25)
+    tf = O.LogitTransform(temperature=2.0)
+    hst = torch.tensor(hs, requires_grad=True)
+    Wst = torch.tensor(Ws, requires_grad=True)
+    zs = (hst @ Wst.T) / 2.0
+    zt = torch.tensor(ht @ Wt.T) / 2.0
+    kl = torch.nn.functional.kl_div(torch.log_softmax(zs, -1), torch.log_softmax(zt, -1),
+                                    log_target=True, reduction="none").sum(-1)
+    m = torch.tensor(t != O.IGNORE_INDEX, dtype=torch.float64)
+    loss = (m * torch.tensor(w) * kl).sum() / m.sum()
+    loss.backward()
+    f = O.kd_forward(hs, Ws, ht, Wt, t, w, tf=tf)
+    b = O.kd_backward(hs, Ws, ht, Wt, t, w, g=1.0 / f.n_valid, tf=tf)
+    assert f.n_valid == 23
+    assert np.allclose(f.kl, (m * kl).detach().numpy(), atol=1e-12)
+    assert f.loss == pytest.approx(float(loss.detach()), rel=1e-12)
+    assert np.allclose(b.dH, hst.grad.numpy(), atol=1e-12) and np.allclose(b.dW, Wst.grad.numpy(), atol=1e-12)
+    # chunking does not change anything
+    fc = O.kd_forward(hs, Ws, ht, Wt, t, w, tf=tf, chunk_rows=4)
+    bc = O.kd_backward(hs, Ws, ht, Wt, t, w, g=1.0 / f.n_valid, tf=tf, chunk_rows=4)
+    assert np.allclose(fc.kl, f.kl, atol=1e-13) and np.allclose(bc.dW, b.dW, atol=1e-13)
+
+
+def test_kd_gradients_by_finite_differences():
+    hs, Ws, ht, Wt = _kd_rand(3, 4, 5, 6, 43)
+    tf = O.LogitTransform(softcap=3.0, temperature=1.5)
+    f = O.kd_forward(hs, Ws, ht, Wt, tf=tf)
+    b = O.kd_backward(hs, Ws, ht, Wt, g=1.0 / f.n_valid, tf=tf)
+    eps = 1e-6
+    num = np.zeros_like(Ws)
+    for v in range(Ws.shape[0]):
+        for k in range(Ws.shape[1]):
+            e = np.zeros_like(Ws)
+            e[v, k] = eps
+            num[v, k] = (O.kd_forward(hs, Ws + e, ht, Wt, tf=tf).loss -
+                         O.kd_forward(hs, Ws - e, ht, Wt, tf=tf).loss) / (2 * eps)
+    assert np.linalg.norm(num - b.dW) <= 1e-7 * np.linalg.norm(b.dW)
+    numh = np.zeros_like(hs)
+    for i in range(hs.shape[0]):
+        for k in range(hs.shape[1]):
+            e = np.zeros_like(hs)
+            e[i, k] = eps
+            numh[i, k] = (O.kd_forward(hs + e, Ws, ht, Wt, tf=tf).loss -
+                          O.kd_forward(hs - e, Ws, ht, Wt, tf=tf).loss) / (2 * eps)
+    assert np.linalg.norm(numh - b.dH) <= 1e-7 * np.linalg.norm(b.dH)
