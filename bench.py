@@ -12,6 +12,7 @@ workload (the only reference this method has).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -183,7 +184,7 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW")
+GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "kd_fwd_logits", "kd_bwd_dlogits")
 
 
 def gpu_arm(args):
@@ -228,19 +229,46 @@ def gpu_arm(args):
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
 
+    tf = None
+    if args.transform:
+        tf = _lib.make_transform({k: float(v) for k, v in
+                                  (kv.split("=") for kv in args.transform.split(","))})
+    tf_ptr = None if tf is None else ctypes.addressof(tf)
+    Ht = args.kd_teacher_hidden
+    if Ht:
+        import dataclasses
+        twl = dataclasses.replace(wl, name=wl.name + "_teacher", H=Ht, w_std=wl.w_std * 1.2,
+                                  seed=wl.seed + 777)
+        tinp = WL.make_inputs(twl)
+        ht = up(tinp.h)
+        Wt = up(tinp.W)
+        lse_t = torch.empty(N, dtype=torch.float32, device=dev)
+        ws_bytes = max(ws_bytes, _lib.flce_kd_workspace_bytes(N, H, Ht, V, chunk_rows))
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def check(name, s):
+        if s != 0:
+            raise RuntimeError(f"{name}: {_lib.STATUS_NAMES.get(s, s)}")
+
     def step():
-        s = lib.flce_forward(h.data_ptr(), W.data_ptr(), t.data_ptr(),
-                             None if w is None else w.data_ptr(), N, H, V, chunk_rows, -100,
-                             logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(),
-                             workspace.data_ptr(), ws_bytes, sh)
-        if s != 0:
-            raise RuntimeError(f"flce_forward: {_lib.STATUS_NAMES.get(s, s)}")
-        s = lib.flce_backward(h.data_ptr(), W.data_ptr(), t.data_ptr(),
-                              None if w is None else w.data_ptr(), lse.data_ptr(), g,
-                              dH.data_ptr(), dW.data_ptr(), N, H, V, chunk_rows, -100,
-                              workspace.data_ptr(), ws_bytes, sh)
-        if s != 0:
-            raise RuntimeError(f"flce_backward: {_lib.STATUS_NAMES.get(s, s)}")
+        wp = None if w is None else w.data_ptr()
+        if Ht:
+            check("flce_kd_forward", lib.flce_kd_forward(
+                h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp, N,
+                V, chunk_rows, -100, tf_ptr, logp.data_ptr(), lse.data_ptr(), lse_t.data_ptr(),
+                loss.data_ptr(), nv.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
+            check("flce_kd_backward", lib.flce_kd_backward(
+                h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp,
+                lse.data_ptr(), lse_t.data_ptr(), g, dH.data_ptr(), dW.data_ptr(), N, V, chunk_rows,
+                -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
+            return
+        check("flce_forward_ex", lib.flce_forward_ex(
+            h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr,
+            logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(), workspace.data_ptr(),
+            ws_bytes, sh))
+        check("flce_backward_ex", lib.flce_backward_ex(
+            h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, lse.data_ptr(), g, dH.data_ptr(),
+            dW.data_ptr(), N, H, V, chunk_rows, -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
 
     def barrier():
         if ws > 1:
@@ -308,18 +336,22 @@ def gpu_arm(args):
         logp_host.copy_(out["logp"], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
+    if Ht or tf is not None:
+        e2e_steps = 0
+    e2e_ms = None
+    if e2e_steps:
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            e2 = torch.cuda.Event(enable_timing=True)
+            e3 = torch.cuda.Event(enable_timing=True)
+            e2.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            e3.record(stream)
         torch.cuda.synchronize(dev)
-        e2 = torch.cuda.Event(enable_timing=True)
-        e3 = torch.cuda.Event(enable_timing=True)
-        e2.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e3.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e2.elapsed_time(e3), device=dev) / e2e_steps
+        e2e_ms = reduce_max(e2.elapsed_time(e3), device=dev) / e2e_steps
     h2d = N * H * 2 + N * 8 + (0 if w_host is None else N * 4)
     d2h = 4 + N * 4
 
@@ -330,6 +362,9 @@ def gpu_arm(args):
     nv = n_valid_host
     flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dlogits": 2.0 * nv * V * H,
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
+    if Ht:  # distillation: both heads in the forward and the dlogits recompute
+        flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "kd_bwd_dlogits": 2.0 * N * V * (H + Ht),
+                      "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
     kern = {}
     for k, (tot_ms, n) in prof.items():
         if n:
@@ -345,7 +380,8 @@ def gpu_arm(args):
     launches_dom = kern[dom]["launches_per_step"]
     achieved = kern[dom]["tflops"]
     traffic = NCU_TRAFFIC_BYTES_PER_LAUNCH.get(dom) if (wl.name == NCU_TRAFFIC_WORKLOAD
-                                                         and chunk_rows == 4096) else None
+                                                         and chunk_rows == 4096 and not Ht
+                                                         and tf is None) else None
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
@@ -356,7 +392,7 @@ def gpu_arm(args):
 
     if rank == 0:
         cpu = None
-        if not args.no_cpu_baseline and ws == 1 and not args.shape:
+        if not args.no_cpu_baseline and ws == 1 and not args.shape and not Ht and tf is None:
             cpu = cpu_oracle_rate(inp, target_s=args.cpu_s)
             cpu.pop("seconds", None)
             cpu.pop("rows", None)
@@ -364,7 +400,9 @@ def gpu_arm(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "N": N, "H": H, "V": V, "chunk_rows": chunk_rows,
+            "config": {"workload": wl.name + (f"+kd_teacher_H{Ht}" if Ht else "")
+                       + (f"+transform({args.transform})" if args.transform else ""),
+                       "N": N, "H": H, "V": V, "chunk_rows": chunk_rows,
                        "targets": wl.targets, "l2": "inputs larger than L2 (W alone "
                        f"{V * H * 2 / 1e9:.2f} GB > 129 MB); no flush",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
@@ -376,8 +414,9 @@ def gpu_arm(args):
             "kernels": kern,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "e2e": {"value": whole_job_rate(N, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "e2e": None if e2e_ms is None else {
+                "value": whole_job_rate(N, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": gpu_launches,
             "peak_extra_mem_bytes": int(extra_mem),
             "workspace_bytes": ws_bytes,
@@ -399,6 +438,11 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of the CPU-oracle sample")
     ap.add_argument("--ref-step-s", type=float, default=8.0, help="reference arm: seconds per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--transform", default="",
+                    help="logit transform, e.g. softcap=30,temperature=0.7 (flce_*_ex path)")
+    ap.add_argument("--kd-teacher-hidden", type=int, default=0,
+                    help="time the distillation step instead: the workload's head is the student, "
+                         "a teacher head of this hidden size is added")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

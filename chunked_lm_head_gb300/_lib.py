@@ -215,6 +215,10 @@ def flce_workspace_bytes(N, H, V, chunk_rows) -> int:
     return int(load().flce_workspace_bytes(N, H, V, chunk_rows))
 
 
+def flce_kd_workspace_bytes(N, H_s, H_t, V, chunk_rows) -> int:
+    return int(load().flce_kd_workspace_bytes(N, H_s, H_t, V, chunk_rows))
+
+
 def flce_status_string(status: int) -> str:
     return load().flce_status_string(status).decode()
 
