@@ -250,8 +250,32 @@ def gpu_arm(args):
         if s != 0:
             raise RuntimeError(f"{name}: {_lib.STATUS_NAMES.get(s, s)}")
 
+    if args.e4m3:
+        if not args.forward_only or Ht:
+            raise SystemExit("--e4m3 needs --forward-only (the backward is bf16)")
+        h8 = torch.empty((N, H), dtype=torch.uint8, device=dev)
+        hsc = torch.empty(N, dtype=torch.float32, device=dev)
+        W8 = torch.empty((V, H), dtype=torch.uint8, device=dev)
+        Wsc = torch.empty(V, dtype=torch.float32, device=dev)
+        check("flce_quantize_e4m3_rows", lib.flce_quantize_e4m3_rows(
+            W.data_ptr(), V, H, W8.data_ptr(), Wsc.data_ptr(), sh))  # frozen head: once
+
     def step():
         wp = None if w is None else w.data_ptr()
+        if args.forward_only:
+            if args.e4m3:
+                check("flce_quantize_e4m3_rows", lib.flce_quantize_e4m3_rows(
+                    h.data_ptr(), N, H, h8.data_ptr(), hsc.data_ptr(), sh))
+                check("flce_forward_e4m3", lib.flce_forward_e4m3(
+                    h8.data_ptr(), hsc.data_ptr(), W8.data_ptr(), Wsc.data_ptr(), t.data_ptr(), wp, N,
+                    H, V, chunk_rows, -100, tf_ptr, logp.data_ptr(), lse.data_ptr(), loss.data_ptr(),
+                    nv.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
+            else:
+                check("flce_forward_ex", lib.flce_forward_ex(
+                    h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr,
+                    logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(),
+                    workspace.data_ptr(), ws_bytes, sh))
+            return
         if Ht:
             check("flce_kd_forward", lib.flce_kd_forward(
                 h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp, N,
@@ -336,7 +360,7 @@ def gpu_arm(args):
         logp_host.copy_(out["logp"], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 10))
-    if Ht or tf is not None:
+    if Ht or tf is not None or args.forward_only:
         e2e_steps = 0
     e2e_ms = None
     if e2e_steps:
@@ -362,6 +386,8 @@ def gpu_arm(args):
     nv = n_valid_host
     flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dlogits": 2.0 * nv * V * H,
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
+    if args.forward_only:
+        flops_step = {"fwd_logits_lse": 2.0 * N * V * H}
     if Ht:  # distillation: both heads in the forward and the dlogits recompute
         flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "kd_bwd_dlogits": 2.0 * N * V * (H + Ht),
                       "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
@@ -377,14 +403,19 @@ def gpu_arm(args):
             kern[k]["tflops"] = flops_step[k] / (kern[k]["ms_per_step"] / 1e3) / 1e12
     dom = max((k for k in kern if k in GEMM_KINDS), key=lambda k: kern[k]["ms_per_step"])
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    peak_note = "measured bf16_tflops_sustained (kernel timed inside a long step)"
+    if args.e4m3:  # e4m3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+        peak_tf = 2.0 * peak_tf
+        peak_note = "2 x measured bf16_tflops_sustained (e4m3 / bf16 nominal ratio)"
     launches_dom = kern[dom]["launches_per_step"]
     achieved = kern[dom]["tflops"]
     traffic = NCU_TRAFFIC_BYTES_PER_LAUNCH.get(dom) if (wl.name == NCU_TRAFFIC_WORKLOAD
                                                          and chunk_rows == 4096 and not Ht
-                                                         and tf is None) else None
+                                                         and tf is None and not args.forward_only
+                                                         ) else None
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
-                "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
+                "peak_source": f"{peaks['source']}: {peak_note}",
                 "flops_per_launch": flops_step[dom] / launches_dom,
                 "launch_ms": kern[dom]["ms_per_step"] / launches_dom}
     step_tflops = sum(flops_step.values()) / (ms_step / 1e3) / 1e12
@@ -392,16 +423,19 @@ def gpu_arm(args):
 
     if rank == 0:
         cpu = None
-        if not args.no_cpu_baseline and ws == 1 and not args.shape and not Ht and tf is None:
+        if (not args.no_cpu_baseline and ws == 1 and not args.shape and not Ht and tf is None
+                and not args.forward_only):
             cpu = cpu_oracle_rate(inp, target_s=args.cpu_s)
             cpu.pop("seconds", None)
             cpu.pop("rows", None)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if args.e4m3 else "bf16",
+            "data": "synthetic",
             "config": {"workload": wl.name + (f"+kd_teacher_H{Ht}" if Ht else "")
-                       + (f"+transform({args.transform})" if args.transform else ""),
+                       + (f"+transform({args.transform})" if args.transform else "")
+                       + ("+forward_only" if args.forward_only else "") + ("+e4m3" if args.e4m3 else ""),
                        "N": N, "H": H, "V": V, "chunk_rows": chunk_rows,
                        "targets": wl.targets, "l2": "inputs larger than L2 (W alone "
                        f"{V * H * 2 / 1e9:.2f} GB > 129 MB); no flush",
@@ -440,6 +474,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--transform", default="",
                     help="logit transform, e.g. softcap=30,temperature=0.7 (flce_*_ex path)")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time the log-prob forward alone (e.g. reference / old-policy log-probs)")
+    ap.add_argument("--e4m3", action="store_true",
+                    help="with --forward-only: e4m3 operands (h quantised every step, W once)")
     ap.add_argument("--kd-teacher-hidden", type=int, default=0,
                     help="time the distillation step instead: the workload's head is the student, "
                          "a teacher head of this hidden size is added")

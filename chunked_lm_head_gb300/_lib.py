@@ -42,6 +42,10 @@ SIGNATURES = {
                                         _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp, _c_i64, _c_i64,
                                         _c_i64, _c_i64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "flce_kd_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64]),
+    "flce_quantize_e4m3_rows": (ctypes.c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp]),
+    "flce_forward_e4m3": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64,
+                                         _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                         _c_vp, ctypes.c_size_t, _c_vp]),
     "flce_forward_static_scratch": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                                    _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
@@ -84,7 +88,7 @@ def header_symbols() -> list[str]:
     """Function names declared in include/flce.h."""
     src = open(os.path.join(_build.INCLUDE, "flce.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return re.findall(r"\b(flce_[a-z_]+)\s*\(", src)
+    return re.findall(r"\b(flce_[a-z0-9_]+)\s*\(", src)
 
 
 def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
@@ -200,6 +204,24 @@ def flce_kd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_
                                 _ptr(weights), _ptr(lse_s), _ptr(lse_t), float(grad_scale),
                                 _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows, ignore_index, tp,
                                 _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_quantize_e4m3_rows(x, rows, cols, q, scale, stream=None) -> int:
+    """Raw C call: per-row e4m3 quantisation."""
+    return load().flce_quantize_e4m3_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scale),
+                                          _stream_handle(stream))
+
+
+def flce_forward_e4m3(h8, h_scale, W8, W_scale, targets, weights, N, H, V, chunk_rows, ignore_index,
+                      transform, out_logp, out_lse, out_loss, out_n_valid, workspace=None,
+                      workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the e4m3 forward."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_forward_e4m3(_ptr(h8), _ptr(h_scale), _ptr(W8), _ptr(W_scale), _ptr(targets),
+                                 _ptr(weights), N, H, V, chunk_rows, ignore_index, tp, _ptr(out_logp),
+                                 _ptr(out_lse), _ptr(out_loss), _ptr(out_n_valid), _ptr(workspace),
+                                 workspace_bytes, _stream_handle(stream))
 
 
 def flce_forward_static_scratch(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp,

@@ -3,6 +3,7 @@
 // reduction, split-K reduction of dH).  The tensor-core work lives in
 // gemm.cuh.  See include/flce.h for the contract of every entry point.
 #include <cuda.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -309,6 +310,43 @@ __global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* _
   }
 }
 
+// Per-row e4m3 quantisation (one warp per row): scale = max|x| / 448 (1 for
+// an all-zero row), q = e4m3(x / scale), round to nearest even, saturating.
+__global__ void quantize_e4m3_rows_kernel(const uint16_t* __restrict__ x, long long rows, int cols,
+                                          uint8_t* __restrict__ q, float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  const uint16_t* xr = x + row * cols;
+  float amax = 0.f;
+  for (int c = lane * 8; c < cols; c += 256) {
+    const uint4 u = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  if (lane == 0) scale[row] = s;
+  uint8_t* qr = q + row * cols;
+  for (int c = lane * 8; c < cols; c += 256) {
+    const uint4 u = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = __nv_cvt_float_to_fp8(__fdiv_rn(__uint_as_float(w[k] << 16), s), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float_to_fp8(__fdiv_rn(__uint_as_float(w[k] & 0xffff0000u), s), __NV_SATFINITE, __NV_E4M3);
+      o[k >> 1] |= (lo | (hi << 8)) << (16 * (k & 1));
+    }
+    *reinterpret_cast<uint2*>(qr + c) = make_uint2(o[0], o[1]);
+  }
+}
+
 // Self-test of the bounded wait: one warp waits on an mbarrier that nothing
 // arrives on, through the same wait routine the GEMM pipelines use, with a
 // short limit; it must give up, raise the device error word and return.
@@ -338,12 +376,13 @@ constexpr int kDefaultSms = 152;
 
 enum Kind {
   K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COMPACT, K_GATHER,
-  K_KD_FWD, K_KD_DLOGITS, K_COUNT
+  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {"prep_targets",  "fwd_logits_lse", "fwd_combine",
                                          "fwd_loss",      "bwd_dlogits",    "bwd_dH",
                                          "bwd_dH_reduce", "bwd_dW",         "bwd_compact_rows",
-                                         "bwd_gather_rows", "kd_fwd_logits",  "kd_bwd_dlogits"};
+                                         "bwd_gather_rows", "kd_fwd_logits",  "kd_bwd_dlogits",
+                                         "quantize_e4m3"};
 
 struct ProfRec {
   int kind;
@@ -602,6 +641,35 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
                  : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, p, workers, st);
   return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, A2, B2, p, workers, st)
                : launch_gemm_t<MODE, false, 1>(a, b, c, A2, B2, p, workers, st);
+}
+
+// The e4m3 forward: MODE_FWD with 8-bit operands.
+cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int workers, cudaStream_t st) {
+  auto go = [&](auto kern, int smem, int grid_mult) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_mult * workers, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid_mult;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, b, b, a, b, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  };
+  if (cg == 2)
+    return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)
+                 : go(flce_gemm_kernel<MODE_FWD, false, 2, true>, TileCfg<2>::SMEM, 2);
+  return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 1, true>, TileCfg<1>::SMEM, 1)
+               : go(flce_gemm_kernel<MODE_FWD, false, 1, true>, TileCfg<1>::SMEM, 1);
 }
 
 // CTA group of the GEMMs: 2 (SM pairs, 256-row tiles) unless FLCE_CTA_GROUP=1.
@@ -1074,6 +1142,120 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
                           void* stream) {
   return flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
                           ignore_index, nullptr, workspace, workspace_bytes, stream);
+}
+
+flce_status flce_quantize_e4m3_rows(const flce_bf16* x, int64_t rows, int64_t cols, uint8_t* q,
+                                    float* scale, void* stream) {
+  if (rows < 0 || cols <= 0 || cols >= INT_MAX || (rows > 0 && (!x || !q || !scale)))
+    return FLCE_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4)) return FLCE_ERR_UNSUPPORTED;
+  if (rows == 0) return FLCE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long threads = rows * 32;
+  ProfScope ps(K_QUANT, st);
+  quantize_e4m3_rows_kernel<<<static_cast<unsigned>(ceil_div(threads, SMALL_THREADS)), SMALL_THREADS, 0,
+                              st>>>(x, rows, static_cast<int>(cols), q, scale);
+  FLCE_CUDA_TRY(cudaGetLastError());
+  return FLCE_OK;
+}
+
+flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, const uint8_t* W8,
+                              const float* W_scale, const int64_t* targets, const float* weights,
+                              int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                              int64_t ignore_index, const flce_logit_transform* transform,
+                              float* out_logp, float* out_lse, float* out_loss,
+                              int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  (void)chunk_rows;
+  if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  GemmParams tfp{};
+  if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
+  if (!out_logp && !out_lse && !out_loss && !out_n_valid) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!h8 || !h_scale || !W8 || !W_scale || !targets)) return FLCE_ERR_INVALID_ARG;
+  if (H % 16 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(h8, 16) || !aligned(W8, 16) || !aligned(W_scale, 16) || !aligned(h_scale, 4) ||
+      !aligned(targets, 8) || !aligned(weights, 4) || !aligned(out_logp, 4) || !aligned(out_lse, 4) ||
+      !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const FwdPlan f = plan_forward(N, H, V, workers, BM * cg);
+  const FwdLayout L = fwd_layout(N, f);
+  Workspace ws;
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  float* zt = reinterpret_cast<float*>(wb + L.zt);
+  float2* part = reinterpret_cast<float2*>(wb + L.part);
+  double* bsum = reinterpret_cast<double*>(wb + L.bsum);
+  long long* bcnt = reinterpret_cast<long long*>(wb + L.bcnt);
+  const int Ni = static_cast<int>(N);
+  if (N > 0) {
+    {
+      ProfScope ps(K_PREP, st);
+      prep_kernel<<<static_cast<int>(ceil_div(N, SMALL_THREADS)), SMALL_THREADS, 0, st>>>(
+          targets, Ni, static_cast<int>(V), ignore_index, zt, nullptr);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    CUtensorMap tA, tB;
+    if (!make_map_t(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, h8, H, N, H, 128, BM) ||
+        !make_map_t(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W8, H, V, H, 128, BN / cg))
+      return FLCE_ERR_CUDA;
+    int* err = nullptr;
+    FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+    GemmParams p{};
+    p.m_tiles = f.m_tiles;
+    p.n_tiles = f.n_tiles;
+    p.k_blocks = static_cast<int>(ceil_div(H, 128));
+    p.cols = f.S;
+    p.n_per_unit = f.tps;
+    p.kb_per_split = p.k_blocks;
+    p.k_splits = 1;
+    p.num_units = f.units;
+    p.group_m = std::min(16, f.m_tiles);
+    p.rows = Ni;
+    p.rows_cap = Ni;
+    p.N = Ni;
+    p.H = static_cast<int>(H);
+    p.V = static_cast<int>(V);
+    p.targets = targets;
+    p.weights = weights;
+    p.ignore_index = ignore_index;
+    p.partials = part;
+    p.zt = zt;
+    p.err = err;
+    p.a_scale = h_scale;
+    p.b_scale = W_scale;
+    p.tf_softcap = tfp.tf_softcap;
+    p.tf_a = tfp.tf_a;
+    p.tf_b = tfp.tf_b;
+    p.tf_d = tfp.tf_d;
+    const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
+                       static_cast<long long>(f.S) * N >= INT_MAX;
+    {
+      ProfScope ps(K_FWD, st);
+      FLCE_CUDA_TRY(launch_fwd_e4m3(cg, kLong, tA, tB, p, f.grid, st));
+    }
+    {
+      ProfScope ps(K_COMBINE, st);
+      if (kLong)
+        combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
+                                                               ignore_index, out_logp, out_lse, bsum, bcnt);
+      else
+        combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
+                                                                ignore_index, out_logp, out_lse, bsum, bcnt);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+  }
+  if (out_loss || out_n_valid) {
+    ProfScope ps(K_FINAL, st);
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
+                                              reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
 }
 
 size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, int64_t chunk_rows) {

@@ -126,6 +126,9 @@ struct GemmParams {
   const float* lse_t;
   float2* partials_t;  // [splits][N] (teacher max*log2e, sum exp2)
   float* partials_c;   // [splits][N] sum exp2(u_t - m_t) * (z_t - z_s)
+  // e4m3 forward: logits = acc * a_scale[row] * b_scale[vocabulary row]
+  const float* a_scale;
+  const float* b_scale;
 };
 
 // Problem extents that depend on the device-side row count of a compacted pass.
@@ -226,12 +229,14 @@ __device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap* map, uin
 
 // One pipeline stage of this CTA: its BM rows of A and its B_ROWS rows of B.
 // `bar` is the full barrier of the MMA-issuing CTA (cluster address for CG 2).
-template <int MODE, int CG>
+template <int MODE, int CG, bool kF8 = false>
 __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensorMap* tB,
                                            const CUtensorMap* tA2, const CUtensorMap* tB2,
                                            uint32_t sA, uint32_t sB, uint32_t bar,
                                            const GemmParams& p, int m, int n, int kb, int rank) {
   using C = TileCfg<CG>;
+  // one stage row is 128 bytes of K: 64 bf16 or 128 e4m3 elements
+  constexpr int BK = kF8 ? 128 : flce::BK;
   const int a0 = m * C::TM + rank * BM;         // first A row (M) of this CTA
   const int b0 = n * BN + rank * C::B_ROWS;     // first B row (N) of this CTA
   if constexpr (is_kd<MODE>()) {
@@ -262,11 +267,13 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
   }
 }
 
-template <int MODE, int CG>
+template <int MODE, int CG, bool kF8 = false>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sA, uint32_t sB, bool first) {
   constexpr bool A_MN = (MODE == MODE_DW);
   constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
-  constexpr uint32_t IDESC = idesc_bf16_f32(TileCfg<CG>::TM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = kF8 ? idesc_e4m3_f32(TileCfg<CG>::TM, BN)
+                                 : idesc_bf16_f32(TileCfg<CG>::TM, BN, A_MN, B_MN);
+  // each instruction consumes 32 bytes of K (16 bf16 or 32 e4m3 elements)
 #pragma unroll
   for (int k = 0; k < BK / UMMA_K; ++k) {
     // K-major: 8-row core groups 1024 B apart, K advances 32 B inside the
@@ -276,10 +283,18 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sA, uint32_t
                              : smem_desc_sw128(sA + k * 32, 16, 1024);
     const uint64_t bd = B_MN ? smem_desc_sw128(sB + k * 2048, MN_BOX_BYTES, 1024)
                              : smem_desc_sw128(sB + k * 32, 16, 1024);
-    if constexpr (CG == 1)
-      umma_bf16(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
-    else
-      umma_bf16_pair(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
+    const uint32_t acc = (first && k == 0) ? 0u : 1u;
+    if constexpr (kF8) {
+      if constexpr (CG == 1)
+        umma_e4m3(d_tmem, ad, bd, IDESC, acc);
+      else
+        umma_e4m3_pair(d_tmem, ad, bd, IDESC, acc);
+    } else {
+      if constexpr (CG == 1)
+        umma_bf16(d_tmem, ad, bd, IDESC, acc);
+      else
+        umma_bf16_pair(d_tmem, ad, bd, IDESC, acc);
+    }
   }
 }
 
@@ -311,7 +326,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int MODE, bool kLong, int CG>
+template <int MODE, bool kLong, int CG, bool kF8 = false>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
@@ -399,7 +414,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t fb = full_bar(stage);
             if constexpr (CG == 2) fb = mapa_shared(fb, 0);
             if (issuer) mbar_arrive_expect_tx(full_bar(stage), C::STAGE * CG);
-            load_stage<MODE, CG>(&tmA, &tmB, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank);
+            load_stage<MODE, CG, kF8>(&tmA, &tmB, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
+                                      rank);
             ++issued;
             if (++stage == NST) {
               stage = 0;
@@ -441,7 +457,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               mma_stage<MODE, CG>(d_tmem + (teacher ? BN : 0), sA, sA + C::A_BYTES,
                                   kb == t.kb0 || kb == p.k_blocks_s);
             } else {
-              mma_stage<MODE, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
+              mma_stage<MODE, CG, kF8>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
             }
             mma_commit_all<CG>(empty_bar(stage));
             if (++stage == NST) {
@@ -500,8 +516,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // DLOGITS also writes zero rows up to the next 64-row K block so that
       // the dW pass over this chunk reads zeros past its last row
       const bool row_store = lr < min((dsh.rows + BK - 1) / BK * BK, p.rows_cap);
+      float a_sc = 1.f;  // e4m3 forward: this row's dequantisation scale
       if constexpr (MODE == MODE_FWD) {
         if (row_ok) tgt = p.targets[grow];
+        if constexpr (kF8) {
+          if (row_ok) a_sc = p.a_scale[grow];
+        }
       }
       if constexpr (MODE == MODE_DLOGITS) {
         if (row_ok) {
@@ -543,6 +563,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           const int col0 = n * BN + c * 32;
           if constexpr (MODE == MODE_FWD) {
+            if constexpr (kF8) {  // dequantise: row scale x per-vocabulary-row scale
+              if (col0 + 32 <= p.V) {
+                const float4* bs = reinterpret_cast<const float4*>(p.b_scale + col0);
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                  const float4 s4 = __ldg(bs + g4);
+                  v[4 * g4] *= a_sc * s4.x;
+                  v[4 * g4 + 1] *= a_sc * s4.y;
+                  v[4 * g4 + 2] *= a_sc * s4.z;
+                  v[4 * g4 + 3] *= a_sc * s4.w;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  v[j] *= (col0 + j < p.V) ? a_sc * __ldg(p.b_scale + col0 + j) : 0.f;
+              }
+            }
             if (p.tf_softcap) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = p.tf_b * tanhf(p.tf_a * v[j]);

@@ -217,6 +217,35 @@ FLCE_API size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int
                                         int64_t chunk_rows);
 
 /*
+ * e4m3 (fp8) operands for the forward log-prob path.  Source: Unsloth, "Reinforcement
+ * Learning GRPO with 7x longer context", introduction: its RL features combine
+ * with float8 training (FP8 RL).  The forward alone is offered in e4m3 -- it
+ * serves log-probs that need no gradient (e.g. reference or old-policy
+ * log-probs in RL); the backward stays bf16, since dlogits with a 3-bit
+ * mantissa cannot keep gradients within 1 % (relative Frobenius).
+ *
+ * flce_quantize_e4m3_rows: x [rows, cols] bf16 -> q [rows, cols] e4m3 bytes
+ * and scale [rows] fp32 with scale = max|x_row| / 448 (1 for an all-zero row)
+ * and q = e4m3(x / scale), round to nearest even, saturating.  cols % 16 == 0.
+ *
+ * flce_forward_e4m3: flce_forward_ex on the dequantised operands, i.e. with
+ * z[i,v] = (sum_k q_h[i,k] q_W[v,k]) * h_scale[i] * W_scale[v], computed by
+ * e4m3 tensor-core MMAs (kind::f8f6f4) into fp32.  h8 [N,H], W8 [V,H] e4m3
+ * row-major; h_scale [N], W_scale [V] fp32 (W_scale 16-byte aligned);
+ * H % 16 == 0.  Other arguments as in flce_forward_ex.
+ */
+FLCE_API flce_status flce_quantize_e4m3_rows(const flce_bf16* x, int64_t rows, int64_t cols,
+                                             uint8_t* q, float* scale, void* stream);
+
+FLCE_API flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, const uint8_t* W8,
+                                       const float* W_scale, const int64_t* targets,
+                                       const float* weights, int64_t N, int64_t H, int64_t V,
+                                       int64_t chunk_rows, int64_t ignore_index,
+                                       const flce_logit_transform* transform, float* out_logp,
+                                       float* out_lse, float* out_loss, int64_t* out_n_valid,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Forward that allocates nothing (no counterpart on the source pages: the
  * method itself does not need it).
  *

@@ -393,6 +393,65 @@ def kd_backward(hs, Ws, ht, Wt, targets=None, weights=None, g: float = 1.0,
     return Backward(dH, dW)
 
 
+# ------------------------------------------------------------------ fp8 (e4m3)
+
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of e4m3 bytes (sign, 4 exponent bits with bias 7, 3 mantissa
+    bits; exponent 0 is subnormal; S.1111.111 is NaN; no infinities)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def f32_to_e4m3(y: np.ndarray) -> np.ndarray:
+    """Round fp32 values to e4m3 bytes: nearest, ties to even, saturating at
+    +-448 (finite inputs)."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    a = np.minimum(np.abs(y), E4M3_MAX)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))  # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)  # unbiased exponent, subnormals share 2^-6
+    quantum = np.exp2(e - 3.0)
+    r = np.rint(a / quantum) * quantum  # exact: powers of two
+    r = np.minimum(r, E4M3_MAX)
+    # encode
+    _, ex2 = np.frexp(np.where(r > 0, r, 1.0))
+    e2 = ex2 - 1
+    normal = r >= 2.0 ** -6
+    mant = np.where(normal, np.rint((r / np.exp2(e2) - 1.0) * 8.0), np.rint(r / 2.0 ** -9))
+    code = np.where(normal, ((e2 + 7) << 3) | mant.astype(np.int64), mant.astype(np.int64))
+    code = np.where(r == 0, 0, code)
+    return (code | np.where(y < 0, 0x80, 0)).astype(np.uint8)
+
+
+def quantize_e4m3_rows(x) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row e4m3 quantisation: scale = max|x_row| / 448 (fp32; 1 for an
+    all-zero row), q = e4m3(x / scale) with the division in fp32.  Returns
+    (q bytes [rows, cols], scale fp32 [rows])."""
+    xf = widen(x).astype(np.float32)
+    amax = np.max(np.abs(xf), axis=1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    return f32_to_e4m3(xf / scale[:, None]), scale
+
+
+def dequantize_e4m3_rows(q, scale) -> np.ndarray:
+    return e4m3_to_f64(q) * np.asarray(scale, dtype=np.float64)[:, None]
+
+
+def forward_fp8(h8, h_scale, W8, W_scale, targets, weights=None, ignore_index: int = IGNORE_INDEX,
+                tf: LogitTransform | None = None, chunk_rows: int | None = None) -> Forward:
+    """The forward of the e4m3-quantised operands: exactly forward() on the
+    dequantised values (logits = (q_h s_h)(q_W s_W)^T)."""
+    return forward(dequantize_e4m3_rows(h8, h_scale), dequantize_e4m3_rows(W8, W_scale), targets,
+                   weights, ignore_index, chunk_rows, tf)
+
+
 def logit_memory_gb(context_length: int, vocab_dim: int, batch_size: int = 1,
                     multiplier: int = 1) -> float:
     """Unsloth GRPO page, flattened-chunking section, Equations 1-3.

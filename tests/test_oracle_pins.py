@@ -463,3 +463,46 @@ def test_kd_gradients_by_finite_differences():
             numh[i, k] = (O.kd_forward(hs + e, Ws, ht, Wt, tf=tf).loss -
                           O.kd_forward(hs - e, Ws, ht, Wt, tf=tf).loss) / (2 * eps)
     assert np.linalg.norm(numh - b.dH) <= 1e-7 * np.linalg.norm(b.dH)
+
+
+# ------------------------------------------------------------------------ fp8
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+
+
+def test_e4m3_rounding_matches_torch_saturating_conversion():
+    r = np.random.default_rng(3)
+    y = np.concatenate([r.standard_normal(20000).astype(np.float32) * s for s in (1e-4, 0.01, 1, 50, 400)]
+                       + [np.array([0.0, -0.0, 448.0, 449.0, 1e6, -1e6, 2.0 ** -10, 3 * 2.0 ** -10,
+                                    464.0, 240.0, 248.0, 232.0], dtype=np.float32)])
+    ref = torch.from_numpy(np.clip(y, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.f32_to_e4m3(y)
+    # -0.0 and 0.0 both decode to zero; compare values, and codes away from zero
+    assert np.array_equal(O.e4m3_to_f64(got), O.e4m3_to_f64(ref))
+    nz = y != 0
+    assert np.array_equal(got[nz], ref[nz])
+
+
+def test_row_quantiser_bounds_and_dequantised_forward():
+    r = np.random.default_rng(4)
+    x = r.standard_normal((50, 64)).astype(np.float32) * np.exp(r.standard_normal((50, 1)))
+    x[7] = 0.0
+    q, s = O.quantize_e4m3_rows(x)
+    assert q.dtype == np.uint8 and s.dtype == np.float32 and s[7] == 1.0
+    back = O.dequantize_e4m3_rows(q, s)
+    # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 for normals, row max exact-ish
+    big = np.abs(x) > np.max(np.abs(x), axis=1, keepdims=True) * 2.0 ** -5
+    assert np.all(np.abs(back - x)[big] <= np.abs(x)[big] * 2.0 ** -4 + 1e-12)
+    assert np.allclose(np.max(np.abs(back), axis=1)[s != 1.0], np.max(np.abs(x), axis=1)[s != 1.0],
+                       rtol=2.0 ** -4)
+    h8, hs = O.quantize_e4m3_rows(r.standard_normal((20, 64)))
+    W8, Ws = O.quantize_e4m3_rows(r.standard_normal((30, 64)) * 0.1)
+    t = r.integers(0, 30, 20)
+    f8 = O.forward_fp8(h8, hs, W8, Ws, t)
+    f = O.forward(O.dequantize_e4m3_rows(h8, hs), O.dequantize_e4m3_rows(W8, Ws), t)
+    assert np.array_equal(f8.logp, f.logp)
