@@ -783,6 +783,111 @@ bool transform_params(const flce_logit_transform* tf, GemmParams& p) {
     }                                    \
   } while (0)
 
+// Final deterministic reduction of the block partials into loss and count.
+flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, const double* bsum,
+                      const long long* bcnt, cudaStream_t st) {
+  if (out_loss || out_n_valid) {
+    ProfScope ps(K_FINAL, st);
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
+                                              reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
+}
+
+// ---- stages shared by the entry points
+
+// dH and dW stages of one backward row chunk, shared by the cross-entropy and
+// the distillation backwards.  The chunk's bf16 dlogits D sit in the chunk
+// buffer (maps D_k / D_mn); B_dw is the map of the chunk's rows of h (the
+// gathered rows when compacted).  ri / dc / first: compaction (original row of
+// each compacted row, device-side row count, first compacted row of the
+// chunk), or null.
+struct DhDwStage {
+  int cg, workers, tm;
+  bool kLong;
+  const BwdPlan* plan;
+  long long H, V;
+  float* dh_part;
+  flce_bf16* dH;
+  float* dW;
+  const CUtensorMap* W_mn;
+  const CUtensorMap* dW_map;
+};
+
+flce_status chunk_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int chunk,
+                        const CUtensorMap& D_k, const CUtensorMap& D_mn, const CUtensorMap& B_dw,
+                        const int* ri, const int* dc, int first, cudaStream_t st) {
+  const BwdPlan& b = *a.plan;
+  if (a.dH) {  // dH[rows] = D W
+    GemmParams q = p;
+    q.m_tiles = static_cast<int>(ceil_div(rows, a.tm));
+    q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    q.k_blocks = static_cast<int>(ceil_div(a.V, BK));
+    q.cols = q.n_tiles;
+    q.n_per_unit = 1;
+    q.kb_per_split = b.dh_kb_per_split;
+    const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
+    q.k_splits = splits;
+    q.num_units = splits * q.m_tiles * q.n_tiles;
+    q.group_m = q.m_tiles;
+    q.dH_part = splits > 1 ? a.dh_part : nullptr;
+    {
+      ProfScope ps(K_DH, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, *a.W_mn, q,
+                                         std::min(q.num_units, a.workers), st));
+    }
+    if (splits > 1) {
+      ProfScope ps(K_DH_REDUCE, st);
+      const long long total = static_cast<long long>(rows) * (a.H / 4);
+      const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
+      if (a.kLong)
+        dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, splits, rows, static_cast<int>(b.R),
+                                                               static_cast<int>(a.H), p.row0, a.dH, ri, dc, first);
+      else
+        dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, splits, rows, static_cast<int>(b.R),
+                                                                static_cast<int>(a.H), p.row0, a.dH, ri, dc, first);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+  }
+  if (a.dW) {  // dW (+)= D^T h[rows]
+    GemmParams q = p;
+    q.m_tiles = static_cast<int>(ceil_div(a.V, a.tm));
+    q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    q.k_blocks = static_cast<int>(ceil_div(rows, BK));
+    q.cols = q.n_tiles;
+    q.n_per_unit = 1;
+    q.kb_per_split = q.k_blocks;
+    q.k_splits = 1;
+    q.num_units = q.m_tiles * q.n_tiles;
+    q.group_m = std::min(8, q.m_tiles);
+    q.dW_accumulate = chunk > 0 ? 1 : 0;
+    ProfScope ps(K_DW, st);
+    FLCE_CUDA_TRY(launch_gemm<MODE_DW>(a.cg, a.kLong, D_mn, B_dw, *a.dW_map, q,
+                                       std::min(q.num_units, a.workers), st));
+  }
+  return FLCE_OK;
+}
+
+// Cross-entropy forward tail: per-row combine of the split partials, then
+// the deterministic loss / count reduction.
+flce_status ce_forward_tail(bool kLong, const FwdPlan& f, int N, const float2* part, const float* zt,
+                            const int64_t* targets, const float* weights, long long ignore,
+                            float* out_logp, float* out_lse, float* out_loss, int64_t* out_n_valid,
+                            double* bsum, long long* bcnt, cudaStream_t st) {
+  if (N > 0) {
+    ProfScope ps(K_COMBINE, st);
+    if (kLong)
+      combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, zt, targets, weights, ignore,
+                                                             out_logp, out_lse, bsum, bcnt);
+    else
+      combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, zt, targets, weights, ignore,
+                                                              out_logp, out_lse, bsum, bcnt);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -897,24 +1002,10 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
       ProfScope ps(K_FWD, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(cg, kLong, tA, tB, tB, p, f.grid, st));
     }
-    {
-      ProfScope ps(K_COMBINE, st);
-      if (kLong)
-        combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
-                                                               ignore_index, out_logp, out_lse, bsum, bcnt);
-      else
-        combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
-                                                                ignore_index, out_logp, out_lse, bsum, bcnt);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
+    return ce_forward_tail(kLong, f, Ni, part, zt, targets, weights, ignore_index, out_logp, out_lse,
+                           out_loss, out_n_valid, bsum, bcnt, st);
   }
-  if (out_loss || out_n_valid) {
-    ProfScope ps(K_FINAL, st);
-    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
-                                              reinterpret_cast<long long*>(out_n_valid));
-    FLCE_CUDA_TRY(cudaGetLastError());
-  }
-  return FLCE_OK;
+  return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
 }
 
 flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
@@ -1026,6 +1117,7 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
       return FLCE_ERR_CUDA;
   }
 
+  const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH, dW, &W_mn, &dW_map};
   int chunk = 0;
   for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
     // rows: exact (plain) or the capacity whose live part the kernels read (compacted)
@@ -1071,56 +1163,11 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
                !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK)) {
       return FLCE_ERR_CUDA;
     }
-    // (2) dH[rows] = D W
-    if (dH) {
-      GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
-      q.n_tiles = static_cast<int>(ceil_div(H, BN));
-      q.k_blocks = static_cast<int>(ceil_div(V, BK));
-      q.cols = q.n_tiles;
-      q.n_per_unit = 1;
-      q.kb_per_split = b.dh_kb_per_split;
-      const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
-      q.k_splits = splits;
-      q.num_units = splits * q.m_tiles * q.n_tiles;
-      q.group_m = q.m_tiles;
-      q.dH_part = splits > 1 ? dh_part : nullptr;
-      {
-        ProfScope ps(K_DH, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(cg, kLong, D_k, W_mn, W_mn, q, std::min(q.num_units, workers), st));
-      }
-      if (splits > 1) {
-        ProfScope ps(K_DH_REDUCE, st);
-        const long long total = static_cast<long long>(rows) * (H / 4);
-        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
-        const int* ri = compact ? cidx : nullptr;
-        const int* dc = compact ? ccount : nullptr;
-        if (kLong)
-          dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
-                                                                 static_cast<int>(H), p.row0, dH, ri, dc,
-                                                                 static_cast<int>(row0));
-        else
-          dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
-                                                                  static_cast<int>(H), p.row0, dH, ri, dc,
-                                                                  static_cast<int>(row0));
-        FLCE_CUDA_TRY(cudaGetLastError());
-      }
-    }
-    // (3) dW (+)= D^T h[rows]
-    if (dW) {
-      GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(V, tm));
-      q.n_tiles = static_cast<int>(ceil_div(H, BN));
-      q.k_blocks = static_cast<int>(ceil_div(rows, BK));
-      q.cols = q.n_tiles;
-      q.n_per_unit = 1;
-      q.kb_per_split = q.k_blocks;
-      q.k_splits = 1;
-      q.num_units = q.m_tiles * q.n_tiles;
-      q.group_m = std::min(8, q.m_tiles);
-      q.dW_accumulate = chunk > 0 ? 1 : 0;
-      ProfScope ps(K_DW, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(cg, kLong, D_mn, B_dw, dW_map, q, std::min(q.num_units, workers), st));
+    // (2) dH[rows] = D W, (3) dW (+)= D^T h[rows]
+    {
+      const flce_status s2 = chunk_dh_dw(dhdw, p, rows, chunk, D_k, D_mn, B_dw, compact ? cidx : nullptr,
+                                         compact ? ccount : nullptr, static_cast<int>(row0), st);
+      if (s2 != FLCE_OK) return s2;
     }
   }
   return FLCE_OK;
@@ -1238,24 +1285,10 @@ flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, const uin
       ProfScope ps(K_FWD, st);
       FLCE_CUDA_TRY(launch_fwd_e4m3(cg, kLong, tA, tB, p, f.grid, st));
     }
-    {
-      ProfScope ps(K_COMBINE, st);
-      if (kLong)
-        combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
-                                                               ignore_index, out_logp, out_lse, bsum, bcnt);
-      else
-        combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, Ni, zt, targets, weights,
-                                                                ignore_index, out_logp, out_lse, bsum, bcnt);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
+    return ce_forward_tail(kLong, f, Ni, part, zt, targets, weights, ignore_index, out_logp, out_lse,
+                           out_loss, out_n_valid, bsum, bcnt, st);
   }
-  if (out_loss || out_n_valid) {
-    ProfScope ps(K_FINAL, st);
-    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
-                                              reinterpret_cast<long long*>(out_n_valid));
-    FLCE_CUDA_TRY(cudaGetLastError());
-  }
-  return FLCE_OK;
+  return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
 }
 
 size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, int64_t chunk_rows) {
@@ -1355,13 +1388,7 @@ flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t 
       FLCE_CUDA_TRY(cudaGetLastError());
     }
   }
-  if (out_loss || out_n_valid) {
-    ProfScope prof(K_FINAL, st);
-    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
-                                              reinterpret_cast<long long*>(out_n_valid));
-    FLCE_CUDA_TRY(cudaGetLastError());
-  }
-  return FLCE_OK;
+  return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
 }
 
 flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
@@ -1437,6 +1464,7 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
   base.tf_b = tfp.tf_b;
   base.tf_d = tfp.tf_d;
 
+  const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH_s, dW_s, &Ws_mn, &dW_map};
   int chunk = 0;
   for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
     const int rows = static_cast<int>(std::min(b.R, N - row0));
@@ -1462,53 +1490,8 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
     if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) ||
         !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
       return FLCE_ERR_CUDA;
-    if (dH_s) {  // (2) dH_s[rows] = D W_s
-      GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
-      q.n_tiles = static_cast<int>(ceil_div(H, BN));
-      q.k_blocks = static_cast<int>(ceil_div(V, BK));
-      q.cols = q.n_tiles;
-      q.n_per_unit = 1;
-      q.kb_per_split = b.dh_kb_per_split;
-      const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
-      q.k_splits = splits;
-      q.num_units = splits * q.m_tiles * q.n_tiles;
-      q.group_m = q.m_tiles;
-      q.dH_part = splits > 1 ? dh_part : nullptr;
-      {
-        ProfScope prof(K_DH, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_DH>(cg, kLong, D_k, Ws_mn, Ws_mn, q, std::min(q.num_units, workers), st));
-      }
-      if (splits > 1) {
-        ProfScope prof(K_DH_REDUCE, st);
-        const long long total = static_cast<long long>(rows) * (H / 4);
-        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
-        if (kLong)
-          dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
-                                                                 static_cast<int>(H), p.row0, dH_s, nullptr,
-                                                                 nullptr, 0);
-        else
-          dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(dh_part, splits, rows, static_cast<int>(b.R),
-                                                                  static_cast<int>(H), p.row0, dH_s, nullptr,
-                                                                  nullptr, 0);
-        FLCE_CUDA_TRY(cudaGetLastError());
-      }
-    }
-    if (dW_s) {  // (3) dW_s (+)= D^T h_s[rows]
-      GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(V, tm));
-      q.n_tiles = static_cast<int>(ceil_div(H, BN));
-      q.k_blocks = static_cast<int>(ceil_div(rows, BK));
-      q.cols = q.n_tiles;
-      q.n_per_unit = 1;
-      q.kb_per_split = q.k_blocks;
-      q.k_splits = 1;
-      q.num_units = q.m_tiles * q.n_tiles;
-      q.group_m = std::min(8, q.m_tiles);
-      q.dW_accumulate = chunk > 0 ? 1 : 0;
-      ProfScope prof(K_DW, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DW>(cg, kLong, D_mn, hs_mn, dW_map, q, std::min(q.num_units, workers), st));
-    }
+    const flce_status s2 = chunk_dh_dw(dhdw, p, rows, chunk, D_k, D_mn, hs_mn, nullptr, nullptr, 0, st);
+    if (s2 != FLCE_OK) return s2;
   }
   return FLCE_OK;
 }
