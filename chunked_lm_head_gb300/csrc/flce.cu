@@ -449,6 +449,13 @@ FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm)
       f.tps = tps;
     }
   }
+  // FLCE_FWD_SPLITS=s pins the number of vocabulary splits (tests compare
+  // split counts; results must not depend on them beyond fp32 rounding)
+  if (const char* e = std::getenv("FLCE_FWD_SPLITS")) {
+    const int want = std::max(1, std::min(std::atoi(e), f.n_tiles));
+    f.tps = static_cast<int>(ceil_div(f.n_tiles, want));
+    f.S = static_cast<int>(ceil_div(f.n_tiles, f.tps));
+  }
   f.units = f.m_tiles * f.S;
   f.grid = std::min(f.units, workers);
   return f;

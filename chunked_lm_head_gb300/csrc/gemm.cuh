@@ -1,27 +1,35 @@
-// Persistent tcgen05 GEMM engine of libflce and its four epilogues.
+// Persistent tcgen05 GEMM engine of libflce and its epilogues.
 //
-// One CTA per SM.  Warp 0 (one lane) streams operand tiles with TMA into a
-// 4-stage shared-memory ring; warp 1 (one lane) issues tcgen05.mma into one
-// of two 128x256 fp32 TMEM accumulators; warps 2-5 drain the other
-// accumulator with tcgen05.ld and run the mode's epilogue, so the epilogue of
-// tile i overlaps the MMAs of tile i+1.
+// One CTA per SM, running alone (CG = 1) or as one half of an SM pair
+// (CG = 2, tcgen05 cta_group::2 with 256 x 256 tiles).  Warp 0 (one lane)
+// streams operand tiles with TMA into a shared-memory ring; warp 1 (one lane
+// of the pair's first CTA) issues tcgen05.mma into fp32 TMEM accumulators;
+// warps 2-5 drain an accumulator with tcgen05.ld and run the mode's epilogue,
+// overlapping the MMAs of the next tile where two accumulators fit in TMEM.
 //
-// Modes (the four contractions of the chunked LM-head cross-entropy):
-//   FWD      Z = h W^T over a split of the vocabulary; epilogue keeps an online
-//            row max / sum of exp in registers (each thread owns one row of
-//            the accumulator, so no cross-thread reduction is needed) and
-//            gathers the target logit.  Emits per-(row, split) partials.
-//   DLOGITS  the same Z recomputed for one row chunk; epilogue forms
-//            D = (exp(Z - lse) - onehot(t)) * m * w * g in bf16.
-//   DH       dH[chunk rows] = D W         (K = vocabulary; W read MN-major)
-//   DW       dW (+)= D^T h[chunk rows]    (K = chunk rows; D and h MN-major)
+// Modes (the contractions of the chunked LM-head losses):
+//   FWD         Z = h W^T over a split of the vocabulary; epilogue keeps an
+//               online row max / sum of exp in registers (each thread owns one
+//               row of the accumulator, so no cross-thread reduction is
+//               needed) and gathers the target logit.  Emits per-(row, split)
+//               partials.  bf16 or (kF8) e4m3 operands with row scales.
+//   DLOGITS     the same Z recomputed for one row chunk; epilogue forms
+//               D = (exp(Z - lse) - onehot(t)) * m * w * g in bf16.
+//   DH          dH[chunk rows] = D W         (K = vocabulary; W read MN-major)
+//   DW          dW (+)= D^T h[chunk rows]    (K = chunk rows; D and h MN-major;
+//               TMA store / fp32 reduce-add epilogue)
+//   KD_FWD      distillation: student and teacher logits of a tile side by
+//               side in TMEM; online log-sum-exp of both heads and the
+//               teacher-weighted logit difference
+//   KD_DLOGITS  distillation: D = (p_s - p_t) * m * w * g
 //
 // Sources: Unsloth, "Reinforcement Learning GRPO with 7x longer context",
 // sections "Flattened sequence-length chunking" (chunk logits are
 // hidden @ lm_head, upcast to fp32, log-softmaxed, target gathered) and
 // "Offloading activations for log-softmax" (backward recomputes the chunk);
 // TRL v1.13 article, speed & memory section (keep both GEMM operands bf16 on
-// the tensor cores instead of the fp32 SIMT path).
+// the tensor cores instead of the fp32 SIMT path; the distillation trainer
+// computes each chunk with both heads).
 #pragma once
 
 #include <cuda_bf16.h>

@@ -265,3 +265,20 @@ def test_row_compaction_matches_full_rows(monkeypatch):
         assert_grad_close(np64(got), ref.dW, name)
     ign = torch.from_numpy(inp.targets == WL.IGNORE_INDEX).cuda()
     assert torch.all(dH_c[ign] == 0)
+
+
+@pytest.mark.parametrize("splits", ["1", "3", "7"])
+def test_forward_independent_of_vocabulary_splits(splits, monkeypatch):
+    """The split-V combine against a single split (and odd split counts):
+    lse / logp agree to fp32 rounding and the loss to the loss tolerance."""
+    wl = WL.custom("splits", 900, 192, 5000, 256, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=112)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    logp0, lse0, loss0, nv0 = run_forward(h, W, t, w, 256)
+    monkeypatch.setenv("FLCE_FWD_SPLITS", splits)
+    logp1, lse1, loss1, nv1 = run_forward(h, W, t, w, 256)
+    assert nv1 == nv0
+    assert torch.allclose(lse1, lse0, atol=2e-5, rtol=0) and torch.allclose(logp1, logp0, atol=2e-5, rtol=0)
+    assert loss1 == pytest.approx(loss0, rel=1e-6)
+    ref = O.forward(inp.h, inp.W, inp.targets)
+    assert_logp_close(np64(logp1), ref.logp, "logp")
