@@ -49,6 +49,8 @@ SIGNATURES = {
     "flce_forward_static_scratch": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                                    _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
+    "flce_backward_plan": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int32,
+                                          ctypes.c_int32, _c_vp]),
     "flce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "flce_device_status": (ctypes.c_int, [_c_vp]),
     "flce_selftest_wait_timeout": (ctypes.c_int, [_c_i64, _c_vp]),
@@ -235,6 +237,22 @@ def flce_forward_static_scratch(h, W, targets, weights, N, H, V, chunk_rows, ign
 
 def flce_workspace_bytes(N, H, V, chunk_rows) -> int:
     return int(load().flce_workspace_bytes(N, H, V, chunk_rows))
+
+
+class BackwardPlanInfo(ctypes.Structure):
+    """flce_backward_plan_info."""
+    _fields_ = [("rows_per_block", ctypes.c_int64), ("vocab_per_slab", ctypes.c_int64),
+                ("row_blocks", ctypes.c_int64), ("vocab_slabs", ctypes.c_int64),
+                ("dh_splits", ctypes.c_int64), ("dlogits_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+def flce_backward_plan(N, H, V, chunk_rows, workers=0, cta_group=0) -> dict:
+    """The backward's tiling (row block, vocabulary slab, dH splits, bytes)."""
+    info = BackwardPlanInfo()
+    st = load().flce_backward_plan(N, H, V, chunk_rows, workers, cta_group, ctypes.addressof(info))
+    check("flce_backward_plan", st)
+    return {name: int(getattr(info, name)) for name, _ in BackwardPlanInfo._fields_}
 
 
 def flce_kd_workspace_bytes(N, H_s, H_t, V, chunk_rows) -> int:

@@ -437,7 +437,10 @@ FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm)
   f.k_blocks = static_cast<int>(ceil_div(H, BK));
   f.nblk = static_cast<int>(ceil_div(N, SMALL_THREADS));
   long long best = LLONG_MAX;
-  const int smax = std::min(f.n_tiles, 256);
+  // at most 256 splits, and split partials (8 bytes per row and split) of
+  // at most 256 MiB
+  const long long s_mem = std::max(1LL, (256LL << 20) / (8 * std::max(1LL, N)));
+  const int smax = static_cast<int>(std::min<long long>(std::min(f.n_tiles, 256), s_mem));
   for (int s = 1; s <= smax; ++s) {
     const int tps = static_cast<int>(ceil_div(f.n_tiles, s));
     const int se = static_cast<int>(ceil_div(f.n_tiles, tps));
@@ -461,20 +464,32 @@ FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm)
   return f;
 }
 
+// Backward tiling.  The dlogits buffer D holds R rows x ldD columns: the
+// caller's chunk_rows x V bound (rows rounded up to 128).  D need not span the
+// whole vocabulary: the backward walks blocks of R rows and, inside each, slabs
+// of Vs vocabulary columns, so R can exceed chunk_rows while R x Vs stays inside
+// the same bound.  dW is then read-modified-written once per row block instead
+// of once per chunk_rows rows, and dH is summed over the slabs in fp32 partials
+// (one per k-split) that are rounded to bf16 once per row block.
 struct BwdPlan {
-  long long R = 0, ldD = 0;
-  int dh_splits = 1;
+  long long R = 0;      // rows per block: the row capacity of D
+  long long Vs = 0;     // vocabulary columns per slab (V when one slab)
+  int n_slabs = 1;
+  long long ldD = 0;    // row pitch of D in elements
+  int dh_splits = 1;    // k-splits of the dH GEMM (fp32 partial sets)
   int dh_kb_per_split = 1;
+  bool dh_f32 = false;  // dH through fp32 partials (several slabs or k-splits)
+  double est_s = 0.0;   // modelled time of the backward GEMMs
 };
 
-BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int workers,
-                      int tm) {
-  BwdPlan b;
-  b.R = round_up(std::max(1LL, chunk_rows), BM);
-  b.R = std::min(b.R, round_up(std::max(1LL, N), BM));
-  b.ldD = round_up(V, 8);
-  const long long tiles = ceil_div(b.R, tm) * ceil_div(H, BN);
-  const long long kb = ceil_div(V, BK);
+constexpr double kPlanFlops = 1.6e15;  // sustained bf16 tensor rate of the GPU (model)
+constexpr double kPlanBytes = 6.0e12;  // sustained HBM bandwidth (model)
+constexpr double kPlanLaunch = 5e-6;   // per launch: prologue, drain and the gap to the next
+
+// Best dH k-split count for `tiles` output tiles and `kb` K blocks: the
+// fewest splits whose last wave is at least 90% full (splits keep >= 8 K
+// blocks each).
+int dh_split_count(long long tiles, long long kb, int workers) {
   int best_s = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= 16; ++s) {
@@ -487,10 +502,127 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
     }
     if (eff >= 0.9) break;
   }
-  b.dh_splits = best_s;
-  b.dh_kb_per_split = static_cast<int>(ceil_div(kb, best_s));
-  b.dh_splits = static_cast<int>(ceil_div(kb, b.dh_kb_per_split));
-  return b;
+  return best_s;
+}
+
+// Completes plan b for row block size R (D budget in elements): slab width,
+// dH splits, memory check and modelled time.  False when R does not fit.
+bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long R,
+                    long long budget, int workers, int tm) {
+  const long long ldV = round_up(V, 8);
+  b.R = R;
+  if (R * ldV <= budget) {
+    b.n_slabs = 1;
+    b.Vs = V;
+    b.ldD = ldV;
+  } else {
+    const long long vs_max = (budget / R) / BN * BN;
+    if (vs_max < BN) return false;
+    b.n_slabs = static_cast<int>(ceil_div(V, vs_max));
+    b.Vs = round_up(ceil_div(V, b.n_slabs), BN);
+    b.ldD = b.Vs;
+  }
+  const long long dh_tiles = ceil_div(R, tm) * ceil_div(H, BN);
+  const long long kb = ceil_div(b.Vs, BK);
+  int s = dh_split_count(dh_tiles, kb, workers);
+  b.dh_kb_per_split = static_cast<int>(ceil_div(kb, s));
+  s = static_cast<int>(ceil_div(kb, b.dh_kb_per_split));
+  // dH partials and the gathered rows stay within the size of D
+  auto aux = [&](int splits, bool f32) {
+    return (f32 ? static_cast<double>(splits) * R * H * 4 : 0.0) + static_cast<double>(R) * H * 2;
+  };
+  while (s > 1 && aux(s, true) > 2.0 * budget) {
+    --s;
+    b.dh_kb_per_split = static_cast<int>(ceil_div(kb, s));
+    s = static_cast<int>(ceil_div(kb, b.dh_kb_per_split));
+  }
+  b.dh_splits = s;
+  b.dh_f32 = b.n_slabs > 1 || s > 1;
+  if (b.n_slabs > 1 && aux(s, b.dh_f32) > 2.0 * budget) return false;
+
+  // modelled time: per launch max(tensor time, HBM time) + launch cost
+  const double t_kb = 2.0 * tm * BN * BK * workers / kPlanFlops;  // one tile x one 64-deep K block
+  auto waves = [&](long long u) { return static_cast<double>(ceil_div(u, workers)); };
+  auto slab_cost = [&](long long rows, long long w, bool first_block, bool first_slab) {
+    const long long mt = ceil_div(rows, tm);
+    const double d_bytes = 2.0 * rows * w;
+    double t = 0.0;
+    // dlogits: W slab read once per 16 row tiles
+    t += std::max(waves(mt * ceil_div(w, BN)) * ceil_div(H, BK) * t_kb,
+                  (d_bytes + 2.0 * w * H * ceil_div(mt, 16) + 2.0 * rows * H) / kPlanBytes);
+    // dH
+    const long long kbw = ceil_div(w, BK);
+    const long long sw = ceil_div(kbw, b.dh_kb_per_split);
+    const double dh_out = b.dh_f32 ? 4.0 * rows * H * sw * (first_slab ? 1 : 2) : 2.0 * rows * H;
+    t += std::max(waves(mt * ceil_div(H, BN) * sw) * b.dh_kb_per_split * t_kb,
+                  (d_bytes + 2.0 * w * H + dh_out) / kPlanBytes);
+    // dW: a store on the first row block, a read-modify-write afterwards
+    const long long vt = ceil_div(w, tm);
+    t += std::max(waves(vt * ceil_div(H, BN)) * ceil_div(rows, BK) * t_kb,
+                  (d_bytes + 2.0 * rows * H * ceil_div(vt, 8) + 4.0 * w * H * (first_block ? 1 : 2)) /
+                      kPlanBytes);
+    return t + 3 * kPlanLaunch;
+  };
+  auto block_cost = [&](long long rows, bool first_block) {
+    const long long w_last = V - (b.n_slabs - 1) * b.Vs;
+    double t = slab_cost(rows, b.n_slabs == 1 ? V : b.Vs, first_block, true);
+    if (b.n_slabs > 2) t += (b.n_slabs - 2) * slab_cost(rows, b.Vs, first_block, false);
+    if (b.n_slabs > 1) t += slab_cost(rows, w_last, first_block, false);
+    if (b.dh_f32) t += rows * H * (4.0 * b.dh_splits + 2.0) / kPlanBytes + kPlanLaunch;
+    return t;
+  };
+  const long long nb = ceil_div(N, R);
+  const long long rows_last = N - (nb - 1) * R;
+  if (nb == 1)
+    b.est_s = block_cost(rows_last, true);
+  else
+    b.est_s = block_cost(R, true) + (nb - 2) * block_cost(R, false) + block_cost(rows_last, false);
+  return true;
+}
+
+// FLCE_BWD_ROWS=<rows> fixes the row block (clamped to the budget) instead of
+// the modelled choice.
+long long bwd_rows_env() {
+  const char* e = std::getenv("FLCE_BWD_ROWS");
+  return e != nullptr ? std::atoll(e) : 0;
+}
+
+BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int workers,
+                      int tm) {
+  N = std::max(1LL, N);
+  const long long nr = round_up(N, BM);
+  const long long R0 = std::min(round_up(std::max(1LL, chunk_rows), BM), nr);
+  const long long budget = R0 * round_up(V, 8);
+  workers = std::max(1, workers);
+  struct Key {
+    long long N, H, V, R0, forced;
+    int workers, tm;
+  };
+  thread_local Key last{-1, -1, -1, -1, -1, -1, -1};
+  thread_local BwdPlan last_plan;
+  const long long forced = bwd_rows_env();
+  if (last.N == N && last.H == H && last.V == V && last.R0 == R0 && last.forced == forced &&
+      last.workers == workers && last.tm == tm)
+    return last_plan;
+
+  BwdPlan best;
+  plan_candidate(best, N, H, V, R0, budget, workers, tm);  // the caller's chunk: always fits
+  if (forced > 0) {
+    BwdPlan b;
+    const long long R = std::min(nr, std::max(R0, round_up(forced, BM)));
+    if (plan_candidate(b, N, H, V, R, budget, workers, tm)) best = b;
+  } else {
+    // larger row blocks in steps of one tile
+    for (long long R = round_up(R0 + 1, tm); R <= round_up(nr, tm); R += tm) {
+      BwdPlan b;
+      if (!plan_candidate(b, N, H, V, std::min(R, nr), budget, workers, tm)) break;
+      if (b.est_s < best.est_s * 0.98) best = b;
+      if (R >= nr) break;
+    }
+  }
+  last = Key{N, H, V, R0, forced, workers, tm};
+  last_plan = best;
+  return best;
 }
 
 struct FwdLayout {
@@ -538,7 +670,7 @@ KdFwdLayout kd_fwd_layout(long long N, const FwdPlan& f) {
 struct BwdLayout {
   size_t D = 0, dh_part = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, total = 0;
 };
-// dlogits chunk, dH split-K partials, validation counter, and the row
+// dlogits block, dH fp32 partials, validation counter, and the row
 // compaction buffers (valid-row indices, per-block counts, their total, the
 // gathered h rows of one chunk).
 BwdLayout bwd_layout(long long N, long long H, const BwdPlan& b) {
@@ -547,7 +679,7 @@ BwdLayout bwd_layout(long long N, long long H, const BwdPlan& b) {
   L.D = o;
   o += align256(static_cast<size_t>(b.R) * b.ldD * 2);
   L.dh_part = o;
-  if (b.dh_splits > 1) o += align256(static_cast<size_t>(b.dh_splits) * b.R * H * 4);
+  if (b.dh_f32) o += align256(static_cast<size_t>(b.dh_splits) * b.R * H * 4);
   L.bad = o;
   o += 256;
   L.idx = o;
@@ -804,12 +936,12 @@ flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, c
 
 // ---- stages shared by the entry points
 
-// dH and dW stages of one backward row chunk, shared by the cross-entropy and
-// the distillation backwards.  The chunk's bf16 dlogits D sit in the chunk
-// buffer (maps D_k / D_mn); B_dw is the map of the chunk's rows of h (the
-// gathered rows when compacted).  ri / dc / first: compaction (original row of
-// each compacted row, device-side row count, first compacted row of the
-// chunk), or null.
+// dH and dW stages of the backward, shared by the cross-entropy and the
+// distillation backwards.  For one row block and one vocabulary slab, the
+// slab's bf16 dlogits sit in D (maps D_k / D_mn, local columns); B_dw maps the
+// block's rows of h (the gathered rows when compacted).  ri / dc / first:
+// compaction (original row of each compacted row, device-side row count, first
+// compacted row of the block), or null.
 struct DhDwStage {
   int cg, workers, tm;
   bool kLong;
@@ -820,17 +952,19 @@ struct DhDwStage {
   float* dW;
   const CUtensorMap* W_mn;
   const CUtensorMap* dW_map;
+  const CUtensorMap* dhp_map;  // fp32 dH partials [dh_splits * R][H]
 };
 
-flce_status chunk_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int chunk,
-                        const CUtensorMap& D_k, const CUtensorMap& D_mn, const CUtensorMap& B_dw,
-                        const int* ri, const int* dc, int first, cudaStream_t st) {
+flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int block, int slab, int v0,
+                       int width, const CUtensorMap& D_k, const CUtensorMap& D_mn,
+                       const CUtensorMap& B_dw, cudaStream_t st) {
   const BwdPlan& b = *a.plan;
-  if (a.dH) {  // dH[rows] = D W
+  if (a.dH) {  // dH[rows] (+)= D[:, slab] W[slab]
     GemmParams q = p;
+    q.v0 = v0;
     q.m_tiles = static_cast<int>(ceil_div(rows, a.tm));
     q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
-    q.k_blocks = static_cast<int>(ceil_div(a.V, BK));
+    q.k_blocks = static_cast<int>(ceil_div(width, BK));
     q.cols = q.n_tiles;
     q.n_per_unit = 1;
     q.kb_per_split = b.dh_kb_per_split;
@@ -838,28 +972,16 @@ flce_status chunk_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int c
     q.k_splits = splits;
     q.num_units = splits * q.m_tiles * q.n_tiles;
     q.group_m = q.m_tiles;
-    q.dH_part = splits > 1 ? a.dh_part : nullptr;
-    {
-      ProfScope ps(K_DH, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, *a.W_mn, q,
-                                         std::min(q.num_units, a.workers), st));
-    }
-    if (splits > 1) {
-      ProfScope ps(K_DH_REDUCE, st);
-      const long long total = static_cast<long long>(rows) * (a.H / 4);
-      const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
-      if (a.kLong)
-        dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, splits, rows, static_cast<int>(b.R),
-                                                               static_cast<int>(a.H), p.row0, a.dH, ri, dc, first);
-      else
-        dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, splits, rows, static_cast<int>(b.R),
-                                                                static_cast<int>(a.H), p.row0, a.dH, ri, dc, first);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
+    q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
+    q.dh_accumulate = slab > 0 ? 1 : 0;
+    ProfScope ps(K_DH, st);
+    FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
+                                       std::min(q.num_units, a.workers), st));
   }
-  if (a.dW) {  // dW (+)= D^T h[rows]
+  if (a.dW) {  // dW[slab] (+)= D[:, slab]^T h[rows]
     GemmParams q = p;
-    q.m_tiles = static_cast<int>(ceil_div(a.V, a.tm));
+    q.v0 = v0;
+    q.m_tiles = static_cast<int>(ceil_div(width, a.tm));
     q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
     q.k_blocks = static_cast<int>(ceil_div(rows, BK));
     q.cols = q.n_tiles;
@@ -868,11 +990,31 @@ flce_status chunk_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int c
     q.k_splits = 1;
     q.num_units = q.m_tiles * q.n_tiles;
     q.group_m = std::min(8, q.m_tiles);
-    q.dW_accumulate = chunk > 0 ? 1 : 0;
+    q.dW_accumulate = block > 0 ? 1 : 0;
     ProfScope ps(K_DW, st);
     FLCE_CUDA_TRY(launch_gemm<MODE_DW>(a.cg, a.kLong, D_mn, B_dw, *a.dW_map, q,
                                        std::min(q.num_units, a.workers), st));
   }
+  return FLCE_OK;
+}
+
+// After the last slab of a row block: the block's fp32 dH partials, summed
+// over the k-splits and rounded to bf16, into its rows of dH.
+flce_status block_dh_finish(const DhDwStage& a, int row0, int rows, const int* ri, const int* dc,
+                            int first, cudaStream_t st) {
+  const BwdPlan& b = *a.plan;
+  if (!a.dH || !b.dh_f32) return FLCE_OK;
+  ProfScope ps(K_DH_REDUCE, st);
+  const long long total = static_cast<long long>(rows) * (a.H / 4);
+  const int grid = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms())));
+  if (a.kLong)
+    dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, b.dh_splits, rows, static_cast<int>(b.R),
+                                                           static_cast<int>(a.H), row0, a.dH, ri, dc, first);
+  else
+    dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, b.dh_splits, rows, static_cast<int>(b.R),
+                                                            static_cast<int>(a.H), row0, a.dH, ri, dc, first);
+  FLCE_CUDA_TRY(cudaGetLastError());
   return FLCE_OK;
 }
 
@@ -919,6 +1061,22 @@ size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows)
   const FwdLayout fl = fwd_layout(N, plan_forward(N, H, V, workers, BM * cg));
   const BwdLayout bl = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
+}
+
+flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int32_t workers,
+                               int32_t cta_group_, flce_backward_plan_info* out) {
+  if (out == nullptr || !sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  const int cg = cta_group_ == 1 || cta_group_ == 2 ? cta_group_ : cta_group();
+  const int w = workers > 0 ? workers : device_workers(cg);
+  const BwdPlan b = plan_backward(N, H, V, chunk_rows, w, BM * cg);
+  out->rows_per_block = b.R;
+  out->vocab_per_slab = b.Vs;
+  out->row_blocks = ceil_div(std::max<int64_t>(N, 1), b.R);
+  out->vocab_slabs = b.n_slabs;
+  out->dh_splits = b.dh_splits;
+  out->dlogits_bytes = b.R * b.ldD * 2;
+  out->workspace_bytes = static_cast<int64_t>(bwd_layout(N, H, b).total);
+  return FLCE_OK;
 }
 
 flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
@@ -1045,7 +1203,7 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
   if (s != FLCE_OK) return s;
   uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
   uint16_t* Dbuf = reinterpret_cast<uint16_t*>(wb + L.D);
-  float* dh_part = b.dh_splits > 1 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
+  float* dh_part = b.dh_f32 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
 
   if (validate_env()) {
     int* bad = reinterpret_cast<int*>(wb + L.bad);
@@ -1124,9 +1282,13 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
       return FLCE_ERR_CUDA;
   }
 
-  const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH, dW, &W_mn, &dW_map};
-  int chunk = 0;
-  for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
+  CUtensorMap dhp_map;
+  if (dH && b.dh_f32 &&
+      !make_map_t(&dhp_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dh_part, H, b.dh_splits * b.R, H, 32, 32))
+    return FLCE_ERR_CUDA;
+  const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH, dW, &W_mn, &dW_map, &dhp_map};
+  int block = 0;
+  for (long long row0 = 0; row0 < N; row0 += b.R, ++block) {
     // rows: exact (plain) or the capacity whose live part the kernels read (compacted)
     const int rows = compact ? static_cast<int>(b.R) : static_cast<int>(std::min(b.R, N - row0));
     GemmParams p = base;
@@ -1145,23 +1307,6 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
     }
     const CUtensorMap& A_dl = compact ? hc_k : h_k;
     const CUtensorMap& B_dw = compact ? hc_mn : h_mn;
-    // (1) recompute logits, dlogits chunk -> D[rows, ldD] bf16
-    {
-      GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
-      q.n_tiles = static_cast<int>(ceil_div(V, BN));
-      q.k_blocks = static_cast<int>(ceil_div(H, BK));
-      q.cols = q.n_tiles;
-      q.n_per_unit = 1;
-      q.kb_per_split = q.k_blocks;
-      q.k_splits = 1;
-      q.num_units = q.m_tiles * q.n_tiles;
-      // 16 row tiles per W run in L2 (16K x 4096 x 151,936: DRAM reads 1.9 GB
-      // per chunk at 16 against 3.5 GB at 8)
-      q.group_m = std::min(16, q.m_tiles);
-      ProfScope ps(K_DLOGITS, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, A_dl, W_k, W_k, q, std::min(q.num_units, workers), st));
-    }
     CUtensorMap D_k, D_mn;
     if (compact) {
       D_k = Dfix_k;
@@ -1170,12 +1315,33 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
                !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK)) {
       return FLCE_ERR_CUDA;
     }
-    // (2) dH[rows] = D W, (3) dW (+)= D^T h[rows]
-    {
-      const flce_status s2 = chunk_dh_dw(dhdw, p, rows, chunk, D_k, D_mn, B_dw, compact ? cidx : nullptr,
-                                         compact ? ccount : nullptr, static_cast<int>(row0), st);
+    for (int slab = 0; slab < b.n_slabs; ++slab) {
+      const int v0 = static_cast<int>(slab * b.Vs);
+      const int width = static_cast<int>(std::min<long long>(b.Vs, V - v0));
+      {  // (1) recompute the slab's logits, dlogits -> D[rows, 0:width] bf16
+        GemmParams q = p;
+        q.v0 = v0;
+        q.m_tiles = static_cast<int>(ceil_div(rows, tm));
+        q.n_tiles = static_cast<int>(ceil_div(width, BN));
+        q.k_blocks = static_cast<int>(ceil_div(H, BK));
+        q.cols = q.n_tiles;
+        q.n_per_unit = 1;
+        q.kb_per_split = q.k_blocks;
+        q.k_splits = 1;
+        q.num_units = q.m_tiles * q.n_tiles;
+        // 16 row tiles per W run in L2 (16K x 4096 x 151,936: DRAM reads 1.9 GB
+        // per 4096-row block at 16 against 3.5 GB at 8)
+        q.group_m = std::min(16, q.m_tiles);
+        ProfScope ps(K_DLOGITS, st);
+        FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, A_dl, W_k, W_k, q, std::min(q.num_units, workers), st));
+      }
+      // (2) dH[rows] (+)= D W[slab], (3) dW[slab] (+)= D^T h[rows]
+      const flce_status s2 = slab_dh_dw(dhdw, p, rows, block, slab, v0, width, D_k, D_mn, B_dw, st);
       if (s2 != FLCE_OK) return s2;
     }
+    const flce_status s3 = block_dh_finish(dhdw, p.row0, rows, compact ? cidx : nullptr,
+                                           compact ? ccount : nullptr, static_cast<int>(row0), st);
+    if (s3 != FLCE_OK) return s3;
   }
   return FLCE_OK;
 }
@@ -1430,7 +1596,7 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
   if (s != FLCE_OK) return s;
   uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
   uint16_t* Dbuf = reinterpret_cast<uint16_t*>(wb + L.D);
-  float* dh_part = b.dh_splits > 1 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
+  float* dh_part = b.dh_f32 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
   int* err = nullptr;
   FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
   CUtensorMap hs_k, Ws_k, ht_k, Wt_k, Ws_mn, hs_mn, dW_map;
@@ -1471,34 +1637,45 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
   base.tf_b = tfp.tf_b;
   base.tf_d = tfp.tf_d;
 
-  const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH_s, dW_s, &Ws_mn, &dW_map};
-  int chunk = 0;
-  for (long long row0 = 0; row0 < N; row0 += b.R, ++chunk) {
+  CUtensorMap dhp_map;
+  if (dH_s && b.dh_f32 &&
+      !make_map_t(&dhp_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dh_part, H, b.dh_splits * b.R, H, 32, 32))
+    return FLCE_ERR_CUDA;
+  const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH_s, dW_s, &Ws_mn, &dW_map, &dhp_map};
+  int block = 0;
+  for (long long row0 = 0; row0 < N; row0 += b.R, ++block) {
     const int rows = static_cast<int>(std::min(b.R, N - row0));
     GemmParams p = base;
     p.row0 = static_cast<int>(row0);
     p.rows = rows;
-    {  // (1) student and teacher logits, distillation dlogits -> D
-      GemmParams q = p;
-      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
-      q.n_tiles = static_cast<int>(ceil_div(V, BN));
-      q.k_blocks = kbs + kbt;
-      q.cols = q.n_tiles;
-      q.n_per_unit = 1;
-      q.kb_per_split = kbs + kbt;
-      q.k_splits = 1;
-      q.num_units = q.m_tiles * q.n_tiles;
-      q.group_m = std::min(16, q.m_tiles);
-      ProfScope prof(K_KD_DLOGITS, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
-                                                 std::min(q.num_units, workers), st, &ht_k, &Wt_k));
-    }
     CUtensorMap D_k, D_mn;
     if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) ||
         !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
       return FLCE_ERR_CUDA;
-    const flce_status s2 = chunk_dh_dw(dhdw, p, rows, chunk, D_k, D_mn, hs_mn, nullptr, nullptr, 0, st);
-    if (s2 != FLCE_OK) return s2;
+    for (int slab = 0; slab < b.n_slabs; ++slab) {
+      const int v0 = static_cast<int>(slab * b.Vs);
+      const int width = static_cast<int>(std::min<long long>(b.Vs, V - v0));
+      {  // (1) student and teacher logits of the slab, distillation dlogits -> D
+        GemmParams q = p;
+        q.v0 = v0;
+        q.m_tiles = static_cast<int>(ceil_div(rows, tm));
+        q.n_tiles = static_cast<int>(ceil_div(width, BN));
+        q.k_blocks = kbs + kbt;
+        q.cols = q.n_tiles;
+        q.n_per_unit = 1;
+        q.kb_per_split = kbs + kbt;
+        q.k_splits = 1;
+        q.num_units = q.m_tiles * q.n_tiles;
+        q.group_m = std::min(16, q.m_tiles);
+        ProfScope prof(K_KD_DLOGITS, st);
+        FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
+                                                   std::min(q.num_units, workers), st, &ht_k, &Wt_k));
+      }
+      const flce_status s2 = slab_dh_dw(dhdw, p, rows, block, slab, v0, width, D_k, D_mn, hs_mn, st);
+      if (s2 != FLCE_OK) return s2;
+    }
+    const flce_status s3 = block_dh_finish(dhdw, p.row0, rows, nullptr, nullptr, 0, st);
+    if (s3 != FLCE_OK) return s3;
   }
   return FLCE_OK;
 }

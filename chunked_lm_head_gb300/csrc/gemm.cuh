@@ -137,6 +137,12 @@ struct GemmParams {
   // e4m3 forward: logits = acc * a_scale[row] * b_scale[vocabulary row]
   const float* a_scale;
   const float* b_scale;
+  // Vocabulary slab of a backward pass: logit columns [v0, v0 + width) held
+  // in D at local columns [0, width).  0 in the forward modes.
+  int v0;
+  // DH into fp32 partials (through tmC): reduce-add onto the previous slabs'
+  // sums, else a plain store
+  int dh_accumulate;
 };
 
 // Problem extents that depend on the device-side row count of a compacted pass.
@@ -252,18 +258,18 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
     const bool teacher = kb >= p.k_blocks_s;
     const int kk = teacher ? kb - p.k_blocks_s : kb;
     tma_ld<MODE, CG>(sA, teacher ? tA2 : tA, bar, kk * BK, p.row0 + a0);
-    tma_ld<MODE, CG>(sB, teacher ? tB2 : tB, bar, kk * BK, b0);
+    tma_ld<MODE, CG>(sB, teacher ? tB2 : tB, bar, kk * BK, p.v0 + b0);
   } else if constexpr (MODE == MODE_FWD || MODE == MODE_DLOGITS) {
     // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x B_ROWS)
     tma_ld<MODE, CG>(sA, tA, bar, kb * BK, p.row0 + a0);
-    tma_ld<MODE, CG>(sB, tB, bar, kb * BK, b0);
+    tma_ld<MODE, CG>(sB, tB, bar, kb * BK, p.v0 + b0);
   } else if constexpr (MODE == MODE_DH) {
-    // A = D rows of this chunk (K-major over the vocabulary), B = W with the
-    // hidden dimension contiguous (MN-major): 64-wide boxes
+    // A = D rows of this chunk (K-major over the slab's vocabulary), B = W
+    // with the hidden dimension contiguous (MN-major): 64-wide boxes
     tma_ld<MODE, CG>(sA, tA, bar, kb * BK, a0);
 #pragma unroll
     for (int j = 0; j < C::B_ROWS / 64; ++j)
-      tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, kb * BK);
+      tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, p.v0 + kb * BK);
   } else {
     // A = D^T (vocabulary contiguous: MN-major), B = h (hidden contiguous:
     // MN-major); K runs over the chunk's rows
@@ -615,7 +621,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           } else if constexpr (MODE == MODE_DLOGITS) {
             uint32_t pk[16];
-            const long long tjl = tgt - col0;
+            const int gcol0 = p.v0 + col0;  // vocabulary column of D's local column col0
+            const long long tjl = tgt - gcol0;
             const int tj = (tjl >= 0 && tjl < 32) ? static_cast<int>(tjl) : -1;
             if (!p.tf_softcap) {
 #pragma unroll
@@ -626,8 +633,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   float p1 = ex2_approx(fmaf(v[j + 1], l2a, nl2));
                   if (j == tj) p0 -= 1.f;
                   if (j + 1 == tj) p1 -= 1.f;
-                  d0 = (col0 + j < p.V) ? p0 * scale_a : 0.f;
-                  d1 = (col0 + j + 1 < p.V) ? p1 * scale_a : 0.f;
+                  d0 = (gcol0 + j < p.V) ? p0 * scale_a : 0.f;
+                  d1 = (gcol0 + j + 1 < p.V) ? p1 * scale_a : 0.f;
                 }
                 pk[j / 2] = pack_bf16x2(d0, d1);
               }
@@ -642,8 +649,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   float p1 = ex2_approx(fmaf(p.tf_b * t1, kLog2e, nl2));
                   if (j == tj) p0 -= 1.f;
                   if (j + 1 == tj) p1 -= 1.f;
-                  d0 = (col0 + j < p.V) ? p0 * scale * p.tf_d * (1.f - t0 * t0) : 0.f;
-                  d1 = (col0 + j + 1 < p.V) ? p1 * scale * p.tf_d * (1.f - t1 * t1) : 0.f;
+                  d0 = (gcol0 + j < p.V) ? p0 * scale * p.tf_d * (1.f - t0 * t0) : 0.f;
+                  d1 = (gcol0 + j + 1 < p.V) ? p1 * scale * p.tf_d * (1.f - t1 * t1) : 0.f;
                 }
                 pk[j / 2] = pack_bf16x2(d0, d1);
               }
@@ -709,6 +716,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             float vt[32];
             tmem_ld32(tbase + BN + c * 32, vt);
             uint32_t pk[16];
+            const int gcol0 = p.v0 + col0;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
               float d[2] = {0.f, 0.f};
@@ -726,7 +734,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const float pt = ex2_approx(fmaf(p.tf_b * tanhf(p.tf_a * vt[j + e]), kLog2e, nlt));
                     de = (ps - pt) * scale * p.tf_d * (1.f - ts * ts);
                   }
-                  d[e] = (col0 + j + e < p.V) ? de : 0.f;
+                  d[e] = (gcol0 + j + e < p.V) ? de : 0.f;
                 }
               }
               pk[j / 2] = pack_bf16x2(d[0], d[1]);
@@ -739,30 +747,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   *reinterpret_cast<uint4*>(dst + 8 * g) =
                       make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
             }
-          } else if constexpr (MODE == MODE_DH) {
-            if (row_ok) {
-              if (p.dH_part == nullptr) {
-                uint16_t* dst = p.dH + static_cast<idx_t>(grow) * p.H + col0;
+          } else if (MODE == MODE_DH && p.dH_part == nullptr) {
+            if (row_ok) {  // the only pass over this row: bf16 dH directly
+              uint16_t* dst = p.dH + static_cast<idx_t>(grow) * p.H + col0;
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                  if (col0 + 8 * g < p.H)
-                    *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(
-                        pack_bf16x2(v[8 * g], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
-                        pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
-              } else {
-                float* dst = p.dH_part + (static_cast<idx_t>(t.split) * p.rows_cap + lr) * p.H + col0;
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                  if (col0 + 4 * g < p.H)
-                    *reinterpret_cast<float4*>(dst + 4 * g) =
-                        make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-              }
+              for (int g = 0; g < 4; ++g)
+                if (col0 + 8 * g < p.H)
+                  *reinterpret_cast<uint4*>(dst + 8 * g) = make_uint4(
+                      pack_bf16x2(v[8 * g], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                      pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
             }
-          } else {  // MODE_DW
+          } else {  // MODE_DW, or MODE_DH into fp32 partials
             // stage this warp's 32 x 32 box (row = lane) in 128B-swizzled
             // shared memory, then one lane hands it to TMA: a plain store on
-            // the first row chunk, an fp32 reduce-add in L2 afterwards.  Rows
-            // and columns outside dW are clipped by TMA.
+            // the first pass over the output, an fp32 reduce-add in L2
+            // afterwards.  Columns past H and dW rows past V are clipped by
+            // TMA; boxes wholly outside the output are skipped.
             const uint32_t box = out_stage + (warp - 2) * (2 * OUT_BOX_BYTES) + (c & 1) * OUT_BOX_BYTES;
             if (lane == 0) bulk_wait_read<1>();  // the copy that last used this box has read it
             __syncwarp();
@@ -774,12 +774,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              const int vrow0 = t.m * C::TM + rank * BM + q * 32;
-              if (col0 < p.H && vrow0 < p.V) {  // boxes wholly outside dW are skipped
-                if (p.dW_accumulate)
-                  tma_reduce_add_2d(&tmC, box, col0, vrow0);
+              const int lrow0 = t.m * C::TM + rank * BM + q * 32;  // first accumulator row of the box
+              int oy;
+              bool inside, accumulate;
+              if constexpr (MODE == MODE_DW) {
+                oy = p.v0 + lrow0;  // vocabulary row of dW
+                inside = oy < p.V;
+                accumulate = p.dW_accumulate != 0;
+              } else {
+                // partial sums of k-split t.split: rows [split * rows_cap, +rows_cap)
+                oy = t.split * p.rows_cap + lrow0;
+                inside = lrow0 < p.rows_cap;
+                accumulate = p.dh_accumulate != 0;
+              }
+              if (col0 < p.H && inside) {
+                if (accumulate)
+                  tma_reduce_add_2d(&tmC, box, col0, oy);
                 else
-                  tma_store_2d(&tmC, box, col0, vrow0);
+                  tma_store_2d(&tmC, box, col0, oy);
               }
               bulk_commit();
             }
@@ -813,8 +825,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
-  if constexpr (MODE == MODE_DW) {
-    if (warp >= 2 && lane == 0) bulk_wait_all();  // dW boxes written before the CTA retires
+  if constexpr (MODE == MODE_DW || MODE == MODE_DH) {
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // output boxes written before the CTA retires
   }
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // neither CTA retires while its peer may still signal it

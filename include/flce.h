@@ -151,12 +151,16 @@ FLCE_API flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, con
  *            skip the dH GEMM.
  *   dW       [V,H] fp32 output (overwritten), or NULL to skip the dW GEMM
  *            (frozen lm_head).
- *   chunk_rows  rows whose dlogits are held at once: the backward walks the
- *            rows in chunks of R = chunk_rows rounded up to 128, keeping one
- *            bf16 dlogits chunk [R, V] (plus, for small chunks, split-K
- *            partials of dH [splits, R, H] fp32) in the workspace: extra memory
- *            O(chunk_rows * V), never O(N * V).  Results do not depend on it
- *            beyond fp32 summation order of dW across chunks.
+ *   chunk_rows  the dlogits memory bound: the workspace holds at most
+ *            C x V bf16 dlogits, C = chunk_rows rounded up to 128 (plus dH
+ *            fp32 partials and gathered rows, together no larger): extra
+ *            memory O(chunk_rows * V), never O(N * V).  Within that bound the
+ *            backward walks blocks of R >= C rows and, inside each block,
+ *            vocabulary slabs of Vs columns with R * Vs <= C * V, choosing R
+ *            by a time model (flce_backward_plan); dW is read-modified-
+ *            written once per row block, and dH is summed over the slabs in
+ *            fp32 and rounded to bf16 once.  Results do not depend on
+ *            chunk_rows beyond fp32 summation order.
  * Other arguments as in flce_forward.  Rows with an out-of-range target get
  * D = softmax * w * g (no one-hot term); FLCE_VALIDATE=1 rejects them.
  */
@@ -281,6 +285,27 @@ FLCE_API flce_status flce_forward_static_scratch(const flce_bf16* h, const flce_
                                                  int64_t ignore_index, float* out_logp,
                                                  float* out_lse, float* out_loss,
                                                  int64_t* out_n_valid, void* stream);
+
+/* The backward's tiling for these sizes (host-only; no device is touched).
+ * Output of flce_backward_plan. */
+typedef struct flce_backward_plan_info {
+  int64_t rows_per_block;   /* R: rows whose dlogits are held at once */
+  int64_t vocab_per_slab;   /* Vs: vocabulary columns per slab (V when one slab) */
+  int64_t row_blocks;       /* ceil(N / R) */
+  int64_t vocab_slabs;      /* ceil(V / Vs) */
+  int64_t dh_splits;        /* k-splits of the dH GEMM (fp32 partial sets) */
+  int64_t dlogits_bytes;    /* bytes of the dlogits block: R * row pitch * 2 */
+  int64_t workspace_bytes;  /* flce_backward's whole workspace for these sizes */
+} flce_backward_plan_info;
+
+/* Backward tiling that flce_backward uses for N, H, V, chunk_rows on a GPU
+ * that holds `workers` persistent tile workers (CTAs for cta_group 1, CTA
+ * pairs for cta_group 2; 148 SMs give 148 or 74).  workers <= 0 or
+ * cta_group == 0: query the current device and the FLCE_CTA_GROUP setting.
+ * FLCE_ERR_INVALID_ARG on invalid sizes or a NULL out. */
+FLCE_API flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                                        int32_t workers, int32_t cta_group,
+                                        flce_backward_plan_info* out);
 
 /* Workspace bytes that both flce_forward and flce_backward need for these
  * sizes on the current device (0 on invalid sizes).  Host-only; if no device

@@ -30,15 +30,67 @@ def test_status_strings(lib):
 
 
 def test_workspace_size_is_chunk_bounded(lib):
-    # dlogits chunk R x V bf16 dominates; growing N at fixed chunk must not grow it
-    # beyond the O(N) forward partials.
+    # the dlogits block (at most round_up(chunk, 128) x V bf16) plus dH partials
+    # and gathered rows (together no larger) dominate; growing N at a fixed
+    # chunk adds only O(N) bytes (per-row split partials, row indices)
     V, H = 151936, 4096
-    a = _lib.flce_workspace_bytes(16384, H, V, 4096)
-    b = _lib.flce_workspace_bytes(131072, H, V, 4096)
-    assert a >= 4096 * V * 2
-    assert b - a < 131072 * 8 * 64  # at most O(N) growth (per-row split partials)
-    assert b < 131072 * V * 2 / 8  # far below the full bf16 logits
-    assert _lib.flce_workspace_bytes(-1, H, V, 256) == 0
+    for chunk in (256, 4096):
+        d_bound = ((chunk + 127) // 128 * 128) * V * 2
+        sizes = [_lib.flce_workspace_bytes(n, H, V, chunk) for n in (16384, 131072, 1 << 20)]
+        assert sizes[0] >= d_bound // 2
+        for n, ws in zip((16384, 131072, 1 << 20), sizes):
+            assert ws <= 2 * d_bound + (256 << 20) + 64 * n, (chunk, n, ws)
+            assert ws < n * V * 2 * (chunk * 4 / n)  # a fraction of the full bf16 logits
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 1000, 16), (256, 2048, 248320, 256),
+                                   (16384, 4096, 151936, 256), (16384, 4096, 151936, 4096),
+                                   (32768, 4096, 128000, 4096), (131072, 2560, 151936, 256),
+                                   (3000, 512, 20000, 256), (2000, 256, 30011, 128),
+                                   (5, 8, 3, 1), (100000, 8, 7, 100000)])
+@pytest.mark.parametrize("workers,cg", [(74, 2), (148, 1), (76, 2), (1, 2)])
+def test_backward_plan_covers_the_problem_within_the_chunk_budget(shape, workers, cg):
+    N, H, V, chunk = shape
+    p = _lib.flce_backward_plan(N, H, V, chunk, workers, cg)
+    c = min((chunk + 127) // 128 * 128, (N + 127) // 128 * 128)
+    budget = c * ((V + 7) // 8 * 8) * 2
+    assert p["dlogits_bytes"] <= budget
+    assert p["rows_per_block"] % 128 == 0 and p["rows_per_block"] >= c
+    assert p["row_blocks"] == -(-N // p["rows_per_block"])
+    assert p["vocab_slabs"] * p["vocab_per_slab"] >= V
+    if p["vocab_slabs"] > 1:
+        assert p["vocab_per_slab"] % 256 == 0
+        assert (p["vocab_slabs"] - 1) * p["vocab_per_slab"] < V  # no empty slab
+    else:
+        assert p["vocab_per_slab"] == V
+    assert 1 <= p["dh_splits"] <= 16
+    assert p["workspace_bytes"] <= 2 * budget + 16 * N + (1 << 20)
+
+
+def test_backward_plan_prefers_row_blocks_over_literal_small_chunks():
+    # 131,072 x 2,560 x 151,936 at 256-row chunks: dW is read-modified-written
+    # once per row block, so the plan must hold many more than 256 rows
+    p = _lib.flce_backward_plan(131072, 2560, 151936, 256, 74, 2)
+    assert p["rows_per_block"] >= 1024 and p["vocab_slabs"] > 1
+    # a chunk that already holds the whole problem stays one block, one slab
+    q = _lib.flce_backward_plan(256, 2048, 248320, 256, 74, 2)
+    assert (q["row_blocks"], q["vocab_slabs"]) == (1, 1)
+
+
+def test_backward_plan_row_override(monkeypatch):
+    monkeypatch.setenv("FLCE_BWD_ROWS", "768")
+    p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
+    assert (p["rows_per_block"], p["vocab_per_slab"], p["row_blocks"], p["vocab_slabs"]) == (768, 5120, 4, 4)
+    monkeypatch.setenv("FLCE_BWD_ROWS", "100000")  # clamped to the problem, then to the budget
+    p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
+    assert p["dlogits_bytes"] <= 256 * 20000 * 2 and p["rows_per_block"] <= 3072
+
+
+def test_backward_plan_rejects_bad_arguments(lib):
+    info = _lib.BackwardPlanInfo()
+    assert lib.flce_backward_plan(-1, 64, 100, 16, 74, 2, ctypes.addressof(info)) == 1
+    assert lib.flce_backward_plan(10, 64, 0, 16, 74, 2, ctypes.addressof(info)) == 1
+    assert lib.flce_backward_plan(10, 64, 100, 16, 74, 2, None) == 1
 
 
 def test_forward_rejects_bad_arguments_before_any_launch(lib):

@@ -31,6 +31,23 @@ CASES = [
 @pytest.mark.parametrize("cg", ["1", "2"])
 def test_kd_parity(case, cg, monkeypatch):
     monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    _kd_check(case)
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_kd_parity_row_blocks_and_vocabulary_slabs(cg, monkeypatch):
+    """Distillation backward over 512-row blocks x 1,280-column vocabulary
+    slabs (3 blocks, the last 76 rows; 5 slabs, the last 880 columns) inside a
+    128-row dlogits budget."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    monkeypatch.setenv("FLCE_BWD_ROWS", "512")
+    case = (1100, 256, 384, 6000, 128, {"temperature": 1.3}, True)
+    plan = flce._lib.flce_backward_plan(case[0], case[1], case[3], case[4])
+    assert (plan["row_blocks"], plan["vocab_slabs"], plan["vocab_per_slab"]) == (3, 5, 1280)
+    _kd_check(case)
+
+
+def _kd_check(case):
     N, Hs, Ht, V, chunk, tfd, masked = case
     si, ti = _heads(N, Hs, Ht, V, seed=601 + N)
     targets = None

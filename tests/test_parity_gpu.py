@@ -282,3 +282,47 @@ def test_forward_independent_of_vocabulary_splits(splits, monkeypatch):
     assert loss1 == pytest.approx(loss0, rel=1e-6)
     ref = O.forward(inp.h, inp.W, inp.targets)
     assert_logp_close(np64(logp1), ref.logp, "logp")
+
+
+@pytest.mark.parametrize("compact", ["0", "1"])
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_backward_row_blocks_and_vocabulary_slabs(cg, compact, monkeypatch):
+    """A 256-row dlogits budget walked as 768-row blocks x 5,120-column
+    vocabulary slabs: 4 row blocks (the last 696 rows) x 4 slabs (the last
+    4,640 columns), dH summed over the slabs in fp32 partials, dW
+    read-modified-written once per row block; with and without row compaction,
+    on both CTA-group paths."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    monkeypatch.setenv("FLCE_COMPACT", compact)
+    monkeypatch.setenv("FLCE_BWD_ROWS", "768")
+    N, H, V, cr = 3000, 512, 20000, 256
+    plan = _lib.flce_backward_plan(N, H, V, cr)
+    assert (plan["rows_per_block"], plan["vocab_per_slab"]) == (768, 5120)
+    assert (plan["row_blocks"], plan["vocab_slabs"]) == (4, 4)
+    assert plan["dlogits_bytes"] <= 256 * V * 2
+    wl = WL.custom(f"slabs{cg}{compact}", N, H, V, cr, w_std=0.04, targets="zipf", ignore_frac=0.08,
+                   seed=113)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(12).standard_normal(N).astype(np.float32)
+    _full_check(inp, cr)
+
+
+def test_backward_default_plan_odd_vocabulary():
+    """The planner's own choice for a small chunk budget and an odd V (row
+    pitch of D a multiple of 256, W rows of odd count) against the oracle,
+    and bitwise repeatable."""
+    N, H, V, cr = 2000, 256, 30011, 128
+    plan = _lib.flce_backward_plan(N, H, V, cr)
+    assert plan["dlogits_bytes"] <= 128 * (V + 5) * 2
+    assert plan["row_blocks"] * plan["rows_per_block"] >= N
+    assert plan["vocab_slabs"] * plan["vocab_per_slab"] >= V
+    wl = WL.custom("oddv", N, H, V, cr, w_std=0.04, targets="zipf", ignore_frac=0.05, seed=114)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, cr)
+    dH, dW = run_backward(h, W, t, w, lse, 1.0 / nv, cr)
+    dH2, dW2 = run_backward(h, W, t, w, lse, 1.0 / nv, cr)
+    assert torch.equal(dH, dH2) and torch.equal(dW, dW2)
+    ref = O.backward(inp.h, inp.W, inp.targets, None, g=1.0 / nv)
+    assert_grad_close(np64(dH), ref.dH, "dH")
+    assert_grad_close(np64(dW), ref.dW, "dW")

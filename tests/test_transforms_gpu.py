@@ -45,6 +45,30 @@ def test_transform_parity(name, cg, monkeypatch):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_transform_parity_row_blocks_and_vocabulary_slabs(cg, monkeypatch):
+    """Soft-cap + temperature through the backward's 512-row blocks x
+    1,280-column vocabulary slabs (128-row dlogits budget; last slab 880
+    columns, last block 76 rows)."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    monkeypatch.setenv("FLCE_BWD_ROWS", "512")
+    tfd = CASES["softcap_temp"]
+    tf = O.LogitTransform(**tfd)
+    N, H, V = 1100, 192, 6000
+    plan = _lib.flce_backward_plan(N, H, V, 128)
+    assert (plan["row_blocks"], plan["vocab_slabs"], plan["vocab_per_slab"]) == (3, 5, 1280)
+    wl = WL.custom("tf_slabs", N, H, V, 128, w_std=0.25, targets="zipf", ignore_frac=0.05, seed=303)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, 128, transform=tfd)
+    g = 1.0 / nv
+    dH, dW = run_backward(h, W, t, w, lse, g, 128, transform=tfd)
+    refb = O.backward(inp.h, inp.W, inp.targets, None, g=g, tf=tf)
+    assert_grad_close(np64(dH), refb.dH, "dH")
+    assert_grad_close(np64(dW), refb.dW, "dW")
+
+
+@pytest.mark.gpu
 def test_identity_transform_is_bitwise_the_plain_path():
     wl = WL.custom("tf_id", 300, 128, 1500, 128, seed=302)
     inp = WL.make_inputs(wl)
