@@ -430,7 +430,10 @@ struct FwdPlan {
 // Split the vocabulary tiles of every row tile (tm rows) into S contiguous
 // ranges so that (row tiles x S) units fill the persistent workers in
 // near-whole waves.
-FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm) {
+constexpr size_t kFwdPartialsCap = size_t(256) << 20;
+
+FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm,
+                     size_t partials_cap = kFwdPartialsCap) {
   FwdPlan f;
   f.m_tiles = static_cast<int>(ceil_div(N, tm));
   f.n_tiles = static_cast<int>(ceil_div(V, BN));
@@ -438,8 +441,9 @@ FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm)
   f.nblk = static_cast<int>(ceil_div(N, SMALL_THREADS));
   long long best = LLONG_MAX;
   // at most 256 splits, and split partials (8 bytes per row and split) of
-  // at most 256 MiB
-  const long long s_mem = std::max(1LL, (256LL << 20) / (8 * std::max(1LL, N)));
+  // at most partials_cap bytes
+  const long long s_mem =
+      std::max(1LL, static_cast<long long>(partials_cap) / (8 * std::max(1LL, N)));
   const int smax = static_cast<int>(std::min<long long>(std::min(f.n_tiles, 256), s_mem));
   for (int s = 1; s <= smax; ++s) {
     const int tps = static_cast<int>(ceil_div(f.n_tiles, s));
@@ -455,7 +459,7 @@ FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm)
   // FLCE_FWD_SPLITS=s pins the number of vocabulary splits (tests compare
   // split counts; results must not depend on them beyond fp32 rounding)
   if (const char* e = std::getenv("FLCE_FWD_SPLITS")) {
-    const int want = std::max(1, std::min(std::atoi(e), f.n_tiles));
+    const int want = std::max(1, std::min(std::min(std::atoi(e), f.n_tiles), smax));
     f.tps = static_cast<int>(ceil_div(f.n_tiles, want));
     f.S = static_cast<int>(ceil_div(f.n_tiles, f.tps));
   }
@@ -1079,13 +1083,14 @@ flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_ro
   return FLCE_OK;
 }
 
-flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
-                            const float* weights, int64_t N, int64_t H, int64_t V,
-                            int64_t chunk_rows, int64_t ignore_index,
-                            const flce_logit_transform* transform, float* out_logp, float* out_lse,
-                            float* out_loss, int64_t* out_n_valid, void* workspace,
-                            size_t workspace_bytes, void* stream) {
-  (void)chunk_rows;
+// The forward; partials_cap bounds the vocabulary-split partials (8 bytes per
+// row and split) so that a fixed scratch can hold them.
+static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                const float* weights, int64_t N, int64_t H, int64_t V,
+                                int64_t ignore_index, const flce_logit_transform* transform,
+                                float* out_logp, float* out_lse, float* out_loss,
+                                int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                                void* stream, size_t partials_cap) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
@@ -1098,7 +1103,7 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  const FwdPlan f = plan_forward(N, H, V, workers, BM * cg);
+  const FwdPlan f = plan_forward(N, H, V, workers, BM * cg, partials_cap);
   const FwdLayout L = fwd_layout(N, f);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
@@ -1171,6 +1176,17 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
                            out_loss, out_n_valid, bsum, bcnt, st);
   }
   return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
+}
+
+flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                            const float* weights, int64_t N, int64_t H, int64_t V,
+                            int64_t chunk_rows, int64_t ignore_index,
+                            const flce_logit_transform* transform, float* out_logp, float* out_lse,
+                            float* out_loss, int64_t* out_n_valid, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  (void)chunk_rows;
+  return forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, out_lse,
+                      out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap);
 }
 
 flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
@@ -1814,10 +1830,19 @@ extern "C" flce_status flce_forward_static_scratch(const flce_bf16* h, const flc
                                                    int64_t chunk_rows, int64_t ignore_index,
                                                    float* out_logp, float* out_lse, float* out_loss,
                                                    int64_t* out_n_valid, void* stream) {
+  (void)chunk_rows;
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   const int cg = cta_group();
-  const size_t need = fwd_layout(N, plan_forward(N, H, V, device_workers(cg), BM * cg)).total;
-  if (need > kStaticScratchBytes) return FLCE_ERR_UNSUPPORTED;
+  // the vocabulary-split partials get what the array leaves after the
+  // per-row target logits and block sums (fewer splits, same results up to
+  // fp32 rounding of the combine)
+  const FwdPlan f1 = plan_forward(N, H, V, device_workers(cg), BM * cg, 0);  // one split
+  const size_t fixed = fwd_layout(N, f1).total - align256(static_cast<size_t>(std::max<int64_t>(N, 0)) * 8);
+  if (fixed + align256(static_cast<size_t>(std::max<int64_t>(N, 0)) * 8) > kStaticScratchBytes)
+    return FLCE_ERR_UNSUPPORTED;
+  const size_t cap = kStaticScratchBytes - fixed - 256;  // 256: alignment of the partials block
+  if (fwd_layout(N, plan_forward(N, H, V, device_workers(cg), BM * cg, cap)).total > kStaticScratchBytes)
+    return FLCE_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   const flce_status s = static_scratch_address(&scratch);
   if (s != FLCE_OK) return s;
@@ -1825,6 +1850,6 @@ extern "C" flce_status flce_forward_static_scratch(const flce_bf16* h, const flc
   // slots by the prep kernel, partials by the GEMM, block sums by the
   // combine, the validation counter by a memset), so stale contents of an
   // earlier call never leak into the result.
-  return flce_forward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, out_logp, out_lse,
-                      out_loss, out_n_valid, scratch, kStaticScratchBytes, stream);
+  return forward_impl(h, W, targets, weights, N, H, V, ignore_index, nullptr, out_logp, out_lse,
+                      out_loss, out_n_valid, scratch, kStaticScratchBytes, stream, cap);
 }

@@ -266,10 +266,11 @@ FLCE_API flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, 
  * NULL, except that no workspace is allocated: the call uses a 16 MiB scratch
  * array that the library keeps in device memory on every device that loads it,
  * for the life of the process.
- *   - Returns FLCE_ERR_UNSUPPORTED, before any launch, when the forward's
- *     scratch for these sizes exceeds 16 MiB (about N * (4 + 8 * S) bytes with
- *     S <= ceil(V / 256) vocabulary splits; e.g. N = 16,384 at V = 151,936
- *     needs about 2.6 MiB).
+ *   - The forward's scratch is about N * (4 + 8 * S) bytes for S vocabulary
+ *     splits; this call uses as many splits as fit in 16 MiB (results equal
+ *     flce_forward's up to fp32 rounding of the split combine).  It returns
+ *     FLCE_ERR_UNSUPPORTED, before any launch, only when one split does not
+ *     fit: N above about 1.3 million rows.
  *   - The first call on each device looks up the array's device address (a
  *     one-time cudaGetSymbolAddress); make that first call outside any stream
  *     capture.

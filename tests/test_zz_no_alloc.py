@@ -52,8 +52,22 @@ def test_static_scratch_forward_matches_regular_forward_on_consecutive_calls():
         assert loss == pytest.approx(ref_loss, rel=LOSS_RTOL)
 
 
+def test_static_scratch_forward_at_the_16k_sft_shape():
+    """16,384 x 4,096 x 151,936: the regular plan's split partials (26 MB)
+    exceed the 16 MiB array, so this call runs fewer vocabulary splits; the
+    results still equal the regular forward's up to fp32 combine rounding."""
+    inp = WL.make_inputs("sft_16k")
+    h, W, t, w = upload(inp)
+    ref_logp, ref_lse, ref_loss, ref_nv = run_forward(h, W, t, w, 4096)
+    logp, lse, loss, nv = _forward_static(h, W, t, w, 4096)
+    assert nv == ref_nv == 16380
+    assert torch.allclose(lse, ref_lse, atol=2e-5, rtol=0)
+    assert torch.allclose(logp, ref_logp, atol=2e-5, rtol=0)
+    assert loss == pytest.approx(ref_loss, rel=1e-6)
+
+
 def test_static_scratch_forward_rejects_problems_beyond_its_scratch():
     p = 256  # never dereferenced: the size check comes before any launch
-    st = _lib.flce_forward_static_scratch(p, p, p, None, 1 << 22, 64, 151936, 256, -100, p, None,
+    st = _lib.flce_forward_static_scratch(p, p, p, None, 1 << 21, 64, 151936, 256, -100, p, None,
                                           None, None, 0)
     assert st == 3  # FLCE_ERR_UNSUPPORTED
