@@ -319,7 +319,10 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    _lib.profile_enable(True)
+    # per-launch CUDA events inside the timed region (default), or only
+    # around it with the per-kernel events taken in a second pass
+    events_in_timed = args.kernel_events == "timed"
+    _lib.profile_enable(events_in_timed)
     e0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
@@ -328,6 +331,12 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop()
+    if not events_in_timed:
+        _lib.profile_enable(True)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                step()
+        torch.cuda.synchronize(dev)
     prof = _lib.profile_read()
     _lib.profile_enable(False)
     st = _lib.flce_device_status(sh)
@@ -452,6 +461,7 @@ def gpu_arm(args):
                 "value": whole_job_rate(N, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": gpu_launches,
+            "kernel_events": args.kernel_events,
             "peak_extra_mem_bytes": int(extra_mem),
             "workspace_bytes": ws_bytes,
         }
@@ -472,6 +482,9 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of the CPU-oracle sample")
     ap.add_argument("--ref-step-s", type=float, default=8.0, help="reference arm: seconds per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-events", default="timed", choices=["timed", "separate"],
+                    help="per-launch CUDA events inside the timed steps (timed), or in a second "
+                         "pass of the same steps so that the timed steps run without them (separate)")
     ap.add_argument("--transform", default="",
                     help="logit transform, e.g. softcap=30,temperature=0.7 (flce_*_ex path)")
     ap.add_argument("--forward-only", action="store_true",

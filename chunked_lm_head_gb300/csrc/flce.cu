@@ -740,6 +740,46 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer
                     box_outer);
 }
 
+// Programmatic dependent launch of the GEMMs (default; FLCE_PDL=0 turns it
+// off): a GEMM may be scheduled while the previous kernel of the stream
+// drains, runs its prologue (barriers, TMEM, descriptor prefetch) and then
+// waits in griddepcontrol.wait until that kernel has completed.  Each GEMM
+// grid fits on the GPU at once, so the waiting CTAs never hold SMs that the
+// kernel they wait for still needs.
+bool pdl_env() {
+  const char* s = std::getenv("FLCE_PDL");
+  return !(s != nullptr && s[0] == '0');
+}
+
+// Launch on `grid` CTAs in clusters of `cluster` with the GEMMs' attributes.
+template <class Kern, class... Args>
+cudaError_t launch_persistent(Kern k, int grid, int cluster, int smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl_env()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int MODE, bool kLong, int CG>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p,
@@ -748,25 +788,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
   constexpr int smem = TileCfg<CG>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if constexpr (CG == 1) {
-    k<<<workers, GEMM_THREADS, smem, st>>>(a, b, c, a2, b2, p);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * workers, 1, 1);
-    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k, a, b, c, a2, b2, p);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaGetLastError();
+  return launch_persistent(k, CG * workers, CG, smem, st, a, b, c, a2, b2, p);
 }
 
 // `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
@@ -792,21 +814,7 @@ cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUte
   auto go = [&](auto kern, int smem, int grid_mult) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_mult * workers, 1, 1);
-    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = grid_mult;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, a, b, b, a, b, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_persistent(kern, grid_mult * workers, grid_mult, smem, st, a, b, b, a, b, p);
   };
   if (cg == 2)
     return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)

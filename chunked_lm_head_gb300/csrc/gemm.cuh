@@ -387,6 +387,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if constexpr (is_kd<MODE>()) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
   }
   if constexpr (CG == 2) cluster_sync();  // peer barriers exist before any remote signal
   if (warp == 1) {
@@ -402,17 +408,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touches only this CTA's shared memory and TMEM, so it
+  // may overlap the previous kernel's tail; nothing below reads or writes
+  // global memory before that kernel has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const DynShape dsh = dyn_shape<MODE, C::TM>(p);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-      if constexpr (is_kd<MODE>()) {
-        tma_prefetch_desc(&tmA2);
-        tma_prefetch_desc(&tmB2);
-      }
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
