@@ -393,6 +393,108 @@ def kd_backward(hs, Ws, ht, Wt, targets=None, weights=None, g: float = 1.0,
     return Backward(dH, dW)
 
 
+@dataclasses.dataclass
+class JSDForward:
+    jsd: np.ndarray     # [N] m * JSD_beta(p_teacher, p_student)
+    lse_s: np.ndarray   # [N]
+    lse_t: np.ndarray   # [N]
+    kl_sm: np.ndarray   # [N] KL(p_student || mixture) of every row (mask not applied)
+    n_valid: int
+    loss: float
+
+
+def _jsd_rows(zs: np.ndarray, zt: np.ndarray, beta: float):
+    """Per-row generalised Jensen-Shannon divergence of two logit blocks.
+
+    With p_s = softmax(zs), p_t = softmax(zt) and the mixture
+    M = beta * p_t + (1 - beta) * p_s:
+        JSD_beta = beta * KL(p_t || M) + (1 - beta) * KL(p_s || M),
+    terms with a zero probability contribute 0 (x log x -> 0).  Returns
+    (jsd, KL(p_s || M), lse_s, lse_t, p_s, M)."""
+    ls, lt = logsumexp_rows(zs), logsumexp_rows(zt)
+    log_ps, log_pt = zs - ls[:, None], zt - lt[:, None]
+    ps, pt = np.exp(log_ps), np.exp(log_pt)
+    mix = beta * pt + (1.0 - beta) * ps
+    with np.errstate(divide="ignore", invalid="ignore"):
+        log_mix = np.log(mix)
+        kl_t = np.sum(np.where(pt > 0, pt * (log_pt - log_mix), 0.0), axis=1)
+        kl_s = np.sum(np.where(ps > 0, ps * (log_ps - log_mix), 0.0), axis=1)
+    return beta * kl_t + (1.0 - beta) * kl_s, kl_s, ls, lt, ps, log_mix
+
+
+def _check_beta(beta: float) -> float:
+    beta = float(beta)
+    if not (0.0 < beta < 1.0):
+        raise ValueError("beta must lie strictly between 0 and 1")
+    return beta
+
+
+def jsd_forward(hs, Ws, ht, Wt, beta: float = 0.5, targets=None, weights=None,
+                ignore_index: int = IGNORE_INDEX, tf: LogitTransform | None = None,
+                chunk_rows: int | None = None) -> JSDForward:
+    """Jensen-Shannon distillation of a teacher head into a student head.
+
+    TRL v1.13 article, section "Other changes in v1.13": TRL's fused linear
+    losses include a JSD loss next to DPO, KTO and GRPO; the page gives no
+    formula.  Reading taken: the generalised Jensen-Shannon divergence with
+    mixture weight beta in (0, 1) (beta = 1/2 is the textbook JSD), per
+    token, masked by ignore_index rows of ``targets`` (all rows when None),
+    weighted and averaged like the cross-entropy; loss = sum(m w jsd) /
+    sum(m).  Both heads pass through the same logit transform.
+    """
+    beta = _check_beta(beta)
+    hsf, Wsf, htf, Wtf = widen(hs), widen(Ws), widen(ht), widen(Wt)
+    N = hsf.shape[0]
+    m = _kd_mask(targets, N, ignore_index)
+    w = _weights(weights, N)
+    step = N if chunk_rows is None else max(1, int(chunk_rows))
+    jsd, kl_sm, lse_s, lse_t = np.zeros(N), np.zeros(N), np.zeros(N), np.zeros(N)
+    for r0 in range(0, N, step):
+        r1 = min(N, r0 + step)
+        zs = _tf(hsf[r0:r1] @ Wsf.T, tf)
+        zt = _tf(htf[r0:r1] @ Wtf.T, tf)
+        j, ksm, ls, lt, _, _ = _jsd_rows(zs, zt, beta)
+        jsd[r0:r1] = np.where(m[r0:r1], j, 0.0)
+        kl_sm[r0:r1], lse_s[r0:r1], lse_t[r0:r1] = ksm, ls, lt
+    n_valid = int(m.sum())
+    loss = float(np.sum(m * w * jsd)) / n_valid if n_valid > 0 else 0.0
+    return JSDForward(jsd, lse_s, lse_t, kl_sm, n_valid, loss)
+
+
+def jsd_backward(hs, Ws, ht, Wt, beta: float = 0.5, targets=None, weights=None, g: float = 1.0,
+                 ignore_index: int = IGNORE_INDEX, tf: LogitTransform | None = None,
+                 chunk_rows: int | None = None) -> Backward:
+    """Student gradients of the JSD distillation loss (teacher frozen).
+
+    JSD_beta = beta sum p_t log p_t + (1 - beta) sum p_s log p_s - sum M log M,
+    so dJSD/dp_s[v] = (1 - beta) log(p_s[v] / M[v]); through the softmax,
+        D[v] = (1 - beta) p_s[v] (log(p_s[v] / M[v]) - KL(p_s || M)) * m w g * f'(z_s[v]),
+    then dH = D Ws and dW = D^T hs."""
+    beta = _check_beta(beta)
+    hsf, Wsf, htf, Wtf = widen(hs), widen(Ws), widen(ht), widen(Wt)
+    N = hsf.shape[0]
+    m = _kd_mask(targets, N, ignore_index)
+    w = _weights(weights, N)
+    step = N if chunk_rows is None else max(1, int(chunk_rows))
+    dH = np.zeros_like(hsf)
+    dW = np.zeros_like(Wsf)
+    for r0 in range(0, N, step):
+        r1 = min(N, r0 + step)
+        z = hsf[r0:r1] @ Wsf.T
+        zs = _tf(z, tf)
+        zt = _tf(htf[r0:r1] @ Wtf.T, tf)
+        _, kl_s, ls, _, ps, log_mix = _jsd_rows(zs, zt, beta)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            g_s = np.where(ps > 0, (zs - ls[:, None]) - log_mix, 0.0)
+        D = (1.0 - beta) * ps * (g_s - kl_s[:, None])
+        D *= (m[r0:r1] * w[r0:r1] * g)[:, None]
+        if tf is not None:
+            D *= tf.grad(z)
+        dH[r0:r1] = D @ Wsf
+        dW += D.T @ hsf[r0:r1]
+    return Backward(dH, dW)
+
+
 # ------------------------------------------------------------------ fp8 (e4m3)
 
 E4M3_MAX = 448.0

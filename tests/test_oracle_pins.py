@@ -465,6 +465,107 @@ def test_kd_gradients_by_finite_differences():
     assert np.linalg.norm(numh - b.dH) <= 1e-7 * np.linalg.norm(b.dH)
 
 
+def _torch_jsd(zs, zt, beta):
+    """Generalised JSD written with torch's kl_div on a log-sum-exp mixture."""
+    log_ps, log_pt = torch.log_softmax(zs, -1), torch.log_softmax(zt, -1)
+    log_m = torch.logsumexp(torch.stack([log_pt + np.log(beta), log_ps + np.log(1 - beta)]), 0)
+    kl_t = torch.nn.functional.kl_div(log_m, log_pt, log_target=True, reduction="none").sum(-1)
+    kl_s = torch.nn.functional.kl_div(log_m, log_ps, log_target=True, reduction="none").sum(-1)
+    return beta * kl_t + (1 - beta) * kl_s, kl_s
+
+
+@pytest.mark.parametrize("beta", [0.5, 0.1, 0.9])
+def test_jsd_matches_torch_mixture_kl_divs_and_autograd(beta):
+    hs, Ws, ht, Wt = _kd_rand(25, 7, 5, 31, 44)
+    t = np.random.default_rng(3).integers(0, 31, 25)
+    t[[2, 9, 17]] = O.IGNORE_INDEX
+    w = np.random.default_rng(4).uniform(0.5, 2, 25)
+    tf = O.LogitTransform(softcap=4.0, temperature=1.5)
+    hst = torch.tensor(hs, requires_grad=True)
+    Wst = torch.tensor(Ws, requires_grad=True)
+    zs = 4.0 * torch.tanh((hst @ Wst.T) / 4.0) / 1.5
+    zt = 4.0 * torch.tanh(torch.tensor(ht @ Wt.T) / 4.0) / 1.5
+    jsd, kl_s = _torch_jsd(zs, zt, beta)
+    m = torch.tensor(t != O.IGNORE_INDEX, dtype=torch.float64)
+    loss = (m * torch.tensor(w) * jsd).sum() / m.sum()
+    loss.backward()
+    f = O.jsd_forward(hs, Ws, ht, Wt, beta, t, w, tf=tf)
+    b = O.jsd_backward(hs, Ws, ht, Wt, beta, t, w, g=1.0 / f.n_valid, tf=tf)
+    assert f.n_valid == 22
+    assert np.allclose(f.jsd, (m * jsd).detach().numpy(), atol=1e-12)
+    assert np.allclose(f.kl_sm, kl_s.detach().numpy(), atol=1e-12)
+    assert f.loss == pytest.approx(float(loss.detach()), rel=1e-12)
+    assert np.allclose(b.dH, hst.grad.numpy(), atol=1e-12) and np.allclose(b.dW, Wst.grad.numpy(), atol=1e-12)
+    # chunking does not change anything
+    fc = O.jsd_forward(hs, Ws, ht, Wt, beta, t, w, tf=tf, chunk_rows=4)
+    bc = O.jsd_backward(hs, Ws, ht, Wt, beta, t, w, g=1.0 / f.n_valid, tf=tf, chunk_rows=4)
+    assert np.allclose(fc.jsd, f.jsd, atol=1e-13) and np.allclose(bc.dW, b.dW, atol=1e-13)
+
+
+def test_jsd_identical_heads_symmetry_and_bounds():
+    hs, Ws, ht, Wt = _kd_rand(16, 6, 9, 23, 45)
+    f = O.jsd_forward(hs, Ws, hs, Ws, 0.3)
+    assert np.allclose(f.jsd, 0.0, atol=1e-13)
+    b = O.jsd_backward(hs, Ws, hs, Ws, 0.3, g=1.0)
+    assert np.allclose(b.dH, 0, atol=1e-13) and np.allclose(b.dW, 0, atol=1e-13)
+    # the textbook JSD (beta = 1/2) is symmetric in its two distributions
+    a = O.jsd_forward(hs, Ws, ht, Wt, 0.5)
+    c = O.jsd_forward(ht, Wt, hs, Ws, 0.5)
+    assert np.allclose(a.jsd, c.jsd, atol=1e-13) and np.all(a.jsd > 0)
+    # 0 <= JSD_beta <= the entropy of the mixing weight, reached by disjoint
+    # supports (huge opposite logits)
+    for beta in (0.5, 0.2):
+        hb = -beta * np.log(beta) - (1 - beta) * np.log(1 - beta)
+        assert np.all(O.jsd_forward(hs, Ws, ht, Wt, beta).jsd <= hb + 1e-12)
+        Wd = np.zeros((4, 1))
+        Wd[0, 0], Wd[1, 0] = 400.0, -400.0
+        far = O.jsd_forward(np.ones((1, 1)), Wd, np.ones((1, 1)), -Wd, beta)
+        assert far.jsd[0] == pytest.approx(hb, abs=1e-12)
+
+
+def test_jsd_limits_are_the_two_kl_divergences():
+    # beta -> 0: JSD_beta / beta -> KL(p_t || p_s) (the forward KL of the
+    # distillation oracle); beta -> 1: JSD_beta / (1 - beta) -> KL(p_s || p_t)
+    hs, Ws, ht, Wt = _kd_rand(10, 5, 7, 19, 46)
+    kl_ts = O.kd_forward(hs, Ws, ht, Wt).kl
+    kl_st = O.kd_forward(ht, Wt, hs, Ws).kl
+    eps = 1e-6
+    assert np.allclose(O.jsd_forward(hs, Ws, ht, Wt, eps).jsd / eps, kl_ts, rtol=1e-4)
+    assert np.allclose(O.jsd_forward(hs, Ws, ht, Wt, 1 - eps).jsd / eps, kl_st, rtol=1e-4)
+
+
+def test_jsd_gradients_by_finite_differences():
+    hs, Ws, ht, Wt = _kd_rand(3, 4, 5, 6, 47)
+    tf = O.LogitTransform(softcap=3.0, temperature=1.5)
+    beta = 0.3
+    f = O.jsd_forward(hs, Ws, ht, Wt, beta, tf=tf)
+    b = O.jsd_backward(hs, Ws, ht, Wt, beta, g=1.0 / f.n_valid, tf=tf)
+    eps = 1e-6
+    num = np.zeros_like(Ws)
+    for v in range(Ws.shape[0]):
+        for k in range(Ws.shape[1]):
+            e = np.zeros_like(Ws)
+            e[v, k] = eps
+            num[v, k] = (O.jsd_forward(hs, Ws + e, ht, Wt, beta, tf=tf).loss -
+                         O.jsd_forward(hs, Ws - e, ht, Wt, beta, tf=tf).loss) / (2 * eps)
+    assert np.linalg.norm(num - b.dW) <= 1e-7 * np.linalg.norm(b.dW)
+    numh = np.zeros_like(hs)
+    for i in range(hs.shape[0]):
+        for k in range(hs.shape[1]):
+            e = np.zeros_like(hs)
+            e[i, k] = eps
+            numh[i, k] = (O.jsd_forward(hs + e, Ws, ht, Wt, beta, tf=tf).loss -
+                          O.jsd_forward(hs - e, Ws, ht, Wt, beta, tf=tf).loss) / (2 * eps)
+    assert np.linalg.norm(numh - b.dH) <= 1e-7 * np.linalg.norm(b.dH)
+
+
+def test_jsd_rejects_beta_outside_the_open_interval():
+    hs, Ws, ht, Wt = _kd_rand(2, 3, 3, 4, 48)
+    for beta in (0.0, 1.0, -0.5, 1.5, float("nan")):
+        with pytest.raises(ValueError):
+            O.jsd_forward(hs, Ws, ht, Wt, beta)
+
+
 # ------------------------------------------------------------------------ fp8
 
 def test_e4m3_decode_matches_torch_for_every_code():
