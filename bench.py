@@ -184,7 +184,8 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "kd_fwd_logits", "kd_bwd_dlogits")
+GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "kd_fwd_logits", "kd_bwd_dlogits",
+              "jsd_fwd_terms", "jsd_bwd_dlogits")
 
 
 def gpu_arm(args):
@@ -243,6 +244,7 @@ def gpu_arm(args):
         ht = up(tinp.h)
         Wt = up(tinp.W)
         lse_t = torch.empty(N, dtype=torch.float32, device=dev)
+        kl_sm = torch.empty(N, dtype=torch.float32, device=dev)
         ws_bytes = max(ws_bytes, _lib.flce_kd_workspace_bytes(N, H, Ht, V, chunk_rows))
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
@@ -275,6 +277,17 @@ def gpu_arm(args):
                     h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr,
                     logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(),
                     workspace.data_ptr(), ws_bytes, sh))
+            return
+        if Ht and args.jsd_beta:
+            check("flce_jsd_forward", lib.flce_jsd_forward(
+                h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp, N,
+                V, chunk_rows, -100, args.jsd_beta, tf_ptr, logp.data_ptr(), lse.data_ptr(),
+                lse_t.data_ptr(), kl_sm.data_ptr(), loss.data_ptr(), nv.data_ptr(),
+                workspace.data_ptr(), ws_bytes, sh))
+            check("flce_jsd_backward", lib.flce_jsd_backward(
+                h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp,
+                lse.data_ptr(), lse_t.data_ptr(), kl_sm.data_ptr(), args.jsd_beta, g, dH.data_ptr(),
+                dW.data_ptr(), N, V, chunk_rows, -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
             return
         if Ht:
             check("flce_kd_forward", lib.flce_kd_forward(
@@ -397,7 +410,11 @@ def gpu_arm(args):
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     if args.forward_only:
         flops_step = {"fwd_logits_lse": 2.0 * N * V * H}
-    if Ht:  # distillation: both heads in the forward and the dlogits recompute
+    if Ht and args.jsd_beta:  # both heads twice in the forward (lse, then mixture terms)
+        flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "jsd_fwd_terms": 2.0 * N * V * (H + Ht),
+                      "jsd_bwd_dlogits": 2.0 * N * V * (H + Ht),
+                      "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
+    elif Ht:  # distillation: both heads in the forward and the dlogits recompute
         flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "kd_bwd_dlogits": 2.0 * N * V * (H + Ht),
                       "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
     kern = {}
@@ -443,6 +460,7 @@ def gpu_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if args.e4m3 else "bf16",
             "data": "synthetic",
             "config": {"workload": wl.name + (f"+kd_teacher_H{Ht}" if Ht else "")
+                       + (f"+jsd_beta{args.jsd_beta:g}" if Ht and args.jsd_beta else "")
                        + (f"+transform({args.transform})" if args.transform else "")
                        + ("+forward_only" if args.forward_only else "") + ("+e4m3" if args.e4m3 else ""),
                        "N": N, "H": H, "V": V, "chunk_rows": chunk_rows,
@@ -494,7 +512,12 @@ def main():
     ap.add_argument("--kd-teacher-hidden", type=int, default=0,
                     help="time the distillation step instead: the workload's head is the student, "
                          "a teacher head of this hidden size is added")
+    ap.add_argument("--jsd-beta", type=float, default=0.0,
+                    help="with --kd-teacher-hidden: Jensen-Shannon distillation with this mixture "
+                         "weight in (0, 1) instead of KL(teacher || student)")
     args = ap.parse_args()
+    if args.jsd_beta and not (0.0 < args.jsd_beta < 1.0 and args.kd_teacher_hidden):
+        ap.error("--jsd-beta needs --kd-teacher-hidden and a value in (0, 1)")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -5,4 +5,5 @@ package holds its ctypes binding, a thin torch-facing API and the seeded
 synthetic workloads.
 """
 from .api import (IGNORE_INDEX, LinearCrossEntropy, backward, forward,  # noqa: F401
-                  kd_backward, kd_forward, linear_cross_entropy, workspace_bytes)
+                  jsd_backward, jsd_forward, kd_backward, kd_forward, linear_cross_entropy,
+                  workspace_bytes)

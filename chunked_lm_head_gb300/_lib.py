@@ -42,6 +42,14 @@ SIGNATURES = {
                                         _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp, _c_i64, _c_i64,
                                         _c_i64, _c_i64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "flce_kd_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64]),
+    "flce_jsd_forward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                        _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_vp, _c_vp,
+                                        _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
+                                        _c_vp]),
+    "flce_jsd_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                         _c_vp, _c_vp, _c_vp, ctypes.c_float, ctypes.c_float, _c_vp,
+                                         _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
+                                         ctypes.c_size_t, _c_vp]),
     "flce_quantize_e4m3_rows": (ctypes.c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp]),
     "flce_forward_e4m3": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64,
                                          _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -206,6 +214,32 @@ def flce_kd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_
                                 _ptr(weights), _ptr(lse_s), _ptr(lse_t), float(grad_scale),
                                 _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows, ignore_index, tp,
                                 _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_jsd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows, ignore_index,
+                     beta, transform, out_jsd, out_lse_s, out_lse_t, out_kl_sm, out_loss,
+                     out_n_valid, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the Jensen-Shannon distillation forward."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_jsd_forward(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                _ptr(weights), N, V, chunk_rows, ignore_index, float(beta), tp,
+                                _ptr(out_jsd), _ptr(out_lse_s), _ptr(out_lse_t), _ptr(out_kl_sm),
+                                _ptr(out_loss), _ptr(out_n_valid), _ptr(workspace), workspace_bytes,
+                                _stream_handle(stream))
+
+
+def flce_jsd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, kl_sm, beta,
+                      grad_scale, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
+                      workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the Jensen-Shannon distillation backward (student gradients)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_jsd_backward(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                 _ptr(weights), _ptr(lse_s), _ptr(lse_t), _ptr(kl_sm), float(beta),
+                                 float(grad_scale), _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows,
+                                 ignore_index, tp, _ptr(workspace), workspace_bytes,
+                                 _stream_handle(stream))
 
 
 def flce_quantize_e4m3_rows(x, rows, cols, q, scale, stream=None) -> int:

@@ -132,6 +132,55 @@ def kd_forward(h_s, W_s, h_t, W_t, targets=None, weights=None, chunk_rows: int =
     return {"kl": kl, "lse_s": lse_s, "lse_t": lse_t, "loss": loss, "n_valid": n_valid}
 
 
+def _check_heads(h_s, W_s, h_t, W_t):
+    for x in (h_s, W_s, h_t, W_t):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 2:
+            raise ValueError("h_s, W_s, h_t, W_t must be contiguous 2-D bfloat16 CUDA tensors")
+    N, H_s = h_s.shape
+    V = W_s.shape[0]
+    if W_s.shape != (V, H_s) or W_t.shape != (V, h_t.shape[1]) or h_t.shape[0] != N:
+        raise ValueError("expected h_s[N,H_s], W_s[V,H_s], h_t[N,H_t], W_t[V,H_t]")
+    return N, H_s, h_t.shape[1], V
+
+
+def jsd_forward(h_s, W_s, h_t, W_t, beta: float = 0.5, targets=None, weights=None,
+                chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX, transform=None,
+                workspace: torch.Tensor | None = None, stream=None):
+    """Jensen-Shannon distillation forward:
+    dict(jsd[N], lse_s[N], lse_t[N], kl_sm[N], loss[], n_valid[]) on device."""
+    N, H_s, H_t, V = _check_heads(h_s, W_s, h_t, W_t)
+    dev = h_s.device
+    jsd = torch.empty(N, dtype=torch.float32, device=dev)
+    lse_s = torch.empty(N, dtype=torch.float32, device=dev)
+    lse_t = torch.empty(N, dtype=torch.float32, device=dev)
+    kl_sm = torch.empty(N, dtype=torch.float32, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    n_valid = torch.empty((), dtype=torch.int64, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.flce_jsd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows,
+                               ignore_index, beta, transform, jsd, lse_s, lse_t, kl_sm, loss, n_valid,
+                               workspace, ws_bytes, stream)
+    _lib.check("flce_jsd_forward", st)
+    return {"jsd": jsd, "lse_s": lse_s, "lse_t": lse_t, "kl_sm": kl_sm, "loss": loss,
+            "n_valid": n_valid}
+
+
+def jsd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, kl_sm, grad_scale: float, beta: float = 0.5,
+                 targets=None, weights=None, chunk_rows: int = 256,
+                 ignore_index: int = IGNORE_INDEX, transform=None, need_dH: bool = True,
+                 need_dW: bool = True, workspace: torch.Tensor | None = None, stream=None):
+    """Jensen-Shannon distillation backward: (dH_s bf16 or None, dW_s f32 or None)."""
+    N, H_s, H_t, V = _check_heads(h_s, W_s, h_t, W_t)
+    dH = torch.empty_like(h_s) if need_dH else None
+    dW = torch.empty((V, H_s), dtype=torch.float32, device=h_s.device) if need_dW else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.flce_jsd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, kl_sm,
+                                beta, grad_scale, dH, dW, N, V, chunk_rows, ignore_index, transform,
+                                workspace, ws_bytes, stream)
+    _lib.check("flce_jsd_backward", st)
+    return dH, dW
+
+
 def kd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, grad_scale: float, targets=None, weights=None,
                 chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX, transform=None,
                 need_dH: bool = True, need_dW: bool = True, workspace: torch.Tensor | None = None,

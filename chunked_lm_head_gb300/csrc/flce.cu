@@ -310,6 +310,60 @@ __global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* _
   }
 }
 
+// Jensen-Shannon combine: per row, the split partials (log2 units) summed in
+// split order -> jsd = ln2 (beta A_t + (1 - beta) A_s) (0 on masked rows) and
+// kl_sm = ln2 A_s = KL(p_s || M); block sums of -w jsd and of the row count
+// for the deterministic loss.
+template <bool kLong>
+__global__ void jsd_combine_kernel(const float2* __restrict__ pj, int S, int N,
+                                   const int64_t* __restrict__ targets,
+                                   const float* __restrict__ weights, long long ignore, float beta,
+                                   float* __restrict__ out_jsd, float* __restrict__ out_kl_sm,
+                                   double* __restrict__ blk_sum, long long* __restrict__ blk_cnt) {
+  using idx_t = typename std::conditional<kLong, long long, int>::type;
+  const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
+  double contrib = 0.0;
+  long long cnt = 0;
+  if (i < N) {
+    float at = 0.f, as = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float2 q = pj[static_cast<idx_t>(s) * N + i];
+      at += q.x;
+      as += q.y;
+    }
+    const bool valid = targets == nullptr || targets[i] != ignore;
+    const float jsd = valid ? kLn2 * (beta * at + (1.f - beta) * as) : 0.f;
+    if (out_jsd) out_jsd[i] = jsd;
+    if (out_kl_sm) out_kl_sm[i] = kLn2 * as;
+    if (valid) {
+      cnt = 1;
+      contrib = -static_cast<double>(weights ? weights[i] : 1.f) * static_cast<double>(jsd);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
+    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
+  }
+  __shared__ double ssum[SMALL_THREADS / 32];
+  __shared__ long long scnt[SMALL_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) {
+    ssum[threadIdx.x >> 5] = contrib;
+    scnt[threadIdx.x >> 5] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0;
+    long long c = 0;
+    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
+      a += ssum[w];
+      c += scnt[w];
+    }
+    blk_sum[blockIdx.x] = a;
+    blk_cnt[blockIdx.x] = c;
+  }
+}
+
 // Per-row e4m3 quantisation (one warp per row): scale = max|x| / 448 (1 for
 // an all-zero row), q = e4m3(x / scale), round to nearest even, saturating.
 __global__ void quantize_e4m3_rows_kernel(const uint16_t* __restrict__ x, long long rows, int cols,
@@ -376,13 +430,13 @@ constexpr int kDefaultSms = 152;
 
 enum Kind {
   K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COMPACT, K_GATHER,
-  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_COUNT
+  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_JSD_FWD, K_JSD_DLOGITS, K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {"prep_targets",  "fwd_logits_lse", "fwd_combine",
                                          "fwd_loss",      "bwd_dlogits",    "bwd_dH",
                                          "bwd_dH_reduce", "bwd_dW",         "bwd_compact_rows",
                                          "bwd_gather_rows", "kd_fwd_logits",  "kd_bwd_dlogits",
-                                         "quantize_e4m3"};
+                                         "quantize_e4m3", "jsd_fwd_terms",  "jsd_bwd_dlogits"};
 
 struct ProfRec {
   int kind;
@@ -667,6 +721,27 @@ KdFwdLayout kd_fwd_layout(long long N, const FwdPlan& f) {
   o += align256(static_cast<size_t>(f.nblk) * 8);
   L.bcnt = o;
   o += align256(static_cast<size_t>(f.nblk) * 8);
+  L.total = o;
+  return L;
+}
+
+// Jensen-Shannon forward scratch: the distillation forward's (pass 1, both
+// heads' log-sum-exp) plus the mixture-term partials of pass 2 and the two lse
+// vectors when the caller does not ask for them.
+struct JsdFwdLayout {
+  KdFwdLayout kd;
+  size_t pj = 0, lse_s = 0, lse_t = 0, total = 0;
+};
+JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f) {
+  JsdFwdLayout L;
+  L.kd = kd_fwd_layout(N, f);
+  size_t o = L.kd.total;
+  L.pj = o;
+  o += align256(static_cast<size_t>(f.S) * N * 8);
+  L.lse_s = o;
+  o += align256(static_cast<size_t>(N) * 4);
+  L.lse_t = o;
+  o += align256(static_cast<size_t>(N) * 4);
   L.total = o;
   return L;
 }
@@ -1492,28 +1567,35 @@ size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, i
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return 0;
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  const KdFwdLayout fl = kd_fwd_layout(N, plan_forward(N, H_s + H_t, V, workers, BM * cg));
+  const JsdFwdLayout fl = jsd_fwd_layout(N, plan_forward(N, H_s + H_t, V, workers, BM * cg));
   const BwdLayout bl = bwd_layout(N, H_s, plan_backward(N, H_s, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
 
-flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
-                            const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
-                            const int64_t* targets, const float* weights, int64_t N, int64_t V,
-                            int64_t chunk_rows, int64_t ignore_index,
-                            const flce_logit_transform* transform, float* out_kl, float* out_lse_s,
-                            float* out_lse_t, float* out_loss, int64_t* out_n_valid,
-                            void* workspace, size_t workspace_bytes, void* stream) {
-  (void)chunk_rows;
+// Distillation forward, KL (jsd == false) or Jensen-Shannon with mixture
+// weight beta.  Pass 1 runs both heads for their online log-sum-exp (and the
+// KL cross term); the Jensen-Shannon terms need both final lse values, so a
+// second pass over both heads forms them.
+static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, const flce_bf16* W_s,
+                                   int64_t H_s, const flce_bf16* h_t, const flce_bf16* W_t,
+                                   int64_t H_t, const int64_t* targets, const float* weights,
+                                   int64_t N, int64_t V, int64_t ignore_index,
+                                   const flce_logit_transform* transform, float* out_kl,
+                                   float* out_lse_s, float* out_lse_t, float* out_kl_sm,
+                                   float* out_loss, int64_t* out_n_valid, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return FLCE_ERR_INVALID_ARG;
+  if (jsd && !(beta > 0.f && beta < 1.f)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
-  if (!out_kl && !out_lse_s && !out_lse_t && !out_loss && !out_n_valid) return FLCE_ERR_INVALID_ARG;
+  if (!out_kl && !out_lse_s && !out_lse_t && !out_kl_sm && !out_loss && !out_n_valid)
+    return FLCE_ERR_INVALID_ARG;
   if (N > 0 && (!h_s || !W_s || !h_t || !W_t)) return FLCE_ERR_INVALID_ARG;
   if (H_s % 8 != 0 || H_t % 8 != 0) return FLCE_ERR_UNSUPPORTED;
   if (!aligned(h_s, 16) || !aligned(W_s, 16) || !aligned(h_t, 16) || !aligned(W_t, 16) ||
       !aligned(targets, 8) || !aligned(weights, 4) || !aligned(out_kl, 4) || !aligned(out_lse_s, 4) ||
-      !aligned(out_lse_t, 4) || !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
+      !aligned(out_lse_t, 4) || !aligned(out_kl_sm, 4) || !aligned(out_loss, 4) ||
+      !aligned(out_n_valid, 8))
     return FLCE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int cg = cta_group();
@@ -1521,9 +1603,10 @@ flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t 
   const int kbs = static_cast<int>(ceil_div(H_s, BK));
   const int kbt = static_cast<int>(ceil_div(H_t, BK));
   const FwdPlan f = plan_forward(N, H_s + H_t, V, workers, BM * cg);
-  const KdFwdLayout L = kd_fwd_layout(N, f);
+  const JsdFwdLayout J = jsd_fwd_layout(N, f);
+  const KdFwdLayout& L = J.kd;
   Workspace ws;
-  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, jsd ? J.total : L.total, st);
   if (s != FLCE_OK) return s;
   uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
   float2* ps = reinterpret_cast<float2*>(wb + L.ps);
@@ -1531,6 +1614,13 @@ flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t 
   float* pc = reinterpret_cast<float*>(wb + L.pc);
   double* bsum = reinterpret_cast<double*>(wb + L.bsum);
   long long* bcnt = reinterpret_cast<long long*>(wb + L.bcnt);
+  // the Jensen-Shannon pass reads both lse vectors: the caller's, or scratch
+  float* lse_s = out_lse_s;
+  float* lse_t = out_lse_t;
+  if (jsd) {
+    if (!lse_s) lse_s = reinterpret_cast<float*>(wb + J.lse_s);
+    if (!lse_t) lse_t = reinterpret_cast<float*>(wb + J.lse_t);
+  }
   const int Ni = static_cast<int>(N);
   if (N > 0) {
     CUtensorMap hs_k, Ws_k, ht_k, Wt_k;
@@ -1574,36 +1664,88 @@ flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t 
     }
     {
       ProfScope prof(K_COMBINE, st);
+      float* kl = jsd ? nullptr : out_kl;
       if (kLong)
         kd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(ps, pt, pc, f.S, Ni, targets, weights,
-                                                                  ignore_index, out_kl, out_lse_s,
-                                                                  out_lse_t, bsum, bcnt);
+                                                                  ignore_index, kl, lse_s, lse_t, bsum, bcnt);
       else
         kd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(ps, pt, pc, f.S, Ni, targets, weights,
-                                                                   ignore_index, out_kl, out_lse_s,
-                                                                   out_lse_t, bsum, bcnt);
+                                                                   ignore_index, kl, lse_s, lse_t, bsum, bcnt);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    if (jsd) {
+      float2* pj = reinterpret_cast<float2*>(wb + J.pj);
+      GemmParams q = p;
+      q.lse = lse_s;
+      q.lse_t = lse_t;
+      q.partials = pj;
+      q.jsd_beta = beta;
+      {
+        ProfScope prof(K_JSD_FWD, st);
+        FLCE_CUDA_TRY(launch_gemm<MODE_JSD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, q, f.grid, st, &ht_k, &Wt_k));
+      }
+      ProfScope prof(K_COMBINE, st);
+      if (kLong)
+        jsd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, f.S, Ni, targets, weights, ignore_index,
+                                                                   beta, out_kl, out_kl_sm, bsum, bcnt);
+      else
+        jsd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, f.S, Ni, targets, weights, ignore_index,
+                                                                    beta, out_kl, out_kl_sm, bsum, bcnt);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
   }
   return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
 }
 
-flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                            const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                            const int64_t* targets, const float* weights, int64_t N, int64_t V,
+                            int64_t chunk_rows, int64_t ignore_index,
+                            const flce_logit_transform* transform, float* out_kl, float* out_lse_s,
+                            float* out_lse_t, float* out_loss, int64_t* out_n_valid,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  (void)chunk_rows;
+  return distill_forward(false, 0.f, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, ignore_index,
+                         transform, out_kl, out_lse_s, out_lse_t, nullptr, out_loss, out_n_valid,
+                         workspace, workspace_bytes, stream);
+}
+
+flce_status flce_jsd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
                              const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
-                             const int64_t* targets, const float* weights, const float* lse_s,
-                             const float* lse_t, float grad_scale, flce_bf16* dH_s, float* dW_s,
-                             int64_t N, int64_t V, int64_t chunk_rows, int64_t ignore_index,
-                             const flce_logit_transform* transform, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+                             const int64_t* targets, const float* weights, int64_t N, int64_t V,
+                             int64_t chunk_rows, int64_t ignore_index, float beta,
+                             const flce_logit_transform* transform, float* out_jsd,
+                             float* out_lse_s, float* out_lse_t, float* out_kl_sm, float* out_loss,
+                             int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  (void)chunk_rows;
+  return distill_forward(true, beta, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, ignore_index,
+                         transform, out_jsd, out_lse_s, out_lse_t, out_kl_sm, out_loss, out_n_valid,
+                         workspace, workspace_bytes, stream);
+}
+
+// Distillation backward (student gradients, teacher frozen): KL dlogits
+// (jsd == false) or Jensen-Shannon dlogits with mixture weight beta and the
+// forward's per-row KL(p_s || M); then the shared dH / dW stages.
+static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, const flce_bf16* h_s,
+                                    const flce_bf16* W_s, int64_t H_s, const flce_bf16* h_t,
+                                    const flce_bf16* W_t, int64_t H_t, const int64_t* targets,
+                                    const float* weights, const float* lse_s, const float* lse_t,
+                                    float grad_scale, flce_bf16* dH_s, float* dW_s, int64_t N,
+                                    int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                    const flce_logit_transform* transform, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return FLCE_ERR_INVALID_ARG;
+  if (jsd && !(beta > 0.f && beta < 1.f)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
   if (!dH_s && !dW_s) return FLCE_ERR_INVALID_ARG;
   if (N > 0 && (!h_s || !W_s || !h_t || !W_t || !lse_s || !lse_t)) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && jsd && !kl_sm) return FLCE_ERR_INVALID_ARG;
   if (H_s % 8 != 0 || H_t % 8 != 0) return FLCE_ERR_UNSUPPORTED;
   if (!aligned(h_s, 16) || !aligned(W_s, 16) || !aligned(h_t, 16) || !aligned(W_t, 16) ||
       !aligned(dH_s, 16) || !aligned(dW_s, 16) || !aligned(targets, 8) || !aligned(weights, 4) ||
-      !aligned(lse_s, 4) || !aligned(lse_t, 4))
+      !aligned(lse_s, 4) || !aligned(lse_t, 4) || !aligned(kl_sm, 4))
     return FLCE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (N == 0) {
@@ -1656,6 +1798,8 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
   base.err = err;
   base.rows_cap = static_cast<int>(b.R);
   base.k_blocks_s = kbs;
+  base.jsd_beta = beta;
+  base.kl_sm = kl_sm;
   base.tf_softcap = tfp.tf_softcap;
   base.tf_a = tfp.tf_a;
   base.tf_b = tfp.tf_b;
@@ -1691,9 +1835,13 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
         q.k_splits = 1;
         q.num_units = q.m_tiles * q.n_tiles;
         q.group_m = std::min(16, q.m_tiles);
-        ProfScope prof(K_KD_DLOGITS, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
-                                                   std::min(q.num_units, workers), st, &ht_k, &Wt_k));
+        ProfScope prof(jsd ? K_JSD_DLOGITS : K_KD_DLOGITS, st);
+        if (jsd)
+          FLCE_CUDA_TRY(launch_gemm<MODE_JSD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
+                                                      std::min(q.num_units, workers), st, &ht_k, &Wt_k));
+        else
+          FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
+                                                     std::min(q.num_units, workers), st, &ht_k, &Wt_k));
       }
       const flce_status s2 = slab_dh_dw(dhdw, p, rows, block, slab, v0, width, D_k, D_mn, hs_mn, st);
       if (s2 != FLCE_OK) return s2;
@@ -1702,6 +1850,30 @@ flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
     if (s3 != FLCE_OK) return s3;
   }
   return FLCE_OK;
+}
+
+flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                             const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                             const int64_t* targets, const float* weights, const float* lse_s,
+                             const float* lse_t, float grad_scale, flce_bf16* dH_s, float* dW_s,
+                             int64_t N, int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                             const flce_logit_transform* transform, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return distill_backward(false, 0.f, nullptr, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s,
+                          lse_t, grad_scale, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
+                          workspace, workspace_bytes, stream);
+}
+
+flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                              const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                              const int64_t* targets, const float* weights, const float* lse_s,
+                              const float* lse_t, const float* kl_sm, float beta, float grad_scale,
+                              flce_bf16* dH_s, float* dW_s, int64_t N, int64_t V, int64_t chunk_rows,
+                              int64_t ignore_index, const flce_logit_transform* transform,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return distill_backward(true, beta, kl_sm, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s,
+                          lse_t, grad_scale, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
+                          workspace, workspace_bytes, stream);
 }
 
 flce_status flce_device_status(void* stream) {

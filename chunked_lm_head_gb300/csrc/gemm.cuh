@@ -72,6 +72,7 @@ constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 constexpr long long DRAIN_LIMIT_CYCLES = 400000000LL;
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2f = 0.6931471805599453f;
 
 enum Mode : int {
   MODE_FWD = 0,
@@ -82,11 +83,21 @@ enum Mode : int {
   // over the student's hidden blocks into TMEM columns [0, BN), then over the
   // teacher's into [BN, 2 BN)
   MODE_KD_FWD = 4,
-  MODE_KD_DLOGITS = 5
+  MODE_KD_DLOGITS = 5,
+  // Jensen-Shannon distillation, same two-head pipeline: the per-row mixture
+  // terms given both heads' log-sum-exp, and the student's dlogits
+  MODE_JSD_FWD = 6,
+  MODE_JSD_DLOGITS = 7
 };
 template <int MODE>
 __host__ __device__ constexpr bool is_kd() {
-  return MODE == MODE_KD_FWD || MODE == MODE_KD_DLOGITS;
+  return MODE == MODE_KD_FWD || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_FWD ||
+         MODE == MODE_JSD_DLOGITS;
+}
+// modes whose units are (row tile, vocabulary split) with per-row partials
+template <int MODE>
+__host__ __device__ constexpr bool is_split_fwd() {
+  return MODE == MODE_FWD || MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD;
 }
 
 // bit 0 of the device error word: a bounded wait ran out.
@@ -143,6 +154,10 @@ struct GemmParams {
   // DH into fp32 partials (through tmC): reduce-add onto the previous slabs'
   // sums, else a plain store
   int dh_accumulate;
+  // Jensen-Shannon distillation: mixture weight of the teacher, and (dlogits)
+  // each row's KL(p_student || mixture) in natural-log units
+  float jsd_beta;
+  const float* kl_sm;
 };
 
 // Problem extents that depend on the device-side row count of a compacted pass.
@@ -199,7 +214,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape&
   t.n1 = min(p.n_tiles, t.n0 + p.n_per_unit);
   t.kb0 = ks * d.kb_per_split;
   t.kb1 = min(d.k_blocks, t.kb0 + d.kb_per_split);
-  t.split = (MODE == MODE_FWD || MODE == MODE_KD_FWD) ? c : ks;
+  t.split = is_split_fwd<MODE>() ? c : ks;
   return t;
 }
 
@@ -517,6 +532,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       long long tgt = -1;
       float run_m = -INFINITY, run_s = 0.f;  // FWD: log2-domain max and sum
       float run_mt = -INFINITY, run_st = 0.f, run_c = 0.f;  // KD_FWD teacher state
+      float jsd_t = 0.f, jsd_s = 0.f, klsm = 0.f;            // JSD: mixture terms (log2 units)
       float scale = 0.f, nl2 = 0.f, nlt = 0.f;              // DLOGITS / KD_DLOGITS
       // linear transform folded into the exp2 prescale, the gathered target
       // logit and the dlogits scale (soft-capped logits are formed explicitly)
@@ -551,11 +567,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           nl2 = -p.lse[grow] * kLog2e;
         }
       }
-      if constexpr (MODE == MODE_KD_DLOGITS) {
+      if constexpr (MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS) {
         if (row_ok) {
           const bool valid = p.targets == nullptr || p.targets[grow] != p.ignore_index;
           const float w = p.weights ? p.weights[grow] : 1.f;
           scale = valid ? w * p.grad_scale : 0.f;
+          nl2 = -p.lse[grow] * kLog2e;
+          nlt = -p.lse_t[grow] * kLog2e;
+          if constexpr (MODE == MODE_JSD_DLOGITS) klsm = p.kl_sm[grow];
+        }
+      }
+      if constexpr (MODE == MODE_JSD_FWD) {
+        if (row_ok) {
           nl2 = -p.lse[grow] * kLog2e;
           nlt = -p.lse_t[grow] * kLog2e;
         }
@@ -752,6 +775,82 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   *reinterpret_cast<uint4*>(dst + 8 * g) =
                       make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
             }
+          } else if constexpr (MODE == MODE_JSD_FWD) {
+            // per row: sum p_t (log2 p_t - log2 M) and sum p_s (log2 p_s - log2 M)
+            // with M = beta p_t + (1 - beta) p_s, given both heads' lse
+            float vt[32];
+            tmem_ld32(tbase + BN + c * 32, vt);
+            if (p.tf_softcap) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                v[j] = p.tf_b * tanhf(p.tf_a * v[j]);
+                vt[j] = p.tf_b * tanhf(p.tf_a * vt[j]);
+              }
+            }
+            if (row_ok) {
+              const int gcol0 = p.v0 + col0;
+              float at = 0.f, as = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float ls2 = fmaf(v[j], l2a, nl2);
+                const float lt2 = fmaf(vt[j], l2a, nlt);
+                const float ps = ex2_approx(ls2);
+                const float pt = ex2_approx(lt2);
+                const float mix = fmaf(p.jsd_beta, pt - ps, ps);
+                // below 1e-37 both probabilities are negligible (each is at
+                // most M / min(beta, 1 - beta)); past V there is no column
+                if (mix > 1e-37f && gcol0 + j < p.V) {
+                  const float lm2 = __log2f(mix);
+                  at = fmaf(pt, lt2 - lm2, at);
+                  as = fmaf(ps, ls2 - lm2, as);
+                }
+              }
+              jsd_t += at;
+              jsd_s += as;
+            }
+          } else if constexpr (MODE == MODE_JSD_DLOGITS) {
+            // D = (1 - beta) p_s (ln(p_s / M) - KL(p_s || M)) m w g f'(z_s)
+            float vt[32];
+            tmem_ld32(tbase + BN + c * 32, vt);
+            uint32_t pk[16];
+            const int gcol0 = p.v0 + col0;
+            const float omb = 1.f - p.jsd_beta;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float d[2] = {0.f, 0.f};
+              if (scale != 0.f) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  float ls2, lt2, fd;
+                  if (!p.tf_softcap) {
+                    ls2 = fmaf(v[j + e], l2a, nl2);
+                    lt2 = fmaf(vt[j + e], l2a, nlt);
+                    fd = scale_a;
+                  } else {
+                    const float ts = tanhf(p.tf_a * v[j + e]);
+                    ls2 = fmaf(p.tf_b * ts, kLog2e, nl2);
+                    lt2 = fmaf(p.tf_b * tanhf(p.tf_a * vt[j + e]), kLog2e, nlt);
+                    fd = scale * p.tf_d * (1.f - ts * ts);
+                  }
+                  const float ps = ex2_approx(ls2);
+                  const float pt = ex2_approx(lt2);
+                  const float mix = fmaf(p.jsd_beta, pt - ps, ps);
+                  float de = 0.f;
+                  if (mix > 1e-37f && ps > 0.f)
+                    de = omb * ps * (fmaf(ls2 - __log2f(mix), kLn2f, -klsm)) * fd;
+                  d[e] = (gcol0 + j + e < p.V) ? de : 0.f;
+                }
+              }
+              pk[j / 2] = pack_bf16x2(d[0], d[1]);
+            }
+            if (row_store) {
+              uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (col0 + 8 * g < p.ldD)
+                  *reinterpret_cast<uint4*>(dst + 8 * g) =
+                      make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
           } else if (MODE == MODE_DH && p.dH_part == nullptr) {
             if (row_ok) {  // the only pass over this row: bf16 dH directly
               uint16_t* dst = p.dH + static_cast<idx_t>(grow) * p.H + col0;
@@ -818,6 +917,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if constexpr (MODE == MODE_FWD) {
         if (ok && row_ok)
           p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(run_m, run_s);
+      }
+      if constexpr (MODE == MODE_JSD_FWD) {
+        if (ok && row_ok) p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(jsd_t, jsd_s);
       }
       if constexpr (MODE == MODE_KD_FWD) {
         if (ok && row_ok) {

@@ -222,7 +222,54 @@ FLCE_API flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s
                                       const flce_logit_transform* transform, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of flce_kd_forward and flce_kd_backward for these sizes. */
+/*
+ * Jensen-Shannon distillation.  Source: TRL v1.13 article, section "Other
+ * changes in v1.13": a fused linear JSD loss is among TRL's fused losses; the
+ * page gives no formula.  Reading taken: per row, the generalised
+ * Jensen-Shannon divergence with mixture weight beta in (0, 1) (1/2 is the
+ * textbook JSD):
+ *   M      = beta * p_t + (1 - beta) * p_s,
+ *   jsd[i] = m[i] * (beta * KL(p_t || M) + (1 - beta) * KL(p_s || M)),
+ *   loss   = sum_i m[i] w[i] jsd[i] / sum_i m[i],
+ * with p_s, p_t, m[i], the logit transform, weights and the two heads as in
+ * flce_kd_forward.  Small beta approaches beta * KL(p_t || p_s) (the KL
+ * calls); beta near 1 approaches (1 - beta) * KL(p_s || p_t).
+ *
+ * flce_jsd_forward needs both heads' final log-sum-exp before it can form M,
+ * so it runs both heads twice: once for the log-sum-exp (as
+ * flce_kd_forward), once for the mixture terms.  Outputs (each may be NULL,
+ * not all): out_jsd [N], out_lse_s [N], out_lse_t [N], out_kl_sm [N] fp32
+ * (KL(p_s || M) of every row, masked or not: flce_jsd_backward needs it),
+ * out_loss, out_n_valid.  beta outside (0, 1) -> FLCE_ERR_INVALID_ARG.
+ */
+FLCE_API flce_status flce_jsd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                      const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                      const int64_t* targets, const float* weights, int64_t N,
+                                      int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                      float beta, const flce_logit_transform* transform,
+                                      float* out_jsd, float* out_lse_s, float* out_lse_t,
+                                      float* out_kl_sm, float* out_loss, int64_t* out_n_valid,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Student gradients of the Jensen-Shannon loss (the teacher is frozen):
+ *   D[i,v] = (1 - beta) p_s[i,v] (ln(p_s[i,v] / M[i,v]) - kl_sm[i]) * m[i] w[i] grad_scale
+ *            * f'(z_s[i,v]),
+ *   dH_s = D W_s, dW_s = D^T h_s,
+ * with lse_s, lse_t, kl_sm from flce_jsd_forward (same beta and transform).
+ * Memory and tiling as flce_kd_backward.
+ */
+FLCE_API flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                       const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                       const int64_t* targets, const float* weights,
+                                       const float* lse_s, const float* lse_t, const float* kl_sm,
+                                       float beta, float grad_scale, flce_bf16* dH_s, float* dW_s,
+                                       int64_t N, int64_t V, int64_t chunk_rows,
+                                       int64_t ignore_index, const flce_logit_transform* transform,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of the distillation calls (flce_kd_* and flce_jsd_*) for
+ * these sizes. */
 FLCE_API size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V,
                                         int64_t chunk_rows);
 

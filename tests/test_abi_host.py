@@ -126,3 +126,12 @@ def test_profile_kinds(lib):
     names = [lib.flce_profile_kind_name(k).decode() for k in range(n)]
     assert "fwd_logits_lse" in names and "bwd_dW" in names
     assert lib.flce_profile_kind_name(n) is None
+
+
+def test_jsd_rejects_beta_outside_the_open_interval_before_any_launch(lib):
+    p = 256  # never dereferenced: the beta check comes before any launch
+    for beta in (0.0, 1.0, -0.25, 2.0, float("nan")):
+        assert _lib.flce_jsd_forward(p, p, 64, p, p, 64, None, None, 8, 100, 16, -100, beta, None,
+                                     p, None, None, None, None, None, stream=0) == 1
+        assert _lib.flce_jsd_backward(p, p, 64, p, p, 64, None, None, p, p, p, beta, 1.0, p, p, 8, 100,
+                                      16, -100, None, stream=0) == 1
