@@ -495,6 +495,55 @@ def jsd_backward(hs, Ws, ht, Wt, beta: float = 0.5, targets=None, weights=None, 
     return Backward(dH, dW)
 
 
+# ------------------------------------------------------------------ GRPO token loss
+
+@dataclasses.dataclass
+class GRPOTokens:
+    token_loss: np.ndarray  # [N] m * per-token loss
+    weights: np.ndarray     # [N] -m * d(token loss)/d(logp): per-token weights for backward()
+    n_valid: int
+    loss: float             # sum(token_loss) / n_valid (0 when n_valid == 0)
+
+
+def grpo_token_loss(logp, advantages, mask, old_logp=None, ref_logp=None, eps_low: float = 0.2,
+                    eps_high: float = 0.2, beta: float = 0.0) -> GRPOTokens:
+    """Per-token GRPO objective on the log-probs of the sampled tokens.
+
+    TRL v1.13 article, section "Other changes in v1.13": TRL's fused linear
+    losses include a GRPO loss; the page gives no formula.  Reading taken
+    (the GRPO objective with a clipped probability ratio and the k3 estimate
+    of the KL divergence to a reference policy), per token with the mask m:
+        r     = exp(logp - old_logp)              (old_logp = logp when absent: r = 1)
+        obj   = min(r A, clip(r, 1 - eps_low, 1 + eps_high) A)
+        kl    = exp(ref - logp) - (ref - logp) - 1  (0 when ref_logp is absent)
+        token = m (beta kl - obj),   loss = sum(token) / sum(m)
+    old_logp and ref_logp are constants (no gradient).  The derivative of the
+    token loss by logp is  m (beta (1 - exp(ref - logp)) - A r [the unclipped
+    term is the minimum]); weights = -that derivative, so that
+    backward(..., weights, g = 1 / n_valid) gives the loss's dH and dW."""
+    lp = np.asarray(logp, dtype=np.float64)
+    A = np.asarray(advantages, dtype=np.float64)
+    m = np.asarray(mask, dtype=bool)
+    old = lp if old_logp is None else np.asarray(old_logp, dtype=np.float64)
+    r = np.exp(lp - old)
+    unclipped = r * A
+    clipped = np.clip(r, 1.0 - eps_low, 1.0 + eps_high) * A
+    obj = np.minimum(unclipped, clipped)
+    d_obj = np.where(unclipped <= clipped, unclipped, 0.0)  # d obj / d logp
+    if ref_logp is None or beta == 0.0:
+        kl = np.zeros_like(lp)
+        d_kl = np.zeros_like(lp)
+    else:
+        diff = np.asarray(ref_logp, dtype=np.float64) - lp
+        kl = np.exp(diff) - diff - 1.0
+        d_kl = 1.0 - np.exp(diff)
+    token = np.where(m, beta * kl - obj, 0.0)
+    weights = np.where(m, -(beta * d_kl - d_obj), 0.0)
+    n_valid = int(m.sum())
+    loss = float(token.sum()) / n_valid if n_valid > 0 else 0.0
+    return GRPOTokens(token, weights, n_valid, loss)
+
+
 # ------------------------------------------------------------------ fp8 (e4m3)
 
 E4M3_MAX = 448.0

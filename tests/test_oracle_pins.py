@@ -566,6 +566,90 @@ def test_jsd_rejects_beta_outside_the_open_interval():
             O.jsd_forward(hs, Ws, ht, Wt, beta)
 
 
+# ------------------------------------------------------------------------ GRPO
+
+def _grpo_rand(N, seed):
+    r = np.random.default_rng(seed)
+    lp = -r.uniform(0.1, 6.0, N)
+    # ratios exp(-delta) kept >= 0.09 away from the clip edges 0.8 / 1.2
+    delta = r.choice([-0.5, -0.1, 0.0, 0.1, 0.5, 1.0], N)
+    A = r.standard_normal(N)
+    ref = lp + r.uniform(-1.0, 1.0, N)
+    mask = r.uniform(size=N) > 0.15
+    return lp, lp + delta, ref, A, mask
+
+
+def test_grpo_token_loss_matches_torch_autograd():
+    lp, old, ref, A, mask = _grpo_rand(200, 50)
+    for eps_low, eps_high, beta in ((0.2, 0.2, 0.0), (0.2, 0.28, 0.04), (0.1, 0.3, 0.5)):
+        t = torch.tensor(lp, requires_grad=True)
+        r = torch.exp(t - torch.tensor(old))
+        At = torch.tensor(A)
+        obj = torch.minimum(r * At, torch.clamp(r, 1 - eps_low, 1 + eps_high) * At)
+        d = torch.tensor(ref) - t
+        kl = torch.exp(d) - d - 1
+        m = torch.tensor(mask, dtype=torch.float64)
+        loss = (m * (beta * kl - obj)).sum() / m.sum()
+        loss.backward()
+        o = O.grpo_token_loss(lp, A, mask, old, ref, eps_low, eps_high, beta)
+        assert o.n_valid == int(mask.sum())
+        assert o.loss == pytest.approx(float(loss.detach()), rel=1e-13)
+        # weights = -n_valid * dloss/dlogp
+        assert np.allclose(o.weights, -o.n_valid * t.grad.numpy(), atol=1e-12)
+
+
+def test_grpo_on_policy_is_the_advantage_weighted_nll_gradient():
+    # old = logp (r = 1), no KL: the gradient is that of -sum(m A logp) / n_valid,
+    # the GRPO-style loss of the per-token-weight path with w = A
+    lp, _, _, A, mask = _grpo_rand(100, 51)
+    o = O.grpo_token_loss(lp, A, mask)
+    assert np.array_equal(o.weights, np.where(mask, A, 0.0))
+    assert o.loss == pytest.approx(-float(np.sum(mask * A)) / int(mask.sum()), rel=1e-13)
+
+
+def test_grpo_clip_region_has_no_gradient_and_kl_vanishes_at_the_reference():
+    lp = np.log(np.array([0.5, 0.5, 0.5, 0.5]))
+    old = lp - np.log(np.array([1.5, 0.5, 1.5, 0.5]))  # ratios 1.5, 0.5, 1.5, 0.5
+    A = np.array([1.0, -1.0, -1.0, 1.0])
+    o = O.grpo_token_loss(lp, A, np.ones(4, bool), old, eps_low=0.2, eps_high=0.2)
+    # r > 1 + eps with A > 0 and r < 1 - eps with A < 0: clipped, no gradient;
+    # the other two sit on the unclipped (smaller) branch
+    assert o.weights[0] == 0.0 and o.weights[1] == 0.0
+    assert o.weights[2] == pytest.approx(-1.5) and o.weights[3] == pytest.approx(0.5)
+    assert o.token_loss[0] == pytest.approx(-1.2) and o.token_loss[1] == pytest.approx(0.8)
+    k = O.grpo_token_loss(lp, np.zeros(4), np.ones(4, bool), ref_logp=lp, beta=0.7)
+    assert np.all(k.token_loss == 0.0) and np.all(k.weights == 0.0)
+    lp2, _, ref2, _, m2 = _grpo_rand(50, 52)
+    k2 = O.grpo_token_loss(lp2, np.zeros(50), m2, ref_logp=ref2, beta=1.0)
+    assert np.all(k2.token_loss >= 0.0)  # the k3 estimate is never negative
+
+
+def test_grpo_full_path_matches_torch_autograd_through_the_head():
+    hs, Ws, _, _ = _kd_rand(30, 6, 6, 23, 53)
+    t = np.random.default_rng(9).integers(0, 23, 30)
+    t[[4, 11]] = O.IGNORE_INDEX
+    r = np.random.default_rng(10)
+    A = r.standard_normal(30)
+    f = O.forward(hs, Ws, t)
+    m = t != O.IGNORE_INDEX
+    old = f.logp + r.choice([-0.5, 0.0, 0.5], 30)
+    ref = f.logp + r.uniform(-0.5, 0.5, 30)
+    o = O.grpo_token_loss(f.logp, A, m, old, ref, 0.2, 0.28, 0.05)
+    b = O.backward(hs, Ws, t, o.weights, g=1.0 / o.n_valid)
+    ht = torch.tensor(hs, requires_grad=True)
+    Wt = torch.tensor(Ws, requires_grad=True)
+    logp = torch.log_softmax(ht @ Wt.T, -1)[torch.arange(30), torch.tensor(np.where(m, t, 0))]
+    ratio = torch.exp(logp - torch.tensor(old))
+    At = torch.tensor(A)
+    obj = torch.minimum(ratio * At, torch.clamp(ratio, 0.8, 1.28) * At)
+    d = torch.tensor(ref) - logp
+    mt = torch.tensor(m, dtype=torch.float64)
+    loss = (mt * (0.05 * (torch.exp(d) - d - 1) - obj)).sum() / mt.sum()
+    loss.backward()
+    assert o.loss == pytest.approx(float(loss.detach()), rel=1e-12)
+    assert np.allclose(b.dH, ht.grad.numpy(), atol=1e-12) and np.allclose(b.dW, Wt.grad.numpy(), atol=1e-12)
+
+
 # ------------------------------------------------------------------------ fp8
 
 def test_e4m3_decode_matches_torch_for_every_code():
