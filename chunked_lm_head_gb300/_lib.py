@@ -42,6 +42,10 @@ SIGNATURES = {
                                         _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp, _c_i64, _c_i64,
                                         _c_i64, _c_i64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
     "flce_kd_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64]),
+    "flce_grpo_token_loss": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64,
+                                            ctypes.c_float, ctypes.c_float, ctypes.c_float, _c_vp,
+                                            _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_grpo_workspace_bytes": (ctypes.c_size_t, [_c_i64]),
     "flce_jsd_forward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
                                         _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_vp, _c_vp,
                                         _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
@@ -240,6 +244,17 @@ def flce_jsd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse
                                  float(grad_scale), _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows,
                                  ignore_index, tp, _ptr(workspace), workspace_bytes,
                                  _stream_handle(stream))
+
+
+def flce_grpo_token_loss(logp, old_logp, ref_logp, advantages, targets, N, ignore_index, eps_low,
+                         eps_high, beta, out_token_loss, out_weights, out_loss, out_n_valid,
+                         workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the GRPO per-token objective."""
+    return load().flce_grpo_token_loss(_ptr(logp), _ptr(old_logp), _ptr(ref_logp), _ptr(advantages),
+                                       _ptr(targets), N, ignore_index, float(eps_low), float(eps_high),
+                                       float(beta), _ptr(out_token_loss), _ptr(out_weights),
+                                       _ptr(out_loss), _ptr(out_n_valid), _ptr(workspace),
+                                       workspace_bytes, _stream_handle(stream))
 
 
 def flce_quantize_e4m3_rows(x, rows, cols, q, scale, stream=None) -> int:

@@ -106,6 +106,71 @@ def linear_cross_entropy(h, W, targets, weights=None, chunk_rows: int = 256,
     return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index, transform)
 
 
+def _f32_vec(x, N, name):
+    if x is None:
+        return None
+    if not x.is_cuda or x.dtype != torch.float32 or x.shape != (N,) or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 [N] CUDA tensor")
+    return x
+
+
+def grpo_token_loss(logp, advantages, targets=None, old_logp=None, ref_logp=None,
+                    eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
+                    ignore_index: int = IGNORE_INDEX, stream=None):
+    """GRPO per-token objective on log-probs (flce_grpo_token_loss):
+    dict(token_loss[N], weights[N], loss[], n_valid[]) on device."""
+    N = logp.shape[0]
+    for x, name in ((logp, "logp"), (advantages, "advantages"), (old_logp, "old_logp"),
+                    (ref_logp, "ref_logp")):
+        _f32_vec(x, N, name)
+    dev = logp.device
+    tok = torch.empty(N, dtype=torch.float32, device=dev)
+    wts = torch.empty(N, dtype=torch.float32, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    n_valid = torch.empty((), dtype=torch.int64, device=dev)
+    st = _lib.flce_grpo_token_loss(logp, old_logp, ref_logp, advantages, targets, N, ignore_index,
+                                   eps_low, eps_high, beta, tok, wts, loss, n_valid, None, 0, stream)
+    _lib.check("flce_grpo_token_loss", st)
+    return {"token_loss": tok, "weights": wts, "loss": loss, "n_valid": n_valid}
+
+
+class GRPOLoss(torch.autograd.Function):
+    """GRPO loss of the LM head: forward log-probs, the per-token objective,
+    and a backward whose per-token weights are -d(token loss)/d(logp)."""
+
+    @staticmethod
+    def forward(ctx, h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta,
+                chunk_rows, ignore_index, transform=None):
+        out = forward(h, W, targets, None, chunk_rows, ignore_index, transform=transform)
+        tok = grpo_token_loss(out["logp"], advantages, targets, old_logp, ref_logp, eps_low, eps_high,
+                              beta, ignore_index)
+        ctx.save_for_backward(h, W, targets, out["lse"], tok["weights"], tok["n_valid"])
+        ctx.chunk_rows = chunk_rows
+        ctx.ignore_index = ignore_index
+        ctx.transform = transform
+        ctx.mark_non_differentiable(out["logp"])
+        return tok["loss"], out["logp"]
+
+    @staticmethod
+    def backward(ctx, grad_loss, grad_logp):
+        h, W, targets, lse, weights, n_valid = ctx.saved_tensors
+        n = int(n_valid.item())
+        g = float(grad_loss.item()) / n if n > 0 else 0.0
+        dH, dW = backward(h, W, targets, weights, lse, g, ctx.chunk_rows, ctx.ignore_index,
+                          need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
+                          transform=ctx.transform)
+        return dH, dW, None, None, None, None, None, None, None, None, None, None
+
+
+def grpo_loss(h, W, targets, advantages, old_logp=None, ref_logp=None, eps_low: float = 0.2,
+              eps_high: float = 0.2, beta: float = 0.0, chunk_rows: int = 256,
+              ignore_index: int = IGNORE_INDEX, transform=None):
+    """Differentiable GRPO loss of softmax(f(h W^T)) on the target tokens;
+    returns (loss, logp).  advantages, old_logp, ref_logp: float32 [N]."""
+    return GRPOLoss.apply(h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta,
+                          chunk_rows, ignore_index, transform)
+
+
 def kd_forward(h_s, W_s, h_t, W_t, targets=None, weights=None, chunk_rows: int = 256,
                ignore_index: int = IGNORE_INDEX, transform=None,
                workspace: torch.Tensor | None = None, stream=None):

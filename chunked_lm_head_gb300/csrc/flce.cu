@@ -45,6 +45,35 @@ __global__ void prep_kernel(const int64_t* __restrict__ targets, int N, int V, l
   }
 }
 
+// This block's sum of `contrib` and of `cnt` over its SMALL_THREADS threads,
+// in a fixed order (warp shuffles, then the warps in turn), stored at
+// blk_sum / blk_cnt[blockIdx.x].  Every thread of the block must call it.
+__device__ __forceinline__ void block_sum_store(double contrib, long long cnt, double* blk_sum,
+                                                long long* blk_cnt) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
+    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
+  }
+  __shared__ double ssum[SMALL_THREADS / 32];
+  __shared__ long long scnt[SMALL_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) {
+    ssum[threadIdx.x >> 5] = contrib;
+    scnt[threadIdx.x >> 5] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0;
+    long long c = 0;
+    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
+      a += ssum[w];
+      c += scnt[w];
+    }
+    blk_sum[blockIdx.x] = a;
+    blk_cnt[blockIdx.x] = c;
+  }
+}
+
 // Split-vocabulary combine: lse = M + log sum_s s_s 2^(m_s - M) (log2 domain,
 // converted to natural log), logp = z_t - lse on non-ignored rows, and this
 // block's share of sum(w * logp) and of the valid-row count.
@@ -77,28 +106,7 @@ __global__ void combine_kernel(const float2* __restrict__ part, int S, int N,
       contrib = static_cast<double>(weights ? weights[i] : 1.f) * static_cast<double>(logp);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
-    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
-  }
-  __shared__ double ssum[SMALL_THREADS / 32];
-  __shared__ long long scnt[SMALL_THREADS / 32];
-  if ((threadIdx.x & 31) == 0) {
-    ssum[threadIdx.x >> 5] = contrib;
-    scnt[threadIdx.x >> 5] = cnt;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0;
-    long long c = 0;
-    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
-      a += ssum[w];
-      c += scnt[w];
-    }
-    blk_sum[blockIdx.x] = a;
-    blk_cnt[blockIdx.x] = c;
-  }
+  block_sum_store(contrib, cnt, blk_sum, blk_cnt);
 }
 
 // Loss = -sum(w logp) / n_valid over the block partials, in a fixed order
@@ -286,28 +294,7 @@ __global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* _
       contrib = -static_cast<double>(weights ? weights[i] : 1.f) * static_cast<double>(kl);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
-    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
-  }
-  __shared__ double ssum[SMALL_THREADS / 32];
-  __shared__ long long scnt[SMALL_THREADS / 32];
-  if ((threadIdx.x & 31) == 0) {
-    ssum[threadIdx.x >> 5] = contrib;
-    scnt[threadIdx.x >> 5] = cnt;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0;
-    long long c = 0;
-    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
-      a += ssum[w];
-      c += scnt[w];
-    }
-    blk_sum[blockIdx.x] = a;
-    blk_cnt[blockIdx.x] = c;
-  }
+  block_sum_store(contrib, cnt, blk_sum, blk_cnt);
 }
 
 // Jensen-Shannon combine: per row, the split partials (log2 units) summed in
@@ -340,28 +327,49 @@ __global__ void jsd_combine_kernel(const float2* __restrict__ pj, int S, int N,
       contrib = -static_cast<double>(weights ? weights[i] : 1.f) * static_cast<double>(jsd);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    contrib += __shfl_down_sync(0xffffffffu, contrib, off);
-    cnt += __shfl_down_sync(0xffffffffu, cnt, off);
-  }
-  __shared__ double ssum[SMALL_THREADS / 32];
-  __shared__ long long scnt[SMALL_THREADS / 32];
-  if ((threadIdx.x & 31) == 0) {
-    ssum[threadIdx.x >> 5] = contrib;
-    scnt[threadIdx.x >> 5] = cnt;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0;
-    long long c = 0;
-    for (int w = 0; w < SMALL_THREADS / 32; ++w) {
-      a += ssum[w];
-      c += scnt[w];
+  block_sum_store(contrib, cnt, blk_sum, blk_cnt);
+}
+
+// GRPO per-token objective on the sampled tokens' log-probs (one thread per
+// row; flce_grpo_token_loss states the formula): the masked token loss, the
+// weights -d(token loss)/d(logp) for the backward, and this block's sums of
+// -(token loss) and of the mask (the final kernel negates the sum).
+__global__ void grpo_token_kernel(const float* __restrict__ logp, const float* __restrict__ old_logp,
+                                  const float* __restrict__ ref_logp, const float* __restrict__ adv,
+                                  const int64_t* __restrict__ targets, int N, long long ignore,
+                                  float eps_low, float eps_high, float beta,
+                                  float* __restrict__ out_tok, float* __restrict__ out_w,
+                                  double* __restrict__ blk_sum, long long* __restrict__ blk_cnt) {
+  const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
+  double contrib = 0.0;
+  long long cnt = 0;
+  if (i < N) {
+    const bool valid = targets == nullptr || targets[i] != ignore;
+    float tok = 0.f, wt = 0.f;
+    if (valid) {
+      const float lp = logp[i];
+      const float A = adv[i];
+      const float r = old_logp != nullptr ? expf(lp - old_logp[i]) : 1.f;
+      const float un = r * A;
+      const float cl = fminf(fmaxf(r, 1.f - eps_low), 1.f + eps_high) * A;
+      const float obj = fminf(un, cl);
+      const float dobj = un <= cl ? un : 0.f;  // the clipped branch is constant in logp
+      float kl = 0.f, dkl = 0.f;
+      if (ref_logp != nullptr && beta != 0.f) {
+        const float d = ref_logp[i] - lp;
+        const float em1 = expm1f(d);
+        kl = em1 - d;  // exp(d) - d - 1 without cancellation near d = 0
+        dkl = -em1;    // d kl / d logp = 1 - exp(d)
+      }
+      tok = beta * kl - obj;
+      wt = dobj - beta * dkl;
+      cnt = 1;
+      contrib = -static_cast<double>(tok);
     }
-    blk_sum[blockIdx.x] = a;
-    blk_cnt[blockIdx.x] = c;
+    if (out_tok) out_tok[i] = tok;
+    if (out_w) out_w[i] = wt;
   }
+  block_sum_store(contrib, cnt, blk_sum, blk_cnt);
 }
 
 // Per-row e4m3 quantisation (one warp per row): scale = max|x| / 448 (1 for
@@ -430,13 +438,14 @@ constexpr int kDefaultSms = 152;
 
 enum Kind {
   K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COMPACT, K_GATHER,
-  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_JSD_FWD, K_JSD_DLOGITS, K_COUNT
+  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_JSD_FWD, K_JSD_DLOGITS, K_GRPO, K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {"prep_targets",  "fwd_logits_lse", "fwd_combine",
                                          "fwd_loss",      "bwd_dlogits",    "bwd_dH",
                                          "bwd_dH_reduce", "bwd_dW",         "bwd_compact_rows",
                                          "bwd_gather_rows", "kd_fwd_logits",  "kd_bwd_dlogits",
-                                         "quantize_e4m3", "jsd_fwd_terms",  "jsd_bwd_dlogits"};
+                                         "quantize_e4m3", "jsd_fwd_terms",  "jsd_bwd_dlogits",
+                                         "grpo_token_loss"};
 
 struct ProfRec {
   int kind;
@@ -1874,6 +1883,51 @@ flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_
   return distill_backward(true, beta, kl_sm, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s,
                           lse_t, grad_scale, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
                           workspace, workspace_bytes, stream);
+}
+
+size_t flce_grpo_workspace_bytes(int64_t N) {
+  if (N < 0 || N >= INT_MAX) return 0;
+  return 2 * align256(static_cast<size_t>(ceil_div(std::max<int64_t>(N, 1), SMALL_THREADS)) * 8);
+}
+
+flce_status flce_grpo_token_loss(const float* logp, const float* old_logp, const float* ref_logp,
+                                 const float* advantages, const int64_t* targets, int64_t N,
+                                 int64_t ignore_index, float eps_low, float eps_high, float beta,
+                                 float* out_token_loss, float* out_weights, float* out_loss,
+                                 int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (N < 0 || N >= INT_MAX) return FLCE_ERR_INVALID_ARG;
+  if (!(std::isfinite(eps_low) && std::isfinite(eps_high) && std::isfinite(beta)) || eps_low < 0.f ||
+      eps_low >= 1.f || eps_high < 0.f || beta < 0.f)
+    return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!logp || !advantages || (beta > 0.f && !ref_logp))) return FLCE_ERR_INVALID_ARG;
+  if (!out_token_loss && !out_weights && !out_loss && !out_n_valid) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(logp, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(advantages, 4) ||
+      !aligned(targets, 8) || !aligned(out_token_loss, 4) || !aligned(out_weights, 4) ||
+      !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int nblk = static_cast<int>(ceil_div(std::max<int64_t>(N, 1), SMALL_THREADS));
+  Workspace ws;
+  const flce_status s = get_workspace(ws, workspace, workspace_bytes, flce_grpo_workspace_bytes(N), st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  double* bsum = reinterpret_cast<double*>(wb);
+  long long* bcnt = reinterpret_cast<long long*>(wb + align256(static_cast<size_t>(nblk) * 8));
+  {
+    ProfScope ps(K_GRPO, st);
+    grpo_token_kernel<<<nblk, SMALL_THREADS, 0, st>>>(logp, old_logp, ref_logp, advantages, targets,
+                                                     static_cast<int>(N), ignore_index, eps_low, eps_high,
+                                                     beta, out_token_loss, out_weights, bsum, bcnt);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  if (out_loss || out_n_valid) {
+    ProfScope ps(K_FINAL, st);
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, nblk, out_loss,
+                                              reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
 }
 
 flce_status flce_device_status(void* stream) {

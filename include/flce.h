@@ -268,6 +268,41 @@ FLCE_API flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_
                                        int64_t ignore_index, const flce_logit_transform* transform,
                                        void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * GRPO per-token objective on the sampled tokens' log-probs.  Source: TRL
+ * v1.13 article, section "Other changes in v1.13": a fused linear GRPO loss is
+ * among TRL's fused losses; the page gives no formula.  Reading taken (the
+ * GRPO objective with a clipped probability ratio and the k3 estimate of the
+ * KL divergence to a reference policy), per row i with m[i] = (targets[i] !=
+ * ignore_index), or 1 for every row when targets == NULL:
+ *   r[i]     = exp(logp[i] - old_logp[i])      (1 when old_logp == NULL)
+ *   obj[i]   = min(r A, clip(r, 1 - eps_low, 1 + eps_high) A),  A = advantages[i]
+ *   kl[i]    = exp(ref - logp) - (ref - logp) - 1   (0 when beta == 0)
+ *   token[i] = m[i] (beta kl[i] - obj[i]),  loss = sum_i token[i] / sum_i m[i]
+ * and weights[i] = -d token[i] / d logp[i] (0 on masked rows).  old_logp and
+ * ref_logp are constants.  The loss's gradients are then
+ *   flce_backward(h, W, targets, weights, lse, 1 / n_valid, ...);
+ * with old_logp == NULL and beta == 0, weights = m A (the GRPO-style
+ * advantage-weighted loss).
+ *
+ *   logp, advantages [N] fp32 (logp from flce_forward); old_logp, ref_logp
+ *   [N] fp32 or NULL (ref_logp required when beta > 0); eps_low in [0, 1),
+ *   eps_high >= 0, beta >= 0, else FLCE_ERR_INVALID_ARG.  Outputs (each may
+ *   be NULL, not all): out_token_loss [N], out_weights [N] fp32, out_loss [1]
+ *   fp32, out_n_valid [1] int64.  Workspace: flce_grpo_workspace_bytes(N),
+ *   or NULL (stream-ordered allocation).
+ */
+FLCE_API flce_status flce_grpo_token_loss(const float* logp, const float* old_logp,
+                                          const float* ref_logp, const float* advantages,
+                                          const int64_t* targets, int64_t N, int64_t ignore_index,
+                                          float eps_low, float eps_high, float beta,
+                                          float* out_token_loss, float* out_weights,
+                                          float* out_loss, int64_t* out_n_valid, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of flce_grpo_token_loss for N rows (0 on invalid N). */
+FLCE_API size_t flce_grpo_workspace_bytes(int64_t N);
+
 /* Workspace bytes of the distillation calls (flce_kd_* and flce_jsd_*) for
  * these sizes. */
 FLCE_API size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V,
