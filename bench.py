@@ -33,10 +33,10 @@ UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "source": "fallback"}
 # DRAM bytes (read + write) per launch of each GEMM kind on the 16K SFT
-# workload, measured at full size (profiles/dram_sft_16k.md; mean over the
-# step's launches).
+# workload at 4,096-row chunks: ncu's one-pass dram__bytes_read/write
+# counters at full size, mean over one step's launches, current kernels.
 NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {
-    "fwd_logits_lse": 18.79e9, "bwd_dlogits": 3.10e9, "bwd_dH": 8.38e9, "bwd_dW": 7.66e9}
+    "fwd_logits_lse": 18.76e9, "bwd_dlogits": 3.52e9, "bwd_dH": 9.51e9, "bwd_dW": 7.66e9}
 NCU_TRAFFIC_WORKLOAD = "sft_16k"
 
 
