@@ -225,6 +225,8 @@ def gpu_arm(args):
     dH = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
     dW = torch.empty((V, H), dtype=torch.float32, device=dev)
     ws_bytes = _lib.flce_workspace_bytes(N, H, V, chunk_rows)
+    if args.fused:
+        ws_bytes = max(ws_bytes, _lib.flce_forward_backward_workspace_bytes(N, H, V, chunk_rows))
     mem0 = torch.cuda.memory_allocated(dev)
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -298,6 +300,12 @@ def gpu_arm(args):
                 h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp,
                 lse.data_ptr(), lse_t.data_ptr(), g, dH.data_ptr(), dW.data_ptr(), N, V, chunk_rows,
                 -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
+            return
+        if args.fused:
+            check("flce_forward_backward", lib.flce_forward_backward(
+                h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr, 1.0,
+                logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
+                dW.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
             return
         check("flce_forward_ex", lib.flce_forward_ex(
             h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr,
@@ -382,7 +390,7 @@ def gpu_arm(args):
         logp_host.copy_(out["logp"], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 10))
-    if Ht or tf is not None or args.forward_only:
+    if Ht or tf is not None or args.forward_only or args.fused:
         e2e_steps = 0
     e2e_ms = None
     if e2e_steps:
@@ -398,6 +406,42 @@ def gpu_arm(args):
             e3.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = reduce_max(e2.elapsed_time(e3), device=dev) / e2e_steps
+    # ---- the same step through flce_forward_backward (no logits recompute),
+    # timed after the headline with a workspace of its own
+    fused_line = None
+    if not (Ht or tf is not None or args.forward_only or args.fused or args.e4m3):
+        fws = _lib.flce_forward_backward_workspace_bytes(N, H, V, chunk_rows)
+        fwork = torch.empty(fws, dtype=torch.uint8, device=dev)
+
+        def fstep():
+            wp = None if w is None else w.data_ptr()
+            check("flce_forward_backward", lib.flce_forward_backward(
+                h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, None, 1.0,
+                logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
+                dW.data_ptr(), fwork.data_ptr(), fws, sh))
+
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fstep()
+            torch.cuda.synchronize(dev)
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(args.steps):
+                fstep()
+            f1.record(stream)
+        torch.cuda.synchronize(dev)
+        f_ms = reduce_max(f0.elapsed_time(f1), device=dev) / args.steps
+        fused_line = {"call": "flce_forward_backward", "value": whole_job_rate(N, ws, f_ms), "unit": UNIT,
+                      "ms_per_step": f_ms,
+                      "tflops_executed": 6.0 * N * V * H / (f_ms / 1e3) / 1e12,
+                      "note": "same loss, logp and gradients without the backward's logits recompute "
+                              "(6 N V H tensor FLOPs instead of 8 N V H)"}
+        del fwork
+        st = _lib.flce_device_status(sh)
+        if st != 0:
+            raise RuntimeError(f"device status after the fused steps: {_lib.STATUS_NAMES.get(st)}")
+
     h2d = N * H * 2 + N * 8 + (0 if w_host is None else N * 4)
     d2h = 4 + N * 4
 
@@ -410,6 +454,9 @@ def gpu_arm(args):
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     if args.forward_only:
         flops_step = {"fwd_logits_lse": 2.0 * N * V * H}
+    if args.fused:  # no recompute: the forward GEMM, dH and dW (bwd_dlogits is elementwise)
+        flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dH": 2.0 * nv * V * H,
+                      "bwd_dW": 2.0 * nv * V * H}
     if Ht and args.jsd_beta:  # both heads twice in the forward (lse, then mixture terms)
         flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "jsd_fwd_terms": 2.0 * N * V * (H + Ht),
                       "jsd_bwd_dlogits": 2.0 * N * V * (H + Ht),
@@ -427,7 +474,7 @@ def gpu_arm(args):
         kern[k]["share"] = kern[k]["ms_per_step"] / tot if tot else None
         if k in flops_step:
             kern[k]["tflops"] = flops_step[k] / (kern[k]["ms_per_step"] / 1e3) / 1e12
-    dom = max((k for k in kern if k in GEMM_KINDS), key=lambda k: kern[k]["ms_per_step"])
+    dom = max((k for k in kern if k in GEMM_KINDS and k in flops_step), key=lambda k: kern[k]["ms_per_step"])
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     peak_note = "measured bf16_tflops_sustained (kernel timed inside a long step)"
     if args.e4m3:  # e4m3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
@@ -437,6 +484,7 @@ def gpu_arm(args):
     achieved = kern[dom]["tflops"]
     traffic = NCU_TRAFFIC_BYTES_PER_LAUNCH.get(dom) if (wl.name == NCU_TRAFFIC_WORKLOAD
                                                          and chunk_rows == 4096 and not Ht
+                                                         and not args.fused
                                                          and tf is None and not args.forward_only
                                                          ) else None
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
@@ -462,7 +510,8 @@ def gpu_arm(args):
             "config": {"workload": wl.name + (f"+kd_teacher_H{Ht}" if Ht else "")
                        + (f"+jsd_beta{args.jsd_beta:g}" if Ht and args.jsd_beta else "")
                        + (f"+transform({args.transform})" if args.transform else "")
-                       + ("+forward_only" if args.forward_only else "") + ("+e4m3" if args.e4m3 else ""),
+                       + ("+forward_only" if args.forward_only else "") + ("+e4m3" if args.e4m3 else "")
+                       + ("+fused_no_recompute(6NVH)" if args.fused else ""),
                        "N": N, "H": H, "V": V, "chunk_rows": chunk_rows,
                        "targets": wl.targets, "l2": "inputs larger than L2 (W alone "
                        f"{V * H * 2 / 1e9:.2f} GB > 129 MB); no flush",
@@ -479,6 +528,7 @@ def gpu_arm(args):
                 "value": whole_job_rate(N, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": gpu_launches,
+            "fused_no_recompute": fused_line,
             "kernel_events": args.kernel_events,
             "peak_extra_mem_bytes": int(extra_mem),
             "workspace_bytes": ws_bytes,
@@ -512,6 +562,9 @@ def main():
     ap.add_argument("--kd-teacher-hidden", type=int, default=0,
                     help="time the distillation step instead: the workload's head is the student, "
                          "a teacher head of this hidden size is added")
+    ap.add_argument("--fused", action="store_true",
+                    help="time flce_forward_backward (no logits recompute: 6 N V H tensor FLOPs) "
+                         "instead of flce_forward + flce_backward")
     ap.add_argument("--jsd-beta", type=float, default=0.0,
                     help="with --kd-teacher-hidden: Jensen-Shannon distillation with this mixture "
                          "weight in (0, 1) instead of KL(teacher || student)")

@@ -5,5 +5,5 @@ package holds its ctypes binding, a thin torch-facing API and the seeded
 synthetic workloads.
 """
 from .api import (IGNORE_INDEX, GRPOLoss, LinearCrossEntropy, backward, forward,  # noqa: F401
-                  grpo_loss, grpo_token_loss, jsd_backward, jsd_forward, kd_backward, kd_forward,
+                  forward_backward, grpo_loss, grpo_token_loss, jsd_backward, jsd_forward, kd_backward, kd_forward,
                   linear_cross_entropy, workspace_bytes)

@@ -61,6 +61,11 @@ SIGNATURES = {
     "flce_forward_static_scratch": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                                    _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "flce_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
+    "flce_forward_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
+                                             _c_i64, _c_i64, _c_vp, ctypes.c_float, _c_vp, _c_vp,
+                                             _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
+                                             _c_vp]),
+    "flce_forward_backward_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
     "flce_backward_plan": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int32,
                                           ctypes.c_int32, _c_vp]),
     "flce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -257,6 +262,19 @@ def flce_grpo_token_loss(logp, old_logp, ref_logp, advantages, targets, N, ignor
                                        workspace_bytes, _stream_handle(stream))
 
 
+def flce_forward_backward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform,
+                          grad_scale, out_logp, out_lse, out_loss, out_n_valid, dH, dW,
+                          workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the forward + backward without the logits recompute."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_forward_backward(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), N, H, V,
+                                     chunk_rows, ignore_index, tp, float(grad_scale), _ptr(out_logp),
+                                     _ptr(out_lse), _ptr(out_loss), _ptr(out_n_valid), _ptr(dH),
+                                     _ptr(dW), _ptr(workspace), workspace_bytes,
+                                     _stream_handle(stream))
+
+
 def flce_quantize_e4m3_rows(x, rows, cols, q, scale, stream=None) -> int:
     """Raw C call: per-row e4m3 quantisation."""
     return load().flce_quantize_e4m3_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scale),
@@ -286,6 +304,10 @@ def flce_forward_static_scratch(h, W, targets, weights, N, H, V, chunk_rows, ign
 
 def flce_workspace_bytes(N, H, V, chunk_rows) -> int:
     return int(load().flce_workspace_bytes(N, H, V, chunk_rows))
+
+
+def flce_forward_backward_workspace_bytes(N, H, V, chunk_rows) -> int:
+    return int(load().flce_forward_backward_workspace_bytes(N, H, V, chunk_rows))
 
 
 class BackwardPlanInfo(ctypes.Structure):

@@ -69,6 +69,30 @@ def backward(h, W, targets, weights, lse, grad_scale: float, chunk_rows: int = 2
     return dH, dW
 
 
+def forward_backward(h, W, targets, weights=None, chunk_rows: int = 4096,
+                     ignore_index: int = IGNORE_INDEX, grad_scale: float = 1.0, need_dH: bool = True,
+                     need_dW: bool = True, workspace: torch.Tensor | None = None, stream=None,
+                     transform=None):
+    """Loss and its gradients in one call without the logits recompute
+    (flce_forward_backward): dict(logp, lse, loss, n_valid, dH, dW)."""
+    _check(h, W, targets, weights)
+    N, H = h.shape
+    V = W.shape[0]
+    dev = h.device
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    n_valid = torch.empty((), dtype=torch.int64, device=dev)
+    dH = torch.empty_like(h) if need_dH else None
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev) if need_dW else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.flce_forward_backward(h, W, targets, weights, N, H, V, chunk_rows, ignore_index,
+                                    transform, grad_scale, logp, lse, loss, n_valid, dH, dW,
+                                    workspace, ws_bytes, stream)
+    _lib.check("flce_forward_backward", st)
+    return {"logp": logp, "lse": lse, "loss": loss, "n_valid": n_valid, "dH": dH, "dW": dW}
+
+
 class LinearCrossEntropy(torch.autograd.Function):
     """loss = -sum(w * logp) / n_valid with logits recomputed in backward.
 

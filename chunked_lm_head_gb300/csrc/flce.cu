@@ -77,8 +77,10 @@ __device__ __forceinline__ void block_sum_store(double contrib, long long cnt, d
 // Split-vocabulary combine: lse = M + log sum_s s_s 2^(m_s - M) (log2 domain,
 // converted to natural log), logp = z_t - lse on non-ignored rows, and this
 // block's share of sum(w * logp) and of the valid-row count.
+// Rows [0, N) of the arrays passed (callers offset them for a row range);
+// `stride` is the distance between two splits' partials of one row.
 template <bool kLong>
-__global__ void combine_kernel(const float2* __restrict__ part, int S, int N,
+__global__ void combine_kernel(const float2* __restrict__ part, int S, int stride, int N,
                                const float* __restrict__ zt, const int64_t* __restrict__ targets,
                                const float* __restrict__ weights, long long ignore,
                                float* __restrict__ out_logp, float* __restrict__ out_lse,
@@ -89,10 +91,10 @@ __global__ void combine_kernel(const float2* __restrict__ part, int S, int N,
   long long cnt = 0;
   if (i < N) {
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, part[static_cast<idx_t>(s) * N + i].x);
+    for (int s = 0; s < S; ++s) M = fmaxf(M, part[static_cast<idx_t>(s) * stride + i].x);
     float sum = 0.f;
     for (int s = 0; s < S; ++s) {
-      const float2 q = part[static_cast<idx_t>(s) * N + i];
+      const float2 q = part[static_cast<idx_t>(s) * stride + i];
       sum += q.y * exp2f(q.x - M);
     }
     const float lse = (M + log2f(sum)) * kLn2;
@@ -370,6 +372,74 @@ __global__ void grpo_token_kernel(const float* __restrict__ logp, const float* _
     if (out_w) out_w[i] = wt;
   }
   block_sum_store(contrib, cnt, blk_sum, blk_cnt);
+}
+
+// dlogits of one row block from the forward's stored exponentials, in place:
+// E[r][v] = 2^(u log2e - mx[r][v / 32]) (bf16) becomes
+//   D[r][v] = (E 2^(mx - lse log2e) - [v == t]) * m * w * g * f'(z),
+// g = grad_scale / max(n_valid, 1) with n_valid read on the device.  The
+// target column is formed from the exact fp32 target logit instead (so that
+// p_t - 1 keeps its precision when p_t is near 1).  Grid: (column blocks of
+// 256 threads x 16 columns, rows); a thread's 16 columns share one chunk max.
+constexpr int FUSED_COLS_PER_THREAD = 16;
+
+template <bool kLong>
+__global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __restrict__ mx, int ldD,
+                                     int V, int row0, const int64_t* __restrict__ targets,
+                                     const float* __restrict__ weights, const float* __restrict__ lse,
+                                     const float* __restrict__ zt, long long ignore,
+                                     const int* __restrict__ n_valid, float grad_scale, int tf_softcap,
+                                     float tf_a, float tf_b, float tf_d) {
+  using idx_t = typename std::conditional<kLong, long long, int>::type;
+  const int r = blockIdx.y;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * FUSED_COLS_PER_THREAD;
+  if (c >= ldD) return;
+  const int row = row0 + r;
+  const long long t = targets[row];
+  const bool valid = t != ignore;
+  const float g = grad_scale / fmaxf(1.f, static_cast<float>(*n_valid));
+  const float scale = valid ? (weights ? weights[row] : 1.f) * g : 0.f;
+  uint4* slot = reinterpret_cast<uint4*>(E + static_cast<idx_t>(r) * ldD + c);
+  uint4 q[2] = {slot[0], slot[1]};
+  const float cmL = mx[static_cast<idx_t>(r) * (ldD / 32) + c / 32];
+  const float nlse2 = -lse[row] * kLog2e;
+  const float base = ex2_approx(cmL + nlse2);  // 2^(chunk max - lse), both x log2(e)
+  const float lin = tf_softcap ? 1.f : tf_a;    // linear transforms: du/dz = tf_a
+  const long long tj = t - c;                   // target column inside this thread's 16, if any
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w4[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+    float d[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t bits = (k & 1) ? (w4[k >> 1] & 0xffff0000u) : (w4[k >> 1] << 16);
+      const float ev = __uint_as_float(bits);
+      const int j = 8 * h + k;
+      float dk = 0.f;
+      if (scale != 0.f && c + j < V) {
+        if (tj == j) {
+          const float ut = zt[row];
+          const float pt = ex2_approx(fmaf(ut, kLog2e, nlse2));
+          const float fd = tf_softcap ? tf_d * (1.f - (ut / tf_b) * (ut / tf_b)) : lin;
+          dk = (pt - 1.f) * scale * fd;
+        } else if (ev > 0.f) {
+          float fd = lin;
+          if (tf_softcap) {  // u = ln(E) + chunk max, tanh(a z) = u / b
+            const float u = (__log2f(ev) + cmL) * kLn2;
+            fd = tf_d * (1.f - (u / tf_b) * (u / tf_b));
+          }
+          dk = ev * base * scale * fd;
+        }
+      }
+      d[k] = dk;
+    }
+    q[h].x = pack_bf16x2(d[0], d[1]);
+    q[h].y = pack_bf16x2(d[2], d[3]);
+    q[h].z = pack_bf16x2(d[4], d[5]);
+    q[h].w = pack_bf16x2(d[6], d[7]);
+  }
+  slot[0] = q[0];
+  slot[1] = q[1];
 }
 
 // Per-row e4m3 quantisation (one warp per row): scale = max|x| / 448 (1 for
@@ -1114,6 +1184,74 @@ flce_status block_dh_finish(const DhDwStage& a, int row0, int rows, const int* r
   return FLCE_OK;
 }
 
+// ---- forward + backward in one call without the logits recompute
+
+// Row blocks of R rows over the whole vocabulary: the forward GEMM keeps the
+// block's exponentials (bf16, R x ldD, within the dlogits budget) and chunk
+// maxima (fp32, R x ldD / 32), so the backward needs no second logits GEMM.  Taken
+// when the budget holds at least 2,048 rows (or every row) of the full
+// vocabulary; otherwise the call runs the forward and the tiled backward.
+struct FusedPlan {
+  bool fused = false;
+  long long R = 0, ldD = 0;
+  FwdPlan f;
+  BwdPlan b;  // dH / dW stages over one slab of V columns
+};
+
+FusedPlan plan_fused(long long N, long long H, long long V, long long chunk_rows, int workers, int tm) {
+  FusedPlan fp;
+  N = std::max(1LL, N);
+  const long long nr = round_up(N, BM);
+  // the block is the caller's chunk (rounded up to 128 rows): exponentials in
+  // its dlogits budget, the chunk maxima (1/16 of it) on top
+  // (at most 32,768 rows: the dlogits pass puts one row per grid row)
+  fp.R = std::min(std::min(round_up(std::max(1LL, chunk_rows), BM), nr), 32768LL);
+  fp.ldD = round_up(V, 32);
+  fp.fused = fp.R >= std::min<long long>(2048, nr);
+  if (!fp.fused) return fp;
+  fp.f = plan_forward(fp.R, H, V, workers, tm);
+  fp.b.R = fp.R;
+  fp.b.Vs = V;
+  fp.b.n_slabs = 1;
+  fp.b.ldD = fp.ldD;
+  const long long kb = ceil_div(V, BK);
+  int sp = dh_split_count(ceil_div(fp.R, tm) * ceil_div(H, BN), kb, workers);
+  fp.b.dh_kb_per_split = static_cast<int>(ceil_div(kb, sp));
+  fp.b.dh_splits = static_cast<int>(ceil_div(kb, fp.b.dh_kb_per_split));
+  fp.b.dh_f32 = fp.b.dh_splits > 1;
+  return fp;
+}
+
+struct FusedLayout {
+  size_t zt = 0, part = 0, bsum = 0, bcnt = 0, bad = 0, E = 0, mx = 0, lse = 0, dh_part = 0, idx = 0,
+         blk = 0, count = 0, total = 0;
+};
+FusedLayout fused_layout(long long N, long long H, const FusedPlan& fp) {
+  FusedLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  L.zt = take(static_cast<size_t>(N) * 4);
+  L.part = take(static_cast<size_t>(fp.f.S) * N * 8);
+  // loss block sums: one segment of ceil(R / 256) per row block
+  const size_t nblk = static_cast<size_t>(ceil_div(std::max(1LL, N), fp.R) * ceil_div(fp.R, SMALL_THREADS));
+  L.bsum = take(nblk * 8);
+  L.bcnt = take(nblk * 8);
+  L.bad = take(256);
+  L.E = take(static_cast<size_t>(fp.R) * fp.ldD * 2);
+  L.mx = take(static_cast<size_t>(fp.R) * (fp.ldD / 32) * 4);
+  L.lse = take(static_cast<size_t>(N) * 4);
+  L.dh_part = take(fp.b.dh_f32 ? static_cast<size_t>(fp.b.dh_splits) * fp.R * H * 4 : 0);
+  L.idx = take(static_cast<size_t>(N) * 4);
+  L.blk = take(static_cast<size_t>(ceil_div(std::max(1LL, N), COMPACT_ROWS_PER_BLOCK)) * 4);
+  L.count = take(256);
+  L.total = o;
+  return L;
+}
+
 // Cross-entropy forward tail: per-row combine of the split partials, then
 // the deterministic loss / count reduction.
 flce_status ce_forward_tail(bool kLong, const FwdPlan& f, int N, const float2* part, const float* zt,
@@ -1123,10 +1261,10 @@ flce_status ce_forward_tail(bool kLong, const FwdPlan& f, int N, const float2* p
   if (N > 0) {
     ProfScope ps(K_COMBINE, st);
     if (kLong)
-      combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, zt, targets, weights, ignore,
+      combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
                                                              out_logp, out_lse, bsum, bcnt);
     else
-      combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, zt, targets, weights, ignore,
+      combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
                                                               out_logp, out_lse, bsum, bcnt);
     FLCE_CUDA_TRY(cudaGetLastError());
   }
@@ -1281,12 +1419,15 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
                       out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap);
 }
 
-flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
-                             const float* weights, const float* lse, float grad_scale,
-                             flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
-                             int64_t chunk_rows, int64_t ignore_index,
-                             const flce_logit_transform* transform, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+// The backward; count_scale (device int64, or NULL) divides grad_scale by
+// max(*count_scale, 1) on the device.
+static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                 const float* weights, const float* lse, float grad_scale,
+                                 flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
+                                 int64_t chunk_rows, int64_t ignore_index,
+                                 const flce_logit_transform* transform, void* workspace,
+                                 size_t workspace_bytes, void* stream,
+                                 const long long* count_scale) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
@@ -1347,6 +1488,7 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
   base.weights = weights;
   base.lse = lse;
   base.grad_scale = grad_scale;
+  base.count_scale = count_scale;
   base.ignore_index = ignore_index;
   base.D = Dbuf;
   base.dH = dH;
@@ -1454,6 +1596,16 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
   return FLCE_OK;
 }
 
+flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                             const float* weights, const float* lse, float grad_scale,
+                             flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
+                             int64_t chunk_rows, int64_t ignore_index,
+                             const flce_logit_transform* transform, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return backward_impl(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                       ignore_index, transform, workspace, workspace_bytes, stream, nullptr);
+}
+
 flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
                          const float* weights, int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
                          int64_t ignore_index, float* out_logp, float* out_lse, float* out_loss,
@@ -1470,6 +1622,222 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
                           void* stream) {
   return flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
                           ignore_index, nullptr, workspace, workspace_bytes, stream);
+}
+
+// Workspace of the fallback (forward, then the tiled backward with the count
+// on the device): the larger of the two, plus lse and n_valid scratch.
+static size_t fallback_workspace(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int workers,
+                                 int tm) {
+  const size_t fwd = fwd_layout(N, plan_forward(N, H, V, workers, tm)).total;
+  const size_t bwd = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, tm)).total;
+  return std::max(fwd, bwd) + align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4) + 256;
+}
+
+size_t flce_forward_backward_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
+  if (!sizes_ok(N, H, V)) return 0;
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const FusedPlan fp = plan_fused(N, H, V, chunk_rows, workers, BM * cg);
+  if (fp.fused) return fused_layout(N, H, fp).total;
+  return fallback_workspace(N, H, V, chunk_rows, workers, BM * cg);
+}
+
+flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                  const float* weights, int64_t N, int64_t H, int64_t V,
+                                  int64_t chunk_rows, int64_t ignore_index,
+                                  const flce_logit_transform* transform, float grad_scale,
+                                  float* out_logp, float* out_lse, float* out_loss,
+                                  int64_t* out_n_valid, flce_bf16* dH, float* dW, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
+  GemmParams tfp{};
+  if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
+  if (!dH && !dW) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!h || !W || !targets)) return FLCE_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_scale)) return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(dH, 16) || !aligned(dW, 16) ||
+      !aligned(targets, 8) || !aligned(weights, 4) || !aligned(out_logp, 4) || !aligned(out_lse, 4) ||
+      !aligned(out_loss, 4) || !aligned(out_n_valid, 8))
+    return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int cg = cta_group();
+  const int workers = device_workers(cg);
+  const int tm = BM * cg;
+  const FusedPlan fp = plan_fused(N, H, V, chunk_rows, workers, tm);
+  if (!fp.fused || N == 0) {
+    // forward (lse and n_valid into scratch when the caller wants neither),
+    // then the tiled backward with grad_scale / n_valid on the device
+    Workspace ws;
+    const size_t need = fallback_workspace(N, H, V, chunk_rows, workers, tm);
+    flce_status s = get_workspace(ws, workspace, workspace_bytes, need, st);
+    if (s != FLCE_OK) return s;
+    uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+    const size_t inner = need - align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4) - 256;
+    float* lse = out_lse ? out_lse : reinterpret_cast<float*>(wb + inner);
+    int64_t* nv = out_n_valid ? out_n_valid
+                              : reinterpret_cast<int64_t*>(wb + inner + align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4));
+    s = forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, lse, out_loss, nv,
+                     wb, inner, stream, kFwdPartialsCap);
+    if (s != FLCE_OK) return s;
+    return backward_impl(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows, ignore_index,
+                         transform, wb, inner, stream, reinterpret_cast<const long long*>(nv));
+  }
+  const FusedLayout L = fused_layout(N, H, fp);
+  Workspace ws;
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  if (s != FLCE_OK) return s;
+  uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
+  float* zt = reinterpret_cast<float*>(wb + L.zt);
+  float2* part = reinterpret_cast<float2*>(wb + L.part);
+  double* bsum = reinterpret_cast<double*>(wb + L.bsum);
+  long long* bcnt = reinterpret_cast<long long*>(wb + L.bcnt);
+  int* bad = reinterpret_cast<int*>(wb + L.bad);
+  uint16_t* E = reinterpret_cast<uint16_t*>(wb + L.E);
+  float* mx = reinterpret_cast<float*>(wb + L.mx);
+  float* lse = out_lse ? out_lse : reinterpret_cast<float*>(wb + L.lse);
+  float* dh_part = fp.b.dh_f32 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
+  int* cidx = reinterpret_cast<int*>(wb + L.idx);
+  int* cblk = reinterpret_cast<int*>(wb + L.blk);
+  int* ccount = reinterpret_cast<int*>(wb + L.count);
+  const int Ni = static_cast<int>(N);
+  const bool validate = validate_env();
+
+  if (validate) FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
+  {
+    ProfScope ps(K_PREP, st);
+    prep_kernel<<<static_cast<int>(ceil_div(N, SMALL_THREADS)), SMALL_THREADS, 0, st>>>(
+        targets, Ni, static_cast<int>(V), ignore_index, zt, validate ? bad : nullptr);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  if (validate) {
+    int nbad = 0;
+    FLCE_CUDA_TRY(cudaMemcpyAsync(&nbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st));
+    FLCE_CUDA_TRY(cudaStreamSynchronize(st));
+    if (nbad != 0) return FLCE_ERR_BAD_TARGET;
+  }
+  {  // n_valid on the device, before any dlogits
+    const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
+    ProfScope ps(K_COMPACT, st);
+    compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk);
+    FLCE_CUDA_TRY(cudaGetLastError());
+    compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk, nblk, cidx, ccount);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  int* err = nullptr;
+  FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
+  CUtensorMap h_k, W_k, W_mn, h_mn, dW_map, dhp_map;
+  if (!make_map(&h_k, h, H, N, H, BK, BM) || !make_map(&W_k, W, H, V, H, BK, BN / cg) ||
+      !make_map(&W_mn, W, H, V, H, 64, BK) || !make_map(&h_mn, h, H, N, H, 64, BK))
+    return FLCE_ERR_CUDA;
+  if (dW && !make_map_t(&dW_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, H, V, H, 32, 32))
+    return FLCE_ERR_CUDA;
+  if (dH && fp.b.dh_f32 &&
+      !make_map_t(&dhp_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dh_part, H, fp.b.dh_splits * fp.R, H, 32, 32))
+    return FLCE_ERR_CUDA;
+  const bool kLong = static_cast<long long>(N) * V >= INT_MAX || fp.R * fp.ldD >= INT_MAX ||
+                     static_cast<long long>(N) * H >= INT_MAX || static_cast<long long>(V) * H >= INT_MAX ||
+                     static_cast<long long>(fp.b.dh_splits) * fp.R * H >= INT_MAX ||
+                     static_cast<long long>(fp.f.S) * N >= INT_MAX;
+
+  GemmParams base{};
+  base.N = Ni;
+  base.H = static_cast<int>(H);
+  base.V = static_cast<int>(V);
+  base.ldD = static_cast<int>(fp.ldD);
+  base.targets = targets;
+  base.weights = weights;
+  base.lse = lse;
+  base.ignore_index = ignore_index;
+  base.D = E;
+  base.dH = dH;
+  base.dH_part = dh_part;
+  base.dW = dW;
+  base.err = err;
+  base.rows_cap = static_cast<int>(fp.R);
+  base.tf_softcap = tfp.tf_softcap;
+  base.tf_a = tfp.tf_a;
+  base.tf_b = tfp.tf_b;
+  base.tf_d = tfp.tf_d;
+  const DhDwStage dhdw{cg, workers, tm, kLong, &fp.b, H, V, dh_part, dH, dW, &W_mn, &dW_map, &dhp_map};
+  {  // the last block's segment may be shorter than the others: zero it whole
+    const long long per = ceil_div(fp.R, SMALL_THREADS);
+    const long long last = (ceil_div(N, fp.R) - 1) * per;
+    FLCE_CUDA_TRY(cudaMemsetAsync(bsum + last, 0, per * 8, st));
+    FLCE_CUDA_TRY(cudaMemsetAsync(bcnt + last, 0, per * 8, st));
+  }
+  int block = 0;
+  for (long long row0 = 0; row0 < N; row0 += fp.R, ++block) {
+    const int rows = static_cast<int>(std::min(fp.R, N - row0));
+    GemmParams p = base;
+    p.row0 = static_cast<int>(row0);
+    p.rows = rows;
+    {  // (1) logits of the block: online lse partials, target logits, exponentials
+      GemmParams q = p;
+      q.m_tiles = static_cast<int>(ceil_div(rows, tm));
+      q.n_tiles = fp.f.n_tiles;
+      q.k_blocks = fp.f.k_blocks;
+      q.cols = fp.f.S;
+      q.n_per_unit = fp.f.tps;
+      q.kb_per_split = fp.f.k_blocks;
+      q.k_splits = 1;
+      q.num_units = q.m_tiles * fp.f.S;
+      q.group_m = std::min(16, q.m_tiles);
+      q.partials = part;
+      q.zt = zt;
+      q.mx = mx;
+      ProfScope ps(K_FWD, st);
+      FLCE_CUDA_TRY(launch_gemm<MODE_FUSED_FWD>(cg, kLong, h_k, W_k, W_k, q, std::min(q.num_units, workers), st));
+    }
+    {  // (2) the block's lse, logp and loss partials
+      ProfScope ps(K_COMBINE, st);
+      const int nb = static_cast<int>(ceil_div(rows, SMALL_THREADS));
+      const long long b0 = block * ceil_div(fp.R, SMALL_THREADS);  // this block's segment
+      if (kLong)
+        combine_kernel<true><<<nb, SMALL_THREADS, 0, st>>>(part + row0, fp.f.S, Ni, rows, zt + row0, targets + row0,
+                                                           weights ? weights + row0 : nullptr, ignore_index,
+                                                           out_logp ? out_logp + row0 : nullptr, lse + row0,
+                                                           bsum + b0, bcnt + b0);
+      else
+        combine_kernel<false><<<nb, SMALL_THREADS, 0, st>>>(part + row0, fp.f.S, Ni, rows, zt + row0, targets + row0,
+                                                            weights ? weights + row0 : nullptr, ignore_index,
+                                                            out_logp ? out_logp + row0 : nullptr, lse + row0,
+                                                            bsum + b0, bcnt + b0);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    {  // (3) exponentials -> dlogits, in place
+      ProfScope ps(K_DLOGITS, st);
+      const dim3 grid(static_cast<unsigned>(ceil_div(fp.ldD, SMALL_THREADS * FUSED_COLS_PER_THREAD)),
+                      static_cast<unsigned>(rows));
+      if (kLong)
+        fused_dlogits_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(
+            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), targets, weights, lse,
+            zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
+      else
+        fused_dlogits_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(
+            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), targets, weights, lse,
+            zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    // (4) dH[rows] = D W, dW (+)= D^T h[rows]
+    CUtensorMap D_k, D_mn;
+    if (!make_map(&D_k, E, fp.ldD, rows, fp.ldD, BK, BM) || !make_map(&D_mn, E, fp.ldD, rows, fp.ldD, 64, BK))
+      return FLCE_ERR_CUDA;
+    s = slab_dh_dw(dhdw, p, rows, block, 0, 0, static_cast<int>(V), D_k, D_mn, h_mn, st);
+    if (s != FLCE_OK) return s;
+    s = block_dh_finish(dhdw, p.row0, rows, nullptr, nullptr, 0, st);
+    if (s != FLCE_OK) return s;
+  }
+  if (out_loss || out_n_valid) {
+    ProfScope ps(K_FINAL, st);
+    // every segment entry was written: full blocks fill theirs, and the last
+    // block's unused entries are zeroed below before the loop
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt,
+                                              static_cast<int>(ceil_div(N, fp.R) * ceil_div(fp.R, SMALL_THREADS)),
+                                              out_loss, reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
 }
 
 flce_status flce_quantize_e4m3_rows(const flce_bf16* x, int64_t rows, int64_t cols, uint8_t* q,

@@ -87,7 +87,10 @@ enum Mode : int {
   // Jensen-Shannon distillation, same two-head pipeline: the per-row mixture
   // terms given both heads' log-sum-exp, and the student's dlogits
   MODE_JSD_FWD = 6,
-  MODE_JSD_DLOGITS = 7
+  MODE_JSD_DLOGITS = 7,
+  // forward that also keeps each row block's exp(logit - chunk max) in bf16
+  // (and the chunk maxima) for a backward without the logits recompute
+  MODE_FUSED_FWD = 8
 };
 template <int MODE>
 __host__ __device__ constexpr bool is_kd() {
@@ -97,7 +100,7 @@ __host__ __device__ constexpr bool is_kd() {
 // modes whose units are (row tile, vocabulary split) with per-row partials
 template <int MODE>
 __host__ __device__ constexpr bool is_split_fwd() {
-  return MODE == MODE_FWD || MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD;
+  return MODE == MODE_FWD || MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD || MODE == MODE_FUSED_FWD;
 }
 
 // bit 0 of the device error word: a bounded wait ran out.
@@ -158,6 +161,11 @@ struct GemmParams {
   // each row's KL(p_student || mixture) in natural-log units
   float jsd_beta;
   const float* kl_sm;
+  // FUSED_FWD: per row and 32-column chunk, the chunk's maximum transformed
+  // logit x log2(e), [rows_cap][ldD / 32]; the exponentials go to D
+  float* mx;
+  // DLOGITS: divide grad_scale by max(*count_scale, 1) (a count on the device)
+  const long long* count_scale;
 };
 
 // Problem extents that depend on the device-side row count of a compacted pass.
@@ -274,7 +282,7 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
     const int kk = teacher ? kb - p.k_blocks_s : kb;
     tma_ld<MODE, CG>(sA, teacher ? tA2 : tA, bar, kk * BK, p.row0 + a0);
     tma_ld<MODE, CG>(sB, teacher ? tB2 : tB, bar, kk * BK, p.v0 + b0);
-  } else if constexpr (MODE == MODE_FWD || MODE == MODE_DLOGITS) {
+  } else if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD || MODE == MODE_DLOGITS) {
     // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x B_ROWS)
     tma_ld<MODE, CG>(sA, tA, bar, kb * BK, p.row0 + a0);
     tma_ld<MODE, CG>(sB, tB, bar, kb * BK, p.v0 + b0);
@@ -286,6 +294,7 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
     for (int j = 0; j < C::B_ROWS / 64; ++j)
       tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, p.v0 + kb * BK);
   } else {
+    static_assert(MODE == MODE_DW, "every mode needs its operand loads");
     // A = D^T (vocabulary contiguous: MN-major), B = h (hidden contiguous:
     // MN-major); K runs over the chunk's rows
 #pragma unroll
@@ -552,7 +561,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // the dW pass over this chunk reads zeros past its last row
       const bool row_store = lr < min((dsh.rows + BK - 1) / BK * BK, p.rows_cap);
       float a_sc = 1.f;  // e4m3 forward: this row's dequantisation scale
-      if constexpr (MODE == MODE_FWD) {
+      if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD) {
         if (row_ok) tgt = p.targets[grow];
         if constexpr (kF8) {
           if (row_ok) a_sc = p.a_scale[grow];
@@ -563,7 +572,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tgt = p.targets[grow];
           const bool valid = tgt != p.ignore_index;
           const float w = p.weights ? p.weights[grow] : 1.f;
-          scale = valid ? w * p.grad_scale : 0.f;
+          const float inv_count =
+              p.count_scale != nullptr ? 1.f / fmaxf(1.f, static_cast<float>(*p.count_scale)) : 1.f;
+          scale = valid ? w * p.grad_scale * inv_count : 0.f;
           nl2 = -p.lse[grow] * kLog2e;
         }
       }
@@ -604,7 +615,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
           }
           const int col0 = n * BN + c * 32;
-          if constexpr (MODE == MODE_FWD) {
+          if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD) {
             if constexpr (kF8) {  // dequantise: row scale x per-vocabulary-row scale
               if (col0 + 32 <= p.V) {
                 const float4* bs = reinterpret_cast<const float4*>(p.b_scale + col0);
@@ -641,6 +652,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < 32; ++j) a += ex2_approx(fmaf(v[j], l2a, -nm));
               run_s = run_s * ex2_approx(run_m - nm) + a;
               run_m = nm;
+            }
+            if constexpr (MODE == MODE_FUSED_FWD) {
+              // 2^(u log2e - chunk max) in [0, 1] as bf16, and the chunk max,
+              // for the dlogits pass once the row's lse is known
+              if (row_ok) {
+                const float cmL = cm * l2a;
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                  const float e0 = cm == -INFINITY ? 0.f : ex2_approx(fmaf(v[j], l2a, -cmL));
+                  const float e1 = cm == -INFINITY ? 0.f : ex2_approx(fmaf(v[j + 1], l2a, -cmL));
+                  pk[j / 2] = pack_bf16x2(e0, e1);
+                }
+                uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                  if (col0 + 8 * g < p.ldD)
+                    *reinterpret_cast<uint4*>(dst + 8 * g) =
+                        make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+                if (col0 < p.ldD) p.mx[static_cast<idx_t>(lr) * (p.ldD / 32) + col0 / 32] = cmL;
+              }
             }
             const long long tj = tgt - col0;
             if (tj >= 0 && tj < 32 && tgt < p.V) {
@@ -914,7 +946,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           acc_phase ^= 1u;
         }
       }
-      if constexpr (MODE == MODE_FWD) {
+      if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD) {
         if (ok && row_ok)
           p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(run_m, run_s);
       }

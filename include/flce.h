@@ -170,6 +170,44 @@ FLCE_API flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const
                           int64_t chunk_rows, int64_t ignore_index, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/*
+ * Forward and backward of the mean loss in one call, without the backward's
+ * logits recompute.  The pages' chunked loops recompute each chunk's logits
+ * in the backward; this call is an addition of this library (no counterpart
+ * on the pages) that trades that GEMM for memory inside the same budget.
+ * Per block of R rows over the whole vocabulary, one GEMM computes the online
+ * log-sum-exp (as flce_forward) and keeps exp(u - chunk max) in bf16 plus the
+ * maximum of every 32-column chunk; once the rows' lse is known, one
+ * elementwise pass turns them into the dlogits in place (the target column
+ * from its exact fp32 logit), and the dH / dW GEMMs follow.  That is
+ * 6 N V H instead of 8 N V H tensor FLOPs; the extra rounding of the stored
+ * exponentials (bf16) is of the same size as that of the bf16 dlogits.
+ *
+ *   Outputs as flce_forward_ex (out_logp, out_lse, out_loss, out_n_valid may
+ *   be NULL) and flce_backward_ex (dH and/or dW), with
+ *     dH, dW = grad_scale * d(loss) / d(h, W),  loss = -sum m w logp / n_valid
+ *   (grad_scale = 1 for the plain mean loss; zero gradients when n_valid = 0).
+ *   chunk_rows sets the block: R = C = chunk_rows rounded up to 128 rows,
+ *   stored as R x ldD bf16 exponentials (ldD = V rounded up to 32) plus
+ *   R x ldD / 32 fp32 maxima (1/16 of that).  When C is below 2,048 rows
+ *   (and below N), the call runs flce_forward_ex and the tiled backward
+ *   instead, with grad_scale / n_valid applied on the device.
+ *   Workspace: flce_forward_backward_workspace_bytes, or NULL.
+ */
+FLCE_API flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W,
+                                           const int64_t* targets, const float* weights,
+                                           int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                                           int64_t ignore_index,
+                                           const flce_logit_transform* transform,
+                                           float grad_scale, float* out_logp, float* out_lse,
+                                           float* out_loss, int64_t* out_n_valid, flce_bf16* dH,
+                                           float* dW, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
+/* Workspace bytes of flce_forward_backward for these sizes (0 on invalid). */
+FLCE_API size_t flce_forward_backward_workspace_bytes(int64_t N, int64_t H, int64_t V,
+                                                      int64_t chunk_rows);
+
 /* flce_backward with a logit transform (NULL = identity); `lse` must come
  * from flce_forward_ex with the same transform. */
 FLCE_API flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W,

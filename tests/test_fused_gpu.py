@@ -1,0 +1,126 @@
+"""Forward + backward in one call without the logits recompute
+(flce_forward_backward) against the fp64 oracle and against the separate
+forward and (recomputing) backward."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_lm_head_gb300 import _lib
+from chunked_lm_head_gb300 import workloads as WL
+from oracle import flce_oracle as O
+
+from gpu_util import (LOSS_RTOL, assert_grad_close, assert_logp_close, np64, rel_fro, run_backward,
+                      run_forward, upload)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fused(h, W, t, w, chunk_rows, grad_scale=1.0, transform=None):
+    N, H = h.shape
+    V = W.shape[0]
+    logp = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    loss = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    nv = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    dH = torch.full((N, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dW = torch.full((V, H), float("nan"), dtype=torch.float32, device="cuda")
+    st = _lib.flce_forward_backward(h, W, t, w, N, H, V, chunk_rows, -100, transform, grad_scale, logp,
+                                    lse, loss, nv, dH, dW)
+    assert st == 0, _lib.STATUS_NAMES.get(st)
+    assert _lib.flce_device_status() == 0
+    return logp, lse, float(loss.item()), int(nv.item()), dH, dW
+
+
+def _check(inp, chunk_rows, grad_scale=1.0, transform=None):
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv, dH, dW = run_fused(h, W, t, w, chunk_rows, grad_scale, transform)
+    tf = None if transform is None else O.LogitTransform(**transform)
+    ref = O.forward(inp.h, inp.W, inp.targets, inp.weights, tf=tf)
+    assert nv == ref.n_valid
+    assert_logp_close(np64(logp), ref.logp, "logp")
+    assert_logp_close(np64(lse), ref.lse, "lse")
+    if ref.n_valid:
+        assert loss == pytest.approx(ref.loss, rel=LOSS_RTOL, abs=1e-6)
+        g = grad_scale / ref.n_valid
+        refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g, tf=tf)
+        assert_grad_close(np64(dH), refb.dH, "dH")
+        assert_grad_close(np64(dW), refb.dW, "dW")
+    else:
+        assert loss == 0.0
+        assert float(dH.float().abs().max()) == 0.0 and float(dW.abs().max()) == 0.0
+    return dH, dW
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_fused_single_block(cg, monkeypatch):
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    wl = WL.custom("fused1", 600, 256, 3000, 768, w_std=0.05, targets="zipf", ignore_frac=0.06, seed=501)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(31).uniform(0.3, 1.8, wl.N).astype(np.float32)
+    _check(inp, 768, grad_scale=2.5)
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_fused_row_blocks_ragged(cg, monkeypatch):
+    """Two 2,048-row blocks (the last 952 rows) over V = 20,000."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    wl = WL.custom("fused2", 3000, 512, 20000, 2048, w_std=0.04, targets="zipf", ignore_frac=0.05, seed=502)
+    _check(WL.make_inputs(wl), 2048)
+
+
+@pytest.mark.parametrize("transform", [{"softcap": 12.0, "temperature": 0.8},
+                                       {"scale_multiply": 1.7, "temperature": 1.3}])
+def test_fused_logit_transforms(transform):
+    wl = WL.custom("fused_tf", 700, 192, 4000, 1024, w_std=0.2, targets="zipf", ignore_frac=0.05, seed=503)
+    _check(WL.make_inputs(wl), 1024, transform=transform)
+
+
+def test_fused_confident_rows_keep_the_target_gradient():
+    """h aligned with its target's W row: p_t is about 0.99, so D_t = p_t - 1
+    is about -0.01.  The call forms it from the exact target logit; the bf16
+    exponentials alone (2^-9 relative rounding of p_t, about 0.002) would put
+    a 20 % error on it.  The recomputing backward passes the same check."""
+    r = np.random.default_rng(32)
+    N, H, V = 512, 128, 700
+    W = r.standard_normal((V, H)) * 0.3
+    t = r.integers(0, V, N)
+    h = 3.5 * W[t] / np.linalg.norm(W[t], axis=1, keepdims=True) + 0.05 * r.standard_normal((N, H))
+    inp = WL.Inputs(WL.custom("conf", N, H, V, 512), WL.f32_to_bf16_bits(h.astype(np.float32)),
+                    WL.f32_to_bf16_bits(W.astype(np.float32)), t.astype(np.int64), None,
+                    np.array([0], dtype=np.int64))
+    ref = O.forward(inp.h, inp.W, inp.targets)
+    assert np.median(np.exp(ref.logp)) > 0.985
+    _check(inp, 512)
+    hd, Wd, td, _ = upload(inp)
+    _, lse0, _, nv0 = run_forward(hd, Wd, td, None, 512)
+    dH0, dW0 = run_backward(hd, Wd, td, None, lse0, 1.0 / nv0, 512)
+    refb = O.backward(inp.h, inp.W, inp.targets, None, g=1.0 / nv0)
+    assert_grad_close(np64(dH0), refb.dH, "dH (recomputing backward)")
+
+
+def test_fused_all_rows_ignored_and_fallback_path():
+    wl = WL.custom("fused_ign", 300, 128, 1500, 512, seed=504)
+    inp = WL.make_inputs(wl)
+    inp.targets[:] = WL.IGNORE_INDEX
+    _check(inp, 512)
+    # a chunk budget below 2,048 rows (and below N): forward + tiled backward,
+    # the mean's 1 / n_valid applied on the device
+    wl = WL.custom("fused_fb", 3000, 256, 5000, 256, w_std=0.05, targets="zipf", ignore_frac=0.1, seed=505)
+    _check(WL.make_inputs(wl), 256, grad_scale=0.5)
+
+
+@pytest.mark.slow
+def test_fused_sft_16k_matches_the_recomputing_path():
+    """16,384 x 4,096 x 151,936 at 4,096-row blocks: the same loss and lse as
+    the separate forward, gradients within the parity tolerance of the
+    recomputing backward's."""
+    inp = WL.make_inputs("sft_16k")
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv, dH, dW = run_fused(h, W, t, w, 4096)
+    logp0, lse0, loss0, nv0 = run_forward(h, W, t, w, 4096)
+    dH0, dW0 = run_backward(h, W, t, w, lse0, 1.0 / nv0, 4096)
+    assert nv == nv0 == 16380
+    assert torch.allclose(lse, lse0, atol=2e-5, rtol=0) and torch.allclose(logp, logp0, atol=2e-5, rtol=0)
+    assert loss == pytest.approx(loss0, rel=1e-6)
+    assert rel_fro(np64(dH), np64(dH0)) <= 1e-2
+    assert rel_fro(np64(dW), np64(dW0)) <= 1e-2
