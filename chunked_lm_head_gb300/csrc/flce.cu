@@ -380,8 +380,8 @@ __global__ void grpo_token_kernel(const float* __restrict__ logp, const float* _
 // g = grad_scale / max(n_valid, 1) with n_valid read on the device.  The
 // target column is formed from the exact fp32 target logit instead (so that
 // p_t - 1 keeps its precision when p_t is near 1).  Grid: (column blocks of
-// 256 threads x 16 columns, rows); a thread's 16 columns share one chunk max.
-constexpr int FUSED_COLS_PER_THREAD = 16;
+// 256 threads x 32 columns, rows); a thread's 32 columns are one chunk.
+constexpr int FUSED_COLS_PER_THREAD = 32;
 
 template <bool kLong>
 __global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __restrict__ mx, int ldD,
@@ -400,14 +400,14 @@ __global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __re
   const float g = grad_scale / fmaxf(1.f, static_cast<float>(*n_valid));
   const float scale = valid ? (weights ? weights[row] : 1.f) * g : 0.f;
   uint4* slot = reinterpret_cast<uint4*>(E + static_cast<idx_t>(r) * ldD + c);
-  uint4 q[2] = {slot[0], slot[1]};
+  uint4 q[4] = {slot[0], slot[1], slot[2], slot[3]};
   const float cmL = mx[static_cast<idx_t>(r) * (ldD / 32) + c / 32];
   const float nlse2 = -lse[row] * kLog2e;
   const float base = ex2_approx(cmL + nlse2);  // 2^(chunk max - lse), both x log2(e)
   const float lin = tf_softcap ? 1.f : tf_a;    // linear transforms: du/dz = tf_a
-  const long long tj = t - c;                   // target column inside this thread's 16, if any
+  const long long tj = t - c;                   // target column inside this thread's 32, if any
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < 4; ++h) {
     uint32_t w4[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
     float d[8];
 #pragma unroll
@@ -438,8 +438,8 @@ __global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __re
     q[h].z = pack_bf16x2(d[4], d[5]);
     q[h].w = pack_bf16x2(d[6], d[7]);
   }
-  slot[0] = q[0];
-  slot[1] = q[1];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) slot[h] = q[h];
 }
 
 // Per-row e4m3 quantisation (one warp per row): scale = max|x| / 448 (1 for
