@@ -124,3 +124,32 @@ def test_fused_sft_16k_matches_the_recomputing_path():
     assert loss == pytest.approx(loss0, rel=1e-6)
     assert rel_fro(np64(dH), np64(dH0)) <= 1e-2
     assert rel_fro(np64(dW), np64(dW0)) <= 1e-2
+
+
+@pytest.mark.slow
+def test_fused_long_131k_sampled_int64_indexing():
+    """131,072 x 2,560 x 151,936 with 4,096-row blocks (N V >= 2^31: the int64
+    kernels): logp / lse and dH on seeded sampled rows, dW on sampled
+    vocabulary rows through its linearity in the per-row weights."""
+    inp = WL.make_inputs("long_131k")
+    wl = inp.wl
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv, dH, dW = run_fused(h, W, t, w, 4096)
+    m = inp.targets != WL.IGNORE_INDEX
+    assert nv == int(m.sum())
+    g = 1.0 / nv
+    rows = WL.sample_rows(wl.N, 2048, seed=wl.seed)
+    vrows = WL.sample_rows(wl.V, 256, seed=wl.seed + 1)
+    ref_lse, ref_logp, ref_dH, ref_dWpart = O.rows_all(inp.h, inp.W, inp.targets, rows, inp.weights,
+                                                       g=g, vocab_rows=vrows)
+    assert_logp_close(np64(logp)[rows], ref_logp, "logp (sampled rows)")
+    assert_logp_close(np64(lse)[rows], ref_lse, "lse (sampled rows)")
+    assert_grad_close(np64(dH[torch.from_numpy(rows).cuda()]), ref_dH, "dH (sampled rows)")
+    # dW: weights zero outside the sampled rows; grad_scale nv * g / (rows' n_valid) undoes
+    # the call's own 1 / n_valid so that the scale is the same g as the oracle's
+    w0 = np.zeros(wl.N, dtype=np.float32)
+    w0[rows] = 1.0
+    _, _, _, nv0, _, dW0 = run_fused(h, W, t, torch.from_numpy(w0).cuda(), 4096, grad_scale=nv * g)
+    assert nv0 == nv
+    vsel = torch.from_numpy(vrows).cuda()
+    assert_grad_close(np64(dW0[vsel]), ref_dWpart, "dW (sampled rows x sampled vocabulary)")
