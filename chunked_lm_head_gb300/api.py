@@ -124,9 +124,41 @@ class LinearCrossEntropy(torch.autograd.Function):
         return dH, dW, None, None, None, None, None
 
 
+class LinearCrossEntropyOneCall(torch.autograd.Function):
+    """The same loss with its gradients computed in the forward call
+    (flce_forward_backward, no logits recompute); the backward only scales
+    them by the incoming gradient of the loss."""
+
+    @staticmethod
+    def forward(ctx, h, W, targets, weights, chunk_rows, ignore_index, transform=None):
+        out = forward_backward(h, W, targets, weights, chunk_rows, ignore_index,
+                               need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
+                               transform=transform)
+        ctx.grads = (out["dH"], out["dW"])
+        ctx.mark_non_differentiable(out["logp"], out["n_valid"])
+        return out["loss"], out["logp"], out["n_valid"]
+
+    @staticmethod
+    def backward(ctx, grad_loss, grad_logp, grad_n):
+        dH, dW = ctx.grads
+        ctx.grads = None
+        s = float(grad_loss.item())
+        if s != 1.0:  # e.g. a loss scale or a weighted sum of losses
+            dH = None if dH is None else dH * s
+            dW = None if dW is None else dW * s
+        return dH, dW, None, None, None, None, None
+
+
 def linear_cross_entropy(h, W, targets, weights=None, chunk_rows: int = 256,
-                         ignore_index: int = IGNORE_INDEX, transform=None):
-    """Differentiable masked (weighted) mean NLL of softmax(f(h W^T)); returns (loss, logp, n_valid)."""
+                         ignore_index: int = IGNORE_INDEX, transform=None, recompute: bool = True):
+    """Differentiable masked (weighted) mean NLL of softmax(f(h W^T)); returns (loss, logp, n_valid).
+
+    recompute=False computes the gradients in the forward call without the
+    logits recompute (faster when chunk_rows >= 2,048; dH and dW are held
+    from the forward to the backward)."""
+    if not recompute:
+        return LinearCrossEntropyOneCall.apply(h, W, targets, weights, chunk_rows, ignore_index,
+                                               transform)
     return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index, transform)
 
 

@@ -13,15 +13,17 @@ from gpu_util import LOSS_RTOL, assert_grad_close, assert_logp_close, np64, uplo
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("recompute", [True, False])
 @pytest.mark.parametrize("transform", [None, {"softcap": 15.0, "temperature": 0.9}])
-def test_autograd_matches_oracle(transform):
+def test_autograd_matches_oracle(transform, recompute):
     wl = WL.custom("api", 400, 256, 2500, 128, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=401)
     inp = WL.make_inputs(wl)
     inp.weights = np.random.default_rng(8).uniform(0.2, 2.0, wl.N).astype(np.float32)
     h, W, t, w = upload(inp)
     h.requires_grad_(True)
     W.requires_grad_(True)
-    loss, logp, n_valid = flce.linear_cross_entropy(h, W, t, w, chunk_rows=128, transform=transform)
+    loss, logp, n_valid = flce.linear_cross_entropy(h, W, t, w, chunk_rows=128 if recompute else 512,
+                                                    transform=transform, recompute=recompute)
     (3.0 * loss).backward()
     tf = None if transform is None else O.LogitTransform(**transform)
     ref = O.forward(inp.h, inp.W, inp.targets, inp.weights, tf=tf)
