@@ -67,7 +67,6 @@ struct TileCfg {
   static constexpr int SMEM = 1024 + NSTAGE * STAGE + OUT_STAGE_BYTES + SMEM_BAR_BYTES;
   static_assert(SMEM <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 };
-constexpr int GEMM_SMEM_BYTES_MAX = TileCfg<1>::SMEM > TileCfg<2>::SMEM ? TileCfg<1>::SMEM : TileCfg<2>::SMEM;
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 constexpr long long DRAIN_LIMIT_CYCLES = 400000000LL;
 
