@@ -1,0 +1,81 @@
+"""Seeded random small problems (ragged N, H down to 8, V down to 1, chunk
+sizes from 1 row up, masks, weights, transforms, both CTA-group paths, row
+compaction on and off, forced backward row blocks, the one-call path) against
+the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_lm_head_gb300 import _lib
+from chunked_lm_head_gb300 import workloads as WL
+from oracle import flce_oracle as O
+
+from gpu_util import LOSS_RTOL, assert_grad_close, assert_logp_close, np64, run_backward, run_forward, upload
+
+pytestmark = pytest.mark.gpu
+
+TRANSFORMS = [None, {"softcap": 8.0, "temperature": 1.2}, {"scale_multiply": 0.7, "temperature": 0.6}]
+
+
+def _cases(n, seed=900):
+    r = np.random.default_rng(seed)
+    fixed = [dict(N=1, H=8, V=1, chunk=1), dict(N=3, H=8, V=5, chunk=1), dict(N=700, H=8, V=3001, chunk=128),
+             dict(N=257, H=520, V=2, chunk=300), dict(N=129, H=64, V=4099, chunk=129)]
+    out = []
+    for k in range(n):
+        c = fixed[k] if k < len(fixed) else dict(
+            N=int(r.integers(1, 1200)), H=int(8 * r.integers(1, 80)), V=int(r.integers(1, 6000)),
+            chunk=int(r.choice([1, 16, 100, 128, 256, 777, 2048])))
+        c.update(cg=str(r.choice(["1", "2"])), compact=str(r.choice(["0", "1"])),
+                 ignore=float(r.choice([0.0, 0.1, 0.5, 1.0], p=[0.35, 0.35, 0.2, 0.1])),
+                 weights=bool(r.uniform() < 0.5), tf=int(r.integers(0, 3)),
+                 rows=int(r.choice([0, 0, 256, 512])), fused=bool(r.uniform() < 0.3), seed=1000 + k)
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("c", _cases(64), ids=lambda c: f"N{c['N']}H{c['H']}V{c['V']}c{c['chunk']}")
+def test_random_problem_matches_oracle(c, monkeypatch):
+    monkeypatch.setenv("FLCE_CTA_GROUP", c["cg"])
+    monkeypatch.setenv("FLCE_COMPACT", c["compact"])
+    if c["rows"]:
+        monkeypatch.setenv("FLCE_BWD_ROWS", str(c["rows"]))
+    wl = WL.custom("fuzz", c["N"], c["H"], c["V"], c["chunk"], w_std=0.1, ignore_frac=0.0, seed=c["seed"])
+    inp = WL.make_inputs(wl)
+    r = np.random.default_rng(c["seed"])
+    inp.targets[r.uniform(size=c["N"]) < c["ignore"]] = WL.IGNORE_INDEX
+    if c["weights"]:
+        inp.weights = r.uniform(-1.0, 2.0, c["N"]).astype(np.float32)
+    tfd = TRANSFORMS[c["tf"]]
+    tf = None if tfd is None else O.LogitTransform(**tfd)
+    ref = O.forward(inp.h, inp.W, inp.targets, inp.weights, tf=tf)
+    g = 1.0 / ref.n_valid if ref.n_valid else 1.0
+    refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g, tf=tf)
+    h, W, t, w = upload(inp)
+    N, H = h.shape
+    V = W.shape[0]
+    if c["fused"]:
+        logp = torch.empty(N, dtype=torch.float32, device="cuda")
+        lse = torch.empty(N, dtype=torch.float32, device="cuda")
+        loss_t = torch.empty(1, dtype=torch.float32, device="cuda")
+        nv_t = torch.empty(1, dtype=torch.int64, device="cuda")
+        dH = torch.empty_like(h)
+        dW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+        # grad_scale g * n_valid: the call divides by n_valid itself
+        assert _lib.flce_forward_backward(h, W, t, w, N, H, V, c["chunk"], -100, tfd,
+                                          g * max(ref.n_valid, 1), logp, lse, loss_t, nv_t, dH, dW) == 0
+        assert _lib.flce_device_status() == 0
+        loss, nv = float(loss_t.item()), int(nv_t.item())
+    else:
+        logp, lse, loss, nv = run_forward(h, W, t, w, c["chunk"], transform=tfd)
+        dH, dW = run_backward(h, W, t, w, lse, g, c["chunk"], transform=tfd)
+    assert nv == ref.n_valid
+    assert_logp_close(np64(logp), ref.logp, "logp")
+    assert_logp_close(np64(lse), ref.lse, "lse")
+    assert loss == pytest.approx(ref.loss, rel=LOSS_RTOL, abs=1e-6)
+    for name, got, want in (("dH", np64(dH), refb.dH), ("dW", np64(dW), refb.dW)):
+        scale = np.linalg.norm(want)
+        if scale < 1e-6:  # no valid row, V = 1, or all-zero weights: fp32 noise only
+            assert np.max(np.abs(got)) <= 1e-5, name
+        else:
+            assert_grad_close(got, want, name)
