@@ -79,3 +79,59 @@ def test_random_problem_matches_oracle(c, monkeypatch):
             assert np.max(np.abs(got)) <= 1e-5, name
         else:
             assert_grad_close(got, want, name)
+
+
+def _kd_cases(n, seed=950):
+    r = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        out.append(dict(N=int(r.integers(1, 700)), Hs=int(8 * r.integers(1, 48)), Ht=int(8 * r.integers(1, 48)),
+                        V=int(r.integers(2, 4000)), chunk=int(r.choice([1, 64, 128, 300, 1024])),
+                        cg=str(r.choice(["1", "2"])), masked=bool(r.uniform() < 0.6),
+                        jsd=float(r.choice([0.0, 0.5, 0.2, 0.85])), tf=int(r.integers(0, 3)), seed=2000 + k))
+    return out
+
+
+@pytest.mark.parametrize("c", _kd_cases(24), ids=lambda c: f"N{c['N']}Hs{c['Hs']}Ht{c['Ht']}V{c['V']}b{c['jsd']}")
+def test_random_distillation_matches_oracle(c, monkeypatch):
+    import chunked_lm_head_gb300 as flce
+    from gpu_util import to_dev_bf16
+    monkeypatch.setenv("FLCE_CTA_GROUP", c["cg"])
+    s = WL.make_inputs(WL.custom("kfs", c["N"], c["Hs"], c["V"], 256, w_std=0.1, seed=c["seed"]))
+    t_ = WL.make_inputs(WL.custom("kft", c["N"], c["Ht"], c["V"], 256, w_std=0.12, seed=c["seed"] + 500))
+    r = np.random.default_rng(c["seed"])
+    targets = None
+    if c["masked"]:
+        targets = r.integers(0, c["V"], c["N"]).astype(np.int64)
+        targets[r.uniform(size=c["N"]) < 0.2] = WL.IGNORE_INDEX
+    weights = r.uniform(0.2, 1.8, c["N"]).astype(np.float32)
+    tfd = TRANSFORMS[c["tf"]]
+    tf = None if tfd is None else O.LogitTransform(**tfd)
+    hs, Ws, ht, Wt = (to_dev_bf16(x) for x in (s.h, s.W, t_.h, t_.W))
+    tg = None if targets is None else torch.from_numpy(targets).cuda()
+    w = torch.from_numpy(weights).cuda()
+    if c["jsd"]:
+        out = flce.jsd_forward(hs, Ws, ht, Wt, c["jsd"], tg, w, c["chunk"], transform=tfd)
+        ref = O.jsd_forward(s.h, s.W, t_.h, t_.W, c["jsd"], targets, weights, tf=tf)
+        assert_logp_close(np64(out["jsd"]), ref.jsd, "jsd")
+    else:
+        out = flce.kd_forward(hs, Ws, ht, Wt, tg, w, c["chunk"], transform=tfd)
+        ref = O.kd_forward(s.h, s.W, t_.h, t_.W, targets, weights, tf=tf)
+        assert_logp_close(np64(out["kl"]), ref.kl, "kl")
+    assert int(out["n_valid"]) == ref.n_valid
+    assert_logp_close(np64(out["lse_s"]), ref.lse_s, "lse_s")
+    assert float(out["loss"]) == pytest.approx(ref.loss, rel=LOSS_RTOL, abs=1e-6)
+    g = 1.0 / ref.n_valid if ref.n_valid else 1.0
+    if c["jsd"]:
+        dH, dW = flce.jsd_backward(hs, Ws, ht, Wt, out["lse_s"], out["lse_t"], out["kl_sm"], g, c["jsd"], tg, w,
+                                   c["chunk"], transform=tfd)
+        refb = O.jsd_backward(s.h, s.W, t_.h, t_.W, c["jsd"], targets, weights, g=g, tf=tf)
+    else:
+        dH, dW = flce.kd_backward(hs, Ws, ht, Wt, out["lse_s"], out["lse_t"], g, tg, w, c["chunk"], transform=tfd)
+        refb = O.kd_backward(s.h, s.W, t_.h, t_.W, targets, weights, g=g, tf=tf)
+    assert _lib.flce_device_status() == 0
+    for name, got, want in (("dH", np64(dH), refb.dH), ("dW", np64(dW), refb.dW)):
+        if np.linalg.norm(want) < 1e-6:
+            assert np.max(np.abs(got)) <= 1e-5, name
+        else:
+            assert_grad_close(got, want, name)
