@@ -646,7 +646,13 @@ struct BwdPlan {
 
 constexpr double kPlanFlops = 1.6e15;  // sustained bf16 tensor rate of the GPU (model)
 constexpr double kPlanBytes = 6.0e12;  // sustained HBM bandwidth (model)
-constexpr double kPlanLaunch = 5e-6;   // per launch: prologue, drain and the gap to the next
+// per launch: prologue, last-wave imbalance, drain and the gap to the next
+// (about 25 us measured inside a short launch; programmatic launch hides some)
+constexpr double kPlanLaunch = 15e-6;
+// share of the read-modify-write traffic of the fp32 outputs (dW, dH
+// partials) that the MMAs do not hide: measured at the 2,816-row slab shape,
+// the dW output added its full DRAM time
+constexpr double kPlanRmwExposed = 0.7;
 
 // Best dH k-split count for `tiles` output tiles and `kb` K blocks: the
 // fewest splits whose last wave is at least 90% full (splits keep >= 8 K
@@ -702,7 +708,8 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
   b.dh_f32 = b.n_slabs > 1 || s > 1;
   if (b.n_slabs > 1 && aux(s, b.dh_f32) > 2.0 * budget) return false;
 
-  // modelled time: per launch max(tensor time, HBM time) + launch cost
+  // modelled time: per launch max(tensor time, HBM operand time) + the
+  // exposed share of the fp32 output traffic + launch cost
   const double t_kb = 2.0 * tm * BN * BK * workers / kPlanFlops;  // one tile x one 64-deep K block
   auto waves = [&](long long u) { return static_cast<double>(ceil_div(u, workers)); };
   auto slab_cost = [&](long long rows, long long w, bool first_block, bool first_slab) {
@@ -717,12 +724,13 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
     const long long sw = ceil_div(kbw, b.dh_kb_per_split);
     const double dh_out = b.dh_f32 ? 4.0 * rows * H * sw * (first_slab ? 1 : 2) : 2.0 * rows * H;
     t += std::max(waves(mt * ceil_div(H, BN) * sw) * b.dh_kb_per_split * t_kb,
-                  (d_bytes + 2.0 * w * H + dh_out) / kPlanBytes);
+                  (d_bytes + 2.0 * w * H) / kPlanBytes) +
+         kPlanRmwExposed * dh_out / kPlanBytes;
     // dW: a store on the first row block, a read-modify-write afterwards
     const long long vt = ceil_div(w, tm);
     t += std::max(waves(vt * ceil_div(H, BN)) * ceil_div(rows, BK) * t_kb,
-                  (d_bytes + 2.0 * rows * H * ceil_div(vt, 8) + 4.0 * w * H * (first_block ? 1 : 2)) /
-                      kPlanBytes);
+                  (d_bytes + 2.0 * rows * H * ceil_div(vt, 8)) / kPlanBytes) +
+         kPlanRmwExposed * 4.0 * w * H * (first_block ? 1 : 2) / kPlanBytes;
     return t + 3 * kPlanLaunch;
   };
   auto block_cost = [&](long long rows, bool first_block) {
@@ -774,11 +782,17 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
     const long long R = std::min(nr, std::max(R0, round_up(forced, BM)));
     if (plan_candidate(b, N, H, V, R, budget, workers, tm)) best = b;
   } else {
-    // larger row blocks in steps of one tile
+    // larger row blocks in steps of one tile; a plan with vocabulary slabs
+    // must beat the single-slab chunk plan by 5 % (the model misses some of
+    // the slabs' extra traffic: on 16,384 x 4,096 x 151,936 at 4,096-row
+    // chunks, 8,192- and 16,384-row blocks measured no faster), and each
+    // later candidate the best so far by 2 %
+    const bool single = best.n_slabs == 1;
     for (long long R = round_up(R0 + 1, tm); R <= round_up(nr, tm); R += tm) {
       BwdPlan b;
       if (!plan_candidate(b, N, H, V, std::min(R, nr), budget, workers, tm)) break;
-      if (b.est_s < best.est_s * 0.98) best = b;
+      const double margin = (single && best.R == R0) ? 0.95 : 0.98;
+      if (b.est_s < best.est_s * margin) best = b;
       if (R >= nr) break;
     }
   }
