@@ -39,8 +39,9 @@
  *   - N, H, V must each be < 2^31.
  *   - Not thread-safe for concurrent calls from several host threads while
  *     profiling is enabled.
- *   - CUDA graphs: flce_forward(_ex), flce_backward(_ex), the distillation
- *     and e4m3 entry points can be captured into a CUDA graph and replayed
+ *   - CUDA graphs: flce_forward(_ex), flce_backward(_ex),
+ *     flce_forward_backward, the distillation and e4m3 entry points can be
+ *     captured into a CUDA graph and replayed
  *     when they are given a caller workspace, FLCE_VALIDATE is unset,
  *     profiling is off, and one eager call of the same kind has run on the
  *     device first (it sets kernel attributes and caches the device's
