@@ -96,3 +96,80 @@ def test_one_call_forward_backward_graph_replay_matches_eager():
     for k in bufs:
         assert torch.equal(bufs[k], eager[k]), k
     assert _lib.flce_device_status() == 0
+
+
+def _capture_and_compare(step, bufs):
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        assert step() == 0
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in bufs.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        assert step() == 0
+    for v in bufs.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for k in bufs:
+        assert torch.equal(bufs[k], eager[k]), k
+    assert _lib.flce_device_status() == 0
+
+
+def test_distillation_graph_replay_matches_eager():
+    """KL and Jensen-Shannon distillation forward + backward, captured."""
+    s = WL.make_inputs(WL.custom("gkd_s", 600, 192, 2500, 256, w_std=0.05, seed=803))
+    tt = WL.make_inputs(WL.custom("gkd_t", 600, 256, 2500, 256, w_std=0.06, seed=804))
+    hs, Ws, _, _ = upload(s)
+    ht, Wt, _, _ = upload(tt)
+    N, Hs, Ht, V, cr = 600, 192, 256, 2500, 256
+    ws_bytes = _lib.flce_kd_workspace_bytes(N, Hs, Ht, V, cr)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    bufs = dict(out=torch.empty(N, device="cuda"), lse_s=torch.empty(N, device="cuda"),
+                lse_t=torch.empty(N, device="cuda"), klsm=torch.empty(N, device="cuda"),
+                loss=torch.empty(1, device="cuda"), nv=torch.empty(1, dtype=torch.int64, device="cuda"),
+                dH=torch.empty_like(hs), dW=torch.empty((V, Hs), device="cuda"))
+
+    def kl_step():
+        a = _lib.flce_kd_forward(hs, Ws, Hs, ht, Wt, Ht, None, None, N, V, cr, -100, None, bufs["out"],
+                                 bufs["lse_s"], bufs["lse_t"], bufs["loss"], bufs["nv"], ws, ws_bytes)
+        b = _lib.flce_kd_backward(hs, Ws, Hs, ht, Wt, Ht, None, None, bufs["lse_s"], bufs["lse_t"], 1.0 / N,
+                                  bufs["dH"], bufs["dW"], N, V, cr, -100, None, ws, ws_bytes)
+        return a | b
+
+    def jsd_step():
+        a = _lib.flce_jsd_forward(hs, Ws, Hs, ht, Wt, Ht, None, None, N, V, cr, -100, 0.5, None, bufs["out"],
+                                  bufs["lse_s"], bufs["lse_t"], bufs["klsm"], bufs["loss"], bufs["nv"], ws,
+                                  ws_bytes)
+        b = _lib.flce_jsd_backward(hs, Ws, Hs, ht, Wt, Ht, None, None, bufs["lse_s"], bufs["lse_t"],
+                                   bufs["klsm"], 0.5, 1.0 / N, bufs["dH"], bufs["dW"], N, V, cr, -100, None,
+                                   ws, ws_bytes)
+        return a | b
+
+    _capture_and_compare(kl_step, {k: v for k, v in bufs.items() if k != "klsm"})  # KL writes no kl_sm
+    _capture_and_compare(jsd_step, bufs)
+
+
+def test_e4m3_forward_graph_replay_matches_eager():
+    """Per-row e4m3 quantisation of h and the e4m3 forward, captured."""
+    inp = WL.make_inputs(WL.custom("g8", 700, 256, 3000, 256, w_std=0.05, seed=805))
+    h, W, t, _ = upload(inp)
+    N, H, V = 700, 256, 3000
+    W8 = torch.empty((V, H), dtype=torch.uint8, device="cuda")
+    Wsc = torch.empty(V, device="cuda")
+    assert _lib.flce_quantize_e4m3_rows(W, V, H, W8, Wsc) == 0
+    ws_bytes = _lib.flce_workspace_bytes(N, H, V, 256)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    bufs = dict(h8=torch.empty((N, H), dtype=torch.uint8, device="cuda"), hsc=torch.empty(N, device="cuda"),
+                logp=torch.empty(N, device="cuda"), lse=torch.empty(N, device="cuda"),
+                loss=torch.empty(1, device="cuda"), nv=torch.empty(1, dtype=torch.int64, device="cuda"))
+
+    def step():
+        a = _lib.flce_quantize_e4m3_rows(h, N, H, bufs["h8"], bufs["hsc"])
+        b = _lib.flce_forward_e4m3(bufs["h8"], bufs["hsc"], W8, Wsc, t, None, N, H, V, 256, -100, None,
+                                   bufs["logp"], bufs["lse"], bufs["loss"], bufs["nv"], ws, ws_bytes)
+        return a | b
+
+    _capture_and_compare(step, bufs)
