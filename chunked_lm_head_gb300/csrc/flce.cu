@@ -1063,6 +1063,13 @@ bool compact_env() {
   return !(s != nullptr && s[0] == '0');
 }
 
+// DLOGITS writes D through TMA boxes (default) or per-thread stores
+// (FLCE_D_TMA=0).
+bool d_tma_env() {
+  const char* s = std::getenv("FLCE_D_TMA");
+  return !(s != nullptr && s[0] == '0');
+}
+
 bool validate_env() {
   const char* s = std::getenv("FLCE_VALIDATE");
   return s != nullptr && s[0] != '\0' && s[0] != '0';
@@ -1537,6 +1544,8 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   base.lse = lse;
   base.grad_scale = grad_scale;
   base.count_scale = count_scale;
+  CUtensorMap D_st;  // D as a TMA store target: [R][ldD] bf16, 64 x 32 boxes
+  base.d_tma = d_tma_env() && make_map(&D_st, Dbuf, b.ldD, b.R, b.ldD, 64, 32) ? 1 : 0;
   base.ignore_index = ignore_index;
   base.D = Dbuf;
   base.dH = dH;
@@ -1631,7 +1640,8 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
         // per 4096-row block at 16 against 3.5 GB at 8)
         q.group_m = std::min(16, q.m_tiles);
         ProfScope ps(K_DLOGITS, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, A_dl, W_k, W_k, q, std::min(q.num_units, workers), st));
+        FLCE_CUDA_TRY(launch_gemm<MODE_DLOGITS>(cg, kLong, A_dl, W_k, q.d_tma ? D_st : W_k, q,
+                                                std::min(q.num_units, workers), st));
       }
       // (2) dH[rows] (+)= D W[slab], (3) dW[slab] (+)= D^T h[rows]
       const flce_status s2 = slab_dh_dw(dhdw, p, rows, block, slab, v0, width, D_k, D_mn, B_dw, st);

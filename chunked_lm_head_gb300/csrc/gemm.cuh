@@ -165,6 +165,9 @@ struct GemmParams {
   float* mx;
   // DLOGITS: divide grad_scale by max(*count_scale, 1) (a count on the device)
   const long long* count_scale;
+  // DLOGITS: write D through tmC (bf16 [rows_cap][ldD], 64 x 32 boxes) from
+  // shared memory instead of per-thread global stores
+  int d_tma;
 };
 
 // Problem extents that depend on the device-side row count of a compacted pass.
@@ -361,6 +364,17 @@ __device__ __forceinline__ float select32(const float (&v)[32], int j) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One 32-column chunk of this thread's row (32 bf16 = 64 bytes) into half
+// `half` of a 32-row x 64-column bf16 box in 128B-swizzled shared memory
+// (row = lane): 16-byte granule g of the row lands at g ^ (row & 7).
+__device__ __forceinline__ void stage_bf16_half(uint32_t box, int lane, int half, const uint32_t (&pk)[16]) {
+  const uint32_t row_addr = box + lane * 128;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    st_shared_v4_u32(row_addr + (((half * 4 + g) ^ (lane & 7)) << 4), pk[4 * g], pk[4 * g + 1],
+                     pk[4 * g + 2], pk[4 * g + 3]);
 }
 
 template <int MODE, bool kLong, int CG, bool kF8 = false>
@@ -714,7 +728,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 pk[j / 2] = pack_bf16x2(d0, d1);
               }
             }
-            if (row_store) {
+            if (p.d_tma) {
+              // two chunks fill one 32 x 64 box; TMA writes it (rows of the
+              // box past the live rows hold zeros: their scale is 0)
+              const int half = c & 1;
+              const uint32_t box = out_stage + (warp - 2) * (2 * OUT_BOX_BYTES) + ((c >> 1) & 1) * OUT_BOX_BYTES;
+              if (half == 0) {
+                if (lane == 0) bulk_wait_read<1>();  // the copy that last used this box has read it
+                __syncwarp();
+              }
+              stage_bf16_half(box, lane, half, pk);
+              if (half == 1) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  const int lrow0 = t.m * C::TM + rank * BM + q * 32;
+                  const int x = col0 - 32;  // first column of the box
+                  if (x < p.ldD && lrow0 < p.rows_cap) tma_store_2d(&tmC, box, x, lrow0);
+                  bulk_commit();
+                }
+              }
+            } else if (row_store) {
               uint16_t* dst = p.D + static_cast<idx_t>(lr) * p.ldD + col0;
 #pragma unroll
               for (int g = 0; g < 4; ++g)
@@ -963,7 +997,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
-  if constexpr (MODE == MODE_DW || MODE == MODE_DH) {
+  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DLOGITS) {
     if (warp >= 2 && lane == 0) bulk_wait_all();  // output boxes written before the CTA retires
   }
   __syncthreads();
