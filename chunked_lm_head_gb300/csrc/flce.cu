@@ -1148,6 +1148,17 @@ flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, c
 
 // ---- stages shared by the entry points
 
+// Row tiles per dH raster group: 8 (FLCE_DH_GROUP overrides).  With 16 (all
+// row tiles of a 4,096-row block) a wave of 76 units reads 16 D slices and
+// ~5 W slices; with 8, 8 and ~9.5.  On 16,384 x 4,096 x 151,936 the dH launch
+// time is unchanged, but the step ran 1.3 % faster: less DRAM traffic under
+// the power cap leaves a higher clock for every kernel.
+int dh_group_rows(int m_tiles) {
+  int g = 8;
+  if (const char* e = std::getenv("FLCE_DH_GROUP")) g = std::atoi(e);
+  return g > 0 ? std::min(g, m_tiles) : m_tiles;
+}
+
 // dH and dW stages of the backward, shared by the cross-entropy and the
 // distillation backwards.  For one row block and one vocabulary slab, the
 // slab's bf16 dlogits sit in D (maps D_k / D_mn, local columns); B_dw maps the
@@ -1183,7 +1194,7 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
     q.k_splits = splits;
     q.num_units = splits * q.m_tiles * q.n_tiles;
-    q.group_m = q.m_tiles;
+    q.group_m = dh_group_rows(q.m_tiles);
     q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
     q.dh_accumulate = slab > 0 ? 1 : 0;
     ProfScope ps(K_DH, st);
