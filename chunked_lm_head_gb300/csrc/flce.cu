@@ -77,19 +77,22 @@ __device__ __forceinline__ void block_sum_store(double contrib, long long cnt, d
 // Split-vocabulary combine: lse = M + log sum_s s_s 2^(m_s - M) (log2 domain,
 // converted to natural log), logp = z_t - lse on non-ignored rows, and this
 // block's share of sum(w * logp) and of the valid-row count.
-// Rows [0, N) of the arrays passed (callers offset them for a row range);
-// `stride` is the distance between two splits' partials of one row.
+// Rows [0, N) of the arrays passed (callers offset them for a row range),
+// or with `ri` the rows ri[0..N) of the whole arrays; `stride` is the
+// distance between two splits' partials of one row.
 template <bool kLong>
 __global__ void combine_kernel(const float2* __restrict__ part, int S, int stride, int N,
                                const float* __restrict__ zt, const int64_t* __restrict__ targets,
                                const float* __restrict__ weights, long long ignore,
                                float* __restrict__ out_logp, float* __restrict__ out_lse,
-                               double* __restrict__ blk_sum, long long* __restrict__ blk_cnt) {
+                               double* __restrict__ blk_sum, long long* __restrict__ blk_cnt,
+                               const int* __restrict__ ri) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
-  const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
+  const int j = blockIdx.x * SMALL_THREADS + threadIdx.x;
   double contrib = 0.0;
   long long cnt = 0;
-  if (i < N) {
+  if (j < N) {
+    const int i = ri ? ri[j] : j;  // the j-th row of this range
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, part[static_cast<idx_t>(s) * stride + i].x);
     float sum = 0.f;
@@ -199,16 +202,22 @@ __global__ void compact_count_kernel(const int64_t* __restrict__ targets, int N,
   }
 }
 
+// tail != 0: idx is a permutation of all N rows, the ignored rows (in row
+// order) after the non-ignored ones.
 __global__ void compact_write_kernel(const int64_t* __restrict__ targets, int N, long long ignore,
                                      const int* __restrict__ blk_cnt, int nblk, int* __restrict__ idx,
-                                     int* __restrict__ total) {
-  __shared__ int s_off;
+                                     int* __restrict__ total, int tail) {
+  __shared__ int s_off, s_total;
   __shared__ int wtot[SMALL_THREADS / 32];
   if (threadIdx.x == 0) {
-    int o = 0;
-    for (int b = 0; b < static_cast<int>(blockIdx.x); ++b) o += blk_cnt[b];
+    int o = 0, all = 0;
+    for (int b = 0; b < nblk; ++b) {
+      if (b < static_cast<int>(blockIdx.x)) o += blk_cnt[b];
+      all += blk_cnt[b];
+    }
     s_off = o;
-    if (static_cast<int>(blockIdx.x) == nblk - 1) *total = o + blk_cnt[blockIdx.x];
+    s_total = all;
+    if (static_cast<int>(blockIdx.x) == nblk - 1) *total = all;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int base = blockIdx.x * COMPACT_ROWS_PER_BLOCK + threadIdx.x * COMPACT_ROWS_PER_THREAD;
@@ -230,16 +239,21 @@ __global__ void compact_write_kernel(const int64_t* __restrict__ targets, int N,
   int pos = s_off + x - c;
   for (int w = 0; w < warp; ++w) pos += wtot[w];
 #pragma unroll
-  for (int k = 0; k < COMPACT_ROWS_PER_THREAD; ++k)
-    if (keep[k]) idx[pos++] = base + k;
+  for (int k = 0; k < COMPACT_ROWS_PER_THREAD; ++k) {
+    if (keep[k])
+      idx[pos++] = base + k;
+    else if (tail && base + k < N)  // pos = non-ignored rows before this one
+      idx[s_total + base + k - pos] = base + k;
+  }
 }
 
-// hc[r, :] = h[idx[first + r], :] for the pass's rows; zero rows up to the
-// next 64-row boundary (the dW pass reads whole 64-row K blocks).
+// hc[r, :] = h[idx[first + r], :] for the pass's rows (min(*count - first,
+// cap), or min(N - first, cap) without a count); zero rows up to the next
+// 64-row boundary (the dW pass reads whole 64-row K blocks).
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ h, int H, const int* __restrict__ idx,
-                                   const int* __restrict__ count, int first, int cap,
+                                   const int* __restrict__ count, int N, int first, int cap,
                                    uint16_t* __restrict__ hc) {
-  const int rows = max(0, min(*count - first, cap));
+  const int rows = max(0, min((count ? *count : N) - first, cap));
   const int pad = min((rows + 63) / 64 * 64, cap);
   const int h8 = H / 8;
   const long long total = static_cast<long long>(pad) * h8;
@@ -250,6 +264,21 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ h, int H, const 
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) v = *reinterpret_cast<const uint4*>(h + static_cast<long long>(idx[first + r]) * H + c);
     *reinterpret_cast<uint4*>(hc + static_cast<long long>(r) * H + c) = v;
+  }
+}
+
+// dH rows of the ignored rows, idx[*count .. N) of a permutation that puts
+// the non-ignored rows first, set to zero.
+__global__ void zero_tail_rows_kernel(uint16_t* __restrict__ dH, int H, const int* __restrict__ idx,
+                                      const int* __restrict__ count, int N) {
+  const int first = *count;
+  const int h8 = H / 8;
+  const long long total = static_cast<long long>(N - first) * h8;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = first + static_cast<int>(e / h8);
+    const int c = static_cast<int>(e % h8) * 8;
+    *reinterpret_cast<uint4*>(dH + static_cast<long long>(idx[j]) * H + c) = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -381,11 +410,15 @@ __global__ void grpo_token_kernel(const float* __restrict__ logp, const float* _
 // target column is formed from the exact fp32 target logit instead (so that
 // p_t - 1 keeps its precision when p_t is near 1).  Grid: (column blocks of
 // 256 threads x 32 columns, rows); a thread's 32 columns are one chunk.
+// Local row r is row row0 + r, or with `ri` row ri[r] of a block whose
+// non-ignored rows come first: rows from the next 64-row boundary past them
+// are read by neither the dH nor the dW GEMM and are skipped.
 constexpr int FUSED_COLS_PER_THREAD = 32;
 
 template <bool kLong>
 __global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __restrict__ mx, int ldD,
-                                     int V, int row0, const int64_t* __restrict__ targets,
+                                     int V, int row0, const int* __restrict__ ri,
+                                     const int64_t* __restrict__ targets,
                                      const float* __restrict__ weights, const float* __restrict__ lse,
                                      const float* __restrict__ zt, long long ignore,
                                      const int* __restrict__ n_valid, float grad_scale, int tf_softcap,
@@ -394,7 +427,8 @@ __global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __re
   const int r = blockIdx.y;
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * FUSED_COLS_PER_THREAD;
   if (c >= ldD) return;
-  const int row = row0 + r;
+  if (ri != nullptr && r >= (*n_valid - row0 + 63) / 64 * 64) return;  // row0: the block's first position
+  const int row = ri ? ri[r] : row0 + r;
   const long long t = targets[row];
   const bool valid = t != ignore;
   const float g = grad_scale / fmaxf(1.f, static_cast<float>(*n_valid));
@@ -1281,7 +1315,7 @@ FusedPlan plan_fused(long long N, long long H, long long V, long long chunk_rows
 
 struct FusedLayout {
   size_t zt = 0, part = 0, bsum = 0, bcnt = 0, bad = 0, E = 0, mx = 0, lse = 0, dh_part = 0, idx = 0,
-         blk = 0, count = 0, total = 0;
+         blk = 0, count = 0, hc = 0, total = 0;
 };
 FusedLayout fused_layout(long long N, long long H, const FusedPlan& fp) {
   FusedLayout L;
@@ -1305,6 +1339,7 @@ FusedLayout fused_layout(long long N, long long H, const FusedPlan& fp) {
   L.idx = take(static_cast<size_t>(N) * 4);
   L.blk = take(static_cast<size_t>(ceil_div(std::max(1LL, N), COMPACT_ROWS_PER_BLOCK)) * 4);
   L.count = take(256);
+  L.hc = take(static_cast<size_t>(fp.R) * H * 2);  // the block's rows of h (row compaction)
   L.total = o;
   return L;
 }
@@ -1319,10 +1354,10 @@ flce_status ce_forward_tail(bool kLong, const FwdPlan& f, int N, const float2* p
     ProfScope ps(K_COMBINE, st);
     if (kLong)
       combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
-                                                             out_logp, out_lse, bsum, bcnt);
+                                                             out_logp, out_lse, bsum, bcnt, nullptr);
     else
       combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
-                                                              out_logp, out_lse, bsum, bcnt);
+                                                              out_logp, out_lse, bsum, bcnt, nullptr);
     FLCE_CUDA_TRY(cudaGetLastError());
   }
   return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
@@ -1590,7 +1625,7 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
     {
       ProfScope ps(K_COMPACT, st);
       compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
-                                                           cblk, nblk, cidx, ccount);
+                                                           cblk, nblk, cidx, ccount, 0);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
     if (dH) FLCE_CUDA_TRY(cudaMemsetAsync(dH, 0, static_cast<size_t>(N) * H * 2, st));
@@ -1620,7 +1655,8 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
       const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
       ProfScope ps(K_GATHER, st);
       gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, ccount,
-                                                          static_cast<int>(row0), static_cast<int>(b.R), hc);
+                                                          static_cast<int>(N), static_cast<int>(row0),
+                                                          static_cast<int>(b.R), hc);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
     const CUtensorMap& A_dl = compact ? hc_k : h_k;
@@ -1769,8 +1805,14 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
   int* cidx = reinterpret_cast<int*>(wb + L.idx);
   int* cblk = reinterpret_cast<int*>(wb + L.blk);
   int* ccount = reinterpret_cast<int*>(wb + L.count);
+  uint16_t* hc = reinterpret_cast<uint16_t*>(wb + L.hc);
   const int Ni = static_cast<int>(N);
   const bool validate = validate_env();
+  // Row compaction: the blocks run over a permutation of the rows with the
+  // non-ignored ones first.  Every block's forward covers all its rows (lse
+  // is defined for ignored rows too); its dH / dW GEMMs read the device-side
+  // count and cover only the non-ignored rows.
+  const bool compact = compact_env();
 
   if (validate) FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
   {
@@ -1790,7 +1832,15 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
     ProfScope ps(K_COMPACT, st);
     compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk);
     FLCE_CUDA_TRY(cudaGetLastError());
-    compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk, nblk, cidx, ccount);
+    compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk, nblk, cidx, ccount,
+                                                         compact ? 1 : 0);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  if (compact && dH) {  // the dH GEMM writes the non-ignored rows only
+    ProfScope ps(K_COMPACT, st);
+    const int grid = static_cast<int>(
+        std::max<long long>(1, std::min<long long>(ceil_div(N * (H / 8), SMALL_THREADS), 4LL * device_sms())));
+    zero_tail_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(dH, static_cast<int>(H), cidx, ccount, Ni);
     FLCE_CUDA_TRY(cudaGetLastError());
   }
   int* err = nullptr;
@@ -1803,6 +1853,9 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
     return FLCE_ERR_CUDA;
   if (dH && fp.b.dh_f32 &&
       !make_map_t(&dhp_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dh_part, H, fp.b.dh_splits * fp.R, H, 32, 32))
+    return FLCE_ERR_CUDA;
+  CUtensorMap hc_k, hc_mn;
+  if (compact && (!make_map(&hc_k, hc, H, fp.R, H, BK, BM) || !make_map(&hc_mn, hc, H, fp.R, H, 64, BK)))
     return FLCE_ERR_CUDA;
   const bool kLong = static_cast<long long>(N) * V >= INT_MAX || fp.R * fp.ldD >= INT_MAX ||
                      static_cast<long long>(N) * H >= INT_MAX || static_cast<long long>(V) * H >= INT_MAX ||
@@ -1839,8 +1892,18 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
   for (long long row0 = 0; row0 < N; row0 += fp.R, ++block) {
     const int rows = static_cast<int>(std::min(fp.R, N - row0));
     GemmParams p = base;
-    p.row0 = static_cast<int>(row0);
+    p.row0 = compact ? 0 : static_cast<int>(row0);
     p.rows = rows;
+    if (compact) {  // the block's rows of h, in permutation order
+      p.row_idx = cidx;
+      p.chunk_first = static_cast<int>(row0);
+      const long long total = fp.R * (H / 8);
+      const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
+      ProfScope ps(K_GATHER, st);
+      gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, nullptr, Ni,
+                                                          static_cast<int>(row0), static_cast<int>(fp.R), hc);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
     {  // (1) logits of the block: online lse partials, target logits, exponentials
       GemmParams q = p;
       q.m_tiles = static_cast<int>(ceil_div(rows, tm));
@@ -1856,45 +1919,53 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
       q.zt = zt;
       q.mx = mx;
       ProfScope ps(K_FWD, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_FUSED_FWD>(cg, kLong, h_k, W_k, W_k, q, std::min(q.num_units, workers), st));
+      FLCE_CUDA_TRY(launch_gemm<MODE_FUSED_FWD>(cg, kLong, compact ? hc_k : h_k, W_k, W_k, q,
+                                                std::min(q.num_units, workers), st));
     }
     {  // (2) the block's lse, logp and loss partials
       ProfScope ps(K_COMBINE, st);
       const int nb = static_cast<int>(ceil_div(rows, SMALL_THREADS));
       const long long b0 = block * ceil_div(fp.R, SMALL_THREADS);  // this block's segment
+      // the block's rows: row0 + j, or cidx[row0 + j] (arrays not offset)
+      const long long off = compact ? 0 : row0;
+      const int* ri = compact ? cidx + row0 : nullptr;
       if (kLong)
-        combine_kernel<true><<<nb, SMALL_THREADS, 0, st>>>(part + row0, fp.f.S, Ni, rows, zt + row0, targets + row0,
-                                                           weights ? weights + row0 : nullptr, ignore_index,
-                                                           out_logp ? out_logp + row0 : nullptr, lse + row0,
-                                                           bsum + b0, bcnt + b0);
+        combine_kernel<true><<<nb, SMALL_THREADS, 0, st>>>(part + off, fp.f.S, Ni, rows, zt + off, targets + off,
+                                                           weights ? weights + off : nullptr, ignore_index,
+                                                           out_logp ? out_logp + off : nullptr, lse + off,
+                                                           bsum + b0, bcnt + b0, ri);
       else
-        combine_kernel<false><<<nb, SMALL_THREADS, 0, st>>>(part + row0, fp.f.S, Ni, rows, zt + row0, targets + row0,
-                                                            weights ? weights + row0 : nullptr, ignore_index,
-                                                            out_logp ? out_logp + row0 : nullptr, lse + row0,
-                                                            bsum + b0, bcnt + b0);
+        combine_kernel<false><<<nb, SMALL_THREADS, 0, st>>>(part + off, fp.f.S, Ni, rows, zt + off, targets + off,
+                                                            weights ? weights + off : nullptr, ignore_index,
+                                                            out_logp ? out_logp + off : nullptr, lse + off,
+                                                            bsum + b0, bcnt + b0, ri);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
     {  // (3) exponentials -> dlogits, in place
       ProfScope ps(K_DLOGITS, st);
       const dim3 grid(static_cast<unsigned>(ceil_div(fp.ldD, SMALL_THREADS * FUSED_COLS_PER_THREAD)),
                       static_cast<unsigned>(rows));
+      const int* ri = compact ? cidx + row0 : nullptr;
       if (kLong)
         fused_dlogits_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(
-            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), targets, weights, lse,
-            zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
+            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), ri, targets, weights,
+            lse, zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
       else
         fused_dlogits_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(
-            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), targets, weights, lse,
-            zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
+            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), ri, targets, weights,
+            lse, zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
-    // (4) dH[rows] = D W, dW (+)= D^T h[rows]
+    // (4) dH[rows] = D W, dW (+)= D^T h[rows]; compacted: the block's
+    // non-ignored rows, min(n_valid - row0, rows) read on the device
+    if (compact) p.dyn_count = ccount;
     CUtensorMap D_k, D_mn;
     if (!make_map(&D_k, E, fp.ldD, rows, fp.ldD, BK, BM) || !make_map(&D_mn, E, fp.ldD, rows, fp.ldD, 64, BK))
       return FLCE_ERR_CUDA;
-    s = slab_dh_dw(dhdw, p, rows, block, 0, 0, static_cast<int>(V), D_k, D_mn, h_mn, st);
+    s = slab_dh_dw(dhdw, p, rows, block, 0, 0, static_cast<int>(V), D_k, D_mn, compact ? hc_mn : h_mn, st);
     if (s != FLCE_OK) return s;
-    s = block_dh_finish(dhdw, p.row0, rows, nullptr, nullptr, 0, st);
+    s = block_dh_finish(dhdw, p.row0, rows, compact ? cidx : nullptr, compact ? ccount : nullptr,
+                        static_cast<int>(row0), st);
     if (s != FLCE_OK) return s;
   }
   if (out_loss || out_n_valid) {

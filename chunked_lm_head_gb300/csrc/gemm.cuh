@@ -137,6 +137,8 @@ struct GemmParams {
   // compacted row to its original row; this pass holds compacted rows
   // [chunk_first, chunk_first + rows) with rows = min(*dyn_count - chunk_first,
   // rows_cap) read on the device.  row_idx == nullptr: rows are row0 + i.
+  // The fused forward reads row_idx too (without dyn_count: the pass's rows
+  // are a block of a permutation that puts the non-ignored rows first).
   const int* row_idx;
   const int* dyn_count;
   int chunk_first;
@@ -565,9 +567,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       } else {
         row_ok = lr < dsh.rows;
       }
-      // original row of this accumulator row (targets, weights, lse, dH)
+      // original row of this accumulator row (targets, weights, lse, dH;
+      // the fused forward's partials and target logit)
       int grow = p.row0 + lr;
-      if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH) {
+      if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD) {
         if (p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
       }
       // DLOGITS also writes zero rows up to the next 64-row K block so that
@@ -668,8 +671,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             if constexpr (MODE == MODE_FUSED_FWD) {
               // 2^(u log2e - chunk max) in [0, 1] as bf16, and the chunk max,
-              // for the dlogits pass once the row's lse is known
-              if (row_ok) {
+              // for the dlogits pass once the row's lse is known (an ignored
+              // row's dlogits are zero: the pass does not read them)
+              if (row_ok && tgt != p.ignore_index) {
                 const float cmL = cm * l2a;
                 uint32_t pk[16];
 #pragma unroll

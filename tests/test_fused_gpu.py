@@ -109,6 +109,52 @@ def test_fused_all_rows_ignored_and_fallback_path():
     _check(WL.make_inputs(wl), 256, grad_scale=0.5)
 
 
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_fused_row_compaction_matches_the_full_rows(cg, monkeypatch):
+    """GRPO-style prompts (an ignored prefix of 690 rows in each of 4
+    sequences of 1,500) over 2,048-row blocks.  Compacted, the blocks run over
+    the non-ignored rows first: the second block mixes 1,192 of them with
+    ignored rows, the ragged third holds ignored rows only.  Both the compacted
+    and the full-row call match the oracle and each other."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    wl = WL.custom("fused_cmp", 6000, 256, 9000, 2048, w_std=0.05, targets="zipf", grpo_seqs=4,
+                   prompt_len=690, seed=506)
+    inp = WL.make_inputs(wl)
+    assert int((inp.targets != WL.IGNORE_INDEX).sum()) == 3240
+    dH, dW = _check(inp, 2048, grad_scale=1.5)
+    ign = torch.from_numpy(inp.targets == WL.IGNORE_INDEX).cuda()
+    assert float(dH[ign].float().abs().max()) == 0.0
+    monkeypatch.setenv("FLCE_COMPACT", "0")
+    h, W, t, w = upload(inp)
+    logp0, lse0, loss0, nv0, dH0, dW0 = run_fused(h, W, t, w, 2048, grad_scale=1.5)
+    monkeypatch.delenv("FLCE_COMPACT")
+    logp1, lse1, loss1, nv1, _, _ = run_fused(h, W, t, w, 2048, grad_scale=1.5)
+    assert nv0 == nv1 == 3240
+    assert torch.allclose(lse1, lse0, atol=2e-5, rtol=0) and torch.allclose(logp1, logp0, atol=2e-5, rtol=0)
+    assert loss1 == pytest.approx(loss0, rel=1e-6)
+    assert rel_fro(np64(dH), np64(dH0)) <= 1e-3
+    assert rel_fro(np64(dW), np64(dW0)) <= 1e-3
+
+
+@pytest.mark.slow
+def test_fused_grpo_32k_row_compaction(monkeypatch):
+    """32,768 x 4,096 x 128,000 at 4,096-row blocks, 12.5 % of the rows in
+    ignored prompts: the compacted call (the eighth block all ignored rows)
+    against the full-row call."""
+    inp = WL.make_inputs("grpo_32k")
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv, dH, dW = run_fused(h, W, t, w, 4096)
+    ign = torch.from_numpy(inp.targets == WL.IGNORE_INDEX).cuda()
+    assert nv == 28672 and float(dH[ign].float().abs().max()) == 0.0
+    monkeypatch.setenv("FLCE_COMPACT", "0")
+    logp0, lse0, loss0, nv0, dH0, dW0 = run_fused(h, W, t, w, 4096)
+    assert nv0 == nv
+    assert torch.allclose(lse, lse0, atol=2e-5, rtol=0) and torch.allclose(logp, logp0, atol=2e-5, rtol=0)
+    assert loss == pytest.approx(loss0, rel=1e-6)
+    assert rel_fro(np64(dH), np64(dH0)) <= 1e-3
+    assert rel_fro(np64(dW), np64(dW0)) <= 1e-3
+
+
 @pytest.mark.slow
 def test_fused_sft_16k_matches_the_recomputing_path():
     """16,384 x 4,096 x 151,936 at 4,096-row blocks: the same loss and lse as
