@@ -690,8 +690,12 @@ constexpr double kPlanRmwExposed = 0.7;
 
 // Best dH k-split count for `tiles` output tiles and `kb` K blocks: the
 // fewest splits whose last wave is at least 90% full (splits keep >= 8 K
-// blocks each).
+// blocks each).  FLCE_DH_SPLITS overrides it in plans made after it is set.
 int dh_split_count(long long tiles, long long kb, int workers) {
+  if (const char* e = std::getenv("FLCE_DH_SPLITS")) {
+    const long long s = std::atoll(e);
+    if (s >= 1) return static_cast<int>(std::min<long long>({s, 16, std::max(1LL, kb / 8)}));
+  }
   int best_s = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= 16; ++s) {
@@ -1182,11 +1186,12 @@ flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, c
 
 // ---- stages shared by the entry points
 
-// Row tiles per dH raster group: 8 (FLCE_DH_GROUP overrides).  With 16 (all
-// row tiles of a 4,096-row block) a wave of 76 units reads 16 D slices and
-// ~5 W slices; with 8, 8 and ~9.5.  On 16,384 x 4,096 x 151,936 the dH launch
-// time is unchanged, but the step ran 1.3 % faster: less DRAM traffic under
-// the power cap leaves a higher clock for every kernel.
+// Row tiles per dH raster group: 8 (FLCE_DH_GROUP overrides).  A wave of 76
+// units then covers 8 row tiles x ~9.5 column tiles, the fewest D and W
+// slices per wave.  On 16,384 x 4,096 x 151,936, interleaved runs timed the
+// step 1.3% faster than with all 16 row tiles (the dH launch itself took the
+// same time); a dH launch's DRAM bytes vary more between GPUs than between
+// the two groups.
 int dh_group_rows(int m_tiles) {
   int g = 8;
   if (const char* e = std::getenv("FLCE_DH_GROUP")) g = std::atoi(e);
