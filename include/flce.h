@@ -193,6 +193,11 @@ FLCE_API flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const
  *   R x ldD / 32 fp32 maxima (1/16 of that).  When C is below 2,048 rows
  *   (and below N), the call runs flce_forward_ex and the tiled backward
  *   instead, with grad_scale / n_valid applied on the device.
+ *   Ignored rows: the blocks run over a permutation that puts the
+ *   non-ignored rows first (written on the device; FLCE_COMPACT=0 keeps
+ *   the row order).  Every row gets its lse; the dH / dW GEMMs cover the
+ *   non-ignored rows only, and the ignored rows' dH is zero.  The block's
+ *   rows of h are gathered into the workspace (R x H bf16 more).
  *   Workspace: flce_forward_backward_workspace_bytes, or NULL.
  */
 FLCE_API flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W,
