@@ -302,9 +302,10 @@ def gpu_arm(args):
                 -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
             return
         if args.fused:
+            # a training step needs no lse: without it the forward skips ignored rows
             check("flce_forward_backward", lib.flce_forward_backward(
                 h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr, 1.0,
-                logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
+                logp.data_ptr(), None, loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
                 dW.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
             return
         check("flce_forward_ex", lib.flce_forward_ex(
@@ -417,7 +418,7 @@ def gpu_arm(args):
             wp = None if w is None else w.data_ptr()
             check("flce_forward_backward", lib.flce_forward_backward(
                 h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, None, 1.0,
-                logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
+                logp.data_ptr(), None, loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
                 dW.data_ptr(), fwork.data_ptr(), fws, sh))
 
         with torch.cuda.stream(stream):
@@ -434,9 +435,10 @@ def gpu_arm(args):
         f_ms = reduce_max(f0.elapsed_time(f1), device=dev) / args.steps
         fused_line = {"call": "flce_forward_backward", "value": whole_job_rate(N, ws, f_ms), "unit": UNIT,
                       "ms_per_step": f_ms,
-                      "tflops_executed": 6.0 * N * V * H / (f_ms / 1e3) / 1e12,
+                      "tflops_executed": 6.0 * n_valid_host * V * H / (f_ms / 1e3) / 1e12,
                       "note": "same loss, logp and gradients without the backward's logits recompute "
-                              "(6 N V H tensor FLOPs instead of 8 N V H)"}
+                              "(6 N V H tensor FLOPs instead of 8 N V H; no lse requested, so "
+                              "ignored rows are skipped in every GEMM)"}
         del fwork
         st = _lib.flce_device_status(sh)
         if st != 0:
@@ -454,8 +456,9 @@ def gpu_arm(args):
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     if args.forward_only:
         flops_step = {"fwd_logits_lse": 2.0 * N * V * H}
-    if args.fused:  # no recompute: the forward GEMM, dH and dW (bwd_dlogits is elementwise)
-        flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dH": 2.0 * nv * V * H,
+    if args.fused:  # no recompute, no lse: the forward GEMM, dH and dW over the non-ignored
+        # rows (bwd_dlogits is elementwise)
+        flops_step = {"fwd_logits_lse": 2.0 * nv * V * H, "bwd_dH": 2.0 * nv * V * H,
                       "bwd_dW": 2.0 * nv * V * H}
     if Ht and args.jsd_beta:  # both heads twice in the forward (lse, then mixture terms)
         flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "jsd_fwd_terms": 2.0 * N * V * (H + Ht),

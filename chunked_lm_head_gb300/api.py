@@ -72,15 +72,17 @@ def backward(h, W, targets, weights, lse, grad_scale: float, chunk_rows: int = 2
 def forward_backward(h, W, targets, weights=None, chunk_rows: int = 4096,
                      ignore_index: int = IGNORE_INDEX, grad_scale: float = 1.0, need_dH: bool = True,
                      need_dW: bool = True, workspace: torch.Tensor | None = None, stream=None,
-                     transform=None):
+                     transform=None, need_lse: bool = True):
     """Loss and its gradients in one call without the logits recompute
-    (flce_forward_backward): dict(logp, lse, loss, n_valid, dH, dW)."""
+    (flce_forward_backward): dict(logp, lse, loss, n_valid, dH, dW).
+    need_lse=False returns lse None and lets the call skip the ignored rows'
+    forward."""
     _check(h, W, targets, weights)
     N, H = h.shape
     V = W.shape[0]
     dev = h.device
     logp = torch.empty(N, dtype=torch.float32, device=dev)
-    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if need_lse else None
     loss = torch.empty((), dtype=torch.float32, device=dev)
     n_valid = torch.empty((), dtype=torch.int64, device=dev)
     dH = torch.empty_like(h) if need_dH else None
@@ -133,7 +135,7 @@ class LinearCrossEntropyOneCall(torch.autograd.Function):
     def forward(ctx, h, W, targets, weights, chunk_rows, ignore_index, transform=None):
         out = forward_backward(h, W, targets, weights, chunk_rows, ignore_index,
                                need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
-                               transform=transform)
+                               transform=transform, need_lse=False)
         ctx.grads = (out["dH"], out["dW"])
         ctx.mark_non_differentiable(out["logp"], out["n_valid"])
         return out["loss"], out["logp"], out["n_valid"]

@@ -1814,10 +1814,12 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
   const int Ni = static_cast<int>(N);
   const bool validate = validate_env();
   // Row compaction: the blocks run over a permutation of the rows with the
-  // non-ignored ones first.  Every block's forward covers all its rows (lse
-  // is defined for ignored rows too); its dH / dW GEMMs read the device-side
-  // count and cover only the non-ignored rows.
+  // non-ignored ones first.  A block's forward covers all its rows when the
+  // caller asks for lse (defined for ignored rows too), else only the
+  // non-ignored ones; its dH / dW GEMMs read the device-side count and cover
+  // only the non-ignored rows.
   const bool compact = compact_env();
+  const bool fwd_valid_only = compact && out_lse == nullptr;
 
   if (validate) FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
   {
@@ -1905,7 +1907,8 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
       const long long total = fp.R * (H / 8);
       const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
       ProfScope ps(K_GATHER, st);
-      gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, nullptr, Ni,
+      gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx,
+                                                          fwd_valid_only ? ccount : nullptr, Ni,
                                                           static_cast<int>(row0), static_cast<int>(fp.R), hc);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
@@ -1923,6 +1926,9 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
       q.partials = part;
       q.zt = zt;
       q.mx = mx;
+      // without out_lse, the ignored rows' lse is never observed: skip them
+      // (their partials stay unwritten; the combine gives them logp 0)
+      if (fwd_valid_only) q.dyn_count = ccount;
       ProfScope ps(K_FWD, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_FUSED_FWD>(cg, kLong, compact ? hc_k : h_k, W_k, W_k, q,
                                                 std::min(q.num_units, workers), st));

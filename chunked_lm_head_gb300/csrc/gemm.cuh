@@ -137,8 +137,9 @@ struct GemmParams {
   // compacted row to its original row; this pass holds compacted rows
   // [chunk_first, chunk_first + rows) with rows = min(*dyn_count - chunk_first,
   // rows_cap) read on the device.  row_idx == nullptr: rows are row0 + i.
-  // The fused forward reads row_idx too (without dyn_count: the pass's rows
-  // are a block of a permutation that puts the non-ignored rows first).
+  // The fused forward reads row_idx too: the pass's rows are a block of a
+  // permutation that puts the non-ignored rows first (with dyn_count, only
+  // those are computed).
   const int* row_idx;
   const int* dyn_count;
   int chunk_first;
@@ -182,7 +183,7 @@ __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
   DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units};
   if (p.dyn_count != nullptr) {
     d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
-    if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH) {
+    if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD) {
       d.m_tiles = (d.rows + TM - 1) / TM;
       d.num_units = p.k_splits * d.m_tiles * p.cols;
     } else if constexpr (MODE == MODE_DW) {

@@ -195,9 +195,11 @@ FLCE_API flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const
  *   instead, with grad_scale / n_valid applied on the device.
  *   Ignored rows: the blocks run over a permutation that puts the
  *   non-ignored rows first (written on the device; FLCE_COMPACT=0 keeps
- *   the row order).  Every row gets its lse; the dH / dW GEMMs cover the
- *   non-ignored rows only, and the ignored rows' dH is zero.  The block's
- *   rows of h are gathered into the workspace (R x H bf16 more).
+ *   the row order).  Every row gets its lse when out_lse is given; with
+ *   out_lse NULL the forward GEMM covers the non-ignored rows only.  The
+ *   dH / dW GEMMs cover the non-ignored rows only, and the ignored rows' dH
+ *   is zero.  The block's rows of h are gathered into the workspace (R x H
+ *   bf16 more).
  *   Workspace: flce_forward_backward_workspace_bytes, or NULL.
  */
 FLCE_API flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W,

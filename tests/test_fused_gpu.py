@@ -136,6 +136,35 @@ def test_fused_row_compaction_matches_the_full_rows(cg, monkeypatch):
     assert rel_fro(np64(dW), np64(dW0)) <= 1e-3
 
 
+def test_fused_without_lse_skips_the_ignored_rows_forward():
+    """out_lse = NULL: the compacted forward covers only the non-ignored rows
+    (their lse is never observed).  Loss, logp and gradients match the oracle
+    and the call that returns lse."""
+    wl = WL.custom("fused_nolse", 6000, 256, 9000, 2048, w_std=0.05, targets="zipf", grpo_seqs=4,
+                   prompt_len=690, seed=507)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    N, H, V = wl.N, wl.H, wl.V
+    logp = torch.full((N,), float("nan"), device="cuda")
+    loss = torch.full((1,), float("nan"), device="cuda")
+    nv = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    dH = torch.full((N, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dW = torch.full((V, H), float("nan"), device="cuda")
+    assert _lib.flce_forward_backward(h, W, t, w, N, H, V, 2048, -100, None, 1.0, logp, None, loss, nv,
+                                      dH, dW) == 0
+    assert _lib.flce_device_status() == 0
+    ref = O.forward(inp.h, inp.W, inp.targets, inp.weights)
+    refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / ref.n_valid)
+    assert int(nv.item()) == ref.n_valid == 3240
+    assert_logp_close(np64(logp), ref.logp, "logp")
+    assert float(loss.item()) == pytest.approx(ref.loss, rel=LOSS_RTOL)
+    assert_grad_close(np64(dH), refb.dH, "dH")
+    assert_grad_close(np64(dW), refb.dW, "dW")
+    logp1, _, loss1, _, dH1, dW1 = run_fused(h, W, t, w, 2048)
+    assert torch.allclose(logp, logp1, atol=2e-5, rtol=0) and float(loss.item()) == pytest.approx(loss1, rel=1e-6)
+    assert rel_fro(np64(dH), np64(dH1)) <= 1e-3 and rel_fro(np64(dW), np64(dW1)) <= 1e-3
+
+
 @pytest.mark.slow
 def test_fused_grpo_32k_row_compaction(monkeypatch):
     """32,768 x 4,096 x 128,000 at 4,096-row blocks, 12.5 % of the rows in
