@@ -308,10 +308,13 @@ def gpu_arm(args):
                 logp.data_ptr(), None, loss.data_ptr(), nv.data_ptr(), dH.data_ptr(),
                 dW.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
             return
-        check("flce_forward_ex", lib.flce_forward_ex(
+        # the training step's forward (as the autograd wrapper runs it): the
+        # backward reads lse of the non-ignored rows only, so the GEMM skips
+        # the ignored ones
+        check("flce_forward_ex2", lib.flce_forward_ex2(
             h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, N, H, V, chunk_rows, -100, tf_ptr,
-            logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(), workspace.data_ptr(),
-            ws_bytes, sh))
+            _lib.FORWARD_SKIP_IGNORED, logp.data_ptr(), lse.data_ptr(), loss.data_ptr(), nv.data_ptr(),
+            workspace.data_ptr(), ws_bytes, sh))
         check("flce_backward_ex", lib.flce_backward_ex(
             h.data_ptr(), W.data_ptr(), t.data_ptr(), wp, lse.data_ptr(), g, dH.data_ptr(),
             dW.data_ptr(), N, H, V, chunk_rows, -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
@@ -385,7 +388,7 @@ def gpu_arm(args):
         if w_e is not None:
             w_e.copy_(w_host, non_blocking=True)
         hb = h_e.view(torch.bfloat16)
-        out = api.forward(hb, W, t_e, w_e, chunk_rows, workspace=workspace)
+        out = api.forward(hb, W, t_e, w_e, chunk_rows, workspace=workspace, skip_ignored=True)
         api.backward(hb, W, t_e, w_e, out["lse"], g, chunk_rows, workspace=workspace)
         loss_host.copy_(out["loss"].view(1), non_blocking=True)
         logp_host.copy_(out["logp"], non_blocking=True)
@@ -449,10 +452,11 @@ def gpu_arm(args):
 
     # ---- roofline of the dominant kernel (algorithmic FLOPs / live event time)
     peaks = load_peaks()
-    # algorithmic FLOPs: the forward needs every row's log-sum-exp; the
-    # backward GEMMs only the non-ignored rows (ignored rows have zero dlogits)
+    # algorithmic FLOPs: every GEMM of the training step covers the
+    # non-ignored rows only (the backward needs no ignored row's lse, and
+    # ignored rows have zero dlogits); the log-prob forward covers every row
     nv = n_valid_host
-    flops_step = {"fwd_logits_lse": 2.0 * N * V * H, "bwd_dlogits": 2.0 * nv * V * H,
+    flops_step = {"fwd_logits_lse": 2.0 * nv * V * H, "bwd_dlogits": 2.0 * nv * V * H,
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     if args.forward_only:
         flops_step = {"fwd_logits_lse": 2.0 * N * V * H}

@@ -32,6 +32,9 @@ SIGNATURES = {
     "flce_forward_ex": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
                                        _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                        ctypes.c_size_t, _c_vp]),
+    "flce_forward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
+                                        _c_i64, _c_vp, ctypes.c_uint32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                        ctypes.c_size_t, _c_vp]),
     "flce_backward_ex": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp,
                                         _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
                                         ctypes.c_size_t, _c_vp]),
@@ -188,6 +191,21 @@ def flce_forward_ex(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, t
                                ignore_index, tp, _ptr(out_logp), _ptr(out_lse), _ptr(out_loss),
                                _ptr(out_n_valid), _ptr(workspace), workspace_bytes,
                                _stream_handle(stream))
+
+
+FORWARD_SKIP_IGNORED = 1
+
+
+def flce_forward_ex2(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform, flags,
+                     out_logp, out_lse, out_loss, out_n_valid, workspace=None, workspace_bytes=0,
+                     stream=None) -> int:
+    """Raw C call with a logit transform and flags (FORWARD_SKIP_IGNORED)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_forward_ex2(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), N, H, V, chunk_rows,
+                                ignore_index, tp, int(flags), _ptr(out_logp), _ptr(out_lse),
+                                _ptr(out_loss), _ptr(out_n_valid), _ptr(workspace), workspace_bytes,
+                                _stream_handle(stream))
 
 
 def flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,

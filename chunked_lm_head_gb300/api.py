@@ -33,11 +33,14 @@ def workspace_bytes(N: int, H: int, V: int, chunk_rows: int) -> int:
 
 
 def forward(h, W, targets, weights=None, chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX,
-            workspace: torch.Tensor | None = None, stream=None, transform=None):
+            workspace: torch.Tensor | None = None, stream=None, transform=None,
+            skip_ignored: bool = False):
     """Returns dict(logp[N] f32, lse[N] f32, loss[] f32, n_valid[] i64), on device.
 
     ``transform``: None, or a dict with scale_multiply / scale_divide /
-    softcap / temperature (flce_logit_transform)."""
+    softcap / temperature (flce_logit_transform).  ``skip_ignored``: the GEMM
+    skips the ignored rows, whose lse is then NaN (the backward never reads
+    it)."""
     _check(h, W, targets, weights)
     N, H = h.shape
     V = W.shape[0]
@@ -47,9 +50,10 @@ def forward(h, W, targets, weights=None, chunk_rows: int = 256, ignore_index: in
     loss = torch.empty((), dtype=torch.float32, device=dev)
     n_valid = torch.empty((), dtype=torch.int64, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_forward_ex(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform,
-                              logp, lse, loss, n_valid, workspace, ws_bytes, stream)
-    _lib.check("flce_forward_ex", st)
+    flags = _lib.FORWARD_SKIP_IGNORED if skip_ignored else 0
+    st = _lib.flce_forward_ex2(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform,
+                               flags, logp, lse, loss, n_valid, workspace, ws_bytes, stream)
+    _lib.check("flce_forward_ex2", st)
     return {"logp": logp, "lse": lse, "loss": loss, "n_valid": n_valid}
 
 
@@ -104,7 +108,9 @@ class LinearCrossEntropy(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, h, W, targets, weights, chunk_rows, ignore_index, transform=None):
-        out = forward(h, W, targets, weights, chunk_rows, ignore_index, transform=transform)
+        # the backward reads lse of the non-ignored rows only
+        out = forward(h, W, targets, weights, chunk_rows, ignore_index, transform=transform,
+                      skip_ignored=True)
         ctx.transform = transform
         ctx.save_for_backward(h, W, targets, weights if weights is not None else torch.empty(0),
                               out["lse"], out["n_valid"])
@@ -199,7 +205,8 @@ class GRPOLoss(torch.autograd.Function):
     @staticmethod
     def forward(ctx, h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta,
                 chunk_rows, ignore_index, transform=None):
-        out = forward(h, W, targets, None, chunk_rows, ignore_index, transform=transform)
+        out = forward(h, W, targets, None, chunk_rows, ignore_index, transform=transform,
+                      skip_ignored=True)
         tok = grpo_token_loss(out["logp"], advantages, targets, old_logp, ref_logp, eps_low, eps_high,
                               beta, ignore_index)
         ctx.save_for_backward(h, W, targets, out["lse"], tok["weights"], tok["n_valid"])

@@ -79,20 +79,24 @@ __device__ __forceinline__ void block_sum_store(double contrib, long long cnt, d
 // block's share of sum(w * logp) and of the valid-row count.
 // Rows [0, N) of the arrays passed (callers offset them for a row range),
 // or with `ri` the rows ri[0..N) of the whole arrays; `stride` is the
-// distance between two splits' partials of one row.
+// distance between two splits' partials of one row.  skip_ignored: the
+// forward skipped the ignored rows, whose lse becomes NaN.
 template <bool kLong>
 __global__ void combine_kernel(const float2* __restrict__ part, int S, int stride, int N,
                                const float* __restrict__ zt, const int64_t* __restrict__ targets,
                                const float* __restrict__ weights, long long ignore,
                                float* __restrict__ out_logp, float* __restrict__ out_lse,
                                double* __restrict__ blk_sum, long long* __restrict__ blk_cnt,
-                               const int* __restrict__ ri) {
+                               const int* __restrict__ ri, int skip_ignored = 0) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   const int j = blockIdx.x * SMALL_THREADS + threadIdx.x;
   double contrib = 0.0;
   long long cnt = 0;
-  if (j < N) {
-    const int i = ri ? ri[j] : j;  // the j-th row of this range
+  const int i = j < N ? (ri ? ri[j] : j) : 0;  // the j-th row of this range
+  if (j < N && skip_ignored && targets[i] == ignore) {  // forward skipped: lse not computed
+    if (out_lse) out_lse[i] = __int_as_float(0x7fc00000);
+    if (out_logp) out_logp[i] = 0.f;
+  } else if (j < N) {
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, part[static_cast<idx_t>(s) * stride + i].x);
     float sum = 0.f;
@@ -839,10 +843,13 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
   return best;
 }
 
+// Forward scratch.  fb_skip > 0 adds what a forward that skips the ignored
+// rows needs: the non-ignored row indices and count, and a gathered [fb_skip,
+// H] block of h rows per launch.
 struct FwdLayout {
-  size_t zt = 0, part = 0, bsum = 0, bcnt = 0, bad = 0, total = 0;
+  size_t zt = 0, part = 0, bsum = 0, bcnt = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, total = 0;
 };
-FwdLayout fwd_layout(long long N, const FwdPlan& f) {
+FwdLayout fwd_layout(long long N, const FwdPlan& f, long long H = 0, long long fb_skip = 0) {
   FwdLayout L;
   size_t o = 0;
   L.zt = o;
@@ -855,6 +862,16 @@ FwdLayout fwd_layout(long long N, const FwdPlan& f) {
   o += align256(static_cast<size_t>(f.nblk) * 8);
   L.bad = o;
   o += 256;
+  if (fb_skip > 0) {
+    L.idx = o;
+    o += align256(static_cast<size_t>(N) * 4);
+    L.blk = o;
+    o += align256(static_cast<size_t>(ceil_div(std::max(1LL, N), COMPACT_ROWS_PER_BLOCK)) * 4);
+    L.count = o;
+    o += 256;
+    L.hc = o;
+    o += align256(static_cast<size_t>(fb_skip) * H * 2);
+  }
   L.total = o;
   return L;
 }
@@ -1354,15 +1371,16 @@ FusedLayout fused_layout(long long N, long long H, const FusedPlan& fp) {
 flce_status ce_forward_tail(bool kLong, const FwdPlan& f, int N, const float2* part, const float* zt,
                             const int64_t* targets, const float* weights, long long ignore,
                             float* out_logp, float* out_lse, float* out_loss, int64_t* out_n_valid,
-                            double* bsum, long long* bcnt, cudaStream_t st) {
+                            double* bsum, long long* bcnt, cudaStream_t st, bool skip_ignored = false) {
   if (N > 0) {
     ProfScope ps(K_COMBINE, st);
+    const int sk = skip_ignored ? 1 : 0;
     if (kLong)
       combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
-                                                             out_logp, out_lse, bsum, bcnt, nullptr);
+                                                             out_logp, out_lse, bsum, bcnt, nullptr, sk);
     else
       combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
-                                                              out_logp, out_lse, bsum, bcnt, nullptr);
+                                                              out_logp, out_lse, bsum, bcnt, nullptr, sk);
     FLCE_CUDA_TRY(cudaGetLastError());
   }
   return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
@@ -1389,7 +1407,9 @@ size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows)
   if (!sizes_ok(N, H, V)) return 0;
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  const FwdLayout fl = fwd_layout(N, plan_forward_call(N, H, V, workers, BM * cg));
+  // the forward's layout with the buffers of flce_forward_ex2's row skipping
+  const FwdLayout fl =
+      fwd_layout(N, plan_forward_call(N, H, V, workers, BM * cg), H, fwd_block_rows(N, BM * cg));
   const BwdLayout bl = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
@@ -1417,7 +1437,7 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
                                 int64_t ignore_index, const flce_logit_transform* transform,
                                 float* out_logp, float* out_lse, float* out_loss,
                                 int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
-                                void* stream, size_t partials_cap) {
+                                void* stream, size_t partials_cap, bool skip_ignored = false) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
@@ -1433,7 +1453,7 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
   // rows per forward launch (FLCE_FWD_BLOCK_ROWS; 0: all rows in one launch)
   const long long fb = fwd_block_rows(N, BM * cg);
   const FwdPlan f = plan_forward_call(N, H, V, workers, BM * cg, partials_cap);
-  const FwdLayout L = fwd_layout(N, f);
+  const FwdLayout L = fwd_layout(N, f, H, skip_ignored ? fb : 0);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
   if (s != FLCE_OK) return s;
@@ -1460,8 +1480,24 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
       FLCE_CUDA_TRY(cudaStreamSynchronize(st));
       if (nbad != 0) return FLCE_ERR_BAD_TARGET;
     }
+    // skip_ignored: the launches run over the non-ignored rows only, each
+    // over a gathered block of fb of them (the count stays on the device)
+    int* cidx = reinterpret_cast<int*>(wb + L.idx);
+    int* ccount = reinterpret_cast<int*>(wb + L.count);
+    uint16_t* hc = reinterpret_cast<uint16_t*>(wb + L.hc);
+    if (skip_ignored) {
+      const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
+      int* cblk = reinterpret_cast<int*>(wb + L.blk);
+      ProfScope ps(K_COMPACT, st);
+      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk);
+      FLCE_CUDA_TRY(cudaGetLastError());
+      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk, nblk, cidx, ccount,
+                                                           0);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
     CUtensorMap tA, tB;
-    if (!make_map(&tA, h, H, N, H, BK, BM) || !make_map(&tB, W, H, V, H, BK, BN / cg))
+    if (!make_map(&tA, skip_ignored ? hc : h, H, skip_ignored ? fb : N, H, BK, BM) ||
+        !make_map(&tB, W, H, V, H, BK, BN / cg))
       return FLCE_ERR_CUDA;
     GemmParams p{};
     p.m_tiles = f.m_tiles;
@@ -1505,11 +1541,23 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
       q.m_tiles = static_cast<int>(ceil_div(q.rows, BM * cg));
       q.num_units = q.m_tiles * f.S;
       q.group_m = std::min(16, q.m_tiles);
+      if (skip_ignored) {  // non-ignored rows [row0, row0 + fb), gathered
+        q.row0 = 0;
+        q.row_idx = cidx;
+        q.dyn_count = ccount;
+        q.chunk_first = static_cast<int>(row0);
+        const long long total = fb * (H / 8);
+        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
+        ProfScope ps(K_GATHER, st);
+        gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, ccount, Ni,
+                                                            static_cast<int>(row0), static_cast<int>(fb), hc);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
       ProfScope ps(K_FWD, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(cg, kLong, tA, tB, tB, q, std::min(q.num_units, workers), st));
     }
     return ce_forward_tail(kLong, f, Ni, part, zt, targets, weights, ignore_index, out_logp, out_lse,
-                           out_loss, out_n_valid, bsum, bcnt, st);
+                           out_loss, out_n_valid, bsum, bcnt, st, skip_ignored);
   }
   return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
 }
@@ -1523,6 +1571,19 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
   (void)chunk_rows;
   return forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, out_lse,
                       out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap);
+}
+
+flce_status flce_forward_ex2(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                             const float* weights, int64_t N, int64_t H, int64_t V,
+                             int64_t chunk_rows, int64_t ignore_index,
+                             const flce_logit_transform* transform, uint32_t flags, float* out_logp,
+                             float* out_lse, float* out_loss, int64_t* out_n_valid, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  (void)chunk_rows;
+  if ((flags & ~static_cast<uint32_t>(FLCE_FORWARD_SKIP_IGNORED)) != 0) return FLCE_ERR_INVALID_ARG;
+  const bool skip = (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_env();
+  return forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, out_lse,
+                      out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap, skip);
 }
 
 // The backward; count_scale (device int64, or NULL) divides grad_scale by

@@ -140,6 +140,26 @@ FLCE_API flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, con
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * flce_forward_ex with flags (0 = flce_forward_ex).
+ *   FLCE_FORWARD_SKIP_IGNORED: the GEMM covers the non-ignored rows only
+ *     (the row skipping of the Unsloth page's "Flattened sequence-length
+ *     chunking" applied to the forward).  Ignored rows get out_lse = NaN
+ *     (not computed) and out_logp = 0; flce_backward never reads their lse.
+ *     The rows are found and gathered on the device (no host sync), in
+ *     blocks of 4,096 rows of h inside the workspace that
+ *     flce_workspace_bytes reports.  FLCE_COMPACT=0 turns the skipping off.
+ * Other flag bits: FLCE_ERR_INVALID_ARG.
+ */
+#define FLCE_FORWARD_SKIP_IGNORED 1u
+FLCE_API flce_status flce_forward_ex2(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                      const float* weights, int64_t N, int64_t H, int64_t V,
+                                      int64_t chunk_rows, int64_t ignore_index,
+                                      const flce_logit_transform* transform, uint32_t flags,
+                                      float* out_logp, float* out_lse, float* out_loss,
+                                      int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/*
  * Backward: dH = D W and dW = D^T h with
  *   D[i,v] = (exp(z[i,v] - lse[i]) - [v == targets[i]]) * m[i] * w[i] * grad_scale.
  *

@@ -23,6 +23,12 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_forward_ex2_rejects_unknown_flags(lib):
+    # checked before any pointer or device access
+    assert _lib.flce_forward_ex2(None, None, None, None, 8, 8, 8, 8, -100, None, 2, None, None, None,
+                                 None, stream=0) == 1  # FLCE_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert _lib.flce_status_string(code) == name

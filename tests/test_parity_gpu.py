@@ -267,6 +267,48 @@ def test_row_compaction_matches_full_rows(monkeypatch):
     assert torch.all(dH_c[ign] == 0)
 
 
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_forward_skipping_ignored_rows(cg, monkeypatch):
+    """flce_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED: 4 forward launches of
+    512 rows over the non-ignored rows (the last two launches hold fewer
+    rows, or none), against the oracle.  Ignored rows get lse NaN and logp 0;
+    the backward from that lse (compacted and over every row) matches the
+    oracle."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    monkeypatch.setenv("FLCE_FWD_BLOCK_ROWS", "512")
+    wl = WL.custom("fskip", 1900, 192, 3100, 256, w_std=0.05, targets="zipf", grpo_seqs=4,
+                   prompt_len=280, seed=112)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(5).uniform(0.2, 2.0, wl.N).astype(np.float32)
+    h, W, t, w = upload(inp)
+    N, H, V = wl.N, wl.H, wl.V
+    logp = torch.full((N,), 7.0, device="cuda")
+    lse = torch.full((N,), 7.0, device="cuda")
+    loss = torch.full((1,), float("nan"), device="cuda")
+    nv = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    assert _lib.flce_forward_ex2(h, W, t, w, N, H, V, 256, -100, None, _lib.FORWARD_SKIP_IGNORED, logp, lse,
+                                 loss, nv) == 0
+    assert _lib.flce_device_status() == 0
+    ref = O.forward(inp.h, inp.W, inp.targets, inp.weights)
+    m = inp.targets != WL.IGNORE_INDEX
+    assert int(nv.item()) == ref.n_valid == 1900 - 4 * 280
+    assert float(loss.item()) == pytest.approx(ref.loss, rel=LOSS_RTOL)
+    assert_logp_close(np64(logp), ref.logp, "logp")
+    assert_logp_close(np64(lse)[m], ref.lse[m], "lse (non-ignored rows)")
+    assert np.all(np.isnan(np64(lse)[~m])) and np.all(np64(logp)[~m] == 0.0)
+    g = 1.0 / ref.n_valid
+    refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g)
+    for compact in ("1", "0"):
+        monkeypatch.setenv("FLCE_COMPACT", compact)
+        dH, dW = run_backward(h, W, t, w, lse, g, 256)
+        assert_grad_close(np64(dH), refb.dH, f"dH (compact {compact})")
+        assert_grad_close(np64(dW), refb.dW, f"dW (compact {compact})")
+    # FLCE_COMPACT=0 turns the skipping off: every row gets its lse
+    assert _lib.flce_forward_ex2(h, W, t, w, N, H, V, 256, -100, None, _lib.FORWARD_SKIP_IGNORED, logp, lse,
+                                 loss, nv) == 0
+    assert_logp_close(np64(lse), ref.lse, "lse (skipping off)")
+
+
 @pytest.mark.parametrize("splits", ["1", "3", "7"])
 def test_forward_independent_of_vocabulary_splits(splits, monkeypatch):
     """The split-V combine against a single split (and odd split counts):
