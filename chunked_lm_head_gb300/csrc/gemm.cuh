@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
       const Unit t = decode_unit<MODE>(p, dsh, u);
       // per-unit row state
-      const int lr = t.m * C::TM + rank * BM + r;  // row inside this pass (FWD: global row)
+      const int lr = t.m * C::TM + rank * BM + r;  // row inside this pass (original row: grow)
       bool row_ok;
       long long tgt = -1;
       float run_m = -INFINITY, run_s = 0.f;  // FWD: log2-domain max and sum
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         row_ok = lr < dsh.rows;
       }
       // original row of this accumulator row (targets, weights, lse, dH;
-      // the fused forward's partials and target logit)
+      // the forward modes' partials and target logit)
       int grow = p.row0 + lr;
       if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD) {
         if (p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
