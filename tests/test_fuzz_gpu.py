@@ -1,7 +1,7 @@
 """Seeded random small problems (ragged N, H down to 8, V down to 1, chunk
 sizes from 1 row up, masks, weights, transforms, both CTA-group paths, row
-compaction on and off, forced backward row blocks, the one-call path) against
-the fp64 oracle."""
+compaction on and off, forced backward row blocks, the one-call path, the
+forward that skips ignored rows) against the fp64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -66,6 +66,20 @@ def test_random_problem_matches_oracle(c, monkeypatch):
                                           g * max(ref.n_valid, 1), logp, lse, loss_t, nv_t, dH, dW) == 0
         assert _lib.flce_device_status() == 0
         loss, nv = float(loss_t.item()), int(nv_t.item())
+    elif c["seed"] % 2 == 0:  # the forward that skips ignored rows (their lse is NaN)
+        logp = torch.empty(N, dtype=torch.float32, device="cuda")
+        lse = torch.empty(N, dtype=torch.float32, device="cuda")
+        loss_t = torch.empty(1, dtype=torch.float32, device="cuda")
+        nv_t = torch.empty(1, dtype=torch.int64, device="cuda")
+        assert _lib.flce_forward_ex2(h, W, t, w, N, H, V, c["chunk"], -100, tfd, _lib.FORWARD_SKIP_IGNORED,
+                                     logp, lse, loss_t, nv_t) == 0
+        assert _lib.flce_device_status() == 0
+        loss, nv = float(loss_t.item()), int(nv_t.item())
+        dH, dW = run_backward(h, W, t, w, lse, g, c["chunk"], transform=tfd)
+        m = inp.targets != WL.IGNORE_INDEX
+        if c["compact"] == "1":
+            assert np.all(np.isnan(np64(lse)[~m]))
+            lse = torch.from_numpy(np.where(m, np64(lse), ref.lse))  # compared on the counted rows
     else:
         logp, lse, loss, nv = run_forward(h, W, t, w, c["chunk"], transform=tfd)
         dH, dW = run_backward(h, W, t, w, lse, g, c["chunk"], transform=tfd)
