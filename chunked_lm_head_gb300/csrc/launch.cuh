@@ -1,0 +1,391 @@
+// libflce host side: argument checks, TMA tensor maps, persistent GEMM
+// launches (clusters, programmatic dependent launch), run-time switches,
+// workspaces, and the stages the entry points share (dH / dW of a slab, the
+// split-K dH reduction, the forward's combine and loss).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdlib>
+
+#include "flce.h"
+#include "plan.cuh"
+
+namespace {
+
+using namespace flce;
+
+bool sizes_ok(long long N, long long H, long long V) {
+  return N >= 0 && H > 0 && V > 0 && N < INT_MAX && H < INT_MAX && V < INT_MAX;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// --------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map: `inner` contiguous elements per row, `outer` rows of `ld_elems`
+// elements; box box_inner x box_outer with 128-byte swizzle; out-of-range
+// elements read as zero (loads) or are skipped (stores).
+bool make_map_t(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, long long inner,
+                long long outer, long long ld_elems, int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * esize};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long ld_elems,
+              int box_inner, int box_outer) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld_elems, box_inner,
+                    box_outer);
+}
+
+// Programmatic dependent launch of the GEMMs (default; FLCE_PDL=0 turns it
+// off): a GEMM may be scheduled while the previous kernel of the stream
+// drains, runs its prologue (barriers, TMEM, descriptor prefetch) and then
+// waits in griddepcontrol.wait until that kernel has completed.  Each GEMM
+// grid fits on the GPU at once, so the waiting CTAs never hold SMs that the
+// kernel they wait for still needs.
+bool pdl_env() {
+  const char* s = std::getenv("FLCE_PDL");
+  return !(s != nullptr && s[0] == '0');
+}
+
+// Launch on `grid` CTAs in clusters of `cluster` with the GEMMs' attributes.
+template <class Kern, class... Args>
+cudaError_t launch_persistent(Kern k, int grid, int cluster, int smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl_env()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int MODE, bool kLong, int CG>
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                          const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p,
+                          int workers, cudaStream_t st) {
+  auto k = flce_gemm_kernel<MODE, kLong, CG>;
+  constexpr int smem = TileCfg<CG>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_persistent(k, CG * workers, CG, smem, st, a, b, c, a2, b2, p);
+}
+
+// `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
+// tile loop.  `c` is the output map of the modes that write through TMA (dW);
+// the other modes ignore it.
+template <int MODE>
+cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st,
+                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr) {
+  // a2 / b2: the teacher's operands of the distillation modes (else unused)
+  const CUtensorMap& A2 = a2 ? *a2 : a;
+  const CUtensorMap& B2 = b2 ? *b2 : b;
+  if (cg == 2)
+    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, A2, B2, p, workers, st)
+                 : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, p, workers, st);
+  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, A2, B2, p, workers, st)
+               : launch_gemm_t<MODE, false, 1>(a, b, c, A2, B2, p, workers, st);
+}
+
+// The e4m3 forward: MODE_FWD with 8-bit operands.
+cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int workers, cudaStream_t st) {
+  auto go = [&](auto kern, int smem, int grid_mult) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_persistent(kern, grid_mult * workers, grid_mult, smem, st, a, b, b, a, b, p);
+  };
+  if (cg == 2)
+    return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)
+                 : go(flce_gemm_kernel<MODE_FWD, false, 2, true>, TileCfg<2>::SMEM, 2);
+  return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 1, true>, TileCfg<1>::SMEM, 1)
+               : go(flce_gemm_kernel<MODE_FWD, false, 1, true>, TileCfg<1>::SMEM, 1);
+}
+
+// CTA group of the GEMMs: 2 (SM pairs, 256-row tiles) unless FLCE_CTA_GROUP=1.
+int cta_group() {
+  const char* s = std::getenv("FLCE_CTA_GROUP");
+  return (s != nullptr && s[0] == '1') ? 1 : 2;
+}
+
+// Persistent workers the GPU holds at once: CTAs, or co-resident CTA pairs.
+int device_workers(int cg) {
+  const int sms = device_sms();
+  if (cg == 1) return sms;
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return sms / 2;
+  }
+  if (dev == cached_dev && cached > 0) return cached;
+  int n = 0;
+  auto k = flce_gemm_kernel<MODE_FWD, false, 2>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = TileCfg<2>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<2>::SMEM) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  cached_dev = dev;
+  cached = n;
+  return n;
+}
+
+// Backward on non-ignored rows only (default); FLCE_COMPACT=0 runs every row.
+bool compact_env() {
+  const char* s = std::getenv("FLCE_COMPACT");
+  return !(s != nullptr && s[0] == '0');
+}
+
+// DLOGITS writes D through TMA boxes (default) or per-thread stores
+// (FLCE_D_TMA=0).
+bool d_tma_env() {
+  const char* s = std::getenv("FLCE_D_TMA");
+  return !(s != nullptr && s[0] == '0');
+}
+
+bool validate_env() {
+  const char* s = std::getenv("FLCE_VALIDATE");
+  return s != nullptr && s[0] != '\0' && s[0] != '0';
+}
+
+// Stream-ordered workspace: the caller's, or one allocated here and freed on
+// the same stream when the call ends.
+struct Workspace {
+  void* ptr = nullptr;
+  bool owned = false;
+  cudaStream_t st = nullptr;
+  ~Workspace() {
+    if (owned && ptr != nullptr) cudaFreeAsync(ptr, st);
+  }
+};
+
+flce_status get_workspace(Workspace& ws, void* user, size_t user_bytes, size_t need, cudaStream_t st) {
+  ws.st = st;
+  if (user != nullptr) {
+    if (user_bytes < need || !aligned(user, 256)) return FLCE_ERR_INVALID_ARG;
+    ws.ptr = user;
+    return FLCE_OK;
+  }
+  if (cudaMallocAsync(&ws.ptr, std::max<size_t>(need, 256), st) != cudaSuccess) {
+    cudaGetLastError();
+    ws.ptr = nullptr;
+    return FLCE_ERR_OOM;
+  }
+  ws.owned = true;
+  return FLCE_OK;
+}
+
+// Kernel form of a logit transform (see flce_logit_transform): y = a * z, or
+// y = b * tanh(a * z) with dy/dz = d * (1 - tanh^2).  False on invalid values.
+bool transform_params(const flce_logit_transform* tf, GemmParams& p) {
+  p.tf_softcap = 0;
+  p.tf_a = 1.f;
+  p.tf_b = 1.f;
+  p.tf_d = 1.f;
+  if (tf == nullptr) return true;
+  const float mul = tf->scale_multiply, div = tf->scale_divide, cap = tf->softcap, T = tf->temperature;
+  if (!(std::isfinite(mul) && std::isfinite(div) && std::isfinite(cap) && std::isfinite(T))) return false;
+  if (mul < 0.f || div < 0.f || cap < 0.f || !(T > 0.f)) return false;
+  const float s1 = (mul != 0.f ? mul : 1.f) / (div != 0.f ? div : 1.f);
+  if (!(s1 > 0.f) || !std::isfinite(s1)) return false;
+  if (cap != 0.f) {
+    p.tf_softcap = 1;
+    p.tf_a = s1 / cap;
+    p.tf_b = cap / T;
+    p.tf_d = s1 / T;
+  } else {
+    p.tf_a = s1 / T;
+  }
+  return std::isfinite(p.tf_a) && std::isfinite(p.tf_b) && std::isfinite(p.tf_d) && p.tf_a > 0.f;
+}
+
+#define FLCE_CUDA_TRY(x)                 \
+  do {                                   \
+    if ((x) != cudaSuccess) {            \
+      cudaGetLastError();                \
+      return FLCE_ERR_CUDA;              \
+    }                                    \
+  } while (0)
+
+// Final deterministic reduction of the block partials into loss and count.
+flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, const double* bsum,
+                      const long long* bcnt, cudaStream_t st) {
+  if (out_loss || out_n_valid) {
+    ProfScope ps(K_FINAL, st);
+    final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt, f.nblk, out_loss,
+                                              reinterpret_cast<long long*>(out_n_valid));
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
+}
+
+// ---- stages shared by the entry points
+
+// Row tiles per dH raster group: 8 (FLCE_DH_GROUP overrides).  A wave of 76
+// units then covers 8 row tiles x ~9.5 column tiles, the fewest D and W
+// slices per wave.  On 16,384 x 4,096 x 151,936, interleaved runs timed the
+// step 1.3% faster than with all 16 row tiles (the dH launch itself took the
+// same time); a dH launch's DRAM bytes vary more between GPUs than between
+// the two groups.
+int dh_group_rows(int m_tiles) {
+  int g = 8;
+  if (const char* e = std::getenv("FLCE_DH_GROUP")) g = std::atoi(e);
+  return g > 0 ? std::min(g, m_tiles) : m_tiles;
+}
+
+// dH and dW stages of the backward, shared by the cross-entropy and the
+// distillation backwards.  For one row block and one vocabulary slab, the
+// slab's bf16 dlogits sit in D (maps D_k / D_mn, local columns); B_dw maps the
+// block's rows of h (the gathered rows when compacted).  ri / dc / first:
+// compaction (original row of each compacted row, device-side row count, first
+// compacted row of the block), or null.
+struct DhDwStage {
+  int cg, workers, tm;
+  bool kLong;
+  const BwdPlan* plan;
+  long long H, V;
+  float* dh_part;
+  flce_bf16* dH;
+  float* dW;
+  const CUtensorMap* W_mn;
+  const CUtensorMap* dW_map;
+  const CUtensorMap* dhp_map;  // fp32 dH partials [dh_splits * R][H]
+};
+
+flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int block, int slab, int v0,
+                       int width, const CUtensorMap& D_k, const CUtensorMap& D_mn,
+                       const CUtensorMap& B_dw, cudaStream_t st) {
+  const BwdPlan& b = *a.plan;
+  if (a.dH) {  // dH[rows] (+)= D[:, slab] W[slab]
+    GemmParams q = p;
+    q.v0 = v0;
+    q.m_tiles = static_cast<int>(ceil_div(rows, a.tm));
+    q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    q.k_blocks = static_cast<int>(ceil_div(width, BK));
+    q.cols = q.n_tiles;
+    q.n_per_unit = 1;
+    q.kb_per_split = b.dh_kb_per_split;
+    const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
+    q.k_splits = splits;
+    q.num_units = splits * q.m_tiles * q.n_tiles;
+    q.group_m = dh_group_rows(q.m_tiles);
+    q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
+    q.dh_accumulate = slab > 0 ? 1 : 0;
+    ProfScope ps(K_DH, st);
+    FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
+                                       std::min(q.num_units, a.workers), st));
+  }
+  if (a.dW) {  // dW[slab] (+)= D[:, slab]^T h[rows]
+    GemmParams q = p;
+    q.v0 = v0;
+    q.m_tiles = static_cast<int>(ceil_div(width, a.tm));
+    q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    q.k_blocks = static_cast<int>(ceil_div(rows, BK));
+    q.cols = q.n_tiles;
+    q.n_per_unit = 1;
+    q.kb_per_split = q.k_blocks;
+    q.k_splits = 1;
+    q.num_units = q.m_tiles * q.n_tiles;
+    q.group_m = std::min(8, q.m_tiles);
+    q.dW_accumulate = block > 0 ? 1 : 0;
+    ProfScope ps(K_DW, st);
+    FLCE_CUDA_TRY(launch_gemm<MODE_DW>(a.cg, a.kLong, D_mn, B_dw, *a.dW_map, q,
+                                       std::min(q.num_units, a.workers), st));
+  }
+  return FLCE_OK;
+}
+
+// After the last slab of a row block: the block's fp32 dH partials, summed
+// over the k-splits and rounded to bf16, into its rows of dH.
+flce_status block_dh_finish(const DhDwStage& a, int row0, int rows, const int* ri, const int* dc,
+                            int first, cudaStream_t st) {
+  const BwdPlan& b = *a.plan;
+  if (!a.dH || !b.dh_f32) return FLCE_OK;
+  ProfScope ps(K_DH_REDUCE, st);
+  const long long total = static_cast<long long>(rows) * (a.H / 4);
+  const int grid = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms())));
+  if (a.kLong)
+    dh_reduce_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, b.dh_splits, rows, static_cast<int>(b.R),
+                                                           static_cast<int>(a.H), row0, a.dH, ri, dc, first);
+  else
+    dh_reduce_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(a.dh_part, b.dh_splits, rows, static_cast<int>(b.R),
+                                                            static_cast<int>(a.H), row0, a.dH, ri, dc, first);
+  FLCE_CUDA_TRY(cudaGetLastError());
+  return FLCE_OK;
+}
+
+// Cross-entropy forward tail: per-row combine of the split partials, then
+// the deterministic loss / count reduction.
+flce_status ce_forward_tail(bool kLong, const FwdPlan& f, int N, const float2* part, const float* zt,
+                            const int64_t* targets, const float* weights, long long ignore,
+                            float* out_logp, float* out_lse, float* out_loss, int64_t* out_n_valid,
+                            double* bsum, long long* bcnt, cudaStream_t st, bool skip_ignored = false) {
+  if (N > 0) {
+    ProfScope ps(K_COMBINE, st);
+    const int sk = skip_ignored ? 1 : 0;
+    if (kLong)
+      combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
+                                                             out_logp, out_lse, bsum, bcnt, nullptr, sk);
+    else
+      combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(part, f.S, N, N, zt, targets, weights, ignore,
+                                                              out_logp, out_lse, bsum, bcnt, nullptr, sk);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return loss_tail(f, out_loss, out_n_valid, bsum, bcnt, st);
+}
+
+}  // namespace
