@@ -683,7 +683,7 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
   if (out_loss || out_n_valid) {
     ProfScope ps(K_FINAL, st);
     // every segment entry was written: full blocks fill theirs, and the last
-    // block's unused entries are zeroed below before the loop
+    // block's unused entries were zeroed before the loop
     final_kernel<<<1, SMALL_THREADS, 0, st>>>(bsum, bcnt,
                                               static_cast<int>(ceil_div(N, fp.R) * ceil_div(fp.R, SMALL_THREADS)),
                                               out_loss, reinterpret_cast<long long*>(out_n_valid));
