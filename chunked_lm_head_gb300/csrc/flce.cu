@@ -213,6 +213,19 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
                       out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap);
 }
 
+}  // extern "C"
+
+namespace {
+// fewest rows for which flce_forward_ex2 skips ignored rows (FLCE_SKIP_MIN_ROWS
+// overrides): below it the three extra launches cost more than the rows save
+int64_t skip_min_rows() {
+  if (const char* e = std::getenv("FLCE_SKIP_MIN_ROWS")) return std::max<int64_t>(0, std::atoll(e));
+  return 2048;
+}
+}  // namespace
+
+extern "C" {
+
 flce_status flce_forward_ex2(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
                              const float* weights, int64_t N, int64_t H, int64_t V,
                              int64_t chunk_rows, int64_t ignore_index,
@@ -221,7 +234,7 @@ flce_status flce_forward_ex2(const flce_bf16* h, const flce_bf16* W, const int64
                              size_t workspace_bytes, void* stream) {
   (void)chunk_rows;
   if ((flags & ~static_cast<uint32_t>(FLCE_FORWARD_SKIP_IGNORED)) != 0) return FLCE_ERR_INVALID_ARG;
-  const bool skip = (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_env();
+  const bool skip = (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_env() && N >= skip_min_rows();
   return forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, out_lse,
                       out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap, skip);
 }

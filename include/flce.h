@@ -147,7 +147,9 @@ FLCE_API flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, con
  *     (not computed) and out_logp = 0; flce_backward never reads their lse.
  *     The rows are found and gathered on the device (no host sync), in
  *     blocks of 4,096 rows of h inside the workspace that
- *     flce_workspace_bytes reports.  FLCE_COMPACT=0 turns the skipping off.
+ *     flce_workspace_bytes reports.  Calls with N < 2,048 rows
+ *     (FLCE_SKIP_MIN_ROWS overrides the bound), or with FLCE_COMPACT=0,
+ *     compute every row as flce_forward_ex does.
  * Other flag bits: FLCE_ERR_INVALID_ARG.
  */
 #define FLCE_FORWARD_SKIP_IGNORED 1u

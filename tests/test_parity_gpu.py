@@ -269,14 +269,14 @@ def test_row_compaction_matches_full_rows(monkeypatch):
 
 @pytest.mark.parametrize("cg", ["1", "2"])
 def test_forward_skipping_ignored_rows(cg, monkeypatch):
-    """flce_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED: 4 forward launches of
-    512 rows over the non-ignored rows (the last two launches hold fewer
-    rows, or none), against the oracle.  Ignored rows get lse NaN and logp 0;
-    the backward from that lse (compacted and over every row) matches the
+    """flce_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED: 5 forward launches of
+    512 rows over the non-ignored rows (the third holds 256, the last two
+    none), against the oracle.  Ignored rows get lse NaN and logp 0; the
+    backward from that lse (compacted and over every row) matches the
     oracle."""
     monkeypatch.setenv("FLCE_CTA_GROUP", cg)
     monkeypatch.setenv("FLCE_FWD_BLOCK_ROWS", "512")
-    wl = WL.custom("fskip", 1900, 192, 3100, 256, w_std=0.05, targets="zipf", grpo_seqs=4,
+    wl = WL.custom("fskip", 2400, 192, 3100, 256, w_std=0.05, targets="zipf", grpo_seqs=4,
                    prompt_len=280, seed=112)
     inp = WL.make_inputs(wl)
     inp.weights = np.random.default_rng(5).uniform(0.2, 2.0, wl.N).astype(np.float32)
@@ -291,7 +291,7 @@ def test_forward_skipping_ignored_rows(cg, monkeypatch):
     assert _lib.flce_device_status() == 0
     ref = O.forward(inp.h, inp.W, inp.targets, inp.weights)
     m = inp.targets != WL.IGNORE_INDEX
-    assert int(nv.item()) == ref.n_valid == 1900 - 4 * 280
+    assert int(nv.item()) == ref.n_valid == 2400 - 4 * 280
     assert float(loss.item()) == pytest.approx(ref.loss, rel=LOSS_RTOL)
     assert_logp_close(np64(logp), ref.logp, "logp")
     assert_logp_close(np64(lse)[m], ref.lse[m], "lse (non-ignored rows)")
@@ -303,10 +303,17 @@ def test_forward_skipping_ignored_rows(cg, monkeypatch):
         dH, dW = run_backward(h, W, t, w, lse, g, 256)
         assert_grad_close(np64(dH), refb.dH, f"dH (compact {compact})")
         assert_grad_close(np64(dW), refb.dW, f"dW (compact {compact})")
-    # FLCE_COMPACT=0 turns the skipping off: every row gets its lse
+    # FLCE_COMPACT=0 turns the skipping off, and so do calls under 2,048 rows:
+    # every row gets its lse
     assert _lib.flce_forward_ex2(h, W, t, w, N, H, V, 256, -100, None, _lib.FORWARD_SKIP_IGNORED, logp, lse,
                                  loss, nv) == 0
     assert_logp_close(np64(lse), ref.lse, "lse (skipping off)")
+    monkeypatch.setenv("FLCE_COMPACT", "1")
+    n = 2000
+    assert _lib.flce_forward_ex2(h[:n], W, t[:n], w[:n], n, H, V, 256, -100, None, _lib.FORWARD_SKIP_IGNORED,
+                                 logp[:n], lse[:n], loss, nv) == 0
+    assert_logp_close(np64(lse[:n]), O.forward(inp.h[:n], inp.W, inp.targets[:n], inp.weights[:n]).lse,
+                      "lse (2,000 rows)")
 
 
 @pytest.mark.parametrize("splits", ["1", "3", "7"])
