@@ -67,6 +67,28 @@ def reduce_max(x: float, device=None) -> float:
     return float(t.item())
 
 
+def algorithmic_bytes_step(N: int, nv: int, H: int, V: int, chunk_rows: int,
+                           forward_rows: int) -> dict[str, float]:
+    """Bytes each GEMM kind must move per step (bf16 operands, fp32 outputs)
+    under the library's launch decomposition, for the forward + recomputing
+    backward: forward launches of 4,096 rows, backward row blocks x
+    vocabulary slabs from flce_backward_plan, over the non-ignored rows.
+    Re-reads beyond one pass per launch are what ncu's DRAM counters add."""
+    from chunked_lm_head_gb300 import _lib
+    plan = _lib.flce_backward_plan(N, H, V, chunk_rows)
+    R, S, splits = plan["rows_per_block"], plan["vocab_slabs"], plan["dh_splits"]
+    B = max(1, -(-nv // R))  # row blocks with rows (compacted)
+    Lf = max(1, -(-forward_rows // 4096))
+    W, hb, Db = V * H * 2.0, H * 2.0, V * 2.0
+    dh_out = nv * H * 2.0 if (splits == 1 and S == 1) else nv * H * 4.0 * splits * (2 * S - 1)
+    return {
+        "fwd_logits_lse": Lf * W + forward_rows * hb,
+        "bwd_dlogits": B * W + S * nv * hb + nv * Db,
+        "bwd_dH": nv * Db + B * W + dh_out,
+        "bwd_dW": nv * Db + S * nv * hb + B * V * H * 4.0 + (B - 1) * V * H * 4.0,
+    }
+
+
 def whole_job_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
     """Tokens/s of the whole job: every rank's rows over the slowest rank's step time."""
     return world * rows_per_rank / (ms_per_step / 1e3)
@@ -494,11 +516,24 @@ def gpu_arm(args):
                                                          and not args.fused
                                                          and tf is None and not args.forward_only
                                                          ) else None
+    launch_s = kern[dom]["ms_per_step"] / launches_dom / 1e3
+    bytes_launch = None
+    if not (Ht or args.fused or args.forward_only or args.e4m3):
+        bytes_launch = algorithmic_bytes_step(N, nv, H, V, chunk_rows, nv)[dom] / launches_dom
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                 "peak_source": f"{peaks['source']}: {peak_note}",
                 "flops_per_launch": flops_step[dom] / launches_dom,
-                "launch_ms": kern[dom]["ms_per_step"] / launches_dom}
+                "algorithmic_bytes_per_launch": bytes_launch,
+                "launch_ms": launch_s * 1e3}
+    if bytes_launch is not None and bytes_launch / (peaks["hbm_gbs"] * 1e9) > \
+            flops_step[dom] / launches_dom / (peak_tf * 1e12):
+        # the kernel's bytes take longer at the copy bandwidth than its FLOPs
+        # at the tensor rate: HBM-bound (e.g. the fp32 dW write at 256 rows)
+        gbs = bytes_launch / launch_s / 1e9
+        roofline.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "peak_source": f"{peaks['source']}: measured hbm_gbs (copy bandwidth)"})
     step_tflops = sum(flops_step.values()) / (ms_step / 1e3) / 1e12
     gpu_launches = int(round(sum(n for _, n in prof.values())))
 
