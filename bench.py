@@ -534,7 +534,12 @@ def gpu_arm(args):
         roofline.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"],
                          "peak_source": f"{peaks['source']}: measured hbm_gbs (copy bandwidth)"})
-    step_tflops = sum(flops_step.values()) / (ms_step / 1e3) / 1e12
+    # the metric counts 8 N V H per step (forward, recompute, dH, dW over every
+    # row); the GEMMs execute the FLOPs of flops_step (non-ignored rows)
+    exec_tflops = sum(flops_step.values()) / (ms_step / 1e3) / 1e12
+    step_tflops = exec_tflops
+    if not (Ht or args.forward_only or args.fused):
+        step_tflops = 8.0 * N * V * H / (ms_step / 1e3) / 1e12
     gpu_launches = int(round(sum(n for _, n in prof.values())))
 
     if rank == 0:
@@ -559,6 +564,7 @@ def gpu_arm(args):
                        f"{V * H * 2 / 1e9:.2f} GB > 129 MB); no flush",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "tflops": step_tflops,
+            "tflops_executed": exec_tflops,
             "tensor_frac_of_peak": {"measured_burst": step_tflops / peaks["bf16_tflops"],
                                     "measured_sustained": step_tflops / peak_tf,
                                     "nominal_2250": step_tflops / 2250.0},
