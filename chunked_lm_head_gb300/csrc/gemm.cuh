@@ -46,7 +46,6 @@ constexpr int BK = 64;   // one 128-byte swizzle row of bf16 per stage
 constexpr int UMMA_K = 16;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) swizzled box
 constexpr int EPI_WARPS = 4;
-constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 // dW epilogue staging: per epilogue warp two 32x32 fp32 boxes (128B-swizzled)
 // handed to TMA store / reduce-add.
@@ -101,6 +100,12 @@ template <int MODE>
 __host__ __device__ constexpr bool is_split_fwd() {
   return MODE == MODE_FWD || MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD || MODE == MODE_FUSED_FWD;
 }
+
+// Threads of a GEMM CTA with `ew` epilogue warps: 4, one per TMEM lane
+// quarter; or 8 (the dW mode at short K), two per quarter, each on half of
+// the tile's columns, so that the fp32 output epilogue keeps up with MMAs
+// over only a few K blocks.
+__host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 
 // bit 0 of the device error word: a bounded wait ran out.
 constexpr int DEVERR_TIMEOUT = 1;
@@ -381,8 +386,8 @@ __device__ __forceinline__ void stage_bf16_half(uint32_t box, int lane, int half
                      pk[4 * g + 2], pk[4 * g + 3]);
 }
 
-template <int MODE, bool kLong, int CG, bool kF8 = false>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+template <int MODE, bool kLong, int CG, bool kF8 = false, int EW = EPI_WARPS>
+__global__ void __launch_bounds__(gemm_threads(EW), 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
                      const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ GemmParams p) {
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), EPI_WARPS * CG);
+      mbar_init(tempty_bar(b), EW * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -545,6 +550,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // accumulator row owned by this thread
+    // columns of the tile this warp takes: all, or one half (8 epilogue warps)
+    static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && MODE == MODE_DW), "8 epilogue warps: dW only");
+    constexpr int kColParts = EW / 4;
+    constexpr int kChunks = BN / 32 / kColParts;
+    const int c_lo = ((warp - 2) / 4) * kChunks;
+    // TMA staging boxes of this warp (the staging area holds 8 boxes)
+    constexpr int kBoxes = 2 * EPI_WARPS / EW;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t tempty_target0 = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     const uint32_t tempty_target1 = CG == 2 ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
@@ -624,7 +636,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_after();
         const uint32_t tbase = tmem_base + lane_addr + acc * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = c_lo; c < c_lo + kChunks; ++c) {
           float v[32];
           if (t.kb1 > t.kb0) {
             tmem_ld32(tbase + c * 32, v);
@@ -938,8 +950,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // the first pass over the output, an fp32 reduce-add in L2
             // afterwards.  Columns past H and dW rows past V are clipped by
             // TMA; boxes wholly outside the output are skipped.
-            const uint32_t box = out_stage + (warp - 2) * (2 * OUT_BOX_BYTES) + (c & 1) * OUT_BOX_BYTES;
-            if (lane == 0) bulk_wait_read<1>();  // the copy that last used this box has read it
+            const uint32_t box = out_stage + (warp - 2) * (kBoxes * OUT_BOX_BYTES) + (c % kBoxes) * OUT_BOX_BYTES;
+            if (lane == 0) bulk_wait_read<kBoxes - 1>();  // the copy that last used this box has read it
             __syncwarp();
             const uint32_t row_addr = box + lane * 128;
 #pragma unroll

@@ -72,10 +72,11 @@ bool pdl_env() {
 
 // Launch on `grid` CTAs in clusters of `cluster` with the GEMMs' attributes.
 template <class Kern, class... Args>
-cudaError_t launch_persistent(Kern k, int grid, int cluster, int smem, cudaStream_t st, Args... args) {
+cudaError_t launch_persistent(Kern k, int grid, int cluster, int threads, int smem, cudaStream_t st,
+                              Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -99,16 +100,22 @@ cudaError_t launch_persistent(Kern k, int grid, int cluster, int smem, cudaStrea
   return cudaGetLastError();
 }
 
-template <int MODE, bool kLong, int CG>
+template <int MODE, bool kLong, int CG, int EW = EPI_WARPS>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p,
                           int workers, cudaStream_t st) {
-  auto k = flce_gemm_kernel<MODE, kLong, CG>;
+  auto k = flce_gemm_kernel<MODE, kLong, CG, false, EW>;
   constexpr int smem = TileCfg<CG>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_persistent(k, CG * workers, CG, smem, st, a, b, c, a2, b2, p);
+  return launch_persistent(k, CG * workers, CG, gemm_threads(EW), smem, st, a, b, c, a2, b2, p);
 }
+
+// dW over at most this many K blocks (64 rows each) runs 8 epilogue warps:
+// at 256 rows (4 blocks) its output epilogue, not the MMAs, set the pace
+// (8 warps: 410 us against 443 us for the 248,320 x 2,048 fp32 gradient); at
+// 4,096 rows 4 warps were 1-2 % faster
+constexpr int kDwWideEpilogueMaxKBlocks = 16;
 
 // `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
 // tile loop.  `c` is the output map of the modes that write through TMA (dW);
@@ -120,6 +127,16 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
   // a2 / b2: the teacher's operands of the distillation modes (else unused)
   const CUtensorMap& A2 = a2 ? *a2 : a;
   const CUtensorMap& B2 = b2 ? *b2 : b;
+  if constexpr (MODE == MODE_DW) {
+    if (p.k_blocks <= kDwWideEpilogueMaxKBlocks) {
+      constexpr int EW = 2 * EPI_WARPS;
+      if (cg == 2)
+        return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, p, workers, st)
+                     : launch_gemm_t<MODE, false, 2, EW>(a, b, c, A2, B2, p, workers, st);
+      return kLong ? launch_gemm_t<MODE, true, 1, EW>(a, b, c, A2, B2, p, workers, st)
+                   : launch_gemm_t<MODE, false, 1, EW>(a, b, c, A2, B2, p, workers, st);
+    }
+  }
   if (cg == 2)
     return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, A2, B2, p, workers, st)
                  : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, p, workers, st);
@@ -133,7 +150,8 @@ cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUte
   auto go = [&](auto kern, int smem, int grid_mult) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_persistent(kern, grid_mult * workers, grid_mult, smem, st, a, b, b, a, b, p);
+    return launch_persistent(kern, grid_mult * workers, grid_mult, gemm_threads(EPI_WARPS), smem, st, a, b, b,
+                             a, b, p);
   };
   if (cg == 2)
     return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)
@@ -163,7 +181,7 @@ int device_workers(int cg) {
   auto k = flce_gemm_kernel<MODE_FWD, false, 2>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.blockDim = dim3(gemm_threads(EPI_WARPS), 1, 1);
   cfg.dynamicSmemBytes = TileCfg<2>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
