@@ -173,3 +173,45 @@ def test_e4m3_forward_graph_replay_matches_eager():
         return a | b
 
     _capture_and_compare(step, bufs)
+
+
+def test_row_skipping_forward_graph_replay_matches_eager():
+    """flce_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED (rows listed and
+    gathered on the device) and the backward from its lse, captured."""
+    wl = WL.custom("gskip", 2600, 256, 3000, 512, w_std=0.05, targets="zipf", grpo_seqs=4, prompt_len=200,
+                   seed=806)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    N, H, V, cr = wl.N, wl.H, wl.V, 512
+    ws_bytes = _lib.flce_workspace_bytes(N, H, V, cr)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    bufs = dict(logp=torch.empty(N, device="cuda"), lse=torch.empty(N, device="cuda"),
+                loss=torch.empty(1, device="cuda"), nv=torch.empty(1, dtype=torch.int64, device="cuda"),
+                dH=torch.empty_like(h), dW=torch.empty((V, H), device="cuda"))
+
+    def step():
+        a = _lib.flce_forward_ex2(h, W, t, w, N, H, V, cr, -100, None, _lib.FORWARD_SKIP_IGNORED, bufs["logp"],
+                                  bufs["lse"], bufs["loss"], bufs["nv"], ws, ws_bytes)
+        b = _lib.flce_backward(h, W, t, w, bufs["lse"], 1.0 / (N - 4 * 200), bufs["dH"], bufs["dW"], N, H, V, cr,
+                               -100, ws, ws_bytes)
+        return a | b
+
+    # lse of the ignored rows is NaN in both runs: compare with NaNs equal
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        assert step() == 0
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in bufs.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        assert step() == 0
+    for v in bufs.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for k in bufs:
+        assert torch.equal(torch.nan_to_num(bufs[k], nan=-7.0), torch.nan_to_num(eager[k], nan=-7.0)), k
+    assert int(torch.isnan(bufs["lse"]).sum()) == 4 * 200
+    assert _lib.flce_device_status() == 0
