@@ -163,6 +163,13 @@ def test_fused_without_lse_skips_the_ignored_rows_forward():
     logp1, _, loss1, _, dH1, dW1 = run_fused(h, W, t, w, 2048)
     assert torch.allclose(logp, logp1, atol=2e-5, rtol=0) and float(loss.item()) == pytest.approx(loss1, rel=1e-6)
     assert rel_fro(np64(dH), np64(dH1)) <= 1e-3 and rel_fro(np64(dW), np64(dW1)) <= 1e-3
+    # every row ignored: no forward rows at all, zero loss and gradients
+    t.fill_(-100)
+    assert _lib.flce_forward_backward(h, W, t, w, N, H, V, 2048, -100, None, 1.0, logp, None, loss, nv,
+                                      dH, dW) == 0
+    assert _lib.flce_device_status() == 0
+    assert int(nv.item()) == 0 and float(loss.item()) == 0.0 and float(logp.abs().max()) == 0.0
+    assert float(dH.float().abs().max()) == 0.0 and float(dW.abs().max()) == 0.0
 
 
 @pytest.mark.slow
