@@ -327,3 +327,53 @@ def kd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, grad_scale: float, targets=Non
                                workspace, ws_bytes, stream)
     _lib.check("flce_kd_backward", st)
     return dH, dW
+
+
+class DistillLoss(torch.autograd.Function):
+    """Distillation loss of a student head against a frozen teacher head:
+    KL(p_teacher || p_student) (beta None) or the generalised Jensen-Shannon
+    divergence with mixture weight beta, masked by ignored targets (all rows
+    when targets is None), weighted and averaged over the counted rows.  The
+    gradients go to h_s and W_s; the backward recomputes both heads' logits."""
+
+    @staticmethod
+    def forward(ctx, h_s, W_s, h_t, W_t, targets, weights, beta, chunk_rows, ignore_index, transform=None):
+        if beta is None:
+            out = kd_forward(h_s, W_s, h_t, W_t, targets, weights, chunk_rows, ignore_index, transform)
+            kl_sm = torch.empty(0, device=h_s.device)
+        else:
+            out = jsd_forward(h_s, W_s, h_t, W_t, beta, targets, weights, chunk_rows, ignore_index,
+                              transform)
+            kl_sm = out["kl_sm"]
+        empty = torch.empty(0, device=h_s.device)
+        ctx.save_for_backward(h_s, W_s, h_t, W_t, targets if targets is not None else empty,
+                              weights if weights is not None else empty, out["lse_s"], out["lse_t"], kl_sm,
+                              out["n_valid"])
+        ctx.has_targets, ctx.has_weights = targets is not None, weights is not None
+        ctx.beta, ctx.chunk_rows, ctx.ignore_index, ctx.transform = beta, chunk_rows, ignore_index, transform
+        return out["loss"]
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        h_s, W_s, h_t, W_t, targets, weights, lse_s, lse_t, kl_sm, n_valid = ctx.saved_tensors
+        targets = targets if ctx.has_targets else None
+        weights = weights if ctx.has_weights else None
+        n = int(n_valid.item())
+        g = float(grad_loss.item()) / n if n > 0 else 0.0
+        need = dict(need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1])
+        if ctx.beta is None:
+            dH, dW = kd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, g, targets, weights, ctx.chunk_rows,
+                                 ctx.ignore_index, ctx.transform, **need)
+        else:
+            dH, dW = jsd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, kl_sm, g, ctx.beta, targets, weights,
+                                  ctx.chunk_rows, ctx.ignore_index, ctx.transform, **need)
+        return dH, dW, None, None, None, None, None, None, None, None
+
+
+def distill_loss(h_s, W_s, h_t, W_t, targets=None, weights=None, beta: float | None = None,
+                 chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX, transform=None):
+    """Autograd distillation loss (DistillLoss): KL(p_teacher || p_student)
+    with beta None, else the Jensen-Shannon divergence with mixture weight
+    beta in (0, 1).  Returns the scalar loss; h_s and W_s receive gradients."""
+    return DistillLoss.apply(h_s, W_s, h_t, W_t, targets, weights, beta, chunk_rows, ignore_index, transform)
+

@@ -57,3 +57,35 @@ def test_extra_memory_is_the_chunk_workspace():
     extra = torch.cuda.max_memory_allocated() - base
     assert extra <= ws_bytes + outputs + (4 << 20), (extra, ws_bytes, outputs)
     assert flce._lib.flce_device_status() == 0
+
+
+@pytest.mark.parametrize("beta", [None, 0.3])
+def test_distill_loss_autograd_matches_oracle(beta):
+    """distill_loss (KL, or Jensen-Shannon at beta 0.3) through autograd:
+    loss and the student's gradients against the oracle, with a mask, weights,
+    a temperature and an upstream gradient of 2."""
+    from gpu_util import to_dev_bf16
+    si = WL.make_inputs(WL.custom("dl_s", 300, 192, 2100, 128, w_std=0.05, seed=421))
+    ti = WL.make_inputs(WL.custom("dl_t", 300, 256, 2100, 128, w_std=0.065, seed=422))
+    targets = np.random.default_rng(3).integers(0, 2100, 300).astype(np.int64)
+    targets[np.random.default_rng(4).permutation(300)[:30]] = WL.IGNORE_INDEX
+    weights = np.random.default_rng(5).uniform(0.3, 1.7, 300).astype(np.float32)
+    tfd = {"temperature": 2.0}
+    tf = O.LogitTransform(**tfd)
+    hs, Ws, ht, Wt = (to_dev_bf16(x) for x in (si.h, si.W, ti.h, ti.W))
+    hs.requires_grad_(True)
+    Ws.requires_grad_(True)
+    tg = torch.from_numpy(targets).cuda()
+    w = torch.from_numpy(weights).cuda()
+    loss = flce.distill_loss(hs, Ws, ht, Wt, tg, w, beta=beta, chunk_rows=128, transform=tfd)
+    (2.0 * loss).backward()
+    if beta is None:
+        ref = O.kd_forward(si.h, si.W, ti.h, ti.W, targets, weights, tf=tf)
+        refb = O.kd_backward(si.h, si.W, ti.h, ti.W, targets, weights, g=2.0 / ref.n_valid, tf=tf)
+    else:
+        ref = O.jsd_forward(si.h, si.W, ti.h, ti.W, beta, targets, weights, tf=tf)
+        refb = O.jsd_backward(si.h, si.W, ti.h, ti.W, beta, targets, weights, g=2.0 / ref.n_valid, tf=tf)
+    assert float(loss.detach()) == pytest.approx(ref.loss, rel=LOSS_RTOL, abs=1e-6)
+    assert_grad_close(np64(hs.grad), refb.dH, "dH_s")
+    assert_grad_close(np64(Ws.grad), refb.dW, "dW_s")
+    assert ht.grad is None and Wt.grad is None
