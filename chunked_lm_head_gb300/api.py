@@ -170,6 +170,38 @@ def linear_cross_entropy(h, W, targets, weights=None, chunk_rows: int = 256,
     return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index, transform)
 
 
+class SelectiveLogSoftmax(torch.autograd.Function):
+    """Per-token log-probabilities of the targets, log softmax(f(h W^T))[i, t_i]
+    (0 on ignored rows), differentiable in h and W for any downstream use: the
+    chunked selective log-softmax of the Unsloth GRPO page ("Flattened
+    sequence-length chunking").  The backward is the weighted backward with
+    w_i = -dL/dlogp_i and g = 1, recomputing the logits."""
+
+    @staticmethod
+    def forward(ctx, h, W, targets, chunk_rows, ignore_index, transform=None):
+        # the backward reads lse of the non-ignored rows only
+        out = forward(h, W, targets, None, chunk_rows, ignore_index, transform=transform, skip_ignored=True)
+        ctx.save_for_backward(h, W, targets, out["lse"])
+        ctx.chunk_rows, ctx.ignore_index, ctx.transform = chunk_rows, ignore_index, transform
+        return out["logp"]
+
+    @staticmethod
+    def backward(ctx, grad_logp):
+        h, W, targets, lse = ctx.saved_tensors
+        w = (-grad_logp).to(torch.float32).contiguous()
+        dH, dW = backward(h, W, targets, w, lse, 1.0, ctx.chunk_rows, ctx.ignore_index,
+                          need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
+                          transform=ctx.transform)
+        return dH, dW, None, None, None, None
+
+
+def selective_log_softmax(h, W, targets, chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX,
+                          transform=None):
+    """logp[N] fp32 of each row's target (0 on ignored rows), differentiable in
+    h and W (SelectiveLogSoftmax)."""
+    return SelectiveLogSoftmax.apply(h, W, targets, chunk_rows, ignore_index, transform)
+
+
 def _f32_vec(x, N, name):
     if x is None:
         return None

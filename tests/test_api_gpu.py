@@ -89,3 +89,23 @@ def test_distill_loss_autograd_matches_oracle(beta):
     assert_grad_close(np64(hs.grad), refb.dH, "dH_s")
     assert_grad_close(np64(Ws.grad), refb.dW, "dW_s")
     assert ht.grad is None and Wt.grad is None
+
+
+@pytest.mark.parametrize("transform", [None, {"softcap": 10.0, "temperature": 0.7}])
+def test_selective_log_softmax_autograd_matches_oracle(transform):
+    """logp through autograd with an arbitrary upstream gradient u:
+    d(sum u logp) / d(h, W) is the oracle's weighted backward with w = -u, g = 1."""
+    wl = WL.custom("sls", 700, 256, 3000, 128, w_std=0.05, targets="zipf", ignore_frac=0.1, seed=431)
+    inp = WL.make_inputs(wl)
+    h, W, t, _ = upload(inp)
+    h.requires_grad_(True)
+    W.requires_grad_(True)
+    logp = flce.selective_log_softmax(h, W, t, chunk_rows=128, transform=transform)
+    u = np.random.default_rng(9).normal(size=wl.N).astype(np.float32)
+    (logp * torch.from_numpy(u).cuda()).sum().backward()
+    tf = None if transform is None else O.LogitTransform(**transform)
+    ref = O.forward(inp.h, inp.W, inp.targets, None, tf=tf)
+    refb = O.backward(inp.h, inp.W, inp.targets, -u, g=1.0, tf=tf)
+    assert_logp_close(np64(logp), ref.logp, "logp")
+    assert_grad_close(np64(h.grad), refb.dH, "dH")
+    assert_grad_close(np64(W.grad), refb.dW, "dW")
