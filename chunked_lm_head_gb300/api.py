@@ -196,9 +196,16 @@ class SelectiveLogSoftmax(torch.autograd.Function):
 
 
 def selective_log_softmax(h, W, targets, chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX,
-                          transform=None):
+                          transform=None, logit_scale_multiply: float = 0.0, logit_scale_divide: float = 0.0,
+                          logit_softcapping: float = 0.0, temperature: float = 1.0):
     """logp[N] fp32 of each row's target (0 on ignored rows), differentiable in
-    h and W (SelectiveLogSoftmax)."""
+    h and W (SelectiveLogSoftmax).  The logit transform is `transform` (a
+    dict or LogitTransform), or the four keyword arguments of the Unsloth
+    page's chunked selective log-softmax (0 disables the first three)."""
+    if transform is None and (logit_scale_multiply or logit_scale_divide or logit_softcapping
+                              or temperature != 1.0):
+        transform = {"scale_multiply": logit_scale_multiply, "scale_divide": logit_scale_divide,
+                     "softcap": logit_softcapping, "temperature": temperature}
     return SelectiveLogSoftmax.apply(h, W, targets, chunk_rows, ignore_index, transform)
 
 

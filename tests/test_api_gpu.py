@@ -109,3 +109,8 @@ def test_selective_log_softmax_autograd_matches_oracle(transform):
     assert_logp_close(np64(logp), ref.logp, "logp")
     assert_grad_close(np64(h.grad), refb.dH, "dH")
     assert_grad_close(np64(W.grad), refb.dW, "dW")
+    if transform is not None:  # the same transform through the page's keyword names
+        logp2 = flce.selective_log_softmax(h.detach(), W.detach(), t, chunk_rows=128,
+                                           logit_softcapping=transform["softcap"],
+                                           temperature=transform["temperature"])
+        assert torch.equal(logp2, logp.detach())
