@@ -170,6 +170,22 @@ def linear_cross_entropy(h, W, targets, weights=None, chunk_rows: int = 256,
     return LinearCrossEntropy.apply(h, W, targets, weights, chunk_rows, ignore_index, transform)
 
 
+class LinearCrossEntropyLoss(torch.nn.Module):
+    """Module form of linear_cross_entropy: forward(h, W, targets, weights=None)
+    returns the masked (weighted) mean NLL of the LM head."""
+
+    def __init__(self, chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX, transform=None,
+                 recompute: bool = True):
+        super().__init__()
+        self.chunk_rows, self.ignore_index = chunk_rows, ignore_index
+        self.transform, self.recompute = transform, recompute
+
+    def forward(self, h, W, targets, weights=None):
+        loss, _, _ = linear_cross_entropy(h, W, targets, weights, self.chunk_rows, self.ignore_index,
+                                          self.transform, self.recompute)
+        return loss
+
+
 class SelectiveLogSoftmax(torch.autograd.Function):
     """Per-token log-probabilities of the targets, log softmax(f(h W^T))[i, t_i]
     (0 on ignored rows), differentiable in h and W for any downstream use: the

@@ -114,3 +114,20 @@ def test_selective_log_softmax_autograd_matches_oracle(transform):
                                            logit_softcapping=transform["softcap"],
                                            temperature=transform["temperature"])
         assert torch.equal(logp2, logp.detach())
+
+
+def test_loss_module_matches_the_function():
+    wl = WL.custom("mod", 500, 256, 2500, 128, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=441)
+    inp = WL.make_inputs(wl)
+    h, W, t, _ = upload(inp)
+    grads = []
+    for use_module in (True, False):
+        hh, WW = h.clone().requires_grad_(True), W.clone().requires_grad_(True)
+        if use_module:
+            loss = flce.LinearCrossEntropyLoss(chunk_rows=128)(hh, WW, t)
+        else:
+            loss = flce.linear_cross_entropy(hh, WW, t, None, 128)[0]
+        loss.backward()
+        grads.append((float(loss.detach()), hh.grad, WW.grad))
+    assert grads[0][0] == grads[1][0]
+    assert torch.equal(grads[0][1], grads[1][1]) and torch.equal(grads[0][2], grads[1][2])
