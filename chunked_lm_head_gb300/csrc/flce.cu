@@ -742,7 +742,9 @@ flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, const uin
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  const FwdPlan f = plan_forward(N, H, V, workers, BM * cg);
+  // launches of one raster group of rows each (as the bf16 forward)
+  const long long fb = fwd_block_rows(N, BM * cg);
+  const FwdPlan f = plan_forward_call(N, H, V, workers, BM * cg);
   const FwdLayout L = fwd_layout(N, f);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
@@ -795,9 +797,16 @@ flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, const uin
     p.tf_d = tfp.tf_d;
     const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
                        static_cast<long long>(f.S) * N >= INT_MAX;
-    {
+    for (long long row0 = 0; row0 < N; row0 += fb) {
+      GemmParams q = p;
+      q.row0 = static_cast<int>(row0);
+      q.rows = static_cast<int>(std::min(fb, N - row0));
+      q.rows_cap = q.rows;
+      q.m_tiles = static_cast<int>(ceil_div(q.rows, BM * cg));
+      q.num_units = q.m_tiles * f.S;
+      q.group_m = std::min(16, q.m_tiles);
       ProfScope ps(K_FWD, st);
-      FLCE_CUDA_TRY(launch_fwd_e4m3(cg, kLong, tA, tB, p, f.grid, st));
+      FLCE_CUDA_TRY(launch_fwd_e4m3(cg, kLong, tA, tB, q, std::min(q.num_units, workers), st));
     }
     return ce_forward_tail(kLong, f, Ni, part, zt, targets, weights, ignore_index, out_logp, out_lse,
                            out_loss, out_n_valid, bsum, bcnt, st);
@@ -809,7 +818,7 @@ size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, i
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return 0;
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  const JsdFwdLayout fl = jsd_fwd_layout(N, plan_forward(N, H_s + H_t, V, workers, BM * cg));
+  const JsdFwdLayout fl = jsd_fwd_layout(N, plan_forward_call(N, H_s + H_t, V, workers, BM * cg));
   const BwdLayout bl = bwd_layout(N, H_s, plan_backward(N, H_s, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
@@ -844,7 +853,9 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
   const int workers = device_workers(cg);
   const int kbs = static_cast<int>(ceil_div(H_s, BK));
   const int kbt = static_cast<int>(ceil_div(H_t, BK));
-  const FwdPlan f = plan_forward(N, H_s + H_t, V, workers, BM * cg);
+  // launches of one raster group of rows each (as the cross-entropy forward)
+  const long long fb = fwd_block_rows(N, BM * cg);
+  const FwdPlan f = plan_forward_call(N, H_s + H_t, V, workers, BM * cg);
   const JsdFwdLayout J = jsd_fwd_layout(N, f);
   const KdFwdLayout& L = J.kd;
   Workspace ws;
@@ -900,9 +911,23 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
     p.tf_d = tfp.tf_d;
     const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
                        static_cast<long long>(f.S) * N >= INT_MAX;
-    {
+    // one launch per block of fb rows: every unit of a launch shares its
+    // rows' h tiles, and the 16 row tiles of a block share each W tile in L2
+    auto block_params = [&](const GemmParams& base, long long row0) {
+      GemmParams q = base;
+      q.row0 = static_cast<int>(row0);
+      q.rows = static_cast<int>(std::min(fb, N - row0));
+      q.rows_cap = q.rows;
+      q.m_tiles = static_cast<int>(ceil_div(q.rows, BM * cg));
+      q.num_units = q.m_tiles * f.S;
+      q.group_m = std::min(16, q.m_tiles);
+      return q;
+    };
+    for (long long row0 = 0; row0 < N; row0 += fb) {
+      const GemmParams q = block_params(p, row0);
       ProfScope prof(K_KD_FWD, st);
-      FLCE_CUDA_TRY(launch_gemm<MODE_KD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, p, f.grid, st, &ht_k, &Wt_k));
+      FLCE_CUDA_TRY(launch_gemm<MODE_KD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, q, std::min(q.num_units, workers), st,
+                                             &ht_k, &Wt_k));
     }
     {
       ProfScope prof(K_COMBINE, st);
@@ -922,9 +947,11 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       q.lse_t = lse_t;
       q.partials = pj;
       q.jsd_beta = beta;
-      {
+      for (long long row0 = 0; row0 < N; row0 += fb) {
+        const GemmParams qb = block_params(q, row0);
         ProfScope prof(K_JSD_FWD, st);
-        FLCE_CUDA_TRY(launch_gemm<MODE_JSD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, q, f.grid, st, &ht_k, &Wt_k));
+        FLCE_CUDA_TRY(launch_gemm<MODE_JSD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, qb, std::min(qb.num_units, workers),
+                                                st, &ht_k, &Wt_k));
       }
       ProfScope prof(K_COMBINE, st);
       if (kLong)
