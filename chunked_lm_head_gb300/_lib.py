@@ -32,6 +32,11 @@ SIGNATURES = {
     "flce_forward_ex": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
                                        _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                        ctypes.c_size_t, _c_vp]),
+    "flce_grpo_forward_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float,
+                                                  ctypes.c_float, ctypes.c_float, _c_i64, _c_i64, _c_i64,
+                                                  _c_i64, _c_i64, _c_vp, ctypes.c_float, _c_vp, _c_vp,
+                                                  _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
+                                                  _c_vp]),
     "flce_forward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
                                         _c_i64, _c_vp, ctypes.c_uint32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                         ctypes.c_size_t, _c_vp]),
@@ -194,6 +199,20 @@ def flce_forward_ex(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, t
 
 
 FORWARD_SKIP_IGNORED = 1
+
+
+def flce_grpo_forward_backward(h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta, N, H,
+                               V, chunk_rows, ignore_index, transform, grad_scale, out_logp, out_token_loss,
+                               out_loss, out_n_valid, dH, dW, workspace=None, workspace_bytes=0,
+                               stream=None) -> int:
+    """Raw C call of the GRPO loss and gradients in one call."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_grpo_forward_backward(_ptr(h), _ptr(W), _ptr(targets), _ptr(advantages), _ptr(old_logp),
+                                          _ptr(ref_logp), float(eps_low), float(eps_high), float(beta), N, H, V,
+                                          chunk_rows, ignore_index, tp, float(grad_scale), _ptr(out_logp),
+                                          _ptr(out_token_loss), _ptr(out_loss), _ptr(out_n_valid), _ptr(dH),
+                                          _ptr(dW), _ptr(workspace), workspace_bytes, _stream_handle(stream))
 
 
 def flce_forward_ex2(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform, flags,

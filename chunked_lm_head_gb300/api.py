@@ -282,11 +282,56 @@ class GRPOLoss(torch.autograd.Function):
         return dH, dW, None, None, None, None, None, None, None, None, None, None
 
 
+class GRPOLossOneCall(torch.autograd.Function):
+    """The GRPO loss with its gradients computed in the forward call
+    (flce_grpo_forward_backward, no logits recompute); the backward only
+    scales them by the incoming gradient of the loss."""
+
+    @staticmethod
+    def forward(ctx, h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta, chunk_rows,
+                ignore_index, transform=None):
+        _check(h, W, targets, None)
+        N, H = h.shape
+        V = W.shape[0]
+        for x, name in ((advantages, "advantages"), (old_logp, "old_logp"), (ref_logp, "ref_logp")):
+            _f32_vec(x, N, name)
+        dev = h.device
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        loss = torch.empty((), dtype=torch.float32, device=dev)
+        n_valid = torch.empty((), dtype=torch.int64, device=dev)
+        need_dW = ctx.needs_input_grad[1]
+        dH = torch.empty_like(h) if (ctx.needs_input_grad[0] or not need_dW) else None
+        dW = torch.empty((V, H), dtype=torch.float32, device=dev) if need_dW else None
+        st = _lib.flce_grpo_forward_backward(h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high,
+                                             beta, N, H, V, chunk_rows, ignore_index, transform, 1.0, logp,
+                                             None, loss, n_valid, dH, dW)
+        _lib.check("flce_grpo_forward_backward", st)
+        ctx.grads = (dH if ctx.needs_input_grad[0] else None, dW)
+        ctx.mark_non_differentiable(logp)
+        return loss, logp
+
+    @staticmethod
+    def backward(ctx, grad_loss, grad_logp):
+        dH, dW = ctx.grads
+        ctx.grads = None
+        s = float(grad_loss.item())
+        if s != 1.0:
+            dH = None if dH is None else dH * s
+            dW = None if dW is None else dW * s
+        return dH, dW, None, None, None, None, None, None, None, None, None, None
+
+
 def grpo_loss(h, W, targets, advantages, old_logp=None, ref_logp=None, eps_low: float = 0.2,
               eps_high: float = 0.2, beta: float = 0.0, chunk_rows: int = 256,
-              ignore_index: int = IGNORE_INDEX, transform=None):
+              ignore_index: int = IGNORE_INDEX, transform=None, recompute: bool = True):
     """Differentiable GRPO loss of softmax(f(h W^T)) on the target tokens;
-    returns (loss, logp).  advantages, old_logp, ref_logp: float32 [N]."""
+    returns (loss, logp).  advantages, old_logp, ref_logp: float32 [N].
+    recompute=False computes the gradients in the forward call without the
+    logits recompute (flce_grpo_forward_backward; faster when chunk_rows >=
+    2,048)."""
+    if not recompute:
+        return GRPOLossOneCall.apply(h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta,
+                                     chunk_rows, ignore_index, transform)
     return GRPOLoss.apply(h, W, targets, advantages, old_logp, ref_logp, eps_low, eps_high, beta,
                           chunk_rows, ignore_index, transform)
 

@@ -450,12 +450,39 @@ flce_status flce_backward(const flce_bf16* h, const flce_bf16* W, const int64_t*
 
 // Workspace of the fallback (forward, then the tiled backward with the count
 // on the device): the larger of the two, plus lse and n_valid scratch.
-static size_t fallback_workspace(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int workers,
-                                 int tm) {
+struct FallbackLayout {
+  size_t inner = 0, lse = 0, nv = 0, lp = 0, wg = 0, gsum = 0, gcnt = 0, total = 0;
+};
+static FallbackLayout fallback_layout(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int workers,
+                                      int tm) {
+  FallbackLayout L;
   const size_t fwd = fwd_layout(N, plan_forward_call(N, H, V, workers, tm)).total;
   const size_t bwd = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, tm)).total;
-  return std::max(fwd, bwd) + align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4) + 256;
+  const size_t n4 = align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4);
+  const size_t nb8 = align256(static_cast<size_t>(ceil_div(std::max<int64_t>(N, 1), SMALL_THREADS)) * 8);
+  L.inner = std::max(fwd, bwd);
+  L.lse = L.inner;
+  L.nv = L.lse + n4;
+  L.lp = L.nv + 256;  // the GRPO call: log-probs, backward weights, loss block sums
+  L.wg = L.lp + n4;
+  L.gsum = L.wg + n4;
+  L.gcnt = L.gsum + nb8;
+  L.total = L.gcnt + nb8;
+  return L;
 }
+static size_t fallback_workspace(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int workers,
+                                 int tm) {
+  return fallback_layout(N, H, V, chunk_rows, workers, tm).total;
+}
+
+// The GRPO objective of flce_grpo_forward_backward (NULL: the cross-entropy).
+struct GrpoArgs {
+  const float* adv;
+  const float* old_logp;
+  const float* ref_logp;
+  float eps_low, eps_high, beta;
+  float* out_token_loss;
+};
 
 size_t flce_forward_backward_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
   if (!sizes_ok(N, H, V)) return 0;
@@ -466,13 +493,13 @@ size_t flce_forward_backward_workspace_bytes(int64_t N, int64_t H, int64_t V, in
   return fallback_workspace(N, H, V, chunk_rows, workers, BM * cg);
 }
 
-flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
-                                  const float* weights, int64_t N, int64_t H, int64_t V,
-                                  int64_t chunk_rows, int64_t ignore_index,
-                                  const flce_logit_transform* transform, float grad_scale,
-                                  float* out_logp, float* out_lse, float* out_loss,
-                                  int64_t* out_n_valid, flce_bf16* dH, float* dW, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+static flce_status forward_backward_impl(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                         const float* weights, int64_t N, int64_t H, int64_t V,
+                                         int64_t chunk_rows, int64_t ignore_index,
+                                         const flce_logit_transform* transform, float grad_scale,
+                                         float* out_logp, float* out_lse, float* out_loss,
+                                         int64_t* out_n_valid, flce_bf16* dH, float* dW, void* workspace,
+                                         size_t workspace_bytes, void* stream, const GrpoArgs* grpo) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
@@ -493,19 +520,48 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
     // forward (lse and n_valid into scratch when the caller wants neither),
     // then the tiled backward with grad_scale / n_valid on the device
     Workspace ws;
-    const size_t need = fallback_workspace(N, H, V, chunk_rows, workers, tm);
-    flce_status s = get_workspace(ws, workspace, workspace_bytes, need, st);
+    const FallbackLayout FL = fallback_layout(N, H, V, chunk_rows, workers, tm);
+    flce_status s = get_workspace(ws, workspace, workspace_bytes, FL.total, st);
     if (s != FLCE_OK) return s;
     uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
-    const size_t inner = need - align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4) - 256;
-    float* lse = out_lse ? out_lse : reinterpret_cast<float*>(wb + inner);
-    int64_t* nv = out_n_valid ? out_n_valid
-                              : reinterpret_cast<int64_t*>(wb + inner + align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4));
-    s = forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, lse, out_loss, nv,
-                     wb, inner, stream, kFwdPartialsCap);
+    float* lse = out_lse ? out_lse : reinterpret_cast<float*>(wb + FL.lse);
+    int64_t* nv = out_n_valid ? out_n_valid : reinterpret_cast<int64_t*>(wb + FL.nv);
+    if (grpo == nullptr) {
+      s = forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, lse, out_loss, nv,
+                       wb, FL.inner, stream, kFwdPartialsCap);
+      if (s != FLCE_OK) return s;
+      return backward_impl(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows, ignore_index,
+                           transform, wb, FL.inner, stream, reinterpret_cast<const long long*>(nv));
+    }
+    // GRPO: the forward's log-probs give each row's token loss and backward
+    // weight, then the tiled backward runs with those weights
+    float* lp = out_logp ? out_logp : reinterpret_cast<float*>(wb + FL.lp);
+    float* wg = reinterpret_cast<float*>(wb + FL.wg);
+    double* gsum = reinterpret_cast<double*>(wb + FL.gsum);
+    long long* gcnt = reinterpret_cast<long long*>(wb + FL.gcnt);
+    s = forward_impl(h, W, targets, nullptr, N, H, V, ignore_index, transform, lp, lse, nullptr, nv, wb,
+                     FL.inner, stream, kFwdPartialsCap);
     if (s != FLCE_OK) return s;
-    return backward_impl(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows, ignore_index,
-                         transform, wb, inner, stream, reinterpret_cast<const long long*>(nv));
+    if (N > 0) {
+      const int nblk = static_cast<int>(ceil_div(N, SMALL_THREADS));
+      {
+        ProfScope ps(K_GRPO, st);
+        grpo_token_kernel<<<nblk, SMALL_THREADS, 0, st>>>(lp, grpo->old_logp, grpo->ref_logp, grpo->adv, targets,
+                                                         static_cast<int>(N), ignore_index, grpo->eps_low,
+                                                         grpo->eps_high, grpo->beta, grpo->out_token_loss, wg,
+                                                         gsum, gcnt);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
+      if (out_loss) {
+        ProfScope ps(K_FINAL, st);
+        final_kernel<<<1, SMALL_THREADS, 0, st>>>(gsum, gcnt, nblk, out_loss, nullptr);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
+    } else if (out_loss) {
+      FLCE_CUDA_TRY(cudaMemsetAsync(out_loss, 0, sizeof(float), st));
+    }
+    return backward_impl(h, W, targets, N > 0 ? wg : nullptr, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                         ignore_index, transform, wb, FL.inner, stream, reinterpret_cast<const long long*>(nv));
   }
   const FusedLayout L = fused_layout(N, H, fp);
   Workspace ws;
@@ -525,6 +581,10 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
   int* cblk = reinterpret_cast<int*>(wb + L.blk);
   int* ccount = reinterpret_cast<int*>(wb + L.count);
   uint16_t* hc = reinterpret_cast<uint16_t*>(wb + L.hc);
+  // GRPO: the block's log-probs feed its token losses and backward weights
+  float* lp = out_logp ? out_logp : (grpo ? reinterpret_cast<float*>(wb + L.lp) : nullptr);
+  float* wg = reinterpret_cast<float*>(wb + L.wg);
+  const float* dl_weights = grpo ? wg : weights;
   const int Ni = static_cast<int>(N);
   const bool validate = validate_env();
   // Row compaction: the blocks run over a permutation of the rows with the
@@ -657,14 +717,23 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
       if (kLong)
         combine_kernel<true><<<nb, SMALL_THREADS, 0, st>>>(part + off, fp.f.S, Ni, rows, zt + off, targets + off,
                                                            weights ? weights + off : nullptr, ignore_index,
-                                                           out_logp ? out_logp + off : nullptr, lse + off,
+                                                           lp ? lp + off : nullptr, lse + off,
                                                            bsum + b0, bcnt + b0, ri);
       else
         combine_kernel<false><<<nb, SMALL_THREADS, 0, st>>>(part + off, fp.f.S, Ni, rows, zt + off, targets + off,
                                                             weights ? weights + off : nullptr, ignore_index,
-                                                            out_logp ? out_logp + off : nullptr, lse + off,
+                                                            lp ? lp + off : nullptr, lse + off,
                                                             bsum + b0, bcnt + b0, ri);
       FLCE_CUDA_TRY(cudaGetLastError());
+      if (grpo) {  // token losses and weights of the block's rows; its loss sums replace the NLL's
+        ProfScope pg(K_GRPO, st);
+        auto at = [&](const float* a) { return a ? a + off : nullptr; };
+        grpo_token_kernel<<<nb, SMALL_THREADS, 0, st>>>(
+            lp + off, at(grpo->old_logp), at(grpo->ref_logp), grpo->adv + off, targets + off, rows, ignore_index,
+            grpo->eps_low, grpo->eps_high, grpo->beta, grpo->out_token_loss ? grpo->out_token_loss + off : nullptr,
+            wg + off, bsum + b0, bcnt + b0, ri);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
     }
     {  // (3) exponentials -> dlogits, in place
       ProfScope ps(K_DLOGITS, st);
@@ -673,12 +742,12 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
       const int* ri = compact ? cidx + row0 : nullptr;
       if (kLong)
         fused_dlogits_kernel<true><<<grid, SMALL_THREADS, 0, st>>>(
-            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), ri, targets, weights,
-            lse, zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
+            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), ri, targets,
+            dl_weights, lse, zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
       else
         fused_dlogits_kernel<false><<<grid, SMALL_THREADS, 0, st>>>(
-            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), ri, targets, weights,
-            lse, zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
+            E, mx, static_cast<int>(fp.ldD), static_cast<int>(V), static_cast<int>(row0), ri, targets,
+            dl_weights, lse, zt, ignore_index, ccount, grad_scale, tfp.tf_softcap, tfp.tf_a, tfp.tf_b, tfp.tf_d);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
     // (4) dH[rows] = D W, dW (+)= D^T h[rows]; compacted: the block's
@@ -703,6 +772,38 @@ flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const 
     FLCE_CUDA_TRY(cudaGetLastError());
   }
   return FLCE_OK;
+}
+
+flce_status flce_forward_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                  const float* weights, int64_t N, int64_t H, int64_t V,
+                                  int64_t chunk_rows, int64_t ignore_index,
+                                  const flce_logit_transform* transform, float grad_scale,
+                                  float* out_logp, float* out_lse, float* out_loss,
+                                  int64_t* out_n_valid, flce_bf16* dH, float* dW, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return forward_backward_impl(h, W, targets, weights, N, H, V, chunk_rows, ignore_index, transform, grad_scale,
+                               out_logp, out_lse, out_loss, out_n_valid, dH, dW, workspace, workspace_bytes,
+                               stream, nullptr);
+}
+
+flce_status flce_grpo_forward_backward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                                       const float* advantages, const float* old_logp,
+                                       const float* ref_logp, float eps_low, float eps_high, float beta,
+                                       int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                                       int64_t ignore_index, const flce_logit_transform* transform,
+                                       float grad_scale, float* out_logp, float* out_token_loss,
+                                       float* out_loss, int64_t* out_n_valid, flce_bf16* dH, float* dW,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!(std::isfinite(eps_low) && std::isfinite(eps_high) && std::isfinite(beta)) || eps_low < 0.f ||
+      eps_low >= 1.f || eps_high < 0.f || beta < 0.f)
+    return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!advantages || (beta > 0.f && !ref_logp))) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(advantages, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(out_token_loss, 4))
+    return FLCE_ERR_UNSUPPORTED;
+  const GrpoArgs g{advantages, old_logp, ref_logp, eps_low, eps_high, beta, out_token_loss};
+  return forward_backward_impl(h, W, targets, nullptr, N, H, V, chunk_rows, ignore_index, transform, grad_scale,
+                               out_logp, nullptr, out_loss, out_n_valid, dH, dW, workspace, workspace_bytes,
+                               stream, &g);
 }
 
 flce_status flce_quantize_e4m3_rows(const flce_bf16* x, int64_t rows, int64_t cols, uint8_t* q,

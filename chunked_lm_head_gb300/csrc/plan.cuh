@@ -405,7 +405,7 @@ FusedPlan plan_fused(long long N, long long H, long long V, long long chunk_rows
 
 struct FusedLayout {
   size_t zt = 0, part = 0, bsum = 0, bcnt = 0, bad = 0, E = 0, mx = 0, lse = 0, dh_part = 0, idx = 0,
-         blk = 0, count = 0, hc = 0, total = 0;
+         blk = 0, count = 0, hc = 0, lp = 0, wg = 0, total = 0;
 };
 FusedLayout fused_layout(long long N, long long H, const FusedPlan& fp) {
   FusedLayout L;
@@ -430,6 +430,8 @@ FusedLayout fused_layout(long long N, long long H, const FusedPlan& fp) {
   L.blk = take(static_cast<size_t>(ceil_div(std::max(1LL, N), COMPACT_ROWS_PER_BLOCK)) * 4);
   L.count = take(256);
   L.hc = take(static_cast<size_t>(fp.R) * H * 2);  // the block's rows of h (row compaction)
+  L.lp = take(static_cast<size_t>(N) * 4);          // GRPO: log-probs and backward weights
+  L.wg = take(static_cast<size_t>(N) * 4);
   L.total = o;
   return L;
 }

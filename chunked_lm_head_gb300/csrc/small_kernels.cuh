@@ -359,17 +359,21 @@ __global__ void jsd_combine_kernel(const float2* __restrict__ pj, int S, int N,
 // GRPO per-token objective on the sampled tokens' log-probs (one thread per
 // row; flce_grpo_token_loss states the formula): the masked token loss, the
 // weights -d(token loss)/d(logp) for the backward, and this block's sums of
-// -(token loss) and of the mask (the final kernel negates the sum).
+// -(token loss) and of the mask (the final kernel negates the sum).  Rows
+// [0, N) of the arrays passed, or with `ri` the rows ri[0..N) of the whole
+// arrays.
 __global__ void grpo_token_kernel(const float* __restrict__ logp, const float* __restrict__ old_logp,
                                   const float* __restrict__ ref_logp, const float* __restrict__ adv,
                                   const int64_t* __restrict__ targets, int N, long long ignore,
                                   float eps_low, float eps_high, float beta,
                                   float* __restrict__ out_tok, float* __restrict__ out_w,
-                                  double* __restrict__ blk_sum, long long* __restrict__ blk_cnt) {
-  const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
+                                  double* __restrict__ blk_sum, long long* __restrict__ blk_cnt,
+                                  const int* __restrict__ ri = nullptr) {
+  const int j = blockIdx.x * SMALL_THREADS + threadIdx.x;
   double contrib = 0.0;
   long long cnt = 0;
-  if (i < N) {
+  if (j < N) {
+    const int i = ri ? ri[j] : j;  // the j-th row of this range (arrays not offset with ri)
     const bool valid = targets == nullptr || targets[i] != ignore;
     float tok = 0.f, wt = 0.f;
     if (valid) {

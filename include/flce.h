@@ -371,6 +371,35 @@ FLCE_API flce_status flce_grpo_token_loss(const float* logp, const float* old_lo
 /* Workspace bytes of flce_grpo_token_loss for N rows (0 on invalid N). */
 FLCE_API size_t flce_grpo_workspace_bytes(int64_t N);
 
+/*
+ * The GRPO loss of flce_grpo_token_loss and its gradients in one call,
+ * without the backward's logits recompute (an addition of this library, as
+ * flce_forward_backward): per block of rows, the forward GEMM keeps the
+ * exponentials, the block's log-probs give its token losses and backward
+ * weights w = -d(token loss)/d(logp), and the dlogits pass and the dH / dW
+ * GEMMs use those weights.
+ *   loss = sum m * token / sum m  (out_loss [1], or NULL),
+ *   dH, dW = grad_scale * d(loss) / d(h, W),
+ *   out_logp [N] and out_token_loss [N] fp32 or NULL; out_n_valid int64 or NULL.
+ * advantages [N] fp32 (required), old_logp / ref_logp [N] fp32 or NULL, and
+ * eps_low, eps_high, beta as flce_grpo_token_loss (ref_logp required when
+ * beta > 0).  Blocks, row compaction (ignored rows are skipped in every
+ * GEMM: no lse is returned), the fallback for budgets under 2,048 rows and
+ * the workspace (flce_forward_backward_workspace_bytes) are those of
+ * flce_forward_backward.
+ */
+FLCE_API flce_status flce_grpo_forward_backward(const flce_bf16* h, const flce_bf16* W,
+                                                const int64_t* targets, const float* advantages,
+                                                const float* old_logp, const float* ref_logp,
+                                                float eps_low, float eps_high, float beta, int64_t N,
+                                                int64_t H, int64_t V, int64_t chunk_rows,
+                                                int64_t ignore_index,
+                                                const flce_logit_transform* transform,
+                                                float grad_scale, float* out_logp,
+                                                float* out_token_loss, float* out_loss,
+                                                int64_t* out_n_valid, flce_bf16* dH, float* dW,
+                                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of the distillation calls (flce_kd_* and flce_jsd_*) for
  * these sizes. */
 FLCE_API size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V,

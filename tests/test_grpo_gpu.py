@@ -56,10 +56,17 @@ def test_grpo_on_policy_weights_are_the_advantages():
     assert float(out["loss"]) == pytest.approx(-float(A[m].astype(np.float64).sum()) / m.sum(), rel=1e-6)
 
 
+@pytest.mark.parametrize("path", ["recompute", "one_call", "one_call_fallback", "one_call_in_row_order"])
 @pytest.mark.parametrize("transform", [None, {"temperature": 0.8}])
-def test_grpo_loss_through_the_head_matches_oracle(transform):
+def test_grpo_loss_through_the_head_matches_oracle(transform, path, monkeypatch):
     """4 sequences x 150 tokens, 40-token prompts masked, one advantage per
-    sequence; old-policy and reference log-probs near the current ones."""
+    sequence; old-policy and reference log-probs near the current ones.  The
+    recomputing autograd path, and the one-call path (flce_grpo_forward_backward)
+    on one 640-row block (with and without the row permutation) and on the
+    forward + tiled backward of a 128-row budget."""
+    if path == "one_call_in_row_order":
+        monkeypatch.setenv("FLCE_COMPACT", "0")
+    chunk = 1024 if path in ("one_call", "one_call_in_row_order") else 128
     wl = WL.custom("grpo_api", 600, 256, 3000, 128, w_std=0.05, targets="zipf", grpo_seqs=4,
                    prompt_len=40, seed=411)
     inp = WL.make_inputs(wl)
@@ -73,7 +80,7 @@ def test_grpo_loss_through_the_head_matches_oracle(transform):
     h.requires_grad_(True)
     W.requires_grad_(True)
     loss, logp = flce.grpo_loss(h, W, t, _cuda32(A), _cuda32(old), _cuda32(refp), 0.2, 0.28, 0.04,
-                                chunk_rows=128, transform=transform)
+                                chunk_rows=chunk, transform=transform, recompute=path == "recompute")
     (2.0 * loss).backward()
     m = inp.targets != WL.IGNORE_INDEX
     o = O.grpo_token_loss(ref_fwd.logp, A, m, old, refp, 0.2, 0.28, 0.04)
