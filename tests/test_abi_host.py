@@ -29,6 +29,15 @@ def test_forward_ex2_rejects_unknown_flags(lib):
                                  None, stream=0) == 1  # FLCE_ERR_INVALID_ARG
 
 
+def test_grpo_one_call_rejects_bad_objective_arguments(lib):
+    # eps_low outside [0, 1), negative beta, beta > 0 without reference
+    # log-probs: all refused before any device access
+    for eps_low, eps_high, beta in ((1.0, 0.2, 0.0), (0.2, 0.2, -0.1), (0.2, 0.2, 0.5)):
+        assert _lib.flce_grpo_forward_backward(None, None, None, 8, None, None, eps_low, eps_high, beta,
+                                               8, 8, 8, 8, -100, None, 1.0, None, None, None, None, 8, None,
+                                               stream=0) == 1
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert _lib.flce_status_string(code) == name
