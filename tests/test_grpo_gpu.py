@@ -89,3 +89,40 @@ def test_grpo_loss_through_the_head_matches_oracle(transform, path, monkeypatch)
     assert float(loss.detach()) == pytest.approx(o.loss, rel=LOSS_RTOL, abs=1e-6)
     assert_grad_close(np64(h.grad), refb.dH, "dH")
     assert_grad_close(np64(W.grad), refb.dW, "dW")
+
+
+def test_grpo_one_call_on_policy_gradients_equal_the_weighted_cross_entropy():
+    """With no old-policy log-probs (ratio 1) and beta 0, the GRPO weights
+    are the advantages: flce_grpo_forward_backward gives bit for bit the
+    gradients of flce_forward_backward with weights = advantages.  With every
+    row ignored, loss and gradients are zero."""
+    from chunked_lm_head_gb300 import _lib
+    wl = WL.custom("grpo_pol", 2400, 256, 3000, 2048, w_std=0.05, targets="zipf", grpo_seqs=4,
+                   prompt_len=100, seed=412)
+    inp = WL.make_inputs(wl)
+    h, W, t, A = upload(inp)
+    N, H, V = wl.N, wl.H, wl.V
+
+    def bufs():
+        return (torch.empty(N, device="cuda"), torch.empty(1, device="cuda"),
+                torch.empty(1, dtype=torch.int64, device="cuda"), torch.empty_like(h),
+                torch.empty((V, H), device="cuda"))
+
+    lp1, loss1, nv1, dH1, dW1 = bufs()
+    assert _lib.flce_grpo_forward_backward(h, W, t, A, None, None, 0.2, 0.2, 0.0, N, H, V, 2048, -100, None, 1.0,
+                                           lp1, None, loss1, nv1, dH1, dW1) == 0
+    lp2, loss2, nv2, dH2, dW2 = bufs()
+    assert _lib.flce_forward_backward(h, W, t, A, N, H, V, 2048, -100, None, 1.0, lp2, None, loss2, nv2,
+                                      dH2, dW2) == 0
+    assert _lib.flce_device_status() == 0
+    m = inp.targets != WL.IGNORE_INDEX
+    assert int(nv1.item()) == int(nv2.item()) == int(m.sum())
+    assert torch.equal(lp1, lp2) and torch.equal(dH1, dH2) and torch.equal(dW1, dW2)
+    # the GRPO loss is sum(-A) / n here (its value, unlike its gradient, has no logp)
+    assert float(loss1.item()) == pytest.approx(-float(inp.weights[m].astype(np.float64).sum()) / m.sum(),
+                                                rel=1e-5)
+    t.fill_(-100)
+    assert _lib.flce_grpo_forward_backward(h, W, t, A, None, None, 0.2, 0.2, 0.0, N, H, V, 2048, -100, None, 1.0,
+                                           lp1, None, loss1, nv1, dH1, dW1) == 0
+    assert int(nv1.item()) == 0 and float(loss1.item()) == 0.0
+    assert float(dH1.float().abs().max()) == 0.0 and float(dW1.abs().max()) == 0.0
