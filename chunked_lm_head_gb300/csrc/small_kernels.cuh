@@ -433,12 +433,32 @@ __global__ void fused_dlogits_kernel(uint16_t* __restrict__ E, const float* __re
   const float g = grad_scale / fmaxf(1.f, static_cast<float>(*n_valid));
   const float scale = valid ? (weights ? weights[row] : 1.f) * g : 0.f;
   uint4* slot = reinterpret_cast<uint4*>(E + static_cast<idx_t>(r) * ldD + c);
+  if (scale == 0.f) {  // ignored row (its exponentials may never have been written) or zero weight
+#pragma unroll
+    for (int h = 0; h < 4; ++h) slot[h] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   uint4 q[4] = {slot[0], slot[1], slot[2], slot[3]};
   const float cmL = mx[static_cast<idx_t>(r) * (ldD / 32) + c / 32];
   const float nlse2 = -lse[row] * kLog2e;
   const float base = ex2_approx(cmL + nlse2);  // 2^(chunk max - lse), both x log2(e)
   const float lin = tf_softcap ? 1.f : tf_a;    // linear transforms: du/dz = tf_a
   const long long tj = t - c;                   // target column inside this thread's 32, if any
+  if (!tf_softcap && c + 32 <= V && (tj < 0 || tj >= 32)) {
+    // the common chunk: inside the vocabulary, no target column, linear
+    // transform: D = E * 2^(max - lse) * scale * a, two columns per step
+    const float kf = base * scale * lin;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t w4[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        o[k] = pack_bf16x2(__uint_as_float(w4[k] << 16) * kf, __uint_as_float(w4[k] & 0xffff0000u) * kf);
+      slot[h] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    return;
+  }
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
     uint32_t w4[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
