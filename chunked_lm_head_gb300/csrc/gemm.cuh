@@ -715,7 +715,18 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
             const int gcol0 = p.v0 + col0;  // vocabulary column of D's local column col0
             const long long tjl = tgt - gcol0;
             const int tj = (tjl >= 0 && tjl < 32) ? static_cast<int>(tjl) : -1;
-            if (!p.tf_softcap) {
+            if (!p.tf_softcap && tj < 0 && gcol0 + 32 <= p.V) {
+              // the common chunk: no target column, inside the vocabulary
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float d0 = 0.f, d1 = 0.f;
+                if (scale != 0.f) {
+                  d0 = ex2_approx(fmaf(v[j], l2a, nl2)) * scale_a;
+                  d1 = ex2_approx(fmaf(v[j + 1], l2a, nl2)) * scale_a;
+                }
+                pk[j / 2] = pack_bf16x2(d0, d1);
+              }
+            } else if (!p.tf_softcap) {
 #pragma unroll
               for (int j = 0; j < 32; j += 2) {
                 float d0 = 0.f, d1 = 0.f;
