@@ -148,9 +148,10 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
     p.kb_per_split = f.k_blocks;
     p.k_splits = 1;
     p.num_units = f.units;
-    // 16 row tiles share each run of vocabulary tiles in L2 (measured on the
-    // 16K x 4096 x 151,936 case: DRAM reads 17.9 GB at 16 against 36.6 GB at
-    // 8 and 23.6 GB at 32, and the fastest launch)
+    // 16 row tiles share each run of vocabulary tiles in L2: one launch's
+    // rows (measured with one launch over all 16K rows of 16K x 4096 x
+    // 151,936: DRAM reads 17.9 GB in groups of 16 against 36.6 GB of 8 and
+    // 23.6 GB of 32, and the fastest launch)
     p.group_m = std::min(16, f.m_tiles);
     p.row0 = 0;
     p.rows = Ni;
