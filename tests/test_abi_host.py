@@ -150,3 +150,9 @@ def test_jsd_rejects_beta_outside_the_open_interval_before_any_launch(lib):
                                      p, None, None, None, None, None, stream=0) == 1
         assert _lib.flce_jsd_backward(p, p, 64, p, p, 64, None, None, p, p, p, beta, 1.0, p, p, 8, 100,
                                       16, -100, None, stream=0) == 1
+
+
+def test_a_missing_library_raises_instead_of_falling_back(tmp_path):
+    # no CPU path stands in for the CUDA library
+    with pytest.raises(FileNotFoundError):
+        _lib.load(str(tmp_path / "libflce.so"), build_if_missing=False)
