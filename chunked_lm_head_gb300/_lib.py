@@ -46,6 +46,13 @@ SIGNATURES = {
     "flce_kd_forward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
                                        _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp,
                                        _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_kd_forward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                           _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, ctypes.c_uint32, _c_vp,
+                                           _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_jsd_forward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                            _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_float, _c_vp,
+                                            ctypes.c_uint32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                            _c_vp, ctypes.c_size_t, _c_vp]),
     "flce_kd_backward": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
                                         _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp, _c_i64, _c_i64,
                                         _c_i64, _c_i64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
@@ -260,6 +267,31 @@ def flce_kd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_
                                 _ptr(weights), _ptr(lse_s), _ptr(lse_t), float(grad_scale),
                                 _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows, ignore_index, tp,
                                 _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_kd_forward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows, ignore_index,
+                        transform, flags, out_kl, out_lse_s, out_lse_t, out_loss, out_n_valid, workspace=None,
+                        workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the distillation forward with flags (FORWARD_SKIP_IGNORED)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_kd_forward_ex2(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                   _ptr(weights), N, V, chunk_rows, ignore_index, tp, int(flags), _ptr(out_kl),
+                                   _ptr(out_lse_s), _ptr(out_lse_t), _ptr(out_loss), _ptr(out_n_valid),
+                                   _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_jsd_forward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows, ignore_index,
+                         beta, transform, flags, out_jsd, out_lse_s, out_lse_t, out_kl_sm, out_loss,
+                         out_n_valid, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the Jensen-Shannon distillation forward with flags."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    return lib.flce_jsd_forward_ex2(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                    _ptr(weights), N, V, chunk_rows, ignore_index, float(beta), tp, int(flags),
+                                    _ptr(out_jsd), _ptr(out_lse_s), _ptr(out_lse_t), _ptr(out_kl_sm),
+                                    _ptr(out_loss), _ptr(out_n_valid), _ptr(workspace), workspace_bytes,
+                                    _stream_handle(stream))
 
 
 def flce_jsd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows, ignore_index,

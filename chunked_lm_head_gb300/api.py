@@ -338,8 +338,9 @@ def grpo_loss(h, W, targets, advantages, old_logp=None, ref_logp=None, eps_low: 
 
 def kd_forward(h_s, W_s, h_t, W_t, targets=None, weights=None, chunk_rows: int = 256,
                ignore_index: int = IGNORE_INDEX, transform=None,
-               workspace: torch.Tensor | None = None, stream=None):
-    """Distillation forward: dict(kl[N], lse_s[N], lse_t[N], loss[], n_valid[]) on device."""
+               workspace: torch.Tensor | None = None, stream=None, skip_ignored: bool = False):
+    """Distillation forward: dict(kl[N], lse_s[N], lse_t[N], loss[], n_valid[]) on device.
+    skip_ignored: both heads skip the ignored rows (their lse become NaN)."""
     for x in (h_s, W_s, h_t, W_t):
         if not x.is_cuda or x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 2:
             raise ValueError("h_s, W_s, h_t, W_t must be contiguous 2-D bfloat16 CUDA tensors")
@@ -355,10 +356,11 @@ def kd_forward(h_s, W_s, h_t, W_t, targets=None, weights=None, chunk_rows: int =
     loss = torch.empty((), dtype=torch.float32, device=dev)
     n_valid = torch.empty((), dtype=torch.int64, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_kd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows,
-                              ignore_index, transform, kl, lse_s, lse_t, loss, n_valid, workspace,
-                              ws_bytes, stream)
-    _lib.check("flce_kd_forward", st)
+    flags = _lib.FORWARD_SKIP_IGNORED if skip_ignored else 0
+    st = _lib.flce_kd_forward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows,
+                                  ignore_index, transform, flags, kl, lse_s, lse_t, loss, n_valid, workspace,
+                                  ws_bytes, stream)
+    _lib.check("flce_kd_forward_ex2", st)
     return {"kl": kl, "lse_s": lse_s, "lse_t": lse_t, "loss": loss, "n_valid": n_valid}
 
 
@@ -375,9 +377,11 @@ def _check_heads(h_s, W_s, h_t, W_t):
 
 def jsd_forward(h_s, W_s, h_t, W_t, beta: float = 0.5, targets=None, weights=None,
                 chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX, transform=None,
-                workspace: torch.Tensor | None = None, stream=None):
+                workspace: torch.Tensor | None = None, stream=None, skip_ignored: bool = False):
     """Jensen-Shannon distillation forward:
-    dict(jsd[N], lse_s[N], lse_t[N], kl_sm[N], loss[], n_valid[]) on device."""
+    dict(jsd[N], lse_s[N], lse_t[N], kl_sm[N], loss[], n_valid[]) on device.
+    skip_ignored: both heads skip the ignored rows (their lse and kl_sm
+    become NaN)."""
     N, H_s, H_t, V = _check_heads(h_s, W_s, h_t, W_t)
     dev = h_s.device
     jsd = torch.empty(N, dtype=torch.float32, device=dev)
@@ -387,10 +391,11 @@ def jsd_forward(h_s, W_s, h_t, W_t, beta: float = 0.5, targets=None, weights=Non
     loss = torch.empty((), dtype=torch.float32, device=dev)
     n_valid = torch.empty((), dtype=torch.int64, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_jsd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows,
-                               ignore_index, beta, transform, jsd, lse_s, lse_t, kl_sm, loss, n_valid,
-                               workspace, ws_bytes, stream)
-    _lib.check("flce_jsd_forward", st)
+    flags = _lib.FORWARD_SKIP_IGNORED if skip_ignored else 0
+    st = _lib.flce_jsd_forward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows,
+                                   ignore_index, beta, transform, flags, jsd, lse_s, lse_t, kl_sm, loss, n_valid,
+                                   workspace, ws_bytes, stream)
+    _lib.check("flce_jsd_forward_ex2", st)
     return {"jsd": jsd, "lse_s": lse_s, "lse_t": lse_t, "kl_sm": kl_sm, "loss": loss,
             "n_valid": n_valid}
 
@@ -438,12 +443,14 @@ class DistillLoss(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, h_s, W_s, h_t, W_t, targets, weights, beta, chunk_rows, ignore_index, transform=None):
+        # the backward reads lse (and kl_sm) of the non-ignored rows only
         if beta is None:
-            out = kd_forward(h_s, W_s, h_t, W_t, targets, weights, chunk_rows, ignore_index, transform)
+            out = kd_forward(h_s, W_s, h_t, W_t, targets, weights, chunk_rows, ignore_index, transform,
+                             skip_ignored=True)
             kl_sm = torch.empty(0, device=h_s.device)
         else:
             out = jsd_forward(h_s, W_s, h_t, W_t, beta, targets, weights, chunk_rows, ignore_index,
-                              transform)
+                              transform, skip_ignored=True)
             kl_sm = out["kl_sm"]
         empty = torch.empty(0, device=h_s.device)
         ctx.save_for_backward(h_s, W_s, h_t, W_t, targets if targets is not None else empty,

@@ -920,7 +920,9 @@ size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, i
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return 0;
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  const JsdFwdLayout fl = jsd_fwd_layout(N, plan_forward_call(N, H_s + H_t, V, workers, BM * cg));
+  // the forward's layout with the buffers of the row-skipping forwards
+  const JsdFwdLayout fl = jsd_fwd_layout(N, plan_forward_call(N, H_s + H_t, V, workers, BM * cg), H_s, H_t,
+                                         fwd_block_rows(N, BM * cg));
   const BwdLayout bl = bwd_layout(N, H_s, plan_backward(N, H_s, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
@@ -936,9 +938,11 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
                                    const flce_logit_transform* transform, float* out_kl,
                                    float* out_lse_s, float* out_lse_t, float* out_kl_sm,
                                    float* out_loss, int64_t* out_n_valid, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+                                   size_t workspace_bytes, void* stream, bool skip_ignored = false) {
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return FLCE_ERR_INVALID_ARG;
   if (jsd && !(beta > 0.f && beta < 1.f)) return FLCE_ERR_INVALID_ARG;
+  // ignored rows are skipped only where targets mark them
+  skip_ignored = skip_ignored && targets != nullptr;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
   if (!out_kl && !out_lse_s && !out_lse_t && !out_kl_sm && !out_loss && !out_n_valid)
@@ -958,10 +962,10 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
   // launches of one raster group of rows each (as the cross-entropy forward)
   const long long fb = fwd_block_rows(N, BM * cg);
   const FwdPlan f = plan_forward_call(N, H_s + H_t, V, workers, BM * cg);
-  const JsdFwdLayout J = jsd_fwd_layout(N, f);
+  const JsdFwdLayout J = jsd_fwd_layout(N, f, H_s, H_t, skip_ignored ? fb : 0);
   const KdFwdLayout& L = J.kd;
   Workspace ws;
-  flce_status s = get_workspace(ws, workspace, workspace_bytes, jsd ? J.total : L.total, st);
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, (jsd || skip_ignored) ? J.total : L.total, st);
   if (s != FLCE_OK) return s;
   uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
   float2* ps = reinterpret_cast<float2*>(wb + L.ps);
@@ -978,10 +982,41 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
   }
   const int Ni = static_cast<int>(N);
   if (N > 0) {
+    // skip_ignored: every launch runs over a gathered block of the
+    // non-ignored rows (listed on the device, count read by the kernels)
+    int* cidx = reinterpret_cast<int*>(wb + J.idx);
+    int* ccount = reinterpret_cast<int*>(wb + J.count);
+    uint16_t* hs_c = reinterpret_cast<uint16_t*>(wb + J.hs);
+    uint16_t* ht_c = reinterpret_cast<uint16_t*>(wb + J.ht);
+    if (skip_ignored) {
+      const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
+      int* cblk = reinterpret_cast<int*>(wb + J.blk);
+      ProfScope prof(K_COMPACT, st);
+      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index, cblk);
+      FLCE_CUDA_TRY(cudaGetLastError());
+      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index, cblk, nblk,
+                                                           cidx, ccount, 0);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
     CUtensorMap hs_k, Ws_k, ht_k, Wt_k;
-    if (!make_map(&hs_k, h_s, H_s, N, H_s, BK, BM) || !make_map(&Ws_k, W_s, H_s, V, H_s, BK, BN / cg) ||
-        !make_map(&ht_k, h_t, H_t, N, H_t, BK, BM) || !make_map(&Wt_k, W_t, H_t, V, H_t, BK, BN / cg))
+    if (!make_map(&hs_k, skip_ignored ? hs_c : h_s, H_s, skip_ignored ? fb : N, H_s, BK, BM) ||
+        !make_map(&Ws_k, W_s, H_s, V, H_s, BK, BN / cg) ||
+        !make_map(&ht_k, skip_ignored ? ht_c : h_t, H_t, skip_ignored ? fb : N, H_t, BK, BM) ||
+        !make_map(&Wt_k, W_t, H_t, V, H_t, BK, BN / cg))
       return FLCE_ERR_CUDA;
+    // the block's rows of both heads, gathered (skip_ignored)
+    auto gather_block = [&](long long row0) -> cudaError_t {
+      ProfScope prof(K_GATHER, st);
+      const int grid_s = static_cast<int>(std::min<long long>(ceil_div(fb * (H_s / 8), SMALL_THREADS), 8LL * device_sms()));
+      gather_rows_kernel<<<grid_s, SMALL_THREADS, 0, st>>>(h_s, static_cast<int>(H_s), cidx, ccount,
+                                                            static_cast<int>(N), static_cast<int>(row0),
+                                                            static_cast<int>(fb), hs_c);
+      const int grid_t = static_cast<int>(std::min<long long>(ceil_div(fb * (H_t / 8), SMALL_THREADS), 8LL * device_sms()));
+      gather_rows_kernel<<<grid_t, SMALL_THREADS, 0, st>>>(h_t, static_cast<int>(H_t), cidx, ccount,
+                                                            static_cast<int>(N), static_cast<int>(row0),
+                                                            static_cast<int>(fb), ht_c);
+      return cudaGetLastError();
+    };
     int* err = nullptr;
     FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
     GemmParams p{};
@@ -1023,9 +1058,16 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       q.m_tiles = static_cast<int>(ceil_div(q.rows, BM * cg));
       q.num_units = q.m_tiles * f.S;
       q.group_m = std::min(16, q.m_tiles);
+      if (skip_ignored) {  // non-ignored rows [row0, row0 + fb), gathered
+        q.row0 = 0;
+        q.row_idx = cidx;
+        q.chunk_first = static_cast<int>(row0);
+        q.dyn_count = ccount;
+      }
       return q;
     };
     for (long long row0 = 0; row0 < N; row0 += fb) {
+      if (skip_ignored) FLCE_CUDA_TRY(gather_block(row0));
       const GemmParams q = block_params(p, row0);
       ProfScope prof(K_KD_FWD, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_KD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, q, std::min(q.num_units, workers), st,
@@ -1034,12 +1076,13 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
     {
       ProfScope prof(K_COMBINE, st);
       float* kl = jsd ? nullptr : out_kl;
+      const int sk = skip_ignored ? 1 : 0;
       if (kLong)
         kd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(ps, pt, pc, f.S, Ni, targets, weights,
-                                                                  ignore_index, kl, lse_s, lse_t, bsum, bcnt);
+                                                                  ignore_index, kl, lse_s, lse_t, bsum, bcnt, sk);
       else
         kd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(ps, pt, pc, f.S, Ni, targets, weights,
-                                                                   ignore_index, kl, lse_s, lse_t, bsum, bcnt);
+                                                                   ignore_index, kl, lse_s, lse_t, bsum, bcnt, sk);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
     if (jsd) {
@@ -1050,18 +1093,20 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       q.partials = pj;
       q.jsd_beta = beta;
       for (long long row0 = 0; row0 < N; row0 += fb) {
+        if (skip_ignored) FLCE_CUDA_TRY(gather_block(row0));
         const GemmParams qb = block_params(q, row0);
         ProfScope prof(K_JSD_FWD, st);
         FLCE_CUDA_TRY(launch_gemm<MODE_JSD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, qb, std::min(qb.num_units, workers),
                                                 st, &ht_k, &Wt_k));
       }
       ProfScope prof(K_COMBINE, st);
+      const int skj = skip_ignored ? 1 : 0;
       if (kLong)
         jsd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, f.S, Ni, targets, weights, ignore_index,
-                                                                   beta, out_kl, out_kl_sm, bsum, bcnt);
+                                                                   beta, out_kl, out_kl_sm, bsum, bcnt, skj);
       else
         jsd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, f.S, Ni, targets, weights, ignore_index,
-                                                                    beta, out_kl, out_kl_sm, bsum, bcnt);
+                                                                    beta, out_kl, out_kl_sm, bsum, bcnt, skj);
       FLCE_CUDA_TRY(cudaGetLastError());
     }
   }
@@ -1093,6 +1138,39 @@ flce_status flce_jsd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
   return distill_forward(true, beta, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, ignore_index,
                          transform, out_jsd, out_lse_s, out_lse_t, out_kl_sm, out_loss, out_n_valid,
                          workspace, workspace_bytes, stream);
+}
+
+static bool distill_skip(uint32_t flags, int64_t N) {
+  return (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_env() && N >= skip_min_rows();
+}
+
+flce_status flce_kd_forward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                const int64_t* targets, const float* weights, int64_t N, int64_t V,
+                                int64_t chunk_rows, int64_t ignore_index,
+                                const flce_logit_transform* transform, uint32_t flags, float* out_kl,
+                                float* out_lse_s, float* out_lse_t, float* out_loss, int64_t* out_n_valid,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  (void)chunk_rows;
+  if ((flags & ~static_cast<uint32_t>(FLCE_FORWARD_SKIP_IGNORED)) != 0) return FLCE_ERR_INVALID_ARG;
+  return distill_forward(false, 0.f, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, ignore_index,
+                         transform, out_kl, out_lse_s, out_lse_t, nullptr, out_loss, out_n_valid,
+                         workspace, workspace_bytes, stream, distill_skip(flags, N));
+}
+
+flce_status flce_jsd_forward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                 const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                 const int64_t* targets, const float* weights, int64_t N, int64_t V,
+                                 int64_t chunk_rows, int64_t ignore_index, float beta,
+                                 const flce_logit_transform* transform, uint32_t flags, float* out_jsd,
+                                 float* out_lse_s, float* out_lse_t, float* out_kl_sm, float* out_loss,
+                                 int64_t* out_n_valid, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  (void)chunk_rows;
+  if ((flags & ~static_cast<uint32_t>(FLCE_FORWARD_SKIP_IGNORED)) != 0) return FLCE_ERR_INVALID_ARG;
+  return distill_forward(true, beta, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, ignore_index,
+                         transform, out_jsd, out_lse_s, out_lse_t, out_kl_sm, out_loss, out_n_valid,
+                         workspace, workspace_bytes, stream, distill_skip(flags, N));
 }
 
 // Distillation backward (student gradients, teacher frozen): KL dlogits

@@ -144,8 +144,8 @@ struct GemmParams {
   // rows_cap) read on the device.  row_idx == nullptr: rows are row0 + i.
   // The forward modes read row_idx too.  The fused forward's rows are a
   // block of a permutation that puts the non-ignored rows first (with
-  // dyn_count, only those are computed); the forward's, with dyn_count, a
-  // block of the non-ignored rows.
+  // dyn_count, only those are computed); the forward's and the distillation
+  // forwards', with dyn_count, a block of the non-ignored rows.
   const int* row_idx;
   const int* dyn_count;
   int chunk_first;
@@ -189,7 +189,8 @@ __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
   DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units};
   if (p.dyn_count != nullptr) {
     d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
-    if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD) {
+    if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD ||
+                  MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD) {
       d.m_tiles = (d.rows + TM - 1) / TM;
       d.num_units = p.k_splits * d.m_tiles * p.cols;
     } else if constexpr (MODE == MODE_DW) {
@@ -584,7 +585,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       // original row of this accumulator row (targets, weights, lse, dH;
       // the forward modes' partials and target logit)
       int grow = p.row0 + lr;
-      if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD) {
+      if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD ||
+                    MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD) {
         if (p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
       }
       // DLOGITS also writes zero rows up to the next 64-row K block so that

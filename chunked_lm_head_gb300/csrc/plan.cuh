@@ -320,11 +320,15 @@ KdFwdLayout kd_fwd_layout(long long N, const FwdPlan& f) {
 // Jensen-Shannon forward scratch: the distillation forward's (pass 1, both
 // heads' log-sum-exp) plus the mixture-term partials of pass 2 and the two lse
 // vectors when the caller does not ask for them.
+// With fb_skip > 0, also what a forward that skips the ignored rows needs:
+// the non-ignored row indices and count, and one launch's gathered rows of
+// both heads ([fb_skip, H_s] and [fb_skip, H_t] bf16).
 struct JsdFwdLayout {
   KdFwdLayout kd;
-  size_t pj = 0, lse_s = 0, lse_t = 0, total = 0;
+  size_t pj = 0, lse_s = 0, lse_t = 0, idx = 0, blk = 0, count = 0, hs = 0, ht = 0, total = 0;
 };
-JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f) {
+JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f, long long H_s = 0, long long H_t = 0,
+                            long long fb_skip = 0) {
   JsdFwdLayout L;
   L.kd = kd_fwd_layout(N, f);
   size_t o = L.kd.total;
@@ -334,6 +338,18 @@ JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f) {
   o += align256(static_cast<size_t>(N) * 4);
   L.lse_t = o;
   o += align256(static_cast<size_t>(N) * 4);
+  if (fb_skip > 0) {
+    L.idx = o;
+    o += align256(static_cast<size_t>(N) * 4);
+    L.blk = o;
+    o += align256(static_cast<size_t>(ceil_div(std::max(1LL, N), COMPACT_ROWS_PER_BLOCK)) * 4);
+    L.count = o;
+    o += 256;
+    L.hs = o;
+    o += align256(static_cast<size_t>(fb_skip) * H_s * 2);
+    L.ht = o;
+    o += align256(static_cast<size_t>(fb_skip) * H_t * 2);
+  }
   L.total = o;
   return L;
 }

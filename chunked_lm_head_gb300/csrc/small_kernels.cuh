@@ -280,6 +280,7 @@ __global__ void zero_tail_rows_kernel(uint16_t* __restrict__ dH, int H, const in
 // Distillation combine: student and teacher log-sum-exps from the split
 // partials, KL(p_t || p_s) = C / S_t - lse_t + lse_s per row, and the block's
 // share of sum(m w kl) and of the counted rows (targets == NULL: all rows).
+// skip_ignored: the forward skipped the ignored rows (lse NaN, kl 0).
 template <bool kLong>
 __global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* __restrict__ pt,
                                   const float* __restrict__ pc, int S, int N,
@@ -287,12 +288,17 @@ __global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* _
                                   const float* __restrict__ weights, long long ignore,
                                   float* __restrict__ out_kl, float* __restrict__ out_lse_s,
                                   float* __restrict__ out_lse_t, double* __restrict__ blk_sum,
-                                  long long* __restrict__ blk_cnt) {
+                                  long long* __restrict__ blk_cnt, int skip_ignored = 0) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
   double contrib = 0.0;
   long long cnt = 0;
-  if (i < N) {
+  if (i < N && skip_ignored && targets != nullptr && targets[i] == ignore) {
+    // the forward skipped this row: its log-sum-exps were not computed
+    if (out_kl) out_kl[i] = 0.f;
+    if (out_lse_s) out_lse_s[i] = __int_as_float(0x7fc00000);
+    if (out_lse_t) out_lse_t[i] = __int_as_float(0x7fc00000);
+  } else if (i < N) {
     float Ms = -INFINITY, Mt = -INFINITY;
     for (int s = 0; s < S; ++s) {
       Ms = fmaxf(Ms, ps[static_cast<idx_t>(s) * N + i].x);
@@ -326,18 +332,23 @@ __global__ void kd_combine_kernel(const float2* __restrict__ ps, const float2* _
 // Jensen-Shannon combine: per row, the split partials (log2 units) summed in
 // split order -> jsd = ln2 (beta A_t + (1 - beta) A_s) (0 on masked rows) and
 // kl_sm = ln2 A_s = KL(p_s || M); block sums of -w jsd and of the row count
-// for the deterministic loss.
+// for the deterministic loss.  skip_ignored: the forward skipped the
+// ignored rows (jsd 0, kl_sm NaN).
 template <bool kLong>
 __global__ void jsd_combine_kernel(const float2* __restrict__ pj, int S, int N,
                                    const int64_t* __restrict__ targets,
                                    const float* __restrict__ weights, long long ignore, float beta,
                                    float* __restrict__ out_jsd, float* __restrict__ out_kl_sm,
-                                   double* __restrict__ blk_sum, long long* __restrict__ blk_cnt) {
+                                   double* __restrict__ blk_sum, long long* __restrict__ blk_cnt,
+                                   int skip_ignored = 0) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   const int i = blockIdx.x * SMALL_THREADS + threadIdx.x;
   double contrib = 0.0;
   long long cnt = 0;
-  if (i < N) {
+  if (i < N && skip_ignored && targets != nullptr && targets[i] == ignore) {
+    if (out_jsd) out_jsd[i] = 0.f;  // the forward skipped this row
+    if (out_kl_sm) out_kl_sm[i] = __int_as_float(0x7fc00000);
+  } else if (i < N) {
     float at = 0.f, as = 0.f;
     for (int s = 0; s < S; ++s) {
       const float2 q = pj[static_cast<idx_t>(s) * N + i];

@@ -275,6 +275,34 @@ FLCE_API flce_status flce_kd_forward(const flce_bf16* h_s, const flce_bf16* W_s,
                                      void* stream);
 
 /*
+ * flce_kd_forward / flce_jsd_forward with flags (0 = the plain call).
+ *   FLCE_FORWARD_SKIP_IGNORED: with targets given, both heads' GEMMs skip
+ *     the ignored rows (as flce_forward_ex2): their kl / jsd is 0 and their
+ *     out_lse_s, out_lse_t and out_kl_sm are NaN (not computed), which the
+ *     backwards never read.  Calls with N < 2,048 rows (FLCE_SKIP_MIN_ROWS
+ *     overrides the bound) or with FLCE_COMPACT=0 compute every row.  The
+ *     workspace is flce_kd_workspace_bytes.
+ * Other flag bits: FLCE_ERR_INVALID_ARG.
+ */
+FLCE_API flce_status flce_kd_forward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                         const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                         const int64_t* targets, const float* weights, int64_t N,
+                                         int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                         const flce_logit_transform* transform, uint32_t flags,
+                                         float* out_kl, float* out_lse_s, float* out_lse_t,
+                                         float* out_loss, int64_t* out_n_valid, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+FLCE_API flce_status flce_jsd_forward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                          const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                          const int64_t* targets, const float* weights, int64_t N,
+                                          int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                          float beta, const flce_logit_transform* transform,
+                                          uint32_t flags, float* out_jsd, float* out_lse_s,
+                                          float* out_lse_t, float* out_kl_sm, float* out_loss,
+                                          int64_t* out_n_valid, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
  * Student gradients of the distillation loss (the teacher is frozen):
  *   D[i,v] = (p_s[i,v] - p_t[i,v]) * m[i] * w[i] * grad_scale * dy/dz_s,
  *   dH_s = D W_s ([N,H_s] bf16, or NULL),  dW_s = D^T h_s ([V,H_s] fp32, or NULL),

@@ -88,3 +88,57 @@ def test_jsd_of_identical_heads_is_zero_and_symmetric_at_one_half():
     b = flce.jsd_forward(ht, Wt, hs, Ws, 0.5)
     assert torch.allclose(a["jsd"], b["jsd"], atol=2e-5, rtol=1e-4)
     assert float(a["jsd"].min()) > 0 and float(a["jsd"].max()) <= float(np.log(2)) + 1e-6
+
+
+@pytest.mark.parametrize("beta", [None, 0.4])
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_distillation_forward_skipping_ignored_rows(beta, cg, monkeypatch):
+    """flce_kd_forward_ex2 / flce_jsd_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED
+    over 4 launches of 256 rows (the last holding fewer non-ignored rows, or
+    none): KL or Jensen-Shannon values, loss and the counted rows' lse against
+    the oracle, NaN lse on ignored rows, and the backwards from those lse
+    (compacted and over every row) against the oracle."""
+    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    monkeypatch.setenv("FLCE_SKIP_MIN_ROWS", "0")
+    monkeypatch.setenv("FLCE_FWD_BLOCK_ROWS", "256")
+    N, Hs, Ht, V = 900, 192, 256, 2100
+    si, ti = _heads(N, Hs, Ht, V, seed=733)
+    targets = np.random.default_rng(8).integers(0, V, N).astype(np.int64)
+    targets[np.random.default_rng(9).permutation(N)[: N // 3]] = WL.IGNORE_INDEX
+    weights = np.random.default_rng(10).uniform(0.3, 1.7, N).astype(np.float32)
+    m = targets != WL.IGNORE_INDEX
+    tfd = {"temperature": 1.5}
+    tf = O.LogitTransform(**tfd)
+    hs, Ws, ht, Wt = (to_dev_bf16(x) for x in (si.h, si.W, ti.h, ti.W))
+    tg = torch.from_numpy(targets).cuda()
+    w = torch.from_numpy(weights).cuda()
+    if beta is None:
+        out = flce.kd_forward(hs, Ws, ht, Wt, tg, w, 256, transform=tfd, skip_ignored=True)
+        ref = O.kd_forward(si.h, si.W, ti.h, ti.W, targets, weights, tf=tf)
+        assert_logp_close(np64(out["kl"]), ref.kl, "kl")
+    else:
+        out = flce.jsd_forward(hs, Ws, ht, Wt, beta, tg, w, 256, transform=tfd, skip_ignored=True)
+        ref = O.jsd_forward(si.h, si.W, ti.h, ti.W, beta, targets, weights, tf=tf)
+        assert_logp_close(np64(out["jsd"]), ref.jsd, "jsd")
+        assert_logp_close(np64(out["kl_sm"])[m], ref.kl_sm[m], "kl_sm")
+        assert np.all(np.isnan(np64(out["kl_sm"])[~m]))
+    assert int(out["n_valid"]) == ref.n_valid == int(m.sum())
+    assert float(out["loss"]) == pytest.approx(ref.loss, rel=LOSS_RTOL, abs=1e-6)
+    for k, r in (("lse_s", ref.lse_s), ("lse_t", ref.lse_t)):
+        assert_logp_close(np64(out[k])[m], r[m], k)
+        assert np.all(np.isnan(np64(out[k])[~m]))
+    g = 1.0 / ref.n_valid
+    if beta is None:
+        refb = O.kd_backward(si.h, si.W, ti.h, ti.W, targets, weights, g=g, tf=tf)
+    else:
+        refb = O.jsd_backward(si.h, si.W, ti.h, ti.W, beta, targets, weights, g=g, tf=tf)
+    for compact in ("1", "0"):
+        monkeypatch.setenv("FLCE_COMPACT", compact)
+        if beta is None:
+            dH, dW = flce.kd_backward(hs, Ws, ht, Wt, out["lse_s"], out["lse_t"], g, tg, w, 256, transform=tfd)
+        else:
+            dH, dW = flce.jsd_backward(hs, Ws, ht, Wt, out["lse_s"], out["lse_t"], out["kl_sm"], g, beta, tg, w,
+                                       256, transform=tfd)
+        assert_grad_close(np64(dH), refb.dH, f"dH_s (compact {compact})")
+        assert_grad_close(np64(dW), refb.dW, f"dW_s (compact {compact})")
+    assert flce._lib.flce_device_status() == 0
