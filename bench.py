@@ -303,21 +303,22 @@ def gpu_arm(args):
                     workspace.data_ptr(), ws_bytes, sh))
             return
         if Ht and args.jsd_beta:
-            check("flce_jsd_forward", lib.flce_jsd_forward(
+            # a training step reads no lse of ignored rows: both heads skip them
+            check("flce_jsd_forward_ex2", lib.flce_jsd_forward_ex2(
                 h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp, N,
-                V, chunk_rows, -100, args.jsd_beta, tf_ptr, logp.data_ptr(), lse.data_ptr(),
-                lse_t.data_ptr(), kl_sm.data_ptr(), loss.data_ptr(), nv.data_ptr(),
-                workspace.data_ptr(), ws_bytes, sh))
+                V, chunk_rows, -100, args.jsd_beta, tf_ptr, _lib.FORWARD_SKIP_IGNORED,
+                logp.data_ptr(), lse.data_ptr(), lse_t.data_ptr(), kl_sm.data_ptr(), loss.data_ptr(),
+                nv.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
             check("flce_jsd_backward", lib.flce_jsd_backward(
                 h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp,
                 lse.data_ptr(), lse_t.data_ptr(), kl_sm.data_ptr(), args.jsd_beta, g, dH.data_ptr(),
                 dW.data_ptr(), N, V, chunk_rows, -100, tf_ptr, workspace.data_ptr(), ws_bytes, sh))
             return
         if Ht:
-            check("flce_kd_forward", lib.flce_kd_forward(
+            check("flce_kd_forward_ex2", lib.flce_kd_forward_ex2(
                 h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp, N,
-                V, chunk_rows, -100, tf_ptr, logp.data_ptr(), lse.data_ptr(), lse_t.data_ptr(),
-                loss.data_ptr(), nv.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
+                V, chunk_rows, -100, tf_ptr, _lib.FORWARD_SKIP_IGNORED, logp.data_ptr(), lse.data_ptr(),
+                lse_t.data_ptr(), loss.data_ptr(), nv.data_ptr(), workspace.data_ptr(), ws_bytes, sh))
             check("flce_kd_backward", lib.flce_kd_backward(
                 h.data_ptr(), W.data_ptr(), H, ht.data_ptr(), Wt.data_ptr(), Ht, t.data_ptr(), wp,
                 lse.data_ptr(), lse_t.data_ptr(), g, dH.data_ptr(), dW.data_ptr(), N, V, chunk_rows,

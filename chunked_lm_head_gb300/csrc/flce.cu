@@ -923,7 +923,8 @@ size_t flce_kd_workspace_bytes(int64_t N, int64_t H_s, int64_t H_t, int64_t V, i
   // the forward's layout with the buffers of the row-skipping forwards
   const JsdFwdLayout fl = jsd_fwd_layout(N, plan_forward_call(N, H_s + H_t, V, workers, BM * cg), H_s, H_t,
                                          fwd_block_rows(N, BM * cg));
-  const BwdLayout bl = bwd_layout(N, H_s, plan_backward(N, H_s, V, chunk_rows, workers, BM * cg));
+  const DistillBwdLayout bl =
+      distill_bwd_layout(N, H_s, H_t, plan_backward(N, H_s, V, chunk_rows, workers, BM * cg));
   return std::max(fl.total, bl.total);
 }
 
@@ -1205,9 +1206,10 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
   const int workers = device_workers(cg);
   const int tm = BM * cg;
   const BwdPlan b = plan_backward(N, H_s, V, chunk_rows, workers, tm);
-  const BwdLayout L = bwd_layout(N, H_s, b);
+  const DistillBwdLayout DL = distill_bwd_layout(N, H_s, H_t, b);
+  const BwdLayout& L = DL.b;
   Workspace ws;
-  flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
+  flce_status s = get_workspace(ws, workspace, workspace_bytes, DL.total, st);
   if (s != FLCE_OK) return s;
   uint8_t* wb = static_cast<uint8_t*>(ws.ptr);
   uint16_t* Dbuf = reinterpret_cast<uint16_t*>(wb + L.D);
@@ -1254,6 +1256,38 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
   base.tf_b = tfp.tf_b;
   base.tf_d = tfp.tf_d;
 
+  // Row compaction, as in the cross-entropy backward: where targets mark
+  // ignored rows, the chunks run over the non-ignored rows of both heads
+  // (gathered per chunk), and the ignored rows' dH is zeroed up front.
+  const bool compact = targets != nullptr && compact_env();
+  int* cidx = reinterpret_cast<int*>(wb + L.idx);
+  int* cblk = reinterpret_cast<int*>(wb + L.blk);
+  int* ccount = reinterpret_cast<int*>(wb + L.count);
+  uint16_t* hcs = reinterpret_cast<uint16_t*>(wb + L.hc);
+  uint16_t* hct = reinterpret_cast<uint16_t*>(wb + DL.hc_t);
+  CUtensorMap hcs_k, hcs_mn, hct_k, Dfix_k, Dfix_mn;
+  if (compact) {
+    const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
+    {
+      ProfScope ps(K_COMPACT, st);
+      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
+                                                           cblk);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    {
+      ProfScope ps(K_COMPACT, st);
+      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
+                                                           cblk, nblk, cidx, ccount, 0);
+      FLCE_CUDA_TRY(cudaGetLastError());
+    }
+    if (dH_s) FLCE_CUDA_TRY(cudaMemsetAsync(dH_s, 0, static_cast<size_t>(N) * H_s * 2, st));
+    if (!make_map(&hcs_k, hcs, H_s, b.R, H_s, BK, BM) || !make_map(&hcs_mn, hcs, H_s, b.R, H_s, 64, BK) ||
+        !make_map(&hct_k, hct, H_t, b.R, H_t, BK, BM) ||
+        !make_map(&Dfix_k, Dbuf, b.ldD, b.R, b.ldD, BK, BM) ||
+        !make_map(&Dfix_mn, Dbuf, b.ldD, b.R, b.ldD, 64, BK))
+      return FLCE_ERR_CUDA;
+  }
+
   CUtensorMap dhp_map;
   if (dH_s && b.dh_f32 &&
       !make_map_t(&dhp_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dh_part, H, b.dh_splits * b.R, H, 32, 32))
@@ -1261,14 +1295,39 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
   const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH_s, dW_s, &Ws_mn, &dW_map, &dhp_map};
   int block = 0;
   for (long long row0 = 0; row0 < N; row0 += b.R, ++block) {
-    const int rows = static_cast<int>(std::min(b.R, N - row0));
+    // rows: exact (plain) or the capacity whose live part the kernels read (compacted)
+    const int rows = compact ? static_cast<int>(b.R) : static_cast<int>(std::min(b.R, N - row0));
     GemmParams p = base;
-    p.row0 = static_cast<int>(row0);
+    p.row0 = compact ? 0 : static_cast<int>(row0);
     p.rows = rows;
+    if (compact) {
+      p.row_idx = cidx;
+      p.dyn_count = ccount;
+      p.chunk_first = static_cast<int>(row0);
+      const long long cap = b.R;
+      ProfScope ps(K_GATHER, st);
+      for (int head = 0; head < 2; ++head) {
+        const long long Hh = head == 0 ? H_s : H_t;
+        const int grid = static_cast<int>(
+            std::min<long long>(ceil_div(cap * (Hh / 8), SMALL_THREADS), 8LL * device_sms()));
+        gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(head == 0 ? h_s : h_t, static_cast<int>(Hh), cidx,
+                                                            ccount, static_cast<int>(N),
+                                                            static_cast<int>(row0), static_cast<int>(cap),
+                                                            head == 0 ? hcs : hct);
+        FLCE_CUDA_TRY(cudaGetLastError());
+      }
+    }
+    const CUtensorMap& As_k = compact ? hcs_k : hs_k;
+    const CUtensorMap& At_k = compact ? hct_k : ht_k;
+    const CUtensorMap& B_dw = compact ? hcs_mn : hs_mn;
     CUtensorMap D_k, D_mn;
-    if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) ||
-        !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK))
+    if (compact) {
+      D_k = Dfix_k;
+      D_mn = Dfix_mn;
+    } else if (!make_map(&D_k, Dbuf, b.ldD, rows, b.ldD, BK, BM) ||
+               !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK)) {
       return FLCE_ERR_CUDA;
+    }
     for (int slab = 0; slab < b.n_slabs; ++slab) {
       const int v0 = static_cast<int>(slab * b.Vs);
       const int width = static_cast<int>(std::min<long long>(b.Vs, V - v0));
@@ -1286,16 +1345,17 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
         q.group_m = std::min(16, q.m_tiles);
         ProfScope prof(jsd ? K_JSD_DLOGITS : K_KD_DLOGITS, st);
         if (jsd)
-          FLCE_CUDA_TRY(launch_gemm<MODE_JSD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
-                                                      std::min(q.num_units, workers), st, &ht_k, &Wt_k));
+          FLCE_CUDA_TRY(launch_gemm<MODE_JSD_DLOGITS>(cg, kLong, As_k, Ws_k, Ws_k, q,
+                                                      std::min(q.num_units, workers), st, &At_k, &Wt_k));
         else
-          FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, hs_k, Ws_k, Ws_k, q,
-                                                     std::min(q.num_units, workers), st, &ht_k, &Wt_k));
+          FLCE_CUDA_TRY(launch_gemm<MODE_KD_DLOGITS>(cg, kLong, As_k, Ws_k, Ws_k, q,
+                                                     std::min(q.num_units, workers), st, &At_k, &Wt_k));
       }
-      const flce_status s2 = slab_dh_dw(dhdw, p, rows, block, slab, v0, width, D_k, D_mn, hs_mn, st);
+      const flce_status s2 = slab_dh_dw(dhdw, p, rows, block, slab, v0, width, D_k, D_mn, B_dw, st);
       if (s2 != FLCE_OK) return s2;
     }
-    const flce_status s3 = block_dh_finish(dhdw, p.row0, rows, nullptr, nullptr, 0, st);
+    const flce_status s3 = block_dh_finish(dhdw, p.row0, rows, compact ? cidx : nullptr,
+                                           compact ? ccount : nullptr, static_cast<int>(row0), st);
     if (s3 != FLCE_OK) return s3;
   }
   return FLCE_OK;

@@ -95,6 +95,13 @@ __host__ __device__ constexpr bool is_kd() {
   return MODE == MODE_KD_FWD || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_FWD ||
          MODE == MODE_JSD_DLOGITS;
 }
+// modes whose accumulator rows are rows of h (all but dW, whose accumulator
+// rows are vocabulary rows): under row compaction they map through row_idx
+// and take their row count from the device
+template <int MODE>
+__host__ __device__ constexpr bool rows_are_tokens() {
+  return MODE != MODE_DW;
+}
 // modes whose units are (row tile, vocabulary split) with per-row partials
 template <int MODE>
 __host__ __device__ constexpr bool is_split_fwd() {
@@ -138,7 +145,7 @@ struct GemmParams {
   float* dW;          // DW out [V][H] fp32
   int dW_accumulate;
   int* err;           // device error word
-  // Row compaction (backward on non-ignored rows only): row_idx maps a
+  // Row compaction (backwards on non-ignored rows only): row_idx maps a
   // compacted row to its original row; this pass holds compacted rows
   // [chunk_first, chunk_first + rows) with rows = min(*dyn_count - chunk_first,
   // rows_cap) read on the device.  row_idx == nullptr: rows are row0 + i.
@@ -189,8 +196,7 @@ __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
   DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units};
   if (p.dyn_count != nullptr) {
     d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
-    if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD ||
-                  MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD) {
+    if constexpr (rows_are_tokens<MODE>()) {
       d.m_tiles = (d.rows + TM - 1) / TM;
       d.num_units = p.k_splits * d.m_tiles * p.cols;
     } else if constexpr (MODE == MODE_DW) {
@@ -585,8 +591,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       // original row of this accumulator row (targets, weights, lse, dH;
       // the forward modes' partials and target logit)
       int grow = p.row0 + lr;
-      if constexpr (MODE == MODE_DLOGITS || MODE == MODE_DH || MODE == MODE_FUSED_FWD || MODE == MODE_FWD ||
-                    MODE == MODE_KD_FWD || MODE == MODE_JSD_FWD) {
+      if constexpr (rows_are_tokens<MODE>()) {
         if (p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
       }
       // DLOGITS also writes zero rows up to the next 64-row K block so that

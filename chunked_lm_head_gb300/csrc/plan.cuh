@@ -381,6 +381,20 @@ BwdLayout bwd_layout(long long N, long long H, const BwdPlan& b) {
   return L;
 }
 
+// The distillation backward: the backward's buffers (student width) and one
+// chunk's gathered teacher rows for the row compaction.
+struct DistillBwdLayout {
+  BwdLayout b;
+  size_t hc_t = 0, total = 0;
+};
+DistillBwdLayout distill_bwd_layout(long long N, long long H_s, long long H_t, const BwdPlan& b) {
+  DistillBwdLayout L;
+  L.b = bwd_layout(N, H_s, b);
+  L.hc_t = L.b.total;
+  L.total = L.hc_t + align256(static_cast<size_t>(b.R) * H_t * 2);
+  return L;
+}
+
 // ---- forward + backward in one call without the logits recompute
 
 // Row blocks of R rows over the whole vocabulary: the forward GEMM keeps the

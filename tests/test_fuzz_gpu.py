@@ -103,7 +103,8 @@ def _kd_cases(n, seed=950):
         out.append(dict(N=int(r.integers(1, 700)), Hs=int(8 * r.integers(1, 48)), Ht=int(8 * r.integers(1, 48)),
                         V=int(r.integers(2, 4000)), chunk=int(r.choice([1, 64, 128, 300, 1024])),
                         cg=str(r.choice(["1", "2"])), masked=bool(r.uniform() < 0.6),
-                        jsd=float(r.choice([0.0, 0.5, 0.2, 0.85])), tf=int(r.integers(0, 3)), seed=2000 + k))
+                        jsd=float(r.choice([0.0, 0.5, 0.2, 0.85])), tf=int(r.integers(0, 3)), seed=2000 + k,
+                        compact="0" if k % 4 == 3 else "1"))
     return out
 
 
@@ -112,6 +113,7 @@ def test_random_distillation_matches_oracle(c, monkeypatch):
     import chunked_lm_head_gb300 as flce
     from gpu_util import to_dev_bf16
     monkeypatch.setenv("FLCE_CTA_GROUP", c["cg"])
+    monkeypatch.setenv("FLCE_COMPACT", c["compact"])  # masked backward: compacted rows or every row
     s = WL.make_inputs(WL.custom("kfs", c["N"], c["Hs"], c["V"], 256, w_std=0.1, seed=c["seed"]))
     t_ = WL.make_inputs(WL.custom("kft", c["N"], c["Ht"], c["V"], 256, w_std=0.12, seed=c["seed"] + 500))
     r = np.random.default_rng(c["seed"])
