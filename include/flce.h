@@ -307,7 +307,11 @@ FLCE_API flce_status flce_jsd_forward_ex2(const flce_bf16* h_s, const flce_bf16*
  *   D[i,v] = (p_s[i,v] - p_t[i,v]) * m[i] * w[i] * grad_scale * dy/dz_s,
  *   dH_s = D W_s ([N,H_s] bf16, or NULL),  dW_s = D^T h_s ([V,H_s] fp32, or NULL),
  * recomputing both heads' logits chunk by chunk (chunk_rows as in
- * flce_backward).  lse_s / lse_t come from flce_kd_forward.
+ * flce_backward).  lse_s / lse_t come from flce_kd_forward (or
+ * flce_kd_forward_ex2).  Where targets mark ignored rows, the chunks run
+ * over the non-ignored rows only (both heads' rows gathered per chunk); the
+ * ignored rows' lse are never read and their dH_s rows are 0.  workspace is
+ * flce_kd_workspace_bytes.
  */
 FLCE_API flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
                                       const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
@@ -352,8 +356,9 @@ FLCE_API flce_status flce_jsd_forward(const flce_bf16* h_s, const flce_bf16* W_s
  *   D[i,v] = (1 - beta) p_s[i,v] (ln(p_s[i,v] / M[i,v]) - kl_sm[i]) * m[i] w[i] grad_scale
  *            * f'(z_s[i,v]),
  *   dH_s = D W_s, dW_s = D^T h_s,
- * with lse_s, lse_t, kl_sm from flce_jsd_forward (same beta and transform).
- * Memory and tiling as flce_kd_backward.
+ * with lse_s, lse_t, kl_sm from flce_jsd_forward or flce_jsd_forward_ex2
+ * (same beta and transform).  Memory, tiling and the skipping of ignored
+ * rows as flce_kd_backward.
  */
 FLCE_API flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
                                        const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
