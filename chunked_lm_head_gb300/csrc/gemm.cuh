@@ -557,8 +557,12 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // accumulator row owned by this thread
-    // columns of the tile this warp takes: all, or one half (8 epilogue warps)
-    static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && MODE == MODE_DW), "8 epilogue warps: dW only");
+    // columns of the tile this warp takes: all, or one half (8 epilogue
+    // warps, for the modes whose epilogue keeps no per-row sums)
+    static_assert(EW == EPI_WARPS ||
+                      (EW == 2 * EPI_WARPS &&
+                       (MODE == MODE_DW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS)),
+                  "8 epilogue warps: dW and the two-head dlogits only");
     constexpr int kColParts = EW / 4;
     constexpr int kChunks = BN / 32 / kColParts;
     const int c_lo = ((warp - 2) / 4) * kChunks;

@@ -70,6 +70,14 @@ bool pdl_env() {
   return !(s != nullptr && s[0] == '0');
 }
 
+// The two-head dlogits GEMMs (distillation) run 8 epilogue warps (default;
+// FLCE_WIDE_EPILOGUE=0 keeps 4): their tile fills TMEM, so the epilogue
+// does not overlap the next tile's MMAs and its length adds to each tile's.
+bool wide_epilogue_env() {
+  const char* s = std::getenv("FLCE_WIDE_EPILOGUE");
+  return !(s != nullptr && s[0] == '0');
+}
+
 // Launch on `grid` CTAs in clusters of `cluster` with the GEMMs' attributes.
 template <class Kern, class... Args>
 cudaError_t launch_persistent(Kern k, int grid, int cluster, int threads, int smem, cudaStream_t st,
@@ -127,8 +135,8 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
   // a2 / b2: the teacher's operands of the distillation modes (else unused)
   const CUtensorMap& A2 = a2 ? *a2 : a;
   const CUtensorMap& B2 = b2 ? *b2 : b;
-  if constexpr (MODE == MODE_DW) {
-    if (p.k_blocks <= kDwWideEpilogueMaxKBlocks) {
+  if constexpr (MODE == MODE_DW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS) {
+    if (MODE == MODE_DW ? p.k_blocks <= kDwWideEpilogueMaxKBlocks : wide_epilogue_env()) {
       constexpr int EW = 2 * EPI_WARPS;
       if (cg == 2)
         return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, p, workers, st)

@@ -104,7 +104,7 @@ def _kd_cases(n, seed=950):
                         V=int(r.integers(2, 4000)), chunk=int(r.choice([1, 64, 128, 300, 1024])),
                         cg=str(r.choice(["1", "2"])), masked=bool(r.uniform() < 0.6),
                         jsd=float(r.choice([0.0, 0.5, 0.2, 0.85])), tf=int(r.integers(0, 3)), seed=2000 + k,
-                        compact="0" if k % 4 == 3 else "1"))
+                        compact="0" if k % 4 == 3 else "1", wide="0" if k % 4 == 1 else "1"))
     return out
 
 
@@ -114,6 +114,7 @@ def test_random_distillation_matches_oracle(c, monkeypatch):
     from gpu_util import to_dev_bf16
     monkeypatch.setenv("FLCE_CTA_GROUP", c["cg"])
     monkeypatch.setenv("FLCE_COMPACT", c["compact"])  # masked backward: compacted rows or every row
+    monkeypatch.setenv("FLCE_WIDE_EPILOGUE", c["wide"])  # dlogits epilogue: 8 warps or 4
     s = WL.make_inputs(WL.custom("kfs", c["N"], c["Hs"], c["V"], 256, w_std=0.1, seed=c["seed"]))
     t_ = WL.make_inputs(WL.custom("kft", c["N"], c["Ht"], c["V"], 256, w_std=0.12, seed=c["seed"] + 500))
     r = np.random.default_rng(c["seed"])
