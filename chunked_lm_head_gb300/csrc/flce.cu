@@ -1042,13 +1042,19 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
     p.partials = ps;
     p.partials_t = pt;
     p.partials_c = pc;
+    // the Jensen-Shannon pass: per-row partials of each column half of a
+    // tile in a slot of their own (8 epilogue warps); pass 1 keeps 4 warps,
+    // which timed as fast for its cheaper epilogue
+    const int jsd_parts = wide_epilogue_env() ? kJsdColParts : 1;
+    const int jsd_slots = f.S * jsd_parts;
+    p.col_parts = 1;
     p.err = err;
     p.tf_softcap = tfp.tf_softcap;
     p.tf_a = tfp.tf_a;
     p.tf_b = tfp.tf_b;
     p.tf_d = tfp.tf_d;
     const bool kLong = static_cast<long long>(N) * V >= INT_MAX ||
-                       static_cast<long long>(f.S) * N >= INT_MAX;
+                       static_cast<long long>(jsd_slots) * N >= INT_MAX;
     // one launch per block of fb rows: every unit of a launch shares its
     // rows' h tiles, and the 16 row tiles of a block share each W tile in L2
     auto block_params = [&](const GemmParams& base, long long row0) {
@@ -1093,6 +1099,7 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       q.lse_t = lse_t;
       q.partials = pj;
       q.jsd_beta = beta;
+      q.col_parts = jsd_parts;
       for (long long row0 = 0; row0 < N; row0 += fb) {
         if (skip_ignored) FLCE_CUDA_TRY(gather_block(row0));
         const GemmParams qb = block_params(q, row0);
@@ -1103,10 +1110,10 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       ProfScope prof(K_COMBINE, st);
       const int skj = skip_ignored ? 1 : 0;
       if (kLong)
-        jsd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, f.S, Ni, targets, weights, ignore_index,
+        jsd_combine_kernel<true><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, jsd_slots, Ni, targets, weights, ignore_index,
                                                                    beta, out_kl, out_kl_sm, bsum, bcnt, skj);
       else
-        jsd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, f.S, Ni, targets, weights, ignore_index,
+        jsd_combine_kernel<false><<<f.nblk, SMALL_THREADS, 0, st>>>(pj, jsd_slots, Ni, targets, weights, ignore_index,
                                                                     beta, out_kl, out_kl_sm, bsum, bcnt, skj);
       FLCE_CUDA_TRY(cudaGetLastError());
     }

@@ -95,6 +95,14 @@ __host__ __device__ constexpr bool is_kd() {
   return MODE == MODE_KD_FWD || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_FWD ||
          MODE == MODE_JSD_DLOGITS;
 }
+// modes that may run 8 epilogue warps, two per TMEM lane quarter, each
+// taking half of the tile's columns: dW, and the two-head modes whose
+// epilogue does not overlap the next tile's MMAs (the Jensen-Shannon
+// forward's per-row partials of each half go to a slot of their own)
+template <int MODE>
+__host__ __device__ constexpr bool wide_epilogue_mode() {
+  return MODE == MODE_DW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS || MODE == MODE_JSD_FWD;
+}
 // modes whose accumulator rows are rows of h (all but dW, whose accumulator
 // rows are vocabulary rows): under row compaction they map through row_idx
 // and take their row count from the device
@@ -163,6 +171,10 @@ struct GemmParams {
   const float* lse_t;
   float2* partials_t;  // [splits][N] (teacher max*log2e, sum exp2)
   float* partials_c;   // [splits][N] sum exp2(u_t - m_t) * (z_t - z_s)
+  // Jensen-Shannon forward terms: 2 = each tile's columns are split between
+  // two epilogue warps, which write their per-row partials to slots 2 split
+  // and 2 split + 1 (the partial array then holds 2 x splits slots); else 1
+  int col_parts;
   // e4m3 forward: logits = acc * a_scale[row] * b_scale[vocabulary row]
   const float* a_scale;
   const float* b_scale;
@@ -557,12 +569,9 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // accumulator row owned by this thread
-    // columns of the tile this warp takes: all, or one half (8 epilogue
-    // warps, for the modes whose epilogue keeps no per-row sums)
-    static_assert(EW == EPI_WARPS ||
-                      (EW == 2 * EPI_WARPS &&
-                       (MODE == MODE_DW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS)),
-                  "8 epilogue warps: dW and the two-head dlogits only");
+    // columns of the tile this warp takes: all, or one half (8 epilogue warps)
+    static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && wide_epilogue_mode<MODE>()),
+                  "8 epilogue warps: dW, the two-head dlogits and the Jensen-Shannon terms only");
     constexpr int kColParts = EW / 4;
     constexpr int kChunks = BN / 32 / kColParts;
     const int c_lo = ((warp - 2) / 4) * kChunks;
@@ -1023,12 +1032,15 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
         if (ok && row_ok)
           p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(run_m, run_s);
       }
+      // the two-head forwards: the partial slot of this split and column part
+      // (8 epilogue warps: the Jensen-Shannon terms only)
+      const int slot = t.split * kColParts + (warp - 2) / 4;
       if constexpr (MODE == MODE_JSD_FWD) {
-        if (ok && row_ok) p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(jsd_t, jsd_s);
+        if (ok && row_ok) p.partials[static_cast<idx_t>(slot) * p.N + grow] = make_float2(jsd_t, jsd_s);
       }
       if constexpr (MODE == MODE_KD_FWD) {
         if (ok && row_ok) {
-          const idx_t o = static_cast<idx_t>(t.split) * p.N + grow;
+          const idx_t o = static_cast<idx_t>(slot) * p.N + grow;
           p.partials[o] = make_float2(run_m, run_s);
           p.partials_t[o] = make_float2(run_mt, run_st);
           p.partials_c[o] = run_c;

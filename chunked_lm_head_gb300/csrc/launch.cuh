@@ -70,9 +70,10 @@ bool pdl_env() {
   return !(s != nullptr && s[0] == '0');
 }
 
-// The two-head dlogits GEMMs (distillation) run 8 epilogue warps (default;
-// FLCE_WIDE_EPILOGUE=0 keeps 4): their tile fills TMEM, so the epilogue
-// does not overlap the next tile's MMAs and its length adds to each tile's.
+// The two-head dlogits GEMMs and the Jensen-Shannon forward terms
+// (distillation) run 8 epilogue warps (default; FLCE_WIDE_EPILOGUE=0 keeps
+// 4): their tile fills TMEM, so the epilogue does not overlap the next tile's
+// MMAs and its length adds to each tile's.
 bool wide_epilogue_env() {
   const char* s = std::getenv("FLCE_WIDE_EPILOGUE");
   return !(s != nullptr && s[0] == '0');
@@ -135,8 +136,13 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
   // a2 / b2: the teacher's operands of the distillation modes (else unused)
   const CUtensorMap& A2 = a2 ? *a2 : a;
   const CUtensorMap& B2 = b2 ? *b2 : b;
-  if constexpr (MODE == MODE_DW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS) {
-    if (MODE == MODE_DW ? p.k_blocks <= kDwWideEpilogueMaxKBlocks : wide_epilogue_env()) {
+  if constexpr (wide_epilogue_mode<MODE>()) {
+    // the Jensen-Shannon forward's caller sized the partials for the column
+    // parts it chose
+    const bool wide = MODE == MODE_DW       ? p.k_blocks <= kDwWideEpilogueMaxKBlocks
+                      : MODE == MODE_JSD_FWD ? p.col_parts == 2
+                                             : wide_epilogue_env();
+    if (wide) {
       constexpr int EW = 2 * EPI_WARPS;
       if (cg == 2)
         return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, p, workers, st)

@@ -319,10 +319,13 @@ KdFwdLayout kd_fwd_layout(long long N, const FwdPlan& f) {
 
 // Jensen-Shannon forward scratch: the distillation forward's (pass 1, both
 // heads' log-sum-exp) plus the mixture-term partials of pass 2 and the two lse
-// vectors when the caller does not ask for them.
+// vectors when the caller does not ask for them.  The mixture-term partials
+// hold kJsdColParts slots per vocabulary split: with 8 epilogue warps, each
+// half of a tile's columns writes its own.
 // With fb_skip > 0, also what a forward that skips the ignored rows needs:
 // the non-ignored row indices and count, and one launch's gathered rows of
 // both heads ([fb_skip, H_s] and [fb_skip, H_t] bf16).
+constexpr int kJsdColParts = 2;
 struct JsdFwdLayout {
   KdFwdLayout kd;
   size_t pj = 0, lse_s = 0, lse_t = 0, idx = 0, blk = 0, count = 0, hs = 0, ht = 0, total = 0;
@@ -333,7 +336,7 @@ JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f, long long H_s = 0, lo
   L.kd = kd_fwd_layout(N, f);
   size_t o = L.kd.total;
   L.pj = o;
-  o += align256(static_cast<size_t>(f.S) * N * 8);
+  o += align256(static_cast<size_t>(f.S) * kJsdColParts * N * 8);
   L.lse_s = o;
   o += align256(static_cast<size_t>(N) * 4);
   L.lse_t = o;
