@@ -156,3 +156,14 @@ def test_a_missing_library_raises_instead_of_falling_back(tmp_path):
     # no CPU path stands in for the CUDA library
     with pytest.raises(FileNotFoundError):
         _lib.load(str(tmp_path / "libflce.so"), build_if_missing=False)
+
+
+@pytest.mark.parametrize("shape", [(32768, 4096, 4096, 128000, 4096), (1100, 256, 384, 6000, 128),
+                                   (900, 192, 256, 2100, 256), (7, 8, 4096, 50, 1)])
+def test_distillation_workspace_holds_the_backward_and_both_gathered_heads(lib, shape):
+    # the distillation backward compacts rows like the cross-entropy backward
+    # and also gathers one row block of the teacher's h ([rows, H_t] bf16)
+    N, Hs, Ht, V, chunk = shape
+    p = _lib.flce_backward_plan(N, Hs, V, chunk)
+    ws = _lib.flce_kd_workspace_bytes(N, Hs, Ht, V, chunk)
+    assert ws >= p["workspace_bytes"] + p["rows_per_block"] * Ht * 2
