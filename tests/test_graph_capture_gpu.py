@@ -98,7 +98,7 @@ def test_one_call_forward_backward_graph_replay_matches_eager():
     assert _lib.flce_device_status() == 0
 
 
-def _capture_and_compare(step, bufs):
+def _capture_and_compare(step, bufs, nan_equal=False):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -114,7 +114,10 @@ def _capture_and_compare(step, bufs):
     graph.replay()
     torch.cuda.synchronize()
     for k in bufs:
-        assert torch.equal(bufs[k], eager[k]), k
+        if nan_equal:  # rows whose lse the forward skipped hold NaN in both runs
+            assert torch.equal(torch.nan_to_num(bufs[k], nan=-7.0), torch.nan_to_num(eager[k], nan=-7.0)), k
+        else:
+            assert torch.equal(bufs[k], eager[k]), k
     assert _lib.flce_device_status() == 0
 
 
@@ -150,6 +153,46 @@ def test_distillation_graph_replay_matches_eager():
 
     _capture_and_compare(kl_step, {k: v for k, v in bufs.items() if k != "klsm"})  # KL writes no kl_sm
     _capture_and_compare(jsd_step, bufs)
+
+
+def test_masked_distillation_graph_replay_matches_eager():
+    """KL and Jensen-Shannon distillation with ignored rows, captured: the
+    forwards skip them (rows listed and both heads gathered on the device)
+    and the backwards run over the compacted rows."""
+    N, Hs, Ht, V, cr = 2600, 192, 256, 2500, 512
+    s = WL.make_inputs(WL.custom("gmk_s", N, Hs, V, cr, w_std=0.05, targets="zipf", grpo_seqs=4, prompt_len=200,
+                                 seed=807))
+    tt = WL.make_inputs(WL.custom("gmk_t", N, Ht, V, cr, w_std=0.06, seed=808))
+    hs, Ws, t, w = upload(s)
+    ht, Wt, _, _ = upload(tt)
+    g = 1.0 / (N - 4 * 200)
+    ws_bytes = _lib.flce_kd_workspace_bytes(N, Hs, Ht, V, cr)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    bufs = dict(out=torch.empty(N, device="cuda"), lse_s=torch.empty(N, device="cuda"),
+                lse_t=torch.empty(N, device="cuda"), klsm=torch.empty(N, device="cuda"),
+                loss=torch.empty(1, device="cuda"), nv=torch.empty(1, dtype=torch.int64, device="cuda"),
+                dH=torch.empty_like(hs), dW=torch.empty((V, Hs), device="cuda"))
+    skip = _lib.FORWARD_SKIP_IGNORED
+
+    def kl_step():
+        a = _lib.flce_kd_forward_ex2(hs, Ws, Hs, ht, Wt, Ht, t, w, N, V, cr, -100, None, skip, bufs["out"],
+                                     bufs["lse_s"], bufs["lse_t"], bufs["loss"], bufs["nv"], ws, ws_bytes)
+        b = _lib.flce_kd_backward(hs, Ws, Hs, ht, Wt, Ht, t, w, bufs["lse_s"], bufs["lse_t"], g, bufs["dH"],
+                                  bufs["dW"], N, V, cr, -100, None, ws, ws_bytes)
+        return a | b
+
+    def jsd_step():
+        a = _lib.flce_jsd_forward_ex2(hs, Ws, Hs, ht, Wt, Ht, t, w, N, V, cr, -100, 0.3, None, skip, bufs["out"],
+                                      bufs["lse_s"], bufs["lse_t"], bufs["klsm"], bufs["loss"], bufs["nv"], ws,
+                                      ws_bytes)
+        b = _lib.flce_jsd_backward(hs, Ws, Hs, ht, Wt, Ht, t, w, bufs["lse_s"], bufs["lse_t"], bufs["klsm"], 0.3,
+                                   g, bufs["dH"], bufs["dW"], N, V, cr, -100, None, ws, ws_bytes)
+        return a | b
+
+    _capture_and_compare(kl_step, {k: v for k, v in bufs.items() if k != "klsm"}, nan_equal=True)
+    _capture_and_compare(jsd_step, bufs, nan_equal=True)
+    assert int(bufs["nv"]) == N - 4 * 200
+    assert bool(torch.isnan(bufs["lse_s"]).any())  # the forward did skip rows
 
 
 def test_e4m3_forward_graph_replay_matches_eager():
