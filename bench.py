@@ -477,7 +477,8 @@ def gpu_arm(args):
     peaks = load_peaks()
     # algorithmic FLOPs: every GEMM of the training step covers the
     # non-ignored rows only (the backward needs no ignored row's lse, and
-    # ignored rows have zero dlogits); the log-prob forward covers every row
+    # ignored rows have zero dlogits); so do the distillation steps, whose
+    # targets mask rows the same way.  --forward-only covers every row.
     nv = n_valid_host
     flops_step = {"fwd_logits_lse": 2.0 * nv * V * H, "bwd_dlogits": 2.0 * nv * V * H,
                   "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
@@ -488,12 +489,12 @@ def gpu_arm(args):
         flops_step = {"fwd_logits_lse": 2.0 * nv * V * H, "bwd_dH": 2.0 * nv * V * H,
                       "bwd_dW": 2.0 * nv * V * H}
     if Ht and args.jsd_beta:  # both heads twice in the forward (lse, then mixture terms)
-        flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "jsd_fwd_terms": 2.0 * N * V * (H + Ht),
-                      "jsd_bwd_dlogits": 2.0 * N * V * (H + Ht),
-                      "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
+        flops_step = {"kd_fwd_logits": 2.0 * nv * V * (H + Ht), "jsd_fwd_terms": 2.0 * nv * V * (H + Ht),
+                      "jsd_bwd_dlogits": 2.0 * nv * V * (H + Ht),
+                      "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     elif Ht:  # distillation: both heads in the forward and the dlogits recompute
-        flops_step = {"kd_fwd_logits": 2.0 * N * V * (H + Ht), "kd_bwd_dlogits": 2.0 * N * V * (H + Ht),
-                      "bwd_dH": 2.0 * N * V * H, "bwd_dW": 2.0 * N * V * H}
+        flops_step = {"kd_fwd_logits": 2.0 * nv * V * (H + Ht), "kd_bwd_dlogits": 2.0 * nv * V * (H + Ht),
+                      "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     kern = {}
     for k, (tot_ms, n) in prof.items():
         if n:
