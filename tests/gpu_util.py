@@ -2,6 +2,9 @@
 its C ABI, and compare with the oracle under the stated tolerances."""
 from __future__ import annotations
 
+import importlib.util
+import os
+
 import numpy as np
 import torch
 
@@ -84,3 +87,22 @@ def assert_grad_close(got: np.ndarray, ref: np.ndarray, what: str):
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     e = rel_fro(got, ref)
     assert e <= GRAD_RTOL, f"{what}: relative Frobenius error {e:.3e}"
+
+
+def _golden_module():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "make_full_forward_golden.py")
+    spec = importlib.util.spec_from_file_location("flce_full_forward_golden", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def load_golden(name: str) -> dict:
+    """The oracle's stored full forward of a workload (tests/golden/)."""
+    return _golden_module().load(name)
+
+
+def input_digest(inp) -> str:
+    """SHA-256 of a workload's generated inputs, as the golden files record it."""
+    return _golden_module().input_digest(inp)

@@ -1,10 +1,8 @@
 """GPU parity: libflce (through its C ABI) against the fp64 oracle on the same
-seeded inputs.  Small cases are compared element by element in full; the large
-workloads on seeded samples of rows (and, for dW, through its linearity in the
-per-row weights: with weights zero outside the sampled rows, dW must equal
-those rows' contribution, which the oracle computes from their own lse)."""
-import os
-
+seeded inputs.  Small cases and the 16,384-token SFT step are compared element
+by element in full.  The GRPO and long-context workloads compare every row's
+forward outputs with the oracle's stored full forward, dH on seeded sampled
+rows and dW on seeded sampled vocabulary rows."""
 import numpy as np
 import pytest
 import torch
@@ -13,8 +11,8 @@ from chunked_lm_head_gb300 import _lib
 from chunked_lm_head_gb300 import workloads as WL
 from oracle import flce_oracle as O
 
-from gpu_util import (LOSS_RTOL, assert_grad_close, assert_logp_close, np64, run_backward,
-                      run_forward, upload)
+from gpu_util import (GRAD_RTOL, LOSS_RTOL, assert_grad_close, assert_logp_close, input_digest,
+                      load_golden, np64, run_backward, run_forward, upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -131,8 +129,7 @@ def test_out_of_range_target():
     ref_lse = O.logsumexp_rows(O.logits(inp.h, inp.W))
     assert_logp_close(np64(lse), ref_lse, "lse")
     # validation mode rejects the call before any GEMM
-    os.environ["FLCE_VALIDATE"] = "1"
-    try:
+    with _lib.options(validate=1):
         N, H, V = 64, 64, 300
         out = torch.empty(N, dtype=torch.float32, device="cuda")
         st = _lib.flce_forward(h, W, t, None, N, H, V, 64, -100, out, None, None, None, None, 0)
@@ -142,8 +139,6 @@ def test_out_of_range_target():
         assert st == 2
         t[5] = 7
         assert _lib.flce_forward(h, W, t, None, N, H, V, 64, -100, out, None, None, None, None, 0) == 0
-    finally:
-        del os.environ["FLCE_VALIDATE"]
     assert _lib.flce_device_status() == 0
     assert ok.sum() == 63
 
@@ -174,14 +169,47 @@ def test_single_chunk_workload_full():
     _full_check(WL.make_inputs("single_chunk"), 256)
 
 
-def _large_check(name, n_rows, n_vocab, full_forward):
+def _sft_16k_oracle_in_full(inp, g, block_rows=2048):
+    """The oracle's forward and backward of every row, one logits block at a
+    time: lse, logp, dH rows and each block's contribution to dW (summed)."""
+    wl = inp.wl
+    lse = np.empty(wl.N)
+    logp = np.empty(wl.N)
+    dH = np.empty((wl.N, wl.H))
+    dW = np.zeros((wl.V, wl.H))
+    for r0 in range(0, wl.N, block_rows):
+        rows = np.arange(r0, min(wl.N, r0 + block_rows))
+        lse[rows], logp[rows], dH[rows], part = O.rows_all(inp.h, inp.W, inp.targets, rows,
+                                                            inp.weights, g=g)
+        dW += part
+    return lse, logp, dH, dW
+
+
+def _fro_rows(got_dev, ref, what, block=8192):
+    """Relative Frobenius error of a device matrix against an fp64 reference,
+    copied back a block of rows at a time."""
+    num = den = 0.0
+    for r0 in range(0, ref.shape[0], block):
+        a = np64(got_dev[r0:r0 + block])
+        assert np.all(np.isfinite(a)), f"{what}: non-finite values in rows {r0}.."
+        b = ref[r0:r0 + block]
+        num += float(np.sum((a - b) ** 2))
+        den += float(np.sum(b * b))
+    e = (num / den) ** 0.5
+    assert e <= GRAD_RTOL, f"{what}: relative Frobenius error {e:.3e}"
+
+
+def _large_check(name, n_rows, n_vocab):
     """Full-size workload in the launch configuration the benchmark times.
 
-    Always: n_valid exact; logp/lse and dH on seeded sampled rows; the loss
-    against the kernels' own per-token log-probs; dW on sampled vocabulary
-    rows through its linearity in the per-row weights.  With full_forward the
-    oracle also runs the whole forward: every row's logp/lse, the loss, and
-    dW (real weights) on the sampled vocabulary rows.
+    The 16,384-token SFT step is compared in full: every row's logp and lse,
+    the loss, every row of dH and every vocabulary row of dW.  The GRPO and
+    long-context workloads take the oracle's full forward from
+    tests/golden/ (written by tests/golden/make_full_forward_golden.py, which
+    calls only the oracle): every row's logp and lse, the loss and the
+    ignored-token count against it; dH on seeded sampled rows; and the
+    call's own dW on seeded sampled vocabulary rows, formed by the oracle from
+    its stored lse of every row.
     """
     inp = WL.make_inputs(name)
     wl = inp.wl
@@ -191,52 +219,53 @@ def _large_check(name, n_rows, n_vocab, full_forward):
     assert nv == int(m.sum())
     g = 1.0 / nv
     dH, dW = run_backward(h, W, t, w, lse, g, wl.chunk_rows)
+    lp, ls = np64(logp), np64(lse)
+    if name == "sft_16k":
+        ref_lse, ref_logp, ref_dH, ref_dW = _sft_16k_oracle_in_full(inp, g)
+        ref_loss = -float(np.sum(np.where(m, ref_logp, 0.0))) / nv
+        assert_logp_close(lp, ref_logp, "logp (all rows)")
+        assert_logp_close(ls, ref_lse, "lse (all rows)")
+        assert loss == pytest.approx(ref_loss, rel=LOSS_RTOL)
+        _fro_rows(dH, ref_dH, "dH (all rows)")
+        _fro_rows(dW, ref_dW, "dW (all vocabulary rows)")
+        return
+    gold = load_golden(name)
+    assert gold["meta"]["input_sha256"] == input_digest(inp), (
+        "this machine drew other inputs than the ones the stored oracle forward was computed on")
+    assert nv == gold["n_valid"]
+    assert_logp_close(lp, gold["logp"], "logp (all rows)")
+    assert_logp_close(ls, gold["lse"], "lse (all rows)")
+    assert loss == pytest.approx(gold["loss"], rel=LOSS_RTOL)
     rows = WL.sample_rows(wl.N, n_rows, seed=wl.seed)
     vrows = WL.sample_rows(wl.V, n_vocab, seed=wl.seed + 1)
-    lp, ls = np64(logp), np64(lse)
-    vsel = torch.from_numpy(vrows).cuda()
-    if full_forward:
-        ref = O.forward(inp.h, inp.W, inp.targets, inp.weights, chunk_rows=2048)
-        assert_logp_close(lp, ref.logp, "logp (all rows)")
-        assert_logp_close(ls, ref.lse, "lse (all rows)")
-        assert loss == pytest.approx(ref.loss, rel=LOSS_RTOL)
-        ref_dWv = O.vocab_rows_dW(inp.h, inp.W, inp.targets, ref.lse, vrows, inp.weights, g=g)
-        assert_grad_close(np64(dW[vsel]), ref_dWv, "dW (sampled vocabulary rows)")
-    ref_lse, ref_logp, ref_dH, ref_dWpart = O.rows_all(inp.h, inp.W, inp.targets, rows, inp.weights,
-                                                       g=g, vocab_rows=vrows)
-    assert_logp_close(lp[rows], ref_logp, "logp (sampled rows)")
-    assert_logp_close(ls[rows], ref_lse, "lse (sampled rows)")
-    wt = np.ones(wl.N) if inp.weights is None else inp.weights.astype(np.float64)
-    assert loss == pytest.approx(-np.sum(m * wt * lp) / nv, rel=LOSS_RTOL)
+    ref_lse, ref_logp, ref_dH, _ = O.rows_all(inp.h, inp.W, inp.targets, rows, inp.weights, g=g,
+                                              vocab_rows=vrows[:1])
+    assert_logp_close(ls[rows], ref_lse, "lse (sampled rows, recomputed)")
     assert_grad_close(np64(dH[torch.from_numpy(rows).cuda()]), ref_dH, "dH (sampled rows)")
-    assert np.all(np.isfinite(np64(dW[vsel])))
-    # dW through its linearity in the per-row weights
-    w0 = np.zeros(wl.N, dtype=np.float32)
-    w0[rows] = 1.0 if inp.weights is None else inp.weights[rows]
-    _, dW0 = run_backward(h, W, t, torch.from_numpy(w0).cuda(), lse, g, wl.chunk_rows, need_dH=False)
-    assert_grad_close(np64(dW0[vsel]), ref_dWpart, "dW (sampled rows x sampled vocabulary)")
+    ref_dWv = O.vocab_rows_dW(inp.h, inp.W, inp.targets, gold["lse"], vrows, inp.weights, g=g)
+    assert_grad_close(np64(dW[torch.from_numpy(vrows).cuda()]), ref_dWv, "dW (sampled vocabulary rows)")
 
 
 @pytest.mark.slow
-def test_sft_16k_full_forward():
-    _large_check("sft_16k", 1024, 512, full_forward=True)
+def test_sft_16k_in_full():
+    _large_check("sft_16k", 0, 0)
 
 
 @pytest.mark.slow
-def test_grpo_32k_sampled():
-    _large_check("grpo_32k", 4096, 512, full_forward=False)
+def test_grpo_32k_full_forward_sampled_backward():
+    _large_check("grpo_32k", 4096, 512)
 
 
 @pytest.mark.slow
-def test_long_131k_sampled():
-    _large_check("long_131k", 4096, 512, full_forward=False)
+def test_long_131k_full_forward_sampled_backward():
+    _large_check("long_131k", 4096, 512)
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_both_cta_group_paths(cg, monkeypatch):
+def test_both_cta_group_paths(cg, flce_opts):
     """Single-CTA tiles (FLCE_CTA_GROUP=1) and SM-pair tiles (the default) both
     match the oracle on a ragged multi-tile, multi-chunk case."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    flce_opts.set("cta_group", cg)
     wl = WL.custom(f"cg{cg}", 600, 264, 2100, 256, w_std=0.05, targets="zipf", ignore_frac=0.05,
                    seed=110)
     inp = WL.make_inputs(wl)
@@ -244,7 +273,7 @@ def test_both_cta_group_paths(cg, monkeypatch):
     _full_check(inp, 256)
 
 
-def test_row_compaction_matches_full_rows(monkeypatch):
+def test_row_compaction_matches_full_rows(flce_opts):
     """The backward on non-ignored rows only (default) against the backward
     over every row (FLCE_COMPACT=0) and the oracle, with a GRPO-like mask
     (prompt prefixes ignored) spanning several chunks and an empty last chunk."""
@@ -256,7 +285,7 @@ def test_row_compaction_matches_full_rows(monkeypatch):
     assert nv == 4 * 90
     g = 1.0 / nv
     dH_c, dW_c = run_backward(h, W, t, w, lse, g, 128)
-    monkeypatch.setenv("FLCE_COMPACT", "0")
+    flce_opts.set("compact", "0")
     dH_f, dW_f = run_backward(h, W, t, w, lse, g, 128)
     ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g)
     for name, got in (("dH compact", dH_c), ("dH full", dH_f)):
@@ -268,14 +297,14 @@ def test_row_compaction_matches_full_rows(monkeypatch):
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_forward_skipping_ignored_rows(cg, monkeypatch):
+def test_forward_skipping_ignored_rows(cg, flce_opts):
     """flce_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED: 5 forward launches of
     512 rows over the non-ignored rows (the third holds 256, the last two
     none), against the oracle.  Ignored rows get lse NaN and logp 0; the
     backward from that lse (compacted and over every row) matches the
     oracle."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
-    monkeypatch.setenv("FLCE_FWD_BLOCK_ROWS", "512")
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("fwd_block_rows", "512")
     wl = WL.custom("fskip", 2400, 192, 3100, 256, w_std=0.05, targets="zipf", grpo_seqs=4,
                    prompt_len=280, seed=112)
     inp = WL.make_inputs(wl)
@@ -299,7 +328,7 @@ def test_forward_skipping_ignored_rows(cg, monkeypatch):
     g = 1.0 / ref.n_valid
     refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=g)
     for compact in ("1", "0"):
-        monkeypatch.setenv("FLCE_COMPACT", compact)
+        flce_opts.set("compact", compact)
         dH, dW = run_backward(h, W, t, w, lse, g, 256)
         assert_grad_close(np64(dH), refb.dH, f"dH (compact {compact})")
         assert_grad_close(np64(dW), refb.dW, f"dW (compact {compact})")
@@ -308,7 +337,7 @@ def test_forward_skipping_ignored_rows(cg, monkeypatch):
     assert _lib.flce_forward_ex2(h, W, t, w, N, H, V, 256, -100, None, _lib.FORWARD_SKIP_IGNORED, logp, lse,
                                  loss, nv) == 0
     assert_logp_close(np64(lse), ref.lse, "lse (skipping off)")
-    monkeypatch.setenv("FLCE_COMPACT", "1")
+    flce_opts.set("compact", "1")
     n = 2000
     assert _lib.flce_forward_ex2(h[:n], W, t[:n], w[:n], n, H, V, 256, -100, None, _lib.FORWARD_SKIP_IGNORED,
                                  logp[:n], lse[:n], loss, nv) == 0
@@ -317,14 +346,14 @@ def test_forward_skipping_ignored_rows(cg, monkeypatch):
 
 
 @pytest.mark.parametrize("splits", ["1", "3", "7"])
-def test_forward_independent_of_vocabulary_splits(splits, monkeypatch):
+def test_forward_independent_of_vocabulary_splits(splits, flce_opts):
     """The split-V combine against a single split (and odd split counts):
     lse / logp agree to fp32 rounding and the loss to the loss tolerance."""
     wl = WL.custom("splits", 900, 192, 5000, 256, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=112)
     inp = WL.make_inputs(wl)
     h, W, t, w = upload(inp)
     logp0, lse0, loss0, nv0 = run_forward(h, W, t, w, 256)
-    monkeypatch.setenv("FLCE_FWD_SPLITS", splits)
+    flce_opts.set("fwd_splits", splits)
     logp1, lse1, loss1, nv1 = run_forward(h, W, t, w, 256)
     assert nv1 == nv0
     assert torch.allclose(lse1, lse0, atol=2e-5, rtol=0) and torch.allclose(logp1, logp0, atol=2e-5, rtol=0)
@@ -335,15 +364,15 @@ def test_forward_independent_of_vocabulary_splits(splits, monkeypatch):
 
 @pytest.mark.parametrize("compact", ["0", "1"])
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_backward_row_blocks_and_vocabulary_slabs(cg, compact, monkeypatch):
+def test_backward_row_blocks_and_vocabulary_slabs(cg, compact, flce_opts):
     """A 256-row dlogits budget walked as 768-row blocks x 5,120-column
     vocabulary slabs: 4 row blocks (the last 696 rows) x 4 slabs (the last
     4,640 columns), dH summed over the slabs in fp32 partials, dW
     read-modified-written once per row block; with and without row compaction,
     on both CTA-group paths."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
-    monkeypatch.setenv("FLCE_COMPACT", compact)
-    monkeypatch.setenv("FLCE_BWD_ROWS", "768")
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("compact", compact)
+    flce_opts.set("bwd_rows", "768")
     N, H, V, cr = 3000, 512, 20000, 256
     plan = _lib.flce_backward_plan(N, H, V, cr)
     assert (plan["rows_per_block"], plan["vocab_per_slab"]) == (768, 5120)
