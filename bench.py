@@ -185,16 +185,22 @@ def reference_arm(args):
     if rank != 0:
         return
     inp = WL.make_inputs(args.workload)
-    vals = []
+    vals, secs, rows = [], [], []
     info = None
     for i in range(args.warmup + args.steps):
         info = cpu_oracle_rate(inp, target_s=args.ref_step_s, max_rows=4096)
         if i >= args.warmup:
             vals.append(info["value"])
+            secs.append(info["seconds"])
+            rows.append(info["rows"])
     v = statistics.median(vals)
     wl = inp.wl
+    # one step of this arm is a bounded sample of the workload's rows, so its
+    # ms_per_step is the measured time of that sample (rows_per_step rows),
+    # not a time for all N rows
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.N / v * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
+            "rows_per_step": int(statistics.median(rows)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "V": wl.V,
@@ -576,7 +582,11 @@ def gpu_arm(args):
             "clocks": clocks,
             "e2e": None if e2e_ms is None else {
                 "value": whole_job_rate(N, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "boundary": "each step copies h, targets and weights from pinned host memory and "
+                            "reads loss and logp back; W stays resident (a model parameter) and "
+                            "dH, dW stay on the device (they feed the model's backward and the "
+                            "optimizer); no per-launch profiling events in this region"},
             "gpu_launches": gpu_launches,
             "fused_no_recompute": fused_line,
             "kernel_events": args.kernel_events,

@@ -8,4 +8,4 @@ from .api import (IGNORE_INDEX, DistillLoss, GRPOLoss, LinearCrossEntropy,  # no
                   LinearCrossEntropyLoss, SelectiveLogSoftmax,
                   backward, distill_loss, forward, forward_backward, grpo_loss, grpo_token_loss,
                   jsd_backward, jsd_forward, kd_backward, kd_forward, linear_cross_entropy,
-                  selective_log_softmax, workspace_bytes)
+                  scale_grads, selective_log_softmax, workspace_bytes)

@@ -83,6 +83,19 @@ SIGNATURES = {
     "flce_forward_backward_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64]),
     "flce_backward_plan": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int32,
                                           ctypes.c_int32, _c_vp]),
+    "flce_backward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp,
+                                         _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
+                                         ctypes.c_size_t, _c_vp]),
+    "flce_kd_backward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                            _c_vp, _c_vp, ctypes.c_float, _c_vp, _c_vp, _c_vp, _c_i64,
+                                            _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, ctypes.c_size_t, _c_vp]),
+    "flce_jsd_backward_ex2": (ctypes.c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp,
+                                             _c_vp, _c_vp, _c_vp, ctypes.c_float, ctypes.c_float, _c_vp,
+                                             _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
+                                             ctypes.c_size_t, _c_vp]),
+    "flce_scale_grads": (ctypes.c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp]),
+    "flce_set_option": (ctypes.c_int, [ctypes.c_int, _c_i64]),
+    "flce_get_option": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]),
     "flce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "flce_device_status": (ctypes.c_int, [_c_vp]),
     "flce_selftest_wait_timeout": (ctypes.c_int, [_c_i64, _c_vp]),
@@ -98,6 +111,20 @@ class LogitTransform(ctypes.Structure):
 
     _fields_ = [("scale_multiply", ctypes.c_float), ("scale_divide", ctypes.c_float),
                 ("softcap", ctypes.c_float), ("temperature", ctypes.c_float)]
+
+
+class DeviceScale(ctypes.Structure):
+    """flce_device_scale: a device fp32 scale and a device int64 count (each may be NULL)."""
+
+    _fields_ = [("scale", ctypes.c_void_p), ("count", ctypes.c_void_p)]
+
+
+def _dscale_ptr(scale, count):
+    """(pointer to a DeviceScale or None, the struct to keep alive)."""
+    if scale is None and count is None:
+        return None, None
+    d = DeviceScale(_ptr(scale), _ptr(count))
+    return ctypes.addressof(d), d
 
 
 def make_transform(tf) -> "LogitTransform | None":
@@ -243,6 +270,51 @@ def flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, c
                                 float(grad_scale), _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
                                 ignore_index, tp, _ptr(workspace), workspace_bytes,
                                 _stream_handle(stream))
+
+
+def flce_backward_ex2(h, W, targets, weights, lse, grad_scale, scale, count, dH, dW, N, H, V,
+                      chunk_rows, ignore_index, transform, workspace=None, workspace_bytes=0,
+                      stream=None) -> int:
+    """Raw C call with a device-side scale (scale: [1] fp32, count: [1] int64; each may be None)."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    dp, keep_d = _dscale_ptr(scale, count)
+    return lib.flce_backward_ex2(_ptr(h), _ptr(W), _ptr(targets), _ptr(weights), _ptr(lse),
+                                 float(grad_scale), dp, _ptr(dH), _ptr(dW), N, H, V, chunk_rows,
+                                 ignore_index, tp, _ptr(workspace), workspace_bytes,
+                                 _stream_handle(stream))
+
+
+def flce_kd_backward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, grad_scale,
+                         scale, count, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
+                         workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the distillation backward with a device-side scale."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    dp, keep_d = _dscale_ptr(scale, count)
+    return lib.flce_kd_backward_ex2(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                    _ptr(weights), _ptr(lse_s), _ptr(lse_t), float(grad_scale), dp,
+                                    _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows, ignore_index, tp,
+                                    _ptr(workspace), workspace_bytes, _stream_handle(stream))
+
+
+def flce_jsd_backward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, kl_sm, beta,
+                          grad_scale, scale, count, dH_s, dW_s, N, V, chunk_rows, ignore_index,
+                          transform, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Raw C call of the Jensen-Shannon backward with a device-side scale."""
+    lib = load()
+    tp, keep = _tf_ptr(transform)
+    dp, keep_d = _dscale_ptr(scale, count)
+    return lib.flce_jsd_backward_ex2(_ptr(h_s), _ptr(W_s), H_s, _ptr(h_t), _ptr(W_t), H_t, _ptr(targets),
+                                     _ptr(weights), _ptr(lse_s), _ptr(lse_t), _ptr(kl_sm), float(beta),
+                                     float(grad_scale), dp, _ptr(dH_s), _ptr(dW_s), N, V, chunk_rows,
+                                     ignore_index, tp, _ptr(workspace), workspace_bytes,
+                                     _stream_handle(stream))
+
+
+def flce_scale_grads(dH, n_dH, dW, n_dW, scale, stream=None) -> int:
+    """Raw C call: dH, dW *= *scale in place (scale a [1] fp32 device tensor)."""
+    return load().flce_scale_grads(_ptr(dH), n_dH, _ptr(dW), n_dW, _ptr(scale), _stream_handle(stream))
 
 
 def flce_kd_forward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, N, V, chunk_rows, ignore_index,
@@ -393,6 +465,44 @@ def flce_backward_plan(N, H, V, chunk_rows, workers=0, cta_group=0) -> dict:
     st = load().flce_backward_plan(N, H, V, chunk_rows, workers, cta_group, ctypes.addressof(info))
     check("flce_backward_plan", st)
     return {name: int(getattr(info, name)) for name, _ in BackwardPlanInfo._fields_}
+
+
+# flce_option values (include/flce.h), by lower-case name without the prefix
+OPTIONS = {
+    "cta_group": 0, "compact": 1, "validate": 2, "pdl": 3, "d_tma": 4, "wide_epilogue": 5,
+    "bwd_rows": 6, "fwd_splits": 7, "dh_splits": 8, "dh_group": 9, "fwd_block_rows": 10,
+    "skip_min_rows": 11,
+}
+
+
+def flce_set_option(name: str, value: int) -> None:
+    """Set a run-time option (e.g. "cta_group", "compact") for later calls."""
+    check("flce_set_option", load().flce_set_option(OPTIONS[name], int(value)))
+
+
+def flce_get_option(name: str) -> int:
+    v = ctypes.c_int64(0)
+    check("flce_get_option", load().flce_get_option(OPTIONS[name], ctypes.byref(v)))
+    return int(v.value)
+
+
+class options:
+    """Context manager: set options for a block, restore the previous values."""
+
+    def __init__(self, **values):
+        self.values = values
+        self.saved = {}
+
+    def __enter__(self):
+        for k, v in self.values.items():
+            self.saved[k] = flce_get_option(k)
+            flce_set_option(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            flce_set_option(k, v)
+        return False
 
 
 def flce_kd_workspace_bytes(N, H_s, H_t, V, chunk_rows) -> int:

@@ -57,19 +57,50 @@ def forward(h, W, targets, weights=None, chunk_rows: int = 256, ignore_index: in
     return {"logp": logp, "lse": lse, "loss": loss, "n_valid": n_valid}
 
 
+def _device_scalar(x, dtype, dev):
+    """A one-element device tensor of x (a tensor already there stays there: no
+    host synchronisation), or None."""
+    if x is None:
+        return None
+    return torch.as_tensor(x).to(device=dev, dtype=dtype).reshape(1).contiguous()
+
+
 def backward(h, W, targets, weights, lse, grad_scale: float, chunk_rows: int = 256,
              ignore_index: int = IGNORE_INDEX, need_dH: bool = True, need_dW: bool = True,
-             workspace: torch.Tensor | None = None, stream=None, transform=None):
-    """Returns (dH[N,H] bf16 or None, dW[V,H] f32 or None)."""
+             workspace: torch.Tensor | None = None, stream=None, transform=None,
+             scale=None, count=None):
+    """Returns (dH[N,H] bf16 or None, dW[V,H] f32 or None).
+
+    scale / count (optional, one-element device tensors, e.g. the incoming
+    gradient of the loss and the forward's n_valid) multiply grad_scale by
+    scale / max(count, 1) on the device."""
     _check(h, W, targets, weights)
     N, H = h.shape
     V = W.shape[0]
     dH = torch.empty_like(h) if need_dH else None
     dW = torch.empty((V, H), dtype=torch.float32, device=h.device) if need_dW else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
-                               ignore_index, transform, workspace, ws_bytes, stream)
-    _lib.check("flce_backward_ex", st)
+    scale = _device_scalar(scale, torch.float32, h.device)
+    count = _device_scalar(count, torch.int64, h.device)
+    if scale is None and count is None:
+        st = _lib.flce_backward_ex(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                                   ignore_index, transform, workspace, ws_bytes, stream)
+        _lib.check("flce_backward_ex", st)
+    else:
+        st = _lib.flce_backward_ex2(h, W, targets, weights, lse, grad_scale, scale, count, dH, dW, N, H,
+                                    V, chunk_rows, ignore_index, transform, workspace, ws_bytes, stream)
+        _lib.check("flce_backward_ex2", st)
+    return dH, dW
+
+
+def scale_grads(dH, dW, scale, stream=None):
+    """dH, dW *= scale in place (scale: a one-element device tensor; a scale of
+    exactly 1 moves no data).  Returns (dH, dW)."""
+    dev = (dH if dH is not None else dW).device
+    s = _device_scalar(scale, torch.float32, dev)
+    st = _lib.flce_scale_grads(dH, 0 if dH is None else dH.numel(), dW, 0 if dW is None else dW.numel(), s,
+                               stream)
+    _lib.check("flce_scale_grads", st)
     return dH, dW
 
 
@@ -124,11 +155,10 @@ class LinearCrossEntropy(torch.autograd.Function):
     def backward(ctx, grad_loss, grad_logp, grad_n):
         h, W, targets, weights, lse, n_valid = ctx.saved_tensors
         weights = weights if ctx.has_weights else None
-        n = int(n_valid.item())
-        g = float(grad_loss.item()) / n if n > 0 else 0.0
-        dH, dW = backward(h, W, targets, weights, lse, g, ctx.chunk_rows, ctx.ignore_index,
+        # grad_loss / n_valid is applied on the device: no host synchronisation
+        dH, dW = backward(h, W, targets, weights, lse, 1.0, ctx.chunk_rows, ctx.ignore_index,
                           need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
-                          transform=ctx.transform)
+                          transform=ctx.transform, scale=grad_loss, count=n_valid)
         return dH, dW, None, None, None, None, None
 
 
@@ -150,10 +180,10 @@ class LinearCrossEntropyOneCall(torch.autograd.Function):
     def backward(ctx, grad_loss, grad_logp, grad_n):
         dH, dW = ctx.grads
         ctx.grads = None
-        s = float(grad_loss.item())
-        if s != 1.0:  # e.g. a loss scale or a weighted sum of losses
-            dH = None if dH is None else dH * s
-            dW = None if dW is None else dW * s
+        # e.g. a loss scale or a weighted sum of losses; read on the device
+        # (no host synchronisation; a gradient of exactly 1 moves no data)
+        if dH is not None or dW is not None:
+            scale_grads(dH, dW, grad_loss)
         return dH, dW, None, None, None, None, None
 
 
@@ -274,11 +304,9 @@ class GRPOLoss(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_loss, grad_logp):
         h, W, targets, lse, weights, n_valid = ctx.saved_tensors
-        n = int(n_valid.item())
-        g = float(grad_loss.item()) / n if n > 0 else 0.0
-        dH, dW = backward(h, W, targets, weights, lse, g, ctx.chunk_rows, ctx.ignore_index,
+        dH, dW = backward(h, W, targets, weights, lse, 1.0, ctx.chunk_rows, ctx.ignore_index,
                           need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
-                          transform=ctx.transform)
+                          transform=ctx.transform, scale=grad_loss, count=n_valid)
         return dH, dW, None, None, None, None, None, None, None, None, None, None
 
 
@@ -314,10 +342,8 @@ class GRPOLossOneCall(torch.autograd.Function):
     def backward(ctx, grad_loss, grad_logp):
         dH, dW = ctx.grads
         ctx.grads = None
-        s = float(grad_loss.item())
-        if s != 1.0:
-            dH = None if dH is None else dH * s
-            dW = None if dW is None else dW * s
+        if dH is not None or dW is not None:  # scaled on the device, no host synchronisation
+            scale_grads(dH, dW, grad_loss)
         return dH, dW, None, None, None, None, None, None, None, None, None, None
 
 
@@ -403,34 +429,41 @@ def jsd_forward(h_s, W_s, h_t, W_t, beta: float = 0.5, targets=None, weights=Non
 def jsd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, kl_sm, grad_scale: float, beta: float = 0.5,
                  targets=None, weights=None, chunk_rows: int = 256,
                  ignore_index: int = IGNORE_INDEX, transform=None, need_dH: bool = True,
-                 need_dW: bool = True, workspace: torch.Tensor | None = None, stream=None):
-    """Jensen-Shannon distillation backward: (dH_s bf16 or None, dW_s f32 or None)."""
+                 need_dW: bool = True, workspace: torch.Tensor | None = None, stream=None,
+                 scale=None, count=None):
+    """Jensen-Shannon distillation backward: (dH_s bf16 or None, dW_s f32 or None).
+    scale / count: device-side factors of grad_scale, as in backward()."""
     N, H_s, H_t, V = _check_heads(h_s, W_s, h_t, W_t)
     dH = torch.empty_like(h_s) if need_dH else None
     dW = torch.empty((V, H_s), dtype=torch.float32, device=h_s.device) if need_dW else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_jsd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, kl_sm,
-                                beta, grad_scale, dH, dW, N, V, chunk_rows, ignore_index, transform,
-                                workspace, ws_bytes, stream)
-    _lib.check("flce_jsd_backward", st)
+    scale = _device_scalar(scale, torch.float32, h_s.device)
+    count = _device_scalar(count, torch.int64, h_s.device)
+    st = _lib.flce_jsd_backward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t, kl_sm,
+                                    beta, grad_scale, scale, count, dH, dW, N, V, chunk_rows, ignore_index,
+                                    transform, workspace, ws_bytes, stream)
+    _lib.check("flce_jsd_backward_ex2", st)
     return dH, dW
 
 
 def kd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, grad_scale: float, targets=None, weights=None,
                 chunk_rows: int = 256, ignore_index: int = IGNORE_INDEX, transform=None,
                 need_dH: bool = True, need_dW: bool = True, workspace: torch.Tensor | None = None,
-                stream=None):
-    """Distillation backward: (dH_s bf16 or None, dW_s f32 or None)."""
+                stream=None, scale=None, count=None):
+    """Distillation backward: (dH_s bf16 or None, dW_s f32 or None).
+    scale / count: device-side factors of grad_scale, as in backward()."""
     N, H_s = h_s.shape
     H_t = h_t.shape[1]
     V = W_s.shape[0]
     dH = torch.empty_like(h_s) if need_dH else None
     dW = torch.empty((V, H_s), dtype=torch.float32, device=h_s.device) if need_dW else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _lib.flce_kd_backward(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t,
-                               grad_scale, dH, dW, N, V, chunk_rows, ignore_index, transform,
-                               workspace, ws_bytes, stream)
-    _lib.check("flce_kd_backward", st)
+    scale = _device_scalar(scale, torch.float32, h_s.device)
+    count = _device_scalar(count, torch.int64, h_s.device)
+    st = _lib.flce_kd_backward_ex2(h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s, lse_t,
+                                   grad_scale, scale, count, dH, dW, N, V, chunk_rows, ignore_index,
+                                   transform, workspace, ws_bytes, stream)
+    _lib.check("flce_kd_backward_ex2", st)
     return dH, dW
 
 
@@ -465,14 +498,14 @@ class DistillLoss(torch.autograd.Function):
         h_s, W_s, h_t, W_t, targets, weights, lse_s, lse_t, kl_sm, n_valid = ctx.saved_tensors
         targets = targets if ctx.has_targets else None
         weights = weights if ctx.has_weights else None
-        n = int(n_valid.item())
-        g = float(grad_loss.item()) / n if n > 0 else 0.0
-        need = dict(need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1])
+        # grad_loss / n_valid is applied on the device: no host synchronisation
+        need = dict(need_dH=ctx.needs_input_grad[0], need_dW=ctx.needs_input_grad[1],
+                    scale=grad_loss, count=n_valid)
         if ctx.beta is None:
-            dH, dW = kd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, g, targets, weights, ctx.chunk_rows,
+            dH, dW = kd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, 1.0, targets, weights, ctx.chunk_rows,
                                  ctx.ignore_index, ctx.transform, **need)
         else:
-            dH, dW = jsd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, kl_sm, g, ctx.beta, targets, weights,
+            dH, dW = jsd_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, kl_sm, 1.0, ctx.beta, targets, weights,
                                   ctx.chunk_rows, ctx.ignore_index, ctx.transform, **need)
         return dH, dW, None, None, None, None, None, None, None, None
 

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libflce.so")
 SOURCES = ["flce.cu"]
-HEADERS = ["ptx.cuh", "gemm.cuh", "small_kernels.cuh", "host_common.cuh", "plan.cuh", "launch.cuh"]
+HEADERS = ["ptx.cuh", "gemm.cuh", "small_kernels.cuh", "host_common.cuh", "options.cuh", "plan.cuh",
+           "launch.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

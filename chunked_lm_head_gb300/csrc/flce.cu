@@ -90,7 +90,7 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int cg = cta_group();
   const int workers = device_workers(cg);
-  // rows per forward launch (FLCE_FWD_BLOCK_ROWS; 0: all rows in one launch)
+  // rows per forward launch (FLCE_OPT_FWD_BLOCK_ROWS; 0: all rows in one launch)
   const long long fb = fwd_block_rows(N, BM * cg);
   const FwdPlan f = plan_forward_call(N, H, V, workers, BM * cg, partials_cap);
   const FwdLayout L = fwd_layout(N, f, H, skip_ignored ? fb : 0);
@@ -103,7 +103,7 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
   double* bsum = reinterpret_cast<double*>(wb + L.bsum);
   long long* bcnt = reinterpret_cast<long long*>(wb + L.bcnt);
   int* bad = reinterpret_cast<int*>(wb + L.bad);
-  const bool validate = validate_env();
+  const bool validate = validate_on();
   const int Ni = static_cast<int>(N);
 
   if (N > 0) {
@@ -217,12 +217,10 @@ flce_status flce_forward_ex(const flce_bf16* h, const flce_bf16* W, const int64_
 }  // extern "C"
 
 namespace {
-// fewest rows for which flce_forward_ex2 skips ignored rows (FLCE_SKIP_MIN_ROWS
-// overrides): below it the three extra launches cost more than the rows save
-int64_t skip_min_rows() {
-  if (const char* e = std::getenv("FLCE_SKIP_MIN_ROWS")) return std::max<int64_t>(0, std::atoll(e));
-  return 2048;
-}
+// fewest rows for which flce_forward_ex2 skips ignored rows (2,048;
+// FLCE_OPT_SKIP_MIN_ROWS overrides): below it the three extra launches cost
+// more than the rows save
+int64_t skip_min_rows() { return opt(FLCE_OPT_SKIP_MIN_ROWS); }
 }  // namespace
 
 extern "C" {
@@ -235,20 +233,21 @@ flce_status flce_forward_ex2(const flce_bf16* h, const flce_bf16* W, const int64
                              size_t workspace_bytes, void* stream) {
   (void)chunk_rows;
   if ((flags & ~static_cast<uint32_t>(FLCE_FORWARD_SKIP_IGNORED)) != 0) return FLCE_ERR_INVALID_ARG;
-  const bool skip = (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_env() && N >= skip_min_rows();
+  const bool skip = (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_on() && N >= skip_min_rows();
   return forward_impl(h, W, targets, weights, N, H, V, ignore_index, transform, out_logp, out_lse,
                       out_loss, out_n_valid, workspace, workspace_bytes, stream, kFwdPartialsCap, skip);
 }
 
 // The backward; count_scale (device int64, or NULL) divides grad_scale by
-// max(*count_scale, 1) on the device.
+// max(*count_scale, 1) on the device, and scale_dev (device fp32, or NULL)
+// multiplies it.
 static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
                                  const float* weights, const float* lse, float grad_scale,
                                  flce_bf16* dH, float* dW, int64_t N, int64_t H, int64_t V,
                                  int64_t chunk_rows, int64_t ignore_index,
                                  const flce_logit_transform* transform, void* workspace,
                                  size_t workspace_bytes, void* stream,
-                                 const long long* count_scale) {
+                                 const long long* count_scale, const float* scale_dev = nullptr) {
   if (!sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
   if (!transform_params(transform, tfp)) return FLCE_ERR_INVALID_ARG;
@@ -256,7 +255,8 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   if (N > 0 && (!h || !W || !targets || !lse)) return FLCE_ERR_INVALID_ARG;
   if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
   if (!aligned(h, 16) || !aligned(W, 16) || !aligned(dH, 16) || !aligned(dW, 16) ||
-      !aligned(targets, 8) || !aligned(weights, 4) || !aligned(lse, 4))
+      !aligned(targets, 8) || !aligned(weights, 4) || !aligned(lse, 4) || !aligned(count_scale, 8) ||
+      !aligned(scale_dev, 4))
     return FLCE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (N == 0) {
@@ -275,7 +275,7 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   uint16_t* Dbuf = reinterpret_cast<uint16_t*>(wb + L.D);
   float* dh_part = b.dh_f32 ? reinterpret_cast<float*>(wb + L.dh_part) : nullptr;
 
-  if (validate_env()) {
+  if (validate_on()) {
     int* bad = reinterpret_cast<int*>(wb + L.bad);
     FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
     prep_kernel<<<static_cast<int>(ceil_div(N, SMALL_THREADS)), SMALL_THREADS, 0, st>>>(
@@ -310,8 +310,9 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   base.lse = lse;
   base.grad_scale = grad_scale;
   base.count_scale = count_scale;
+  base.scale_dev = scale_dev;
   CUtensorMap D_st;  // D as a TMA store target: [R][ldD] bf16, 64 x 32 boxes
-  base.d_tma = d_tma_env() && make_map(&D_st, Dbuf, b.ldD, b.R, b.ldD, 64, 32) ? 1 : 0;
+  base.d_tma = d_tma_on() && make_map(&D_st, Dbuf, b.ldD, b.R, b.ldD, 64, 32) ? 1 : 0;
   base.ignore_index = ignore_index;
   base.D = Dbuf;
   base.dH = dH;
@@ -328,7 +329,7 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   // indices stay on the device; the kernels read each chunk's row count), so
   // ignored rows cost nothing in the three backward GEMMs.  Their dH rows are
   // zeroed up front.
-  const bool compact = compact_env();
+  const bool compact = compact_on();
   int* cidx = reinterpret_cast<int*>(wb + L.idx);
   int* cblk = reinterpret_cast<int*>(wb + L.blk);
   int* ccount = reinterpret_cast<int*>(wb + L.count);
@@ -429,6 +430,18 @@ flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W, const int64
                              size_t workspace_bytes, void* stream) {
   return backward_impl(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
                        ignore_index, transform, workspace, workspace_bytes, stream, nullptr);
+}
+
+flce_status flce_backward_ex2(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
+                              const float* weights, const float* lse, float grad_scale,
+                              const flce_device_scale* device_scale, flce_bf16* dH, float* dW,
+                              int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                              int64_t ignore_index, const flce_logit_transform* transform,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  const long long* count = device_scale ? reinterpret_cast<const long long*>(device_scale->count) : nullptr;
+  const float* scale = device_scale ? device_scale->scale : nullptr;
+  return backward_impl(h, W, targets, weights, lse, grad_scale, dH, dW, N, H, V, chunk_rows,
+                       ignore_index, transform, workspace, workspace_bytes, stream, count, scale);
 }
 
 flce_status flce_forward(const flce_bf16* h, const flce_bf16* W, const int64_t* targets,
@@ -587,13 +600,13 @@ static flce_status forward_backward_impl(const flce_bf16* h, const flce_bf16* W,
   float* wg = reinterpret_cast<float*>(wb + L.wg);
   const float* dl_weights = grpo ? wg : weights;
   const int Ni = static_cast<int>(N);
-  const bool validate = validate_env();
+  const bool validate = validate_on();
   // Row compaction: the blocks run over a permutation of the rows with the
   // non-ignored ones first.  A block's forward covers all its rows when the
   // caller asks for lse (defined for ignored rows too), else only the
   // non-ignored ones; its dH / dW GEMMs read the device-side count and cover
   // only the non-ignored rows.
-  const bool compact = compact_env();
+  const bool compact = compact_on();
   const bool fwd_valid_only = compact && out_lse == nullptr;
 
   if (validate) FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));
@@ -1045,7 +1058,7 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
     // the Jensen-Shannon pass: per-row partials of each column half of a
     // tile in a slot of their own (8 epilogue warps); pass 1 keeps 4 warps,
     // which timed as fast for its cheaper epilogue
-    const int jsd_parts = wide_epilogue_env() ? kJsdColParts : 1;
+    const int jsd_parts = wide_epilogue_on() ? kJsdColParts : 1;
     const int jsd_slots = f.S * jsd_parts;
     p.col_parts = 1;
     p.err = err;
@@ -1149,7 +1162,7 @@ flce_status flce_jsd_forward(const flce_bf16* h_s, const flce_bf16* W_s, int64_t
 }
 
 static bool distill_skip(uint32_t flags, int64_t N) {
-  return (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_env() && N >= skip_min_rows();
+  return (flags & FLCE_FORWARD_SKIP_IGNORED) != 0 && compact_on() && N >= skip_min_rows();
 }
 
 flce_status flce_kd_forward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
@@ -1191,7 +1204,12 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
                                     float grad_scale, flce_bf16* dH_s, float* dW_s, int64_t N,
                                     int64_t V, int64_t chunk_rows, int64_t ignore_index,
                                     const flce_logit_transform* transform, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
+                                    size_t workspace_bytes, void* stream,
+                                    const flce_device_scale* device_scale = nullptr) {
+  const long long* count_scale =
+      device_scale ? reinterpret_cast<const long long*>(device_scale->count) : nullptr;
+  const float* scale_dev = device_scale ? device_scale->scale : nullptr;
+  if (!aligned(count_scale, 8) || !aligned(scale_dev, 4)) return FLCE_ERR_UNSUPPORTED;
   if (!sizes_ok(N, H_s, V) || !sizes_ok(N, H_t, V)) return FLCE_ERR_INVALID_ARG;
   if (jsd && !(beta > 0.f && beta < 1.f)) return FLCE_ERR_INVALID_ARG;
   GemmParams tfp{};
@@ -1248,6 +1266,8 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
   base.lse = lse_s;
   base.lse_t = lse_t;
   base.grad_scale = grad_scale;
+  base.count_scale = count_scale;
+  base.scale_dev = scale_dev;
   base.ignore_index = ignore_index;
   base.D = Dbuf;
   base.dH = dH_s;
@@ -1266,7 +1286,7 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
   // Row compaction, as in the cross-entropy backward: where targets mark
   // ignored rows, the chunks run over the non-ignored rows of both heads
   // (gathered per chunk), and the ignored rows' dH is zeroed up front.
-  const bool compact = targets != nullptr && compact_env();
+  const bool compact = targets != nullptr && compact_on();
   int* cidx = reinterpret_cast<int*>(wb + L.idx);
   int* cblk = reinterpret_cast<int*>(wb + L.blk);
   int* ccount = reinterpret_cast<int*>(wb + L.count);
@@ -1392,6 +1412,51 @@ flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_s, int64_
                           workspace, workspace_bytes, stream);
 }
 
+flce_status flce_kd_backward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                 const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                 const int64_t* targets, const float* weights, const float* lse_s,
+                                 const float* lse_t, float grad_scale,
+                                 const flce_device_scale* device_scale, flce_bf16* dH_s, float* dW_s,
+                                 int64_t N, int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                 const flce_logit_transform* transform, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return distill_backward(false, 0.f, nullptr, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s,
+                          lse_t, grad_scale, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
+                          workspace, workspace_bytes, stream, device_scale);
+}
+
+flce_status flce_jsd_backward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                  const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                  const int64_t* targets, const float* weights, const float* lse_s,
+                                  const float* lse_t, const float* kl_sm, float beta, float grad_scale,
+                                  const flce_device_scale* device_scale, flce_bf16* dH_s, float* dW_s,
+                                  int64_t N, int64_t V, int64_t chunk_rows, int64_t ignore_index,
+                                  const flce_logit_transform* transform, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return distill_backward(true, beta, kl_sm, h_s, W_s, H_s, h_t, W_t, H_t, targets, weights, lse_s,
+                          lse_t, grad_scale, dH_s, dW_s, N, V, chunk_rows, ignore_index, transform,
+                          workspace, workspace_bytes, stream, device_scale);
+}
+
+flce_status flce_scale_grads(flce_bf16* dH, int64_t n_dH, float* dW, int64_t n_dW, const float* scale,
+                             void* stream) {
+  if (n_dH < 0 || n_dW < 0 || scale == nullptr || (n_dH > 0 && dH == nullptr) ||
+      (n_dW > 0 && dW == nullptr))
+    return FLCE_ERR_INVALID_ARG;
+  if (!aligned(dH, 16) || !aligned(dW, 16) || !aligned(scale, 4)) return FLCE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int grid = 8 * device_sms();
+  if (n_dH > 0) {
+    scale_bf16_kernel<<<grid, SMALL_THREADS, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(dH), n_dH, scale);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  if (n_dW > 0) {
+    scale_f32_kernel<<<grid, SMALL_THREADS, 0, st>>>(dW, n_dW, scale);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  return FLCE_OK;
+}
+
 size_t flce_grpo_workspace_bytes(int64_t N) {
   if (N < 0 || N >= INT_MAX) return 0;
   return 2 * align256(static_cast<size_t>(ceil_div(std::max<int64_t>(N, 1), SMALL_THREADS)) * 8);
@@ -1471,6 +1536,22 @@ flce_status flce_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
   return h_gave_up ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
+flce_status flce_set_option(flce_option o, int64_t value) {
+  const int i = static_cast<int>(o);
+  if (i < 0 || i >= FLCE_OPT_COUNT) return FLCE_ERR_INVALID_ARG;
+  if (value < kOptionDefs[i].lo || value > kOptionDefs[i].hi) return FLCE_ERR_INVALID_ARG;
+  init_options();
+  g_options[i].store(value);
+  return FLCE_OK;
+}
+
+flce_status flce_get_option(flce_option o, int64_t* value) {
+  const int i = static_cast<int>(o);
+  if (i < 0 || i >= FLCE_OPT_COUNT || value == nullptr) return FLCE_ERR_INVALID_ARG;
+  *value = opt(o);
+  return FLCE_OK;
+}
+
 flce_status flce_profile_enable(int enable) {
   for (auto& r : g_prof_pending) {
     cudaEventDestroy(r.a);
@@ -1517,19 +1598,20 @@ flce_status flce_profile_read(int kind, double* total_ms, int64_t* launches) {
 // ===========================================================================
 // Forward for callers that cannot allocate device memory.
 //
-// Some callers are not allowed to allocate at all: code that runs while a
-// CUDA graph is being captured (an allocation there would be recorded or is
-// forbidden), inference runtimes that own every byte of device memory through
-// a fixed pool, and callers that must keep a constant memory footprint.  This
-// entry point serves them: it takes the same inputs and outputs as
+// Some callers are not allowed to allocate at all: inference runtimes that
+// own every byte of device memory through a fixed pool of their own (any other
+// allocation breaks their accounting or fails outright), and services that
+// must keep a constant memory footprint from start-up on (an allocation on
+// the hot path could fail under memory pressure, or stall on the allocator).
+// This entry point serves them: it takes the same inputs and outputs as
 // flce_forward, but its scratch lives in one file-scope device array that the
 // library owns, so nothing is allocated or freed by any call.
 //
 // The array is a fixed 16 MiB, resident on every device that loads this
 // library until the process exits.  On the host its name is only a stand-in
-// for the device copy, never a device address: the address is looked up once
-// per device with cudaGetSymbolAddress (device code could name the array
-// directly, host code must not).
+// for the device copy, never a device address: the address is looked up with
+// cudaGetSymbolAddress once per device and context (device code could name
+// the array directly, host code must not).
 namespace {
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 }  // namespace
@@ -1538,11 +1620,43 @@ static __device__ __align__(256) unsigned char g_flce_static_scratch[kStaticScra
 
 namespace {
 constexpr int kMaxStaticScratchDevices = 128;
+struct StaticScratchSlot {
+  unsigned long long ctx_id = 0;  // context the address belongs to (0: none yet)
+  void* addr = nullptr;
+};
 std::mutex g_static_scratch_mu;
-void* g_static_scratch_addr[kMaxStaticScratchDevices];
+StaticScratchSlot g_static_scratch[kMaxStaticScratchDevices];
 
-// Device address of g_flce_static_scratch on the current device (looked up on
-// the first call per device, with that device current).
+// Unique id of the calling thread's current context (cuCtxGetId), or 0 when
+// there is none yet.  A context rebuilt after a reset gets a new id, and a
+// module reload in it may put the array at another address.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_flce_static_scratch in the current device's context.
+// Set-up runs once per device and context: on the first call with that
+// device current, and again only if the context was rebuilt since (a device
+// reset), since the array may then sit at another address.
 flce_status static_scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -1550,17 +1664,23 @@ flce_status static_scratch_address(void** out) {
     return FLCE_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxStaticScratchDevices) return FLCE_ERR_UNSUPPORTED;
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return FLCE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (g_static_scratch_addr[dev] == nullptr) {
+  StaticScratchSlot& slot = g_static_scratch[dev];
+  if (id == 0 || slot.addr == nullptr || slot.ctx_id != id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_flce_static_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return FLCE_ERR_CUDA;
     }
-    g_static_scratch_addr[dev] = p;
+    // the lookup creates the device's primary context if there was none
+    if (id == 0 && (!current_context_id(&id) || id == 0)) return FLCE_ERR_CUDA;
+    slot.ctx_id = id;
+    slot.addr = p;
   }
-  *out = g_static_scratch_addr[dev];
+  *out = slot.addr;
   return FLCE_OK;
 }
 }  // namespace

@@ -191,12 +191,23 @@ struct GemmParams {
   // FUSED_FWD: per row and 32-column chunk, the chunk's maximum transformed
   // logit x log2(e), [rows_cap][ldD / 32]; the exponentials go to D
   float* mx;
-  // DLOGITS: divide grad_scale by max(*count_scale, 1) (a count on the device)
+  // dlogits modes: divide grad_scale by max(*count_scale, 1) (a count on the
+  // device) and multiply it by *scale_dev (a scale on the device), when set
   const long long* count_scale;
+  const float* scale_dev;
   // DLOGITS: write D through tmC (bf16 [rows_cap][ldD], 64 x 32 boxes) from
   // shared memory instead of per-thread global stores
   int d_tma;
 };
+
+// grad_scale of the dlogits modes with its device-side factors: / max(count, 1)
+// and * scale, each when given.
+__device__ __forceinline__ float device_grad_scale(const GemmParams& p) {
+  float g = p.grad_scale;
+  if (p.count_scale != nullptr) g *= 1.f / fmaxf(1.f, static_cast<float>(*p.count_scale));
+  if (p.scale_dev != nullptr) g *= *p.scale_dev;
+  return g;
+}
 
 // Problem extents that depend on the device-side row count of a compacted pass.
 struct DynShape {
@@ -622,9 +633,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
           tgt = p.targets[grow];
           const bool valid = tgt != p.ignore_index;
           const float w = p.weights ? p.weights[grow] : 1.f;
-          const float inv_count =
-              p.count_scale != nullptr ? 1.f / fmaxf(1.f, static_cast<float>(*p.count_scale)) : 1.f;
-          scale = valid ? w * p.grad_scale * inv_count : 0.f;
+          scale = valid ? w * device_grad_scale(p) : 0.f;
           nl2 = -p.lse[grow] * kLog2e;
         }
       }
@@ -632,7 +641,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
         if (row_ok) {
           const bool valid = p.targets == nullptr || p.targets[grow] != p.ignore_index;
           const float w = p.weights ? p.weights[grow] : 1.f;
-          scale = valid ? w * p.grad_scale : 0.f;
+          scale = valid ? w * device_grad_scale(p) : 0.f;
           nl2 = -p.lse[grow] * kLog2e;
           nlt = -p.lse_t[grow] * kLog2e;
           if constexpr (MODE == MODE_JSD_DLOGITS) klsm = p.kl_sm[grow];

@@ -59,25 +59,19 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer
                     box_outer);
 }
 
-// Programmatic dependent launch of the GEMMs (default; FLCE_PDL=0 turns it
-// off): a GEMM may be scheduled while the previous kernel of the stream
+// Programmatic dependent launch of the GEMMs (default; FLCE_OPT_PDL = 0 turns
+// it off): a GEMM may be scheduled while the previous kernel of the stream
 // drains, runs its prologue (barriers, TMEM, descriptor prefetch) and then
 // waits in griddepcontrol.wait until that kernel has completed.  Each GEMM
 // grid fits on the GPU at once, so the waiting CTAs never hold SMs that the
 // kernel they wait for still needs.
-bool pdl_env() {
-  const char* s = std::getenv("FLCE_PDL");
-  return !(s != nullptr && s[0] == '0');
-}
+bool pdl_on() { return opt_on(FLCE_OPT_PDL); }
 
 // The two-head dlogits GEMMs and the Jensen-Shannon forward terms
-// (distillation) run 8 epilogue warps (default; FLCE_WIDE_EPILOGUE=0 keeps
-// 4): their tile fills TMEM, so the epilogue does not overlap the next tile's
+// (distillation) run 8 epilogue warps (default; FLCE_OPT_WIDE_EPILOGUE = 0
+// keeps 4): their tile fills TMEM, so the epilogue does not overlap the next tile's
 // MMAs and its length adds to each tile's.
-bool wide_epilogue_env() {
-  const char* s = std::getenv("FLCE_WIDE_EPILOGUE");
-  return !(s != nullptr && s[0] == '0');
-}
+bool wide_epilogue_on() { return opt_on(FLCE_OPT_WIDE_EPILOGUE); }
 
 // Launch on `grid` CTAs in clusters of `cluster` with the GEMMs' attributes.
 template <class Kern, class... Args>
@@ -97,7 +91,7 @@ cudaError_t launch_persistent(Kern k, int grid, int cluster, int threads, int sm
     attr[n].val.clusterDim.z = 1;
     ++n;
   }
-  if (pdl_env()) {
+  if (pdl_on()) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
@@ -141,7 +135,7 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
     // parts it chose
     const bool wide = MODE == MODE_DW       ? p.k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_JSD_FWD ? p.col_parts == 2
-                                             : wide_epilogue_env();
+                                             : wide_epilogue_on();
     if (wide) {
       constexpr int EW = 2 * EPI_WARPS;
       if (cg == 2)
@@ -174,11 +168,9 @@ cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUte
                : go(flce_gemm_kernel<MODE_FWD, false, 1, true>, TileCfg<1>::SMEM, 1);
 }
 
-// CTA group of the GEMMs: 2 (SM pairs, 256-row tiles) unless FLCE_CTA_GROUP=1.
-int cta_group() {
-  const char* s = std::getenv("FLCE_CTA_GROUP");
-  return (s != nullptr && s[0] == '1') ? 1 : 2;
-}
+// CTA group of the GEMMs: 2 (SM pairs, 256-row tiles) unless
+// FLCE_OPT_CTA_GROUP = 1.
+int cta_group() { return opt(FLCE_OPT_CTA_GROUP) == 1 ? 1 : 2; }
 
 // Persistent workers the GPU holds at once: CTAs, or co-resident CTA pairs.
 int device_workers(int cg) {
@@ -215,23 +207,15 @@ int device_workers(int cg) {
   return n;
 }
 
-// Backward on non-ignored rows only (default); FLCE_COMPACT=0 runs every row.
-bool compact_env() {
-  const char* s = std::getenv("FLCE_COMPACT");
-  return !(s != nullptr && s[0] == '0');
-}
+// Backward on non-ignored rows only (default); FLCE_OPT_COMPACT = 0 runs
+// every row.
+bool compact_on() { return opt_on(FLCE_OPT_COMPACT); }
 
 // DLOGITS writes D through TMA boxes (default) or per-thread stores
-// (FLCE_D_TMA=0).
-bool d_tma_env() {
-  const char* s = std::getenv("FLCE_D_TMA");
-  return !(s != nullptr && s[0] == '0');
-}
+// (FLCE_OPT_D_TMA = 0).
+bool d_tma_on() { return opt_on(FLCE_OPT_D_TMA); }
 
-bool validate_env() {
-  const char* s = std::getenv("FLCE_VALIDATE");
-  return s != nullptr && s[0] != '\0' && s[0] != '0';
-}
+bool validate_on() { return opt_on(FLCE_OPT_VALIDATE); }
 
 // Stream-ordered workspace: the caller's, or one allocated here and freed on
 // the same stream when the call ends.
@@ -306,16 +290,15 @@ flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, c
 
 // ---- stages shared by the entry points
 
-// Row tiles per dH raster group: 8 (FLCE_DH_GROUP overrides).  A wave of 76
+// Row tiles per dH raster group: 8 (FLCE_OPT_DH_GROUP overrides).  A wave of 76
 // units then covers 8 row tiles x ~9.5 column tiles, the fewest D and W
 // slices per wave.  On 16,384 x 4,096 x 151,936, interleaved runs timed the
 // step 1.3% faster than with all 16 row tiles (the dH launch itself took the
 // same time); a dH launch's DRAM bytes vary more between GPUs than between
 // the two groups.
 int dh_group_rows(int m_tiles) {
-  int g = 8;
-  if (const char* e = std::getenv("FLCE_DH_GROUP")) g = std::atoi(e);
-  return g > 0 ? std::min(g, m_tiles) : m_tiles;
+  const int64_t g = opt(FLCE_OPT_DH_GROUP);
+  return g > 0 ? static_cast<int>(std::min<int64_t>(g, m_tiles)) : m_tiles;
 }
 
 // dH and dW stages of the backward, shared by the cross-entropy and the

@@ -8,6 +8,7 @@
 #include <cstdlib>
 
 #include "host_common.cuh"
+#include "options.cuh"
 
 namespace {
 
@@ -25,15 +26,14 @@ constexpr size_t kFwdPartialsCap = size_t(256) << 20;
 // Rows per forward GEMM launch: one raster group of 16 row tiles (4,096 rows
 // on SM pairs).  Measured on 16,384 x 4,096 x 151,936: 11.3 ms per forward
 // in four such launches against 11.8 ms in one launch over all rows (whose
-// DRAM reads of W are twice as high).  FLCE_FWD_BLOCK_ROWS overrides it
+// DRAM reads of W are twice as high).  FLCE_OPT_FWD_BLOCK_ROWS overrides it
 // (rounded up to a tile; 0: all rows in one launch).
 long long fwd_block_rows(long long N, int tm) {
   N = std::max(1LL, N);
   long long b = 16LL * tm;
-  if (const char* e = std::getenv("FLCE_FWD_BLOCK_ROWS")) {
-    b = std::atoll(e);
-    if (b <= 0) return N;
-  }
+  const int64_t o = opt(FLCE_OPT_FWD_BLOCK_ROWS);
+  if (o == 0) return N;
+  if (o > 0) b = o;
   return std::min(N, round_up(b, tm));
 }
 
@@ -62,10 +62,11 @@ FwdPlan plan_forward(long long N, long long H, long long V, int workers, int tm,
       f.tps = tps;
     }
   }
-  // FLCE_FWD_SPLITS=s pins the number of vocabulary splits (tests compare
-  // split counts; results must not depend on them beyond fp32 rounding)
-  if (const char* e = std::getenv("FLCE_FWD_SPLITS")) {
-    const int want = std::max(1, std::min(std::min(std::atoi(e), f.n_tiles), smax));
+  // FLCE_OPT_FWD_SPLITS = s pins the number of vocabulary splits (tests
+  // compare split counts; results must not depend on them beyond fp32
+  // rounding)
+  if (const int64_t fs = opt(FLCE_OPT_FWD_SPLITS); fs > 0) {
+    const int want = std::max(1, std::min(std::min(static_cast<int>(fs), f.n_tiles), smax));
     f.tps = static_cast<int>(ceil_div(f.n_tiles, want));
     f.S = static_cast<int>(ceil_div(f.n_tiles, f.tps));
   }
@@ -113,12 +114,11 @@ constexpr double kPlanRmwExposed = 0.7;
 
 // Best dH k-split count for `tiles` output tiles and `kb` K blocks: the
 // fewest splits whose last wave is at least 90% full (splits keep >= 8 K
-// blocks each).  FLCE_DH_SPLITS overrides it in plans made after it is set.
+// blocks each).  FLCE_OPT_DH_SPLITS overrides it in plans made after it is
+// set.
 int dh_split_count(long long tiles, long long kb, int workers) {
-  if (const char* e = std::getenv("FLCE_DH_SPLITS")) {
-    const long long s = std::atoll(e);
-    if (s >= 1) return static_cast<int>(std::min<long long>({s, 16, std::max(1LL, kb / 8)}));
-  }
+  if (const long long s = opt(FLCE_OPT_DH_SPLITS); s >= 1)
+    return static_cast<int>(std::min<long long>({s, 16, std::max(1LL, kb / 8)}));
   int best_s = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= 16; ++s) {
@@ -211,12 +211,9 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
   return true;
 }
 
-// FLCE_BWD_ROWS=<rows> fixes the row block (clamped to the budget) instead of
-// the modelled choice.
-long long bwd_rows_env() {
-  const char* e = std::getenv("FLCE_BWD_ROWS");
-  return e != nullptr ? std::atoll(e) : 0;
-}
+// FLCE_OPT_BWD_ROWS = rows fixes the row block (clamped to the budget)
+// instead of the modelled choice.
+long long bwd_rows_forced() { return opt(FLCE_OPT_BWD_ROWS); }
 
 BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int workers,
                       int tm) {
@@ -231,7 +228,7 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
   };
   thread_local Key last{-1, -1, -1, -1, -1, -1, -1};
   thread_local BwdPlan last_plan;
-  const long long forced = bwd_rows_env();
+  const long long forced = bwd_rows_forced();
   if (last.N == N && last.H == H && last.V == V && last.R0 == R0 && last.forced == forced &&
       last.workers == workers && last.tm == tm)
     return last_plan;

@@ -546,6 +546,48 @@ __global__ void quantize_e4m3_rows_kernel(const uint16_t* __restrict__ x, long l
 // Self-test of the bounded wait: one warp waits on an mbarrier that nothing
 // arrives on, through the same wait routine the GEMM pipelines use, with a
 // short limit; it must give up, raise the device error word and return.
+// In-place scale of gradients by a scalar held in device memory (the
+// incoming gradient of a loss, without a host synchronisation).  A scale of
+// exactly 1 leaves the data untouched and moves no bytes.  Grid-stride over
+// 16-byte vectors, then a scalar tail.
+__global__ void scale_bf16_kernel(__nv_bfloat16* __restrict__ x, long long n, const float* __restrict__ scale) {
+  const float s = *scale;
+  if (s == 1.f) return;
+  const long long nv = n / 8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  uint4* xv = reinterpret_cast<uint4*>(x);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nv; i += stride) {
+    uint4 u = xv[i];
+    __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      b[j] = __floats2bfloat162_rn(f.x * s, f.y * s);
+    }
+    xv[i] = u;
+  }
+  for (long long i = nv * 8 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n; i += stride)
+    x[i] = __float2bfloat16_rn(__bfloat162float(x[i]) * s);
+}
+
+__global__ void scale_f32_kernel(float* __restrict__ x, long long n, const float* __restrict__ scale) {
+  const float s = *scale;
+  if (s == 1.f) return;
+  const long long nv = n / 4;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  float4* xv = reinterpret_cast<float4*>(x);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nv; i += stride) {
+    float4 v = xv[i];
+    v.x *= s;
+    v.y *= s;
+    v.z *= s;
+    v.w *= s;
+    xv[i] = v;
+  }
+  for (long long i = nv * 4 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n; i += stride)
+    x[i] *= s;
+}
+
 __global__ void wait_selftest_kernel(long long limit_cycles, int* err, int* gave_up) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;

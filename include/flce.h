@@ -248,6 +248,42 @@ FLCE_API flce_status flce_backward_ex(const flce_bf16* h, const flce_bf16* W,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * A gradient scale held in device memory, so that a caller can pass the
+ * incoming gradient of the loss and the count the forward produced without
+ * synchronising the host (no counterpart on the pages: the mean loss of the
+ * TRL and Unsloth loops divides by the token count; here the division happens
+ * on the device).  The dlogits are multiplied by
+ *   grad_scale * (*scale) / max(*count, 1),
+ * where a NULL scale or count stands for 1 (and no division).  Both are read
+ * by the kernels when they run, in stream order.
+ */
+typedef struct flce_device_scale {
+  const float* scale;    /* [1] fp32 device, 4-byte aligned, or NULL */
+  const int64_t* count;  /* [1] int64 device, 8-byte aligned, or NULL (e.g. out_n_valid) */
+} flce_device_scale;
+
+/* flce_backward_ex with D's scale grad_scale * (*scale) / max(*count, 1) from
+ * device memory (device_scale may be NULL: grad_scale alone).  For the
+ * gradient of the mean loss with an incoming gradient dLoss on the device:
+ * grad_scale = 1, scale = &dLoss, count = the forward's out_n_valid. */
+FLCE_API flce_status flce_backward_ex2(const flce_bf16* h, const flce_bf16* W,
+                                       const int64_t* targets, const float* weights,
+                                       const float* lse, float grad_scale,
+                                       const flce_device_scale* device_scale, flce_bf16* dH,
+                                       float* dW, int64_t N, int64_t H, int64_t V,
+                                       int64_t chunk_rows, int64_t ignore_index,
+                                       const flce_logit_transform* transform, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/* Multiply dH ([n_dH] bf16, rounded to nearest even) and dW ([n_dW] fp32) in
+ * place by *scale (a device fp32 scalar) -- e.g. gradients that
+ * flce_forward_backward computed for an incoming gradient of 1, once the
+ * real one is known on the device.  A scale of exactly 1 moves no data.
+ * Either array may be NULL with its count 0; arrays 16-byte aligned. */
+FLCE_API flce_status flce_scale_grads(flce_bf16* dH, int64_t n_dH, float* dW, int64_t n_dW,
+                                      const float* scale, void* stream);
+
+/*
  * Distillation: a student head (h_s [N,H_s], W_s [V,H_s]) learns a frozen
  * teacher head's (h_t [N,H_t], W_t [V,H_t]) token distribution.  Source: TRL
  * v1.13 article, speed & memory section: the distillation trainer computes
@@ -322,6 +358,18 @@ FLCE_API flce_status flce_kd_backward(const flce_bf16* h_s, const flce_bf16* W_s
                                       const flce_logit_transform* transform, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/* flce_kd_backward with D's scale grad_scale * (*scale) / max(*count, 1) from
+ * device memory (see flce_device_scale; NULL: grad_scale alone). */
+FLCE_API flce_status flce_kd_backward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                          const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                          const int64_t* targets, const float* weights,
+                                          const float* lse_s, const float* lse_t, float grad_scale,
+                                          const flce_device_scale* device_scale, flce_bf16* dH_s,
+                                          float* dW_s, int64_t N, int64_t V, int64_t chunk_rows,
+                                          int64_t ignore_index,
+                                          const flce_logit_transform* transform, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /*
  * Jensen-Shannon distillation.  Source: TRL v1.13 article, section "Other
  * changes in v1.13": a fused linear JSD loss is among TRL's fused losses; the
@@ -368,6 +416,19 @@ FLCE_API flce_status flce_jsd_backward(const flce_bf16* h_s, const flce_bf16* W_
                                        int64_t N, int64_t V, int64_t chunk_rows,
                                        int64_t ignore_index, const flce_logit_transform* transform,
                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* flce_jsd_backward with D's scale grad_scale * (*scale) / max(*count, 1)
+ * from device memory (see flce_device_scale; NULL: grad_scale alone). */
+FLCE_API flce_status flce_jsd_backward_ex2(const flce_bf16* h_s, const flce_bf16* W_s, int64_t H_s,
+                                           const flce_bf16* h_t, const flce_bf16* W_t, int64_t H_t,
+                                           const int64_t* targets, const float* weights,
+                                           const float* lse_s, const float* lse_t, const float* kl_sm,
+                                           float beta, float grad_scale,
+                                           const flce_device_scale* device_scale, flce_bf16* dH_s,
+                                           float* dW_s, int64_t N, int64_t V, int64_t chunk_rows,
+                                           int64_t ignore_index,
+                                           const flce_logit_transform* transform, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /*
  * GRPO per-token objective on the sampled tokens' log-probs.  Source: TRL
@@ -471,10 +532,12 @@ FLCE_API flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, 
  * Forward that allocates nothing (no counterpart on the source pages: the
  * method itself does not need it).
  *
- * For callers that may not allocate device memory at all -- code running
- * while a CUDA graph is captured, runtimes that hand out every byte of device
- * memory from their own fixed pool, callers that must keep a constant
- * footprint.  Same arguments and results as flce_forward with workspace =
+ * For callers that may not allocate device memory at all: runtimes that hand
+ * out every byte of device memory from a fixed pool of their own (an
+ * allocation behind their back breaks their accounting or fails), and
+ * services that must keep a constant footprint from start-up on (an
+ * allocation on the hot path could fail under memory pressure or stall on the
+ * allocator).  Same arguments and results as flce_forward with workspace =
  * NULL, except that no workspace is allocated: the call uses a 16 MiB scratch
  * array that the library keeps in device memory on every device that loads it,
  * for the life of the process.
@@ -482,15 +545,16 @@ FLCE_API flce_status flce_forward_e4m3(const uint8_t* h8, const float* h_scale, 
  *     splits; this call uses as many splits as fit in 16 MiB (results equal
  *     flce_forward's up to fp32 rounding of the split combine).  It returns
  *     FLCE_ERR_UNSUPPORTED, before any launch, only when one split does not
- *     fit: N above about 1.3 million rows.
- *   - The first call on each device looks up the array's device address (a
- *     one-time cudaGetSymbolAddress); make that first call outside any stream
- *     capture.
+ *     fit: about 12 bytes per row, so N above about 1.39 million rows.
+ *   - The first call on each device (and the first after the device's
+ *     context was rebuilt, e.g. by a reset) looks up the array's device
+ *     address with cudaGetSymbolAddress, which may also create the device's
+ *     primary context; make that first call before any stream capture.
  *   - All calls share the one array: calls whose kernels may overlap on the
  *     GPU (different streams without ordering between them) race on it and
  *     must not be issued.  Each call writes every scratch word it reads, so
  *     what an earlier call left there does not affect the result.
- *   - Calls no cudaMalloc/cudaFree or other allocating routine.
+ *   - Makes no cudaMalloc/cudaFree or other allocating call.
  */
 FLCE_API flce_status flce_forward_static_scratch(const flce_bf16* h, const flce_bf16* W,
                                                  const int64_t* targets, const float* weights,
@@ -533,6 +597,52 @@ FLCE_API const char* flce_status_string(flce_status s);
  * wait since the last call, FLCE_ERR_CUDA if the stream reports an error,
  * else FLCE_OK. */
 FLCE_API flce_status flce_device_status(void* stream);
+
+/*
+ * Run-time options (no counterpart on the source pages: they select among
+ * equivalent schedules of the same computation, or add checks).
+ *
+ * One process-wide table that every entry point reads when it is called.
+ * Each option starts from its environment variable (read once, when the
+ * library first consults an option), else from its built-in default; after
+ * that only flce_set_option changes it.  Results depend on no option beyond
+ * fp32 rounding of summation orders, except FLCE_OPT_VALIDATE (an extra
+ * check).  Setting an option while another host thread is inside a call is
+ * allowed but gives that call either value.
+ */
+typedef enum flce_option {
+  FLCE_OPT_CTA_GROUP = 0,   /* FLCE_CTA_GROUP: 2 = SM-pair GEMMs (default), 1 = one SM per tile */
+  FLCE_OPT_COMPACT,         /* FLCE_COMPACT: 1 = backwards (and flagged forwards) skip ignored
+                               rows (default), 0 = every row */
+  FLCE_OPT_VALIDATE,        /* FLCE_VALIDATE: 1 = check targets first (one stream sync;
+                               FLCE_ERR_BAD_TARGET), 0 = no check (default) */
+  FLCE_OPT_PDL,             /* FLCE_PDL: 1 = programmatic dependent launch of the GEMMs
+                               (default), 0 = plain stream order */
+  FLCE_OPT_D_TMA,           /* FLCE_D_TMA: 1 = dlogits written through TMA boxes (default),
+                               0 = per-thread stores */
+  FLCE_OPT_WIDE_EPILOGUE,   /* FLCE_WIDE_EPILOGUE: 1 = 8 epilogue warps in the two-head
+                               dlogits modes (default), 0 = 4 */
+  FLCE_OPT_BWD_ROWS,        /* FLCE_BWD_ROWS: backward row block R (clamped to the budget);
+                               0 = the planner's choice (default) */
+  FLCE_OPT_FWD_SPLITS,      /* FLCE_FWD_SPLITS: forward vocabulary splits; 0 = planner (default) */
+  FLCE_OPT_DH_SPLITS,       /* FLCE_DH_SPLITS: dH k-splits (1..16); 0 = planner (default) */
+  FLCE_OPT_DH_GROUP,        /* FLCE_DH_GROUP: row tiles per dH raster group (default 8);
+                               0 = all row tiles */
+  FLCE_OPT_FWD_BLOCK_ROWS,  /* FLCE_FWD_BLOCK_ROWS: rows per forward launch, rounded up to a
+                               tile; -1 = 16 row tiles (default), 0 = all rows in one launch */
+  FLCE_OPT_SKIP_MIN_ROWS,   /* FLCE_SKIP_MIN_ROWS: fewest rows for which a forward skips
+                               ignored rows (default 2,048) */
+  FLCE_OPT_COUNT
+} flce_option;
+
+/* Set option `opt` to `value` for every later call in this process.
+ * FLCE_ERR_INVALID_ARG (nothing changed) for an unknown option or a value
+ * outside the range listed above. */
+FLCE_API flce_status flce_set_option(flce_option opt, int64_t value);
+
+/* Current value of option `opt` into *value (a host pointer).
+ * FLCE_ERR_INVALID_ARG for an unknown option or a NULL value. */
+FLCE_API flce_status flce_get_option(flce_option opt, int64_t* value);
 
 /* Diagnostic of the kernels' bounded waits (failure detection without a GPU
  * fault).  Launches one warp that waits, through the same bounded-wait

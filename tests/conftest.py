@@ -21,3 +21,23 @@ def cuda_lib():
         pytest.skip("no CUDA device")
     from chunked_lm_head_gb300 import _lib
     return _lib.load()
+
+
+@pytest.fixture
+def flce_opts():
+    """Sets libflce run-time options for one test and restores them after it."""
+    from chunked_lm_head_gb300 import _lib
+
+    class _Opts:
+        def __init__(self):
+            self.saved = {}
+
+        def set(self, name, value):
+            if name not in self.saved:
+                self.saved[name] = _lib.flce_get_option(name)
+            _lib.flce_set_option(name, int(value))
+
+    o = _Opts()
+    yield o
+    for name, value in o.saved.items():
+        _lib.flce_set_option(name, value)

@@ -92,11 +92,11 @@ def test_backward_plan_prefers_row_blocks_over_literal_small_chunks():
     assert (q["row_blocks"], q["vocab_slabs"]) == (1, 1)
 
 
-def test_backward_plan_row_override(monkeypatch):
-    monkeypatch.setenv("FLCE_BWD_ROWS", "768")
+def test_backward_plan_row_override(flce_opts):
+    flce_opts.set("bwd_rows", "768")
     p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
     assert (p["rows_per_block"], p["vocab_per_slab"], p["row_blocks"], p["vocab_slabs"]) == (768, 5120, 4, 4)
-    monkeypatch.setenv("FLCE_BWD_ROWS", "100000")  # clamped to the problem, then to the budget
+    flce_opts.set("bwd_rows", "100000")  # clamped to the problem, then to the budget
     p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
     assert p["dlogits_bytes"] <= 256 * 20000 * 2 and p["rows_per_block"] <= 3072
 
@@ -167,3 +167,44 @@ def test_distillation_workspace_holds_the_backward_and_both_gathered_heads(lib, 
     p = _lib.flce_backward_plan(N, Hs, V, chunk)
     ws = _lib.flce_kd_workspace_bytes(N, Hs, Ht, V, chunk)
     assert ws >= p["workspace_bytes"] + p["rows_per_block"] * Ht * 2
+
+
+def test_options_round_trip_and_range_checks(lib, flce_opts):
+    # every option in the header's enum has a name here, and reads back what was set
+    for name in _lib.OPTIONS:
+        v = _lib.flce_get_option(name)
+        flce_opts.set(name, v)
+        assert _lib.flce_get_option(name) == v
+    flce_opts.set("cta_group", 1)
+    assert _lib.flce_get_option("cta_group") == 1
+    flce_opts.set("dh_group", 0)
+    assert _lib.flce_get_option("dh_group") == 0
+    # out-of-range values and unknown options change nothing
+    for name, bad in (("cta_group", 3), ("compact", 2), ("validate", -1), ("fwd_splits", 257),
+                      ("dh_splits", 17), ("fwd_block_rows", -2)):
+        before = _lib.flce_get_option(name)
+        assert lib.flce_set_option(_lib.OPTIONS[name], bad) == 1
+        assert _lib.flce_get_option(name) == before
+    v = ctypes.c_int64(0)
+    assert lib.flce_set_option(len(_lib.OPTIONS), 0) == 1
+    assert lib.flce_get_option(len(_lib.OPTIONS), ctypes.byref(v)) == 1
+    assert lib.flce_get_option(0, None) == 1
+
+
+def test_options_change_the_plan_without_the_environment(lib, flce_opts, monkeypatch):
+    # the environment is read once; later changes to it are not seen
+    p0 = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
+    monkeypatch.setenv("FLCE_BWD_ROWS", "768")
+    assert _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2) == p0
+    flce_opts.set("bwd_rows", 768)
+    assert _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)["rows_per_block"] == 768
+
+
+def test_option_names_follow_the_header_enum():
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    h = open(os.path.join(root, "include", "flce.h")).read()
+    body = h[h.index("typedef enum flce_option"):h.index("} flce_option;")]
+    names = [n.lower() for n in re.findall(r"FLCE_OPT_([A-Z_]+)[ ,=]", body) if n != "COUNT"]
+    assert [k for k, _ in sorted(_lib.OPTIONS.items(), key=lambda kv: kv[1])] == names

@@ -131,3 +131,78 @@ def test_loss_module_matches_the_function():
         grads.append((float(loss.detach()), hh.grad, WW.grad))
     assert grads[0][0] == grads[1][0]
     assert torch.equal(grads[0][1], grads[1][1]) and torch.equal(grads[0][2], grads[1][2])
+
+
+def test_autograd_backwards_do_not_synchronise_the_host():
+    """The incoming gradient of the loss and the token count reach the
+    kernels as device pointers: no backward of the autograd wrappers reads a
+    value back to the host (torch's sync debug mode raises if one does)."""
+    from gpu_util import to_dev_bf16
+    wl = WL.custom("nosync", 600, 256, 3000, 128, w_std=0.05, targets="zipf", grpo_seqs=2,
+                   prompt_len=60, seed=451)
+    inp = WL.make_inputs(wl)
+    h, W, t, _ = upload(inp)
+    adv = torch.from_numpy(np.random.default_rng(2).standard_normal(wl.N).astype(np.float32)).cuda()
+    ti = WL.make_inputs(WL.custom("nosync_t", 600, 128, 3000, 128, w_std=0.06, seed=452))
+    ht, Wt = to_dev_bf16(ti.h), to_dev_bf16(ti.W)
+    cases = [
+        lambda a, b: flce.linear_cross_entropy(a, b, t, None, 128)[0],
+        lambda a, b: flce.linear_cross_entropy(a, b, t, None, 2048, recompute=False)[0],
+        lambda a, b: flce.grpo_loss(a, b, t, adv, chunk_rows=128)[0],
+        lambda a, b: flce.grpo_loss(a, b, t, adv, chunk_rows=2048, recompute=False)[0],
+        lambda a, b: flce.distill_loss(a, b, ht, Wt, t, None, beta=None, chunk_rows=128),
+        lambda a, b: flce.distill_loss(a, b, ht, Wt, t, None, beta=0.5, chunk_rows=128),
+    ]
+    for k, f in enumerate(cases):
+        a, b = h.clone().requires_grad_(True), W.clone().requires_grad_(True)
+        loss = f(a, b)
+        torch.cuda.synchronize()
+        torch.cuda.set_sync_debug_mode("error")
+        try:
+            (0.5 * loss).backward()
+        finally:
+            torch.cuda.set_sync_debug_mode("default")
+        torch.cuda.synchronize()
+        assert a.grad is not None and b.grad is not None, k
+        assert torch.isfinite(a.grad.float()).all() and torch.isfinite(b.grad).all(), k
+        assert flce._lib.flce_device_status() == 0
+
+
+def test_device_side_scale_equals_the_host_scale():
+    """flce_backward_ex2 with grad_scale * scale / max(count, 1) read on the
+    device against flce_backward_ex with the same factor from the host; and
+    flce_scale_grads (a scale of 1 moves nothing, 0.25 scales exactly)."""
+    from chunked_lm_head_gb300 import _lib
+    wl = WL.custom("dscale", 500, 192, 2600, 128, w_std=0.05, targets="zipf", ignore_frac=0.1, seed=453)
+    inp = WL.make_inputs(wl)
+    h, W, t, _ = upload(inp)
+    out = flce.forward(h, W, t, None, 128)
+    nv = out["n_valid"]
+    s = torch.tensor([0.75], device="cuda")
+    dH1, dW1 = flce.backward(h, W, t, None, out["lse"], 2.0, 128, scale=s, count=nv)
+    dH0, dW0 = flce.backward(h, W, t, None, out["lse"], 2.0 * 0.75 / int(nv), 128)
+    assert rel_fro_t(dH1, dH0) <= 1e-6 and rel_fro_t(dW1, dW0) <= 1e-6
+    ref = O.backward(inp.h, inp.W, inp.targets, None, g=1.5 / int(nv))
+    assert_grad_close(np64(dH1), ref.dH, "dH")
+    assert_grad_close(np64(dW1), ref.dW, "dW")
+    # a zero count divides by 1
+    zero = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _, dWz = flce.backward(h, W, t, None, out["lse"], 2.0, 128, need_dH=False, scale=s, count=zero)
+    _, dWh = flce.backward(h, W, t, None, out["lse"], 1.5, 128, need_dH=False)
+    assert rel_fro_t(dWz, dWh) <= 1e-6
+    # in-place scaling by a device scalar
+    a, b = dH1.clone(), dW1.clone()
+    flce.scale_grads(a, b, torch.ones(1, device="cuda"))
+    assert torch.equal(a, dH1) and torch.equal(b, dW1)
+    flce.scale_grads(a, b, torch.full((1,), 0.25, device="cuda"))
+    assert torch.equal(a, (dH1.float() * 0.25).to(torch.bfloat16)) and torch.equal(b, dW1 * 0.25)
+    odd = torch.randn(1001, device="cuda")  # a scalar tail past the 16-byte vectors
+    o2 = odd.clone()
+    flce.scale_grads(None, o2, torch.full((1,), -3.0, device="cuda"))
+    assert torch.equal(o2, odd * -3.0)
+    assert _lib.flce_device_status() == 0
+
+
+def rel_fro_t(a, b):
+    a, b = a.double(), b.double()
+    return float((a - b).norm() / b.norm().clamp_min(1e-300))

@@ -29,18 +29,18 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_kd_parity(case, cg, monkeypatch):
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+def test_kd_parity(case, cg, flce_opts):
+    flce_opts.set("cta_group", cg)
     _kd_check(case)
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_kd_parity_row_blocks_and_vocabulary_slabs(cg, monkeypatch):
+def test_kd_parity_row_blocks_and_vocabulary_slabs(cg, flce_opts):
     """Distillation backward over 512-row blocks x 1,280-column vocabulary
     slabs (3 blocks, the last 76 rows; 5 slabs, the last 880 columns) inside a
     128-row dlogits budget."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
-    monkeypatch.setenv("FLCE_BWD_ROWS", "512")
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("bwd_rows", "512")
     case = (1100, 256, 384, 6000, 128, {"temperature": 1.3}, True)
     plan = flce._lib.flce_backward_plan(case[0], case[1], case[3], case[4])
     assert (plan["row_blocks"], plan["vocab_slabs"], plan["vocab_per_slab"]) == (3, 5, 1280)

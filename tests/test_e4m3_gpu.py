@@ -37,8 +37,8 @@ def test_quantiser_is_bit_exact():
 
 @pytest.mark.parametrize("cg", ["1", "2"])
 @pytest.mark.parametrize("shape,tfd", [((300, 192, 2100), None), ((520, 512, 3000), {"softcap": 20.0})])
-def test_e4m3_forward_parity(cg, shape, tfd, monkeypatch):
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+def test_e4m3_forward_parity(cg, shape, tfd, flce_opts):
+    flce_opts.set("cta_group", cg)
     N, H, V = shape
     wl = WL.custom("e4m3", N, H, V, 256, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=700 + N)
     inp = WL.make_inputs(wl)

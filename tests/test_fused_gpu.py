@@ -52,8 +52,8 @@ def _check(inp, chunk_rows, grad_scale=1.0, transform=None):
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_fused_single_block(cg, monkeypatch):
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+def test_fused_single_block(cg, flce_opts):
+    flce_opts.set("cta_group", cg)
     wl = WL.custom("fused1", 600, 256, 3000, 768, w_std=0.05, targets="zipf", ignore_frac=0.06, seed=501)
     inp = WL.make_inputs(wl)
     inp.weights = np.random.default_rng(31).uniform(0.3, 1.8, wl.N).astype(np.float32)
@@ -61,9 +61,9 @@ def test_fused_single_block(cg, monkeypatch):
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_fused_row_blocks_ragged(cg, monkeypatch):
+def test_fused_row_blocks_ragged(cg, flce_opts):
     """Two 2,048-row blocks (the last 952 rows) over V = 20,000."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    flce_opts.set("cta_group", cg)
     wl = WL.custom("fused2", 3000, 512, 20000, 2048, w_std=0.04, targets="zipf", ignore_frac=0.05, seed=502)
     _check(WL.make_inputs(wl), 2048)
 
@@ -110,13 +110,13 @@ def test_fused_all_rows_ignored_and_fallback_path():
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_fused_row_compaction_matches_the_full_rows(cg, monkeypatch):
+def test_fused_row_compaction_matches_the_full_rows(cg, flce_opts):
     """GRPO-style prompts (an ignored prefix of 690 rows in each of 4
     sequences of 1,500) over 2,048-row blocks.  Compacted, the blocks run over
     the non-ignored rows first: the second block mixes 1,192 of them with
     ignored rows, the ragged third holds ignored rows only.  Both the compacted
     and the full-row call match the oracle and each other."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+    flce_opts.set("cta_group", cg)
     wl = WL.custom("fused_cmp", 6000, 256, 9000, 2048, w_std=0.05, targets="zipf", grpo_seqs=4,
                    prompt_len=690, seed=506)
     inp = WL.make_inputs(wl)
@@ -124,10 +124,10 @@ def test_fused_row_compaction_matches_the_full_rows(cg, monkeypatch):
     dH, dW = _check(inp, 2048, grad_scale=1.5)
     ign = torch.from_numpy(inp.targets == WL.IGNORE_INDEX).cuda()
     assert float(dH[ign].float().abs().max()) == 0.0
-    monkeypatch.setenv("FLCE_COMPACT", "0")
+    flce_opts.set("compact", "0")
     h, W, t, w = upload(inp)
     logp0, lse0, loss0, nv0, dH0, dW0 = run_fused(h, W, t, w, 2048, grad_scale=1.5)
-    monkeypatch.delenv("FLCE_COMPACT")
+    flce_opts.set("compact", 1)
     logp1, lse1, loss1, nv1, _, _ = run_fused(h, W, t, w, 2048, grad_scale=1.5)
     assert nv0 == nv1 == 3240
     assert torch.allclose(lse1, lse0, atol=2e-5, rtol=0) and torch.allclose(logp1, logp0, atol=2e-5, rtol=0)
@@ -173,7 +173,7 @@ def test_fused_without_lse_skips_the_ignored_rows_forward():
 
 
 @pytest.mark.slow
-def test_fused_grpo_32k_row_compaction(monkeypatch):
+def test_fused_grpo_32k_row_compaction(flce_opts):
     """32,768 x 4,096 x 128,000 at 4,096-row blocks, 12.5 % of the rows in
     ignored prompts: the compacted call (the eighth block all ignored rows)
     against the full-row call."""
@@ -182,7 +182,7 @@ def test_fused_grpo_32k_row_compaction(monkeypatch):
     logp, lse, loss, nv, dH, dW = run_fused(h, W, t, w, 4096)
     ign = torch.from_numpy(inp.targets == WL.IGNORE_INDEX).cuda()
     assert nv == 28672 and float(dH[ign].float().abs().max()) == 0.0
-    monkeypatch.setenv("FLCE_COMPACT", "0")
+    flce_opts.set("compact", "0")
     logp0, lse0, loss0, nv0, dH0, dW0 = run_fused(h, W, t, w, 4096)
     assert nv0 == nv
     assert torch.allclose(lse, lse0, atol=2e-5, rtol=0) and torch.allclose(logp, logp0, atol=2e-5, rtol=0)

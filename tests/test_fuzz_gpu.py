@@ -35,11 +35,11 @@ def _cases(n, seed=900):
 
 
 @pytest.mark.parametrize("c", _cases(64), ids=lambda c: f"N{c['N']}H{c['H']}V{c['V']}c{c['chunk']}")
-def test_random_problem_matches_oracle(c, monkeypatch):
-    monkeypatch.setenv("FLCE_CTA_GROUP", c["cg"])
-    monkeypatch.setenv("FLCE_COMPACT", c["compact"])
+def test_random_problem_matches_oracle(c, flce_opts):
+    flce_opts.set("cta_group", c["cg"])
+    flce_opts.set("compact", c["compact"])
     if c["rows"]:
-        monkeypatch.setenv("FLCE_BWD_ROWS", str(c["rows"]))
+        flce_opts.set("bwd_rows", str(c["rows"]))
     wl = WL.custom("fuzz", c["N"], c["H"], c["V"], c["chunk"], w_std=0.1, ignore_frac=0.0, seed=c["seed"])
     inp = WL.make_inputs(wl)
     r = np.random.default_rng(c["seed"])
@@ -67,7 +67,7 @@ def test_random_problem_matches_oracle(c, monkeypatch):
         assert _lib.flce_device_status() == 0
         loss, nv = float(loss_t.item()), int(nv_t.item())
     elif c["seed"] % 2 == 0:  # the forward that skips ignored rows (their lse is NaN)
-        monkeypatch.setenv("FLCE_SKIP_MIN_ROWS", "0")  # at every size
+        flce_opts.set("skip_min_rows", "0")  # at every size
         logp = torch.empty(N, dtype=torch.float32, device="cuda")
         lse = torch.empty(N, dtype=torch.float32, device="cuda")
         loss_t = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -109,12 +109,12 @@ def _kd_cases(n, seed=950):
 
 
 @pytest.mark.parametrize("c", _kd_cases(24), ids=lambda c: f"N{c['N']}Hs{c['Hs']}Ht{c['Ht']}V{c['V']}b{c['jsd']}")
-def test_random_distillation_matches_oracle(c, monkeypatch):
+def test_random_distillation_matches_oracle(c, flce_opts):
     import chunked_lm_head_gb300 as flce
     from gpu_util import to_dev_bf16
-    monkeypatch.setenv("FLCE_CTA_GROUP", c["cg"])
-    monkeypatch.setenv("FLCE_COMPACT", c["compact"])  # masked backward: compacted rows or every row
-    monkeypatch.setenv("FLCE_WIDE_EPILOGUE", c["wide"])  # dlogits epilogue: 8 warps or 4
+    flce_opts.set("cta_group", c["cg"])
+    flce_opts.set("compact", c["compact"])  # masked backward: compacted rows or every row
+    flce_opts.set("wide_epilogue", c["wide"])  # dlogits epilogue: 8 warps or 4
     s = WL.make_inputs(WL.custom("kfs", c["N"], c["Hs"], c["V"], 256, w_std=0.1, seed=c["seed"]))
     t_ = WL.make_inputs(WL.custom("kft", c["N"], c["Ht"], c["V"], 256, w_std=0.12, seed=c["seed"] + 500))
     r = np.random.default_rng(c["seed"])

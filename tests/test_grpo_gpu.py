@@ -58,14 +58,14 @@ def test_grpo_on_policy_weights_are_the_advantages():
 
 @pytest.mark.parametrize("path", ["recompute", "one_call", "one_call_fallback", "one_call_in_row_order"])
 @pytest.mark.parametrize("transform", [None, {"temperature": 0.8}])
-def test_grpo_loss_through_the_head_matches_oracle(transform, path, monkeypatch):
+def test_grpo_loss_through_the_head_matches_oracle(transform, path, flce_opts):
     """4 sequences x 150 tokens, 40-token prompts masked, one advantage per
     sequence; old-policy and reference log-probs near the current ones.  The
     recomputing autograd path, and the one-call path (flce_grpo_forward_backward)
     on one 640-row block (with and without the row permutation) and on the
     forward + tiled backward of a 128-row budget."""
     if path == "one_call_in_row_order":
-        monkeypatch.setenv("FLCE_COMPACT", "0")
+        flce_opts.set("compact", "0")
     chunk = 1024 if path in ("one_call", "one_call_in_row_order") else 128
     wl = WL.custom("grpo_api", 600, 256, 3000, 128, w_std=0.05, targets="zipf", grpo_seqs=4,
                    prompt_len=40, seed=411)

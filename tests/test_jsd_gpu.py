@@ -58,18 +58,18 @@ def _jsd_check(case):
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_jsd_parity(case, cg, monkeypatch):
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+def test_jsd_parity(case, cg, flce_opts):
+    flce_opts.set("cta_group", cg)
     _jsd_check(case)
 
 
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_jsd_parity_row_blocks_and_vocabulary_slabs(cg, monkeypatch):
+def test_jsd_parity_row_blocks_and_vocabulary_slabs(cg, flce_opts):
     """The JSD backward over 512-row blocks x 1,280-column vocabulary slabs
     (3 blocks, the last 76 rows; 5 slabs, the last 880 columns) inside a
     128-row dlogits budget."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
-    monkeypatch.setenv("FLCE_BWD_ROWS", "512")
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("bwd_rows", "512")
     case = (1100, 256, 384, 6000, 128, 0.3, {"temperature": 1.3}, True)
     plan = flce._lib.flce_backward_plan(case[0], case[1], case[3], case[4])
     assert (plan["row_blocks"], plan["vocab_slabs"], plan["vocab_per_slab"]) == (3, 5, 1280)
@@ -92,15 +92,15 @@ def test_jsd_of_identical_heads_is_zero_and_symmetric_at_one_half():
 
 @pytest.mark.parametrize("beta", [None, 0.4])
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_distillation_forward_skipping_ignored_rows(beta, cg, monkeypatch):
+def test_distillation_forward_skipping_ignored_rows(beta, cg, flce_opts):
     """flce_kd_forward_ex2 / flce_jsd_forward_ex2 with FLCE_FORWARD_SKIP_IGNORED
     over 4 launches of 256 rows (the last holding fewer non-ignored rows, or
     none): KL or Jensen-Shannon values, loss and the counted rows' lse against
     the oracle, NaN lse on ignored rows, and the backwards from those lse
     (compacted and over every row) against the oracle."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
-    monkeypatch.setenv("FLCE_SKIP_MIN_ROWS", "0")
-    monkeypatch.setenv("FLCE_FWD_BLOCK_ROWS", "256")
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("skip_min_rows", "0")
+    flce_opts.set("fwd_block_rows", "256")
     N, Hs, Ht, V = 900, 192, 256, 2100
     si, ti = _heads(N, Hs, Ht, V, seed=733)
     targets = np.random.default_rng(8).integers(0, V, N).astype(np.int64)
@@ -133,7 +133,7 @@ def test_distillation_forward_skipping_ignored_rows(beta, cg, monkeypatch):
     else:
         refb = O.jsd_backward(si.h, si.W, ti.h, ti.W, beta, targets, weights, g=g, tf=tf)
     for compact in ("1", "0"):
-        monkeypatch.setenv("FLCE_COMPACT", compact)
+        flce_opts.set("compact", compact)
         if beta is None:
             dH, dW = flce.kd_backward(hs, Ws, ht, Wt, out["lse_s"], out["lse_t"], g, tg, w, 256, transform=tfd)
         else:

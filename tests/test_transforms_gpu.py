@@ -22,8 +22,8 @@ CASES = {
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", list(CASES))
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_transform_parity(name, cg, monkeypatch):
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
+def test_transform_parity(name, cg, flce_opts):
+    flce_opts.set("cta_group", cg)
     tfd = CASES[name]
     tf = O.LogitTransform(**tfd)
     wl = WL.custom(f"tf_{name}", 520, 192, 3100, 256, w_std=0.25, targets="zipf", ignore_frac=0.05,
@@ -46,12 +46,12 @@ def test_transform_parity(name, cg, monkeypatch):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("cg", ["1", "2"])
-def test_transform_parity_row_blocks_and_vocabulary_slabs(cg, monkeypatch):
+def test_transform_parity_row_blocks_and_vocabulary_slabs(cg, flce_opts):
     """Soft-cap + temperature through the backward's 512-row blocks x
     1,280-column vocabulary slabs (128-row dlogits budget; last slab 880
     columns, last block 76 rows)."""
-    monkeypatch.setenv("FLCE_CTA_GROUP", cg)
-    monkeypatch.setenv("FLCE_BWD_ROWS", "512")
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("bwd_rows", "512")
     tfd = CASES["softcap_temp"]
     tf = O.LogitTransform(**tfd)
     N, H, V = 1100, 192, 6000

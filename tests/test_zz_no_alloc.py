@@ -1,13 +1,17 @@
 """The allocation-free forward against the regular forward.
 
 flce_forward_static_scratch is for callers that may not allocate device
-memory (work recorded during CUDA graph capture, runtimes that own all device
-memory through a fixed pool): it runs the forward on a scratch array the
-library keeps in device memory instead of a caller-provided or stream-allocated
-workspace.  Here it must reproduce flce_forward, call after call, even though
-each call finds the previous call's leftovers in that shared scratch.
+memory (runtimes that own all device memory through a fixed pool of their own,
+services that must keep a constant footprint): it runs the forward on a scratch
+array the library keeps in device memory instead of a caller-provided or
+stream-allocated workspace.  Here it must reproduce flce_forward, call after
+call, even though each call finds the previous call's leftovers in that shared
+scratch, and it must leave the stream-ordered memory pool's high-water mark
+and torch's allocator where they were.
 
 This file is named so that pytest collects it last."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -50,6 +54,63 @@ def test_static_scratch_forward_matches_regular_forward_on_consecutive_calls():
         assert_logp_close(np64(logp), np64(ref_logp), "logp")
         assert_logp_close(np64(lse), np64(ref_lse), "lse")
         assert loss == pytest.approx(ref_loss, rel=LOSS_RTOL)
+
+
+# CUmemPool_attribute values (cuda.h): bytes in use, and its high-water mark
+_POOL_USED_MEM_CURRENT, _POOL_USED_MEM_HIGH = 7, 8
+
+
+class _StreamPool:
+    """The current device's stream-ordered memory pool (the one cudaMallocAsync
+    draws from), through the driver API."""
+
+    def __init__(self):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        self.pool = ctypes.c_void_p()
+        dev = torch.cuda.current_device()
+        assert self.cu.cuDeviceGetMemPool(ctypes.byref(self.pool), ctypes.c_int(dev)) == 0
+
+    def get(self, attr):
+        v = ctypes.c_uint64(0)
+        assert self.cu.cuMemPoolGetAttribute(self.pool, ctypes.c_int(attr), ctypes.byref(v)) == 0
+        return v.value
+
+    def reset_high(self):
+        v = ctypes.c_uint64(0)  # the high-water mark can only be reset, to zero
+        assert self.cu.cuMemPoolSetAttribute(self.pool, ctypes.c_int(_POOL_USED_MEM_HIGH),
+                                             ctypes.byref(v)) == 0
+
+
+def test_static_scratch_forward_allocates_nothing():
+    """The regular forward without a workspace raises the pool's high-water
+    mark (it allocates on the stream); the allocation-free forward, from its
+    second call on, leaves it and torch's allocator untouched."""
+    wl = WL.custom("noalloc_c", 2000, 256, 12000, 256, w_std=0.04, targets="zipf", ignore_frac=0.05,
+                   seed=203)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    ref = run_forward(h, W, t, w, wl.chunk_rows)
+    _forward_static(h, W, t, w, wl.chunk_rows)  # first call on the device: address set-up
+    torch.cuda.synchronize()
+    pool = _StreamPool()
+    pool.reset_high()
+    used0 = pool.get(_POOL_USED_MEM_CURRENT)
+    assert pool.get(_POOL_USED_MEM_HIGH) <= used0
+    run_forward(h, W, t, w, wl.chunk_rows)
+    torch.cuda.synchronize()
+    assert pool.get(_POOL_USED_MEM_HIGH) > used0  # the check sees a stream allocation
+    pool.reset_high()
+    used0 = pool.get(_POOL_USED_MEM_CURRENT)
+    alloc0, reserved0 = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
+    logp, lse, loss, nv = _forward_static(h, W, t, w, wl.chunk_rows)
+    torch.cuda.synchronize()
+    assert pool.get(_POOL_USED_MEM_HIGH) <= used0  # no allocation at any point of the call
+    assert pool.get(_POOL_USED_MEM_CURRENT) == used0
+    assert torch.cuda.memory_reserved() == reserved0
+    assert torch.cuda.memory_allocated() == alloc0
+    assert nv == ref[3]
+    assert_logp_close(np64(logp), np64(ref[0]), "logp")
+    assert loss == pytest.approx(ref[2], rel=LOSS_RTOL)
 
 
 def test_static_scratch_forward_at_the_16k_sft_shape():
