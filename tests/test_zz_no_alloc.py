@@ -99,18 +99,27 @@ def test_static_scratch_forward_allocates_nothing():
     run_forward(h, W, t, w, wl.chunk_rows)
     torch.cuda.synchronize()
     assert pool.get(_POOL_USED_MEM_HIGH) > used0  # the check sees a stream allocation
+    # the outputs are the caller's: allocated before the measured call
+    N, H, V = wl.N, wl.H, wl.V
+    logp = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    loss = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    nv = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    torch.cuda.synchronize()
     pool.reset_high()
     used0 = pool.get(_POOL_USED_MEM_CURRENT)
     alloc0, reserved0 = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
-    logp, lse, loss, nv = _forward_static(h, W, t, w, wl.chunk_rows)
+    st = _lib.flce_forward_static_scratch(h, W, t, w, N, H, V, wl.chunk_rows, -100, logp, lse, loss, nv)
     torch.cuda.synchronize()
+    assert st == 0, _lib.STATUS_NAMES.get(st)
     assert pool.get(_POOL_USED_MEM_HIGH) <= used0  # no allocation at any point of the call
     assert pool.get(_POOL_USED_MEM_CURRENT) == used0
     assert torch.cuda.memory_reserved() == reserved0
     assert torch.cuda.memory_allocated() == alloc0
-    assert nv == ref[3]
+    assert _lib.flce_device_status() == 0
+    assert int(nv.item()) == ref[3]
     assert_logp_close(np64(logp), np64(ref[0]), "logp")
-    assert loss == pytest.approx(ref[2], rel=LOSS_RTOL)
+    assert float(loss.item()) == pytest.approx(ref[2], rel=LOSS_RTOL)
 
 
 def test_static_scratch_forward_at_the_16k_sft_shape():
