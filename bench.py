@@ -81,12 +81,15 @@ def algorithmic_bytes_step(N: int, nv: int, H: int, V: int, chunk_rows: int,
     Lf = max(1, -(-forward_rows // 4096))
     W, hb, Db = V * H * 2.0, H * 2.0, V * 2.0
     dh_out = nv * H * 2.0 if (splits == 1 and S == 1) else nv * H * 4.0 * splits * (2 * S - 1)
-    return {
+    out = {
         "fwd_logits_lse": Lf * W + forward_rows * hb,
         "bwd_dlogits": B * W + S * nv * hb + nv * Db,
         "bwd_dH": nv * Db + B * W + dh_out,
         "bwd_dW": nv * Db + S * nv * hb + B * V * H * 4.0 + (B - 1) * V * H * 4.0,
     }
+    # a slab's dH and dW units in one launch (the library's default)
+    out["bwd_dH_dW"] = out["bwd_dH"] + out["bwd_dW"]
+    return out
 
 
 def whole_job_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
@@ -212,7 +215,7 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "kd_fwd_logits", "kd_bwd_dlogits",
+GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "bwd_dH_dW", "kd_fwd_logits", "kd_bwd_dlogits",
               "jsd_fwd_terms", "jsd_bwd_dlogits")
 
 
@@ -373,8 +376,8 @@ def gpu_arm(args):
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    # per-launch CUDA events inside the timed region (default), or only
-    # around it with the per-kernel events taken in a second pass
+    # per-launch CUDA events in a second pass of the same steps right after
+    # the timed region (default), or inside it (--kernel-events timed)
     events_in_timed = args.kernel_events == "timed"
     _lib.profile_enable(events_in_timed)
     e0.record(stream)
@@ -501,6 +504,8 @@ def gpu_arm(args):
     elif Ht:  # distillation: both heads in the forward and the dlogits recompute
         flops_step = {"kd_fwd_logits": 2.0 * nv * V * (H + Ht), "kd_bwd_dlogits": 2.0 * nv * V * (H + Ht),
                       "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
+    if "bwd_dH" in flops_step and "bwd_dW" in flops_step:  # one launch per slab for both
+        flops_step["bwd_dH_dW"] = flops_step["bwd_dH"] + flops_step["bwd_dW"]
     kern = {}
     for k, (tot_ms, n) in prof.items():
         if n:
@@ -544,7 +549,7 @@ def gpu_arm(args):
                          "peak_source": f"{peaks['source']}: measured hbm_gbs (copy bandwidth)"})
     # the metric counts 8 N V H per step (forward, recompute, dH, dW over every
     # row); the GEMMs execute the FLOPs of flops_step (non-ignored rows)
-    exec_tflops = sum(flops_step.values()) / (ms_step / 1e3) / 1e12
+    exec_tflops = sum(v for k, v in flops_step.items() if k != "bwd_dH_dW") / (ms_step / 1e3) / 1e12
     step_tflops = exec_tflops
     if not (Ht or args.forward_only or args.fused):
         step_tflops = 8.0 * N * V * H / (ms_step / 1e3) / 1e12
@@ -610,9 +615,11 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=12.0, help="target seconds of the CPU-oracle sample")
     ap.add_argument("--ref-step-s", type=float, default=8.0, help="reference arm: seconds per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-events", default="timed", choices=["timed", "separate"],
-                    help="per-launch CUDA events inside the timed steps (timed), or in a second "
-                         "pass of the same steps so that the timed steps run without them (separate)")
+    ap.add_argument("--kernel-events", default="separate", choices=["timed", "separate"],
+                    help="per-launch CUDA events in a second pass of the same K steps, right after "
+                         "the timed steps, so that the timed steps run as a user's would (separate, "
+                         "default: events between launches would serialise the GEMMs' programmatic "
+                         "dependent launches); or inside the timed steps (timed)")
     ap.add_argument("--transform", default="",
                     help="logit transform, e.g. softcap=30,temperature=0.7 (flce_*_ex path)")
     ap.add_argument("--forward-only", action="store_true",

@@ -328,8 +328,10 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   // Row compaction: the chunks run over the non-ignored rows (count and
   // indices stay on the device; the kernels read each chunk's row count), so
   // ignored rows cost nothing in the three backward GEMMs.  Their dH rows are
-  // zeroed up front.
-  const bool compact = compact_on();
+  // zeroed up front.  A problem of one row tile gains nothing from it (its
+  // GEMMs cover one tile of rows whatever the count), so it skips the listing
+  // and gathering launches.
+  const bool compact = compact_on() && N > tm;
   int* cidx = reinterpret_cast<int*>(wb + L.idx);
   int* cblk = reinterpret_cast<int*>(wb + L.blk);
   int* ccount = reinterpret_cast<int*>(wb + L.count);
@@ -606,7 +608,8 @@ static flce_status forward_backward_impl(const flce_bf16* h, const flce_bf16* W,
   // caller asks for lse (defined for ignored rows too), else only the
   // non-ignored ones; its dH / dW GEMMs read the device-side count and cover
   // only the non-ignored rows.
-  const bool compact = compact_on();
+  // (one row tile gains nothing from compaction: see backward_impl)
+  const bool compact = compact_on() && N > tm;
   const bool fwd_valid_only = compact && out_lse == nullptr;
 
   if (validate) FLCE_CUDA_TRY(cudaMemsetAsync(bad, 0, sizeof(int), st));

@@ -22,6 +22,9 @@
 //               side in TMEM; online log-sum-exp of both heads and the
 //               teacher-weighted logit difference
 //   KD_DLOGITS  distillation: D = (p_s - p_t) * m * w * g
+//   DHDW        the DH and DW units of one vocabulary slab in one launch (dH
+//               units first, then dW units): one launch's fixed cost per
+//               slab instead of two, and the dH and dW streams overlap
 //
 // Sources: Unsloth, "Reinforcement Learning GRPO with 7x longer context",
 // sections "Flattened sequence-length chunking" (chunk logits are
@@ -88,7 +91,10 @@ enum Mode : int {
   MODE_JSD_DLOGITS = 7,
   // forward that also keeps each row block's exp(logit - chunk max) in bf16
   // (and the chunk maxima) for a backward without the logits recompute
-  MODE_FUSED_FWD = 8
+  MODE_FUSED_FWD = 8,
+  // DH and DW of one slab in one launch: units [0, dH units) are DH units
+  // (operands tmA / tmB, output tmC), the rest DW units (tmA2 / tmB2, tmC2)
+  MODE_DHDW = 9
 };
 template <int MODE>
 __host__ __device__ constexpr bool is_kd() {
@@ -101,14 +107,15 @@ __host__ __device__ constexpr bool is_kd() {
 // forward's per-row partials of each half go to a slot of their own)
 template <int MODE>
 __host__ __device__ constexpr bool wide_epilogue_mode() {
-  return MODE == MODE_DW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS || MODE == MODE_JSD_FWD;
+  return MODE == MODE_DW || MODE == MODE_DHDW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS ||
+         MODE == MODE_JSD_FWD;
 }
 // modes whose accumulator rows are rows of h (all but dW, whose accumulator
 // rows are vocabulary rows): under row compaction they map through row_idx
-// and take their row count from the device
+// and take their row count from the device (DHDW: its DH units only)
 template <int MODE>
 __host__ __device__ constexpr bool rows_are_tokens() {
-  return MODE != MODE_DW;
+  return MODE != MODE_DW && MODE != MODE_DHDW;
 }
 // modes whose units are (row tile, vocabulary split) with per-row partials
 template <int MODE>
@@ -198,6 +205,9 @@ struct GemmParams {
   // DLOGITS: write D through tmC (bf16 [rows_cap][ldD], 64 x 32 boxes) from
   // shared memory instead of per-thread global stores
   int d_tma;
+  // DHDW: the DW units' grid (vocabulary tiles of the slab x hidden tiles,
+  // K = the block's rows, one split); the DH units use the fields above
+  int dw_m_tiles, dw_n_tiles, dw_k_blocks, dw_group_m;
 };
 
 // grad_scale of the dlogits modes with its device-side factors: / max(count, 1)
@@ -210,13 +220,31 @@ __device__ __forceinline__ float device_grad_scale(const GemmParams& p) {
 }
 
 // Problem extents that depend on the device-side row count of a compacted pass.
+// DHDW: m_tiles / k_blocks / kb_per_split are its DH units', dh_units of them,
+// followed by dw_units DW units of dw_k_blocks K blocks.
 struct DynShape {
   int rows, m_tiles, k_blocks, kb_per_split, num_units;
+  int dh_units, dw_units, dw_k_blocks;
 };
 
 template <int MODE, int TM>
 __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
-  DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units};
+  DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units, 0, 0, 0};
+  if constexpr (MODE == MODE_DHDW) {
+    if (p.dyn_count != nullptr) {
+      d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
+      d.m_tiles = (d.rows + TM - 1) / TM;
+      d.dw_k_blocks = (d.rows + BK - 1) / BK;
+    } else {
+      d.dw_k_blocks = p.dw_k_blocks;
+    }
+    d.dh_units = p.k_splits * d.m_tiles * p.cols;
+    // an empty first pass still writes zeros to dW, an empty later pass has
+    // nothing to add
+    d.dw_units = (d.rows == 0 && p.dW_accumulate) ? 0 : p.dw_m_tiles * p.dw_n_tiles;
+    d.num_units = d.dh_units + d.dw_units;
+    return d;
+  }
   if (p.dyn_count != nullptr) {
     d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
     if constexpr (rows_are_tokens<MODE>()) {
@@ -235,36 +263,54 @@ __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
 
 struct Unit {
   int m, n0, n1, kb0, kb1, split;
+  bool dw;  // DHDW: a DW unit
 };
 
-template <int MODE>
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape& d, int u) {
-  const int m_tiles = d.m_tiles;
-  const int group_m = min(p.group_m, max(m_tiles, 1));
-  const int per_split = m_tiles * p.cols;
+// Unit u of a grid of (k-splits x m_tiles x cols) units, rasterised in
+// groups of group_m row tiles that share their column units.
+__device__ __forceinline__ Unit decode_grid(int u, int m_tiles, int cols, int n_tiles, int n_per_unit,
+                                            int group_m_req, int kb_per_split, int k_blocks,
+                                            bool col_split) {
+  const int group_m = min(group_m_req, max(m_tiles, 1));
+  const int per_split = m_tiles * cols;
   const int ks = u / per_split;
   const int r = u - ks * per_split;
   const int full_groups = m_tiles / group_m;
   int first_m, gsize, local;
-  if (r < full_groups * group_m * p.cols) {
-    const int g = r / (group_m * p.cols);
+  if (r < full_groups * group_m * cols) {
+    const int g = r / (group_m * cols);
     first_m = g * group_m;
     gsize = group_m;
-    local = r - g * group_m * p.cols;
+    local = r - g * group_m * cols;
   } else {
     first_m = full_groups * group_m;
     gsize = m_tiles - first_m;
-    local = r - full_groups * group_m * p.cols;
+    local = r - full_groups * group_m * cols;
   }
   Unit t;
   t.m = first_m + local % gsize;
   const int c = local / gsize;
-  t.n0 = c * p.n_per_unit;
-  t.n1 = min(p.n_tiles, t.n0 + p.n_per_unit);
-  t.kb0 = ks * d.kb_per_split;
-  t.kb1 = min(d.k_blocks, t.kb0 + d.kb_per_split);
-  t.split = is_split_fwd<MODE>() ? c : ks;
+  t.n0 = c * n_per_unit;
+  t.n1 = min(n_tiles, t.n0 + n_per_unit);
+  t.kb0 = ks * kb_per_split;
+  t.kb1 = min(k_blocks, t.kb0 + kb_per_split);
+  t.split = col_split ? c : ks;
+  t.dw = false;
   return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape& d, int u) {
+  if constexpr (MODE == MODE_DHDW) {
+    if (u >= d.dh_units) {
+      Unit t = decode_grid(u - d.dh_units, p.dw_m_tiles, p.dw_n_tiles, p.dw_n_tiles, 1, p.dw_group_m,
+                           max(d.dw_k_blocks, 1), d.dw_k_blocks, false);
+      t.dw = true;
+      return t;
+    }
+  }
+  return decode_grid(u, d.m_tiles, p.cols, p.n_tiles, p.n_per_unit, p.group_m, d.kb_per_split, d.k_blocks,
+                     is_split_fwd<MODE>());
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
@@ -420,7 +466,8 @@ template <int MODE, bool kLong, int CG, bool kF8 = false, int EW = EPI_WARPS>
 __global__ void __launch_bounds__(gemm_threads(EW), 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
-                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC2,
+                     const __grid_constant__ GemmParams p) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   using C = TileCfg<CG>;
   constexpr int NST = C::NSTAGE;
@@ -465,7 +512,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (is_kd<MODE>()) {
+    if constexpr (is_kd<MODE>() || MODE == MODE_DHDW) {
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
     }
@@ -509,8 +556,16 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
             uint32_t fb = full_bar(stage);
             if constexpr (CG == 2) fb = mapa_shared(fb, 0);
             if (issuer) mbar_arrive_expect_tx(full_bar(stage), C::STAGE * CG);
-            load_stage<MODE, CG, kF8>(&tmA, &tmB, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
-                                      rank);
+            if constexpr (MODE == MODE_DHDW) {
+              if (t.dw)
+                load_stage<MODE_DW, CG>(&tmA2, &tmB2, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
+                                        rank);
+              else
+                load_stage<MODE_DH, CG>(&tmA, &tmB, &tmA, &tmB, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank);
+            } else {
+              load_stage<MODE, CG, kF8>(&tmA, &tmB, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
+                                        rank);
+            }
             ++issued;
             if (++stage == NST) {
               stage = 0;
@@ -551,6 +606,11 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
               const bool teacher = kb >= p.k_blocks_s;
               mma_stage<MODE, CG>(d_tmem + (teacher ? BN : 0), sA, sA + C::A_BYTES,
                                   kb == t.kb0 || kb == p.k_blocks_s);
+            } else if constexpr (MODE == MODE_DHDW) {
+              if (t.dw)
+                mma_stage<MODE_DW, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
+              else
+                mma_stage<MODE_DH, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
             } else {
               mma_stage<MODE, CG, kF8>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
             }
@@ -607,7 +667,9 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       // logit and the dlogits scale (soft-capped logits are formed explicitly)
       const float lin_a = p.tf_softcap ? 1.f : p.tf_a;
       const float l2a = kLog2e * lin_a;
-      if constexpr (MODE == MODE_DW) {
+      // DHDW: this unit's kind (a DW unit's accumulator rows are vocabulary rows)
+      const bool unit_dw = MODE == MODE_DW || (MODE == MODE_DHDW && t.dw);
+      if (unit_dw) {
         row_ok = lr < p.V;  // rows of the accumulator are vocabulary rows here
       } else {
         row_ok = lr < dsh.rows;
@@ -615,8 +677,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       // original row of this accumulator row (targets, weights, lse, dH;
       // the forward modes' partials and target logit)
       int grow = p.row0 + lr;
-      if constexpr (rows_are_tokens<MODE>()) {
-        if (p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
+      if constexpr (rows_are_tokens<MODE>() || MODE == MODE_DHDW) {
+        if (!unit_dw && p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
       }
       // DLOGITS also writes zero rows up to the next 64-row K block so that
       // the dW pass over this chunk reads zeros past its last row
@@ -974,7 +1036,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
                   *reinterpret_cast<uint4*>(dst + 8 * g) =
                       make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
             }
-          } else if (MODE == MODE_DH && p.dH_part == nullptr) {
+          } else if ((MODE == MODE_DH || (MODE == MODE_DHDW && !unit_dw)) && p.dH_part == nullptr) {
             if (row_ok) {  // the only pass over this row: bf16 dH directly
               uint16_t* dst = p.dH + static_cast<idx_t>(grow) * p.H + col0;
 #pragma unroll
@@ -984,7 +1046,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
                       pack_bf16x2(v[8 * g], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
                       pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
             }
-          } else {  // MODE_DW, or MODE_DH into fp32 partials
+          } else {  // MODE_DW, or MODE_DH into fp32 partials (DHDW: either unit kind)
             // stage this warp's 32 x 32 box (row = lane) in 128B-swizzled
             // shared memory, then one lane hands it to TMA: a plain store on
             // the first pass over the output, an fp32 reduce-add in L2
@@ -1004,7 +1066,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
               const int lrow0 = t.m * C::TM + rank * BM + q * 32;  // first accumulator row of the box
               int oy;
               bool inside, accumulate;
-              if constexpr (MODE == MODE_DW) {
+              if (unit_dw) {
                 oy = p.v0 + lrow0;  // vocabulary row of dW
                 inside = oy < p.V;
                 accumulate = p.dW_accumulate != 0;
@@ -1014,11 +1076,13 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
                 inside = lrow0 < p.rows_cap;
                 accumulate = p.dh_accumulate != 0;
               }
+              // DHDW: dW goes through tmC2, the dH partials through tmC
+              const CUtensorMap* omap = (MODE == MODE_DHDW && unit_dw) ? &tmC2 : &tmC;
               if (col0 < p.H && inside) {
                 if (accumulate)
-                  tma_reduce_add_2d(&tmC, box, col0, oy);
+                  tma_reduce_add_2d(omap, box, col0, oy);
                 else
-                  tma_store_2d(&tmC, box, col0, oy);
+                  tma_store_2d(omap, box, col0, oy);
               }
               bulk_commit();
             }
@@ -1058,7 +1122,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     }
   }
 
-  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DLOGITS) {
+  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DHDW || MODE == MODE_DLOGITS) {
     if (warp >= 2 && lane == 0) bulk_wait_all();  // output boxes written before the CTA retires
   }
   __syncthreads();

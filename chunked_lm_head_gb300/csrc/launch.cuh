@@ -105,13 +105,13 @@ cudaError_t launch_persistent(Kern k, int grid, int cluster, int threads, int sm
 
 template <int MODE, bool kLong, int CG, int EW = EPI_WARPS>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                          const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p,
-                          int workers, cudaStream_t st) {
+                          const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
+                          const GemmParams& p, int workers, cudaStream_t st) {
   auto k = flce_gemm_kernel<MODE, kLong, CG, false, EW>;
   constexpr int smem = TileCfg<CG>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_persistent(k, CG * workers, CG, gemm_threads(EW), smem, st, a, b, c, a2, b2, p);
+  return launch_persistent(k, CG * workers, CG, gemm_threads(EW), smem, st, a, b, c, a2, b2, c2, p);
 }
 
 // dW over at most this many K blocks (64 rows each) runs 8 epilogue warps:
@@ -121,35 +121,39 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
 constexpr int kDwWideEpilogueMaxKBlocks = 16;
 
 // `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
-// tile loop.  `c` is the output map of the modes that write through TMA (dW);
-// the other modes ignore it.
+// tile loop.  `c` is the output map of the modes that write through TMA (dW,
+// dH partials, dlogits); the other modes ignore it.
 template <int MODE>
 cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st,
-                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr) {
-  // a2 / b2: the teacher's operands of the distillation modes (else unused)
+                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr,
+                        const CUtensorMap* c2 = nullptr) {
+  // a2 / b2: the teacher's operands of the distillation modes, or the DW
+  // units' operands of DHDW, whose dW output map is c2 (else unused)
   const CUtensorMap& A2 = a2 ? *a2 : a;
   const CUtensorMap& B2 = b2 ? *b2 : b;
+  const CUtensorMap& C2 = c2 ? *c2 : c;
   if constexpr (wide_epilogue_mode<MODE>()) {
     // the Jensen-Shannon forward's caller sized the partials for the column
     // parts it chose
-    const bool wide = MODE == MODE_DW       ? p.k_blocks <= kDwWideEpilogueMaxKBlocks
+    const bool wide = MODE == MODE_DW         ? p.k_blocks <= kDwWideEpilogueMaxKBlocks
+                      : MODE == MODE_DHDW    ? p.dw_k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_JSD_FWD ? p.col_parts == 2
                                              : wide_epilogue_on();
     if (wide) {
       constexpr int EW = 2 * EPI_WARPS;
       if (cg == 2)
-        return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, p, workers, st)
-                     : launch_gemm_t<MODE, false, 2, EW>(a, b, c, A2, B2, p, workers, st);
-      return kLong ? launch_gemm_t<MODE, true, 1, EW>(a, b, c, A2, B2, p, workers, st)
-                   : launch_gemm_t<MODE, false, 1, EW>(a, b, c, A2, B2, p, workers, st);
+        return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, C2, p, workers, st)
+                     : launch_gemm_t<MODE, false, 2, EW>(a, b, c, A2, B2, C2, p, workers, st);
+      return kLong ? launch_gemm_t<MODE, true, 1, EW>(a, b, c, A2, B2, C2, p, workers, st)
+                   : launch_gemm_t<MODE, false, 1, EW>(a, b, c, A2, B2, C2, p, workers, st);
     }
   }
   if (cg == 2)
-    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, A2, B2, p, workers, st)
-                 : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, p, workers, st);
-  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, A2, B2, p, workers, st)
-               : launch_gemm_t<MODE, false, 1>(a, b, c, A2, B2, p, workers, st);
+    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, A2, B2, C2, p, workers, st)
+                 : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, C2, p, workers, st);
+  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, A2, B2, C2, p, workers, st)
+               : launch_gemm_t<MODE, false, 1>(a, b, c, A2, B2, C2, p, workers, st);
 }
 
 // The e4m3 forward: MODE_FWD with 8-bit operands.
@@ -159,7 +163,7 @@ cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_persistent(kern, grid_mult * workers, grid_mult, gemm_threads(EPI_WARPS), smem, st, a, b, b,
-                             a, b, p);
+                             a, b, b, p);
   };
   if (cg == 2)
     return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)
@@ -206,6 +210,10 @@ int device_workers(int cg) {
   cached = n;
   return n;
 }
+
+// A slab's dH and dW GEMMs in one launch when the plan has several slabs
+// (default); FLCE_OPT_FUSE_DH_DW = 0 always launches them one after the other.
+bool fuse_dh_dw_on() { return opt_on(FLCE_OPT_FUSE_DH_DW); }
 
 // Backward on non-ignored rows only (default); FLCE_OPT_COMPACT = 0 runs
 // every row.
@@ -324,6 +332,37 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
                        int width, const CUtensorMap& D_k, const CUtensorMap& D_mn,
                        const CUtensorMap& B_dw, cudaStream_t st) {
   const BwdPlan& b = *a.plan;
+  if (a.dH && a.dW && fuse_dh_dw_on() && b.n_slabs > 1) {
+    // both in one launch: the DH units (as below), then the DW units.  Only
+    // for plans of several vocabulary slabs, whose short launches pay their
+    // fixed cost twice per slab otherwise (131,072 x 2,560 x 151,936 at
+    // 256-row chunks: 460 against 468 ms x GHz per step).  With one slab the
+    // two long launches ran 3 % faster apart (16,384 x 4,096 x 151,936: 50.6
+    // against 52.0 ms per step, same clocks).
+    GemmParams q = p;
+    q.v0 = v0;
+    q.m_tiles = static_cast<int>(ceil_div(rows, a.tm));
+    q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    q.k_blocks = static_cast<int>(ceil_div(width, BK));
+    q.cols = q.n_tiles;
+    q.n_per_unit = 1;
+    q.kb_per_split = b.dh_kb_per_split;
+    const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
+    q.k_splits = splits;
+    q.group_m = dh_group_rows(q.m_tiles);
+    q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
+    q.dh_accumulate = slab > 0 ? 1 : 0;
+    q.dw_m_tiles = static_cast<int>(ceil_div(width, a.tm));
+    q.dw_n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    q.dw_k_blocks = static_cast<int>(ceil_div(rows, BK));
+    q.dw_group_m = std::min(8, q.dw_m_tiles);
+    q.dW_accumulate = block > 0 ? 1 : 0;
+    q.num_units = splits * q.m_tiles * q.n_tiles + q.dw_m_tiles * q.dw_n_tiles;
+    ProfScope ps(K_DHDW, st);
+    FLCE_CUDA_TRY(launch_gemm<MODE_DHDW>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
+                                         std::min(q.num_units, a.workers), st, &D_mn, &B_dw, a.dW_map));
+    return FLCE_OK;
+  }
   if (a.dH) {  // dH[rows] (+)= D[:, slab] W[slab]
     GemmParams q = p;
     q.v0 = v0;

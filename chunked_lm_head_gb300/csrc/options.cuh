@@ -36,6 +36,7 @@ constexpr OptionDef kOptionDefs[FLCE_OPT_COUNT] = {
     {"FLCE_DH_GROUP", 8, 0, 1 << 20},         // FLCE_OPT_DH_GROUP
     {"FLCE_FWD_BLOCK_ROWS", -1, -1, INT_MAX},  // FLCE_OPT_FWD_BLOCK_ROWS
     {"FLCE_SKIP_MIN_ROWS", 2048, 0, INT_MAX},  // FLCE_OPT_SKIP_MIN_ROWS
+    {"FLCE_FUSE_DH_DW", 1, 0, 1},             // FLCE_OPT_FUSE_DH_DW
 };
 
 std::atomic<int64_t> g_options[FLCE_OPT_COUNT];
@@ -59,6 +60,7 @@ int64_t option_from_env(int o) {
     case FLCE_OPT_CTA_GROUP:
       return s[0] == '1' ? 1 : 2;
     case FLCE_OPT_COMPACT:
+    case FLCE_OPT_FUSE_DH_DW:
     case FLCE_OPT_PDL:
     case FLCE_OPT_D_TMA:
     case FLCE_OPT_WIDE_EPILOGUE:

@@ -632,6 +632,9 @@ typedef enum flce_option {
                                tile; -1 = 16 row tiles (default), 0 = all rows in one launch */
   FLCE_OPT_SKIP_MIN_ROWS,   /* FLCE_SKIP_MIN_ROWS: fewest rows for which a forward skips
                                ignored rows (default 2,048) */
+  FLCE_OPT_FUSE_DH_DW,      /* FLCE_FUSE_DH_DW: 1 = a vocabulary slab's dH and dW GEMMs run in one
+                               launch when the backward has several slabs (default),
+                               0 = always two launches */
   FLCE_OPT_COUNT
 } flce_option;
 

@@ -385,6 +385,37 @@ def test_backward_row_blocks_and_vocabulary_slabs(cg, compact, flce_opts):
     _full_check(inp, cr)
 
 
+@pytest.mark.parametrize("compact", ["0", "1"])
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_one_launch_per_slab_for_dh_and_dw_is_bitwise_the_two_launches(cg, compact, flce_opts):
+    """A slab's dH and dW units in one launch (the default) against two
+    launches: every output element is accumulated by the same unit in the same
+    order, so the results are bitwise equal; over 4 row blocks x 4 slabs, one
+    slab (the default plan of a large chunk) and the one-call path."""
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("compact", compact)
+    N, H, V = 3000, 512, 20000
+    wl = WL.custom(f"fuse{cg}{compact}", N, H, V, 256, w_std=0.04, targets="zipf", ignore_frac=0.08,
+                   seed=115)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(13).standard_normal(N).astype(np.float32)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, 256)
+    import chunked_lm_head_gb300 as flce
+    for rows, chunk in ((768, 256), (0, 4096)):
+        flce_opts.set("bwd_rows", rows)
+        out = []
+        for fuse in (1, 0):
+            flce_opts.set("fuse_dh_dw", fuse)
+            out.append(run_backward(h, W, t, w, lse, 1.0 / nv, chunk))
+            out.append(tuple(flce.forward_backward(h, W, t, w, chunk)[k] for k in ("dH", "dW")))
+        assert torch.equal(out[0][0], out[2][0]) and torch.equal(out[0][1], out[2][1]), rows
+        assert torch.equal(out[1][0], out[3][0]) and torch.equal(out[1][1], out[3][1]), rows
+    ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / nv)
+    assert_grad_close(np64(out[0][0]), ref.dH, "dH")
+    assert_grad_close(np64(out[0][1]), ref.dW, "dW")
+
+
 def test_backward_default_plan_odd_vocabulary():
     """The planner's own choice for a small chunk budget and an odd V (row
     pitch of D a multiple of 256, W rows of odd count) against the oracle,
