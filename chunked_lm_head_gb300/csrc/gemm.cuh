@@ -96,6 +96,21 @@ enum Mode : int {
   // (operands tmA / tmB, output tmC), the rest DW units (tmA2 / tmB2, tmC2)
   MODE_DHDW = 9
 };
+// Shared-memory layout of one kernel instantiation: the operand ring and the
+// output staging boxes.  dW at short K with 16 epilogue warps (four per TMEM
+// lane quarter, each on a quarter of the tile's columns) trades two operand
+// stages for one staging box per warp: its units are a few K blocks long and
+// their fp32 output, not the MMAs, sets the pace.
+template <int MODE, int CG, int EW>
+struct KernelCfg {
+  static constexpr bool kDeepOut = MODE == MODE_DW && EW == 16;
+  static constexpr int NSTAGE = kDeepOut ? (CG == 1 ? 3 : 4) : TileCfg<CG>::NSTAGE;
+  static constexpr int OUT_BYTES = kDeepOut ? EW * OUT_BOX_BYTES : OUT_STAGE_BYTES;
+  static constexpr int BOXES_PER_WARP = OUT_BYTES / OUT_BOX_BYTES / EW > 0 ? OUT_BYTES / OUT_BOX_BYTES / EW : 1;
+  static constexpr int SMEM = 1024 + NSTAGE * TileCfg<CG>::STAGE + OUT_BYTES + SMEM_BAR_BYTES;
+  static_assert(SMEM <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+  static_assert(BOXES_PER_WARP * EW * OUT_BOX_BYTES <= OUT_BYTES, "staging boxes exceed the staging area");
+};
 template <int MODE>
 __host__ __device__ constexpr bool is_kd() {
   return MODE == MODE_KD_FWD || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_FWD ||
@@ -124,9 +139,9 @@ __host__ __device__ constexpr bool is_split_fwd() {
 }
 
 // Threads of a GEMM CTA with `ew` epilogue warps: 4, one per TMEM lane
-// quarter; or 8 (the dW mode at short K), two per quarter, each on half of
-// the tile's columns, so that the fp32 output epilogue keeps up with MMAs
-// over only a few K blocks.
+// quarter; or 8 / 16 (the dW mode at short K), two / four per quarter, each
+// on a share of the tile's columns, so that the fp32 output epilogue keeps
+// up with MMAs over only a few K blocks.
 __host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
 
 // bit 0 of the device error word: a bounded wait ran out.
@@ -208,6 +223,10 @@ struct GemmParams {
   // DHDW: the DW units' grid (vocabulary tiles of the slab x hidden tiles,
   // K = the block's rows, one split); the DH units use the fields above
   int dw_m_tiles, dw_n_tiles, dw_k_blocks, dw_group_m;
+  // DH units: soft K-lockstep of the workers (see dh_lockstep); kprog holds
+  // one progress word per worker, tagged with this launch's epoch (0: off)
+  unsigned long long* kprog;
+  unsigned int kprog_epoch;
 };
 
 // grad_scale of the dlogits modes with its device-side factors: / max(count, 1)
@@ -329,6 +348,44 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
   }
   return true;
+}
+
+// Soft K-lockstep of the DH units of one launch.  A DH unit walks K over a
+// whole vocabulary slab (up to ~1,200 blocks), and the units of a wave share
+// their D rows and W columns; when the workers drift apart by more than L2
+// holds, the shared slices are read from DRAM again by every straggler.
+// Every kDhLockstepStride K blocks the producer publishes how many DH K
+// blocks it has issued in this launch (tagged with the launch's epoch) and,
+// while it is more than kDhLockstepWindow blocks ahead of the slowest worker
+// of the same launch, holds back its next loads -- for at most
+// kDhLockstepMaxCycles per check, after which it goes on regardless: the
+// throttle can delay a worker but never stop it, and entries of other
+// launches (another epoch) or of workers that have not started are ignored.
+// A worker done with its DH units publishes UINT32_MAX.
+constexpr int kDhLockstepStride = 8;
+constexpr unsigned kDhLockstepWindow = 32;
+constexpr long long kDhLockstepMaxCycles = 20000;
+
+__device__ __forceinline__ void dh_publish(unsigned long long* prog, int worker, unsigned epoch,
+                                           unsigned issued) {
+  const unsigned long long v = (static_cast<unsigned long long>(epoch) << 32) | issued;
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(prog + worker), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void dh_lockstep(unsigned long long* prog, int worker, int nworkers, unsigned epoch,
+                                            unsigned issued) {
+  dh_publish(prog, worker, epoch, issued);
+  const long long t0 = clock64();
+  while (true) {
+    unsigned lo = 0xFFFFFFFFu;
+    for (int w = 0; w < nworkers; ++w) {
+      unsigned long long v;
+      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(prog + w) : "memory");
+      if (static_cast<unsigned>(v >> 32) == epoch) lo = min(lo, static_cast<unsigned>(v));
+    }
+    if (issued <= lo + kDhLockstepWindow || clock64() - t0 > kDhLockstepMaxCycles) return;
+    __nanosleep(200);
+  }
 }
 
 // Bounded wait used only while shutting down (copies or MMAs in flight).
@@ -470,7 +527,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
                      const __grid_constant__ GemmParams p) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   using C = TileCfg<CG>;
-  constexpr int NST = C::NSTAGE;
+  using K = KernelCfg<MODE, CG, EW>;
+  constexpr int NST = K::NSTAGE;
   // accumulator buffers in TMEM: two (double-buffered) tiles, or one tile of
   // two accumulators (student, teacher) in the distillation modes
   constexpr int NACC = is_kd<MODE>() ? 1 : 2;
@@ -478,7 +536,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t out_stage = sbase + NST * C::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE + OUT_STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE + K::OUT_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   // barrier layout: full[NST], empty[NST], tfull[2], tempty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -544,10 +602,24 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
+      // DH units: K blocks issued in this launch (soft lockstep, when on)
+      const bool lockstep = (MODE == MODE_DH || MODE == MODE_DHDW) && p.kprog != nullptr;
+      unsigned dh_issued = 0;
+      bool dh_published_done = false;
       for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
         const Unit t = decode_unit<MODE>(p, dsh, u);
+        const bool dh_unit = lockstep && !t.dw;
+        if (lockstep && !dh_unit && !dh_published_done) {  // no DH unit left for this worker
+          dh_publish(p.kprog, worker, p.kprog_epoch, 0xFFFFFFFFu);
+          dh_published_done = true;
+        }
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
+            if (dh_unit) {
+              if (dh_issued % kDhLockstepStride == 0)
+                dh_lockstep(p.kprog, worker, nworkers, p.kprog_epoch, dh_issued);
+              ++dh_issued;
+            }
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
               ok = false;
               break;
@@ -574,6 +646,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
           }
         }
       }
+      if (lockstep && !dh_published_done) dh_publish(p.kprog, worker, p.kprog_epoch, 0xFFFFFFFFu);
       // no copy into shared memory may still be in flight when the CTA
       // retires: the issuing CTA's full barriers count both CTAs' bytes
       if (issuer)
@@ -641,13 +714,16 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // accumulator row owned by this thread
     // columns of the tile this warp takes: all, or one half (8 epilogue warps)
-    static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && wide_epilogue_mode<MODE>()),
-                  "8 epilogue warps: dW, the two-head dlogits and the Jensen-Shannon terms only");
+    static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && wide_epilogue_mode<MODE>()) ||
+                      (EW == 4 * EPI_WARPS && MODE == MODE_DW),
+                  "8 epilogue warps: dW, DHDW, the two-head dlogits and the Jensen-Shannon terms; "
+                  "16: dW only");
     constexpr int kColParts = EW / 4;
     constexpr int kChunks = BN / 32 / kColParts;
     const int c_lo = ((warp - 2) / 4) * kChunks;
-    // TMA staging boxes of this warp (the staging area holds 8 boxes)
-    constexpr int kBoxes = 2 * EPI_WARPS / EW;
+    // TMA staging boxes of this warp (KernelCfg: 8 boxes shared by 4 or 8
+    // warps, or one per warp of 16)
+    constexpr int kBoxes = K::BOXES_PER_WARP;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t tempty_target0 = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     const uint32_t tempty_target1 = CG == 2 ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdlib>
 
@@ -108,7 +109,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
                           const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
                           const GemmParams& p, int workers, cudaStream_t st) {
   auto k = flce_gemm_kernel<MODE, kLong, CG, false, EW>;
-  constexpr int smem = TileCfg<CG>::SMEM;
+  constexpr int smem = KernelCfg<MODE, CG, EW>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_persistent(k, CG * workers, CG, gemm_threads(EW), smem, st, a, b, c, a2, b2, c2, p);
@@ -140,6 +141,17 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
                       : MODE == MODE_DHDW    ? p.dw_k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_JSD_FWD ? p.col_parts == 2
                                              : wide_epilogue_on();
+    if constexpr (MODE == MODE_DW) {
+      // short K: 16 epilogue warps when FLCE_OPT_DW_EPILOGUE_WARPS says so
+      if (wide && opt(FLCE_OPT_DW_EPILOGUE_WARPS) == 16) {
+        constexpr int EW = 4 * EPI_WARPS;
+        if (cg == 2)
+          return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, C2, p, workers, st)
+                       : launch_gemm_t<MODE, false, 2, EW>(a, b, c, A2, B2, C2, p, workers, st);
+        return kLong ? launch_gemm_t<MODE, true, 1, EW>(a, b, c, A2, B2, C2, p, workers, st)
+                     : launch_gemm_t<MODE, false, 1, EW>(a, b, c, A2, B2, C2, p, workers, st);
+      }
+    }
     if (wide) {
       constexpr int EW = 2 * EPI_WARPS;
       if (cg == 2)
@@ -209,6 +221,24 @@ int device_workers(int cg) {
   cached_dev = dev;
   cached = n;
   return n;
+}
+
+// Soft K-lockstep of the dH units (FLCE_OPT_DH_LOCKSTEP; see dh_lockstep):
+// the progress array and a fresh epoch for each launch, or none.
+void dh_lockstep_params(GemmParams& q, int workers) {
+  q.kprog = nullptr;
+  q.kprog_epoch = 0;
+  if (!opt_on(FLCE_OPT_DH_LOCKSTEP) || workers > kDhLockstepMaxWorkers) return;
+  static std::atomic<unsigned> epoch{0};
+  unsigned e = ++epoch;
+  if (e == 0) e = ++epoch;  // 0 marks words no launch has written
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dh_kprog) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  q.kprog = static_cast<unsigned long long*>(p);
+  q.kprog_epoch = e;
 }
 
 // A slab's dH and dW GEMMs in one launch when the plan has several slabs
@@ -358,6 +388,7 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     q.dw_group_m = std::min(8, q.dw_m_tiles);
     q.dW_accumulate = block > 0 ? 1 : 0;
     q.num_units = splits * q.m_tiles * q.n_tiles + q.dw_m_tiles * q.dw_n_tiles;
+    dh_lockstep_params(q, std::min(q.num_units, a.workers));
     ProfScope ps(K_DHDW, st);
     FLCE_CUDA_TRY(launch_gemm<MODE_DHDW>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
                                          std::min(q.num_units, a.workers), st, &D_mn, &B_dw, a.dW_map));
@@ -378,6 +409,7 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     q.group_m = dh_group_rows(q.m_tiles);
     q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
     q.dh_accumulate = slab > 0 ? 1 : 0;
+    dh_lockstep_params(q, std::min(q.num_units, a.workers));
     ProfScope ps(K_DH, st);
     FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
                                        std::min(q.num_units, a.workers), st));
