@@ -223,10 +223,6 @@ struct GemmParams {
   // DHDW: the DW units' grid (vocabulary tiles of the slab x hidden tiles,
   // K = the block's rows, one split); the DH units use the fields above
   int dw_m_tiles, dw_n_tiles, dw_k_blocks, dw_group_m;
-  // DH units: soft K-lockstep of the workers (see dh_lockstep); kprog holds
-  // one progress word per worker, tagged with this launch's epoch (0: off)
-  unsigned long long* kprog;
-  unsigned int kprog_epoch;
 };
 
 // grad_scale of the dlogits modes with its device-side factors: / max(count, 1)
@@ -348,44 +344,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
   }
   return true;
-}
-
-// Soft K-lockstep of the DH units of one launch.  A DH unit walks K over a
-// whole vocabulary slab (up to ~1,200 blocks), and the units of a wave share
-// their D rows and W columns; when the workers drift apart by more than L2
-// holds, the shared slices are read from DRAM again by every straggler.
-// Every kDhLockstepStride K blocks the producer publishes how many DH K
-// blocks it has issued in this launch (tagged with the launch's epoch) and,
-// while it is more than kDhLockstepWindow blocks ahead of the slowest worker
-// of the same launch, holds back its next loads -- for at most
-// kDhLockstepMaxCycles per check, after which it goes on regardless: the
-// throttle can delay a worker but never stop it, and entries of other
-// launches (another epoch) or of workers that have not started are ignored.
-// A worker done with its DH units publishes UINT32_MAX.
-constexpr int kDhLockstepStride = 8;
-constexpr unsigned kDhLockstepWindow = 32;
-constexpr long long kDhLockstepMaxCycles = 20000;
-
-__device__ __forceinline__ void dh_publish(unsigned long long* prog, int worker, unsigned epoch,
-                                           unsigned issued) {
-  const unsigned long long v = (static_cast<unsigned long long>(epoch) << 32) | issued;
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(prog + worker), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void dh_lockstep(unsigned long long* prog, int worker, int nworkers, unsigned epoch,
-                                            unsigned issued) {
-  dh_publish(prog, worker, epoch, issued);
-  const long long t0 = clock64();
-  while (true) {
-    unsigned lo = 0xFFFFFFFFu;
-    for (int w = 0; w < nworkers; ++w) {
-      unsigned long long v;
-      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(prog + w) : "memory");
-      if (static_cast<unsigned>(v >> 32) == epoch) lo = min(lo, static_cast<unsigned>(v));
-    }
-    if (issued <= lo + kDhLockstepWindow || clock64() - t0 > kDhLockstepMaxCycles) return;
-    __nanosleep(200);
-  }
 }
 
 // Bounded wait used only while shutting down (copies or MMAs in flight).
@@ -602,24 +560,10 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      // DH units: K blocks issued in this launch (soft lockstep, when on)
-      const bool lockstep = (MODE == MODE_DH || MODE == MODE_DHDW) && p.kprog != nullptr;
-      unsigned dh_issued = 0;
-      bool dh_published_done = false;
       for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
         const Unit t = decode_unit<MODE>(p, dsh, u);
-        const bool dh_unit = lockstep && !t.dw;
-        if (lockstep && !dh_unit && !dh_published_done) {  // no DH unit left for this worker
-          dh_publish(p.kprog, worker, p.kprog_epoch, 0xFFFFFFFFu);
-          dh_published_done = true;
-        }
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
-            if (dh_unit) {
-              if (dh_issued % kDhLockstepStride == 0)
-                dh_lockstep(p.kprog, worker, nworkers, p.kprog_epoch, dh_issued);
-              ++dh_issued;
-            }
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
               ok = false;
               break;
@@ -646,7 +590,6 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
           }
         }
       }
-      if (lockstep && !dh_published_done) dh_publish(p.kprog, worker, p.kprog_epoch, 0xFFFFFFFFu);
       // no copy into shared memory may still be in flight when the CTA
       // retires: the issuing CTA's full barriers count both CTAs' bytes
       if (issuer)

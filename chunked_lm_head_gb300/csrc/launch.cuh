@@ -7,7 +7,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <atomic>
 #include <climits>
 #include <cstdlib>
 
@@ -142,7 +141,8 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
                       : MODE == MODE_JSD_FWD ? p.col_parts == 2
                                              : wide_epilogue_on();
     if constexpr (MODE == MODE_DW) {
-      // short K: 16 epilogue warps when FLCE_OPT_DW_EPILOGUE_WARPS says so
+      // short K: 16 epilogue warps (default; FLCE_OPT_DW_EPILOGUE_WARPS = 8
+      // keeps 8)
       if (wide && opt(FLCE_OPT_DW_EPILOGUE_WARPS) == 16) {
         constexpr int EW = 4 * EPI_WARPS;
         if (cg == 2)
@@ -221,24 +221,6 @@ int device_workers(int cg) {
   cached_dev = dev;
   cached = n;
   return n;
-}
-
-// Soft K-lockstep of the dH units (FLCE_OPT_DH_LOCKSTEP; see dh_lockstep):
-// the progress array and a fresh epoch for each launch, or none.
-void dh_lockstep_params(GemmParams& q, int workers) {
-  q.kprog = nullptr;
-  q.kprog_epoch = 0;
-  if (!opt_on(FLCE_OPT_DH_LOCKSTEP) || workers > kDhLockstepMaxWorkers) return;
-  static std::atomic<unsigned> epoch{0};
-  unsigned e = ++epoch;
-  if (e == 0) e = ++epoch;  // 0 marks words no launch has written
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_dh_kprog) != cudaSuccess) {
-    cudaGetLastError();
-    return;
-  }
-  q.kprog = static_cast<unsigned long long*>(p);
-  q.kprog_epoch = e;
 }
 
 // A slab's dH and dW GEMMs in one launch when the plan has several slabs
@@ -388,7 +370,6 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     q.dw_group_m = std::min(8, q.dw_m_tiles);
     q.dW_accumulate = block > 0 ? 1 : 0;
     q.num_units = splits * q.m_tiles * q.n_tiles + q.dw_m_tiles * q.dw_n_tiles;
-    dh_lockstep_params(q, std::min(q.num_units, a.workers));
     ProfScope ps(K_DHDW, st);
     FLCE_CUDA_TRY(launch_gemm<MODE_DHDW>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
                                          std::min(q.num_units, a.workers), st, &D_mn, &B_dw, a.dW_map));
@@ -409,7 +390,6 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     q.group_m = dh_group_rows(q.m_tiles);
     q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
     q.dh_accumulate = slab > 0 ? 1 : 0;
-    dh_lockstep_params(q, std::min(q.num_units, a.workers));
     ProfScope ps(K_DH, st);
     FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
                                        std::min(q.num_units, a.workers), st));

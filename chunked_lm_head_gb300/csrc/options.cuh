@@ -37,8 +37,7 @@ constexpr OptionDef kOptionDefs[FLCE_OPT_COUNT] = {
     {"FLCE_FWD_BLOCK_ROWS", -1, -1, INT_MAX},  // FLCE_OPT_FWD_BLOCK_ROWS
     {"FLCE_SKIP_MIN_ROWS", 2048, 0, INT_MAX},  // FLCE_OPT_SKIP_MIN_ROWS
     {"FLCE_FUSE_DH_DW", 1, 0, 1},             // FLCE_OPT_FUSE_DH_DW
-    {"FLCE_DH_LOCKSTEP", 0, 0, 1},            // FLCE_OPT_DH_LOCKSTEP
-    {"FLCE_DW_EPILOGUE_WARPS", 8, 8, 16},     // FLCE_OPT_DW_EPILOGUE_WARPS
+    {"FLCE_DW_EPILOGUE_WARPS", 16, 8, 16},    // FLCE_OPT_DW_EPILOGUE_WARPS
 };
 
 std::atomic<int64_t> g_options[FLCE_OPT_COUNT];
@@ -63,7 +62,6 @@ int64_t option_from_env(int o) {
       return s[0] == '1' ? 1 : 2;
     case FLCE_OPT_COMPACT:
     case FLCE_OPT_FUSE_DH_DW:
-    case FLCE_OPT_DH_LOCKSTEP:
     case FLCE_OPT_PDL:
     case FLCE_OPT_D_TMA:
     case FLCE_OPT_WIDE_EPILOGUE:

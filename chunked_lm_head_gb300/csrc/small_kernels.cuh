@@ -15,9 +15,6 @@ namespace flce {
 
 __device__ int g_device_error;  // bit DEVERR_TIMEOUT: a bounded wait ran out
 __device__ int g_selftest_flag;  // verdict of wait_selftest_kernel
-// per-worker progress words of the DH units' soft K-lockstep (dh_lockstep)
-constexpr int kDhLockstepMaxWorkers = 1024;
-__device__ unsigned long long g_dh_kprog[kDhLockstepMaxWorkers];
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int SMALL_THREADS = 256;

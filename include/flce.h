@@ -635,12 +635,8 @@ typedef enum flce_option {
   FLCE_OPT_FUSE_DH_DW,      /* FLCE_FUSE_DH_DW: 1 = a vocabulary slab's dH and dW GEMMs run in one
                                launch when the backward has several slabs (default),
                                0 = always two launches */
-  FLCE_OPT_DH_LOCKSTEP,     /* FLCE_DH_LOCKSTEP: 1 = the dH workers of a launch hold back loads
-                               while more than 32 K blocks ahead of the slowest (each wait at
-                               most ~10 us), so the D and W slices they share stay in L2;
-                               0 = off (default) */
   FLCE_OPT_DW_EPILOGUE_WARPS,  /* FLCE_DW_EPILOGUE_WARPS: epilogue warps of the dW GEMM at
-                                  short K (at most 1,024 rows): 8 (default) or 16 */
+                                  short K (at most 1,024 rows): 16 (default) or 8 */
   FLCE_OPT_COUNT
 } flce_option;
 
