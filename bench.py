@@ -87,8 +87,10 @@ def algorithmic_bytes_step(N: int, nv: int, H: int, V: int, chunk_rows: int,
         "bwd_dH": nv * Db + B * W + dh_out,
         "bwd_dW": nv * Db + S * nv * hb + B * V * H * 4.0 + (B - 1) * V * H * 4.0,
     }
-    # a slab's dH and dW units in one launch (the library's default)
+    # a slab's dH and dW units in one launch, and a row block's dlogits, dH
+    # and dW units in one launch (the library's defaults with several slabs)
     out["bwd_dH_dW"] = out["bwd_dH"] + out["bwd_dW"]
+    out["bwd_pipeline"] = out["bwd_dlogits"] + out["bwd_dH_dW"]
     return out
 
 
@@ -215,8 +217,10 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "bwd_dH_dW", "kd_fwd_logits", "kd_bwd_dlogits",
-              "jsd_fwd_terms", "jsd_bwd_dlogits")
+GEMM_KINDS = ("fwd_logits_lse", "bwd_dlogits", "bwd_dH", "bwd_dW", "bwd_dH_dW", "bwd_pipeline", "kd_fwd_logits",
+              "kd_bwd_dlogits", "jsd_fwd_terms", "jsd_bwd_dlogits")
+# launch kinds that run the units of several kinds above (counted once in the step's FLOPs)
+COMPOSITE_KINDS = ("bwd_dH_dW", "bwd_pipeline")
 
 
 def gpu_arm(args):
@@ -506,6 +510,8 @@ def gpu_arm(args):
                       "bwd_dH": 2.0 * nv * V * H, "bwd_dW": 2.0 * nv * V * H}
     if "bwd_dH" in flops_step and "bwd_dW" in flops_step:  # one launch per slab for both
         flops_step["bwd_dH_dW"] = flops_step["bwd_dH"] + flops_step["bwd_dW"]
+    if all(k in flops_step for k in ("bwd_dlogits", "bwd_dH", "bwd_dW")):  # one launch per row block
+        flops_step["bwd_pipeline"] = flops_step["bwd_dlogits"] + flops_step["bwd_dH"] + flops_step["bwd_dW"]
     kern = {}
     for k, (tot_ms, n) in prof.items():
         if n:
@@ -549,7 +555,7 @@ def gpu_arm(args):
                          "peak_source": f"{peaks['source']}: measured hbm_gbs (copy bandwidth)"})
     # the metric counts 8 N V H per step (forward, recompute, dH, dW over every
     # row); the GEMMs execute the FLOPs of flops_step (non-ignored rows)
-    exec_tflops = sum(v for k, v in flops_step.items() if k != "bwd_dH_dW") / (ms_step / 1e3) / 1e12
+    exec_tflops = sum(v for k, v in flops_step.items() if k not in COMPOSITE_KINDS) / (ms_step / 1e3) / 1e12
     step_tflops = exec_tflops
     if not (Ht or args.forward_only or args.fused):
         step_tflops = 8.0 * N * V * H / (ms_step / 1e3) / 1e12

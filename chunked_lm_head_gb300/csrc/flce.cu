@@ -50,8 +50,7 @@ size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows)
   // the forward's layout with the buffers of flce_forward_ex2's row skipping
   const FwdLayout fl =
       fwd_layout(N, plan_forward_call(N, H, V, workers, BM * cg), H, fwd_block_rows(N, BM * cg));
-  const BwdLayout bl = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, BM * cg));
-  return std::max(fl.total, bl.total);
+  return std::max(fl.total, bwd_workspace(N, H, V, chunk_rows, workers, BM * cg));
 }
 
 flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int32_t workers,
@@ -59,14 +58,15 @@ flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_ro
   if (out == nullptr || !sizes_ok(N, H, V)) return FLCE_ERR_INVALID_ARG;
   const int cg = cta_group_ == 1 || cta_group_ == 2 ? cta_group_ : cta_group();
   const int w = workers > 0 ? workers : device_workers(cg);
-  const BwdPlan b = plan_backward(N, H, V, chunk_rows, w, BM * cg);
+  const BwdPlan b = plan_backward_call(N, H, V, chunk_rows, w, BM * cg, true);
   out->rows_per_block = b.R;
   out->vocab_per_slab = b.Vs;
   out->row_blocks = ceil_div(std::max<int64_t>(N, 1), b.R);
   out->vocab_slabs = b.n_slabs;
   out->dh_splits = b.dh_splits;
-  out->dlogits_bytes = b.R * b.ldD * 2;
-  out->workspace_bytes = static_cast<int64_t>(bwd_layout(N, H, b).total);
+  out->dlogits_bytes = b.buffers * b.R * b.ldD * 2;
+  out->workspace_bytes = static_cast<int64_t>(bwd_workspace(N, H, V, chunk_rows, w, BM * cg));
+  out->dlogits_buffers = b.buffers;
   return FLCE_OK;
 }
 
@@ -266,7 +266,7 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   const int cg = cta_group();
   const int workers = device_workers(cg);
   const int tm = BM * cg;
-  const BwdPlan b = plan_backward(N, H, V, chunk_rows, workers, tm);
+  const BwdPlan b = plan_backward_call(N, H, V, chunk_rows, workers, tm, dH != nullptr && dW != nullptr);
   const BwdLayout L = bwd_layout(N, H, b);
   Workspace ws;
   flce_status s = get_workspace(ws, workspace, workspace_bytes, L.total, st);
@@ -311,8 +311,8 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   base.grad_scale = grad_scale;
   base.count_scale = count_scale;
   base.scale_dev = scale_dev;
-  CUtensorMap D_st;  // D as a TMA store target: [R][ldD] bf16, 64 x 32 boxes
-  base.d_tma = d_tma_on() && make_map(&D_st, Dbuf, b.ldD, b.R, b.ldD, 64, 32) ? 1 : 0;
+  CUtensorMap D_st;  // D as a TMA store target: [buffers * R][ldD] bf16, 64 x 32 boxes
+  base.d_tma = d_tma_on() && make_map(&D_st, Dbuf, b.ldD, b.buffers * b.R, b.ldD, 64, 32) ? 1 : 0;
   base.ignore_index = ignore_index;
   base.D = Dbuf;
   base.dH = dH;
@@ -363,6 +363,20 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
       !make_map_t(&dhp_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dh_part, H, b.dh_splits * b.R, H, 32, 32))
     return FLCE_ERR_CUDA;
   const DhDwStage dhdw{cg, workers, tm, kLong, &b, H, V, dh_part, dH, dW, &W_mn, &dW_map, &dhp_map};
+  // a pipelined plan: each row block in one launch whose units wait on one
+  // another through counters in the workspace (two sets, alternate blocks),
+  // D in two buffers of R rows (maps over both)
+  const bool pipe = b.buffers == 2 && dH && dW && base.d_tma && b.dh_f32 && b.n_slabs > 1;
+  if (b.buffers == 2 && !pipe) return FLCE_ERR_CUDA;  // the planner and this call disagree
+  unsigned* dep = reinterpret_cast<unsigned*>(wb + L.dep);
+  const long long dep_words = pipe_dep_words(b);
+  CUtensorMap Dpipe_k, Dpipe_mn;
+  if (pipe) {
+    if (!make_map(&Dpipe_k, Dbuf, b.ldD, 2 * b.R, b.ldD, BK, BM) ||
+        !make_map(&Dpipe_mn, Dbuf, b.ldD, 2 * b.R, b.ldD, 64, BK))
+      return FLCE_ERR_CUDA;
+    FLCE_CUDA_TRY(cudaMemsetAsync(dep, 0, static_cast<size_t>(2 * dep_words) * 4, st));
+  }
   int block = 0;
   for (long long row0 = 0; row0 < N; row0 += b.R, ++block) {
     // rows: exact (plain) or the capacity whose live part the kernels read (compacted)
@@ -392,7 +406,12 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
                !make_map(&D_mn, Dbuf, b.ldD, rows, b.ldD, 64, BK)) {
       return FLCE_ERR_CUDA;
     }
-    for (int slab = 0; slab < b.n_slabs; ++slab) {
+    if (pipe) {
+      const flce_status s2 = pipe_block(dhdw, p, rows, block, A_dl, W_k, D_st, Dpipe_k, Dpipe_mn, B_dw,
+                                        dep + (block % 2) * dep_words, dep + ((block + 1) % 2) * dep_words, st);
+      if (s2 != FLCE_OK) return s2;
+    }
+    for (int slab = 0; slab < (pipe ? 0 : b.n_slabs); ++slab) {
       const int v0 = static_cast<int>(slab * b.Vs);
       const int width = static_cast<int>(std::min<long long>(b.Vs, V - v0));
       {  // (1) recompute the slab's logits, dlogits -> D[rows, 0:width] bf16
@@ -473,7 +492,7 @@ static FallbackLayout fallback_layout(int64_t N, int64_t H, int64_t V, int64_t c
                                       int tm) {
   FallbackLayout L;
   const size_t fwd = fwd_layout(N, plan_forward_call(N, H, V, workers, tm)).total;
-  const size_t bwd = bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, tm)).total;
+  const size_t bwd = bwd_workspace(N, H, V, chunk_rows, workers, tm);
   const size_t n4 = align256(static_cast<size_t>(std::max<int64_t>(N, 1)) * 4);
   const size_t nb8 = align256(static_cast<size_t>(ceil_div(std::max<int64_t>(N, 1), SMALL_THREADS)) * 8);
   L.inner = std::max(fwd, bwd);

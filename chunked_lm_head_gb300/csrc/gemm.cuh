@@ -94,8 +94,15 @@ enum Mode : int {
   MODE_FUSED_FWD = 8,
   // DH and DW of one slab in one launch: units [0, dH units) are DH units
   // (operands tmA / tmB, output tmC), the rest DW units (tmA2 / tmB2, tmC2)
-  MODE_DHDW = 9
+  MODE_DHDW = 9,
+  // the whole backward of one row block in one launch: for each vocabulary
+  // slab its DLOGITS units (tmA3 / tmB3, D out through tmC3), then its DH
+  // units (tmA / tmB, tmC) and DW units (tmA2 / tmB2, tmC2).  Units wait on
+  // device-side counters for the units whose output they read or overwrite.
+  MODE_PIPE = 10
 };
+// unit kinds of MODE_PIPE
+constexpr int KIND_DL = 0, KIND_DH = 1, KIND_DW = 2;
 // Shared-memory layout of one kernel instantiation: the operand ring and the
 // output staging boxes.  dW at short K with 16 epilogue warps (four per TMEM
 // lane quarter, each on a quarter of the tile's columns) trades two operand
@@ -104,8 +111,14 @@ enum Mode : int {
 template <int MODE, int CG, int EW>
 struct KernelCfg {
   static constexpr bool kDeepOut = MODE == MODE_DW && EW == 16;
-  static constexpr int NSTAGE = kDeepOut ? (CG == 1 ? 3 : 4) : TileCfg<CG>::NSTAGE;
-  static constexpr int OUT_BYTES = kDeepOut ? EW * OUT_BOX_BYTES : OUT_STAGE_BYTES;
+  // dlogits with 8 epilogue warps (alone or in PIPE): two bf16 staging boxes
+  // per warp, paid for with one operand stage
+  static constexpr bool kWideD = (MODE == MODE_DLOGITS || MODE == MODE_PIPE) && EW == 8;
+  static constexpr int NSTAGE =
+      kDeepOut ? (CG == 1 ? 3 : 4) : (kWideD ? TileCfg<CG>::NSTAGE - 1 : TileCfg<CG>::NSTAGE);
+  static constexpr int OUT_BYTES = kDeepOut ? EW * OUT_BOX_BYTES
+                                   : kWideD ? EW * 2 * OUT_BOX_BYTES
+                                            : OUT_STAGE_BYTES;
   static constexpr int BOXES_PER_WARP = OUT_BYTES / OUT_BOX_BYTES / EW > 0 ? OUT_BYTES / OUT_BOX_BYTES / EW : 1;
   static constexpr int SMEM = 1024 + NSTAGE * TileCfg<CG>::STAGE + OUT_BYTES + SMEM_BAR_BYTES;
   static_assert(SMEM <= 232448, "exceeds the 227 KiB shared memory of one CTA");
@@ -123,14 +136,15 @@ __host__ __device__ constexpr bool is_kd() {
 template <int MODE>
 __host__ __device__ constexpr bool wide_epilogue_mode() {
   return MODE == MODE_DW || MODE == MODE_DHDW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS ||
-         MODE == MODE_JSD_FWD;
+         MODE == MODE_JSD_FWD || MODE == MODE_DLOGITS || MODE == MODE_PIPE;
 }
 // modes whose accumulator rows are rows of h (all but dW, whose accumulator
 // rows are vocabulary rows): under row compaction they map through row_idx
-// and take their row count from the device (DHDW: its DH units only)
+// and take their row count from the device (DHDW, PIPE: their DH and DLOGITS
+// units only)
 template <int MODE>
 __host__ __device__ constexpr bool rows_are_tokens() {
-  return MODE != MODE_DW && MODE != MODE_DHDW;
+  return MODE != MODE_DW && MODE != MODE_DHDW && MODE != MODE_PIPE;
 }
 // modes whose units are (row tile, vocabulary split) with per-row partials
 template <int MODE>
@@ -143,6 +157,12 @@ __host__ __device__ constexpr bool is_split_fwd() {
 // on a share of the tile's columns, so that the fp32 output epilogue keeps
 // up with MMAs over only a few K blocks.
 __host__ __device__ constexpr int gemm_threads(int ew) { return 64 + 32 * ew; }
+// PIPE adds one warp that waits on the units' dependency counters ahead of
+// the producer (see pipe_wait_deps).
+template <int MODE>
+__host__ __device__ constexpr int kernel_threads(int ew) {
+  return gemm_threads(ew) + (MODE == MODE_PIPE ? 32 : 0);
+}
 
 // bit 0 of the device error word: a bounded wait ran out.
 constexpr int DEVERR_TIMEOUT = 1;
@@ -223,6 +243,15 @@ struct GemmParams {
   // DHDW: the DW units' grid (vocabulary tiles of the slab x hidden tiles,
   // K = the block's rows, one split); the DH units use the fields above
   int dw_m_tiles, dw_n_tiles, dw_k_blocks, dw_group_m;
+  // PIPE: slabs of pp_vs vocabulary columns (the last one narrower) over the
+  // whole vocabulary; pp_kh K blocks of H per DLOGITS tile; row tiles at most
+  // m_tiles (the capacity); dH k-splits of dh_kbps K blocks.  D holds two
+  // buffers of rows_cap rows, slab s in buffer s % 2.  Dependency counters:
+  // pp_dep (this launch's, zero at its start) and pp_dep_zero (the next
+  // launch's, zeroed here), pp_dep_words each.
+  int pp_slabs, pp_vs, pp_kh, pp_dh_kbps, pp_dl_group, pp_dep_words;
+  unsigned* pp_dep;
+  unsigned* pp_dep_zero;
 };
 
 // grad_scale of the dlogits modes with its device-side factors: / max(count, 1)
@@ -237,14 +266,55 @@ __device__ __forceinline__ float device_grad_scale(const GemmParams& p) {
 // Problem extents that depend on the device-side row count of a compacted pass.
 // DHDW: m_tiles / k_blocks / kb_per_split are its DH units', dh_units of them,
 // followed by dw_units DW units of dw_k_blocks K blocks.
+// PIPE: dh_units = the units of one full slab.
 struct DynShape {
   int rows, m_tiles, k_blocks, kb_per_split, num_units;
   int dh_units, dw_units, dw_k_blocks;
 };
 
+// PIPE: one vocabulary slab of the row block -- its columns, its tiles for
+// DLOGITS (BN wide), DW (TM wide) and DH (BK-deep K blocks, dh_kbps per
+// split), and its unit counts.
+struct PipeSlab {
+  int v0, width, vt, dwt, kb, splits, n_dl, n_dh, n_dw;
+};
+
+template <int TM>
+__device__ __forceinline__ PipeSlab pipe_slab(const GemmParams& p, const DynShape& d, int s) {
+  PipeSlab q;
+  q.v0 = s * p.pp_vs;
+  q.width = min(p.pp_vs, p.V - q.v0);
+  q.vt = (q.width + BN - 1) / BN;
+  q.dwt = (q.width + TM - 1) / TM;
+  q.kb = (q.width + BK - 1) / BK;
+  q.splits = (q.kb + p.pp_dh_kbps - 1) / p.pp_dh_kbps;
+  q.n_dl = d.m_tiles * q.vt;
+  q.n_dh = q.splits * d.m_tiles * p.n_tiles;
+  // an empty first row block still writes zeros to dW, an empty later one
+  // has nothing to add
+  q.n_dw = (d.rows == 0 && p.dW_accumulate) ? 0 : q.dwt * p.n_tiles;
+  return q;
+}
+
 template <int MODE, int TM>
 __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
   DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units, 0, 0, 0};
+  if constexpr (MODE == MODE_PIPE) {
+    if (p.dyn_count != nullptr) {
+      d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
+      d.m_tiles = (d.rows + TM - 1) / TM;
+      d.dw_k_blocks = (d.rows + BK - 1) / BK;
+    } else {
+      d.dw_k_blocks = p.dw_k_blocks;
+    }
+    // units of phase p: slab p's DLOGITS units, then slab p - 1's DH and DW
+    // units (phases 0 .. slabs); dh_units = the units of a middle phase
+    const PipeSlab q0 = pipe_slab<TM>(p, d, 0);
+    const PipeSlab ql = pipe_slab<TM>(p, d, p.pp_slabs - 1);
+    d.dh_units = q0.n_dl + q0.n_dh + q0.n_dw;
+    d.num_units = (p.pp_slabs - 1) * d.dh_units + ql.n_dl + ql.n_dh + ql.n_dw;  // every slab's units
+    return d;
+  }
   if constexpr (MODE == MODE_DHDW) {
     if (p.dyn_count != nullptr) {
       d.rows = max(0, min(*p.dyn_count - p.chunk_first, p.rows_cap));
@@ -278,7 +348,9 @@ __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
 
 struct Unit {
   int m, n0, n1, kb0, kb1, split;
-  bool dw;  // DHDW: a DW unit
+  bool dw;   // DHDW, PIPE: a DW unit
+  int kind;  // PIPE: KIND_DL / KIND_DH / KIND_DW
+  int slab;  // PIPE: its vocabulary slab
 };
 
 // Unit u of a grid of (k-splits x m_tiles x cols) units, rasterised in
@@ -311,11 +383,60 @@ __device__ __forceinline__ Unit decode_grid(int u, int m_tiles, int cols, int n_
   t.kb1 = min(k_blocks, t.kb0 + kb_per_split);
   t.split = col_split ? c : ks;
   t.dw = false;
+  t.kind = 0;
+  t.slab = 0;
   return t;
 }
 
-template <int MODE>
+template <int MODE, int TM = BM>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape& d, int u) {
+  if constexpr (MODE == MODE_PIPE) {
+    // phase by phase: phase p holds slab p's DLOGITS units (p < slabs), then
+    // slab p - 1's DH units and DW units (p > 0).  Phase 0 has the first
+    // slab's DLOGITS units; every middle phase a full slab's DLOGITS, DH and
+    // DW units (F of them); phase slabs - 1 the last slab's DLOGITS units and
+    // a full slab's DH and DW; phase slabs the last slab's DH and DW.
+    const int S = p.pp_slabs;
+    const PipeSlab qf = pipe_slab<TM>(p, d, 0);
+    const PipeSlab ql = pipe_slab<TM>(p, d, S - 1);
+    const int F = d.dh_units;
+    int ph, local;
+    if (u < qf.n_dl) {
+      ph = 0;
+      local = u;
+    } else if (u < qf.n_dl + (S - 2) * F) {
+      ph = 1 + (u - qf.n_dl) / F;
+      local = u - qf.n_dl - (ph - 1) * F;
+    } else if (u < qf.n_dl + (S - 2) * F + ql.n_dl + qf.n_dh + qf.n_dw) {
+      ph = S - 1;
+      local = u - qf.n_dl - (S - 2) * F;
+    } else {
+      ph = S;
+      local = u - qf.n_dl - (S - 2) * F - ql.n_dl - qf.n_dh - qf.n_dw;
+    }
+    Unit t;
+    const PipeSlab qd = ph < S ? pipe_slab<TM>(p, d, ph) : ql;  // DLOGITS slab of the phase
+    const int n_dl = ph < S ? qd.n_dl : 0;
+    if (local < n_dl) {
+      t = decode_grid(local, d.m_tiles, qd.vt, qd.vt, 1, p.pp_dl_group, p.pp_kh, p.pp_kh, false);
+      t.kind = KIND_DL;
+      t.slab = ph;
+      return t;
+    }
+    local -= n_dl;
+    const PipeSlab q = ph == S ? ql : qf;  // slab ph - 1: full unless the last
+    if (local < q.n_dh) {
+      t = decode_grid(local, d.m_tiles, p.n_tiles, p.n_tiles, 1, p.group_m, p.pp_dh_kbps, q.kb, false);
+      t.kind = KIND_DH;
+    } else {
+      t = decode_grid(local - q.n_dh, q.dwt, p.n_tiles, p.n_tiles, 1, p.dw_group_m, max(d.dw_k_blocks, 1),
+                      d.dw_k_blocks, false);
+      t.kind = KIND_DW;
+      t.dw = true;
+    }
+    t.slab = ph - 1;
+    return t;
+  }
   if constexpr (MODE == MODE_DHDW) {
     if (u >= d.dh_units) {
       Unit t = decode_grid(u - d.dh_units, p.dw_m_tiles, p.dw_n_tiles, p.dw_n_tiles, 1, p.dw_group_m,
@@ -346,6 +467,130 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return true;
 }
 
+// ---- PIPE: dependency counters between the units of one launch
+//
+// Four arrays of counters, each epilogue warp of a unit adding one when its
+// share of the unit's output is in global memory: per slab and row tile, the
+// DLOGITS units done (dl_row) and the DH units done (dh_row); per slab and
+// BN-wide vocabulary tile, the DLOGITS units done (dl_col) and the DW units
+// done (dw_col).  D holds two slabs (slab s in buffer s % 2), so
+//   - a DH unit of slab s reads D rows of its row tile over the slab: it waits
+//     for dl_row[s][m], and, so that the dH partials are summed slab after
+//     slab, for dh_row[s - 1][m];
+//   - a DW unit reads D columns of its vocabulary tile over all rows: it
+//     waits for dl_col[s][vt];
+//   - a DLOGITS unit of slab s overwrites a tile of the buffer that slab
+//     s - 2's DH units of its row tile and DW units of its vocabulary tile
+//     read: it waits for dh_row[s - 2][m] and dw_col[s - 2][vt].
+// Units run in phases (phase p: slab p's DLOGITS units, then slab p - 1's DH
+// and DW units), so every wait is on units of an earlier phase, i.e. earlier
+// in the unit order; with all CTAs of the grid resident at once (the grid is
+// the device's co-resident cluster count), the lowest unfinished unit can
+// always run.  Slab s + 1's dlogits are formed while slab s's dH and dW run.
+struct PipeDeps {
+  int mt_cap, vt_cap, slabs;
+  __device__ __forceinline__ int dl_row(int s, int m) const { return s * mt_cap + m; }
+  __device__ __forceinline__ int dh_row(int s, int m) const { return (slabs + s) * mt_cap + m; }
+  __device__ __forceinline__ int dl_col(int s, int vt) const { return 2 * slabs * mt_cap + s * vt_cap + vt; }
+  __device__ __forceinline__ int dw_col(int s, int vt) const {
+    return 2 * slabs * mt_cap + (slabs + s) * vt_cap + vt;
+  }
+};
+
+__device__ __forceinline__ PipeDeps pipe_deps(const GemmParams& p) {
+  return PipeDeps{p.m_tiles, (p.pp_vs + BN - 1) / BN, p.pp_slabs};
+}
+
+// Bounded wait until counter c reaches target.  Gives up (raising the CTA's
+// abort flag) when another role of the CTA has aborted, when another CTA has
+// raised the device error word, or when the limit runs out (raising it).
+__device__ __forceinline__ bool pipe_wait(const unsigned* c, unsigned target, volatile int* abort_flag,
+                                          int* err) {
+  if (target == 0 || ld_acquire_gpu(c) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(c) < target) {
+    if (*abort_flag) return false;
+    if (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT) {
+      *abort_flag = 1;
+      return false;
+    }
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      *abort_flag = 1;
+      atomicOr(err, DEVERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(100);
+  }
+  return true;
+}
+
+// The waits of unit t before its operands are loaded (ARR arrivals per
+// unit: one per epilogue warp of each CTA).  Run by the dependency warp; the
+// producer then orders its bulk loads after them (fence.proxy.async).
+template <int TM, int ARR>
+__device__ __forceinline__ bool pipe_wait_deps(const GemmParams& p, const DynShape& d, const Unit& t,
+                                               volatile int* abort_flag) {
+  const PipeDeps g = pipe_deps(p);
+  const unsigned* c = p.pp_dep;
+  bool ok = true;
+  if (t.kind == KIND_DH) {
+    const PipeSlab q = pipe_slab<TM>(p, d, t.slab);
+    ok = pipe_wait(c + g.dl_row(t.slab, t.m), q.vt * ARR, abort_flag, p.err);
+    if (ok && t.slab > 0) {
+      const PipeSlab qp = pipe_slab<TM>(p, d, t.slab - 1);
+      ok = pipe_wait(c + g.dh_row(t.slab - 1, t.m), qp.splits * p.n_tiles * ARR, abort_flag, p.err);
+    }
+  } else if (t.kind == KIND_DW) {
+    ok = pipe_wait(c + g.dl_col(t.slab, t.m * TM / BN), d.m_tiles * ARR, abort_flag, p.err);
+  } else if (t.slab > 1) {
+    // DLOGITS over a tile of the buffer that slab s - 2 read
+    const PipeSlab q = pipe_slab<TM>(p, d, t.slab - 2);
+    const int vt = t.n0;
+    const int dw_in = min(BN / TM, q.dwt - vt * (BN / TM));  // DW vocabulary tiles inside it
+    ok = pipe_wait(c + g.dh_row(t.slab - 2, t.m), q.splits * p.n_tiles * ARR, abort_flag, p.err) &&
+         pipe_wait(c + g.dw_col(t.slab - 2, vt), q.n_dw > 0 ? dw_in * p.n_tiles * ARR : 0, abort_flag,
+                   p.err);
+  }
+  return ok;
+}
+
+// Producer side of the dependency warp (PIPE): bounded wait until this
+// worker's unit k is marked ready, giving up when another role of the CTA
+// has aborted or the limit runs out.
+__device__ __forceinline__ bool wait_units_ready(volatile int* ready, int k, volatile int* abort_flag,
+                                                 int* err) {
+  if (*ready > k) {
+    __threadfence_block();
+    return true;
+  }
+  const long long t0 = clock64();
+  while (*ready <= k) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      *abort_flag = 1;
+      atomicOr(err, DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  __threadfence_block();
+  return true;
+}
+
+// This epilogue warp's share of unit t is complete in global memory: count it.
+template <int TM>
+__device__ __forceinline__ void pipe_signal(const GemmParams& p, const Unit& t) {
+  const PipeDeps g = pipe_deps(p);
+  unsigned* c = p.pp_dep;
+  if (t.kind == KIND_DL) {
+    red_release_gpu_add(c + g.dl_row(t.slab, t.m), 1u);
+    red_release_gpu_add(c + g.dl_col(t.slab, t.n0), 1u);
+  } else if (t.kind == KIND_DH) {
+    red_release_gpu_add(c + g.dh_row(t.slab, t.m), 1u);
+  } else {
+    red_release_gpu_add(c + g.dw_col(t.slab, t.m * TM / BN), 1u);
+  }
+}
+
 // Bounded wait used only while shutting down (copies or MMAs in flight).
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int* err) {
   const long long t0 = clock64();
@@ -367,12 +612,15 @@ __device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap* map, uin
 }
 
 // One pipeline stage of this CTA: its BM rows of A and its B_ROWS rows of B.
-// `bar` is the full barrier of the MMA-issuing CTA (cluster address for CG 2).
+// `bar` is the full barrier of the MMA-issuing CTA (cluster address for CG 2);
+// v0 is the first vocabulary column of the unit's slab, doff the first row of
+// its D buffer (DH, DW).
 template <int MODE, int CG, bool kF8 = false>
 __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensorMap* tB,
                                            const CUtensorMap* tA2, const CUtensorMap* tB2,
                                            uint32_t sA, uint32_t sB, uint32_t bar,
-                                           const GemmParams& p, int m, int n, int kb, int rank) {
+                                           const GemmParams& p, int m, int n, int kb, int rank, int v0,
+                                           int doff = 0) {
   using C = TileCfg<CG>;
   // one stage row is 128 bytes of K: 64 bf16 or 128 e4m3 elements
   constexpr int BK = kF8 ? 128 : flce::BK;
@@ -383,24 +631,24 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
     const bool teacher = kb >= p.k_blocks_s;
     const int kk = teacher ? kb - p.k_blocks_s : kb;
     tma_ld<MODE, CG>(sA, teacher ? tA2 : tA, bar, kk * BK, p.row0 + a0);
-    tma_ld<MODE, CG>(sB, teacher ? tB2 : tB, bar, kk * BK, p.v0 + b0);
+    tma_ld<MODE, CG>(sB, teacher ? tB2 : tB, bar, kk * BK, v0 + b0);
   } else if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD || MODE == MODE_DLOGITS) {
     // A = h rows (K-major, box 64 x 128), B = W vocabulary rows (K-major, box 64 x B_ROWS)
     tma_ld<MODE, CG>(sA, tA, bar, kb * BK, p.row0 + a0);
-    tma_ld<MODE, CG>(sB, tB, bar, kb * BK, p.v0 + b0);
+    tma_ld<MODE, CG>(sB, tB, bar, kb * BK, v0 + b0);
   } else if constexpr (MODE == MODE_DH) {
     // A = D rows of this chunk (K-major over the slab's vocabulary), B = W
     // with the hidden dimension contiguous (MN-major): 64-wide boxes
-    tma_ld<MODE, CG>(sA, tA, bar, kb * BK, a0);
+    tma_ld<MODE, CG>(sA, tA, bar, kb * BK, doff + a0);
 #pragma unroll
     for (int j = 0; j < C::B_ROWS / 64; ++j)
-      tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, p.v0 + kb * BK);
+      tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, v0 + kb * BK);
   } else {
     static_assert(MODE == MODE_DW, "every mode needs its operand loads");
     // A = D^T (vocabulary contiguous: MN-major), B = h (hidden contiguous:
     // MN-major); K runs over the chunk's rows
 #pragma unroll
-    for (int j = 0; j < 2; ++j) tma_ld<MODE, CG>(sA + j * MN_BOX_BYTES, tA, bar, a0 + 64 * j, kb * BK);
+    for (int j = 0; j < 2; ++j) tma_ld<MODE, CG>(sA + j * MN_BOX_BYTES, tA, bar, a0 + 64 * j, doff + kb * BK);
 #pragma unroll
     for (int j = 0; j < C::B_ROWS / 64; ++j)
       tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, p.row0 + kb * BK);
@@ -478,11 +726,12 @@ __device__ __forceinline__ void stage_bf16_half(uint32_t box, int lane, int half
 }
 
 template <int MODE, bool kLong, int CG, bool kF8 = false, int EW = EPI_WARPS>
-__global__ void __launch_bounds__(gemm_threads(EW), 1)
+__global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
                      const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC2,
-                     const __grid_constant__ GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB3,
+                     const __grid_constant__ CUtensorMap tmC3, const __grid_constant__ GemmParams p) {
   using idx_t = typename std::conditional<kLong, long long, int>::type;
   using C = TileCfg<CG>;
   using K = KernelCfg<MODE, CG, EW>;
@@ -504,6 +753,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
   const uint32_t drain = bar0 + 8u * (2 * NST + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // PIPE: how many of this worker's units have their dependencies met
+  volatile int* units_ready = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -525,12 +776,17 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *units_ready = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (is_kd<MODE>() || MODE == MODE_DHDW) {
+    if constexpr (is_kd<MODE>() || MODE == MODE_DHDW || MODE == MODE_PIPE) {
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
+    }
+    if constexpr (MODE == MODE_PIPE) {
+      tma_prefetch_desc(&tmA3);
+      tma_prefetch_desc(&tmB3);
     }
   }
   if constexpr (CG == 2) cluster_sync();  // peer barriers exist before any remote signal
@@ -553,6 +809,13 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
   grid_dependency_wait();
   grid_launch_dependents();
   const DynShape dsh = dyn_shape<MODE, C::TM>(p);
+  if constexpr (MODE == MODE_PIPE) {
+    // the next launch's counters start at zero (the previous launch, which
+    // used them, has completed)
+    if (p.pp_dep_zero != nullptr)
+      for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.pp_dep_words; i += gridDim.x * blockDim.x)
+        p.pp_dep_zero[i] = 0u;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -560,8 +823,19 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
-        const Unit t = decode_unit<MODE>(p, dsh, u);
+      int k_unit = 0;
+      for (int u = worker; u < dsh.num_units && ok; u += nworkers, ++k_unit) {
+        const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
+        if constexpr (MODE == MODE_PIPE) {
+          // the dependency warp has seen this unit's inputs published
+          if (!wait_units_ready(units_ready, k_unit, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // the bulk loads below read what was published
+        }
+        const int uv0 = MODE == MODE_PIPE ? t.slab * p.pp_vs : p.v0;  // the unit's first vocabulary column
+        const int udoff = MODE == MODE_PIPE ? (t.slab & 1) * p.rows_cap : 0;  // its D buffer
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           for (int kb = t.kb0; kb < t.kb1; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
@@ -572,15 +846,19 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
             uint32_t fb = full_bar(stage);
             if constexpr (CG == 2) fb = mapa_shared(fb, 0);
             if (issuer) mbar_arrive_expect_tx(full_bar(stage), C::STAGE * CG);
-            if constexpr (MODE == MODE_DHDW) {
+            if constexpr (MODE == MODE_DHDW || MODE == MODE_PIPE) {
               if (t.dw)
                 load_stage<MODE_DW, CG>(&tmA2, &tmB2, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
-                                        rank);
+                                        rank, uv0, udoff);
+              else if (MODE == MODE_PIPE && t.kind == KIND_DL)
+                load_stage<MODE_DLOGITS, CG>(&tmA3, &tmB3, &tmA3, &tmB3, sA, sA + C::A_BYTES, fb, p, t.m, n,
+                                             kb, rank, uv0);
               else
-                load_stage<MODE_DH, CG>(&tmA, &tmB, &tmA, &tmB, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank);
+                load_stage<MODE_DH, CG>(&tmA, &tmB, &tmA, &tmB, sA, sA + C::A_BYTES, fb, p, t.m, n, kb, rank,
+                                        uv0, udoff);
             } else {
               load_stage<MODE, CG, kF8>(&tmA, &tmB, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
-                                        rank);
+                                        rank, uv0);
             }
             ++issued;
             if (++stage == NST) {
@@ -603,7 +881,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
-        const Unit t = decode_unit<MODE>(p, dsh, u);
+        const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -622,9 +900,11 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
               const bool teacher = kb >= p.k_blocks_s;
               mma_stage<MODE, CG>(d_tmem + (teacher ? BN : 0), sA, sA + C::A_BYTES,
                                   kb == t.kb0 || kb == p.k_blocks_s);
-            } else if constexpr (MODE == MODE_DHDW) {
+            } else if constexpr (MODE == MODE_DHDW || MODE == MODE_PIPE) {
               if (t.dw)
                 mma_stage<MODE_DW, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
+              else if (MODE == MODE_PIPE && t.kind == KIND_DL)
+                mma_stage<MODE_DLOGITS, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
               else
                 mma_stage<MODE_DH, CG>(d_tmem, sA, sA + C::A_BYTES, kb == t.kb0);
             } else {
@@ -652,6 +932,22 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       drain_bar(drain, 0, p.err);
     }
     __syncwarp();
+  } else if (MODE == MODE_PIPE && warp == 2 + EW) {
+    // ------------------------------------------------------- dependencies
+    // (PIPE) waits, unit by unit of this worker, until the units whose
+    // output it reads or overwrites are counted, and tells the producer
+    if constexpr (MODE == MODE_PIPE) {
+      if (lane == 0) {
+        int k_unit = 0;
+        for (int u = worker; u < dsh.num_units; u += nworkers, ++k_unit) {
+          const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
+          if (!pipe_wait_deps<C::TM, EW * CG>(p, dsh, t, abort_flag)) break;
+          __threadfence_block();
+          *units_ready = k_unit + 1;
+        }
+      }
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
@@ -659,7 +955,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     // columns of the tile this warp takes: all, or one half (8 epilogue warps)
     static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && wide_epilogue_mode<MODE>()) ||
                       (EW == 4 * EPI_WARPS && MODE == MODE_DW),
-                  "8 epilogue warps: dW, DHDW, the two-head dlogits and the Jensen-Shannon terms; "
+                  "8 epilogue warps: dW, DHDW, the dlogits modes, PIPE and the Jensen-Shannon terms; "
                   "16: dW only");
     constexpr int kColParts = EW / 4;
     constexpr int kChunks = BN / 32 / kColParts;
@@ -673,7 +969,11 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
-      const Unit t = decode_unit<MODE>(p, dsh, u);
+      const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
+      // PIPE: the unit's kind (else the mode's) and its slab's first column
+      const bool unit_dl = MODE == MODE_DLOGITS || (MODE == MODE_PIPE && t.kind == KIND_DL);
+      const int uv0 = MODE == MODE_PIPE ? t.slab * p.pp_vs : p.v0;
+      const int udoff = MODE == MODE_PIPE ? (t.slab & 1) * p.rows_cap : 0;  // D buffer of the slab
       // per-unit row state
       const int lr = t.m * C::TM + rank * BM + r;  // row inside this pass (original row: grow)
       bool row_ok;
@@ -687,7 +987,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       const float lin_a = p.tf_softcap ? 1.f : p.tf_a;
       const float l2a = kLog2e * lin_a;
       // DHDW: this unit's kind (a DW unit's accumulator rows are vocabulary rows)
-      const bool unit_dw = MODE == MODE_DW || (MODE == MODE_DHDW && t.dw);
+      const bool unit_dw = MODE == MODE_DW || ((MODE == MODE_DHDW || MODE == MODE_PIPE) && t.dw);
       if (unit_dw) {
         row_ok = lr < p.V;  // rows of the accumulator are vocabulary rows here
       } else {
@@ -696,7 +996,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
       // original row of this accumulator row (targets, weights, lse, dH;
       // the forward modes' partials and target logit)
       int grow = p.row0 + lr;
-      if constexpr (rows_are_tokens<MODE>() || MODE == MODE_DHDW) {
+      if constexpr (rows_are_tokens<MODE>() || MODE == MODE_DHDW || MODE == MODE_PIPE) {
         if (!unit_dw && p.row_idx != nullptr) grow = row_ok ? p.row_idx[p.chunk_first + lr] : 0;
       }
       // DLOGITS also writes zero rows up to the next 64-row K block so that
@@ -709,7 +1009,7 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
           if (row_ok) a_sc = p.a_scale[grow];
         }
       }
-      if constexpr (MODE == MODE_DLOGITS) {
+      if (unit_dl) {
         if (row_ok) {
           tgt = p.targets[grow];
           const bool valid = tgt != p.ignore_index;
@@ -820,9 +1120,9 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
               const float z = select32(v, static_cast<int>(tj)) * lin_a;
               if (row_ok) p.zt[grow] = z;
             }
-          } else if constexpr (MODE == MODE_DLOGITS) {
+          } else if (unit_dl) {
             uint32_t pk[16];
-            const int gcol0 = p.v0 + col0;  // vocabulary column of D's local column col0
+            const int gcol0 = uv0 + col0;  // vocabulary column of D's local column col0
             const long long tjl = tgt - gcol0;
             const int tj = (tjl >= 0 && tjl < 32) ? static_cast<int>(tjl) : -1;
             if (!p.tf_softcap && tj < 0 && gcol0 + 32 <= p.V) {
@@ -883,7 +1183,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
                 if (lane == 0) {
                   const int lrow0 = t.m * C::TM + rank * BM + q * 32;
                   const int x = col0 - 32;  // first column of the box
-                  if (x < p.ldD && lrow0 < p.rows_cap) tma_store_2d(&tmC, box, x, lrow0);
+                  if (x < p.ldD && lrow0 < p.rows_cap)
+                    tma_store_2d(MODE == MODE_PIPE ? &tmC3 : &tmC, box, x, udoff + lrow0);
                   bulk_commit();
                 }
               }
@@ -1086,17 +1387,18 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
               int oy;
               bool inside, accumulate;
               if (unit_dw) {
-                oy = p.v0 + lrow0;  // vocabulary row of dW
+                oy = uv0 + lrow0;  // vocabulary row of dW
                 inside = oy < p.V;
                 accumulate = p.dW_accumulate != 0;
               } else {
                 // partial sums of k-split t.split: rows [split * rows_cap, +rows_cap)
                 oy = t.split * p.rows_cap + lrow0;
                 inside = lrow0 < p.rows_cap;
-                accumulate = p.dh_accumulate != 0;
+                // PIPE: a plain store on the block's first slab
+                accumulate = MODE == MODE_PIPE ? t.slab > 0 : p.dh_accumulate != 0;
               }
               // DHDW: dW goes through tmC2, the dH partials through tmC
-              const CUtensorMap* omap = (MODE == MODE_DHDW && unit_dw) ? &tmC2 : &tmC;
+              const CUtensorMap* omap = ((MODE == MODE_DHDW || MODE == MODE_PIPE) && unit_dw) ? &tmC2 : &tmC;
               if (col0 < p.H && inside) {
                 if (accumulate)
                   tma_reduce_add_2d(omap, box, col0, oy);
@@ -1120,6 +1422,16 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
           acc_phase ^= 1u;
         }
       }
+      if constexpr (MODE == MODE_PIPE) {
+        // this warp's boxes of the unit are in global memory before it
+        // counts them (each epilogue warp of each CTA counts once)
+        if (ok && lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          pipe_signal<C::TM>(p, t);
+        }
+        __syncwarp();
+      }
       if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD) {
         if (ok && row_ok)
           p.partials[static_cast<idx_t>(t.split) * p.N + grow] = make_float2(run_m, run_s);
@@ -1141,7 +1453,8 @@ __global__ void __launch_bounds__(gemm_threads(EW), 1)
     }
   }
 
-  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DHDW || MODE == MODE_DLOGITS) {
+  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DHDW || MODE == MODE_DLOGITS ||
+                MODE == MODE_PIPE) {
     if (warp >= 2 && lane == 0) bulk_wait_all();  // output boxes written before the CTA retires
   }
   __syncthreads();

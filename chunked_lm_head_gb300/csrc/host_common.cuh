@@ -18,14 +18,15 @@ constexpr int kDefaultSms = 152;
 
 enum Kind {
   K_PREP, K_FWD, K_COMBINE, K_FINAL, K_DLOGITS, K_DH, K_DH_REDUCE, K_DW, K_COMPACT, K_GATHER,
-  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_JSD_FWD, K_JSD_DLOGITS, K_GRPO, K_DHDW, K_COUNT
+  K_KD_FWD, K_KD_DLOGITS, K_QUANT, K_JSD_FWD, K_JSD_DLOGITS, K_GRPO, K_DHDW, K_PIPE, K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {"prep_targets",  "fwd_logits_lse", "fwd_combine",
                                          "fwd_loss",      "bwd_dlogits",    "bwd_dH",
                                          "bwd_dH_reduce", "bwd_dW",         "bwd_compact_rows",
                                          "bwd_gather_rows", "kd_fwd_logits",  "kd_bwd_dlogits",
                                          "quantize_e4m3", "jsd_fwd_terms",  "jsd_bwd_dlogits",
-                                         "grpo_token_loss", "bwd_dH_dW"};
+                                         "grpo_token_loss", "bwd_dH_dW",
+                                         "bwd_pipeline"};
 
 struct ProfRec {
   int kind;

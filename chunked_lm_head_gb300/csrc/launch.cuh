@@ -103,15 +103,21 @@ cudaError_t launch_persistent(Kern k, int grid, int cluster, int threads, int sm
   return cudaGetLastError();
 }
 
+// The operand / output maps of one launch: (a, b, c) for every mode, (a2, b2,
+// c2) for the second operand set of the two-head and DHDW modes, (a3, b3, c3)
+// for the DLOGITS units of PIPE.  Unused ones repeat (a, b, c).
+struct Maps {
+  const CUtensorMap *a, *b, *c, *a2, *b2, *c2, *a3, *b3, *c3;
+};
+
 template <int MODE, bool kLong, int CG, int EW = EPI_WARPS>
-cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                          const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
-                          const GemmParams& p, int workers, cudaStream_t st) {
+cudaError_t launch_gemm_t(const Maps& m, const GemmParams& p, int workers, cudaStream_t st) {
   auto k = flce_gemm_kernel<MODE, kLong, CG, false, EW>;
   constexpr int smem = KernelCfg<MODE, CG, EW>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_persistent(k, CG * workers, CG, gemm_threads(EW), smem, st, a, b, c, a2, b2, c2, p);
+  return launch_persistent(k, CG * workers, CG, kernel_threads<MODE>(EW), smem, st, *m.a, *m.b, *m.c, *m.a2, *m.b2,
+                           *m.c2, *m.a3, *m.b3, *m.c3, p);
 }
 
 // dW over at most this many K blocks (64 rows each) runs 8 epilogue warps:
@@ -127,45 +133,48 @@ template <int MODE>
 cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st,
                         const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr,
-                        const CUtensorMap* c2 = nullptr) {
+                        const CUtensorMap* c2 = nullptr, const CUtensorMap* a3 = nullptr,
+                        const CUtensorMap* b3 = nullptr, const CUtensorMap* c3 = nullptr) {
   // a2 / b2: the teacher's operands of the distillation modes, or the DW
-  // units' operands of DHDW, whose dW output map is c2 (else unused)
-  const CUtensorMap& A2 = a2 ? *a2 : a;
-  const CUtensorMap& B2 = b2 ? *b2 : b;
-  const CUtensorMap& C2 = c2 ? *c2 : c;
+  // units' operands of DHDW and PIPE, whose dW output map is c2; a3 / b3 /
+  // c3: the DLOGITS units' operands and D output of PIPE (else unused)
+  const Maps mp{&a, &b, &c, a2 ? a2 : &a, b2 ? b2 : &b, c2 ? c2 : &c, a3 ? a3 : &a, b3 ? b3 : &b,
+                c3 ? c3 : &c};
   if constexpr (wide_epilogue_mode<MODE>()) {
     // the Jensen-Shannon forward's caller sized the partials for the column
     // parts it chose
     const bool wide = MODE == MODE_DW         ? p.k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_DHDW    ? p.dw_k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_JSD_FWD ? p.col_parts == 2
-                                             : wide_epilogue_on();
+                      : (MODE == MODE_DLOGITS || MODE == MODE_PIPE)
+                          ? opt(FLCE_OPT_DLOGITS_EPILOGUE_WARPS) == 8
+                          : wide_epilogue_on();
     if constexpr (MODE == MODE_DW) {
       // short K: 16 epilogue warps (default; FLCE_OPT_DW_EPILOGUE_WARPS = 8
       // keeps 8)
       if (wide && opt(FLCE_OPT_DW_EPILOGUE_WARPS) == 16) {
         constexpr int EW = 4 * EPI_WARPS;
         if (cg == 2)
-          return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, C2, p, workers, st)
-                       : launch_gemm_t<MODE, false, 2, EW>(a, b, c, A2, B2, C2, p, workers, st);
-        return kLong ? launch_gemm_t<MODE, true, 1, EW>(a, b, c, A2, B2, C2, p, workers, st)
-                     : launch_gemm_t<MODE, false, 1, EW>(a, b, c, A2, B2, C2, p, workers, st);
+          return kLong ? launch_gemm_t<MODE, true, 2, EW>(mp, p, workers, st)
+                       : launch_gemm_t<MODE, false, 2, EW>(mp, p, workers, st);
+        return kLong ? launch_gemm_t<MODE, true, 1, EW>(mp, p, workers, st)
+                     : launch_gemm_t<MODE, false, 1, EW>(mp, p, workers, st);
       }
     }
     if (wide) {
       constexpr int EW = 2 * EPI_WARPS;
       if (cg == 2)
-        return kLong ? launch_gemm_t<MODE, true, 2, EW>(a, b, c, A2, B2, C2, p, workers, st)
-                     : launch_gemm_t<MODE, false, 2, EW>(a, b, c, A2, B2, C2, p, workers, st);
-      return kLong ? launch_gemm_t<MODE, true, 1, EW>(a, b, c, A2, B2, C2, p, workers, st)
-                   : launch_gemm_t<MODE, false, 1, EW>(a, b, c, A2, B2, C2, p, workers, st);
+        return kLong ? launch_gemm_t<MODE, true, 2, EW>(mp, p, workers, st)
+                     : launch_gemm_t<MODE, false, 2, EW>(mp, p, workers, st);
+      return kLong ? launch_gemm_t<MODE, true, 1, EW>(mp, p, workers, st)
+                   : launch_gemm_t<MODE, false, 1, EW>(mp, p, workers, st);
     }
   }
   if (cg == 2)
-    return kLong ? launch_gemm_t<MODE, true, 2>(a, b, c, A2, B2, C2, p, workers, st)
-                 : launch_gemm_t<MODE, false, 2>(a, b, c, A2, B2, C2, p, workers, st);
-  return kLong ? launch_gemm_t<MODE, true, 1>(a, b, c, A2, B2, C2, p, workers, st)
-               : launch_gemm_t<MODE, false, 1>(a, b, c, A2, B2, C2, p, workers, st);
+    return kLong ? launch_gemm_t<MODE, true, 2>(mp, p, workers, st)
+                 : launch_gemm_t<MODE, false, 2>(mp, p, workers, st);
+  return kLong ? launch_gemm_t<MODE, true, 1>(mp, p, workers, st)
+               : launch_gemm_t<MODE, false, 1>(mp, p, workers, st);
 }
 
 // The e4m3 forward: MODE_FWD with 8-bit operands.
@@ -175,7 +184,7 @@ cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_persistent(kern, grid_mult * workers, grid_mult, gemm_threads(EPI_WARPS), smem, st, a, b, b,
-                             a, b, b, p);
+                             a, b, b, a, b, b, p);
   };
   if (cg == 2)
     return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)
@@ -226,6 +235,11 @@ int device_workers(int cg) {
 // A slab's dH and dW GEMMs in one launch when the plan has several slabs
 // (default); FLCE_OPT_FUSE_DH_DW = 0 always launches them one after the other.
 bool fuse_dh_dw_on() { return opt_on(FLCE_OPT_FUSE_DH_DW); }
+
+// A backward of several vocabulary slabs runs each row block as one
+// MODE_PIPE launch (default); FLCE_OPT_PIPELINE = 0 launches a slab's
+// dlogits GEMM and its dH / dW GEMMs one after the other.
+bool pipeline_on() { return opt_on(FLCE_OPT_PIPELINE); }
 
 // Backward on non-ignored rows only (default); FLCE_OPT_COMPACT = 0 runs
 // every row.
@@ -411,6 +425,41 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     FLCE_CUDA_TRY(launch_gemm<MODE_DW>(a.cg, a.kLong, D_mn, B_dw, *a.dW_map, q,
                                        std::min(q.num_units, a.workers), st));
   }
+  return FLCE_OK;
+}
+
+// The whole backward of one row block in one MODE_PIPE launch: for each
+// vocabulary slab its dlogits units (A_dl x W_k into D through D_st), then its
+// dH and dW units as slab_dh_dw runs them.  dep: this launch's dependency
+// counters (zero at its start); dep_zero: the next launch's, which this one
+// zeroes.  The grid is every co-resident SM pair, which the units' waits on
+// one another need.
+flce_status pipe_block(const DhDwStage& a, const GemmParams& p, int rows, int block, const CUtensorMap& A_dl,
+                       const CUtensorMap& W_k, const CUtensorMap& D_st, const CUtensorMap& D_k,
+                       const CUtensorMap& D_mn, const CUtensorMap& B_dw, unsigned* dep, unsigned* dep_zero,
+                       cudaStream_t st) {
+  const BwdPlan& b = *a.plan;
+  GemmParams q = p;
+  q.m_tiles = static_cast<int>(ceil_div(rows, a.tm));  // row tiles at most (compacted: fewer)
+  q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+  q.cols = q.n_tiles;
+  q.n_per_unit = 1;
+  q.pp_slabs = b.n_slabs;
+  q.pp_vs = static_cast<int>(b.Vs);
+  q.pp_kh = static_cast<int>(ceil_div(a.H, BK));
+  q.pp_dh_kbps = b.dh_kb_per_split;
+  q.pp_dl_group = std::min(16, q.m_tiles);
+  q.group_m = dh_group_rows(q.m_tiles);
+  q.dw_group_m = static_cast<int>(std::min<long long>(8, ceil_div(b.Vs, a.tm)));
+  q.dw_k_blocks = static_cast<int>(ceil_div(rows, BK));
+  q.dH_part = a.dh_part;
+  q.dW_accumulate = block > 0 ? 1 : 0;
+  q.pp_dep = dep;
+  q.pp_dep_zero = dep_zero;
+  q.pp_dep_words = static_cast<int>(pipe_dep_words(b));
+  ProfScope ps(K_PIPE, st);
+  FLCE_CUDA_TRY(launch_gemm<MODE_PIPE>(a.cg, a.kLong, D_k, *a.W_mn, *a.dhp_map, q, a.workers, st, &D_mn, &B_dw,
+                                       a.dW_map, &A_dl, &W_k, &D_st));
   return FLCE_OK;
 }
 

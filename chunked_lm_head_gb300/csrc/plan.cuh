@@ -100,6 +100,7 @@ struct BwdPlan {
   int dh_kb_per_split = 1;
   bool dh_f32 = false;  // dH through fp32 partials (several slabs or k-splits)
   double est_s = 0.0;   // modelled time of the backward GEMMs
+  int buffers = 1;      // D buffers: 2 when the row blocks run pipelined (MODE_PIPE)
 };
 
 constexpr double kPlanFlops = 1.6e15;  // sustained bf16 tensor rate of the GPU (model)
@@ -136,8 +137,10 @@ int dh_split_count(long long tiles, long long kb, int workers) {
 
 // Completes plan b for row block size R (D budget in elements): slab width,
 // dH splits, memory check and modelled time.  False when R does not fit.
+// pipelined: the row block runs as one launch (MODE_PIPE), so its slabs pay
+// no launch cost of their own.
 bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long R,
-                    long long budget, int workers, int tm) {
+                    long long budget, int workers, int tm, bool pipelined = false) {
   const long long ldV = round_up(V, 8);
   b.R = R;
   if (R * ldV <= budget) {
@@ -160,14 +163,16 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
   auto aux = [&](int splits, bool f32) {
     return (f32 ? static_cast<double>(splits) * R * H * 4 : 0.0) + static_cast<double>(R) * H * 2;
   };
-  while (s > 1 && aux(s, true) > 2.0 * budget) {
+  // (a pipelined plan's budget is one of two buffers: the bound is the whole)
+  const double aux_cap = 2.0 * budget * (pipelined ? 2 : 1);
+  while (s > 1 && aux(s, true) > aux_cap) {
     --s;
     b.dh_kb_per_split = static_cast<int>(ceil_div(kb, s));
     s = static_cast<int>(ceil_div(kb, b.dh_kb_per_split));
   }
   b.dh_splits = s;
   b.dh_f32 = b.n_slabs > 1 || s > 1;
-  if (b.n_slabs > 1 && aux(s, b.dh_f32) > 2.0 * budget) return false;
+  if (b.n_slabs > 1 && aux(s, b.dh_f32) > aux_cap) return false;
 
   // modelled time: per launch max(tensor time, HBM operand time) + the
   // exposed share of the fp32 output traffic + launch cost
@@ -192,7 +197,7 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
     t += std::max(waves(vt * ceil_div(H, BN)) * ceil_div(rows, BK) * t_kb,
                   (d_bytes + 2.0 * rows * H * ceil_div(vt, 8)) / kPlanBytes) +
          kPlanRmwExposed * 4.0 * w * H * (first_block ? 1 : 2) / kPlanBytes;
-    return t + 3 * kPlanLaunch;
+    return t + (pipelined ? 0.0 : 3 * kPlanLaunch);
   };
   auto block_cost = [&](long long rows, bool first_block) {
     const long long w_last = V - (b.n_slabs - 1) * b.Vs;
@@ -215,30 +220,34 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
 // instead of the modelled choice.
 long long bwd_rows_forced() { return opt(FLCE_OPT_BWD_ROWS); }
 
+// buffers = 2: the plan of one of two D buffers that share the budget (the
+// pipelined row blocks); R = 0 when no row block fits.
 BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_rows, int workers,
-                      int tm) {
+                      int tm, int buffers = 1) {
   N = std::max(1LL, N);
   const long long nr = round_up(N, BM);
   const long long R0 = std::min(round_up(std::max(1LL, chunk_rows), BM), nr);
-  const long long budget = R0 * round_up(V, 8);
+  const long long budget = R0 * round_up(V, 8) / buffers;
   workers = std::max(1, workers);
   struct Key {
     long long N, H, V, R0, forced;
-    int workers, tm;
+    int workers, tm, buffers;
   };
-  thread_local Key last{-1, -1, -1, -1, -1, -1, -1};
+  thread_local Key last{-1, -1, -1, -1, -1, -1, -1, -1};
   thread_local BwdPlan last_plan;
   const long long forced = bwd_rows_forced();
   if (last.N == N && last.H == H && last.V == V && last.R0 == R0 && last.forced == forced &&
-      last.workers == workers && last.tm == tm)
+      last.workers == workers && last.tm == tm && last.buffers == buffers)
     return last_plan;
 
   BwdPlan best;
-  plan_candidate(best, N, H, V, R0, budget, workers, tm);  // the caller's chunk: always fits
+  // the caller's chunk: always fits one buffer; half of it may not
+  const bool piped = buffers == 2;
+  if (!plan_candidate(best, N, H, V, R0, budget, workers, tm, piped)) best = BwdPlan{};
   if (forced > 0) {
     BwdPlan b;
     const long long R = std::min(nr, std::max(R0, round_up(forced, BM)));
-    if (plan_candidate(b, N, H, V, R, budget, workers, tm)) best = b;
+    if (plan_candidate(b, N, H, V, R, budget, workers, tm, piped)) best = b;
   } else {
     // larger row blocks in steps of one tile; a plan with vocabulary slabs
     // must beat the single-slab chunk plan by 5 % (the model misses some of
@@ -248,15 +257,31 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
     const bool single = best.n_slabs == 1;
     for (long long R = round_up(R0 + 1, tm); R <= round_up(nr, tm); R += tm) {
       BwdPlan b;
-      if (!plan_candidate(b, N, H, V, std::min(R, nr), budget, workers, tm)) break;
+      if (!plan_candidate(b, N, H, V, std::min(R, nr), budget, workers, tm, piped)) break;
       const double margin = (single && best.R == R0) ? 0.95 : 0.98;
-      if (b.est_s < best.est_s * margin) best = b;
+      if (best.R == 0 || b.est_s < best.est_s * margin) best = b;
       if (R >= nr) break;
     }
   }
-  last = Key{N, H, V, R0, forced, workers, tm};
+  last = Key{N, H, V, R0, forced, workers, tm, buffers};
   last_plan = best;
   return best;
+}
+
+// The plan a backward call runs.  With several vocabulary slabs, both
+// gradients wanted and pipelining on (FLCE_OPT_PIPELINE, dlogits written
+// through TMA), the row blocks run pipelined (MODE_PIPE) over two D buffers
+// that together stay within the dlogits budget, so that slab s + 1's
+// dlogits are formed while slab s's dH and dW run: the plan of half the
+// budget.  Otherwise the plain plan.
+BwdPlan plan_backward_call(long long N, long long H, long long V, long long chunk_rows, int workers, int tm,
+                           bool both) {
+  const BwdPlan b = plan_backward(N, H, V, chunk_rows, workers, tm);
+  if (!both || b.n_slabs <= 1 || !opt_on(FLCE_OPT_PIPELINE) || !opt_on(FLCE_OPT_D_TMA)) return b;
+  BwdPlan q = plan_backward(N, H, V, chunk_rows, workers, tm, 2);
+  if (q.R == 0 || q.n_slabs <= 1 || !q.dh_f32) return b;
+  q.buffers = 2;
+  return q;
 }
 
 // Forward scratch.  fb_skip > 0 adds what a forward that skips the ignored
@@ -354,17 +379,25 @@ JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f, long long H_s = 0, lo
   return L;
 }
 
+// Dependency counters of one pipelined row-block launch (MODE_PIPE): per
+// slab, two per row tile (at most R / 128 of them) and two per BN-wide
+// vocabulary tile of the slab.
+long long pipe_dep_words(const BwdPlan& b) {
+  return 2LL * b.n_slabs * (ceil_div(b.R, BM) + ceil_div(b.Vs, BN));
+}
+
 struct BwdLayout {
-  size_t D = 0, dh_part = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, total = 0;
+  size_t D = 0, dh_part = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, dep = 0, total = 0;
 };
-// dlogits block, dH fp32 partials, validation counter, and the row
-// compaction buffers (valid-row indices, per-block counts, their total, the
-// gathered h rows of one chunk).
+// dlogits block, dH fp32 partials, validation counter, the row compaction
+// buffers (valid-row indices, per-block counts, their total, the gathered h
+// rows of one chunk), and for a pipelined plan two sets of dependency
+// counters (used by alternate row blocks).
 BwdLayout bwd_layout(long long N, long long H, const BwdPlan& b) {
   BwdLayout L;
   size_t o = 0;
   L.D = o;
-  o += align256(static_cast<size_t>(b.R) * b.ldD * 2);
+  o += align256(static_cast<size_t>(b.buffers) * b.R * b.ldD * 2);
   L.dh_part = o;
   if (b.dh_f32) o += align256(static_cast<size_t>(b.dh_splits) * b.R * H * 4);
   L.bad = o;
@@ -377,8 +410,17 @@ BwdLayout bwd_layout(long long N, long long H, const BwdPlan& b) {
   o += 256;
   L.hc = o;
   o += align256(static_cast<size_t>(b.R) * H * 2);
+  L.dep = o;
+  if (b.buffers == 2) o += align256(static_cast<size_t>(2 * pipe_dep_words(b)) * 4);
   L.total = o;
   return L;
+}
+
+// Workspace a backward call may need for these sizes: the larger of the
+// plain plan's and the pipelined plan's (the call takes one of them).
+size_t bwd_workspace(long long N, long long H, long long V, long long chunk_rows, int workers, int tm) {
+  return std::max(bwd_layout(N, H, plan_backward(N, H, V, chunk_rows, workers, tm)).total,
+                  bwd_layout(N, H, plan_backward_call(N, H, V, chunk_rows, workers, tm, true)).total);
 }
 
 // The distillation backward: the backward's buffers (student width) and one

@@ -573,6 +573,9 @@ typedef struct flce_backward_plan_info {
   int64_t dh_splits;        /* k-splits of the dH GEMM (fp32 partial sets) */
   int64_t dlogits_bytes;    /* bytes of the dlogits block: R * row pitch * 2 */
   int64_t workspace_bytes;  /* flce_backward's whole workspace for these sizes */
+  int64_t dlogits_buffers;  /* 1, or 2 when the row blocks run pipelined: slab s + 1's dlogits
+                               formed while slab s's dH and dW run (both gradients wanted,
+                               several slabs; dlogits_bytes covers both buffers) */
 } flce_backward_plan_info;
 
 /* Backward tiling that flce_backward uses for N, H, V, chunk_rows on a GPU
@@ -637,6 +640,12 @@ typedef enum flce_option {
                                0 = always two launches */
   FLCE_OPT_DW_EPILOGUE_WARPS,  /* FLCE_DW_EPILOGUE_WARPS: epilogue warps of the dW GEMM at
                                   short K (at most 1,024 rows): 16 (default) or 8 */
+  FLCE_OPT_PIPELINE,        /* FLCE_PIPELINE: 1 = a backward of several vocabulary slabs runs
+                               each row block in one launch, its units ordered by device-side
+                               counters (default), 0 = two launches per slab */
+  FLCE_OPT_DLOGITS_EPILOGUE_WARPS,  /* FLCE_DLOGITS_EPILOGUE_WARPS: epilogue warps of the
+                                       cross-entropy dlogits GEMM and of the pipelined row
+                                       block: 4 (default) or 8 (one operand stage fewer) */
   FLCE_OPT_COUNT
 } flce_option;
 

@@ -94,8 +94,15 @@ def test_backward_plan_prefers_row_blocks_over_literal_small_chunks():
 
 def test_backward_plan_row_override(flce_opts):
     flce_opts.set("bwd_rows", "768")
+    flce_opts.set("pipeline", "0")  # one dlogits buffer
     p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
     assert (p["rows_per_block"], p["vocab_per_slab"], p["row_blocks"], p["vocab_slabs"]) == (768, 5120, 4, 4)
+    assert p["dlogits_buffers"] == 1
+    # pipelined row blocks: two buffers of half the budget each
+    flce_opts.set("pipeline", "1")
+    p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
+    assert (p["rows_per_block"], p["vocab_per_slab"], p["row_blocks"], p["vocab_slabs"]) == (768, 3072, 4, 7)
+    assert p["dlogits_buffers"] == 2 and p["dlogits_bytes"] == 2 * 768 * 3072 * 2 <= 256 * 20000 * 2
     flce_opts.set("bwd_rows", "100000")  # clamped to the problem, then to the budget
     p = _lib.flce_backward_plan(3000, 512, 20000, 256, 74, 2)
     assert p["dlogits_bytes"] <= 256 * 20000 * 2 and p["rows_per_block"] <= 3072

@@ -70,6 +70,7 @@ def test_jsd_parity_row_blocks_and_vocabulary_slabs(cg, flce_opts):
     128-row dlogits budget."""
     flce_opts.set("cta_group", cg)
     flce_opts.set("bwd_rows", "512")
+    flce_opts.set("pipeline", "0")  # the distillation backward's plan: one dlogits buffer
     case = (1100, 256, 384, 6000, 128, 0.3, {"temperature": 1.3}, True)
     plan = flce._lib.flce_backward_plan(case[0], case[1], case[3], case[4])
     assert (plan["row_blocks"], plan["vocab_slabs"], plan["vocab_per_slab"]) == (3, 5, 1280)

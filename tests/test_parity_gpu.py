@@ -373,6 +373,7 @@ def test_backward_row_blocks_and_vocabulary_slabs(cg, compact, flce_opts):
     flce_opts.set("cta_group", cg)
     flce_opts.set("compact", compact)
     flce_opts.set("bwd_rows", "768")
+    flce_opts.set("pipeline", "0")  # the per-slab launches (the pipelined blocks: test_pipelined_row_blocks)
     N, H, V, cr = 3000, 512, 20000, 256
     plan = _lib.flce_backward_plan(N, H, V, cr)
     assert (plan["rows_per_block"], plan["vocab_per_slab"]) == (768, 5120)
@@ -394,6 +395,7 @@ def test_one_launch_per_slab_for_dh_and_dw_is_bitwise_the_two_launches(cg, compa
     slab (the default plan of a large chunk) and the one-call path."""
     flce_opts.set("cta_group", cg)
     flce_opts.set("compact", compact)
+    flce_opts.set("pipeline", 0)  # the per-slab launches (the pipelined block has its own test)
     N, H, V = 3000, 512, 20000
     wl = WL.custom(f"fuse{cg}{compact}", N, H, V, 256, w_std=0.04, targets="zipf", ignore_frac=0.08,
                    seed=115)
@@ -416,11 +418,62 @@ def test_one_launch_per_slab_for_dh_and_dw_is_bitwise_the_two_launches(cg, compa
     assert_grad_close(np64(out[0][1]), ref.dW, "dW")
 
 
+# (N, H, V, chunk_rows, row block, logit transform): 4 row blocks (the last
+# partial) x 4 slabs; an odd vocabulary with a narrow last slab, a ragged
+# hidden tile and a soft-capped, tempered logit
+PIPE_CASES = {
+    "blocks4_slabs4": (3000, 512, 20000, 256, 768, None),
+    "odd_v_softcap": (1000, 264, 7777, 128, 512, {"softcap": 20.0, "temperature": 0.8}),
+}
+
+
+@pytest.mark.parametrize("case", list(PIPE_CASES))
+@pytest.mark.parametrize("compact", ["0", "1"])
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_pipelined_row_blocks(case, cg, compact, flce_opts):
+    """A row block's dlogits, dH and dW units of every slab in one launch over
+    two dlogits buffers, ordered by device-side counters (the default with
+    several slabs): against the oracle, bitwise repeatable (every output
+    element is summed by the same unit in the same order, the dH partials
+    slab after slab), bitwise the same with 8 dlogits epilogue warps; and the
+    launch-per-slab path (one buffer of twice the slab) against the oracle."""
+    N, H, V, chunk, rows, tfd = PIPE_CASES[case]
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("compact", compact)
+    flce_opts.set("bwd_rows", rows)
+    plan = _lib.flce_backward_plan(N, H, V, chunk)
+    assert plan["dlogits_buffers"] == 2 and plan["vocab_slabs"] > 1 and plan["row_blocks"] > 1, plan
+    wl = WL.custom(f"pipe{case}{cg}{compact}", N, H, V, chunk, w_std=0.04, targets="zipf", ignore_frac=0.08,
+                   seed=118)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(15).standard_normal(N).astype(np.float32)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, chunk, transform=tfd)
+    out = []
+    for ew in (4, 4, 8):
+        flce_opts.set("dlogits_epilogue_warps", ew)
+        out.append(run_backward(h, W, t, w, lse, 1.0 / nv, chunk, transform=tfd))
+    flce_opts.set("dlogits_epilogue_warps", 4)
+    flce_opts.set("pipeline", 0)
+    assert _lib.flce_backward_plan(N, H, V, chunk)["dlogits_buffers"] == 1
+    slabs = run_backward(h, W, t, w, lse, 1.0 / nv, chunk, transform=tfd)
+    _lib.check("flce_device_status", _lib.flce_device_status())
+    for k in (0, 1):
+        for j in (1, 2):
+            assert torch.equal(out[0][k], out[j][k]), (("dH", "dW")[k], j)
+    tf = None if tfd is None else O.LogitTransform(**tfd)
+    ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / nv, tf=tf)
+    for name, got in (("pipelined", out[0]), ("per slab", slabs)):
+        assert_grad_close(np64(got[0]), ref.dH, f"dH ({name})")
+        assert_grad_close(np64(got[1]), ref.dW, f"dW ({name})")
+
+
 @pytest.mark.parametrize("cg", ["1", "2"])
 def test_schedule_options_leave_the_gradients_bitwise_unchanged(cg, flce_opts):
-    """An option that only changes the schedule: the dW epilogue with 16
-    warps at short K (the default) against 8.  Every output element is summed
-    by the same unit in the same order either way."""
+    """Options that only change the schedule: the dW epilogue with 16 warps
+    at short K (the default) against 8, and the dlogits epilogue with 8
+    warps against 4 (one slab).  Every output element is summed by the same
+    unit in the same order either way."""
     flce_opts.set("cta_group", cg)
     import chunked_lm_head_gb300 as flce
     # short K: 500 rows (8 K blocks) -> 8 or 16 dW epilogue warps
@@ -436,6 +489,9 @@ def test_schedule_options_leave_the_gradients_bitwise_unchanged(cg, flce_opts):
         outs.append(run_backward(h, W, t, w, lse, 1.0 / nv, 512))
         outs.append(tuple(flce.forward_backward(h, W, t, w, 512)[k] for k in ("dH", "dW")))
     assert torch.equal(outs[0][1], outs[2][1]) and torch.equal(outs[1][1], outs[3][1])
+    flce_opts.set("dlogits_epilogue_warps", 8)
+    d8 = run_backward(h, W, t, w, lse, 1.0 / nv, 512)
+    assert torch.equal(d8[0], outs[2][0]) and torch.equal(d8[1], outs[2][1])
     ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / nv)
     assert_grad_close(np64(outs[2][1]), ref.dW, "dW (16 epilogue warps)")
     assert_grad_close(np64(outs[3][0]), ref.dH, "dH (one call, 16 epilogue warps)")

@@ -52,6 +52,7 @@ def test_transform_parity_row_blocks_and_vocabulary_slabs(cg, flce_opts):
     columns, last block 76 rows)."""
     flce_opts.set("cta_group", cg)
     flce_opts.set("bwd_rows", "512")
+    flce_opts.set("pipeline", "0")  # the per-slab launches (the pipelined blocks: test_parity_gpu)
     tfd = CASES["softcap_temp"]
     tf = O.LogitTransform(**tfd)
     N, H, V = 1100, 192, 6000
