@@ -456,7 +456,8 @@ class BackwardPlanInfo(ctypes.Structure):
     _fields_ = [("rows_per_block", ctypes.c_int64), ("vocab_per_slab", ctypes.c_int64),
                 ("row_blocks", ctypes.c_int64), ("vocab_slabs", ctypes.c_int64),
                 ("dh_splits", ctypes.c_int64), ("dlogits_bytes", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64), ("dlogits_buffers", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("dlogits_buffers", ctypes.c_int64),
+                ("dh_wide", ctypes.c_int64)]
 
 
 def flce_backward_plan(N, H, V, chunk_rows, workers=0, cta_group=0) -> dict:
@@ -472,7 +473,7 @@ OPTIONS = {
     "cta_group": 0, "compact": 1, "validate": 2, "pdl": 3, "d_tma": 4, "wide_epilogue": 5,
     "bwd_rows": 6, "fwd_splits": 7, "dh_splits": 8, "dh_group": 9, "fwd_block_rows": 10,
     "skip_min_rows": 11, "fuse_dh_dw": 12,
-    "dw_epilogue_warps": 13, "pipeline": 14, "dlogits_epilogue_warps": 15,
+    "dw_epilogue_warps": 13, "pipeline": 14, "dlogits_epilogue_warps": 15, "dh_wide": 16,
 }
 
 

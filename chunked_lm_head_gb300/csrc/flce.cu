@@ -67,6 +67,7 @@ flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_ro
   out->dlogits_bytes = b.buffers * b.R * b.ldD * 2;
   out->workspace_bytes = static_cast<int64_t>(bwd_workspace(N, H, V, chunk_rows, w, BM * cg));
   out->dlogits_buffers = b.buffers;
+  out->dh_wide = b.dh_wide ? 1 : 0;
   return FLCE_OK;
 }
 

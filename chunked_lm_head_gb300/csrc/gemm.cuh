@@ -99,7 +99,12 @@ enum Mode : int {
   // slab its DLOGITS units (tmA3 / tmB3, D out through tmC3), then its DH
   // units (tmA / tmB, tmC) and DW units (tmA2 / tmB2, tmC2).  Units wait on
   // device-side counters for the units whose output they read or overwrite.
-  MODE_PIPE = 10
+  MODE_PIPE = 10,
+  // DH over 256 x 512 tiles (SM pairs only): each stage holds one A block and
+  // the B blocks of two adjacent 256-column tiles, whose two accumulators fill
+  // TMEM; a quarter fewer operand bytes per FLOP than two separate tiles.  For
+  // K walks long enough that the epilogue's lack of overlap does not count
+  MODE_DH2 = 11
 };
 // unit kinds of MODE_PIPE
 constexpr int KIND_DL = 0, KIND_DH = 1, KIND_DW = 2;
@@ -110,18 +115,23 @@ constexpr int KIND_DL = 0, KIND_DH = 1, KIND_DW = 2;
 // their fp32 output, not the MMAs, sets the pace.
 template <int MODE, int CG, int EW>
 struct KernelCfg {
+  static constexpr bool kWideN = MODE == MODE_DH2;  // two B tiles per stage
+  static constexpr int STAGE = TileCfg<CG>::A_BYTES + (kWideN ? 2 : 1) * TileCfg<CG>::B_BYTES;
+  static constexpr int TILE_N = (kWideN ? 2 : 1) * BN;  // accumulator columns of a unit's tile
   static constexpr bool kDeepOut = MODE == MODE_DW && EW == 16;
   // dlogits with 8 epilogue warps (alone or in PIPE): two bf16 staging boxes
   // per warp, paid for with one operand stage
   static constexpr bool kWideD = (MODE == MODE_DLOGITS || MODE == MODE_PIPE) && EW == 8;
-  static constexpr int NSTAGE =
-      kDeepOut ? (CG == 1 ? 3 : 4) : (kWideD ? TileCfg<CG>::NSTAGE - 1 : TileCfg<CG>::NSTAGE);
+  static constexpr int NSTAGE = kWideN     ? 4
+                               : kDeepOut ? (CG == 1 ? 3 : 4)
+                                          : (kWideD ? TileCfg<CG>::NSTAGE - 1 : TileCfg<CG>::NSTAGE);
   static constexpr int OUT_BYTES = kDeepOut ? EW * OUT_BOX_BYTES
                                    : kWideD ? EW * 2 * OUT_BOX_BYTES
                                             : OUT_STAGE_BYTES;
   static constexpr int BOXES_PER_WARP = OUT_BYTES / OUT_BOX_BYTES / EW > 0 ? OUT_BYTES / OUT_BOX_BYTES / EW : 1;
-  static constexpr int SMEM = 1024 + NSTAGE * TileCfg<CG>::STAGE + OUT_BYTES + SMEM_BAR_BYTES;
+  static constexpr int SMEM = 1024 + NSTAGE * STAGE + OUT_BYTES + SMEM_BAR_BYTES;
   static_assert(SMEM <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+  static_assert(!kWideN || CG == 2, "256 x 512 dH tiles run on SM pairs");
   static_assert(BOXES_PER_WARP * EW * OUT_BOX_BYTES <= OUT_BYTES, "staging boxes exceed the staging area");
 };
 template <int MODE>
@@ -643,6 +653,15 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
 #pragma unroll
     for (int j = 0; j < C::B_ROWS / 64; ++j)
       tma_ld<MODE, CG>(sB + j * MN_BOX_BYTES, tB, bar, b0 + 64 * j, v0 + kb * BK);
+  } else if constexpr (MODE == MODE_DH2) {
+    // as DH, with the B blocks of tiles 2n and 2n + 1 one after the other
+    tma_ld<MODE, CG>(sA, tA, bar, kb * BK, doff + a0);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int j = 0; j < C::B_ROWS / 64; ++j)
+        tma_ld<MODE, CG>(sB + h * C::B_BYTES + j * MN_BOX_BYTES, tB, bar,
+                         (2 * n + h) * BN + rank * C::B_ROWS + 64 * j, v0 + kb * BK);
   } else {
     static_assert(MODE == MODE_DW, "every mode needs its operand loads");
     // A = D^T (vocabulary contiguous: MN-major), B = h (hidden contiguous:
@@ -657,6 +676,12 @@ __device__ __forceinline__ void load_stage(const CUtensorMap* tA, const CUtensor
 
 template <int MODE, int CG, bool kF8 = false>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sA, uint32_t sB, bool first) {
+  if constexpr (MODE == MODE_DH2) {
+    // the two 256-column tiles of the stage into accumulators d_tmem and d_tmem + BN
+    mma_stage<MODE_DH, CG>(d_tmem, sA, sB, first);
+    mma_stage<MODE_DH, CG>(d_tmem + BN, sA, sB + TileCfg<CG>::B_BYTES, first);
+    return;
+  }
   constexpr bool A_MN = (MODE == MODE_DW);
   constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
   constexpr uint32_t IDESC = kF8 ? idesc_e4m3_f32(TileCfg<CG>::TM, BN)
@@ -738,12 +763,12 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
   constexpr int NST = K::NSTAGE;
   // accumulator buffers in TMEM: two (double-buffered) tiles, or one tile of
   // two accumulators (student, teacher) in the distillation modes
-  constexpr int NACC = is_kd<MODE>() ? 1 : 2;
+  constexpr int NACC = (is_kd<MODE>() || MODE == MODE_DH2) ? 1 : 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t out_stage = sbase + NST * C::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE + K::OUT_BYTES);
+  const uint32_t out_stage = sbase + NST * K::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * K::STAGE + K::OUT_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   // barrier layout: full[NST], empty[NST], tfull[2], tempty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -842,10 +867,10 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
               ok = false;
               break;
             }
-            const uint32_t sA = sbase + stage * C::STAGE;
+            const uint32_t sA = sbase + stage * K::STAGE;
             uint32_t fb = full_bar(stage);
             if constexpr (CG == 2) fb = mapa_shared(fb, 0);
-            if (issuer) mbar_arrive_expect_tx(full_bar(stage), C::STAGE * CG);
+            if (issuer) mbar_arrive_expect_tx(full_bar(stage), K::STAGE * CG);
             if constexpr (MODE == MODE_DHDW || MODE == MODE_PIPE) {
               if (t.dw)
                 load_stage<MODE_DW, CG>(&tmA2, &tmB2, &tmA2, &tmB2, sA, sA + C::A_BYTES, fb, p, t.m, n, kb,
@@ -895,7 +920,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
               break;
             }
             tc_fence_after();
-            const uint32_t sA = sbase + stage * C::STAGE;
+            const uint32_t sA = sbase + stage * K::STAGE;
             if constexpr (is_kd<MODE>()) {
               const bool teacher = kb >= p.k_blocks_s;
               mma_stage<MODE, CG>(d_tmem + (teacher ? BN : 0), sA, sA + C::A_BYTES,
@@ -958,7 +983,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
                   "8 epilogue warps: dW, DHDW, the dlogits modes, PIPE and the Jensen-Shannon terms; "
                   "16: dW only");
     constexpr int kColParts = EW / 4;
-    constexpr int kChunks = BN / 32 / kColParts;
+    constexpr int kChunks = K::TILE_N / 32 / kColParts;
     const int c_lo = ((warp - 2) / 4) * kChunks;
     // TMA staging boxes of this warp (KernelCfg: 8 boxes shared by 4 or 8
     // warps, or one per warp of 16)
@@ -1054,7 +1079,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
           }
-          const int col0 = n * BN + c * 32;
+          const int col0 = n * K::TILE_N + c * 32;
           if constexpr (MODE == MODE_FWD || MODE == MODE_FUSED_FWD) {
             if constexpr (kF8) {  // dequantise: row scale x per-vocabulary-row scale
               if (col0 + 32 <= p.V) {
@@ -1356,7 +1381,8 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
                   *reinterpret_cast<uint4*>(dst + 8 * g) =
                       make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
             }
-          } else if ((MODE == MODE_DH || (MODE == MODE_DHDW && !unit_dw)) && p.dH_part == nullptr) {
+          } else if ((MODE == MODE_DH || MODE == MODE_DH2 || (MODE == MODE_DHDW && !unit_dw)) &&
+                     p.dH_part == nullptr) {
             if (row_ok) {  // the only pass over this row: bf16 dH directly
               uint16_t* dst = p.dH + static_cast<idx_t>(grow) * p.H + col0;
 #pragma unroll
@@ -1453,7 +1479,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
     }
   }
 
-  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DHDW || MODE == MODE_DLOGITS ||
+  if constexpr (MODE == MODE_DW || MODE == MODE_DH || MODE == MODE_DH2 || MODE == MODE_DHDW || MODE == MODE_DLOGITS ||
                 MODE == MODE_PIPE) {
     if (warp >= 2 && lane == 0) bulk_wait_all();  // output boxes written before the CTA retires
   }

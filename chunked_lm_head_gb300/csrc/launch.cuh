@@ -140,6 +140,11 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
   // c3: the DLOGITS units' operands and D output of PIPE (else unused)
   const Maps mp{&a, &b, &c, a2 ? a2 : &a, b2 ? b2 : &b, c2 ? c2 : &c, a3 ? a3 : &a, b3 ? b3 : &b,
                 c3 ? c3 : &c};
+  if constexpr (MODE == MODE_DH2) {  // SM pairs only
+    (void)cg;
+    return kLong ? launch_gemm_t<MODE, true, 2>(mp, p, workers, st)
+                 : launch_gemm_t<MODE, false, 2>(mp, p, workers, st);
+  } else {
   if constexpr (wide_epilogue_mode<MODE>()) {
     // the Jensen-Shannon forward's caller sized the partials for the column
     // parts it chose
@@ -175,6 +180,7 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
                  : launch_gemm_t<MODE, false, 2>(mp, p, workers, st);
   return kLong ? launch_gemm_t<MODE, true, 1>(mp, p, workers, st)
                : launch_gemm_t<MODE, false, 1>(mp, p, workers, st);
+  }
 }
 
 // The e4m3 forward: MODE_FWD with 8-bit operands.
@@ -393,7 +399,8 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     GemmParams q = p;
     q.v0 = v0;
     q.m_tiles = static_cast<int>(ceil_div(rows, a.tm));
-    q.n_tiles = static_cast<int>(ceil_div(a.H, BN));
+    // 256 x 512 tiles: n_tiles counts pairs of 256-column tiles
+    q.n_tiles = static_cast<int>(ceil_div(a.H, b.dh_wide ? 2 * BN : BN));
     q.k_blocks = static_cast<int>(ceil_div(width, BK));
     q.cols = q.n_tiles;
     q.n_per_unit = 1;
@@ -401,12 +408,16 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     const int splits = static_cast<int>(ceil_div(q.k_blocks, q.kb_per_split));
     q.k_splits = splits;
     q.num_units = splits * q.m_tiles * q.n_tiles;
-    q.group_m = dh_group_rows(q.m_tiles);
+    q.group_m = b.dh_wide ? q.m_tiles : dh_group_rows(q.m_tiles);
     q.dH_part = b.dh_f32 ? a.dh_part : nullptr;
     q.dh_accumulate = slab > 0 ? 1 : 0;
     ProfScope ps(K_DH, st);
-    FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
-                                       std::min(q.num_units, a.workers), st));
+    if (b.dh_wide && a.cg == 2)
+      FLCE_CUDA_TRY(launch_gemm<MODE_DH2>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
+                                          std::min(q.num_units, a.workers), st));
+    else
+      FLCE_CUDA_TRY(launch_gemm<MODE_DH>(a.cg, a.kLong, D_k, *a.W_mn, b.dh_f32 ? *a.dhp_map : *a.W_mn, q,
+                                         std::min(q.num_units, a.workers), st));
   }
   if (a.dW) {  // dW[slab] (+)= D[:, slab]^T h[rows]
     GemmParams q = p;

@@ -40,6 +40,7 @@ constexpr OptionDef kOptionDefs[FLCE_OPT_COUNT] = {
     {"FLCE_DW_EPILOGUE_WARPS", 16, 8, 16},    // FLCE_OPT_DW_EPILOGUE_WARPS
     {"FLCE_PIPELINE", 1, 0, 1},               // FLCE_OPT_PIPELINE
     {"FLCE_DLOGITS_EPILOGUE_WARPS", 4, 4, 8},  // FLCE_OPT_DLOGITS_EPILOGUE_WARPS
+    {"FLCE_DH_WIDE", 1, 0, 1},                // FLCE_OPT_DH_WIDE
 };
 
 std::atomic<int64_t> g_options[FLCE_OPT_COUNT];
@@ -65,6 +66,7 @@ int64_t option_from_env(int o) {
     case FLCE_OPT_COMPACT:
     case FLCE_OPT_FUSE_DH_DW:
     case FLCE_OPT_PIPELINE:
+    case FLCE_OPT_DH_WIDE:
     case FLCE_OPT_PDL:
     case FLCE_OPT_D_TMA:
     case FLCE_OPT_WIDE_EPILOGUE:

@@ -101,7 +101,17 @@ struct BwdPlan {
   bool dh_f32 = false;  // dH through fp32 partials (several slabs or k-splits)
   double est_s = 0.0;   // modelled time of the backward GEMMs
   int buffers = 1;      // D buffers: 2 when the row blocks run pipelined (MODE_PIPE)
+  bool dh_wide = false; // dH GEMM over 256 x 512 tiles (MODE_DH2; one slab, SM pairs)
 };
+
+// The dH GEMM of a one-slab plan with at least two waves of 256 x 256 tiles
+// runs 256 x 512 tiles on SM pairs (default; FLCE_OPT_DH_WIDE = 0 keeps 256 x
+// 256): its K walk (the whole vocabulary, over a few k-splits) leaves the
+// non-overlapped epilogue small.  16,384 x 4,096 x 151,936: dH 11.7 -> 11.0
+// ms per step; with fewer tiles (256 rows) it would only cut the parallelism.
+bool dh_wide_for(int n_slabs, int tm, long long tiles, int workers) {
+  return n_slabs == 1 && tm == 2 * BM && tiles >= 2LL * workers && opt_on(FLCE_OPT_DH_WIDE);
+}
 
 constexpr double kPlanFlops = 1.6e15;  // sustained bf16 tensor rate of the GPU (model)
 constexpr double kPlanBytes = 6.0e12;  // sustained HBM bandwidth (model)
@@ -115,8 +125,7 @@ constexpr double kPlanRmwExposed = 0.7;
 
 // Best dH k-split count for `tiles` output tiles and `kb` K blocks: the
 // fewest splits whose last wave is at least 90% full (splits keep >= 8 K
-// blocks each).  FLCE_OPT_DH_SPLITS overrides it in plans made after it is
-// set.
+// blocks each).  FLCE_OPT_DH_SPLITS overrides it.
 int dh_split_count(long long tiles, long long kb, int workers) {
   if (const long long s = opt(FLCE_OPT_DH_SPLITS); s >= 1)
     return static_cast<int>(std::min<long long>({s, 16, std::max(1LL, kb / 8)}));
@@ -154,7 +163,8 @@ bool plan_candidate(BwdPlan& b, long long N, long long H, long long V, long long
     b.Vs = round_up(ceil_div(V, b.n_slabs), BN);
     b.ldD = b.Vs;
   }
-  const long long dh_tiles = ceil_div(R, tm) * ceil_div(H, BN);
+  b.dh_wide = dh_wide_for(b.n_slabs, tm, ceil_div(R, tm) * ceil_div(H, BN), workers);
+  const long long dh_tiles = ceil_div(R, tm) * ceil_div(H, b.dh_wide ? 2 * BN : BN);
   const long long kb = ceil_div(b.Vs, BK);
   int s = dh_split_count(dh_tiles, kb, workers);
   b.dh_kb_per_split = static_cast<int>(ceil_div(kb, s));
@@ -229,15 +239,18 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
   const long long R0 = std::min(round_up(std::max(1LL, chunk_rows), BM), nr);
   const long long budget = R0 * round_up(V, 8) / buffers;
   workers = std::max(1, workers);
+  // the last plan, reused while the sizes and the options it reads are the same
   struct Key {
-    long long N, H, V, R0, forced;
+    long long N, H, V, R0, forced, splits, wide;
     int workers, tm, buffers;
   };
-  thread_local Key last{-1, -1, -1, -1, -1, -1, -1, -1};
+  thread_local Key last{-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
   thread_local BwdPlan last_plan;
   const long long forced = bwd_rows_forced();
+  const long long splits_opt = opt(FLCE_OPT_DH_SPLITS), wide_opt = opt(FLCE_OPT_DH_WIDE);
   if (last.N == N && last.H == H && last.V == V && last.R0 == R0 && last.forced == forced &&
-      last.workers == workers && last.tm == tm && last.buffers == buffers)
+      last.splits == splits_opt && last.wide == wide_opt && last.workers == workers && last.tm == tm &&
+      last.buffers == buffers)
     return last_plan;
 
   BwdPlan best;
@@ -263,7 +276,7 @@ BwdPlan plan_backward(long long N, long long H, long long V, long long chunk_row
       if (R >= nr) break;
     }
   }
-  last = Key{N, H, V, R0, forced, workers, tm, buffers};
+  last = Key{N, H, V, R0, forced, splits_opt, wide_opt, workers, tm, buffers};
   last_plan = best;
   return best;
 }
@@ -468,7 +481,8 @@ FusedPlan plan_fused(long long N, long long H, long long V, long long chunk_rows
   fp.b.n_slabs = 1;
   fp.b.ldD = fp.ldD;
   const long long kb = ceil_div(V, BK);
-  int sp = dh_split_count(ceil_div(fp.R, tm) * ceil_div(H, BN), kb, workers);
+  fp.b.dh_wide = dh_wide_for(1, tm, ceil_div(fp.R, tm) * ceil_div(H, BN), workers);
+  int sp = dh_split_count(ceil_div(fp.R, tm) * ceil_div(H, fp.b.dh_wide ? 2 * BN : BN), kb, workers);
   fp.b.dh_kb_per_split = static_cast<int>(ceil_div(kb, sp));
   fp.b.dh_splits = static_cast<int>(ceil_div(kb, fp.b.dh_kb_per_split));
   fp.b.dh_f32 = fp.b.dh_splits > 1;

@@ -576,6 +576,8 @@ typedef struct flce_backward_plan_info {
   int64_t dlogits_buffers;  /* 1, or 2 when the row blocks run pipelined: slab s + 1's dlogits
                                formed while slab s's dH and dW run (both gradients wanted,
                                several slabs; dlogits_bytes covers both buffers) */
+  int64_t dh_wide;          /* 1 when the dH GEMM runs 256 x 512 tiles on SM pairs (one slab, at
+                               least two waves of 256 x 256 tiles), else 0 */
 } flce_backward_plan_info;
 
 /* Backward tiling that flce_backward uses for N, H, V, chunk_rows on a GPU
@@ -646,6 +648,8 @@ typedef enum flce_option {
   FLCE_OPT_DLOGITS_EPILOGUE_WARPS,  /* FLCE_DLOGITS_EPILOGUE_WARPS: epilogue warps of the
                                        cross-entropy dlogits GEMM and of the pipelined row
                                        block: 4 (default) or 8 (one operand stage fewer) */
+  FLCE_OPT_DH_WIDE,         /* FLCE_DH_WIDE: 1 = the dH GEMM of a one-slab backward runs 256 x
+                               512 tiles on SM pairs (default), 0 = 256 x 256 */
   FLCE_OPT_COUNT
 } flce_option;
 

@@ -58,17 +58,20 @@ def test_gpu_arm_json_line():
 
 def test_algorithmic_bytes_follow_the_launch_decomposition():
     """The bytes bench.py's roofline charges each GEMM kind, on the 16K SFT
-    step (one 4,096-row block x one slab per launch, 2 dH splits): W read
-    once per launch, D written / read once, h rows once per slab, dW written
-    once per row block and read back on the later ones."""
+    step (one 4,096-row block x one slab per launch, the planner's dH
+    k-splits): W read once per launch, D written / read once, h rows once per
+    slab, dW written once per row block and read back on the later ones."""
     sys.path.insert(0, ROOT)
     import bench
+    from chunked_lm_head_gb300 import _lib
     N, nv, H, V = 16384, 16380, 4096, 151936
     b = bench.algorithmic_bytes_step(N, nv, H, V, 4096, nv)
+    splits = _lib.flce_backward_plan(N, H, V, 4096)["dh_splits"]
+    assert splits > 1
     W, D, h = V * H * 2, nv * V * 2, nv * H * 2
     assert b["fwd_logits_lse"] == 4 * W + h
     assert b["bwd_dlogits"] == 4 * W + h + D
-    assert b["bwd_dH"] == D + 4 * W + nv * H * 4 * 2  # two k-splits of fp32 partials, one slab
+    assert b["bwd_dH"] == D + 4 * W + nv * H * 4 * splits  # k-splits of fp32 partials, one slab
     assert b["bwd_dW"] == D + h + 4 * V * H * 4 + 3 * V * H * 4
     # dW per launch: D + h + the fp32 write, plus the read on 3 of 4 blocks
     assert b["bwd_dW"] / 4 == pytest.approx(5.634e9, rel=1e-3)

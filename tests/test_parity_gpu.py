@@ -468,6 +468,40 @@ def test_pipelined_row_blocks(case, cg, compact, flce_opts):
         assert_grad_close(np64(got[1]), ref.dW, f"dW ({name})")
 
 
+@pytest.mark.parametrize("H", [4104, 4608])
+@pytest.mark.parametrize("compact", ["0", "1"])
+def test_wide_dh_tiles(H, compact, flce_opts):
+    """dH over 256 x 512 tiles on SM pairs (the default for one slab with at
+    least two waves of 256 x 256 tiles: 10 row tiles x 17 or 18 column tiles
+    here): two 256-column tiles share each A stage, the last pair's second
+    tile wholly past H when H = 4,104; against 256 x 256 tiles and the
+    oracle, through the two-call backward and the one-call path."""
+    import chunked_lm_head_gb300 as flce
+    flce_opts.set("cta_group", 2)
+    flce_opts.set("compact", compact)
+    N, V, chunk = 2560, 3001, 2560
+    wl = WL.custom(f"dh2_{H}{compact}", N, H, V, chunk, w_std=0.05, targets="zipf", ignore_frac=0.07,
+                   seed=119 + H)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(16).uniform(0.2, 1.8, N).astype(np.float32)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, chunk)
+    out = {}
+    for wide in (1, 0):
+        flce_opts.set("dh_wide", wide)
+        plan = _lib.flce_backward_plan(N, H, V, chunk)
+        assert plan["vocab_slabs"] == 1 and plan["dh_wide"] == wide, plan
+        out[wide] = (run_backward(h, W, t, w, lse, 1.0 / nv, chunk),
+                     tuple(flce.forward_backward(h, W, t, w, chunk)[k] for k in ("dH", "dW")))
+    _lib.check("flce_device_status", _lib.flce_device_status())
+    ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / nv)
+    for wide in (1, 0):
+        for path in (0, 1):
+            assert_grad_close(np64(out[wide][path][0]), ref.dH, f"dH (wide {wide}, path {path})")
+        # dW does not depend on the dH tiling
+        assert torch.equal(out[wide][0][1], out[0][0][1])
+
+
 @pytest.mark.parametrize("cg", ["1", "2"])
 def test_schedule_options_leave_the_gradients_bitwise_unchanged(cg, flce_opts):
     """Options that only change the schedule: the dW epilogue with 16 warps
