@@ -206,3 +206,22 @@ def test_device_side_scale_equals_the_host_scale():
 def rel_fro_t(a, b):
     a, b = a.double(), b.double()
     return float((a - b).norm() / b.norm().clamp_min(1e-300))
+
+
+def test_data_parallel_step_on_one_rank_matches_oracle():
+    """The data-parallel step with libflce as the per-rank compute and no
+    process group (one rank): the count reaches the backward as a device
+    scalar; loss, dH and dW against the oracle."""
+    from chunked_lm_head_gb300 import dp
+    wl = WL.custom("dp1", 700, 256, 5003, 256, w_std=0.05, targets="zipf", ignore_frac=0.1, seed=171)
+    inp = WL.make_inputs(wl)
+    inp.weights = np.random.default_rng(17).uniform(0.3, 1.7, wl.N).astype(np.float32)
+    h, W, t, w = upload(inp)
+    out = dp.data_parallel_step(h, W, t, w, grad=0.5, local=dp.LibflceStep(chunk_rows=256))
+    ref = O.forward(inp.h, inp.W, inp.targets, inp.weights)
+    refb = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=0.5 / ref.n_valid)
+    assert int(out["n_valid"]) == ref.n_valid
+    assert float(out["loss"]) == pytest.approx(ref.loss, rel=LOSS_RTOL)
+    assert_logp_close(np64(out["logp"]), ref.logp, "logp")
+    assert_grad_close(np64(out["dH"]), refb.dH, "dH")
+    assert_grad_close(np64(out["dW"]), refb.dW, "dW")
