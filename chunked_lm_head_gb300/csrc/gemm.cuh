@@ -119,15 +119,8 @@ struct KernelCfg {
   static constexpr int STAGE = TileCfg<CG>::A_BYTES + (kWideN ? 2 : 1) * TileCfg<CG>::B_BYTES;
   static constexpr int TILE_N = (kWideN ? 2 : 1) * BN;  // accumulator columns of a unit's tile
   static constexpr bool kDeepOut = MODE == MODE_DW && EW == 16;
-  // dlogits with 8 epilogue warps (alone or in PIPE): two bf16 staging boxes
-  // per warp, paid for with one operand stage
-  static constexpr bool kWideD = (MODE == MODE_DLOGITS || MODE == MODE_PIPE) && EW == 8;
-  static constexpr int NSTAGE = kWideN     ? 4
-                               : kDeepOut ? (CG == 1 ? 3 : 4)
-                                          : (kWideD ? TileCfg<CG>::NSTAGE - 1 : TileCfg<CG>::NSTAGE);
-  static constexpr int OUT_BYTES = kDeepOut ? EW * OUT_BOX_BYTES
-                                   : kWideD ? EW * 2 * OUT_BOX_BYTES
-                                            : OUT_STAGE_BYTES;
+  static constexpr int NSTAGE = kWideN ? 4 : kDeepOut ? (CG == 1 ? 3 : 4) : TileCfg<CG>::NSTAGE;
+  static constexpr int OUT_BYTES = kDeepOut ? EW * OUT_BOX_BYTES : OUT_STAGE_BYTES;
   static constexpr int BOXES_PER_WARP = OUT_BYTES / OUT_BOX_BYTES / EW > 0 ? OUT_BYTES / OUT_BOX_BYTES / EW : 1;
   static constexpr int SMEM = 1024 + NSTAGE * STAGE + OUT_BYTES + SMEM_BAR_BYTES;
   static_assert(SMEM <= 232448, "exceeds the 227 KiB shared memory of one CTA");
@@ -146,7 +139,7 @@ __host__ __device__ constexpr bool is_kd() {
 template <int MODE>
 __host__ __device__ constexpr bool wide_epilogue_mode() {
   return MODE == MODE_DW || MODE == MODE_DHDW || MODE == MODE_KD_DLOGITS || MODE == MODE_JSD_DLOGITS ||
-         MODE == MODE_JSD_FWD || MODE == MODE_DLOGITS || MODE == MODE_PIPE;
+         MODE == MODE_JSD_FWD;
 }
 // modes whose accumulator rows are rows of h (all but dW, whose accumulator
 // rows are vocabulary rows): under row compaction they map through row_idx
@@ -980,7 +973,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
     // columns of the tile this warp takes: all, or one half (8 epilogue warps)
     static_assert(EW == EPI_WARPS || (EW == 2 * EPI_WARPS && wide_epilogue_mode<MODE>()) ||
                       (EW == 4 * EPI_WARPS && MODE == MODE_DW),
-                  "8 epilogue warps: dW, DHDW, the dlogits modes, PIPE and the Jensen-Shannon terms; "
+                  "8 epilogue warps: dW, DHDW, the two-head dlogits and the Jensen-Shannon terms; "
                   "16: dW only");
     constexpr int kColParts = EW / 4;
     constexpr int kChunks = K::TILE_N / 32 / kColParts;

@@ -151,9 +151,7 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
     const bool wide = MODE == MODE_DW         ? p.k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_DHDW    ? p.dw_k_blocks <= kDwWideEpilogueMaxKBlocks
                       : MODE == MODE_JSD_FWD ? p.col_parts == 2
-                      : (MODE == MODE_DLOGITS || MODE == MODE_PIPE)
-                          ? opt(FLCE_OPT_DLOGITS_EPILOGUE_WARPS) == 8
-                          : wide_epilogue_on();
+                                             : wide_epilogue_on();
     if constexpr (MODE == MODE_DW) {
       // short K: 16 epilogue warps (default; FLCE_OPT_DW_EPILOGUE_WARPS = 8
       // keeps 8)

@@ -39,7 +39,6 @@ constexpr OptionDef kOptionDefs[FLCE_OPT_COUNT] = {
     {"FLCE_FUSE_DH_DW", 1, 0, 1},             // FLCE_OPT_FUSE_DH_DW
     {"FLCE_DW_EPILOGUE_WARPS", 16, 8, 16},    // FLCE_OPT_DW_EPILOGUE_WARPS
     {"FLCE_PIPELINE", 1, 0, 1},               // FLCE_OPT_PIPELINE
-    {"FLCE_DLOGITS_EPILOGUE_WARPS", 4, 4, 8},  // FLCE_OPT_DLOGITS_EPILOGUE_WARPS
     {"FLCE_DH_WIDE", 1, 0, 1},                // FLCE_OPT_DH_WIDE
 };
 

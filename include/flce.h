@@ -645,9 +645,6 @@ typedef enum flce_option {
   FLCE_OPT_PIPELINE,        /* FLCE_PIPELINE: 1 = a backward of several vocabulary slabs runs
                                each row block in one launch, its units ordered by device-side
                                counters (default), 0 = two launches per slab */
-  FLCE_OPT_DLOGITS_EPILOGUE_WARPS,  /* FLCE_DLOGITS_EPILOGUE_WARPS: epilogue warps of the
-                                       cross-entropy dlogits GEMM and of the pipelined row
-                                       block: 4 (default) or 8 (one operand stage fewer) */
   FLCE_OPT_DH_WIDE,         /* FLCE_DH_WIDE: 1 = the dH GEMM of a one-slab backward runs 256 x
                                512 tiles on SM pairs (default), 0 = 256 x 256 */
   FLCE_OPT_COUNT

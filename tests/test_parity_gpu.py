@@ -433,10 +433,10 @@ PIPE_CASES = {
 def test_pipelined_row_blocks(case, cg, compact, flce_opts):
     """A row block's dlogits, dH and dW units of every slab in one launch over
     two dlogits buffers, ordered by device-side counters (the default with
-    several slabs): against the oracle, bitwise repeatable (every output
+    several slabs): against the oracle and bitwise repeatable (every output
     element is summed by the same unit in the same order, the dH partials
-    slab after slab), bitwise the same with 8 dlogits epilogue warps; and the
-    launch-per-slab path (one buffer of twice the slab) against the oracle."""
+    slab after slab); and the launch-per-slab path (one buffer of twice the
+    slab) against the oracle."""
     N, H, V, chunk, rows, tfd = PIPE_CASES[case]
     flce_opts.set("cta_group", cg)
     flce_opts.set("compact", compact)
@@ -450,10 +450,8 @@ def test_pipelined_row_blocks(case, cg, compact, flce_opts):
     h, W, t, w = upload(inp)
     logp, lse, loss, nv = run_forward(h, W, t, w, chunk, transform=tfd)
     out = []
-    for ew in (4, 4, 8):
-        flce_opts.set("dlogits_epilogue_warps", ew)
+    for _ in range(3):
         out.append(run_backward(h, W, t, w, lse, 1.0 / nv, chunk, transform=tfd))
-    flce_opts.set("dlogits_epilogue_warps", 4)
     flce_opts.set("pipeline", 0)
     assert _lib.flce_backward_plan(N, H, V, chunk)["dlogits_buffers"] == 1
     slabs = run_backward(h, W, t, w, lse, 1.0 / nv, chunk, transform=tfd)
@@ -504,10 +502,9 @@ def test_wide_dh_tiles(H, compact, flce_opts):
 
 @pytest.mark.parametrize("cg", ["1", "2"])
 def test_schedule_options_leave_the_gradients_bitwise_unchanged(cg, flce_opts):
-    """Options that only change the schedule: the dW epilogue with 16 warps
-    at short K (the default) against 8, and the dlogits epilogue with 8
-    warps against 4 (one slab).  Every output element is summed by the same
-    unit in the same order either way."""
+    """An option that only changes the schedule: the dW epilogue with 16
+    warps at short K (the default) against 8.  Every output element is summed
+    by the same unit in the same order either way."""
     flce_opts.set("cta_group", cg)
     import chunked_lm_head_gb300 as flce
     # short K: 500 rows (8 K blocks) -> 8 or 16 dW epilogue warps
@@ -523,9 +520,6 @@ def test_schedule_options_leave_the_gradients_bitwise_unchanged(cg, flce_opts):
         outs.append(run_backward(h, W, t, w, lse, 1.0 / nv, 512))
         outs.append(tuple(flce.forward_backward(h, W, t, w, 512)[k] for k in ("dH", "dW")))
     assert torch.equal(outs[0][1], outs[2][1]) and torch.equal(outs[1][1], outs[3][1])
-    flce_opts.set("dlogits_epilogue_warps", 8)
-    d8 = run_backward(h, W, t, w, lse, 1.0 / nv, 512)
-    assert torch.equal(d8[0], outs[2][0]) and torch.equal(d8[1], outs[2][1])
     ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / nv)
     assert_grad_close(np64(outs[2][1]), ref.dW, "dW (16 epilogue warps)")
     assert_grad_close(np64(outs[3][0]), ref.dH, "dH (one call, 16 epilogue warps)")
