@@ -13,11 +13,17 @@ from gpu_util import upload
 pytestmark = pytest.mark.gpu
 
 
-def test_forward_backward_graph_replay_matches_eager():
+@pytest.mark.parametrize("rows", [0, 512], ids=["one_slab", "pipelined"])
+def test_forward_backward_graph_replay_matches_eager(rows, flce_opts):
+    """rows = 512: 512-row blocks x vocabulary slabs, run as pipelined row
+    blocks (the dependency counters are zeroed in the captured work)."""
     wl = WL.custom("graph", 700, 256, 3000, 256, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=801)
     inp = WL.make_inputs(wl)
     h, W, t, w = upload(inp)
     N, H, V, cr = wl.N, wl.H, wl.V, 256
+    flce_opts.set("bwd_rows", rows)
+    plan = _lib.flce_backward_plan(N, H, V, cr)
+    assert plan["dlogits_buffers"] == (2 if rows else 1), plan
     ws_bytes = _lib.flce_workspace_bytes(N, H, V, cr)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     bufs = dict(logp=torch.empty(N, device="cuda"), lse=torch.empty(N, device="cuda"),
@@ -45,6 +51,10 @@ def test_forward_backward_graph_replay_matches_eager():
     for v in bufs.values():
         v.zero_()
     graph.replay()
+    torch.cuda.synchronize()
+    for k in bufs:
+        assert torch.equal(bufs[k], eager[k]), k
+    graph.replay()  # a second replay: the same again
     torch.cuda.synchronize()
     for k in bufs:
         assert torch.equal(bufs[k], eager[k]), k
