@@ -36,7 +36,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workload at 4,096-row chunks: ncu's one-pass dram__bytes_read/write
 # counters at full size, mean over one step's launches, current kernels.
 NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {
-    "bwd_dH": 4.85e9, "bwd_dW": 7.68e9}
+    "bwd_dH": 4.85e9, "bwd_dW": 6.27e9}
 NCU_TRAFFIC_WORKLOAD = "sft_16k"
 
 

@@ -97,6 +97,27 @@ def test_all_rows_ignored():
     assert torch.all(dH == 0) and torch.all(dW == 0)
 
 
+@pytest.mark.parametrize("compact", ["0", "1"])
+def test_pipelined_row_blocks_all_rows_ignored(compact, flce_opts):
+    """Pipelined row blocks (2 x 4 blocks, several slabs) where every row is
+    ignored: without compaction the dlogits units write zero rows, with it
+    the blocks have no rows and only the first writes dW's zeros; dH and dW
+    are zero either way."""
+    flce_opts.set("compact", compact)
+    flce_opts.set("bwd_rows", 256)
+    N, H, V, cr = 1000, 128, 4000, 128
+    assert _lib.flce_backward_plan(N, H, V, cr)["dlogits_buffers"] == 2
+    wl = WL.custom(f"pipeign{compact}", N, H, V, cr, w_std=0.05, seed=120)
+    inp = WL.make_inputs(wl)
+    inp.targets[:] = WL.IGNORE_INDEX
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, cr)
+    assert nv == 0 and loss == 0.0
+    dH, dW = run_backward(h, W, t, w, lse, 1.0, cr)
+    _lib.check("flce_device_status", _lib.flce_device_status())
+    assert torch.all(dH == 0) and torch.all(dW == 0)
+
+
 def test_results_do_not_depend_on_chunk_rows_and_are_deterministic():
     wl = WL.custom("chunks", 700, 256, 3000, 128, w_std=0.05, targets="zipf", seed=107)
     inp = WL.make_inputs(wl)
