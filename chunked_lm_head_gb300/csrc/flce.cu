@@ -127,14 +127,9 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
     int* ccount = reinterpret_cast<int*>(wb + L.count);
     uint16_t* hc = reinterpret_cast<uint16_t*>(wb + L.hc);
     if (skip_ignored) {
-      const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
-      int* cblk = reinterpret_cast<int*>(wb + L.blk);
-      ProfScope ps(K_COMPACT, st);
-      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk);
-      FLCE_CUDA_TRY(cudaGetLastError());
-      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk, nblk, cidx, ccount,
-                                                           0);
-      FLCE_CUDA_TRY(cudaGetLastError());
+      const flce_status sl =
+          list_valid_rows(targets, Ni, ignore_index, reinterpret_cast<int*>(wb + L.blk), cidx, ccount, false, st);
+      if (sl != FLCE_OK) return sl;
     }
     CUtensorMap tA, tB;
     if (!make_map(&tA, skip_ignored ? hc : h, H, skip_ignored ? fb : N, H, BK, BM) ||
@@ -188,12 +183,8 @@ static flce_status forward_impl(const flce_bf16* h, const flce_bf16* W, const in
         q.row_idx = cidx;
         q.dyn_count = ccount;
         q.chunk_first = static_cast<int>(row0);
-        const long long total = fb * (H / 8);
-        const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
-        ProfScope ps(K_GATHER, st);
-        gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, ccount, Ni,
-                                                            static_cast<int>(row0), static_cast<int>(fb), hc);
-        FLCE_CUDA_TRY(cudaGetLastError());
+        const flce_status sg = gather_rows(h, H, cidx, ccount, Ni, row0, fb, hc, st);
+        if (sg != FLCE_OK) return sg;
       }
       ProfScope ps(K_FWD, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_FWD>(cg, kLong, tA, tB, tB, q, std::min(q.num_units, workers), st));
@@ -339,19 +330,9 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
   uint16_t* hc = reinterpret_cast<uint16_t*>(wb + L.hc);
   CUtensorMap hc_k, hc_mn, Dfix_k, Dfix_mn;
   if (compact) {
-    const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
-    {
-      ProfScope ps(K_COMPACT, st);
-      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
-                                                           cblk);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
-    {
-      ProfScope ps(K_COMPACT, st);
-      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
-                                                           cblk, nblk, cidx, ccount, 0);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
+    const flce_status sl =
+        list_valid_rows(targets, static_cast<int>(N), ignore_index, cblk, cidx, ccount, false, st);
+    if (sl != FLCE_OK) return sl;
     if (dH) FLCE_CUDA_TRY(cudaMemsetAsync(dH, 0, static_cast<size_t>(N) * H * 2, st));
     if (!make_map(&hc_k, hc, H, b.R, H, BK, BM) || !make_map(&hc_mn, hc, H, b.R, H, 64, BK) ||
         !make_map(&Dfix_k, Dbuf, b.ldD, b.R, b.ldD, BK, BM) ||
@@ -389,13 +370,8 @@ static flce_status backward_impl(const flce_bf16* h, const flce_bf16* W, const i
       p.row_idx = cidx;
       p.dyn_count = ccount;
       p.chunk_first = static_cast<int>(row0);
-      const long long total = b.R * (H / 8);
-      const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
-      ProfScope ps(K_GATHER, st);
-      gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx, ccount,
-                                                          static_cast<int>(N), static_cast<int>(row0),
-                                                          static_cast<int>(b.R), hc);
-      FLCE_CUDA_TRY(cudaGetLastError());
+      const flce_status sg = gather_rows(h, H, cidx, ccount, static_cast<int>(N), row0, b.R, hc, st);
+      if (sg != FLCE_OK) return sg;
     }
     const CUtensorMap& A_dl = compact ? hc_k : h_k;
     const CUtensorMap& B_dw = compact ? hc_mn : h_mn;
@@ -646,13 +622,8 @@ static flce_status forward_backward_impl(const flce_bf16* h, const flce_bf16* W,
     if (nbad != 0) return FLCE_ERR_BAD_TARGET;
   }
   {  // n_valid on the device, before any dlogits
-    const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
-    ProfScope ps(K_COMPACT, st);
-    compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk);
-    FLCE_CUDA_TRY(cudaGetLastError());
-    compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, Ni, ignore_index, cblk, nblk, cidx, ccount,
-                                                         compact ? 1 : 0);
-    FLCE_CUDA_TRY(cudaGetLastError());
+    const flce_status sl = list_valid_rows(targets, Ni, ignore_index, cblk, cidx, ccount, compact, st);
+    if (sl != FLCE_OK) return sl;
   }
   if (compact && dH) {  // the dH GEMM writes the non-ignored rows only
     ProfScope ps(K_COMPACT, st);
@@ -715,13 +686,8 @@ static flce_status forward_backward_impl(const flce_bf16* h, const flce_bf16* W,
     if (compact) {  // the block's rows of h, in permutation order
       p.row_idx = cidx;
       p.chunk_first = static_cast<int>(row0);
-      const long long total = fp.R * (H / 8);
-      const int grid = static_cast<int>(std::min<long long>(ceil_div(total, SMALL_THREADS), 8LL * device_sms()));
-      ProfScope ps(K_GATHER, st);
-      gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), cidx,
-                                                          fwd_valid_only ? ccount : nullptr, Ni,
-                                                          static_cast<int>(row0), static_cast<int>(fp.R), hc);
-      FLCE_CUDA_TRY(cudaGetLastError());
+      const flce_status sg = gather_rows(h, H, cidx, fwd_valid_only ? ccount : nullptr, Ni, row0, fp.R, hc, st);
+      if (sg != FLCE_OK) return sg;
     }
     {  // (1) logits of the block: online lse partials, target logits, exponentials
       GemmParams q = p;
@@ -1026,14 +992,9 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
     uint16_t* hs_c = reinterpret_cast<uint16_t*>(wb + J.hs);
     uint16_t* ht_c = reinterpret_cast<uint16_t*>(wb + J.ht);
     if (skip_ignored) {
-      const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
-      int* cblk = reinterpret_cast<int*>(wb + J.blk);
-      ProfScope prof(K_COMPACT, st);
-      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index, cblk);
-      FLCE_CUDA_TRY(cudaGetLastError());
-      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index, cblk, nblk,
-                                                           cidx, ccount, 0);
-      FLCE_CUDA_TRY(cudaGetLastError());
+      const flce_status sl = list_valid_rows(targets, static_cast<int>(N), ignore_index,
+                                             reinterpret_cast<int*>(wb + J.blk), cidx, ccount, false, st);
+      if (sl != FLCE_OK) return sl;
     }
     CUtensorMap hs_k, Ws_k, ht_k, Wt_k;
     if (!make_map(&hs_k, skip_ignored ? hs_c : h_s, H_s, skip_ignored ? fb : N, H_s, BK, BM) ||
@@ -1042,17 +1003,9 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
         !make_map(&Wt_k, W_t, H_t, V, H_t, BK, BN / cg))
       return FLCE_ERR_CUDA;
     // the block's rows of both heads, gathered (skip_ignored)
-    auto gather_block = [&](long long row0) -> cudaError_t {
-      ProfScope prof(K_GATHER, st);
-      const int grid_s = static_cast<int>(std::min<long long>(ceil_div(fb * (H_s / 8), SMALL_THREADS), 8LL * device_sms()));
-      gather_rows_kernel<<<grid_s, SMALL_THREADS, 0, st>>>(h_s, static_cast<int>(H_s), cidx, ccount,
-                                                            static_cast<int>(N), static_cast<int>(row0),
-                                                            static_cast<int>(fb), hs_c);
-      const int grid_t = static_cast<int>(std::min<long long>(ceil_div(fb * (H_t / 8), SMALL_THREADS), 8LL * device_sms()));
-      gather_rows_kernel<<<grid_t, SMALL_THREADS, 0, st>>>(h_t, static_cast<int>(H_t), cidx, ccount,
-                                                            static_cast<int>(N), static_cast<int>(row0),
-                                                            static_cast<int>(fb), ht_c);
-      return cudaGetLastError();
+    auto gather_block = [&](long long row0) -> flce_status {
+      const flce_status sg = gather_rows(h_s, H_s, cidx, ccount, static_cast<int>(N), row0, fb, hs_c, st);
+      return sg != FLCE_OK ? sg : gather_rows(h_t, H_t, cidx, ccount, static_cast<int>(N), row0, fb, ht_c, st);
     };
     int* err = nullptr;
     FLCE_CUDA_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_device_error));
@@ -1110,7 +1063,10 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       return q;
     };
     for (long long row0 = 0; row0 < N; row0 += fb) {
-      if (skip_ignored) FLCE_CUDA_TRY(gather_block(row0));
+      if (skip_ignored) {
+        const flce_status sg = gather_block(row0);
+        if (sg != FLCE_OK) return sg;
+      }
       const GemmParams q = block_params(p, row0);
       ProfScope prof(K_KD_FWD, st);
       FLCE_CUDA_TRY(launch_gemm<MODE_KD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, q, std::min(q.num_units, workers), st,
@@ -1137,7 +1093,10 @@ static flce_status distill_forward(bool jsd, float beta, const flce_bf16* h_s, c
       q.jsd_beta = beta;
       q.col_parts = jsd_parts;
       for (long long row0 = 0; row0 < N; row0 += fb) {
-        if (skip_ignored) FLCE_CUDA_TRY(gather_block(row0));
+        if (skip_ignored) {
+          const flce_status sg = gather_block(row0);
+          if (sg != FLCE_OK) return sg;
+        }
         const GemmParams qb = block_params(q, row0);
         ProfScope prof(K_JSD_FWD, st);
         FLCE_CUDA_TRY(launch_gemm<MODE_JSD_FWD>(cg, kLong, hs_k, Ws_k, Ws_k, qb, std::min(qb.num_units, workers),
@@ -1317,19 +1276,9 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
   uint16_t* hct = reinterpret_cast<uint16_t*>(wb + DL.hc_t);
   CUtensorMap hcs_k, hcs_mn, hct_k, Dfix_k, Dfix_mn;
   if (compact) {
-    const int nblk = static_cast<int>(ceil_div(N, COMPACT_ROWS_PER_BLOCK));
-    {
-      ProfScope ps(K_COMPACT, st);
-      compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
-                                                           cblk);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
-    {
-      ProfScope ps(K_COMPACT, st);
-      compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, static_cast<int>(N), ignore_index,
-                                                           cblk, nblk, cidx, ccount, 0);
-      FLCE_CUDA_TRY(cudaGetLastError());
-    }
+    const flce_status sl =
+        list_valid_rows(targets, static_cast<int>(N), ignore_index, cblk, cidx, ccount, false, st);
+    if (sl != FLCE_OK) return sl;
     if (dH_s) FLCE_CUDA_TRY(cudaMemsetAsync(dH_s, 0, static_cast<size_t>(N) * H_s * 2, st));
     if (!make_map(&hcs_k, hcs, H_s, b.R, H_s, BK, BM) || !make_map(&hcs_mn, hcs, H_s, b.R, H_s, 64, BK) ||
         !make_map(&hct_k, hct, H_t, b.R, H_t, BK, BM) ||
@@ -1354,17 +1303,10 @@ static flce_status distill_backward(bool jsd, float beta, const float* kl_sm, co
       p.row_idx = cidx;
       p.dyn_count = ccount;
       p.chunk_first = static_cast<int>(row0);
-      const long long cap = b.R;
-      ProfScope ps(K_GATHER, st);
       for (int head = 0; head < 2; ++head) {
-        const long long Hh = head == 0 ? H_s : H_t;
-        const int grid = static_cast<int>(
-            std::min<long long>(ceil_div(cap * (Hh / 8), SMALL_THREADS), 8LL * device_sms()));
-        gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(head == 0 ? h_s : h_t, static_cast<int>(Hh), cidx,
-                                                            ccount, static_cast<int>(N),
-                                                            static_cast<int>(row0), static_cast<int>(cap),
-                                                            head == 0 ? hcs : hct);
-        FLCE_CUDA_TRY(cudaGetLastError());
+        const flce_status sg = gather_rows(head == 0 ? h_s : h_t, head == 0 ? H_s : H_t, cidx, ccount,
+                                           static_cast<int>(N), row0, b.R, head == 0 ? hcs : hct, st);
+        if (sg != FLCE_OK) return sg;
       }
     }
     const CUtensorMap& As_k = compact ? hcs_k : hs_k;

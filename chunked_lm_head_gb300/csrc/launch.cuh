@@ -314,6 +314,40 @@ bool transform_params(const flce_logit_transform* tf, GemmParams& p) {
     }                                    \
   } while (0)
 
+// ---- row listing and gathering (row compaction)
+
+// The non-ignored rows of targets[N], listed on the device: their indices in
+// order into idx (followed by the ignored rows' when tail), their count into
+// *count.  blk: scratch of ceil(N / COMPACT_ROWS_PER_BLOCK) ints.
+flce_status list_valid_rows(const int64_t* targets, int N, long long ignore_index, int* blk, int* idx,
+                            int* count, bool tail, cudaStream_t st) {
+  const int nblk = static_cast<int>(ceil_div(std::max(N, 1), COMPACT_ROWS_PER_BLOCK));
+  {
+    ProfScope ps(K_COMPACT, st);
+    compact_count_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, N, ignore_index, blk);
+    FLCE_CUDA_TRY(cudaGetLastError());
+  }
+  ProfScope ps(K_COMPACT, st);
+  compact_write_kernel<<<nblk, SMALL_THREADS, 0, st>>>(targets, N, ignore_index, blk, nblk, idx, count,
+                                                       tail ? 1 : 0);
+  FLCE_CUDA_TRY(cudaGetLastError());
+  return FLCE_OK;
+}
+
+// Listed rows [first, first + cap) (idx; at most *count - first of them, or
+// all when count is null) gathered from h[N][H] into hc[cap][H], with zero
+// rows after the last up to the next 64.
+flce_status gather_rows(const flce_bf16* h, long long H, const int* idx, const int* count, int N,
+                        long long first, long long cap, uint16_t* hc, cudaStream_t st) {
+  const int grid = static_cast<int>(
+      std::max<long long>(1, std::min<long long>(ceil_div(cap * (H / 8), SMALL_THREADS), 8LL * device_sms())));
+  ProfScope ps(K_GATHER, st);
+  gather_rows_kernel<<<grid, SMALL_THREADS, 0, st>>>(h, static_cast<int>(H), idx, count, N,
+                                                      static_cast<int>(first), static_cast<int>(cap), hc);
+  FLCE_CUDA_TRY(cudaGetLastError());
+  return FLCE_OK;
+}
+
 // Final deterministic reduction of the block partials into loss and count.
 flce_status loss_tail(const FwdPlan& f, float* out_loss, int64_t* out_n_valid, const double* bsum,
                       const long long* bcnt, cudaStream_t st) {
