@@ -126,25 +126,15 @@ cudaError_t launch_gemm_t(const Maps& m, const GemmParams& p, int workers, cudaS
 // 4,096 rows 4 warps were 1-2 % faster
 constexpr int kDwWideEpilogueMaxKBlocks = 16;
 
-// `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
-// tile loop.  `c` is the output map of the modes that write through TMA (dW,
-// dH partials, dlogits); the other modes ignore it.
+// The epilogue width (4, 8 or 16 warps) and CTA group of one launch of MODE.
 template <int MODE>
-cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st,
-                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr,
-                        const CUtensorMap* c2 = nullptr, const CUtensorMap* a3 = nullptr,
-                        const CUtensorMap* b3 = nullptr, const CUtensorMap* c3 = nullptr) {
-  // a2 / b2: the teacher's operands of the distillation modes, or the DW
-  // units' operands of DHDW and PIPE, whose dW output map is c2; a3 / b3 /
-  // c3: the DLOGITS units' operands and D output of PIPE (else unused)
-  const Maps mp{&a, &b, &c, a2 ? a2 : &a, b2 ? b2 : &b, c2 ? c2 : &c, a3 ? a3 : &a, b3 ? b3 : &b,
-                c3 ? c3 : &c};
+cudaError_t launch_gemm_maps(int cg, bool kLong, const Maps& mp, const GemmParams& p, int workers,
+                             cudaStream_t st) {
   if constexpr (MODE == MODE_DH2) {  // SM pairs only
     (void)cg;
     return kLong ? launch_gemm_t<MODE, true, 2>(mp, p, workers, st)
                  : launch_gemm_t<MODE, false, 2>(mp, p, workers, st);
-  } else {
+  }
   if constexpr (wide_epilogue_mode<MODE>()) {
     // the Jensen-Shannon forward's caller sized the partials for the column
     // parts it chose
@@ -173,12 +163,30 @@ cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensor
                    : launch_gemm_t<MODE, false, 1, EW>(mp, p, workers, st);
     }
   }
-  if (cg == 2)
-    return kLong ? launch_gemm_t<MODE, true, 2>(mp, p, workers, st)
-                 : launch_gemm_t<MODE, false, 2>(mp, p, workers, st);
-  return kLong ? launch_gemm_t<MODE, true, 1>(mp, p, workers, st)
-               : launch_gemm_t<MODE, false, 1>(mp, p, workers, st);
+  if constexpr (MODE != MODE_DH2) {
+    if (cg == 2)
+      return kLong ? launch_gemm_t<MODE, true, 2>(mp, p, workers, st)
+                   : launch_gemm_t<MODE, false, 2>(mp, p, workers, st);
+    return kLong ? launch_gemm_t<MODE, true, 1>(mp, p, workers, st)
+                 : launch_gemm_t<MODE, false, 1>(mp, p, workers, st);
   }
+}
+
+// `workers`: CTAs (cg 1) or CTA pairs (cg 2), each running one persistent
+// tile loop.  `c` is the output map of the modes that write through TMA (dW,
+// dH partials, dlogits); the other modes ignore it.
+template <int MODE>
+cudaError_t launch_gemm(int cg, bool kLong, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const GemmParams& p, int workers, cudaStream_t st,
+                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr,
+                        const CUtensorMap* c2 = nullptr, const CUtensorMap* a3 = nullptr,
+                        const CUtensorMap* b3 = nullptr, const CUtensorMap* c3 = nullptr) {
+  // a2 / b2: the teacher's operands of the distillation modes, or the DW
+  // units' operands of DHDW and PIPE, whose dW output map is c2; a3 / b3 /
+  // c3: the DLOGITS units' operands and D output of PIPE (else unused)
+  const Maps mp{&a, &b, &c, a2 ? a2 : &a, b2 ? b2 : &b, c2 ? c2 : &c, a3 ? a3 : &a, b3 ? b3 : &b,
+                c3 ? c3 : &c};
+  return launch_gemm_maps<MODE>(cg, kLong, mp, p, workers, st);
 }
 
 // The e4m3 forward: MODE_FWD with 8-bit operands.
