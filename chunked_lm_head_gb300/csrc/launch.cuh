@@ -385,8 +385,12 @@ int dh_group_rows(int m_tiles) {
 // wave covers few D slices, each read once.  16,384 x 4,096 x 151,936: a dW
 // launch read 2.25 / 4.34 GB (store / reduce-add) from DRAM against 3.67 /
 // 5.75 GB with groups of 8 vocabulary tiles and 4.2 / 6.3 GB with 16, in the
-// same time.
-constexpr int kDwGroup = 1;
+// same time.  At short K the launch is bound by its fp32 write stream, which
+// groups of 8 vocabulary tiles write faster: 256 x 2,048 x 248,320 took 381
+// against 407 us with groups of 1.
+int dw_group(int k_blocks, int m_tiles) {
+  return k_blocks <= kDwWideEpilogueMaxKBlocks ? std::min(8, std::max(1, m_tiles)) : 1;
+}
 
 // dH and dW stages of the backward, shared by the cross-entropy and the
 // distillation backwards.  For one row block and one vocabulary slab, the
@@ -434,7 +438,7 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     q.dw_m_tiles = static_cast<int>(ceil_div(width, a.tm));
     q.dw_n_tiles = static_cast<int>(ceil_div(a.H, BN));
     q.dw_k_blocks = static_cast<int>(ceil_div(rows, BK));
-    q.dw_group_m = kDwGroup;
+    q.dw_group_m = dw_group(q.dw_k_blocks, q.dw_m_tiles);
     q.dW_accumulate = block > 0 ? 1 : 0;
     q.num_units = splits * q.m_tiles * q.n_tiles + q.dw_m_tiles * q.dw_n_tiles;
     ProfScope ps(K_DHDW, st);
@@ -477,7 +481,7 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
     q.kb_per_split = q.k_blocks;
     q.k_splits = 1;
     q.num_units = q.m_tiles * q.n_tiles;
-    q.group_m = kDwGroup;
+    q.group_m = dw_group(q.k_blocks, q.m_tiles);
     q.dW_accumulate = block > 0 ? 1 : 0;
     ProfScope ps(K_DW, st);
     FLCE_CUDA_TRY(launch_gemm<MODE_DW>(a.cg, a.kLong, D_mn, B_dw, *a.dW_map, q,
@@ -508,8 +512,8 @@ flce_status pipe_block(const DhDwStage& a, const GemmParams& p, int rows, int bl
   q.pp_dh_kbps = b.dh_kb_per_split;
   q.pp_dl_group = std::min(16, q.m_tiles);
   q.group_m = dh_group_rows(q.m_tiles);
-  q.dw_group_m = kDwGroup;
   q.dw_k_blocks = static_cast<int>(ceil_div(rows, BK));
+  q.dw_group_m = dw_group(q.dw_k_blocks, static_cast<int>(ceil_div(b.Vs, a.tm)));
   q.dH_part = a.dh_part;
   q.dW_accumulate = block > 0 ? 1 : 0;
   q.pp_dep = dep;
