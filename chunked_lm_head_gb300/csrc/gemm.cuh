@@ -574,6 +574,7 @@ __device__ __forceinline__ bool wait_units_ready(volatile int* ready, int k, vol
       atomicOr(err, DEVERR_TIMEOUT);
       return false;
     }
+    __nanosleep(32);  // leave the issue slots to the epilogue warps
   }
   __threadfence_block();
   return true;
