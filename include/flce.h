@@ -580,10 +580,12 @@ typedef struct flce_backward_plan_info {
                                least two waves of 256 x 256 tiles), else 0 */
 } flce_backward_plan_info;
 
-/* Backward tiling that flce_backward uses for N, H, V, chunk_rows on a GPU
- * that holds `workers` persistent tile workers (CTAs for cta_group 1, CTA
- * pairs for cta_group 2; 148 SMs give 148 or 74).  workers <= 0 or
- * cta_group == 0: query the current device and the FLCE_CTA_GROUP setting.
+/* Backward tiling that flce_backward uses for N, H, V, chunk_rows when it
+ * computes both dH and dW (under the current run-time options) on a GPU that
+ * holds `workers` persistent tile workers (CTAs for cta_group 1, CTA pairs
+ * for cta_group 2; 152 SMs give 152 or 76).  workers <= 0 or cta_group == 0:
+ * query the current device and the FLCE_CTA_GROUP setting.  workspace_bytes
+ * covers the tiling of a call that computes only one of the gradients too.
  * FLCE_ERR_INVALID_ARG on invalid sizes or a NULL out. */
 FLCE_API flce_status flce_backward_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
                                         int32_t workers, int32_t cta_group,
