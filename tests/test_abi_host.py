@@ -92,6 +92,26 @@ def test_backward_plan_prefers_row_blocks_over_literal_small_chunks():
     assert (q["row_blocks"], q["vocab_slabs"]) == (1, 1)
 
 
+def test_backward_plan_kinds_on_the_workloads(flce_opts):
+    """Which backward the workloads run (76 SM pairs): the 16K SFT step one
+    slab per 4,096-row block with 256 x 512 dH tiles; the long-context step
+    at 256-row chunks pipelined row blocks over two dlogits buffers inside
+    the chunk's budget; the single chunk 256 x 256 dH tiles (too few tiles
+    for two waves)."""
+    p = _lib.flce_backward_plan(16384, 4096, 151936, 4096, 76, 2)
+    assert (p["vocab_slabs"], p["dlogits_buffers"], p["dh_wide"]) == (1, 1, 1)
+    q = _lib.flce_backward_plan(131072, 2560, 151936, 256, 76, 2)
+    assert q["vocab_slabs"] > 1 and q["dlogits_buffers"] == 2 and q["dh_wide"] == 0
+    assert q["dlogits_bytes"] <= 256 * 151936 * 2
+    r = _lib.flce_backward_plan(256, 2048, 248320, 256, 76, 2)
+    assert (r["vocab_slabs"], r["dlogits_buffers"], r["dh_wide"]) == (1, 1, 0)
+    # the options turn them off
+    flce_opts.set("dh_wide", "0")
+    flce_opts.set("pipeline", "0")
+    assert _lib.flce_backward_plan(16384, 4096, 151936, 4096, 76, 2)["dh_wide"] == 0
+    assert _lib.flce_backward_plan(131072, 2560, 151936, 256, 76, 2)["dlogits_buffers"] == 1
+
+
 def test_backward_plan_row_override(flce_opts):
     flce_opts.set("bwd_rows", "768")
     flce_opts.set("pipeline", "0")  # one dlogits buffer
