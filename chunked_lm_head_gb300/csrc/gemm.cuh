@@ -54,7 +54,10 @@ constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 // handed to TMA store / reduce-add.
 constexpr int OUT_BOX_BYTES = 32 * 32 * 4;
 constexpr int OUT_STAGE_BYTES = EPI_WARPS * 2 * OUT_BOX_BYTES;
-constexpr int SMEM_BAR_BYTES = 256;
+constexpr int SMEM_BAR_BYTES = 512;
+// PIPE: unit indices in flight between the fetching thread and the CTA's
+// roles (a ring of this many slots, each with a full and an empty mbarrier)
+constexpr int kUnitRing = 6;
 
 // Tile geometry of one CTA (CG = 1) or of an SM pair running 2-CTA MMAs
 // (CG = 2: a 256 x 256 tile, A rows and B columns split across the pair).
@@ -252,7 +255,8 @@ struct GemmParams {
   // buffers of rows_cap rows, slab s in buffer s % 2.  Dependency counters:
   // pp_dep (this launch's, zero at its start) and pp_dep_zero (the next
   // launch's, zeroed here), pp_dep_words each.
-  int pp_slabs, pp_vs, pp_kh, pp_dh_kbps, pp_dl_group, pp_dep_words;
+  // pp_lookahead: units a pair may hold drawn but not finished (1..kUnitRing)
+  int pp_slabs, pp_vs, pp_kh, pp_dh_kbps, pp_dl_group, pp_dep_words, pp_lookahead;
   unsigned* pp_dep;
   unsigned* pp_dep_zero;
 };
@@ -487,9 +491,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 //     read: it waits for dh_row[s - 2][m] and dw_col[s - 2][vt].
 // Units run in phases (phase p: slab p's DLOGITS units, then slab p - 1's DH
 // and DW units), so every wait is on units of an earlier phase, i.e. earlier
-// in the unit order; with all CTAs of the grid resident at once (the grid is
-// the device's co-resident cluster count), the lowest unfinished unit can
-// always run.  Slab s + 1's dlogits are formed while slab s's dH and dW run.
+// in the unit order.  Workers draw units from a counter in that order, so
+// every unit a wait names has been drawn by a running worker and the lowest
+// unfinished unit can always run, however many CTAs of the grid are
+// resident.  Slab s + 1's dlogits are formed while slab s's dH and dW run.
 struct PipeDeps {
   int mt_cap, vt_cap, slabs;
   __device__ __forceinline__ int dl_row(int s, int m) const { return s * mt_cap + m; }
@@ -557,26 +562,20 @@ __device__ __forceinline__ bool pipe_wait_deps(const GemmParams& p, const DynSha
   return ok;
 }
 
-// Producer side of the dependency warp (PIPE): bounded wait until this
-// worker's unit k is marked ready, giving up when another role of the CTA
-// has aborted or the limit runs out.
-__device__ __forceinline__ bool wait_units_ready(volatile int* ready, int k, volatile int* abort_flag,
+// Bounded wait on an mbarrier phase completed by a release-arrive of a peer
+// CTA (cluster-scope acquire); as wait_bar otherwise.
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                  int* err) {
-  if (*ready > k) {
-    __threadfence_block();
-    return true;
-  }
+  if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = clock64();
-  while (*ready <= k) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
       *abort_flag = 1;
       atomicOr(err, DEVERR_TIMEOUT);
       return false;
     }
-    __nanosleep(32);  // leave the issue slots to the epilogue warps
   }
-  __threadfence_block();
   return true;
 }
 
@@ -770,10 +769,15 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * NST + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * NST + 2 + b); };
   const uint32_t drain = bar0 + 8u * (2 * NST + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5);
+  // PIPE: unit ring (full: published by the pair's fetching thread in both
+  // CTAs; empty: in the first CTA, one arrival per epilogue warp of the pair)
+  auto ufull_bar = [&](int s) { return bar0 + 8u * (2 * NST + 5 + s); };
+  auto uempty_bar = [&](int s) { return bar0 + 8u * (2 * NST + 5 + kUnitRing + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5 + 2 * kUnitRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // PIPE: how many of this worker's units have their dependencies met
-  volatile int* units_ready = abort_flag + 1;
+  volatile int* unit_ring = abort_flag + 1;  // kUnitRing unit indices (-1: no more units)
+  static_assert((2 * NST + 5 + 2 * kUnitRing) * 8 + 8 + 4 * kUnitRing <= SMEM_BAR_BYTES,
+                "barriers exceed their shared-memory area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -794,8 +798,13 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
       mbar_init(tempty_bar(b), EW * CG);
     }
     mbar_init(drain, 1);
+    if constexpr (MODE == MODE_PIPE) {
+      for (int r = 0; r < kUnitRing; ++r) {
+        mbar_init(ufull_bar(r), 1);
+        mbar_init(uempty_bar(r), EW * CG);
+      }
+    }
     *abort_flag = 0;
-    *units_ready = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -835,6 +844,20 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
       for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.pp_dep_words; i += gridDim.x * blockDim.x)
         p.pp_dep_zero[i] = 0u;
   }
+  // The k-th unit of this worker, or -1 when it has none left: round-robin
+  // over the grid, or (PIPE) taken from the unit ring, whose indices the
+  // pair's fetching thread draws from a counter in increasing order.
+  auto unit_at = [&](int k) -> int {
+    if constexpr (MODE == MODE_PIPE) {
+      const int sl = k % kUnitRing;
+      if (!wait_bar_cluster(ufull_bar(sl), static_cast<uint32_t>((k / kUnitRing) & 1), abort_flag, p.err))
+        return -1;
+      return unit_ring[sl];
+    } else {
+      const int u = worker + k * nworkers;
+      return u < dsh.num_units ? u : -1;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -842,16 +865,14 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      int k_unit = 0;
-      for (int u = worker; u < dsh.num_units && ok; u += nworkers, ++k_unit) {
+      for (int k_unit = 0; ok; ++k_unit) {
+        const int u = unit_at(k_unit);
+        if (u < 0) break;
         const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
         if constexpr (MODE == MODE_PIPE) {
-          // the dependency warp has seen this unit's inputs published
-          if (!wait_units_ready(units_ready, k_unit, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();  // the bulk loads below read what was published
+          // the fetching thread saw this unit's inputs published; the bulk
+          // loads below read them
+          fence_proxy_async_global();
         }
         const int uv0 = MODE == MODE_PIPE ? t.slab * p.pp_vs : p.v0;  // the unit's first vocabulary column
         const int udoff = MODE == MODE_PIPE ? (t.slab & 1) * p.rows_cap : 0;  // its D buffer
@@ -899,7 +920,9 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
     if (lane == 0 && issuer) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
+      for (int k_unit = 0; ok; ++k_unit) {
+        const int u = unit_at(k_unit);
+        if (u < 0) break;
         const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
         for (int n = t.n0; n < t.n1 && ok; ++n) {
           if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
@@ -952,17 +975,36 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
     }
     __syncwarp();
   } else if (MODE == MODE_PIPE && warp == 2 + EW) {
-    // ------------------------------------------------------- dependencies
-    // (PIPE) waits, unit by unit of this worker, until the units whose
-    // output it reads or overwrites are counted, and tells the producer
+    // ------------------------------------------------------------ fetching
+    // (PIPE; the pair's first CTA) draws unit indices in increasing order
+    // from the launch's counter, waits until the units whose output each one
+    // reads or overwrites are counted, and publishes it in both CTAs' unit
+    // rings; -1 ends the loops.  Every unit waits only on lower indices,
+    // which running workers have drawn, so the launch completes whichever of
+    // its CTAs are resident.
     if constexpr (MODE == MODE_PIPE) {
-      if (lane == 0) {
-        int k_unit = 0;
-        for (int u = worker; u < dsh.num_units; u += nworkers, ++k_unit) {
-          const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
-          if (!pipe_wait_deps<C::TM, EW * CG>(p, dsh, t, abort_flag)) break;
-          __threadfence_block();
-          *units_ready = k_unit + 1;
+      if (lane == 0 && issuer) {
+        unsigned* counter = p.pp_dep + p.pp_dep_words - 1;
+        const int ahead = min(max(p.pp_lookahead, 1), kUnitRing);
+        for (int k = 0;; ++k) {
+          const int sl = k % kUnitRing;
+          // unit k - ahead finished (so its slot, and unit k - kUnitRing's, is free)
+          const int j = k - ahead;
+          if (j >= 0 && !wait_bar_cluster(uempty_bar(j % kUnitRing), static_cast<uint32_t>((j / kUnitRing) & 1),
+                                          abort_flag, p.err))
+            break;
+          int u = static_cast<int>(atomicAdd(counter, 1u));
+          if (u >= dsh.num_units) u = -1;
+          if (u >= 0 && !pipe_wait_deps<C::TM, EW * CG>(p, dsh, decode_unit<MODE, C::TM>(p, dsh, u), abort_flag))
+            u = -1;
+          for (int r = 0; r < CG; ++r) {
+            const uint32_t ring_r = CG == 2 ? mapa_shared(smem_u32(const_cast<int*>(unit_ring + sl)), r)
+                                            : smem_u32(const_cast<int*>(unit_ring + sl));
+            const uint32_t full_r = CG == 2 ? mapa_shared(ufull_bar(sl), r) : ufull_bar(sl);
+            st_shared_cluster_u32(ring_r, static_cast<uint32_t>(u));
+            mbar_arrive_cluster(full_r);
+          }
+          if (u < 0) break;
         }
       }
       __syncwarp();
@@ -987,7 +1029,11 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
     const uint32_t tempty_target1 = CG == 2 ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int u = worker; u < dsh.num_units && ok; u += nworkers) {
+    for (int k_unit = 0; ok; ++k_unit) {
+      int u = 0;
+      if (lane == 0) u = unit_at(k_unit);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u < 0) break;
       const Unit t = decode_unit<MODE, C::TM>(p, dsh, u);
       // PIPE: the unit's kind (else the mode's) and its slab's first column
       const bool unit_dl = MODE == MODE_DLOGITS || (MODE == MODE_PIPE && t.kind == KIND_DL);
@@ -1449,6 +1495,12 @@ __global__ void __launch_bounds__(kernel_threads<MODE>(EW), 1)
           bulk_wait_all();
           fence_proxy_async_global();
           pipe_signal<C::TM>(p, t);
+          // the unit's ring slot may take the next unit (the first CTA counts)
+          const uint32_t ue = uempty_bar(k_unit % kUnitRing);
+          if constexpr (CG == 1)
+            mbar_arrive(ue);
+          else
+            mbar_arrive_cluster(mapa_shared(ue, 0));
         }
         __syncwarp();
       }

@@ -126,6 +126,13 @@ cudaError_t launch_gemm_t(const Maps& m, const GemmParams& p, int workers, cudaS
 // 4,096 rows 4 warps were 1-2 % faster
 constexpr int kDwWideEpilogueMaxKBlocks = 16;
 
+// Pipelined row blocks: how many units an SM pair may hold drawn but not
+// finished.  Two keep the next unit's loads behind the current unit's MMAs;
+// on the 131,072 x 2,560 x 151,936 step (256-row chunks) three took as long
+// and six 6 % longer (the drawn units run further ahead of the finished
+// ones); on 8,192 rows of the same shape one took 30 % longer.
+constexpr int kPipeLookahead = 2;
+
 // The epilogue width (4, 8 or 16 warps) and CTA group of one launch of MODE.
 template <int MODE>
 cudaError_t launch_gemm_maps(int cg, bool kLong, const Maps& mp, const GemmParams& p, int workers,
@@ -494,8 +501,8 @@ flce_status slab_dh_dw(const DhDwStage& a, const GemmParams& p, int rows, int bl
 // vocabulary slab its dlogits units (A_dl x W_k into D through D_st), then its
 // dH and dW units as slab_dh_dw runs them.  dep: this launch's dependency
 // counters (zero at its start); dep_zero: the next launch's, which this one
-// zeroes.  The grid is every co-resident SM pair, which the units' waits on
-// one another need.
+// zeroes.  The grid is every co-resident SM pair; the pairs draw units in
+// order, so the launch also completes on fewer.
 flce_status pipe_block(const DhDwStage& a, const GemmParams& p, int rows, int block, const CUtensorMap& A_dl,
                        const CUtensorMap& W_k, const CUtensorMap& D_st, const CUtensorMap& D_k,
                        const CUtensorMap& D_mn, const CUtensorMap& B_dw, unsigned* dep, unsigned* dep_zero,
@@ -519,6 +526,7 @@ flce_status pipe_block(const DhDwStage& a, const GemmParams& p, int rows, int bl
   q.pp_dep = dep;
   q.pp_dep_zero = dep_zero;
   q.pp_dep_words = static_cast<int>(pipe_dep_words(b));
+  q.pp_lookahead = kPipeLookahead;
   ProfScope ps(K_PIPE, st);
   FLCE_CUDA_TRY(launch_gemm<MODE_PIPE>(a.cg, a.kLong, D_k, *a.W_mn, *a.dhp_map, q, a.workers, st, &D_mn, &B_dw,
                                        a.dW_map, &A_dl, &W_k, &D_st));

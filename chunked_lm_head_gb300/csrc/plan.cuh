@@ -394,9 +394,9 @@ JsdFwdLayout jsd_fwd_layout(long long N, const FwdPlan& f, long long H_s = 0, lo
 
 // Dependency counters of one pipelined row-block launch (MODE_PIPE): per
 // slab, two per row tile (at most R / 128 of them) and two per BN-wide
-// vocabulary tile of the slab.
+// vocabulary tile of the slab; the last word counts the units drawn.
 long long pipe_dep_words(const BwdPlan& b) {
-  return 2LL * b.n_slabs * (ceil_div(b.R, BM) + ceil_div(b.Vs, BN));
+  return 2LL * b.n_slabs * (ceil_div(b.R, BM) + ceil_div(b.Vs, BN)) + 1;
 }
 
 struct BwdLayout {

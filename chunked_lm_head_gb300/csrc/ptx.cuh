@@ -129,11 +129,6 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// Barrier `id` (1..15) over `threads` threads of this CTA (a subset of warps).
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA) before a bulk copy reads them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -164,6 +159,25 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
+}
+
+// try_wait with cluster-scope acquire: what a peer CTA wrote before its
+// release-arrive on this barrier is visible after the phase completes
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 32-bit store to shared memory of a CTA of the cluster (mapa address)
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // Address, in the cluster shared window, of the same shared variable in CTA `rank`.
