@@ -34,9 +34,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "source": "fallback"}
 # DRAM bytes (read + write) per launch of each GEMM kind on the 16K SFT
 # workload at 4,096-row chunks: ncu's one-pass dram__bytes_read/write
-# counters at full size, mean over one step's launches, current kernels.
+# counters at full size, mean over one step's launches (dW: one store launch,
+# three fp32 reduce-add launches), current kernels.
 NCU_TRAFFIC_BYTES_PER_LAUNCH: dict[str, float | None] = {
-    "bwd_dH": 4.85e9, "bwd_dW": 6.27e9}
+    "bwd_dH": 5.17e9, "bwd_dW": 6.73e9}
 NCU_TRAFFIC_WORKLOAD = "sft_16k"
 
 
