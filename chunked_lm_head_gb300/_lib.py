@@ -473,7 +473,7 @@ OPTIONS = {
     "cta_group": 0, "compact": 1, "validate": 2, "pdl": 3, "d_tma": 4, "wide_epilogue": 5,
     "bwd_rows": 6, "fwd_splits": 7, "dh_splits": 8, "dh_group": 9, "fwd_block_rows": 10,
     "skip_min_rows": 11, "fuse_dh_dw": 12,
-    "dw_epilogue_warps": 13, "pipeline": 14, "dh_wide": 15,
+    "dw_epilogue_warps": 13, "pipeline": 14, "dh_wide": 15, "grid_workers": 16,
 }
 
 

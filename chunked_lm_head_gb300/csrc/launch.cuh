@@ -110,14 +110,22 @@ struct Maps {
   const CUtensorMap *a, *b, *c, *a2, *b2, *c2, *a3, *b3, *c3;
 };
 
+// Workers a GEMM launch starts: `workers`, or FLCE_OPT_GRID_WORKERS when set.
+// Units are dealt round-robin or drawn from a counter, never tied to a
+// particular worker, so any count computes the same result.
+int grid_workers(int workers) {
+  const int64_t g = opt(FLCE_OPT_GRID_WORKERS);
+  return g > 0 ? static_cast<int>(g) : workers;
+}
+
 template <int MODE, bool kLong, int CG, int EW = EPI_WARPS>
 cudaError_t launch_gemm_t(const Maps& m, const GemmParams& p, int workers, cudaStream_t st) {
   auto k = flce_gemm_kernel<MODE, kLong, CG, false, EW>;
   constexpr int smem = KernelCfg<MODE, CG, EW>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_persistent(k, CG * workers, CG, kernel_threads<MODE>(EW), smem, st, *m.a, *m.b, *m.c, *m.a2, *m.b2,
-                           *m.c2, *m.a3, *m.b3, *m.c3, p);
+  return launch_persistent(k, CG * grid_workers(workers), CG, kernel_threads<MODE>(EW), smem, st, *m.a, *m.b, *m.c,
+                           *m.a2, *m.b2, *m.c2, *m.a3, *m.b3, *m.c3, p);
 }
 
 // dW over at most this many K blocks (64 rows each) runs 8 epilogue warps:
@@ -202,8 +210,8 @@ cudaError_t launch_fwd_e4m3(int cg, bool kLong, const CUtensorMap& a, const CUte
   auto go = [&](auto kern, int smem, int grid_mult) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_persistent(kern, grid_mult * workers, grid_mult, gemm_threads(EPI_WARPS), smem, st, a, b, b,
-                             a, b, b, a, b, b, p);
+    return launch_persistent(kern, grid_mult * grid_workers(workers), grid_mult, gemm_threads(EPI_WARPS), smem, st,
+                             a, b, b, a, b, b, a, b, b, p);
   };
   if (cg == 2)
     return kLong ? go(flce_gemm_kernel<MODE_FWD, true, 2, true>, TileCfg<2>::SMEM, 2)

@@ -40,6 +40,7 @@ constexpr OptionDef kOptionDefs[FLCE_OPT_COUNT] = {
     {"FLCE_DW_EPILOGUE_WARPS", 16, 8, 16},    // FLCE_OPT_DW_EPILOGUE_WARPS
     {"FLCE_PIPELINE", 1, 0, 1},               // FLCE_OPT_PIPELINE
     {"FLCE_DH_WIDE", 1, 0, 1},                // FLCE_OPT_DH_WIDE
+    {"FLCE_GRID_WORKERS", 0, 0, 4096},        // FLCE_OPT_GRID_WORKERS
 };
 
 std::atomic<int64_t> g_options[FLCE_OPT_COUNT];

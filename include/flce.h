@@ -649,6 +649,11 @@ typedef enum flce_option {
                                counters (default), 0 = two launches per slab */
   FLCE_OPT_DH_WIDE,         /* FLCE_DH_WIDE: 1 = the dH GEMM of a one-slab backward runs 256 x
                                512 tiles on SM pairs (default), 0 = 256 x 256 */
+  FLCE_OPT_GRID_WORKERS,    /* FLCE_GRID_WORKERS: persistent workers (CTAs, or CTA pairs) that
+                               each GEMM launch starts, 1..4,096; 0 = as many as the device
+                               holds at once (default).  Plans stay those of the device's
+                               count: fewer workers leave SMs to other work, more queue
+                               behind the resident ones and find the units taken */
   FLCE_OPT_COUNT
 } flce_option;
 

@@ -208,7 +208,7 @@ def test_options_round_trip_and_range_checks(lib, flce_opts):
     assert _lib.flce_get_option("dh_group") == 0
     # out-of-range values and unknown options change nothing
     for name, bad in (("cta_group", 3), ("compact", 2), ("validate", -1), ("fwd_splits", 257),
-                      ("dh_splits", 17), ("fwd_block_rows", -2)):
+                      ("dh_splits", 17), ("fwd_block_rows", -2), ("grid_workers", 4097), ("grid_workers", -1)):
         before = _lib.flce_get_option(name)
         assert lib.flce_set_option(_lib.OPTIONS[name], bad) == 1
         assert _lib.flce_get_option(name) == before

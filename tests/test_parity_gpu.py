@@ -487,6 +487,57 @@ def test_pipelined_row_blocks(case, cg, compact, flce_opts):
         assert_grad_close(np64(got[1]), ref.dW, f"dW ({name})")
 
 
+@pytest.mark.parametrize("grid", ["few", "queued"])
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_pipelined_row_blocks_any_grid(grid, cg, flce_opts):
+    """The pipelined launch on 3 workers, and on three times as many as the
+    device holds at once (the extra ones start only as resident ones
+    retire).  Workers draw units from a counter in an order in which every
+    wait points back, so the launch completes either way; the plan is the
+    device's and no summation order depends on the worker that runs a unit,
+    so the gradients are bitwise those of the default grid."""
+    N, H, V, chunk, rows, _ = PIPE_CASES["blocks4_slabs4"]
+    flce_opts.set("cta_group", cg)
+    flce_opts.set("bwd_rows", rows)
+    plan = _lib.flce_backward_plan(N, H, V, chunk)
+    assert plan["dlogits_buffers"] == 2 and plan["vocab_slabs"] > 1 and plan["row_blocks"] > 1, plan
+    wl = WL.custom(f"pipegrid{cg}", N, H, V, chunk, w_std=0.04, targets="zipf", ignore_frac=0.08, seed=121)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    logp, lse, loss, nv = run_forward(h, W, t, w, chunk)
+    dflt = run_backward(h, W, t, w, lse, 1.0 / nv, chunk)
+    resident = torch.cuda.get_device_properties(0).multi_processor_count // int(cg)
+    flce_opts.set("grid_workers", 3 if grid == "few" else 3 * resident)
+    got = run_backward(h, W, t, w, lse, 1.0 / nv, chunk)
+    _lib.check("flce_device_status", _lib.flce_device_status())
+    assert torch.equal(got[0], dflt[0]) and torch.equal(got[1], dflt[1])
+    ref = O.backward(inp.h, inp.W, inp.targets, inp.weights, g=1.0 / nv)
+    assert_grad_close(np64(got[0]), ref.dH, "dH")
+    assert_grad_close(np64(got[1]), ref.dW, "dW")
+
+
+@pytest.mark.parametrize("grid", [5, 600])
+def test_one_slab_step_on_any_grid(grid, flce_opts):
+    """Forward and one-slab backward with the GEMMs on 5 workers, and on 600
+    (more than the device holds at once): bitwise the default grid's
+    results."""
+    wl = WL.custom("anygrid", 1500, 512, 5000, 256, w_std=0.05, targets="zipf", ignore_frac=0.05, seed=122)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+
+    def step():
+        logp, lse, loss, nv = run_forward(h, W, t, w, 256)
+        dH, dW = run_backward(h, W, t, w, lse, 1.0 / nv, 256)
+        return logp, lse, torch.tensor([loss]), dH, dW
+
+    dflt = step()
+    flce_opts.set("grid_workers", grid)
+    got = step()
+    _lib.check("flce_device_status", _lib.flce_device_status())
+    for name, a, b in zip(("logp", "lse", "loss", "dH", "dW"), got, dflt):
+        assert torch.equal(a, b), name
+
+
 @pytest.mark.parametrize("H", [4104, 4608])
 @pytest.mark.parametrize("compact", ["0", "1"])
 def test_wide_dh_tiles(H, compact, flce_opts):
