@@ -141,3 +141,52 @@ def test_static_scratch_forward_rejects_problems_beyond_its_scratch():
     st = _lib.flce_forward_static_scratch(p, p, p, None, 1 << 21, 64, 151936, 256, -100, p, None,
                                           None, None, 0)
     assert st == 3  # FLCE_ERR_UNSUPPORTED
+
+
+def test_static_scratch_forward_graph_replay():
+    """After one eager call on the device, the allocation-free forward is
+    captured into a CUDA graph; each replay reproduces the eager call bit for
+    bit, and follows new inputs copied into the captured buffers."""
+    wl = WL.custom("noalloc_g", 1200, 256, 9000, 256, w_std=0.04, targets="zipf", ignore_frac=0.05,
+                   seed=204)
+    inp = WL.make_inputs(wl)
+    h, W, t, w = upload(inp)
+    N, H, V = wl.N, wl.H, wl.V
+    out = dict(logp=torch.empty(N, device="cuda"), lse=torch.empty(N, device="cuda"),
+               loss=torch.empty(1, device="cuda"), nv=torch.empty(1, dtype=torch.int64, device="cuda"))
+
+    def call(stream):
+        return _lib.flce_forward_static_scratch(h, W, t, w, N, H, V, wl.chunk_rows, -100, out["logp"],
+                                                out["lse"], out["loss"], out["nv"], stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        assert call(side.cuda_stream) == 0  # eager: the scratch address is looked up here
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in out.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        assert call(torch.cuda.current_stream().cuda_stream) == 0
+    for _ in range(2):
+        for v in out.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in out:
+            assert torch.equal(out[k], eager[k]), k
+    # the regular forward on the same inputs: the same results
+    ref = run_forward(h, W, t, w, wl.chunk_rows)
+    assert int(out["nv"].item()) == ref[3]
+    assert_logp_close(np64(out["logp"]), np64(ref[0]), "logp")
+    # new inputs in the captured buffers: the replay follows them
+    h.copy_(torch.flip(h, dims=[0]))
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = out["lse"].clone()
+    with torch.cuda.stream(side):
+        assert call(side.cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out["lse"], replayed)
+    assert _lib.flce_device_status() == 0
