@@ -287,7 +287,7 @@ struct PipeSlab {
 };
 
 template <int TM>
-__device__ __forceinline__ PipeSlab pipe_slab(const GemmParams& p, const DynShape& d, int s) {
+__host__ __device__ __forceinline__ PipeSlab pipe_slab(const GemmParams& p, const DynShape& d, int s) {
   PipeSlab q;
   q.v0 = s * p.pp_vs;
   q.width = min(p.pp_vs, p.V - q.v0);
@@ -304,7 +304,7 @@ __device__ __forceinline__ PipeSlab pipe_slab(const GemmParams& p, const DynShap
 }
 
 template <int MODE, int TM>
-__device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
+__host__ __device__ __forceinline__ DynShape dyn_shape(const GemmParams& p) {
   DynShape d{p.rows, p.m_tiles, p.k_blocks, p.kb_per_split, p.num_units, 0, 0, 0};
   if constexpr (MODE == MODE_PIPE) {
     if (p.dyn_count != nullptr) {
@@ -362,7 +362,7 @@ struct Unit {
 
 // Unit u of a grid of (k-splits x m_tiles x cols) units, rasterised in
 // groups of group_m row tiles that share their column units.
-__device__ __forceinline__ Unit decode_grid(int u, int m_tiles, int cols, int n_tiles, int n_per_unit,
+__host__ __device__ __forceinline__ Unit decode_grid(int u, int m_tiles, int cols, int n_tiles, int n_per_unit,
                                             int group_m_req, int kb_per_split, int k_blocks,
                                             bool col_split) {
   const int group_m = min(group_m_req, max(m_tiles, 1));
@@ -396,7 +396,7 @@ __device__ __forceinline__ Unit decode_grid(int u, int m_tiles, int cols, int n_
 }
 
 template <int MODE, int TM = BM>
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape& d, int u) {
+__host__ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const DynShape& d, int u) {
   if constexpr (MODE == MODE_PIPE) {
     // phase by phase: phase p holds slab p's DLOGITS units (p < slabs), then
     // slab p - 1's DH units and DW units (p > 0).  Phase 0 has the first
@@ -497,16 +497,63 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // resident.  Slab s + 1's dlogits are formed while slab s's dH and dW run.
 struct PipeDeps {
   int mt_cap, vt_cap, slabs;
-  __device__ __forceinline__ int dl_row(int s, int m) const { return s * mt_cap + m; }
-  __device__ __forceinline__ int dh_row(int s, int m) const { return (slabs + s) * mt_cap + m; }
-  __device__ __forceinline__ int dl_col(int s, int vt) const { return 2 * slabs * mt_cap + s * vt_cap + vt; }
-  __device__ __forceinline__ int dw_col(int s, int vt) const {
+  __host__ __device__ int dl_row(int s, int m) const { return s * mt_cap + m; }
+  __host__ __device__ int dh_row(int s, int m) const { return (slabs + s) * mt_cap + m; }
+  __host__ __device__ int dl_col(int s, int vt) const { return 2 * slabs * mt_cap + s * vt_cap + vt; }
+  __host__ __device__ int dw_col(int s, int vt) const {
     return 2 * slabs * mt_cap + (slabs + s) * vt_cap + vt;
   }
 };
 
-__device__ __forceinline__ PipeDeps pipe_deps(const GemmParams& p) {
+__host__ __device__ __forceinline__ PipeDeps pipe_deps(const GemmParams& p) {
   return PipeDeps{p.m_tiles, (p.pp_vs + BN - 1) / BN, p.pp_slabs};
+}
+
+// A dependency counter of a pipelined launch and the count it must reach.
+struct PipeWait {
+  int idx;
+  unsigned target;
+};
+
+// The counters unit t waits on before its operands are loaded (at most 2,
+// into w; returns how many), with ARR arrivals per finished unit.
+template <int TM, int ARR>
+__host__ __device__ __forceinline__ int pipe_unit_waits(const GemmParams& p, const DynShape& d, const Unit& t,
+                                                        PipeWait* w) {
+  const PipeDeps g = pipe_deps(p);
+  int n = 0;
+  if (t.kind == KIND_DH) {
+    const PipeSlab q = pipe_slab<TM>(p, d, t.slab);
+    w[n++] = PipeWait{g.dl_row(t.slab, t.m), static_cast<unsigned>(q.vt * ARR)};
+    if (t.slab > 0) {
+      const PipeSlab qp = pipe_slab<TM>(p, d, t.slab - 1);
+      w[n++] = PipeWait{g.dh_row(t.slab - 1, t.m), static_cast<unsigned>(qp.splits * p.n_tiles * ARR)};
+    }
+  } else if (t.kind == KIND_DW) {
+    w[n++] = PipeWait{g.dl_col(t.slab, t.m * TM / BN), static_cast<unsigned>(d.m_tiles * ARR)};
+  } else if (t.slab > 1) {
+    // DLOGITS over a tile of the buffer that slab s - 2 read
+    const PipeSlab q = pipe_slab<TM>(p, d, t.slab - 2);
+    const int vt = t.n0;
+    const int dw_in = min(BN / TM, q.dwt - vt * (BN / TM));  // DW vocabulary tiles inside it
+    w[n++] = PipeWait{g.dh_row(t.slab - 2, t.m), static_cast<unsigned>(q.splits * p.n_tiles * ARR)};
+    w[n++] = PipeWait{g.dw_col(t.slab - 2, vt), static_cast<unsigned>(q.n_dw > 0 ? dw_in * p.n_tiles * ARR : 0)};
+  }
+  return n;
+}
+
+// The counters that each epilogue warp of unit t adds one arrival to once
+// its share of the unit is in global memory (at most 2, into idx).
+template <int TM>
+__host__ __device__ __forceinline__ int pipe_unit_signals(const GemmParams& p, const Unit& t, int* idx) {
+  const PipeDeps g = pipe_deps(p);
+  if (t.kind == KIND_DL) {
+    idx[0] = g.dl_row(t.slab, t.m);
+    idx[1] = g.dl_col(t.slab, t.n0);
+    return 2;
+  }
+  idx[0] = t.kind == KIND_DH ? g.dh_row(t.slab, t.m) : g.dw_col(t.slab, t.m * TM / BN);
+  return 1;
 }
 
 // Bounded wait until counter c reaches target.  Gives up (raising the CTA's
@@ -533,33 +580,16 @@ __device__ __forceinline__ bool pipe_wait(const unsigned* c, unsigned target, vo
 }
 
 // The waits of unit t before its operands are loaded (ARR arrivals per
-// unit: one per epilogue warp of each CTA).  Run by the dependency warp; the
+// unit: one per epilogue warp of each CTA).  Run by the fetching thread; the
 // producer then orders its bulk loads after them (fence.proxy.async).
 template <int TM, int ARR>
 __device__ __forceinline__ bool pipe_wait_deps(const GemmParams& p, const DynShape& d, const Unit& t,
                                                volatile int* abort_flag) {
-  const PipeDeps g = pipe_deps(p);
-  const unsigned* c = p.pp_dep;
-  bool ok = true;
-  if (t.kind == KIND_DH) {
-    const PipeSlab q = pipe_slab<TM>(p, d, t.slab);
-    ok = pipe_wait(c + g.dl_row(t.slab, t.m), q.vt * ARR, abort_flag, p.err);
-    if (ok && t.slab > 0) {
-      const PipeSlab qp = pipe_slab<TM>(p, d, t.slab - 1);
-      ok = pipe_wait(c + g.dh_row(t.slab - 1, t.m), qp.splits * p.n_tiles * ARR, abort_flag, p.err);
-    }
-  } else if (t.kind == KIND_DW) {
-    ok = pipe_wait(c + g.dl_col(t.slab, t.m * TM / BN), d.m_tiles * ARR, abort_flag, p.err);
-  } else if (t.slab > 1) {
-    // DLOGITS over a tile of the buffer that slab s - 2 read
-    const PipeSlab q = pipe_slab<TM>(p, d, t.slab - 2);
-    const int vt = t.n0;
-    const int dw_in = min(BN / TM, q.dwt - vt * (BN / TM));  // DW vocabulary tiles inside it
-    ok = pipe_wait(c + g.dh_row(t.slab - 2, t.m), q.splits * p.n_tiles * ARR, abort_flag, p.err) &&
-         pipe_wait(c + g.dw_col(t.slab - 2, vt), q.n_dw > 0 ? dw_in * p.n_tiles * ARR : 0, abort_flag,
-                   p.err);
-  }
-  return ok;
+  PipeWait w[2];
+  const int n = pipe_unit_waits<TM, ARR>(p, d, t, w);
+  for (int i = 0; i < n; ++i)
+    if (!pipe_wait(p.pp_dep + w[i].idx, w[i].target, abort_flag, p.err)) return false;
+  return true;
 }
 
 // Bounded wait on an mbarrier phase completed by a release-arrive of a peer
@@ -582,16 +612,9 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
 // This epilogue warp's share of unit t is complete in global memory: count it.
 template <int TM>
 __device__ __forceinline__ void pipe_signal(const GemmParams& p, const Unit& t) {
-  const PipeDeps g = pipe_deps(p);
-  unsigned* c = p.pp_dep;
-  if (t.kind == KIND_DL) {
-    red_release_gpu_add(c + g.dl_row(t.slab, t.m), 1u);
-    red_release_gpu_add(c + g.dl_col(t.slab, t.n0), 1u);
-  } else if (t.kind == KIND_DH) {
-    red_release_gpu_add(c + g.dh_row(t.slab, t.m), 1u);
-  } else {
-    red_release_gpu_add(c + g.dw_col(t.slab, t.m * TM / BN), 1u);
-  }
+  int idx[2];
+  const int n = pipe_unit_signals<TM>(p, t, idx);
+  for (int i = 0; i < n; ++i) red_release_gpu_add(p.pp_dep + idx[i], 1u);
 }
 
 // Bounded wait used only while shutting down (copies or MMAs in flight).

@@ -399,6 +399,65 @@ long long pipe_dep_words(const BwdPlan& b) {
   return 2LL * b.n_slabs * (ceil_div(b.R, BM) + ceil_div(b.Vs, BN)) + 1;
 }
 
+// dW over at most this many K blocks (64 rows each) runs 8 epilogue warps:
+// at 256 rows (4 blocks) its output epilogue, not the MMAs, set the pace
+// (8 warps: 410 us against 443 us for the 248,320 x 2,048 fp32 gradient); at
+// 4,096 rows 4 warps were 1-2 % faster
+constexpr int kDwWideEpilogueMaxKBlocks = 16;
+
+// Pipelined row blocks: how many units an SM pair may hold drawn but not
+// finished.  Two keep the next unit's loads behind the current unit's MMAs;
+// on the 131,072 x 2,560 x 151,936 step (256-row chunks) three took as long
+// and six 6 % longer (the drawn units run further ahead of the finished
+// ones); on 8,192 rows of the same shape one took 30 % longer.
+constexpr int kPipeLookahead = 2;
+
+// Row tiles per dH raster group: 8 (FLCE_OPT_DH_GROUP overrides).  A wave of 76
+// units then covers 8 row tiles x ~9.5 column tiles, the fewest D and W
+// slices per wave.  On 16,384 x 4,096 x 151,936, interleaved runs timed the
+// step 1.3% faster than with all 16 row tiles (the dH launch itself took the
+// same time); a dH launch's DRAM bytes vary more between GPUs than between
+// the two groups.
+int dh_group_rows(int m_tiles) {
+  const int64_t g = opt(FLCE_OPT_DH_GROUP);
+  return g > 0 ? static_cast<int>(std::min<int64_t>(g, m_tiles)) : m_tiles;
+}
+
+// dW raster: one vocabulary tile's column tiles after one another, so that a
+// wave covers few D slices, each read once.  16,384 x 4,096 x 151,936: a dW
+// launch read 2.25 / 4.34 GB (store / reduce-add) from DRAM against 3.67 /
+// 5.75 GB with groups of 8 vocabulary tiles and 4.2 / 6.3 GB with 16, in the
+// same time.  At short K the launch is bound by its fp32 write stream, which
+// groups of 8 vocabulary tiles write faster: 256 x 2,048 x 248,320 took 381
+// against 407 us with groups of 1.
+int dw_group(int k_blocks, int m_tiles) {
+  return k_blocks <= kDwWideEpilogueMaxKBlocks ? std::min(8, std::max(1, m_tiles)) : 1;
+}
+
+// Parameters of the pipelined launch (MODE_PIPE) of one row block: base
+// carries the call's fields (V, rows_cap, the row count or the compaction's
+// device-side count); rows is the block's row capacity (compacted) or its
+// rows, block its index (block 0 stores dW, later blocks add to it).
+GemmParams pipe_params(const BwdPlan& b, const GemmParams& base, long long H, int tm, int rows, int block) {
+  GemmParams q = base;
+  q.m_tiles = static_cast<int>(ceil_div(rows, tm));  // row tiles at most (compacted: fewer)
+  q.n_tiles = static_cast<int>(ceil_div(H, BN));
+  q.cols = q.n_tiles;
+  q.n_per_unit = 1;
+  q.pp_slabs = b.n_slabs;
+  q.pp_vs = static_cast<int>(b.Vs);
+  q.pp_kh = static_cast<int>(ceil_div(H, BK));
+  q.pp_dh_kbps = b.dh_kb_per_split;
+  q.pp_dl_group = std::min(16, q.m_tiles);
+  q.group_m = dh_group_rows(q.m_tiles);
+  q.dw_k_blocks = static_cast<int>(ceil_div(rows, BK));
+  q.dw_group_m = dw_group(q.dw_k_blocks, static_cast<int>(ceil_div(b.Vs, tm)));
+  q.dW_accumulate = block > 0 ? 1 : 0;
+  q.pp_dep_words = static_cast<int>(pipe_dep_words(b));
+  q.pp_lookahead = kPipeLookahead;
+  return q;
+}
+
 struct BwdLayout {
   size_t D = 0, dh_part = 0, bad = 0, idx = 0, blk = 0, count = 0, hc = 0, dep = 0, total = 0;
 };

@@ -4,6 +4,7 @@
 // reductions, e4m3 quantisation) and the device error word.
 #pragma once
 
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>

@@ -1,0 +1,225 @@
+// Host-side check of the pipelined backward's unit schedule (MODE_PIPE).
+//
+// A pipelined row block runs as one launch whose SM pairs draw unit indices
+// from a counter in increasing order; a unit waits until some dependency
+// counters reach their targets.  The launch finishes, whichever of its pairs
+// are resident, when every unit that adds to a counter a unit waits on comes
+// earlier in the order; and the unit reads complete data when each target
+// equals the number of units that add to that counter.  This program decodes
+// every unit of many launches with the library's own decoding and counter
+// helpers (compiled for the host) and checks, per launch:
+//   - every counter a unit waits on or adds to lies inside the launch's
+//     counter words (the last word, the draw counter, excluded);
+//   - every wait's target equals the number of units that add to its counter,
+//     and all of those units come before the waiting unit;
+//   - each slab's dlogits, dH and dW units are decoded exactly once, within
+//     their tile ranges, and the launch's unit count is their sum.
+// The launches are those the planner makes for the library's workloads (with
+// and without row compaction, both CTA-group tile heights) and a seeded sweep
+// of plans.  Exit status 0 and "ok" when every check passes.
+#include <cstdint>
+#include <cstdio>
+#include <set>
+#include <tuple>
+#include <vector>
+
+#include "plan.cuh"
+
+namespace {
+
+int g_fails = 0;
+long long g_launches = 0, g_units = 0;
+
+#define EXPECT(cond, ...)                      \
+  do {                                         \
+    if (!(cond)) {                             \
+      if (g_fails++ < 20) {                    \
+        std::fprintf(stderr, "FAIL: ");        \
+        std::fprintf(stderr, __VA_ARGS__);     \
+        std::fprintf(stderr, "\n");            \
+      }                                        \
+    }                                          \
+  } while (0)
+
+template <int TM>
+void check_launch(const GemmParams& q, const char* what) {
+  const DynShape d = dyn_shape<MODE_PIPE, TM>(q);
+  const int words = q.pp_dep_words - 1;  // the last word counts the units drawn
+  const int S = q.pp_slabs;
+  std::vector<Unit> units(d.num_units > 0 ? d.num_units : 0);
+  std::vector<long long> total(words, 0), seen(words, 0);
+  for (int u = 0; u < d.num_units; ++u) {
+    units[u] = decode_unit<MODE_PIPE, TM>(q, d, u);
+    int idx[2];
+    const int n = pipe_unit_signals<TM>(q, units[u], idx);
+    for (int i = 0; i < n; ++i) {
+      EXPECT(idx[i] >= 0 && idx[i] < words, "%s: unit %d adds to counter %d of %d", what, u, idx[i], words);
+      if (idx[i] >= 0 && idx[i] < words) ++total[idx[i]];
+    }
+  }
+  for (int u = 0; u < d.num_units; ++u) {
+    PipeWait w[2];
+    const int n = pipe_unit_waits<TM, 1>(q, d, units[u], w);
+    for (int i = 0; i < n; ++i) {
+      const int c = w[i].idx;
+      EXPECT(c >= 0 && c < words, "%s: unit %d waits on counter %d of %d", what, u, c, words);
+      if (c < 0 || c >= words) continue;
+      EXPECT(w[i].target == total[c], "%s: unit %d (kind %d, slab %d) waits for %u arrivals on counter %d, which %lld units add to",
+             what, u, units[u].kind, units[u].slab, w[i].target, c, total[c]);
+      EXPECT(seen[c] >= static_cast<long long>(w[i].target),
+             "%s: unit %d (kind %d, slab %d) waits on counter %d, of whose %u arrivals only %lld come from earlier units",
+             what, u, units[u].kind, units[u].slab, c, w[i].target, seen[c]);
+    }
+    int idx[2];
+    const int m = pipe_unit_signals<TM>(q, units[u], idx);
+    for (int i = 0; i < m; ++i)
+      if (idx[i] >= 0 && idx[i] < words) ++seen[idx[i]];
+  }
+  // every unit of every slab and kind exactly once
+  std::set<std::tuple<int, int, int, int, int>> keys;
+  std::vector<long long> count(3 * (S + 1), 0);
+  for (int u = 0; u < d.num_units; ++u) {
+    const Unit& t = units[u];
+    EXPECT(t.slab >= 0 && t.slab < S, "%s: unit %d in slab %d of %d", what, u, t.slab, S);
+    if (t.slab < 0 || t.slab >= S) continue;
+    const PipeSlab ps = pipe_slab<TM>(q, d, t.slab);
+    const int m_hi = t.kind == KIND_DW ? ps.dwt : d.m_tiles;
+    const int n_hi = t.kind == KIND_DL ? ps.vt : q.n_tiles;
+    const int k_hi = t.kind == KIND_DL ? q.pp_kh : t.kind == KIND_DH ? ps.kb : d.dw_k_blocks;
+    EXPECT(t.m >= 0 && t.m < m_hi && t.n0 >= 0 && t.n0 < n_hi && t.n1 == t.n0 + 1,
+           "%s: unit %d (kind %d) tile (%d, %d..%d) outside (%d, %d)", what, u, t.kind, t.m, t.n0, t.n1, m_hi, n_hi);
+    // an empty K range only for the dW units of a block without rows (their
+    // epilogue writes the zero product)
+    const bool k_ok = t.kb0 >= 0 && t.kb1 <= k_hi &&
+                      (t.kb0 < t.kb1 || (t.kind == KIND_DW && k_hi == 0 && t.kb0 == 0 && t.kb1 == 0));
+    EXPECT(k_ok, "%s: unit %d (kind %d) K blocks %d..%d of %d", what, u, t.kind, t.kb0, t.kb1, k_hi);
+    EXPECT(keys.insert(std::make_tuple(t.kind, t.slab, t.m, t.n0, t.kb0)).second, "%s: unit %d decoded twice",
+           what, u);
+    ++count[3 * t.slab + t.kind];
+  }
+  long long sum = 0;
+  for (int s = 0; s < S; ++s) {
+    const PipeSlab ps = pipe_slab<TM>(q, d, s);
+    EXPECT(count[3 * s + KIND_DL] == ps.n_dl && count[3 * s + KIND_DH] == ps.n_dh &&
+               count[3 * s + KIND_DW] == ps.n_dw,
+           "%s: slab %d has %lld / %lld / %lld units, expected %d / %d / %d", what, s, count[3 * s],
+           count[3 * s + 1], count[3 * s + 2], ps.n_dl, ps.n_dh, ps.n_dw);
+    sum += ps.n_dl + ps.n_dh + ps.n_dw;
+  }
+  EXPECT(sum == d.num_units, "%s: %d units, expected %lld", what, d.num_units, sum);
+  ++g_launches;
+  g_units += d.num_units;
+}
+
+// Every row block of one backward call, as the library launches them.
+// valid < 0: no row compaction (each block has its own rows); else the
+// number of non-ignored rows, which the compacted blocks take in turn.
+void check_call(const BwdPlan& b, long long N, long long H, long long V, int tm, long long valid,
+                const char* name) {
+  if (b.buffers != 2 || b.n_slabs < 2) {
+    EXPECT(false, "%s: the plan is not pipelined (buffers %d, slabs %d)", name, b.buffers, b.n_slabs);
+    return;
+  }
+  int count_dev = static_cast<int>(valid);
+  GemmParams base{};
+  base.N = static_cast<int>(N);
+  base.H = static_cast<int>(H);
+  base.V = static_cast<int>(V);
+  base.ldD = static_cast<int>(b.ldD);
+  base.rows_cap = static_cast<int>(b.R);
+  int block = 0;
+  for (long long row0 = 0; row0 < N; row0 += b.R, ++block) {
+    GemmParams p = base;
+    int rows;
+    if (valid >= 0) {
+      rows = static_cast<int>(b.R);
+      p.row0 = 0;
+      p.rows = rows;
+      p.dyn_count = &count_dev;
+      p.chunk_first = static_cast<int>(row0);
+    } else {
+      rows = static_cast<int>(std::min(b.R, N - row0));
+      p.row0 = static_cast<int>(row0);
+      p.rows = rows;
+    }
+    const GemmParams q = pipe_params(b, p, H, tm, rows, block);
+    char what[160];
+    std::snprintf(what, sizeof(what), "%s block %d", name, block);
+    if (tm == 2 * BM)
+      check_launch<2 * BM>(q, what);
+    else
+      check_launch<BM>(q, what);
+  }
+}
+
+void set_rows(long long r) {
+  init_options();
+  g_options[FLCE_OPT_BWD_ROWS].store(r);
+}
+
+void planned(long long N, long long H, long long V, long long chunk, int cg, long long rows, long long valid,
+             const char* name) {
+  set_rows(rows);
+  const int tm = cg * BM;
+  const int workers = cg == 2 ? 76 : 152;
+  const BwdPlan b = plan_backward_call(N, H, V, chunk, workers, tm, true);
+  check_call(b, N, H, V, tm, valid, name);
+}
+
+// splitmix64 (Steele, Lea, Flood: "Fast splittable pseudorandom number
+// generators"), for the seeded sweep
+uint64_t g_state = 0x5eed;
+uint64_t next_u64() {
+  uint64_t z = (g_state += 0x9e3779b97f4a7c15ULL);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+  return z ^ (z >> 31);
+}
+long long uniform(long long lo, long long hi) {  // [lo, hi]
+  return lo + static_cast<long long>(next_u64() % static_cast<uint64_t>(hi - lo + 1));
+}
+
+}  // namespace
+
+int main() {
+  // the planner's launches for the library's workloads and the GPU tests'
+  // pipelined cases, with and without row compaction, both tile heights
+  planned(131072, 2560, 151936, 256, 2, 0, -1, "131072x2560x151936");
+  planned(131072, 2560, 151936, 256, 2, 0, 131072 - 1000, "131072x2560x151936 compacted");
+  planned(131072, 2560, 151936, 256, 1, 0, -1, "131072x2560x151936 cg1");
+  for (int cg = 1; cg <= 2; ++cg) {
+    planned(3000, 512, 20000, 256, cg, 768, -1, "3000x512x20000");
+    planned(3000, 512, 20000, 256, cg, 768, 2760, "3000x512x20000 compacted");
+    planned(1000, 264, 7777, 128, cg, 512, -1, "1000x264x7777");
+    planned(1000, 264, 7777, 128, cg, 512, 920, "1000x264x7777 compacted");
+    planned(1000, 128, 4000, 128, cg, 256, 0, "1000x128x4000 all rows ignored");
+    planned(8192, 2560, 151936, 256, cg, 3328, -1, "8192x2560x151936");
+  }
+  set_rows(0);
+  // a seeded sweep of plans: row capacity, slab width, vocabulary, width,
+  // dH k-split depth, tile height, live rows (some blocks empty)
+  for (int i = 0; i < 400; ++i) {
+    const int tm = (i & 1) ? 2 * BM : BM;
+    BwdPlan b;
+    b.R = 64 * uniform(1, 48);
+    b.Vs = BN * uniform(1, 24);
+    const long long V = uniform(b.Vs + 1, 7 * b.Vs);
+    b.n_slabs = static_cast<int>(ceil_div(V, b.Vs));
+    b.ldD = b.Vs;
+    b.dh_kb_per_split = static_cast<int>(uniform(1, ceil_div(b.Vs, BK)));
+    b.dh_f32 = true;
+    b.buffers = 2;
+    const long long H = 8 * uniform(1, 512);
+    const long long N = uniform(1, 4 * b.R);
+    const long long valid = (i % 3 == 0) ? -1 : uniform(0, N);
+    char name[96];
+    std::snprintf(name, sizeof(name), "sweep %d (R %lld, Vs %lld, V %lld, H %lld, N %lld)", i, b.R, b.Vs, V, H, N);
+    check_call(b, N, H, V, tm, valid, name);
+  }
+  if (g_fails) {
+    std::printf("FAILED: %d checks in %lld launches\n", g_fails, g_launches);
+    return 1;
+  }
+  std::printf("ok: %lld launches, %lld units\n", g_launches, g_units);
+  return 0;
+}
