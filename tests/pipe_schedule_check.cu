@@ -13,7 +13,15 @@
 //   - every wait's target equals the number of units that add to its counter,
 //     and all of those units come before the waiting unit;
 //   - each slab's dlogits, dH and dW units are decoded exactly once, within
-//     their tile ranges, and the launch's unit count is their sum.
+//     their tile ranges, and the launch's unit count is their sum;
+//   - independently of how the counters are laid out, from the data each
+//     unit touches: a dH or dW unit waits for every dlogits unit of its slab
+//     that wrote a tile of the dlogits it reads; a dlogits unit of slab s
+//     waits for every dH and dW unit of slab s - 2 that read a tile it
+//     overwrites (the same buffer); a dH unit waits for the dH unit of the
+//     previous slab that added to the same fp32 partial tile -- each such
+//     unit earlier in the order and adding to a counter the waiting unit
+//     waits on.
 // The launches are those the planner makes for the library's workloads (with
 // and without row compaction, both CTA-group tile heights) and a seeded sweep
 // of plans.  Exit status 0 and "ok" when every check passes.
@@ -21,6 +29,7 @@
 #include <cstdio>
 #include <set>
 #include <tuple>
+#include <unordered_map>
 #include <vector>
 
 #include "plan.cuh"
@@ -40,6 +49,101 @@ long long g_launches = 0, g_units = 0;
       }                                        \
     }                                          \
   } while (0)
+
+uint64_t unit_key(int kind, int slab, int m, int n, int kb0) {
+  return (static_cast<uint64_t>(kind) << 60) | (static_cast<uint64_t>(slab) << 44) |
+         (static_cast<uint64_t>(m) << 28) | (static_cast<uint64_t>(n) << 16) | static_cast<uint64_t>(kb0);
+}
+
+// Unit `later` must not start before unit `earlier` has finished (a data
+// hazard between them): `earlier` comes first in the order and adds to a
+// counter that `later` waits on (whose target counts all its adders).
+template <int TM>
+void expect_ordered(const GemmParams& q, const DynShape& d, const std::vector<Unit>& units, int earlier, int later,
+                    const char* why, const char* what) {
+  EXPECT(earlier < later, "%s: unit %d must follow unit %d (%s) but comes first", what, later, earlier, why);
+  PipeWait w[2];
+  const int nw = pipe_unit_waits<TM, 1>(q, d, units[later], w);
+  int idx[2];
+  const int ns = pipe_unit_signals<TM>(q, units[earlier], idx);
+  bool covered = false;
+  for (int i = 0; i < nw; ++i)
+    for (int j = 0; j < ns; ++j) covered = covered || (w[i].idx == idx[j] && w[i].target > 0);
+  EXPECT(covered, "%s: unit %d (kind %d, slab %d) does not wait for unit %d (kind %d, slab %d): %s", what, later,
+         units[later].kind, units[later].slab, earlier, units[earlier].kind, units[earlier].slab, why);
+}
+
+// The hazards on the two dlogits buffers (slab s in buffer s % 2) and on the
+// fp32 dH partials, enumerated from the tiles each unit reads or writes:
+//   dlogits unit (s, m, vt): writes rows of row tile m, columns [vt*BN, +BN)
+//     of slab s's buffer;
+//   dH unit (s, m, ht, K blocks kb0..kb1): reads rows of row tile m, columns
+//     [kb0*BK, kb1*BK) of that buffer; adds to partial tile (split, m, ht);
+//   dW unit (s, dvt, ht): reads every row, columns [dvt*TM, +TM).
+template <int TM>
+void check_hazards(const GemmParams& q, const DynShape& d, const std::vector<Unit>& units, const char* what) {
+  std::unordered_map<uint64_t, int> at;
+  at.reserve(units.size() * 2);
+  for (int u = 0; u < static_cast<int>(units.size()); ++u) {
+    const Unit& t = units[u];
+    at[unit_key(t.kind, t.slab, t.m, t.n0, t.kb0)] = u;
+  }
+  auto find = [&](int kind, int slab, int m, int n, int kb0) -> int {
+    const auto it = at.find(unit_key(kind, slab, m, n, kb0));
+    return it == at.end() ? -1 : it->second;
+  };
+  for (int u = 0; u < static_cast<int>(units.size()); ++u) {
+    const Unit& t = units[u];
+    const PipeSlab ps = pipe_slab<TM>(q, d, t.slab);
+    if (t.kind == KIND_DH) {
+      // read after write: the dlogits tiles of its row tile that its K range covers
+      const int c0 = t.kb0 * BK, c1 = std::min(t.kb1 * BK, ps.width);
+      for (int vt = c0 / BN; vt * BN < c1; ++vt) {
+        const int w = find(KIND_DL, t.slab, t.m, vt, 0);
+        EXPECT(w >= 0, "%s: no dlogits unit (slab %d, %d, %d) for dH unit %d", what, t.slab, t.m, vt, u);
+        if (w >= 0) expect_ordered<TM>(q, d, units, w, u, "dH reads the dlogits it wrote", what);
+      }
+      // the fp32 partial tile: the previous slab's unit of the same tile and split
+      if (t.slab > 0) {
+        const PipeSlab pp = pipe_slab<TM>(q, d, t.slab - 1);
+        if (t.split < pp.splits) {
+          const int w = find(KIND_DH, t.slab - 1, t.m, t.n0, t.split * q.pp_dh_kbps);
+          EXPECT(w >= 0, "%s: no dH unit of slab %d for partial tile (%d, %d, %d)", what, t.slab - 1, t.split,
+                 t.m, t.n0);
+          if (w >= 0) expect_ordered<TM>(q, d, units, w, u, "dH adds to the partial the previous slab left", what);
+        }
+      }
+    } else if (t.kind == KIND_DW) {
+      // read after write: the dlogits tile (every row tile) holding its columns
+      const int vt = t.m * TM / BN;
+      for (int m = 0; m < d.m_tiles; ++m) {
+        const int w = find(KIND_DL, t.slab, m, vt, 0);
+        EXPECT(w >= 0, "%s: no dlogits unit (slab %d, %d, %d) for dW unit %d", what, t.slab, m, vt, u);
+        if (w >= 0) expect_ordered<TM>(q, d, units, w, u, "dW reads the dlogits it wrote", what);
+      }
+    } else if (t.slab >= 2) {
+      // write after read: slab s - 2's readers of this tile of the same buffer
+      const PipeSlab po = pipe_slab<TM>(q, d, t.slab - 2);
+      const int c0 = t.n0 * BN, c1 = std::min(c0 + BN, po.width);
+      for (int split = 0; split < po.splits; ++split) {
+        const int k0 = split * q.pp_dh_kbps * BK, k1 = std::min((split + 1) * q.pp_dh_kbps * BK, po.width);
+        if (k1 <= c0 || k0 >= c1) continue;
+        for (int ht = 0; ht < q.n_tiles; ++ht) {
+          const int r = find(KIND_DH, t.slab - 2, t.m, ht, split * q.pp_dh_kbps);
+          EXPECT(r >= 0, "%s: no dH unit (slab %d, %d, %d, split %d)", what, t.slab - 2, t.m, ht, split);
+          if (r >= 0) expect_ordered<TM>(q, d, units, r, u, "dlogits overwrites what dH read", what);
+        }
+      }
+      if (po.n_dw > 0)
+        for (int dvt = c0 / TM; dvt * TM < c1 && dvt < po.dwt; ++dvt)
+          for (int ht = 0; ht < q.n_tiles; ++ht) {
+            const int r = find(KIND_DW, t.slab - 2, dvt, ht, 0);
+            EXPECT(r >= 0, "%s: no dW unit (slab %d, %d, %d)", what, t.slab - 2, dvt, ht);
+            if (r >= 0) expect_ordered<TM>(q, d, units, r, u, "dlogits overwrites what dW read", what);
+          }
+    }
+  }
+}
 
 template <int TM>
 void check_launch(const GemmParams& q, const char* what) {
@@ -107,6 +211,7 @@ void check_launch(const GemmParams& q, const char* what) {
     sum += ps.n_dl + ps.n_dh + ps.n_dw;
   }
   EXPECT(sum == d.num_units, "%s: %d units, expected %lld", what, d.num_units, sum);
+  check_hazards<TM>(q, d, units, what);
   ++g_launches;
   g_units += d.num_units;
 }
