@@ -24,7 +24,10 @@
 //     waits on.
 // The launches are those the planner makes for the library's workloads (with
 // and without row compaction, both CTA-group tile heights) and a seeded sweep
-// of plans.  Exit status 0 and "ok" when every check passes.
+// of plans.  It also checks that the raster decoding every GEMM launch uses
+// (decode_grid) maps its unit indices one to one onto (k-split, row tile,
+// column unit), over a sweep of grid shapes and raster groups.  Exit status
+// 0 and "ok" when every check passes.
 #include <cstdint>
 #include <cstdio>
 #include <set>
@@ -257,6 +260,43 @@ void check_call(const BwdPlan& b, long long N, long long H, long long V, int tm,
   }
 }
 
+// decode_grid over one grid: every (k-split, row tile, column unit) once, in
+// range, with its K blocks and output columns.
+void check_grid(int m_tiles, int cols, int n_per_unit, int group_m, int k_splits, int kb_per_split, bool col_split) {
+  const int n_tiles = cols * n_per_unit - (n_per_unit > 1 ? 1 : 0);  // a ragged last column unit
+  const int k_blocks = col_split ? kb_per_split : k_splits * kb_per_split - (kb_per_split > 1 ? 1 : 0);
+  const int splits = col_split ? 1 : k_splits;
+  std::vector<char> hit(static_cast<size_t>(splits) * m_tiles * cols, 0);
+  const int units = splits * m_tiles * cols;
+  for (int u = 0; u < units; ++u) {
+    const Unit t = decode_grid(u, m_tiles, cols, n_tiles, n_per_unit, group_m, kb_per_split, k_blocks, col_split);
+    const int c = t.n0 / n_per_unit;
+    const int ks = col_split ? 0 : t.kb0 / kb_per_split;
+    const bool in = t.m >= 0 && t.m < m_tiles && c >= 0 && c < cols && ks >= 0 && ks < splits &&
+                    t.n0 == c * n_per_unit && t.n1 == std::min(n_tiles, t.n0 + n_per_unit) && t.n1 > t.n0 &&
+                    t.kb1 == std::min(k_blocks, t.kb0 + kb_per_split) && t.kb1 > t.kb0 &&
+                    t.split == (col_split ? c : ks);
+    EXPECT(in, "grid %dx%d (n/unit %d, group %d, splits %d): unit %d decodes to (%d, %d..%d, K %d..%d, split %d)",
+           m_tiles, cols, n_per_unit, group_m, k_splits, u, t.m, t.n0, t.n1, t.kb0, t.kb1, t.split);
+    if (!in) continue;
+    char& h = hit[(static_cast<size_t>(ks) * m_tiles + t.m) * cols + c];
+    EXPECT(!h, "grid %dx%d (group %d, splits %d): (%d, %d, %d) decoded twice", m_tiles, cols, group_m, k_splits, ks,
+           t.m, c);
+    h = 1;
+  }
+  // a row tile's column units stay inside one raster group of group_m rows
+  // (units of a group list its row tiles first, then move to the next column)
+  const int g = std::min(group_m, std::max(m_tiles, 1));
+  if (m_tiles > 0 && cols > 1) {
+    const Unit a = decode_grid(0, m_tiles, cols, n_tiles, n_per_unit, group_m, kb_per_split, k_blocks, col_split);
+    const Unit b = decode_grid(std::min(g, m_tiles), m_tiles, cols, n_tiles, n_per_unit, group_m, kb_per_split,
+                               k_blocks, col_split);
+    EXPECT(a.m == 0 && a.n0 == 0 && b.m == 0 && b.n0 == n_per_unit,
+           "grid %dx%d (group %d): unit %d is not the first row tile's second column unit", m_tiles, cols, group_m,
+           std::min(g, m_tiles));
+  }
+}
+
 void set_rows(long long r) {
   init_options();
   g_options[FLCE_OPT_BWD_ROWS].store(r);
@@ -321,10 +361,22 @@ int main() {
     std::snprintf(name, sizeof(name), "sweep %d (R %lld, Vs %lld, V %lld, H %lld, N %lld)", i, b.R, b.Vs, V, H, N);
     check_call(b, N, H, V, tm, valid, name);
   }
+  // the raster decoding of every GEMM launch
+  long long grids = 0;
+  for (int i = 0; i < 3000; ++i) {
+    const int m_tiles = static_cast<int>(uniform(1, 40));
+    const int cols = static_cast<int>(uniform(1, 40));
+    const int n_per_unit = static_cast<int>(uniform(1, 3));
+    const int group_m = static_cast<int>(uniform(1, 48));
+    const int k_splits = static_cast<int>(uniform(1, 6));
+    const int kb = static_cast<int>(uniform(1, 9));
+    check_grid(m_tiles, cols, n_per_unit, group_m, k_splits, kb, (i % 4) == 0);
+    ++grids;
+  }
   if (g_fails) {
     std::printf("FAILED: %d checks in %lld launches\n", g_fails, g_launches);
     return 1;
   }
-  std::printf("ok: %lld launches, %lld units\n", g_launches, g_units);
+  std::printf("ok: %lld launches, %lld units; %lld raster grids\n", g_launches, g_units, grids);
   return 0;
 }

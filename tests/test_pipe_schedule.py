@@ -7,8 +7,11 @@ seeded sweep of plans, with the library's own decoding and counter helpers
 compiled for the host, and checks that every wait's target is the number of
 units adding to its counter, that all of them come earlier in the order (so
 the launch completes on however many pairs are resident), that every counter
-lies inside the launch's counter words, and that each slab's units are
-decoded exactly once.  Needs nvcc, no GPU."""
+lies inside the launch's counter words, that each slab's units are decoded
+exactly once, and that the hazards on the dlogits buffers and dH partials
+(enumerated from the tiles each unit reads and writes) are all ordered.  It
+also checks the raster decoding every GEMM launch uses, over a sweep of grid
+shapes and raster groups.  Needs nvcc, no GPU."""
 import os
 import subprocess
 
