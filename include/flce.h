@@ -652,8 +652,11 @@ typedef enum flce_option {
   FLCE_OPT_GRID_WORKERS,    /* FLCE_GRID_WORKERS: persistent workers (CTAs, or CTA pairs) that
                                each GEMM launch starts, 1..4,096; 0 = as many as the device
                                holds at once (default).  Plans stay those of the device's
-                               count: fewer workers leave SMs to other work, more queue
-                               behind the resident ones and find the units taken */
+                               count: fewer workers leave SMs to other work; more start as
+                               resident ones retire (the round-robin units of a GEMM run
+                               in further waves; in the pipelined backward, whose workers
+                               draw units, the late ones find them taken).  Results do not
+                               depend on it */
   FLCE_OPT_COUNT
 } flce_option;
 
