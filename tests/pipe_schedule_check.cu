@@ -24,7 +24,12 @@
 //     waits on.
 // The launches are those the planner makes for the library's workloads (with
 // and without row compaction, both CTA-group tile heights) and a seeded sweep
-// of plans.  It also checks that the raster decoding every GEMM launch uses
+// of plans.  For the planner's plans it checks the backward's workspace: the
+// regions (dlogits buffers, dH partials, compaction buffers, dependency
+// counters) 256-byte aligned and disjoint, inside the size the library
+// reports, the dlogits inside the O(chunk_rows x V) budget, and room in the
+// dH partials for every k-split a slab's units write.  It also checks that
+// the raster decoding every GEMM launch uses
 // (decode_grid) maps its unit indices one to one onto (k-split, row tile,
 // column unit), over a sweep of grid shapes and raster groups.  Exit status
 // 0 and "ok" when every check passes.
@@ -297,6 +302,55 @@ void check_grid(int m_tiles, int cols, int n_per_unit, int group_m, int k_splits
   }
 }
 
+// The backward's workspace for plan b: regions aligned, disjoint, inside
+// what flce_workspace_bytes reports (bwd_workspace), the dlogits inside the
+// caller's budget, and a dH partial set for each k-split of any slab.
+void check_layout(long long N, long long H, long long V, long long chunk, int workers, int tm, const BwdPlan& b,
+                  const char* name) {
+  if (b.R <= 0) {
+    EXPECT(false, "%s: no row block fits", name);
+    return;
+  }
+  const BwdLayout L = bwd_layout(N, H, b);
+  struct Region {
+    const char* what;
+    size_t off, bytes;
+  };
+  const Region regs[] = {
+      {"dlogits", L.D, static_cast<size_t>(b.buffers) * b.R * b.ldD * 2},
+      {"dH partials", L.dh_part, b.dh_f32 ? static_cast<size_t>(b.dh_splits) * b.R * H * 4 : 0},
+      {"validation word", L.bad, 4},
+      {"row indices", L.idx, static_cast<size_t>(N) * 4},
+      {"block counts", L.blk, static_cast<size_t>(ceil_div(N, COMPACT_ROWS_PER_BLOCK)) * 4},
+      {"row count", L.count, 4},
+      {"gathered rows", L.hc, static_cast<size_t>(b.R) * H * 2},
+      {"dependency counters", L.dep, b.buffers == 2 ? static_cast<size_t>(2 * pipe_dep_words(b)) * 4 : 0},
+  };
+  const int n = static_cast<int>(sizeof(regs) / sizeof(regs[0]));
+  for (int i = 0; i < n; ++i) {
+    EXPECT(regs[i].off % 256 == 0, "%s: %s at offset %zu", name, regs[i].what, regs[i].off);
+    EXPECT(regs[i].off + regs[i].bytes <= L.total, "%s: %s ends past the layout", name, regs[i].what);
+    for (int j = 0; j < n; ++j)
+      if (i != j && regs[i].bytes > 0 && regs[j].bytes > 0)
+        EXPECT(regs[i].off + regs[i].bytes <= regs[j].off || regs[j].off + regs[j].bytes <= regs[i].off,
+               "%s: %s and %s overlap", name, regs[i].what, regs[j].what);
+  }
+  EXPECT(L.total <= bwd_workspace(N, H, V, chunk, workers, tm), "%s: layout of %zu bytes above the reported %zu",
+         name, L.total, bwd_workspace(N, H, V, chunk, workers, tm));
+  const long long r0 = std::min(round_up(std::max(1LL, chunk), BM), round_up(std::max(1LL, N), BM));
+  EXPECT(static_cast<long long>(b.buffers) * b.R * b.ldD <= r0 * round_up(V, 8),
+         "%s: dlogits %d x %lld x %lld above the budget %lld x %lld", name, b.buffers, b.R, b.ldD, r0,
+         round_up(V, 8));
+  if (b.dh_f32) {
+    for (int s = 0; s < b.n_slabs; ++s) {
+      const long long width = std::min(b.Vs, V - s * b.Vs);
+      const long long splits = ceil_div(ceil_div(width, BK), b.dh_kb_per_split);
+      EXPECT(splits <= b.dh_splits, "%s: slab %d needs %lld dH partial sets, the workspace holds %d", name, s,
+             splits, b.dh_splits);
+    }
+  }
+}
+
 void set_rows(long long r) {
   init_options();
   g_options[FLCE_OPT_BWD_ROWS].store(r);
@@ -308,6 +362,7 @@ void planned(long long N, long long H, long long V, long long chunk, int cg, lon
   const int tm = cg * BM;
   const int workers = cg == 2 ? 76 : 152;
   const BwdPlan b = plan_backward_call(N, H, V, chunk, workers, tm, true);
+  check_layout(N, H, V, chunk, workers, tm, b, name);
   check_call(b, N, H, V, tm, valid, name);
 }
 
@@ -341,6 +396,26 @@ int main() {
     planned(8192, 2560, 151936, 256, cg, 3328, -1, "8192x2560x151936");
   }
   set_rows(0);
+  // the planner's plans over a seeded sweep of problem sizes: the workspace
+  // layout of the plain and the pipelined plan, and the schedule of the
+  // pipelined one
+  long long plans = 0;
+  for (int i = 0; i < 300; ++i) {
+    const int cg = (i & 1) ? 2 : 1;
+    const int tm = cg * BM, workers = cg == 2 ? 76 : 152;
+    const long long N = uniform(1, 140000), H = 8 * uniform(8, 1024), V = uniform(1000, 260000);
+    const long long chunks[] = {128, 256, 1024, 4096};
+    const long long chunk = chunks[uniform(0, 3)];
+    char name[96];
+    std::snprintf(name, sizeof(name), "planned %d (N %lld, H %lld, V %lld, chunk %lld, cg %d)", i, N, H, V, chunk,
+                  cg);
+    const BwdPlan plain = plan_backward(N, H, V, chunk, workers, tm);
+    check_layout(N, H, V, chunk, workers, tm, plain, name);
+    const BwdPlan b = plan_backward_call(N, H, V, chunk, workers, tm, true);
+    check_layout(N, H, V, chunk, workers, tm, b, name);
+    if (b.buffers == 2 && N <= 20000) check_call(b, N, H, V, tm, (i % 3 == 0) ? -1 : uniform(0, N), name);
+    ++plans;
+  }
   // a seeded sweep of plans: row capacity, slab width, vocabulary, width,
   // dH k-split depth, tile height, live rows (some blocks empty)
   for (int i = 0; i < 400; ++i) {
@@ -377,6 +452,7 @@ int main() {
     std::printf("FAILED: %d checks in %lld launches\n", g_fails, g_launches);
     return 1;
   }
-  std::printf("ok: %lld launches, %lld units; %lld raster grids\n", g_launches, g_units, grids);
+  std::printf("ok: %lld launches, %lld units; %lld planned layouts; %lld raster grids\n", g_launches, g_units,
+              plans, grids);
   return 0;
 }

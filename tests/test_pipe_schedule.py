@@ -9,9 +9,12 @@ units adding to its counter, that all of them come earlier in the order (so
 the launch completes on however many pairs are resident), that every counter
 lies inside the launch's counter words, that each slab's units are decoded
 exactly once, and that the hazards on the dlogits buffers and dH partials
-(enumerated from the tiles each unit reads and writes) are all ordered.  It
-also checks the raster decoding every GEMM launch uses, over a sweep of grid
-shapes and raster groups.  Needs nvcc, no GPU."""
+(enumerated from the tiles each unit reads and writes) are all ordered.  For
+the planner's plans over a sweep of problem sizes it checks the backward's
+workspace layout (regions aligned and disjoint, inside the reported size, the
+dlogits inside the O(chunk_rows x V) budget, a dH partial set for every
+k-split).  It also checks the raster decoding every GEMM launch uses, over a
+sweep of grid shapes and raster groups.  Needs nvcc, no GPU."""
 import os
 import subprocess
 
