@@ -28,7 +28,8 @@
 // regions (dlogits buffers, dH partials, compaction buffers, dependency
 // counters) 256-byte aligned and disjoint, inside the size the library
 // reports, the dlogits inside the O(chunk_rows x V) budget, and room in the
-// dH partials for every k-split a slab's units write.  It also checks that
+// dH partials for every k-split a slab's units write; and the forward's
+// vocabulary splits and workspace.  It also checks that
 // the raster decoding every GEMM launch uses
 // (decode_grid) maps its unit indices one to one onto (k-split, row tile,
 // column unit), over a sweep of grid shapes and raster groups.  Exit status
@@ -351,6 +352,46 @@ void check_layout(long long N, long long H, long long V, long long chunk, int wo
   }
 }
 
+// The forward's plan and workspace for one call: the vocabulary splits cover
+// every vocabulary tile once (S ranges of tps tiles, the last one partial),
+// the split partials fit their cap, and the regions (target logits, split
+// partials, block sums, validation word, and the row-skipping buffers) are
+// 256-byte aligned, disjoint and inside the layout.
+void check_forward(long long N, long long H, long long V, int workers, int tm, const char* name) {
+  const FwdPlan f = plan_forward_call(N, H, V, workers, tm);
+  EXPECT(f.S >= 1 && f.S <= 256 && f.tps >= 1 && static_cast<long long>(f.S - 1) * f.tps < f.n_tiles &&
+             static_cast<long long>(f.S) * f.tps >= f.n_tiles,
+         "%s: %d splits of %d tiles for %d vocabulary tiles", name, f.S, f.tps, f.n_tiles);
+  EXPECT(static_cast<size_t>(f.S) * N * 8 <= std::max(kFwdPartialsCap, static_cast<size_t>(N) * 8),
+         "%s: split partials %d x %lld rows above their cap", name, f.S, N);
+  const long long fb = fwd_block_rows(N, tm);
+  const FwdLayout L = fwd_layout(N, f, H, fb);
+  struct Region {
+    const char* what;
+    size_t off, bytes;
+  };
+  const Region regs[] = {
+      {"target logits", L.zt, static_cast<size_t>(N) * 4},
+      {"split partials", L.part, static_cast<size_t>(f.S) * N * 8},
+      {"block sums", L.bsum, static_cast<size_t>(f.nblk) * 8},
+      {"block counts", L.bcnt, static_cast<size_t>(f.nblk) * 8},
+      {"validation word", L.bad, 4},
+      {"row indices", L.idx, static_cast<size_t>(N) * 4},
+      {"index block counts", L.blk, static_cast<size_t>(ceil_div(std::max(1LL, N), COMPACT_ROWS_PER_BLOCK)) * 4},
+      {"row count", L.count, 4},
+      {"gathered rows", L.hc, static_cast<size_t>(fb) * H * 2},
+  };
+  const int n = static_cast<int>(sizeof(regs) / sizeof(regs[0]));
+  for (int i = 0; i < n; ++i) {
+    EXPECT(regs[i].off % 256 == 0, "%s: forward %s at offset %zu", name, regs[i].what, regs[i].off);
+    EXPECT(regs[i].off + regs[i].bytes <= L.total, "%s: forward %s ends past the layout", name, regs[i].what);
+    for (int j = 0; j < n; ++j)
+      if (i != j && regs[i].bytes > 0 && regs[j].bytes > 0)
+        EXPECT(regs[i].off + regs[i].bytes <= regs[j].off || regs[j].off + regs[j].bytes <= regs[i].off,
+               "%s: forward %s and %s overlap", name, regs[i].what, regs[j].what);
+  }
+}
+
 void set_rows(long long r) {
   init_options();
   g_options[FLCE_OPT_BWD_ROWS].store(r);
@@ -409,6 +450,7 @@ int main() {
     char name[96];
     std::snprintf(name, sizeof(name), "planned %d (N %lld, H %lld, V %lld, chunk %lld, cg %d)", i, N, H, V, chunk,
                   cg);
+    check_forward(N, H, V, workers, tm, name);
     const BwdPlan plain = plan_backward(N, H, V, chunk, workers, tm);
     check_layout(N, H, V, chunk, workers, tm, plain, name);
     const BwdPlan b = plan_backward_call(N, H, V, chunk, workers, tm, true);

@@ -13,7 +13,8 @@ exactly once, and that the hazards on the dlogits buffers and dH partials
 the planner's plans over a sweep of problem sizes it checks the backward's
 workspace layout (regions aligned and disjoint, inside the reported size, the
 dlogits inside the O(chunk_rows x V) budget, a dH partial set for every
-k-split).  It also checks the raster decoding every GEMM launch uses, over a
+k-split) and the forward's (vocabulary splits covering every tile once,
+regions aligned and disjoint).  It also checks the raster decoding every GEMM launch uses, over a
 sweep of grid shapes and raster groups.  Needs nvcc, no GPU."""
 import os
 import subprocess
