@@ -646,7 +646,10 @@ typedef enum flce_option {
                                   short K (at most 1,024 rows): 16 (default) or 8 */
   FLCE_OPT_PIPELINE,        /* FLCE_PIPELINE: 1 = a backward of several vocabulary slabs runs
                                each row block in one launch, its units ordered by device-side
-                               counters (default), 0 = two launches per slab */
+                               counters (default), 0 = two launches per slab.  The launch's
+                               SM pairs draw units in an order in which every wait points to
+                               earlier units, so it completes on however many SMs other work
+                               leaves it; each wait is bounded (FLCE_ERR_TIMEOUT) */
   FLCE_OPT_DH_WIDE,         /* FLCE_DH_WIDE: 1 = the dH GEMM of a one-slab backward runs 256 x
                                512 tiles on SM pairs (default), 0 = 256 x 256 */
   FLCE_OPT_GRID_WORKERS,    /* FLCE_GRID_WORKERS: persistent workers (CTAs, or CTA pairs) that
